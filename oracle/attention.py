@@ -1,0 +1,156 @@
+"""Attention restricted to a key set, in float64.
+
+For query i with allowed key set S(i) (from a CSR row or an offset set) and scale c
+(default 1/sqrt(d), as in the [BB] section 3 sketch which divides scores by d**0.5):
+
+    s_ij   = c * sum_t q_it k_jt                       (j in S(i))
+    LSE_i  = m_i + ln sum_{j in S(i)} exp(s_ij - m_i),  m_i = max_j s_ij
+    O_i    = sum_{j in S(i)} exp(s_ij - LSE_i) v_j
+
+An empty key set gives O_i = 0 and LSE_i = -inf. Inputs are float64 arrays with layout
+[batch, tokens, heads, d]; query head h reads key/value head h // (H / H_kv).
+Outputs: O [batch, tokens, heads, d] and LSE [batch, heads, tokens] (natural log).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def _softmax_rows(s: np.ndarray):
+    """Row-wise exact softmax of a score matrix whose masked entries are -inf."""
+    m = np.max(s, axis=1, keepdims=True) if s.shape[1] else np.full((s.shape[0], 1), -np.inf)
+    empty = ~np.isfinite(m[:, 0])
+    m_safe = np.where(np.isfinite(m), m, 0.0)
+    e = np.exp(s - m_safe)
+    tot = e.sum(axis=1, keepdims=True)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        p = np.where(tot > 0, e / np.where(tot > 0, tot, 1.0), 0.0)
+        lse = np.where(empty, -np.inf, m_safe[:, 0] + np.log(np.where(tot[:, 0] > 0, tot[:, 0], 1.0)))
+    return p, lse
+
+
+def _csr_batch(row_ptr, s):
+    return s if row_ptr.shape[0] > 1 else 0
+
+
+def attention_csr(q, k, v, row_ptr, col_idx, block: int, causal: int, scale: float | None = None):
+    """Block-CSR attention for every query; see module docstring."""
+    bt, n, h, d = q.shape
+    hkv = k.shape[2]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    nb = n // block
+    o = np.zeros((bt, n, h, d), dtype=np.float64)
+    lse = np.full((bt, h, n), -np.inf, dtype=np.float64)
+    for s in range(bt):
+        cs = _csr_batch(row_ptr, s)
+        for I in range(nb):
+            row = col_idx[row_ptr[cs, I]:row_ptr[cs, I + 1]]
+            if len(row) == 0:
+                continue
+            keys = np.concatenate([np.arange(J * block, (J + 1) * block) for J in row])
+            qi = np.arange(I * block, (I + 1) * block)
+            allowed = np.ones((block, len(keys)), dtype=bool)
+            if causal:
+                allowed = keys[None, :] <= qi[:, None]
+            for hh in range(h):
+                hk = hh // (h // hkv)
+                sc = (q[s, qi, hh, :] @ k[s, keys, hk, :].T) * scale
+                sc = np.where(allowed, sc, -np.inf)
+                p, l = _softmax_rows(sc)
+                o[s, qi, hh, :] = p @ v[s, keys, hk, :]
+                lse[s, hh, qi] = l
+    return o, lse
+
+
+def attention_rows_csr(q, k, v, row_ptr, col_idx, block: int, causal: int, samples,
+                       scale: float | None = None):
+    """The same definition evaluated only at sampled (batch, token, head) triples.
+
+    Returns ``o [len(samples), d]`` and ``lse [len(samples)]``.
+    """
+    d = q.shape[3]
+    h = q.shape[2]
+    hkv = k.shape[2]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    o = np.zeros((len(samples), d))
+    lse = np.full(len(samples), -np.inf)
+    for t, (s, i, hh) in enumerate(samples):
+        cs = _csr_batch(row_ptr, s)
+        I = i // block
+        row = col_idx[row_ptr[cs, I]:row_ptr[cs, I + 1]]
+        keys = [j for J in row for j in range(J * block, (J + 1) * block) if not causal or j <= i]
+        if not keys:
+            continue
+        hk = hh // (h // hkv)
+        sc = (k[s, keys, hk, :] @ q[s, i, hh, :]) * scale
+        p, l = _softmax_rows(sc[None, :])
+        o[t] = p[0] @ v[s, keys, hk, :]
+        lse[t] = l[0]
+    return o, lse
+
+
+def attention_offsets(q, k, v, window: int, offsets, scale: float | None = None,
+                      samples=None):
+    """Token-granular window-plus-offset attention ([FIB] section 2 "Attended set").
+
+    Key set of query i: {i - delta : delta in {0..window} u offsets, i - delta >= 0},
+    deduplicated. If ``samples`` (list of (batch, token, head)) is given, only those
+    queries are evaluated and ``o [len, d]``, ``lse [len]`` are returned.
+    """
+    bt, n, h, d = q.shape
+    hkv = k.shape[2]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    deltas = np.array(sorted(set(range(window + 1)) | {int(x) for x in offsets}), dtype=np.int64)
+    if samples is not None:
+        o = np.zeros((len(samples), d))
+        lse = np.full(len(samples), -np.inf)
+        for t, (s, i, hh) in enumerate(samples):
+            keys = i - deltas[deltas <= i]
+            hk = hh // (h // hkv)
+            sc = (k[s, keys, hk, :] @ q[s, i, hh, :]) * scale
+            p, l = _softmax_rows(sc[None, :])
+            o[t] = p[0] @ v[s, keys, hk, :]
+            lse[t] = l[0]
+        return o, lse
+    o = np.zeros((bt, n, h, d))
+    lse = np.full((bt, h, n), -np.inf)
+    idx = np.arange(n)[:, None] - deltas[None, :]          # [n, n_delta] key index
+    valid = idx >= 0
+    idx_c = np.where(valid, idx, 0)
+    for s in range(bt):
+        for hh in range(h):
+            hk = hh // (h // hkv)
+            kk = k[s, :, hk, :][idx_c]                       # [n, n_delta, d]
+            sc = np.einsum("nd,nkd->nk", q[s, :, hh, :], kk) * scale
+            sc = np.where(valid, sc, -np.inf)
+            p, l = _softmax_rows(sc)
+            o[s, :, hh, :] = np.einsum("nk,nkd->nd", p, v[s, :, hk, :][idx_c])
+            lse[s, hh, :] = l
+    return o, lse
+
+
+def dense_masked_attention(q, k, v, token_mask: np.ndarray, scale: float | None = None):
+    """Second route: full N x N scores, masked fill with -inf, softmax, times V.
+
+    This is the dense formulation both [CAS] (section 5 "Limitations": the mask is
+    applied to the materialised N x N matrix) and the [BB] section 3 sketch use.
+    ``token_mask`` is bool [N, N] (shared over batch and heads).
+    """
+    bt, n, h, d = q.shape
+    hkv = k.shape[2]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    o = np.zeros((bt, n, h, d))
+    lse = np.full((bt, h, n), -np.inf)
+    for s in range(bt):
+        for hh in range(h):
+            hk = hh // (h // hkv)
+            sc = (q[s, :, hh, :] @ k[s, :, hk, :].T) * scale
+            sc = np.where(token_mask, sc, -np.inf)
+            p, l = _softmax_rows(sc)
+            o[s, :, hh, :] = p @ v[s, :, hk, :]
+            lse[s, hh, :] = l
+    return o, lse

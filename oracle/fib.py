@@ -1,0 +1,51 @@
+"""Fibonacci offsets with a per-layer scale ([FIB] section 2 "Method").
+
+* Rungs: f = 1, 2, 3, 5, 8, ..., 987 (K = 15) in [FIB]; the workload statement instead
+  allows every f_k <= N. Both are available (``fib_rungs(K)`` / ``fib_rungs_upto(N)``).
+* Linear stagger: alpha_l = alpha_lo + (alpha_hi - alpha_lo) * l / (L - 1), held as an
+  exact fraction ([FIB]: 0.5 -> 1.5; the workload statement: 0.5 -> 2.0).
+* Offsets d_k = round(alpha * f_k). Reading: [FIB] only says the fixed and staggered
+  variants have integer offsets; "round" is taken as round-half-to-even (Python and
+  torch ``round``). Ties occur (alpha = 1/2 with odd f).
+* Key set of query i: { i - delta : delta in {0, ..., W} u D, i - delta >= 0 } as a set
+  (the union is deduplicated; offsets inside the window add nothing).
+"""
+from __future__ import annotations
+
+from fractions import Fraction
+
+
+def fib_rungs(n_rungs: int = 15) -> list[int]:
+    out = []
+    a, b = 1, 2
+    for _ in range(n_rungs):
+        out.append(a)
+        a, b = b, a + b
+    return out
+
+
+def fib_rungs_upto(n: int) -> list[int]:
+    out = []
+    a, b = 1, 2
+    while a <= n:
+        out.append(a)
+        a, b = b, a + b
+    return out
+
+
+def alpha_schedule(layers: int, lo=(1, 2), hi=(3, 2)) -> list[Fraction]:
+    a_lo = Fraction(*lo)
+    a_hi = Fraction(*hi)
+    if layers == 1:
+        return [a_lo]
+    return [a_lo + (a_hi - a_lo) * Fraction(l, layers - 1) for l in range(layers)]
+
+
+def fib_offsets(alpha: Fraction, rungs: list[int]) -> list[int]:
+    """Sorted distinct d_k = round_half_even(alpha * f_k)."""
+    return sorted({round(Fraction(alpha) * f) for f in rungs})
+
+
+def offset_key_set(i: int, window: int, offsets: list[int]) -> list[int]:
+    deltas = set(range(window + 1)) | set(offsets)
+    return sorted({i - d for d in deltas if i - d >= 0})
