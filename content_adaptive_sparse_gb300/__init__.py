@@ -1,0 +1,198 @@
+"""Sparse-graph attention for GB300 (sm_103a): thin ctypes binding over libsa.so.
+
+Every function here only marshals arguments (torch tensors -> device pointers, the
+current CUDA stream) and calls the C ABI declared in ``include/sa_api.h``; all the
+work of the hot path runs in the library's CUDA kernels. There is no CPU fallback:
+if the library is missing or the device is not an sm_103 GPU, calls raise.
+
+Names follow the C ABI: ``sa_build_mask``, ``sa_attn_fwd``, ``sa_offset_attn_fwd``,
+``sa_fib_offsets``, ``sa_block_ratios``, ``sa_mask_nnz_bound``, ``sa_device_status``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from .build import LIB, build as build_library
+
+MASK_TOPK, MASK_BIGBIRD, MASK_FULL, MASK_LITERAL_MEAN = 0, 1, 2, 3
+_MODES = {"topk": MASK_TOPK, "bigbird": MASK_BIGBIRD, "full": MASK_FULL, "literal_mean": MASK_LITERAL_MEAN}
+
+STATUS = {0: "SA_OK", -1: "SA_ERR_INVALID_ARG", -2: "SA_ERR_UNSUPPORTED", -3: "SA_ERR_CAPACITY",
+          -4: "SA_ERR_CUDA", -5: "SA_ERR_TIMEOUT", -6: "SA_ERR_DEVICE"}
+
+
+class SAError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {STATUS.get(code, code)}")
+        self.code = code
+
+
+class MaskParams(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int32), ("block", ctypes.c_int32), ("n_tokens", ctypes.c_int32),
+                ("batch", ctypes.c_int32), ("causal", ctypes.c_int32), ("window_blocks", ctypes.c_int32),
+                ("global_blocks", ctypes.c_int32), ("topk", ctypes.c_int32), ("random_blocks", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("seed", ctypes.c_uint64)]
+
+
+_lib = None
+_I64x3 = ctypes.c_int64 * 3
+_P = ctypes.c_void_p
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load libsa.so (built in-tree by ``build_library``); raise if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with content_adaptive_sparse_gb300.build_library()")
+    lib = ctypes.CDLL(path)
+    lib.sa_version.restype = ctypes.c_int
+    lib.sa_status_string.restype = ctypes.c_char_p
+    lib.sa_status_string.argtypes = [ctypes.c_int]
+    lib.sa_mask_nnz_bound.argtypes = [ctypes.POINTER(MaskParams), ctypes.POINTER(ctypes.c_int64)]
+    lib.sa_build_mask.argtypes = [ctypes.POINTER(MaskParams), _P, _P, _P, ctypes.c_int64, _P]
+    lib.sa_attn_fwd.argtypes = [_P, _P, _P, _I64x3, _I64x3, _I64x3, ctypes.c_int32, ctypes.c_int32,
+                                ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                _P, _P, ctypes.c_int32, ctypes.c_float, _P, _P, _P]
+    lib.sa_offset_attn_fwd.argtypes = [_P, _P, _P, _I64x3, _I64x3, _I64x3, ctypes.c_int32, ctypes.c_int32,
+                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P,
+                                       ctypes.c_int32, ctypes.c_float, _P, _P, _P]
+    lib.sa_fib_offsets.argtypes = [ctypes.c_int32] * 5 + [_P, ctypes.c_int32, _P]
+    lib.sa_block_ratios.argtypes = [_P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P,
+                                    ctypes.c_int32]
+    lib.sa_device_status.argtypes = [_P]
+    for name in ("sa_mask_nnz_bound", "sa_build_mask", "sa_attn_fwd", "sa_offset_attn_fwd", "sa_fib_offsets",
+                 "sa_block_ratios", "sa_device_status"):
+        getattr(lib, name).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _check(fn: str, code: int):
+    if code != 0:
+        raise SAError(fn, code)
+
+
+def _stream_ptr(stream=None) -> int:
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def _strides(t) -> _I64x3:
+    st = t.stride()
+    if t.dim() != 4 or st[3] != 1:
+        raise ValueError("expected a [batch, tokens, heads, head_dim] tensor with contiguous head_dim")
+    return _I64x3(st[0], st[1], st[2])
+
+
+def mask_params(mode, block, n_tokens, batch, causal=1, window_blocks=0, global_blocks=0, topk=0,
+                random_blocks=0, seed=0) -> MaskParams:
+    return MaskParams(_MODES.get(mode, mode) if isinstance(mode, str) else mode, block, n_tokens, batch, causal,
+                      window_blocks, global_blocks, topk, random_blocks, 0, seed)
+
+
+# ------------------------------------------------------------------ C ABI, same names
+
+def sa_mask_nnz_bound(params: MaskParams) -> int:
+    out = ctypes.c_int64(0)
+    _check("sa_mask_nnz_bound", load_library().sa_mask_nnz_bound(ctypes.byref(params), ctypes.byref(out)))
+    return int(out.value)
+
+
+def sa_build_mask(params: MaskParams, ratio, row_ptr, col_idx, stream=None) -> None:
+    """Writes ``row_ptr`` (int32 [batch, nb+1]) and ``col_idx`` (int32 [capacity]) on the GPU."""
+    rp = 0 if ratio is None else ratio.data_ptr()
+    _check("sa_build_mask", load_library().sa_build_mask(ctypes.byref(params), rp, row_ptr.data_ptr(),
+                                                          col_idx.data_ptr(), col_idx.numel(), _stream_ptr(stream)))
+
+
+def sa_attn_fwd(q, k, v, row_ptr, col_idx, block: int, causal: int, o, lse, csr_shared: bool = False,
+                softmax_scale: float | None = None, stream=None) -> None:
+    b, n, h, d = q.shape
+    hkv = k.shape[2]
+    scale = 1.0 / float(np.sqrt(d)) if softmax_scale is None else float(softmax_scale)
+    _check("sa_attn_fwd", load_library().sa_attn_fwd(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), _strides(q), _strides(k), _strides(o), b, n, h, hkv, d, block,
+        int(causal), row_ptr.data_ptr(), col_idx.data_ptr(), int(bool(csr_shared)), scale, o.data_ptr(),
+        lse.data_ptr(), _stream_ptr(stream)))
+
+
+def sa_offset_attn_fwd(q, k, v, window: int, offsets, o, lse, softmax_scale: float | None = None,
+                       stream=None) -> None:
+    b, n, h, d = q.shape
+    hkv = k.shape[2]
+    offs = np.ascontiguousarray(np.asarray(offsets, dtype=np.int32))
+    scale = 1.0 / float(np.sqrt(d)) if softmax_scale is None else float(softmax_scale)
+    _check("sa_offset_attn_fwd", load_library().sa_offset_attn_fwd(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), _strides(q), _strides(k), _strides(o), b, n, h, hkv, d, window,
+        offs.ctypes.data if offs.size else None, int(offs.size), scale, o.data_ptr(), lse.data_ptr(),
+        _stream_ptr(stream)))
+
+
+def sa_fib_offsets(alpha_num: int, alpha_den: int, n_rungs: int, window: int, n_tokens: int) -> list[int]:
+    buf = (ctypes.c_int32 * 128)()
+    cnt = ctypes.c_int32(0)
+    _check("sa_fib_offsets", load_library().sa_fib_offsets(alpha_num, alpha_den, n_rungs, window, n_tokens,
+                                                            ctypes.cast(buf, _P), 128, ctypes.byref(cnt)))
+    return [int(buf[i]) for i in range(cnt.value)]
+
+
+def sa_block_ratios(data: np.ndarray, block: int, level: int = 6, n_threads: int = 0) -> np.ndarray:
+    """Host zlib ratios of ``uint8 [batch, n_tokens]``; returns float32 [batch, nb]."""
+    arr = np.ascontiguousarray(np.asarray(data, dtype=np.uint8))
+    if arr.ndim == 1:
+        arr = arr[None, :]
+    out = np.empty((arr.shape[0], arr.shape[1] // block), dtype=np.float32)
+    _check("sa_block_ratios", load_library().sa_block_ratios(arr.ctypes.data, arr.shape[0], arr.shape[1], block,
+                                                              level, out.ctypes.data, n_threads))
+    return out
+
+
+def sa_device_status(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device error status code."""
+    return int(load_library().sa_device_status(_stream_ptr(stream)))
+
+
+# ------------------------------------------------------------------ conveniences (allocation + one call)
+
+def build_mask(params: MaskParams, ratio=None, device="cuda"):
+    """Allocate CSR buffers of the exact size bound and build the mask."""
+    import torch
+    nb = params.n_tokens // params.block
+    cap = sa_mask_nnz_bound(params)
+    row_ptr = torch.empty((params.batch, nb + 1), dtype=torch.int32, device=device)
+    col_idx = torch.empty((max(cap, 1),), dtype=torch.int32, device=device)
+    sa_build_mask(params, ratio, row_ptr, col_idx)
+    return row_ptr, col_idx
+
+
+def attn_fwd(q, k, v, row_ptr, col_idx, block: int, causal: int, csr_shared: bool = False,
+             softmax_scale: float | None = None):
+    import torch
+    b, n, h, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((b, h, n), dtype=torch.float32, device=q.device)
+    sa_attn_fwd(q, k, v, row_ptr, col_idx, block, causal, o, lse, csr_shared, softmax_scale)
+    return o, lse
+
+
+def offset_attn_fwd(q, k, v, window: int, offsets, softmax_scale: float | None = None):
+    import torch
+    b, n, h, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((b, h, n), dtype=torch.float32, device=q.device)
+    sa_offset_attn_fwd(q, k, v, window, offsets, o, lse, softmax_scale)
+    return o, lse
+
+
+__all__ = [
+    "build_library", "load_library", "SAError", "MaskParams", "mask_params", "sa_mask_nnz_bound", "sa_build_mask",
+    "sa_attn_fwd", "sa_offset_attn_fwd", "sa_fib_offsets", "sa_block_ratios", "sa_device_status", "build_mask",
+    "attn_fwd", "offset_attn_fwd", "MASK_TOPK", "MASK_BIGBIRD", "MASK_FULL", "MASK_LITERAL_MEAN",
+]

@@ -1,0 +1,419 @@
+// GPU block-CSR builder: per-block ratios and pattern parameters -> row_ptr / col_idx.
+//
+// One CTA (1024 threads) per sequence. The CTA
+//   1. computes the per-sequence state the mode needs (ratio rank order for TOPK,
+//      literal flags from the mean threshold for LITERAL_MEAN),
+//   2. computes every row length and an exclusive scan of them (row_ptr), offset by the
+//      entries of the sequences before it,
+//   3. fills the rows, one warp per row, in ascending block order.
+// All decisions are integer or exact float compares, so the output is bit-identical
+// to the definitions in include/sa_api.h on every run.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sa_internal.h"
+
+namespace sa {
+namespace {
+
+constexpr int kThreads = 1024;
+constexpr int kWarps = kThreads / 32;
+
+struct MaskArgs {
+  int mode, block, nb, batch, causal, w, g, k, r;
+  uint64_t seed;
+  const float* ratio;
+  int32_t* row_ptr;
+  int32_t* col_idx;
+};
+
+// ---------------------------------------------------------------- Philox4x64-10
+// Salmon, Moraes, Dror, Shaw, SC'11: two 64x64->128 multiplies per round with the
+// published multipliers, key bumped by the Weyl constants between rounds.
+__device__ __forceinline__ uint64_t philox_word(uint64_t seed, uint64_t p) {
+  uint64_t c0 = p / 4 + 1, c1 = 0, c2 = 0, c3 = 0;
+  uint64_t k0 = seed, k1 = 0;
+  const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+#pragma unroll
+  for (int round = 0; round < 10; ++round) {
+    const uint64_t hi0 = __umul64hi(M0, c0), lo0 = M0 * c0;
+    const uint64_t hi1 = __umul64hi(M1, c2), lo1 = M1 * c2;
+    const uint64_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+    c0 = n0;
+    c1 = lo1;
+    c2 = n2;
+    c3 = lo0;
+    k0 += 0x9E3779B97F4A7C15ull;
+    k1 += 0xBB67AE8584CAA73Bull;
+  }
+  const uint32_t lane = static_cast<uint32_t>(p & 3u);
+  return lane == 0 ? c0 : lane == 1 ? c1 : lane == 2 ? c2 : c3;
+}
+
+// ---------------------------------------------------------------- block helpers
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+  unsigned m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// Sum of one int64 per thread over the CTA.
+__device__ int64_t block_sum(int64_t v, int64_t* red) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();
+  if (lane == 0) red[wid] = v;
+  __syncthreads();
+  int64_t t = 0;
+  for (int i = 0; i < kWarps; ++i) t += red[i];
+  __syncthreads();
+  return t;
+}
+
+__device__ double block_sum_f64(double v, double* red) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();
+  if (lane == 0) red[wid] = v;
+  __syncthreads();
+  double t = 0.0;
+  for (int i = 0; i < kWarps; ++i) t += red[i];
+  __syncthreads();
+  return t;
+}
+
+// In-place exclusive scan of a[0..n), n <= 4 * kThreads. Returns the total.
+__device__ int block_exclusive_scan(int* a, int n, int* tmp) {
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int per = (n + kThreads - 1) / kThreads;
+  const int base = tid * per;
+  int local[4];
+  int s = 0;
+  for (int i = 0; i < per; ++i) {
+    const int idx = base + i;
+    const int v = idx < n ? a[idx] : 0;
+    local[i] = s;
+    s += v;
+  }
+  int x = s;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  __syncthreads();
+  if (lane == 31) tmp[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    const int w = tmp[lane];
+    int wx = w;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, wx, o);
+      if (lane >= o) wx += y;
+    }
+    tmp[lane] = wx - w;
+    if (lane == 31) tmp[32] = wx;
+  }
+  __syncthreads();
+  const int excl = tmp[wid] + x - s;
+  for (int i = 0; i < per; ++i) {
+    const int idx = base + i;
+    if (idx < n) a[idx] = excl + local[i];
+  }
+  const int total = tmp[32];
+  __syncthreads();
+  return total;
+}
+
+// ---------------------------------------------------------------- per-mode pieces
+
+struct Smem {
+  float* r;        // [nb] ratios of the current sequence
+  int* order;      // [nb] TOPK: blocks by (ratio desc, index asc); LITERAL_MEAN: literal prefix [nb+1]
+  int* cnt;        // [nb] row lengths, scanned in place into row offsets
+  uint32_t* bm;    // [kWarps][words] per-warp bitmaps
+  int words;
+  int64_t* red;
+  double* redf;
+  int* scan_tmp;   // [33]
+};
+
+__device__ void load_ratios(const MaskArgs& a, const Smem& s, int seq) {
+  for (int j = threadIdx.x; j < a.nb; j += kThreads) s.r[j] = a.ratio[(size_t)seq * a.nb + j];
+  __syncthreads();
+}
+
+// TOPK: rank by (ratio desc, index asc) over all blocks; order[rank] = block.
+__device__ void topk_order(const MaskArgs& a, const Smem& s) {
+  for (int j = threadIdx.x; j < a.nb; j += kThreads) {
+    const float rj = s.r[j];
+    int rank = 0;
+    for (int t = 0; t < a.nb; ++t) {
+      const float rt = s.r[t];
+      rank += (rt > rj) || (rt == rj && t < j);
+    }
+    s.order[rank] = j;
+  }
+  __syncthreads();
+}
+
+// LITERAL_MEAN: literal flag l_j = (r_j > mean r); stored as prefix counts lit[0..nb].
+__device__ void literal_prefix(const MaskArgs& a, const Smem& s) {
+  double part = 0.0;
+  for (int j = threadIdx.x; j < a.nb; j += kThreads) part += (double)s.r[j];
+  const double mean = block_sum_f64(part, s.redf) / (double)a.nb;
+  int* lit = s.order;
+  for (int j = threadIdx.x; j < a.nb; j += kThreads) lit[j] = ((double)s.r[j] > mean) ? 1 : 0;
+  __syncthreads();
+  const int total = block_exclusive_scan(lit, a.nb, s.scan_tmp);
+  if (threadIdx.x == 0) lit[a.nb] = total;
+  __syncthreads();
+}
+
+__device__ __forceinline__ int lit_at(const int* litpre, int j) { return litpre[j + 1] - litpre[j]; }
+
+__device__ __forceinline__ int bigbird_wlo(const MaskArgs& a, int I) { return I - a.w / 2; }
+
+// Length of row I.
+__device__ int row_len(const MaskArgs& a, const Smem& s, int I) {
+  switch (a.mode) {
+    case SA_MASK_TOPK: {
+      const int n_w = min(a.w, I + 1);
+      const int n_g = max(0, min(a.g, I - a.w + 1));
+      const int n_c = max(0, I - a.w + 1 - a.g);
+      return n_w + n_g + min(a.k, n_c);
+    }
+    case SA_MASK_FULL:
+      return a.causal ? I + 1 : a.nb;
+    case SA_MASK_BIGBIRD: {
+      if (I < a.g) return a.nb;
+      const int g = min(a.g, a.nb);
+      const int lo = max(0, bigbird_wlo(a, I)), hi = min(a.nb - 1, bigbird_wlo(a, I) + a.w - 1);
+      const int n_w = max(0, hi - lo + 1);
+      const int n_wg = max(0, min(hi, g - 1) - lo + 1);  // window blocks that are global
+      const int n_union = n_w + g - n_wg;
+      return n_union + min(a.r, a.nb - n_union);
+    }
+    case SA_MASK_LITERAL_MEAN: {
+      const int* lp = s.order;
+      const int lo = max(0, I - a.w);
+      const int hi = a.causal ? I : min(a.nb - 1, I + a.w);
+      int n = hi - lo + 1;
+      if (lit_at(lp, I)) {
+        if (I - a.w - 1 >= 0) n += lp[I - a.w];                       // literals in [0, I-w-1]
+        if (!a.causal && I + a.w + 1 < a.nb) n += lp[a.nb] - lp[I + a.w + 1];
+      }
+      return n;
+    }
+  }
+  return 0;
+}
+
+// Total entries of one sequence (state for that sequence already in smem).
+__device__ int64_t seq_total(const MaskArgs& a, const Smem& s) {
+  int64_t part = 0;
+  for (int I = threadIdx.x; I < a.nb; I += kThreads) part += row_len(a, s, I);
+  return block_sum(part, s.red);
+}
+
+// ---------------------------------------------------------------- row fills (one warp)
+
+__device__ void fill_topk(const MaskArgs& a, const Smem& s, int I, int32_t* out, uint32_t* bm) {
+  const int lane = threadIdx.x & 31;
+  const int n_w = min(a.w, I + 1);
+  const int n_g = max(0, min(a.g, I - a.w + 1));
+  const int hi_c = I - a.w;                                  // candidates [g, hi_c]
+  const int n_c = max(0, hi_c - a.g + 1);
+  const int kk = min(a.k, n_c);
+  for (int j = lane; j < n_g; j += 32) out[j] = j;
+  if (kk == n_c) {
+    for (int j = lane; j < n_c; j += 32) out[n_g + j] = a.g + j;
+  } else if (kk > 0) {
+    for (int wd = (a.g >> 5) + lane; wd <= (hi_c >> 5); wd += 32) bm[wd] = 0u;
+    __syncwarp();
+    int taken = 0;
+    for (int base = 0; base < a.nb && taken < kk; base += 32) {
+      const int J = (base + lane < a.nb) ? s.order[base + lane] : -1;
+      const bool cand = J >= a.g && J <= hi_c;
+      const unsigned m = __ballot_sync(0xffffffffu, cand);
+      const int before = __popc(m & lanemask_lt());
+      if (cand && taken + before < kk) atomicOr(&bm[J >> 5], 1u << (J & 31));
+      taken += __popc(m);
+    }
+    __syncwarp();
+    int pos = n_g;
+    for (int base = a.g; base <= hi_c; base += 32) {
+      const int J = base + lane;
+      const bool sel = J <= hi_c && ((bm[J >> 5] >> (J & 31)) & 1u);
+      const unsigned m = __ballot_sync(0xffffffffu, sel);
+      if (sel) out[pos + __popc(m & lanemask_lt())] = J;
+      pos += __popc(m);
+    }
+    __syncwarp();
+  }
+  for (int j = lane; j < n_w; j += 32) out[n_g + kk + j] = I - n_w + 1 + j;
+}
+
+__device__ void fill_literal_mean(const MaskArgs& a, const Smem& s, int I, int32_t* out) {
+  const int lane = threadIdx.x & 31;
+  const int* lp = s.order;
+  const bool lit_i = lit_at(lp, I) != 0;
+  const int lo = lit_i ? 0 : max(0, I - a.w);
+  const int hi = a.causal ? I : (lit_i ? a.nb - 1 : min(a.nb - 1, I + a.w));
+  int pos = 0;
+  for (int base = lo; base <= hi; base += 32) {
+    const int J = base + lane;
+    bool sel = false;
+    if (J <= hi) {
+      const int dist = J > I ? J - I : I - J;
+      sel = dist <= a.w || (lit_i && lit_at(lp, J) && dist > a.w);
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, sel);
+    if (sel) out[pos + __popc(m & lanemask_lt())] = J;
+    pos += __popc(m);
+  }
+}
+
+__device__ void fill_bigbird(const MaskArgs& a, int I, int32_t* out, int* picks) {
+  const int lane = threadIdx.x & 31;
+  if (I < a.g) {
+    for (int j = lane; j < a.nb; j += 32) out[j] = j;
+    return;
+  }
+  const int g = min(a.g, a.nb);
+  const int wlo = max(0, bigbird_wlo(a, I));
+  const int whi = min(a.nb - 1, bigbird_wlo(a, I) + a.w - 1);
+  // Interval part: [0, g) u [wlo, whi] as at most two disjoint ascending segments.
+  int s0lo = 0, s0hi = g - 1, s1lo = wlo, s1hi = whi;         // inclusive bounds
+  if (whi < wlo) { s1lo = 1; s1hi = 0; }                       // empty window
+  if (s1lo <= s1hi && s1lo <= g) {                             // overlapping / adjacent
+    s0hi = max(s0hi, s1hi);
+    s1lo = 1;
+    s1hi = 0;
+  }
+  const int n0 = max(0, s0hi - s0lo + 1), n1 = max(0, s1hi - s1lo + 1);
+  const int n_int = n0 + n1;
+  // Candidates A = [g, nb) minus [wlo, whi], ascending: segment a1 = [g, wlo), a2 = [max(g, whi+1), nb).
+  const int a1 = max(0, wlo - g);
+  const int a2start = max(g, whi + 1);
+  const int a2 = max(0, a.nb - a2start);
+  const int n_a = (whi < wlo) ? (a.nb - g) : a1 + a2;
+  const int n_r = min(a.r, n_a);
+  if (lane == 0) {
+    // picks[0..n_r): chosen indices into A, kept sorted ascending.
+    for (int t = 0; t < n_r; ++t) {
+      const uint64_t x = philox_word(static_cast<uint64_t>(a.seed), (uint64_t)I * (uint64_t)a.r + (uint64_t)t);
+      const uint64_t remaining = (uint64_t)(n_a - t);
+      int j = (int)(((x >> 32) * remaining) >> 32);
+      int ins = 0;
+      for (; ins < t; ++ins) {
+        if (picks[ins] <= j) ++j;
+        else break;
+      }
+      for (int u = t; u > ins; --u) picks[u] = picks[u - 1];
+      picks[ins] = j;
+    }
+    for (int t = 0; t < n_r; ++t) {                            // A-index -> block index
+      const int m = picks[t];
+      picks[t] = (whi < wlo) ? g + m : (m < a1 ? g + m : a2start + (m - a1));
+    }
+  }
+  __syncwarp();
+  for (int e = lane; e < n_int; e += 32) {
+    const int x = e < n0 ? s0lo + e : s1lo + (e - n0);
+    int below = 0;
+    for (int t = 0; t < n_r; ++t) below += picks[t] < x;
+    out[e + below] = x;
+  }
+  for (int t = lane; t < n_r; t += 32) {
+    const int x = picks[t];
+    const int below = max(0, min(x, s0hi + 1) - s0lo) + max(0, min(x, s1hi + 1) - s1lo);
+    out[below + t] = x;
+  }
+  __syncwarp();
+}
+
+__global__ void __launch_bounds__(kThreads) build_mask_kernel(MaskArgs a) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  __shared__ int64_t red[kWarps];
+  __shared__ double redf[kWarps];
+  __shared__ int scan_tmp[33];
+  __shared__ int picks_all[kWarps][kMaxRandomBlocks];
+  const int seq = blockIdx.x;
+  Smem s;
+  s.words = (a.nb + 31) / 32;
+  s.r = reinterpret_cast<float*>(smem_raw);
+  s.order = reinterpret_cast<int*>(s.r + a.nb);
+  s.cnt = s.order + (a.nb + 1);
+  s.bm = reinterpret_cast<uint32_t*>(s.cnt + a.nb);
+  s.red = red;
+  s.redf = redf;
+  s.scan_tmp = scan_tmp;
+
+  // Entries of the sequences before this one.
+  int64_t base = 0;
+  if (a.mode == SA_MASK_LITERAL_MEAN) {
+    for (int p = 0; p < seq; ++p) {
+      load_ratios(a, s, p);
+      literal_prefix(a, s);
+      base += seq_total(a, s);
+    }
+  }
+  const bool needs_ratio = a.mode == SA_MASK_TOPK || a.mode == SA_MASK_LITERAL_MEAN;
+  if (needs_ratio) load_ratios(a, s, seq);
+  if (a.mode == SA_MASK_TOPK) topk_order(a, s);
+  if (a.mode == SA_MASK_LITERAL_MEAN) literal_prefix(a, s);
+  if (a.mode != SA_MASK_LITERAL_MEAN) base = (int64_t)seq * seq_total(a, s);
+
+  for (int I = threadIdx.x; I < a.nb; I += kThreads) s.cnt[I] = row_len(a, s, I);
+  __syncthreads();
+  const int total = block_exclusive_scan(s.cnt, a.nb, s.scan_tmp);
+  int32_t* rp = a.row_ptr + (size_t)seq * (a.nb + 1);
+  for (int I = threadIdx.x; I < a.nb; I += kThreads) rp[I] = (int32_t)(base + s.cnt[I]);
+  if (threadIdx.x == 0) rp[a.nb] = (int32_t)(base + total);
+
+  const int wid = threadIdx.x >> 5;
+  uint32_t* bm = s.bm + (size_t)wid * s.words;
+  for (int I = wid; I < a.nb; I += kWarps) {
+    int32_t* out = a.col_idx + base + s.cnt[I];
+    switch (a.mode) {
+      case SA_MASK_TOPK: fill_topk(a, s, I, out, bm); break;
+      case SA_MASK_LITERAL_MEAN: fill_literal_mean(a, s, I, out); break;
+      case SA_MASK_BIGBIRD: fill_bigbird(a, I, out, picks_all[wid]); break;
+      case SA_MASK_FULL: {
+        const int n = a.causal ? I + 1 : a.nb;
+        for (int j = threadIdx.x & 31; j < n; j += 32) out[j] = j;
+        break;
+      }
+    }
+  }
+}
+
+}  // namespace
+
+int launch_build_mask(const sa_mask_params& p, const float* d_ratio, int32_t* d_row_ptr, int32_t* d_col_idx,
+                      cudaStream_t stream) {
+  MaskArgs a;
+  a.mode = p.mode;
+  a.block = p.block;
+  a.nb = p.n_tokens / p.block;
+  a.batch = p.batch;
+  a.causal = p.causal;
+  a.w = p.window_blocks;
+  a.g = p.global_blocks;
+  a.k = p.topk;
+  a.r = p.random_blocks;
+  a.seed = p.seed;
+  a.ratio = d_ratio;
+  a.row_ptr = d_row_ptr;
+  a.col_idx = d_col_idx;
+  const int words = (a.nb + 31) / 32;
+  const size_t smem = (size_t)a.nb * 4 + (size_t)(a.nb + 1) * 4 + (size_t)a.nb * 4 + (size_t)kWarps * words * 4;
+  if (cudaFuncSetAttribute(build_mask_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
+    return SA_ERR_CUDA;
+  build_mask_kernel<<<a.batch, kThreads, smem, stream>>>(a);
+  return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+}
+
+}  // namespace sa

@@ -1,0 +1,324 @@
+// Host side of the C ABI declared in include/sa_api.h: argument validation, the
+// closed-form CSR size bound, Fibonacci offsets, host zlib ratios and kernel dispatch.
+#include <dlfcn.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <algorithm>
+#include <atomic>
+#include <thread>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "sa_api.h"
+#include "sa_internal.h"
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool strides_ok(const int64_t s[3]) {
+  for (int i = 0; i < 3; ++i)
+    if (s[i] <= 0 || (s[i] * 2) % 16 != 0) return false;
+  return true;
+}
+
+// The kernels are built for sm_103a only (GB300); refuse any other device up front.
+bool device_ok() {
+  static int cached[64] = {0};   // 0 unknown, 1 ok, 2 not ok
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return false;
+  if (dev < 64 && cached[dev]) return cached[dev] == 1;
+  int major = 0, minor = 0;
+  const bool ok = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+                  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
+                  major == 10 && minor == 3;
+  if (dev < 64) cached[dev] = ok ? 1 : 2;
+  return ok;
+}
+
+int64_t nnz_bound(const sa_mask_params& p) {
+  const int64_t nb = p.n_tokens / p.block;
+  int64_t per_seq = 0;
+  for (int64_t I = 0; I < nb; ++I) {
+    switch (p.mode) {
+      case SA_MASK_TOPK: {
+        const int64_t n_w = std::min<int64_t>(p.window_blocks, I + 1);
+        const int64_t n_g = std::max<int64_t>(0, std::min<int64_t>(p.global_blocks, I - p.window_blocks + 1));
+        const int64_t n_c = std::max<int64_t>(0, I - p.window_blocks + 1 - p.global_blocks);
+        per_seq += n_w + n_g + std::min<int64_t>(p.topk, n_c);
+        break;
+      }
+      case SA_MASK_FULL:
+        per_seq += p.causal ? I + 1 : nb;
+        break;
+      case SA_MASK_BIGBIRD: {
+        if (I < p.global_blocks) {
+          per_seq += nb;
+          break;
+        }
+        const int64_t g = std::min<int64_t>(p.global_blocks, nb);
+        const int64_t wlo_raw = I - p.window_blocks / 2;
+        const int64_t lo = std::max<int64_t>(0, wlo_raw), hi = std::min<int64_t>(nb - 1, wlo_raw + p.window_blocks - 1);
+        const int64_t n_w = std::max<int64_t>(0, hi - lo + 1);
+        const int64_t n_wg = std::max<int64_t>(0, std::min<int64_t>(hi, g - 1) - lo + 1);
+        const int64_t n_union = n_w + g - n_wg;
+        per_seq += n_union + std::min<int64_t>(p.random_blocks, nb - n_union);
+        break;
+      }
+      case SA_MASK_LITERAL_MEAN:
+        per_seq += p.causal ? I + 1 : nb;   // every block literal
+        break;
+    }
+  }
+  return per_seq * p.batch;
+}
+
+int check_mask_params(const sa_mask_params* p) {
+  if (!p) return SA_ERR_INVALID_ARG;
+  if (p->mode < SA_MASK_TOPK || p->mode > SA_MASK_LITERAL_MEAN) return SA_ERR_INVALID_ARG;
+  if (p->block <= 0 || p->n_tokens <= 0 || p->batch <= 0 || p->n_tokens % p->block != 0) return SA_ERR_INVALID_ARG;
+  if (p->window_blocks < 0 || p->global_blocks < 0 || p->topk < 0 || p->random_blocks < 0 || p->reserved != 0)
+    return SA_ERR_INVALID_ARG;
+  if (p->causal != 0 && p->causal != 1) return SA_ERR_INVALID_ARG;
+  if (p->n_tokens / p->block > sa::kMaxMaskBlocks) return SA_ERR_UNSUPPORTED;
+  if (p->mode == SA_MASK_TOPK && !p->causal) return SA_ERR_UNSUPPORTED;
+  if (p->mode == SA_MASK_BIGBIRD && p->causal) return SA_ERR_UNSUPPORTED;
+  if (p->mode == SA_MASK_BIGBIRD && p->random_blocks > sa::kMaxRandomBlocks) return SA_ERR_UNSUPPORTED;
+  if (p->mode == SA_MASK_LITERAL_MEAN && p->global_blocks != 0) return SA_ERR_UNSUPPORTED;
+  return SA_OK;
+}
+
+int check_attn_common(const void* q, const void* k, const void* v, const int64_t qs[3], const int64_t kvs[3],
+                      const int64_t os[3], int32_t batch, int32_t n_tokens, int32_t heads, int32_t kv_heads, void* o,
+                      float* lse) {
+  if (!q || !k || !v || !qs || !kvs || !os || !o || !lse) return SA_ERR_INVALID_ARG;
+  if (batch <= 0 || n_tokens <= 0 || heads <= 0 || kv_heads <= 0 || heads % kv_heads != 0) return SA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return SA_ERR_UNSUPPORTED;
+  if (!strides_ok(qs) || !strides_ok(kvs) || !strides_ok(os)) return SA_ERR_UNSUPPORTED;
+  return SA_OK;
+}
+
+// ---------------------------------------------------------------- zlib (loaded at run time)
+
+typedef int (*compress2_fn)(unsigned char*, unsigned long*, const unsigned char*, unsigned long, int);
+typedef unsigned long (*compress_bound_fn)(unsigned long);
+
+struct Zlib {
+  compress2_fn compress2 = nullptr;
+  compress_bound_fn bound = nullptr;
+};
+
+const Zlib& zlib() {
+  static Zlib z;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* h = dlopen("libz.so.1", RTLD_NOW | RTLD_LOCAL);
+    if (!h) h = dlopen("libz.so", RTLD_NOW | RTLD_LOCAL);
+    if (h) {
+      z.compress2 = reinterpret_cast<compress2_fn>(dlsym(h, "compress2"));
+      z.bound = reinterpret_cast<compress_bound_fn>(dlsym(h, "compressBound"));
+    }
+  }
+  return z;
+}
+
+}  // namespace
+
+extern "C" {
+
+int sa_version(void) { return 1; }
+
+const char* sa_status_string(int status) {
+  switch (status) {
+    case SA_OK: return "SA_OK";
+    case SA_ERR_INVALID_ARG: return "SA_ERR_INVALID_ARG";
+    case SA_ERR_UNSUPPORTED: return "SA_ERR_UNSUPPORTED";
+    case SA_ERR_CAPACITY: return "SA_ERR_CAPACITY";
+    case SA_ERR_CUDA: return "SA_ERR_CUDA";
+    case SA_ERR_TIMEOUT: return "SA_ERR_TIMEOUT";
+    case SA_ERR_DEVICE: return "SA_ERR_DEVICE";
+  }
+  return "SA_ERR_UNKNOWN";
+}
+
+int sa_mask_nnz_bound(const sa_mask_params* params, int64_t* h_nnz) {
+  const int st = check_mask_params(params);
+  if (st != SA_OK) return st;
+  if (!h_nnz) return SA_ERR_INVALID_ARG;
+  *h_nnz = nnz_bound(*params);
+  return SA_OK;
+}
+
+int sa_build_mask(const sa_mask_params* params, const float* d_ratio, int32_t* d_row_ptr, int32_t* d_col_idx,
+                  int64_t col_capacity, void* stream) {
+  const int st = check_mask_params(params);
+  if (st != SA_OK) return st;
+  if (!d_row_ptr || !d_col_idx) return SA_ERR_INVALID_ARG;
+  const bool needs_ratio = params->mode == SA_MASK_TOPK || params->mode == SA_MASK_LITERAL_MEAN;
+  if (needs_ratio && !d_ratio) return SA_ERR_INVALID_ARG;
+  const int64_t need = nnz_bound(*params);
+  if (need > INT32_MAX) return SA_ERR_UNSUPPORTED;
+  if (col_capacity < need) return SA_ERR_CAPACITY;
+  if (!device_ok()) return SA_ERR_CUDA;
+  return sa::launch_build_mask(*params, d_ratio, d_row_ptr, d_col_idx, static_cast<cudaStream_t>(stream));
+}
+
+int sa_attn_fwd(const void* q, const void* k, const void* v, const int64_t q_strides[3], const int64_t kv_strides[3],
+                const int64_t o_strides[3], int32_t batch, int32_t n_tokens, int32_t heads, int32_t kv_heads,
+                int32_t head_dim, int32_t block, int32_t causal, const int32_t* d_row_ptr, const int32_t* d_col_idx,
+                int32_t csr_shared, float softmax_scale, void* o, float* lse, void* stream) {
+  int st = check_attn_common(q, k, v, q_strides, kv_strides, o_strides, batch, n_tokens, heads, kv_heads, o, lse);
+  if (st != SA_OK) return st;
+  if (!d_row_ptr || !d_col_idx) return SA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return SA_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f)) return SA_ERR_INVALID_ARG;
+  if (head_dim != 32 && head_dim != 64 && head_dim != 128) return SA_ERR_UNSUPPORTED;
+  if (block != 32 && block != 64 && block != 128) return SA_ERR_UNSUPPORTED;
+  if (n_tokens % block != 0) return SA_ERR_UNSUPPORTED;
+  if ((int64_t)batch * heads > 65535 * 32 || (n_tokens + 127) / 128 > 65535) return SA_ERR_UNSUPPORTED;
+  if (!device_ok()) return SA_ERR_CUDA;
+  sa::AttnArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  for (int i = 0; i < 3; ++i) {
+    a.q_strides[i] = q_strides[i];
+    a.kv_strides[i] = kv_strides[i];
+    a.o_strides[i] = o_strides[i];
+  }
+  a.batch = batch;
+  a.n_tokens = n_tokens;
+  a.heads = heads;
+  a.kv_heads = kv_heads;
+  a.head_dim = head_dim;
+  a.block = block;
+  a.causal = causal;
+  a.csr_shared = csr_shared != 0;
+  a.row_ptr = d_row_ptr;
+  a.col_idx = d_col_idx;
+  a.softmax_scale = softmax_scale;
+  return sa::launch_attn_fwd(a, static_cast<cudaStream_t>(stream));
+}
+
+int sa_offset_attn_fwd(const void* q, const void* k, const void* v, const int64_t q_strides[3],
+                       const int64_t kv_strides[3], const int64_t o_strides[3], int32_t batch, int32_t n_tokens,
+                       int32_t heads, int32_t kv_heads, int32_t head_dim, int32_t window, const int32_t* h_offsets,
+                       int32_t n_offsets, float softmax_scale, void* o, float* lse, void* stream) {
+  int st = check_attn_common(q, k, v, q_strides, kv_strides, o_strides, batch, n_tokens, heads, kv_heads, o, lse);
+  if (st != SA_OK) return st;
+  if (n_offsets < 0 || (n_offsets > 0 && !h_offsets)) return SA_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f)) return SA_ERR_INVALID_ARG;
+  if (window < 0) return SA_ERR_INVALID_ARG;
+  if (window > sa::kMaxWindow || n_offsets > sa::kMaxOffsets) return SA_ERR_UNSUPPORTED;
+  if (head_dim != 64) return SA_ERR_UNSUPPORTED;
+  for (int i = 0; i < n_offsets; ++i) {
+    if (h_offsets[i] <= window || h_offsets[i] >= n_tokens) return SA_ERR_INVALID_ARG;
+    if (i > 0 && h_offsets[i] <= h_offsets[i - 1]) return SA_ERR_INVALID_ARG;
+  }
+  if ((int64_t)batch * heads > 65535 * 32 || (n_tokens + 127) / 128 > 65535) return SA_ERR_UNSUPPORTED;
+  if (!device_ok()) return SA_ERR_CUDA;
+  sa::OffsetArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  for (int i = 0; i < 3; ++i) {
+    a.q_strides[i] = q_strides[i];
+    a.kv_strides[i] = kv_strides[i];
+    a.o_strides[i] = o_strides[i];
+  }
+  a.batch = batch;
+  a.n_tokens = n_tokens;
+  a.heads = heads;
+  a.kv_heads = kv_heads;
+  a.head_dim = head_dim;
+  a.window = window;
+  a.n_offsets = n_offsets;
+  for (int i = 0; i < sa::kMaxOffsets; ++i) a.offsets[i] = i < n_offsets ? h_offsets[i] : 0;
+  a.softmax_scale = softmax_scale;
+  return sa::launch_offset_attn_fwd(a, static_cast<cudaStream_t>(stream));
+}
+
+int sa_fib_offsets(int32_t alpha_num, int32_t alpha_den, int32_t n_rungs, int32_t window, int32_t n_tokens,
+                   int32_t* h_out, int32_t capacity, int32_t* h_count) {
+  if (alpha_num <= 0 || alpha_den <= 0 || n_rungs < 0 || window < 0 || n_tokens <= 0 || !h_count ||
+      capacity < 0 || (capacity > 0 && !h_out))
+    return SA_ERR_INVALID_ARG;
+  std::vector<int64_t> out;
+  int64_t a = 1, b = 2;
+  for (int k = 0;; ++k) {
+    if (n_rungs > 0 ? k >= n_rungs : a > n_tokens) break;
+    // round_half_even(alpha_num * f / alpha_den) in integer arithmetic
+    const int64_t num = 2 * (int64_t)alpha_num * a + alpha_den;
+    const int64_t den2 = 2 * (int64_t)alpha_den;
+    int64_t q = num / den2;
+    if (num % den2 == 0 && (q & 1)) --q;   // exact tie: go to the even neighbour
+    if (q > window && q < n_tokens && std::find(out.begin(), out.end(), q) == out.end()) out.push_back(q);
+    const int64_t nxt = a + b;
+    a = b;
+    b = nxt;
+    if (a > (int64_t)1 << 40) break;
+  }
+  std::sort(out.begin(), out.end());
+  *h_count = (int32_t)out.size();
+  if ((int64_t)out.size() > capacity) return SA_ERR_CAPACITY;
+  for (size_t i = 0; i < out.size(); ++i) h_out[i] = (int32_t)out[i];
+  return SA_OK;
+}
+
+int sa_block_ratios(const uint8_t* h_bytes, int32_t batch, int32_t n_tokens, int32_t block, int32_t level,
+                    float* h_ratio, int32_t n_threads) {
+  if (!h_bytes || !h_ratio || batch <= 0 || n_tokens <= 0 || block <= 0 || n_tokens % block != 0 || level < 0 ||
+      level > 9 || n_threads < 0)
+    return SA_ERR_INVALID_ARG;
+  const Zlib& z = zlib();
+  if (!z.compress2 || !z.bound) return SA_ERR_UNSUPPORTED;
+  const int64_t nb = n_tokens / block;
+  const int64_t total = nb * batch;
+  int threads = n_threads > 0 ? n_threads : (int)std::max(1u, std::thread::hardware_concurrency());
+  threads = (int)std::min<int64_t>(threads, std::max<int64_t>(1, total / 64));
+  std::atomic<int> failed{0};
+  auto work = [&](int64_t begin, int64_t end) {
+    std::vector<unsigned char> buf(z.bound((unsigned long)block));
+    for (int64_t idx = begin; idx < end; ++idx) {
+      const int64_t s = idx / nb, i = idx % nb;
+      unsigned long out_len = (unsigned long)buf.size();
+      if (z.compress2(buf.data(), &out_len, h_bytes + s * (int64_t)n_tokens + i * block, (unsigned long)block, level) !=
+          0) {
+        failed = 1;
+        return;
+      }
+      h_ratio[idx] = (float)((double)out_len / (double)block);
+    }
+  };
+  if (threads <= 1) {
+    work(0, total);
+  } else {
+    std::vector<std::thread> pool;
+    const int64_t per = (total + threads - 1) / threads;
+    for (int t = 0; t < threads; ++t) {
+      const int64_t b0 = t * per, b1 = std::min(total, b0 + per);
+      if (b0 < b1) pool.emplace_back(work, b0, b1);
+    }
+    for (auto& th : pool) th.join();
+  }
+  return failed ? SA_ERR_UNSUPPORTED : SA_OK;
+}
+
+int sa_device_status(void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SA_ERR_CUDA;
+  const unsigned int e = sa::attn_read_and_clear_error(s) | sa::offset_read_and_clear_error(s);
+  if (cudaGetLastError() != cudaSuccess) return SA_ERR_CUDA;
+  if (e & sa::kErrTimeout) return SA_ERR_TIMEOUT;
+  if (e & sa::kErrBadIndex) return SA_ERR_DEVICE;
+  return SA_OK;
+}
+
+}  // extern "C"

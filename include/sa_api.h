@@ -1,0 +1,169 @@
+/*
+ * sa_api.h - C ABI of the GB300 (sm_103a) sparse-graph attention library (libsa.so).
+ *
+ * The library computes attention restricted to a sparse key graph:
+ *   - block graphs given as a CSR list of key blocks per query block, built on the GPU
+ *     from per-block compression ratios ("Parameter-free Adaptive Sparse Attention via
+ *     Compression-Based Content Selection", section 3.1 Eq. 1-2, section 3.2 Eq. 3,
+ *     Appendix B Algorithm 1) or from the BigBird window/global/random pattern
+ *     ("BigBird", section 2 "Derivation");
+ *   - token-granular graphs made of a dense window plus alpha-scaled Fibonacci offsets
+ *     ("Depth-Staggered Fibonacci Spacing for Sparse Attention", section 2 "Method").
+ *
+ * Conventions (all entry points):
+ *   - Device pointers are marked d_*, host pointers h_*; q/k/v/o/lse are device memory.
+ *   - The caller owns all memory. The library allocates no device memory and keeps no
+ *     state besides a per-library device error word (see sa_device_status).
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream). Argument errors are returned synchronously before anything is launched.
+ *   - Tensors q, k, v, o are bf16 with layout [batch, tokens, heads, head_dim]:
+ *     head_dim contiguous, and strides[3] = {batch, token, head} strides in ELEMENTS.
+ *     Every stride times 2 bytes and every base pointer must be a multiple of 16 bytes.
+ *     LSE is fp32 [batch, heads, tokens], contiguous, natural logarithm.
+ *   - Attention: s_ij = softmax_scale * <q_i, k_j> over the allowed keys j of query i;
+ *     LSE_i = ln sum_j exp(s_ij); O_i = sum_j exp(s_ij - LSE_i) v_j. A query with no
+ *     allowed key gets O_i = 0 and LSE_i = -inf. Query head h reads key/value head
+ *     h / (heads / kv_heads) (grouped-query attention).
+ *   - There is no CPU fallback: without a usable sm_103a device every compute entry
+ *     point returns SA_ERR_CUDA or SA_ERR_UNSUPPORTED.
+ */
+#ifndef SA_API_H
+#define SA_API_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SA_OK = 0,
+  SA_ERR_INVALID_ARG = -1, /* null pointer, negative size, inconsistent shapes        */
+  SA_ERR_UNSUPPORTED = -2, /* valid request outside the supported shapes / modes      */
+  SA_ERR_CAPACITY = -3,    /* caller buffer too small (e.g. col_idx capacity)         */
+  SA_ERR_CUDA = -4,        /* a CUDA runtime call or kernel launch failed             */
+  SA_ERR_TIMEOUT = -5,     /* a bounded device-side wait expired (sa_device_status)   */
+  SA_ERR_DEVICE = -6       /* a kernel found invalid data, e.g. an out-of-range CSR   */
+} sa_status;
+
+typedef enum {
+  /* Compression-guided, causal. Row I = window W(I) = [max(0, I-w+1), I] (w blocks
+   * counting the diagonal) u global key blocks {J < g, J <= I} u the top-k blocks of
+   * C(I) = [0, I] minus window and globals, ordered by ratio descending then block
+   * index ascending. The top-k rule is the workload's reading of "literal" blocks;
+   * the page's own rule is SA_MASK_LITERAL_MEAN. */
+  SA_MASK_TOPK = 0,
+  /* BigBird, bidirectional ("BigBird", section 2): global rows I < g attend to every
+   * block; other rows attend to window [I - w/2, I - w/2 + w - 1], the g global
+   * blocks, and r random blocks drawn without replacement from the remaining blocks
+   * with the Philox4x64-10 stream (Salmon et al., SC'11) keyed by `seed`: draw t of
+   * row I takes word p = I*r + t of the stream
+   *   word(p) = Philox4x64_10(counter = (p/4 + 1, 0, 0, 0), key = (seed, 0))[p % 4]
+   * and picks index ((word >> 32) * |A|) >> 32 of the ascending remaining list A. */
+  SA_MASK_BIGBIRD = 1,
+  /* Every block J <= I (causal) or every block (bidirectional). */
+  SA_MASK_FULL = 2,
+  /* "Parameter-free Adaptive Sparse Attention ...", Eq. 2-3 / Algorithm 1: block i is
+   * literal iff r_i > mean(r); M = {|I-J| <= w} u identity u {literal I and J,
+   * |I-J| > w}; causal keeps J <= I. global_blocks must be 0. */
+  SA_MASK_LITERAL_MEAN = 3
+} sa_mask_mode;
+
+typedef struct {
+  int32_t mode;          /* sa_mask_mode                                               */
+  int32_t block;         /* b: 32, 64 or 128 tokens per block                           */
+  int32_t n_tokens;      /* N, a multiple of b; nb = N / b <= 4096                      */
+  int32_t batch;         /* number of sequences (one CSR per sequence)                  */
+  int32_t causal;        /* 1 = causal (TOPK requires 1, BIGBIRD requires 0)            */
+  int32_t window_blocks; /* w (meaning per mode, see sa_mask_mode)                      */
+  int32_t global_blocks; /* g                                                           */
+  int32_t topk;          /* k (TOPK)                                                    */
+  int32_t random_blocks; /* r (BIGBIRD), <= 64                                          */
+  int32_t reserved;      /* must be 0                                                   */
+  uint64_t seed;         /* Philox key (BIGBIRD)                                        */
+} sa_mask_params;
+
+/* Upper bound on the number of CSR entries sa_build_mask writes for these parameters
+ * (exact for TOPK, BIGBIRD and FULL, whose row lengths do not depend on the ratios;
+ * the all-literal worst case for LITERAL_MEAN). Host only; no device work. */
+int sa_mask_nnz_bound(const sa_mask_params* params, int64_t* h_nnz);
+
+/* Build the block CSR of every sequence on the GPU.
+ *   d_ratio   : fp32 [batch][nb] per-block compression ratios (Eq. 1); finite values.
+ *               Read by TOPK and LITERAL_MEAN, may be NULL for the other modes.
+ *   d_row_ptr : int32 [batch][nb + 1], written. Offsets are absolute into d_col_idx:
+ *               sequence s occupies [row_ptr[s][0], row_ptr[s][nb]), and
+ *               row_ptr[s][0] == row_ptr[s-1][nb].
+ *   d_col_idx : int32 [col_capacity], written; each row ascending and duplicate-free.
+ * Returns SA_ERR_CAPACITY (nothing launched) if col_capacity < sa_mask_nnz_bound.
+ * The output is a pure function of (params, ratios): bit-identical on every run. */
+int sa_build_mask(const sa_mask_params* params, const float* d_ratio, int32_t* d_row_ptr, int32_t* d_col_idx,
+                  int64_t col_capacity, void* stream);
+
+/* Block-sparse attention forward over a block CSR (tcgen05 / TMEM / TMA kernel).
+ * Token pair (i, j) is attended iff blk(j) is in row(blk(i)) and, if causal, j <= i
+ * ("Parameter-free Adaptive Sparse Attention ...", section 3.4 "Block-to-token
+ * expansion"; "BigBird", section 3: a production kernel gathers the selected keys
+ * instead of masking N x N scores).
+ *   q [batch, n_tokens, heads, head_dim], k/v [batch, n_tokens, kv_heads, head_dim]
+ *   q_strides / kv_strides / o_strides : element strides {batch, token, head}
+ *   head_dim in {32, 64, 128}; block in {32, 64, 128}; n_tokens % block == 0;
+ *   heads % kv_heads == 0.
+ *   d_row_ptr / d_col_idx : CSR as written by sa_build_mask. If csr_shared != 0 every
+ *   sequence uses the CSR of sequence 0, else sequence s uses row_ptr[s][*].
+ *   Column indices must lie in [0, nb); rows must be ascending without duplicates.
+ *   An out-of-range index is skipped and reported as SA_ERR_DEVICE by
+ *   sa_device_status.
+ *   o : bf16 output, lse : fp32 [batch, heads, n_tokens]. */
+int sa_attn_fwd(const void* q, const void* k, const void* v, const int64_t q_strides[3],
+                const int64_t kv_strides[3], const int64_t o_strides[3], int32_t batch, int32_t n_tokens,
+                int32_t heads, int32_t kv_heads, int32_t head_dim, int32_t block, int32_t causal,
+                const int32_t* d_row_ptr, const int32_t* d_col_idx, int32_t csr_shared, float softmax_scale,
+                void* o, float* lse, void* stream);
+
+/* Token-granular window-plus-offset attention forward ("Depth-Staggered Fibonacci
+ * Spacing ...", section 2 "Attended set"): query i attends to keys
+ *   { i - delta : delta in {0, ..., window} u offsets, i - delta >= 0 }   (a set).
+ *   h_offsets : host int32[n_offsets], strictly ascending, each > window and
+ *               < n_tokens (see sa_fib_offsets); n_offsets <= 64.
+ *   window in [0, 64]; head_dim == 64; other arguments as in sa_attn_fwd. */
+int sa_offset_attn_fwd(const void* q, const void* k, const void* v, const int64_t q_strides[3],
+                       const int64_t kv_strides[3], const int64_t o_strides[3], int32_t batch, int32_t n_tokens,
+                       int32_t heads, int32_t kv_heads, int32_t head_dim, int32_t window, const int32_t* h_offsets,
+                       int32_t n_offsets, float softmax_scale, void* o, float* lse, void* stream);
+
+/* Distinct offsets d_k = round_half_even(alpha * f_k), alpha = alpha_num / alpha_den > 0,
+ * over Fibonacci rungs f = 1, 2, 3, 5, 8, ... ("Depth-Staggered Fibonacci Spacing ...",
+ * section 2: K = 15 rungs up to 987). n_rungs > 0 takes the first n_rungs rungs;
+ * n_rungs == 0 takes every rung f_k <= n_tokens. Only offsets with
+ * window < d < n_tokens are returned (the window already covers the others), ascending,
+ * in h_out[0 .. *h_count). Host only. Returns SA_ERR_CAPACITY if capacity is short. */
+int sa_fib_offsets(int32_t alpha_num, int32_t alpha_den, int32_t n_rungs, int32_t window, int32_t n_tokens,
+                   int32_t* h_out, int32_t capacity, int32_t* h_count);
+
+/* Per-block compression ratios r_i = |zlib(x[i*b:(i+1)*b], level)| / b of a host byte
+ * array h_bytes [batch][n_tokens] ("Parameter-free Adaptive Sparse Attention ...",
+ * section 3.1 Eq. 1; zlib framing instead of gzip shifts every length by the same
+ * constant). Writes h_ratio fp32 [batch][n_tokens / block]. Runs on up to n_threads
+ * host threads (0 = hardware concurrency). Uses the system zlib (libz.so.1) loaded at
+ * run time; returns SA_ERR_UNSUPPORTED if it cannot be loaded. Host only. */
+int sa_block_ratios(const uint8_t* h_bytes, int32_t batch, int32_t n_tokens, int32_t block, int32_t level,
+                    float* h_ratio, int32_t n_threads);
+
+/* Synchronises `stream`, then reads and clears the library's device error word.
+ * Returns SA_OK, SA_ERR_TIMEOUT (a bounded wait expired; the kernel unwound and its
+ * outputs are undefined) or SA_ERR_DEVICE (invalid CSR data was skipped). */
+int sa_device_status(void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* sa_status_string(int status);
+
+/* Library ABI version, currently 1. */
+int sa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SA_API_H */

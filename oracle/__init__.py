@@ -28,7 +28,7 @@ from .philox import philox4x64_10, philox_word
 from .masks import (MaskParams, build_csr, csr_topk_rows, csr_bigbird_rows, csr_full_rows,
                     csr_literal_mean_rows, csr_to_block_mask, block_mask_to_token_mask,
                     literal_flags, topk_row_count)
-from .fib import fib_rungs, alpha_schedule, fib_offsets, offset_key_set
+from .fib import fib_rungs, fib_rungs_upto, alpha_schedule, fib_offsets, offset_key_set
 from .attention import (attention_csr, attention_offsets, dense_masked_attention,
                         attention_rows_csr)
 
@@ -36,6 +36,6 @@ __all__ = [
     "block_ratios", "zlib_version", "philox4x64_10", "philox_word", "MaskParams", "build_csr",
     "csr_topk_rows", "csr_bigbird_rows", "csr_full_rows", "csr_literal_mean_rows",
     "csr_to_block_mask", "block_mask_to_token_mask", "literal_flags", "topk_row_count",
-    "fib_rungs", "alpha_schedule", "fib_offsets", "offset_key_set", "attention_csr",
+    "fib_rungs", "fib_rungs_upto", "alpha_schedule", "fib_offsets", "offset_key_set", "attention_csr",
     "attention_offsets", "dense_masked_attention", "attention_rows_csr",
 ]

@@ -64,11 +64,14 @@ def attention_csr(q, k, v, row_ptr, col_idx, block: int, causal: int, scale: flo
 
 
 def attention_rows_csr(q, k, v, row_ptr, col_idx, block: int, causal: int, samples,
-                       scale: float | None = None):
+                       scale: float | None = None, convert=None):
     """The same definition evaluated only at sampled (batch, token, head) triples.
 
+    ``convert`` (optional) widens gathered rows to float64 (e.g. from bf16 bit
+    patterns), so that large inputs need not be converted as a whole.
     Returns ``o [len(samples), d]`` and ``lse [len(samples)]``.
     """
+    cv = convert if convert is not None else (lambda x: x)
     d = q.shape[3]
     h = q.shape[2]
     hkv = k.shape[2]
@@ -84,15 +87,15 @@ def attention_rows_csr(q, k, v, row_ptr, col_idx, block: int, causal: int, sampl
         if not keys:
             continue
         hk = hh // (h // hkv)
-        sc = (k[s, keys, hk, :] @ q[s, i, hh, :]) * scale
+        sc = (cv(k[s, keys, hk, :]) @ cv(q[s, i, hh, :])) * scale
         p, l = _softmax_rows(sc[None, :])
-        o[t] = p[0] @ v[s, keys, hk, :]
+        o[t] = p[0] @ cv(v[s, keys, hk, :])
         lse[t] = l[0]
     return o, lse
 
 
 def attention_offsets(q, k, v, window: int, offsets, scale: float | None = None,
-                      samples=None):
+                      samples=None, convert=None):
     """Token-granular window-plus-offset attention ([FIB] section 2 "Attended set").
 
     Key set of query i: {i - delta : delta in {0..window} u offsets, i - delta >= 0},
@@ -104,15 +107,16 @@ def attention_offsets(q, k, v, window: int, offsets, scale: float | None = None,
     if scale is None:
         scale = 1.0 / np.sqrt(d)
     deltas = np.array(sorted(set(range(window + 1)) | {int(x) for x in offsets}), dtype=np.int64)
+    cv = convert if convert is not None else (lambda x: x)
     if samples is not None:
         o = np.zeros((len(samples), d))
         lse = np.full(len(samples), -np.inf)
         for t, (s, i, hh) in enumerate(samples):
             keys = i - deltas[deltas <= i]
             hk = hh // (h // hkv)
-            sc = (k[s, keys, hk, :] @ q[s, i, hh, :]) * scale
+            sc = (cv(k[s, keys, hk, :]) @ cv(q[s, i, hh, :])) * scale
             p, l = _softmax_rows(sc[None, :])
-            o[t] = p[0] @ v[s, keys, hk, :]
+            o[t] = p[0] @ cv(v[s, keys, hk, :])
             lse[t] = l[0]
         return o, lse
     o = np.zeros((bt, n, h, d))

@@ -1,0 +1,128 @@
+"""Host-side checks of libsa.so that need no GPU: the library loads, exports every
+symbol include/sa_api.h declares, and its host-only entry points (size bound,
+Fibonacci offsets, zlib ratios, argument validation) agree with the oracle."""
+import ctypes
+import os
+import re
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import content_adaptive_sparse_gb300 as sa
+import oracle
+from oracle import masks as om
+from workloads import byte_stream, bytes_phrase_random, workload
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    sa.build_library()
+    return sa.load_library()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "sa_api.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(sa_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_symbols_exported(lib):
+    names = _declared_functions()
+    assert {"sa_build_mask", "sa_attn_fwd", "sa_offset_attn_fwd", "sa_fib_offsets", "sa_block_ratios",
+            "sa_mask_nnz_bound", "sa_device_status", "sa_status_string", "sa_version"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert lib.sa_version() == 1
+    assert lib.sa_status_string(-3) == b"SA_ERR_CAPACITY"
+
+
+@pytest.mark.parametrize("name", ["tiny_topk", "bytelm_topk_8k", "long_topk_64k"])
+def test_block_ratios_match_oracle(lib, name):
+    cfg = workload(name, batch=1) if name == "long_topk_64k" else workload(name)
+    data = byte_stream(cfg)
+    r_lib = sa.sa_block_ratios(data, cfg["block"], 6)
+    r_ora = oracle.block_ratios(data, cfg["block"], 6)
+    assert r_lib.dtype == np.float32 and np.array_equal(r_lib, r_ora)
+
+
+def test_fib_offsets_match_oracle(lib):
+    for lo, hi in (((1, 2), (2, 1)), ((1, 2), (3, 2))):
+        for alpha in oracle.alpha_schedule(16, lo, hi):
+            for W in (6, 8, 10, 12):
+                for n in (2048, 8192):
+                    want = [d for d in oracle.fib_offsets(alpha, oracle.fib_rungs(15)) if W < d < n]
+                    got = sa.sa_fib_offsets(alpha.numerator, alpha.denominator, 15, W, n)
+                    assert got == want
+                    want_all = [d for d in oracle.fib_offsets(alpha, oracle.fib_rungs_upto(n)) if W < d < n]
+                    assert sa.sa_fib_offsets(alpha.numerator, alpha.denominator, 0, W, n) == want_all
+
+
+def _params(p: om.MaskParams, batch: int):
+    mode = {"topk": 0, "bigbird": 1, "full": 2, "literal_mean": 3}[p.mode]
+    return sa.mask_params(mode, p.block, p.n_tokens, batch, p.causal, p.window_blocks, p.global_blocks, p.topk,
+                          p.random_blocks, p.seed)
+
+
+@pytest.mark.parametrize("p", [
+    om.MaskParams("topk", 64, 8192, 1, 4, 1, 16),
+    om.MaskParams("topk", 128, 65536, 1, 4, 1, 256),
+    om.MaskParams("bigbird", 32, 16384, 0, 8, 1, 0, 1, 45),
+    om.MaskParams("bigbird", 32, 1024, 0, 5, 2, 0, 3, 7),
+    om.MaskParams("full", 128, 16384, 1),
+    om.MaskParams("full", 32, 512, 0),
+])
+def test_nnz_bound_exact_for_data_independent_modes(lib, p):
+    rng = np.random.default_rng(0)
+    ratios = rng.random((2, p.nb)).astype(np.float32)
+    _, ci = om.build_csr(p, ratios if p.mode == "topk" else None, 2)
+    assert sa.sa_mask_nnz_bound(_params(p, 2)) == len(ci)
+
+
+def test_argument_validation_before_any_launch(lib):
+    bad = [
+        sa.mask_params(0, 64, 8192, 1, causal=0, window_blocks=4),        # topk must be causal
+        sa.mask_params(1, 32, 1024, 1, causal=1, window_blocks=8),        # bigbird bidirectional only
+        sa.mask_params(0, 64, 1000, 1, window_blocks=4),                   # N % b != 0
+        sa.mask_params(3, 64, 1024, 1, global_blocks=1),                   # literal_mean has no globals
+        sa.mask_params(0, 1, 8192, 1),                                     # nb > 4096
+    ]
+    expect = [-2, -2, -1, -2, -2]
+    for prm, code in zip(bad, expect):
+        out = ctypes.c_int64(0)
+        assert lib.sa_mask_nnz_bound(ctypes.byref(prm), ctypes.byref(out)) == code
+    ok = sa.mask_params(0, 64, 8192, 1, window_blocks=4, global_blocks=1, topk=16)
+    # capacity short -> SA_ERR_CAPACITY, decided on the host before touching the device
+    dummy = ctypes.c_void_p(16)
+    assert lib.sa_build_mask(ctypes.byref(ok), dummy, dummy, dummy, 10, None) == -3
+    I3 = ctypes.c_int64 * 3
+    s = I3(8192 * 12 * 64, 12 * 64, 64)
+    p16 = ctypes.c_void_p(256)
+    # head_dim 48 unsupported, heads % kv_heads != 0 invalid, misaligned pointer unsupported
+    assert lib.sa_attn_fwd(p16, p16, p16, s, s, s, 1, 8192, 12, 12, 48, 64, 1, p16, p16, 0,
+                           ctypes.c_float(0.125), p16, p16, None) == -2
+    assert lib.sa_attn_fwd(p16, p16, p16, s, s, s, 1, 8192, 12, 5, 64, 64, 1, p16, p16, 0,
+                           ctypes.c_float(0.125), p16, p16, None) == -1
+    assert lib.sa_attn_fwd(ctypes.c_void_p(258), p16, p16, s, s, s, 1, 8192, 12, 12, 64, 64, 1, p16, p16, 0,
+                           ctypes.c_float(0.125), p16, p16, None) == -2
+    offs = (ctypes.c_int32 * 2)(5, 9)        # offset inside the window -> invalid
+    assert lib.sa_offset_attn_fwd(p16, p16, p16, s, s, s, 1, 8192, 8, 8, 64, 8, offs, 2,
+                                  ctypes.c_float(0.125), p16, p16, None) == -1
+
+
+def test_compute_entry_points_refuse_without_gpu(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    ok = sa.mask_params(0, 64, 8192, 1, window_blocks=4, global_blocks=1, topk=16)
+    dummy = ctypes.c_void_p(16)
+    assert lib.sa_build_mask(ctypes.byref(ok), dummy, dummy, dummy, 10**6, None) == -4   # SA_ERR_CUDA
+
+
+def test_ratio_threads_are_deterministic(lib):
+    data = np.stack([bytes_phrase_random(s, 4096) for s in range(3)])
+    a = sa.sa_block_ratios(data, 32, 6, n_threads=1)
+    b = sa.sa_block_ratios(data, 32, 6, n_threads=7)
+    assert np.array_equal(a, b)

@@ -1,0 +1,186 @@
+"""Block-sparse attention forward (tcgen05 kernel) vs the float64 oracle."""
+import numpy as np
+import pytest
+
+import content_adaptive_sparse_gb300 as sa
+import oracle
+from oracle import masks as om
+from workloads import bf16_bits_to_f64, bf16_normal_bits, byte_stream, qkv_bits, workload
+from gpu_helpers import assert_attention_close, bf16_to_f64, to_dev, torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+def _mask_on_gpu(p: om.MaskParams, batch: int, ratios=None):
+    torch = torch_cuda()
+    mode = {"topk": 0, "bigbird": 1, "full": 2, "literal_mean": 3}[p.mode]
+    prm = sa.mask_params(mode, p.block, p.n_tokens, batch, p.causal, p.window_blocks, p.global_blocks, p.topk,
+                         p.random_blocks, p.seed)
+    r = None if ratios is None else torch.from_numpy(np.ascontiguousarray(ratios)).cuda()
+    return sa.build_mask(prm, r)
+
+
+def _run_case(p: om.MaskParams, bt, h, hkv, d, seed=0, qmul=1.0, ratios=None, csr_shared=False, std=0.125):
+    """Full comparison at a size the oracle finishes in seconds."""
+    torch = torch_cuda()
+    rng = np.random.default_rng(seed)
+    n = p.n_tokens
+    qb = bf16_normal_bits(rng, (bt, n, h, d), std * qmul)
+    kb = bf16_normal_bits(rng, (bt, n, hkv, d), std)
+    vb = bf16_normal_bits(rng, (bt, n, hkv, d), std)
+    rp_d, ci_d = _mask_on_gpu(p, 1 if csr_shared else bt, ratios)
+    o, lse = sa.attn_fwd(to_dev(qb), to_dev(kb), to_dev(vb), rp_d, ci_d, p.block, p.causal, csr_shared=csr_shared)
+    torch.cuda.synchronize()
+    assert sa.sa_device_status() == 0
+    rp_o, ci_o = om.build_csr(p, ratios, 1 if csr_shared else bt)
+    o_ref, lse_ref = oracle.attention_csr(bf16_bits_to_f64(qb), bf16_bits_to_f64(kb), bf16_bits_to_f64(vb), rp_o,
+                                          ci_o, p.block, p.causal)
+    return assert_attention_close(bf16_to_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref,
+                                  f"{p} d={d}")
+
+
+def test_tiny_topk_workload():
+    cfg = workload("tiny_topk")
+    data = byte_stream(cfg)
+    ratios = oracle.block_ratios(data, cfg["block"])
+    p = om.MaskParams("topk", cfg["block"], cfg["n_tokens"], 1, cfg["window_blocks"], cfg["global_blocks"],
+                      cfg["topk"])
+    for qmul in (1.0, 8.0):   # 8x: softmax far from uniform (stress of the running max)
+        _run_case(p, 1, cfg["heads"], cfg["kv_heads"], cfg["head_dim"], seed=43, qmul=qmul, ratios=ratios,
+                  std=cfg["std"])
+
+
+@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("b", [32, 64, 128])
+def test_full_causal_all_shapes(d, b):
+    _run_case(om.MaskParams("full", b, 512, 1), 2, 2, 2, d, seed=d + b, qmul=4.0)
+
+
+@pytest.mark.parametrize("d,b", [(64, 32), (128, 128), (32, 64)])
+def test_full_bidirectional(d, b):
+    _run_case(om.MaskParams("full", b, 384, 0), 1, 3, 1, d, seed=7)
+
+
+@pytest.mark.parametrize("b,d", [(64, 64), (128, 128), (32, 32), (32, 64)])
+def test_topk_several_tiles_gqa(b, d):
+    n = 2048
+    rng = np.random.default_rng(b * d)
+    ratios = (rng.integers(20, 80, (2, n // b)) / np.float32(b)).astype(np.float32)
+    p = om.MaskParams("topk", b, n, 1, 3, 1, 5)
+    _run_case(p, 2, 4, 2, d, seed=3, qmul=3.0, ratios=ratios)
+
+
+def test_bigbird_small_shared_csr():
+    p = om.MaskParams("bigbird", 32, 1024, 0, 8, 1, 0, 1, 45)
+    _run_case(p, 2, 2, 2, 64, seed=11, qmul=2.0, csr_shared=True)
+
+
+def test_literal_mean_mode():
+    n, b = 2048, 64
+    rng = np.random.default_rng(5)
+    ratios = (rng.integers(20, 90, (2, n // b)) / np.float32(b)).astype(np.float32)
+    for causal in (1, 0):
+        _run_case(om.MaskParams("literal_mean", b, n, causal, 1), 2, 2, 2, 64, seed=causal, ratios=ratios)
+
+
+def test_ragged_tail_tile():
+    # 13 blocks of 32: the last 128-row tile holds one query block
+    p = om.MaskParams("full", 32, 416, 1)
+    _run_case(p, 1, 2, 2, 64, seed=5, qmul=2.0)
+    p = om.MaskParams("bigbird", 32, 416, 0, 4, 1, 0, 2, 3)
+    _run_case(p, 2, 2, 1, 64, seed=6)
+
+
+def test_empty_rows_and_strided_inputs():
+    torch = torch_cuda()
+    rng = np.random.default_rng(9)
+    bt, n, h, d, b = 2, 256, 2, 64, 32
+    packed = bf16_normal_bits(rng, (bt, n, 3, h, d), 0.5)   # q, k, v interleaved: strided views
+    t = to_dev(packed)
+    q, k, v = t[:, :, 0], t[:, :, 1], t[:, :, 2]
+    nb = n // b
+    rows = [[0], [], [0, 1], [2], [], [1, 3, 5], [6], [0, 7]]
+    rp = np.zeros((bt, nb + 1), dtype=np.int32)
+    cols = []
+    for s in range(bt):
+        rp[s, 0] = len(cols)
+        for I, row in enumerate(rows):
+            cols += row
+            rp[s, I + 1] = len(cols)
+    ci = np.array(cols, dtype=np.int32)
+    o, lse = sa.attn_fwd(q, k, v, torch.from_numpy(rp).cuda(), torch.from_numpy(ci).cuda(), b, 1)
+    torch.cuda.synchronize()
+    assert sa.sa_device_status() == 0
+    f = bf16_bits_to_f64(packed)
+    o_ref, lse_ref = oracle.attention_csr(f[:, :, 0], f[:, :, 1], f[:, :, 2], rp, ci, b, 1)
+    assert_attention_close(bf16_to_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref, "empty rows")
+    assert np.all(bf16_to_f64(o)[:, 32:64] == 0)
+
+
+def test_bad_csr_index_is_reported():
+    torch = torch_cuda()
+    bt, n, h, d, b = 1, 256, 1, 64, 64
+    x = torch.zeros((bt, n, h, d), dtype=torch.bfloat16, device="cuda")
+    rp = torch.tensor([[0, 1, 3, 4, 5]], dtype=torch.int32, device="cuda")
+    ci = torch.tensor([0, 0, 9, 2, 3], dtype=torch.int32, device="cuda")   # 9 is out of range
+    o, lse = sa.attn_fwd(x, x, x, rp, ci, b, 1)
+    assert sa.sa_device_status() == -6
+    assert sa.sa_device_status() == 0          # the status word was cleared
+
+
+# ---------------------------------------------------------------- full-size workloads, sampled outputs
+
+def _samples(rng, bt, n, h, k=48, extra=()):
+    out = [(int(rng.integers(bt)), int(rng.integers(n)), int(rng.integers(h))) for _ in range(k)]
+    return out + list(extra)
+
+
+def _full_size(cfg, p, csr_batch, ratios_gpu, ratios_oracle, samples_extra=()):
+    torch = torch_cuda()
+    qb, kb, vb = qkv_bits(cfg)
+    rp_d, ci_d = _mask_on_gpu(p, csr_batch, ratios_gpu)
+    o, lse = sa.attn_fwd(to_dev(qb), to_dev(kb), to_dev(vb), rp_d, ci_d, p.block, p.causal,
+                         csr_shared=(csr_batch == 1 and cfg["batch"] > 1))
+    torch.cuda.synchronize()
+    assert sa.sa_device_status() == 0
+    o_np = bf16_to_f64(o)
+    lse_np = lse.cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(o_np)) and np.all(np.isfinite(lse_np))   # no row is empty in these graphs
+    rp_o, ci_o = om.build_csr(p, ratios_oracle, csr_batch)
+    rng = np.random.default_rng(1)
+    bt, n, h = cfg["batch"], cfg["n_tokens"], cfg["heads"]
+    smp = _samples(rng, bt, n, h, extra=samples_extra)
+    o_ref, lse_ref = oracle.attention_rows_csr(qb, kb, vb, rp_o, ci_o, p.block, p.causal, smp,
+                                               convert=bf16_bits_to_f64)
+    o_g = np.stack([o_np[s, i, hh] for s, i, hh in smp])
+    l_g = np.array([lse_np[s, hh, i] for s, i, hh in smp])
+    assert_attention_close(o_g, l_g, o_ref, lse_ref, cfg["name"])
+
+
+def test_bytelm_topk_8k_sampled():
+    cfg = workload("bytelm_topk_8k")
+    data = byte_stream(cfg)
+    p = om.MaskParams("topk", cfg["block"], cfg["n_tokens"], 1, cfg["window_blocks"], cfg["global_blocks"],
+                      cfg["topk"])
+    n = cfg["n_tokens"]
+    _full_size(cfg, p, cfg["batch"], sa.sa_block_ratios(data, cfg["block"]), oracle.block_ratios(data, cfg["block"]),
+               [(0, 0, 0), (3, n - 1, 11), (1, 127, 5), (2, 128, 6), (0, 4095, 3)])
+
+
+def test_bigbird_16k_sampled():
+    cfg = workload("bigbird_16k")
+    b = cfg["block"]
+    p = om.MaskParams("bigbird", b, cfg["n_tokens"], 0, cfg["window_tokens"] // b, cfg["global_tokens"] // b, 0,
+                      cfg["random_tokens"] // b, cfg["seed"])
+    n = cfg["n_tokens"]
+    _full_size(cfg, p, 1, None, None, [(0, 0, 0), (7, 31, 11), (3, 32, 2), (5, n - 1, 4), (1, 100, 7)])
+
+
+@pytest.mark.parametrize("topk", [64])
+def test_long_topk_64k_sampled(topk):
+    cfg = workload("long_topk_64k", topk=topk)
+    data = byte_stream(cfg)
+    p = om.MaskParams("topk", cfg["block"], cfg["n_tokens"], 1, cfg["window_blocks"], cfg["global_blocks"], topk)
+    n = cfg["n_tokens"]
+    _full_size(cfg, p, 1, sa.sa_block_ratios(data, cfg["block"]), oracle.block_ratios(data, cfg["block"]),
+               [(0, n - 1, 15), (0, 0, 0), (0, 40000, 8)])

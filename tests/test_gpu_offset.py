@@ -1,0 +1,72 @@
+"""Window-plus-Fibonacci-offset attention kernel vs the float64 oracle."""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import content_adaptive_sparse_gb300 as sa
+import oracle
+from workloads import bf16_bits_to_f64, bf16_normal_bits, qkv_bits, workload
+from gpu_helpers import assert_attention_close, bf16_to_f64, to_dev, torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(bt, n, h, hkv, window, alpha: Fraction, n_rungs=15, seed=0, qmul=1.0):
+    torch = torch_cuda()
+    rng = np.random.default_rng(seed)
+    qb = bf16_normal_bits(rng, (bt, n, h, 64), 0.125 * qmul)
+    kb = bf16_normal_bits(rng, (bt, n, hkv, 64), 0.125)
+    vb = bf16_normal_bits(rng, (bt, n, hkv, 64), 0.125)
+    offs = sa.sa_fib_offsets(alpha.numerator, alpha.denominator, n_rungs, window, n)
+    rungs = oracle.fib_rungs(n_rungs) if n_rungs else oracle.fib_rungs_upto(n)
+    assert offs == [d for d in oracle.fib_offsets(alpha, rungs) if window < d < n]
+    o, lse = sa.offset_attn_fwd(to_dev(qb), to_dev(kb), to_dev(vb), window, offs)
+    torch.cuda.synchronize()
+    assert sa.sa_device_status() == 0
+    o_ref, lse_ref = oracle.attention_offsets(bf16_bits_to_f64(qb), bf16_bits_to_f64(kb), bf16_bits_to_f64(vb),
+                                              window, oracle.fib_offsets(alpha, rungs))
+    return assert_attention_close(bf16_to_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref,
+                                  f"W={window} alpha={alpha}")
+
+
+@pytest.mark.parametrize("window", [6, 8, 10, 12])
+def test_windows_mid_alpha(window):
+    _run(2, 1024, 2, 2, window, Fraction(7, 10), seed=window, qmul=4.0)
+
+
+@pytest.mark.parametrize("alpha", [Fraction(1, 2), Fraction(1, 1), Fraction(3, 2), Fraction(2, 1)])
+def test_alpha_range_gqa(alpha):
+    _run(1, 2048, 4, 2, 8, alpha, seed=3)
+
+
+def test_all_rungs_up_to_n_and_ragged_tail():
+    _run(1, 1000, 2, 1, 8, Fraction(13, 10), n_rungs=0, seed=4, qmul=2.0)
+
+
+def test_small_edge_cases():
+    _run(1, 130, 1, 1, 0, Fraction(1, 1), seed=5)          # window 0: self plus offsets
+    _run(1, 64, 1, 1, 64, Fraction(1, 2), seed=6)          # window covers everything: dense causal
+
+
+def test_fib_8k_one_layer_sampled():
+    torch = torch_cuda()
+    cfg = workload("fib_8k")
+    qb, kb, vb = qkv_bits(cfg)
+    alpha = oracle.alpha_schedule(16, cfg["alpha_lo"], cfg["alpha_hi"])[11]
+    W, n = cfg["window"], cfg["n_tokens"]
+    offs = sa.sa_fib_offsets(alpha.numerator, alpha.denominator, cfg["n_rungs"], W, n)
+    o, lse = sa.offset_attn_fwd(to_dev(qb), to_dev(kb), to_dev(vb), W, offs)
+    torch.cuda.synchronize()
+    assert sa.sa_device_status() == 0
+    rng = np.random.default_rng(2)
+    smp = [(int(rng.integers(8)), int(rng.integers(n)), int(rng.integers(8))) for _ in range(64)]
+    smp += [(0, 0, 0), (7, n - 1, 7), (3, 127, 1), (4, 128, 2)]
+    o_ref, lse_ref = oracle.attention_offsets(qb, kb, vb, W, oracle.fib_offsets(alpha, oracle.fib_rungs(15)),
+                                              samples=smp, convert=bf16_bits_to_f64)
+    o_np = bf16_to_f64(o)
+    lse_np = lse.cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(o_np)) and np.all(np.isfinite(lse_np))
+    o_g = np.stack([o_np[s, i, h] for s, i, h in smp])
+    l_g = np.array([lse_np[s, h, i] for s, i, h in smp])
+    assert_attention_close(o_g, l_g, o_ref, lse_ref, "fib_8k")
