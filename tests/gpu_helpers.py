@@ -36,7 +36,8 @@ def assert_attention_close(o_gpu: np.ndarray, lse_gpu: np.ndarray, o_ref: np.nda
     err = np.abs(o_gpu - o_ref)
     both_inf = np.isneginf(lse_gpu) & np.isneginf(lse_ref)
     assert np.array_equal(np.isneginf(lse_gpu), np.isneginf(lse_ref)), f"{what}: empty-row pattern differs"
-    lerr = np.where(both_inf, 0.0, np.abs(lse_gpu - lse_ref))
+    with np.errstate(invalid="ignore"):
+        lerr = np.where(both_inf, 0.0, np.abs(lse_gpu - lse_ref))
     msg = f"{what}: O max {err.max():.3e} mean {err.mean():.3e}, LSE max {lerr.max():.3e}"
     assert err.max() <= O_MAX_ABS, msg
     assert err.mean() <= O_MEAN_ABS, msg
