@@ -29,7 +29,7 @@ from .masks import (MaskParams, build_csr, csr_topk_rows, csr_bigbird_rows, csr_
                     csr_literal_mean_rows, csr_to_block_mask, block_mask_to_token_mask,
                     literal_flags, topk_row_count)
 from .fib import fib_rungs, fib_rungs_upto, alpha_schedule, fib_offsets, offset_key_set
-from .attention import (attention_csr, attention_offsets, dense_masked_attention,
+from .attention import (attention_csr, attention_csr_block, attention_offsets, dense_masked_attention,
                         attention_rows_csr)
 
 __all__ = [
@@ -37,5 +37,6 @@ __all__ = [
     "csr_topk_rows", "csr_bigbird_rows", "csr_full_rows", "csr_literal_mean_rows",
     "csr_to_block_mask", "block_mask_to_token_mask", "literal_flags", "topk_row_count",
     "fib_rungs", "fib_rungs_upto", "alpha_schedule", "fib_offsets", "offset_key_set", "attention_csr",
+    "attention_csr_block",
     "attention_offsets", "dense_masked_attention", "attention_rows_csr",
 ]

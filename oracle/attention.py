@@ -33,33 +33,43 @@ def _csr_batch(row_ptr, s):
     return s if row_ptr.shape[0] > 1 else 0
 
 
+def attention_csr_block(q, k, v, row_ptr, col_idx, block: int, causal: int, s: int, I: int, hh: int,
+                        scale: float | None = None, convert=None):
+    """One query block I of sequence s and head hh: returns O [block, d] and LSE [block].
+
+    ``convert`` (optional) widens gathered rows to float64 (e.g. from bf16 bit patterns).
+    """
+    cv = convert if convert is not None else (lambda x: x)
+    d = q.shape[3]
+    h, hkv = q.shape[2], k.shape[2]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    cs = _csr_batch(row_ptr, s)
+    row = col_idx[row_ptr[cs, I]:row_ptr[cs, I + 1]]
+    if len(row) == 0:
+        return np.zeros((block, d)), np.full(block, -np.inf)
+    keys = np.concatenate([np.arange(J * block, (J + 1) * block) for J in row])
+    qi = np.arange(I * block, (I + 1) * block)
+    allowed = keys[None, :] <= qi[:, None] if causal else np.ones((block, len(keys)), dtype=bool)
+    hk = hh // (h // hkv)
+    sc = (cv(q[s, qi, hh, :]) @ cv(k[s, keys, hk, :]).T) * scale
+    sc = np.where(allowed, sc, -np.inf)
+    p, l = _softmax_rows(sc)
+    return p @ cv(v[s, keys, hk, :]), l
+
+
 def attention_csr(q, k, v, row_ptr, col_idx, block: int, causal: int, scale: float | None = None):
     """Block-CSR attention for every query; see module docstring."""
     bt, n, h, d = q.shape
-    hkv = k.shape[2]
-    if scale is None:
-        scale = 1.0 / np.sqrt(d)
     nb = n // block
     o = np.zeros((bt, n, h, d), dtype=np.float64)
     lse = np.full((bt, h, n), -np.inf, dtype=np.float64)
     for s in range(bt):
-        cs = _csr_batch(row_ptr, s)
         for I in range(nb):
-            row = col_idx[row_ptr[cs, I]:row_ptr[cs, I + 1]]
-            if len(row) == 0:
-                continue
-            keys = np.concatenate([np.arange(J * block, (J + 1) * block) for J in row])
-            qi = np.arange(I * block, (I + 1) * block)
-            allowed = np.ones((block, len(keys)), dtype=bool)
-            if causal:
-                allowed = keys[None, :] <= qi[:, None]
             for hh in range(h):
-                hk = hh // (h // hkv)
-                sc = (q[s, qi, hh, :] @ k[s, keys, hk, :].T) * scale
-                sc = np.where(allowed, sc, -np.inf)
-                p, l = _softmax_rows(sc)
-                o[s, qi, hh, :] = p @ v[s, keys, hk, :]
-                lse[s, hh, qi] = l
+                ob, lb = attention_csr_block(q, k, v, row_ptr, col_idx, block, causal, s, I, hh, scale)
+                o[s, I * block:(I + 1) * block, hh, :] = ob
+                lse[s, hh, I * block:(I + 1) * block] = lb
     return o, lse
 
 
