@@ -201,11 +201,35 @@ __device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t* r) {
       : "r"(taddr));
 }
 
+// Same load, ordered after the computation of `dep` (an otherwise unused operand): code
+// that consumed earlier chunks into `dep` cannot be scheduled after this load, which
+// bounds how many loaded values stay live.
+__device__ __forceinline__ void tmem_ld_x32_after(uint32_t taddr, uint32_t* r, float dep0, float dep1) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr), "f"(dep0), "f"(dep1));
+}
+
 // Wait for outstanding tcgen05.ld of this thread; the register operands tie the
 // loaded values to the wait so no use is scheduled before it.
 template <int N>
 __device__ __forceinline__ void tmem_ld_wait(uint32_t* r) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
+
+// Wait for outstanding tcgen05.ld, ordered after the computation of `dep`: work that
+// feeds `dep` is issued before the wait and overlaps the loads in flight.
+template <int N>
+__device__ __forceinline__ void tmem_ld_wait_after(uint32_t* r, float dep) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::"f"(dep) : "memory");
 #pragma unroll
   for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
 }

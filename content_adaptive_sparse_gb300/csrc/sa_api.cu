@@ -178,6 +178,7 @@ int sa_attn_fwd(const void* q, const void* k, const void* v, const int64_t q_str
   if (head_dim != 32 && head_dim != 64 && head_dim != 128) return SA_ERR_UNSUPPORTED;
   if (block != 32 && block != 64 && block != 128) return SA_ERR_UNSUPPORTED;
   if (n_tokens % block != 0) return SA_ERR_UNSUPPORTED;
+  if (n_tokens / block > sa::kMaxMaskBlocks) return SA_ERR_UNSUPPORTED;
   if ((int64_t)batch * heads > 65535 * 32 || (n_tokens + 127) / 128 > 65535) return SA_ERR_UNSUPPORTED;
   if (!device_ok()) return SA_ERR_CUDA;
   sa::AttnArgs a;

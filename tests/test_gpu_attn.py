@@ -117,6 +117,39 @@ def test_empty_rows_and_strided_inputs():
     assert np.all(bf16_to_f64(o)[:, 32:64] == 0)
 
 
+@pytest.mark.parametrize("d,b", [(64, 64), (128, 128), (64, 32)])
+def test_running_max_rescale_paths(d, b):
+    """Logits that grow along the sequence (and jump inside a key tile) force the
+    lazy running-max updates: in-tile P rescale, O rescale, and first-tile init."""
+    torch = torch_cuda()
+    rng = np.random.default_rng(d + b)
+    n, h = 768, 2
+    base = np.arange(n, dtype=np.float32)[None, :, None, None] / 6.0
+    sign = np.where(rng.random((1, n, h, 1)) < 0.5, -1.0, 1.0).astype(np.float32)
+    qf = np.ones((1, n, h, d), np.float32) * 0.5 + 0.05 * rng.standard_normal((1, n, h, d), dtype=np.float32)
+    kf = (base * (1.0 + 0.3 * sign)) * np.ones((1, n, h, d), np.float32) / np.float32(np.sqrt(d))
+    vf = rng.standard_normal((1, n, h, d), dtype=np.float32)
+    from workloads import _f32_to_bf16_bits
+    qb, kb, vb = (_f32_to_bf16_bits(a) for a in (qf, kf, vf))
+    for mode in ("full", "topk"):
+        if mode == "full":
+            p = om.MaskParams("full", b, n, 1)
+            ratios = None
+        else:
+            p = om.MaskParams("topk", b, n, 1, 2, 1, 3)
+            ratios = (rng.integers(20, 60, (1, n // b)) / np.float32(b)).astype(np.float32)
+        rp_d, ci_d = _mask_on_gpu(p, 1, ratios)
+        o, lse = sa.attn_fwd(to_dev(qb), to_dev(kb), to_dev(vb), rp_d, ci_d, b, 1)
+        torch.cuda.synchronize()
+        assert sa.sa_device_status() == 0
+        rp_o, ci_o = om.build_csr(p, ratios, 1)
+        o_ref, lse_ref = oracle.attention_csr(bf16_bits_to_f64(qb), bf16_bits_to_f64(kb), bf16_bits_to_f64(vb),
+                                              rp_o, ci_o, b, 1)
+        assert np.max(lse_ref) > 60.0          # the logit range really spans many 2^8 steps
+        assert_attention_close(bf16_to_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref,
+                               f"rescale {mode} d={d} b={b}")
+
+
 def test_bad_csr_index_is_reported():
     torch = torch_cuda()
     bt, n, h, d, b = 1, 256, 1, 64, 64
