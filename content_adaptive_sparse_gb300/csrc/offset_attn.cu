@@ -2,14 +2,26 @@
 //
 // "Depth-Staggered Fibonacci Spacing for Sparse Attention", section 2 "Attended set":
 // query i attends to keys i - delta, delta in {0..W} u D (D = distinct scaled Fibonacci
-// offsets > W). Offsets are shared by all queries, so for a tile of 128 consecutive
-// queries every delta needs one contiguous slab of 128 key/value rows (the window
-// needs one slab of 128 + W rows). The kernel streams those slabs into shared memory
-// with TMA (128-byte swizzle, so the per-thread row reads are bank-conflict free) and
-// each thread owns one query: fp32 dot products with packed f32x2 FMAs, an online
-// softmax with a lazily rescaled running max, and an fp32 output accumulator.
+// offsets > W). Offsets are shared by all queries, so the key set of 16 consecutive
+// queries is a band plus a few diagonals:
+//   * band: every delta <= 64 (the window and the small offsets). For queries
+//     [i0, i0+16) the keys [i0 - Dr, i0 + 16) (Dr = the largest such delta rounded up to
+//     16) form a dense 16 x (16 + Dr) score block; a per-lane bit mask (built on the host)
+//     keeps the distances that belong to the set. Computed with mma.sync m16n8k16
+//     (bf16 -> f32); the row sums come from one more MMA against a ones matrix.
+//   * each larger offset delta: keys [i0 - delta, i0 + 16 - delta], of which query i0+r
+//     uses only key r: the diagonal of a 16 x 16 block. Computed with 8 mma.sync for QK
+//     and 8 for PV; the zero off-diagonal P entries cost tensor work, not memory traffic.
 //
-// Work item: one CTA of 128 threads per (sequence, head, 128-query tile).
+// Work item: one CTA of 8 warps per (sequence, head, 64-query tile). Warps 4g..4g+3 form
+// group g; warp w of a group owns queries q0 + 16w .. q0 + 16w + 15. The two groups split
+// the keys (group 0 the first half of the band steps and the even offset slabs, group 1
+// the rest) and merge their partial softmax states through shared memory at the end.
+// K/V arrive by TMA: the band (rows [q0 - 64, q0 + 64)) once, the offset slabs (64 rows
+// each) through a ring of four buffers that the last warp done with a buffer refills,
+// so loads are issued from many warps (one issuing thread streams boxes slowly).
+// Softmax: exact max over the band part, then the offsets with a lazily rescaled
+// running max (threshold 2^8).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -24,227 +36,412 @@ namespace {
 
 __device__ unsigned int g_offset_err;
 
-constexpr int kQ = 128;              // queries per CTA
-constexpr int kD = 64;               // head dim supported by this kernel
-constexpr int kRowBytes = kD * 2;    // 128 B per K/V row
+constexpr int kQ = 64;                   // queries per CTA
+constexpr int kGroupWarps = 4;           // 16 queries per warp: one group covers the tile
+constexpr int kWarps = 2 * kGroupWarps;  // two groups split the keys of the tile
+constexpr int kRing = 4;                 // offset slabs in flight per CTA (two per group)
+constexpr int kD = 64;                   // head dim supported by this kernel
+constexpr int kRowBytes = kD * 2;        // 128 B per K/V row
+constexpr int kBandMax = 64;             // deltas up to this go through the band
+constexpr int kBandRows = kQ + kBandMax; // band slab rows [q0 - 64, q0 + 64)
 constexpr int kSlabBytes = kQ * kRowBytes;
+constexpr int kBandBytes = kBandRows * kRowBytes;
+constexpr int kMaxLarge = kMaxOffsets;
+constexpr uint32_t kOnesBf16x2 = 0x3f803f80u;   // (1.0, 1.0) in bf16
 
 struct OffParams {
-  int n_tokens, heads, heads_per_kv, window, n_offsets, ntiles;
+  int n_tokens, heads, heads_per_kv, ntiles;
+  int dr;                       // band reach Dr (multiple of 16, <= 64)
+  int n_large;                  // offsets > 64, ascending
+  int large[kMaxLarge];
+  // per lane: bit 4*nt + e set if score fragment element e of band n-tile nt is at a
+  // distance in the key set (the same for every warp and tile)
+  unsigned long long keep[32];
   const __nv_bfloat16* q;
   __nv_bfloat16* o;
   float* lse;
   int64_t q_sb, q_sn, q_sh, o_sb, o_sn, o_sh;
   float scale_log2;
-  int offsets[kMaxOffsets];
 };
 
-// Byte offset of 16-byte chunk c of row r in a 128B-swizzled tile of 128-byte rows.
-__device__ __forceinline__ uint32_t swz_off(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
-
-__device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float* f) {
-  f[0] = __uint_as_float(u.x << 16);
-  f[1] = __uint_as_float(u.x & 0xffff0000u);
-  f[2] = __uint_as_float(u.y << 16);
-  f[3] = __uint_as_float(u.y & 0xffff0000u);
-  f[4] = __uint_as_float(u.z << 16);
-  f[5] = __uint_as_float(u.z & 0xffff0000u);
-  f[6] = __uint_as_float(u.w << 16);
-  f[7] = __uint_as_float(u.w & 0xffff0000u);
+// 128B swizzle of a tile of 128-byte rows: 16-byte chunk c of row r.
+__device__ __forceinline__ uint32_t swz(uint32_t base, int r, int c) {
+  return base + (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
-__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ void f2_unpack(uint64_t v, float& a, float& b) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
 }
 
-struct Acc {
-  uint64_t o[kD / 2];   // packed f32 pairs of the output accumulator
-  float m, l;
-};
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
 
-// One key: score, lazy max update, accumulate p * v. `krow`/`vrow` point at the
-// swizzled shared-memory row.
-__device__ __forceinline__ void visit_key(const uint64_t* q2, const uint8_t* kt, const uint8_t* vt, int r, Acc& a) {
-  uint64_t s2a = 0, s2b = 0;
+// D += A (16x16 bf16, row) * B (16x8 bf16, col), f32 accumulate.
+__device__ __forceinline__ void mma16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// The QK contraction runs over the head dimension in a permuted order: in k-step ks,
+// fragment slot j (0: k = 2t, 2t+1; 1: k = 2t+8, 2t+9) of lane (g, t) holds the physical
+// dimensions 16t + 4ks + 2j + {0, 1}. A dot product does not depend on the order of its
+// terms, and with this order every lane's Q and K operands are the 32 contiguous bytes
+// [16t, 16t + 16) of a row: plain 16-byte loads instead of ldmatrix.
+// K operand of one 8-key n-tile: the lane's 32 bytes of key row `row` of a swizzled tile.
+__device__ __forceinline__ void load_kfrag(uint32_t tile, int row, int t, uint32_t (&u)[8]) {
+  const uint4 a = lds128(swz(tile, row, 2 * t)), b = lds128(swz(tile, row, 2 * t + 1));
+  u[0] = a.x; u[1] = a.y; u[2] = a.z; u[3] = a.w;
+  u[4] = b.x; u[5] = b.y; u[6] = b.z; u[7] = b.w;
+}
+
+// 16 x 8 scores of one n-tile: d = Q (16 x 64) . K^T (64 x 8).
+__device__ __forceinline__ void qk_ntile(float* d, const uint32_t (&qa)[4][4], const uint32_t (&u)[8]) {
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const uint4 u = *reinterpret_cast<const uint4*>(kt + swz_off(r, c));
-    float f[8];
-    bf16x8_to_f32(u, f);
-    s2a = f2_fma(q2[4 * c + 0], f2_pack(f[0], f[1]), s2a);
-    s2b = f2_fma(q2[4 * c + 1], f2_pack(f[2], f[3]), s2b);
-    s2a = f2_fma(q2[4 * c + 2], f2_pack(f[4], f[5]), s2a);
-    s2b = f2_fma(q2[4 * c + 3], f2_pack(f[6], f[7]), s2b);
-  }
-  float x0, x1, y0, y1;
-  f2_unpack(s2a, x0, x1);
-  f2_unpack(s2b, y0, y1);
-  const float s = (x0 + x1) + (y0 + y1);          // already in log2 units (q pre-scaled)
-  if (s > a.m + 8.0f) {                            // rare: rescale the accumulator
-    const float alpha = ex2_approx(a.m - s);       // 0 on the first key
-    const uint64_t al2 = f2_pack(alpha, alpha);
+  for (int ks = 0; ks < 4; ++ks) mma16816(d, qa[ks], u[2 * ks], u[2 * ks + 1]);
+}
+
+// B fragments (transposed) of 16 key rows x 64 dims of V: vb[nt2][*] covers d n-tiles
+// 2*nt2 and 2*nt2+1 for the 16 keys.
+__device__ __forceinline__ void load_v16(uint32_t tile, int row0, int lane, uint32_t (&vb)[4][4]) {
+  // matrices: (keys 0-7, d chunk c), (keys 8-15, d chunk c), (keys 0-7, chunk c+1), (keys 8-15, chunk c+1)
+  const int r = row0 + (lane & 7) + (((lane >> 3) & 1) << 3);
+  const int cc = lane >> 4;
 #pragma unroll
-    for (int i = 0; i < kD / 2; ++i) a.o[i] = f2_mul(a.o[i], al2);
-    a.l *= alpha;
-    a.m = s;
-  }
-  const float p = ex2_approx(s - a.m);
-  a.l += p;
-  const uint64_t p2 = f2_pack(p, p);
+  for (int nt2 = 0; nt2 < 4; ++nt2) ldsm_x4_t(swz(tile, r, 2 * nt2 + cc), vb[nt2][0], vb[nt2][1], vb[nt2][2], vb[nt2][3]);
+}
+
+__device__ __forceinline__ void pv_16(float (&o)[8][4], const uint32_t* pa, const uint32_t (&vb)[4][4]) {
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const uint4 u = *reinterpret_cast<const uint4*>(vt + swz_off(r, c));
-    float f[8];
-    bf16x8_to_f32(u, f);
-    a.o[4 * c + 0] = f2_fma(p2, f2_pack(f[0], f[1]), a.o[4 * c + 0]);
-    a.o[4 * c + 1] = f2_fma(p2, f2_pack(f[2], f[3]), a.o[4 * c + 1]);
-    a.o[4 * c + 2] = f2_fma(p2, f2_pack(f[4], f[5]), a.o[4 * c + 2]);
-    a.o[4 * c + 3] = f2_fma(p2, f2_pack(f[6], f[7]), a.o[4 * c + 3]);
+  for (int nt2 = 0; nt2 < 4; ++nt2) {
+    mma16816(o[2 * nt2], pa, vb[nt2][0], vb[nt2][1]);
+    mma16816(o[2 * nt2 + 1], pa, vb[nt2][2], vb[nt2][3]);
   }
 }
 
-__global__ void __launch_bounds__(kQ) offset_attn_kernel(const __grid_constant__ CUtensorMap tk_win,
-                                                          const __grid_constant__ CUtensorMap tv_win,
-                                                          const __grid_constant__ CUtensorMap tk_slab,
-                                                          const __grid_constant__ CUtensorMap tv_slab,
-                                                          const OffParams p) {
+// Raw diagonal scores q_{i} . k_{i - delta} of rows g and g+8 from one slab (all lanes of
+// the quad receive them).
+__device__ __forceinline__ void diag_scores(uint32_t kt, int wq, int g, int t, int hl, int e_sel,
+                                            const uint32_t (&qa)[4][4], float& s_lo, float& s_hi) {
+  uint32_t u0[8], u1[8];
+  load_kfrag(kt, 16 * wq + g, t, u0);
+  load_kfrag(kt, 16 * wq + 8 + g, t, u1);
+  float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+  qk_ntile(d0, qa, u0);
+  qk_ntile(d1, qa, u1);
+  // query row g meets key row g at fragment column g: n-tile 0, lane t = g/2, element g%2
+  s_lo = __shfl_sync(0xffffffffu, e_sel ? d0[1] : d0[0], hl);
+  s_hi = __shfl_sync(0xffffffffu, e_sel ? d1[3] : d1[2], hl);
+}
+
+// O += P_diag V_slab for one slab; pb = bf16 bits (p_lo | p_hi << 16) of this quad's rows.
+__device__ __forceinline__ void diag_pv(uint32_t vt, int wq, int lane, bool holder, int e_sel, uint32_t pb,
+                                        float (&o)[8][4]) {
+  uint32_t pa[4];
+  pa[0] = holder ? (e_sel ? (pb << 16) : (pb & 0xffffu)) : 0u;
+  pa[1] = 0u;
+  pa[2] = 0u;
+  pa[3] = holder ? (e_sel ? (pb & 0xffff0000u) : (pb >> 16)) : 0u;
+  uint32_t vb[4][4];
+  load_v16(vt, 16 * wq, lane, vb);
+  pv_16(o, pa, vb);
+}
+
+template <int NKT>
+__global__ void __launch_bounds__(kWarps * 32, 2)
+    offset_attn_kernel(const __grid_constant__ CUtensorMap tk_band, const __grid_constant__ CUtensorMap tv_band,
+                       const __grid_constant__ CUtensorMap tk_slab, const __grid_constant__ CUtensorMap tv_slab,
+                       const __grid_constant__ OffParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int win_rows = kQ + p.window;
-  const int win_bytes = ((win_rows * kRowBytes) + 1023) & ~1023;
-  uint8_t* sKw = sm;
-  uint8_t* sVw = sKw + win_bytes;
-  uint8_t* sSlab = sVw + win_bytes;   // [2 buffers][K slab, V slab]
-  __shared__ uint64_t bar_win, bar_slab[2];
+  uint8_t* sKb = sm;                        // band K, 16 KB
+  uint8_t* sVb = sKb + kBandBytes;          // band V, 16 KB
+  uint8_t* sRing = sVb + kBandBytes;        // kRing x (K slab, V slab), 64 KB; merge buffer at the end
+  __shared__ uint64_t bar_band, bar_slab[kRing];
+  __shared__ int done_cnt[kRing];           // warps finished with the slab in each buffer
+  __shared__ int n_issued;                  // slabs issued so far
   __shared__ int abort_flag;
-  int last_issued[2] = {-1, -1};   // slab index last loaded into each buffer (thread 0)
 
-  const int t = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int grp = warp / kGroupWarps, wq = warp % kGroupWarps;
   const int h = blockIdx.x % p.heads;
   const int s = blockIdx.x / p.heads;
   const int tile = p.ntiles - 1 - (int)blockIdx.y;   // later tiles reach more offsets: start them first
   const int q0 = tile * kQ;
   const int hk = h / p.heads_per_kv;
-  const int i = q0 + t;
-  // offsets that reach at least one query of this tile: delta <= q0 + kQ - 1
+  // larger offsets that reach at least one query of this tile
   int n_off = 0;
-  while (n_off < p.n_offsets && p.offsets[n_off] <= q0 + kQ - 1) ++n_off;
+  while (n_off < p.n_large && p.large[n_off] <= q0 + kQ - 1) ++n_off;
 
-  if (t == 0) {
-    mbar_init(&bar_win, 1);
-    mbar_init(&bar_slab[0], 1);
-    mbar_init(&bar_slab[1], 1);
+  if (tid == 0) {
+    mbar_init(&bar_band, 1);
+#pragma unroll
+    for (int b = 0; b < kRing; ++b) {
+      mbar_init(&bar_slab[b], 1);
+      done_cnt[b] = 0;
+    }
     abort_flag = 0;
+    n_issued = n_off < kRing ? n_off : kRing;
     fence_mbar_init();
-    mbar_arrive_expect_tx(&bar_win, 2u * win_rows * kRowBytes);
-    tma_load_4d(sKw, &tk_win, &bar_win, 0, hk, q0 - p.window, s);
-    tma_load_4d(sVw, &tv_win, &bar_win, 0, hk, q0 - p.window, s);
-    for (int k = 0; k < 2 && k < n_off; ++k) {
-      last_issued[k] = k;
-      mbar_arrive_expect_tx(&bar_slab[k], 2u * kSlabBytes);
-      tma_load_4d(sSlab + k * 2 * kSlabBytes, &tk_slab, &bar_slab[k], 0, hk, q0 - p.offsets[k], s);
-      tma_load_4d(sSlab + k * 2 * kSlabBytes + kSlabBytes, &tv_slab, &bar_slab[k], 0, hk, q0 - p.offsets[k], s);
+    mbar_arrive_expect_tx(&bar_band, (uint32_t)(2 * kBandBytes));
+  }
+  __syncthreads();
+  // A single thread streams TMA boxes at a limited rate, so several warps issue loads:
+  // warp w < kRing the first slab of buffer w, warps 4 and 5 the band.
+  if (lane == 0) {
+    if (warp == 4) tma_load_4d(sKb, &tk_band, &bar_band, 0, hk, q0 - kBandMax, s);
+    if (warp == 5) tma_load_4d(sVb, &tv_band, &bar_band, 0, hk, q0 - kBandMax, s);
+    if (warp < kRing && warp < n_off) {
+      uint8_t* dst = sRing + warp * 2 * kSlabBytes;
+      mbar_arrive_expect_tx(&bar_slab[warp], 2u * kSlabBytes);
+      tma_load_4d(dst, &tk_slab, &bar_slab[warp], 0, hk, q0 - p.large[warp], s);
+      tma_load_4d(dst + kSlabBytes, &tv_slab, &bar_slab[warp], 0, hk, q0 - p.large[warp], s);
     }
   }
 
-  // query row, pre-scaled by softmax_scale * log2(e)
-  uint64_t q2[kD / 2];
+  const int g = lane >> 2, t = lane & 3;     // mma fragment coordinates: rows g, g+8; cols 2t, 2t+1
+  const int qw = q0 + 16 * wq;               // first query of this warp
+  const float c = p.scale_log2;
+  const float kNegInf = __int_as_float(0xff800000);
+
+  // Q operand straight from global memory (rows past the end read the last row; never stored)
+  uint32_t qa[4][4];
   {
-    const int iq = i < p.n_tokens ? i : p.n_tokens - 1;
-    const uint4* qrow = reinterpret_cast<const uint4*>(p.q + (int64_t)s * p.q_sb + (int64_t)iq * p.q_sn +
-                                                       (int64_t)h * p.q_sh);
+    const int last = p.n_tokens - 1;
+    const int i_lo = qw + g < last ? qw + g : last, i_hi = qw + g + 8 < last ? qw + g + 8 : last;
+    const __nv_bfloat16* base = p.q + (int64_t)s * p.q_sb + (int64_t)h * p.q_sh + 16 * t;
+    const uint4* lo = reinterpret_cast<const uint4*>(base + (int64_t)i_lo * p.q_sn);
+    const uint4* hi = reinterpret_cast<const uint4*>(base + (int64_t)i_hi * p.q_sn);
+    const uint4 a = __ldg(lo), b = __ldg(lo + 1), x = __ldg(hi), y = __ldg(hi + 1);
+    const uint32_t wl[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    const uint32_t wh[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      float f[8];
-      bf16x8_to_f32(qrow[c], f);
-#pragma unroll
-      for (int e = 0; e < 8; e += 2) q2[4 * c + e / 2] = f2_pack(f[e] * p.scale_log2, f[e + 1] * p.scale_log2);
+    for (int ks = 0; ks < 4; ++ks) {
+      qa[ks][0] = wl[2 * ks];
+      qa[ks][1] = wh[2 * ks];
+      qa[ks][2] = wl[2 * ks + 1];
+      qa[ks][3] = wh[2 * ks + 1];
     }
   }
-  Acc a;
-#pragma unroll
-  for (int k = 0; k < kD / 2; ++k) a.o[k] = 0ull;
-  a.m = __int_as_float(0xff800000);
-  a.l = 0.f;
-  __syncthreads();
 
-  bool ok = mbar_wait(&bar_win, 0, &abort_flag, &g_offset_err, kErrTimeout);
-  __syncthreads();
-  ok = ok && !abort_flag;   // every thread takes the same path below
+  // warp-uniform wait results: the fragment code below uses full-warp shuffles
+  bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_band, 0, &abort_flag, &g_offset_err, kErrTimeout));
+
+  float o[8][4];                             // O fragments: d n-tiles 0..7
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+  // running max of rows g, g+8 (log2 units); -inf until this group has seen a kept key
+  float m_lo = kNegInf, m_hi = kNegInf;
+  float l_lo = 0.f, l_hi = 0.f;
+
   if (ok) {
-    // window: keys i - delta, delta = 0..W; slab row of key i - delta is t + W - delta
-    for (int d = 0; d <= p.window; ++d)
-      if (i - d >= 0) visit_key(q2, sKw, sVw, t + p.window - d, a);
-  }
-  for (int k = 0; k < n_off && ok; ++k) {
-    const int buf = k & 1;
-    ok = mbar_wait(&bar_slab[buf], (k >> 1) & 1, &abort_flag, &g_offset_err, kErrTimeout);
-    if (ok && i - p.offsets[k] >= 0) {
-      const uint8_t* kt = sSlab + buf * 2 * kSlabBytes;
-      visit_key(q2, kt, kt + kSlabBytes, t, a);
+    // ---------------- band: keys [qw - Dr, qw + 16), band slab row = key - (q0 - 64);
+    // group 0 takes the first (NKT + 1) / 2 16-key steps, group 1 the rest
+    constexpr int kSplit = (NKT + 1) / 2;
+    uint64_t keep = p.keep[lane];
+    const int lim = p.dr - qw;               // band columns below lim are keys < 0 (first tile only)
+    if (lim > 0) {
+#pragma unroll
+      for (int nt = 0; nt < 2 * NKT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (8 * nt + 2 * t + (e & 1) < lim) keep &= ~(1ull << (4 * nt + e));
     }
-    __syncthreads();
-    if (t == 0 && ok && k + 2 < n_off) {
-      last_issued[buf] = k + 2;
-      mbar_arrive_expect_tx(&bar_slab[buf], 2u * kSlabBytes);
-      tma_load_4d(sSlab + buf * 2 * kSlabBytes, &tk_slab, &bar_slab[buf], 0, hk, q0 - p.offsets[k + 2], s);
-      tma_load_4d(sSlab + buf * 2 * kSlabBytes + kSlabBytes, &tv_slab, &bar_slab[buf], 0, hk,
-                  q0 - p.offsets[k + 2], s);
+    const int row0 = 16 * wq + kBandMax - p.dr;
+    const uint32_t kb_tile = smem_u32(sKb), vb_tile = smem_u32(sVb);
+    float sb[2 * NKT][4];
+    float mx_lo = kNegInf, mx_hi = kNegInf;
+#pragma unroll
+    for (int nt = 0; nt < 2 * NKT; ++nt) {
+      if ((nt / 2 < kSplit) == (grp == 0)) {
+        uint32_t u[8];
+        load_kfrag(kb_tile, row0 + 8 * nt + g, t, u);
+        sb[nt][0] = sb[nt][1] = sb[nt][2] = sb[nt][3] = 0.f;
+        qk_ntile(sb[nt], qa, u);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float v = (keep >> (4 * nt + e)) & 1ull ? sb[nt][e] : kNegInf;
+          sb[nt][e] = v;
+          if (e < 2) mx_lo = fmaxf(mx_lo, v);
+          else mx_hi = fmaxf(mx_hi, v);
+        }
+      }
     }
-    ok = !abort_flag && ok;
+    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+    m_lo = mx_lo * c;                        // -inf * c stays -inf
+    m_hi = mx_hi * c;
+    const float e_lo = m_lo == kNegInf ? 0.f : m_lo, e_hi = m_hi == kNegInf ? 0.f : m_hi;
+    // P = exp2(s c - m); row sums of the bf16 P the PV product uses come from one more
+    // MMA against a ones matrix
+    float lsum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < NKT; ++j) {
+      if ((j < kSplit) == (grp == 0)) {
+        uint32_t pa[4];
+        pa[0] = pack_bf16x2(ex2_approx(fmaf(sb[2 * j][0], c, -e_lo)), ex2_approx(fmaf(sb[2 * j][1], c, -e_lo)));
+        pa[1] = pack_bf16x2(ex2_approx(fmaf(sb[2 * j][2], c, -e_hi)), ex2_approx(fmaf(sb[2 * j][3], c, -e_hi)));
+        pa[2] = pack_bf16x2(ex2_approx(fmaf(sb[2 * j + 1][0], c, -e_lo)),
+                            ex2_approx(fmaf(sb[2 * j + 1][1], c, -e_lo)));
+        pa[3] = pack_bf16x2(ex2_approx(fmaf(sb[2 * j + 1][2], c, -e_hi)),
+                            ex2_approx(fmaf(sb[2 * j + 1][3], c, -e_hi)));
+        mma16816(lsum, pa, kOnesBf16x2, kOnesBf16x2);
+        uint32_t vb[4][4];
+        load_v16(vb_tile, row0 + 16 * j, lane, vb);
+        pv_16(o, pa, vb);
+      }
+    }
+    l_lo = lsum[0];
+    l_hi = lsum[2];
   }
-  if (!ok) {
-    // drain this CTA's own copies before exit
-    if (t == 0) {
+
+  // ---------------- larger offsets: group 0 takes slabs 0, 2, 4, ..., group 1 slabs 1, 3, ...
+  // (buffers {0, 2} and {1, 3}); one diagonal 16 x 16 block per slab
+  const int hl = (lane & ~3) | (g >> 1);     // lane of this quad that holds the diagonal
+  const bool holder = (t == (g >> 1));
+  const int e_sel = g & 1;                   // which of the two fragment columns is diagonal
+  for (int k = grp; k < n_off && ok; k += 2) {
+    const int buf = k % kRing;
+    ok = __all_sync(0xffffffffu, mbar_wait(&bar_slab[buf], (uint32_t)(k / kRing) & 1u, &abort_flag,
+                                           &g_offset_err, kErrTimeout));
+    if (!ok) break;
+    const uint32_t kt = smem_u32(sRing + buf * 2 * kSlabBytes);
+    float s_lo, s_hi;
+    diag_scores(kt, wq, g, t, hl, e_sel, qa, s_lo, s_hi);
+    const int delta = p.large[k];
+    if (qw + g - delta < 0) s_lo = kNegInf;
+    if (qw + g + 8 - delta < 0) s_hi = kNegInf;
+    // lazy running max (log2 units): rescale only when a score passes the max by 2^8
+    const float x_lo = s_lo * c, x_hi = s_hi * c;
+    float a_lo = 1.f, a_hi = 1.f;
+    if (x_lo > m_lo + 8.f) { a_lo = ex2_approx(m_lo - x_lo); m_lo = x_lo; }
+    if (x_hi > m_hi + 8.f) { a_hi = ex2_approx(m_hi - x_hi); m_hi = x_hi; }
+    if (__any_sync(0xffffffffu, a_lo != 1.f || a_hi != 1.f)) {
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        o[nt][0] *= a_lo;
+        o[nt][1] *= a_lo;
+        o[nt][2] *= a_hi;
+        o[nt][3] *= a_hi;
+      }
+      l_lo *= a_lo;
+      l_hi *= a_hi;
+    }
+    const float e_lo = m_lo == kNegInf ? 0.f : m_lo, e_hi = m_hi == kNegInf ? 0.f : m_hi;
+    const uint32_t pb = pack_bf16x2(ex2_approx(fmaf(s_lo, c, -e_lo)), ex2_approx(fmaf(s_hi, c, -e_hi)));
+    l_lo += __uint_as_float(pb << 16);
+    l_hi += __uint_as_float(pb & 0xffff0000u);
+    diag_pv(kt + kSlabBytes, wq, lane, holder, e_sel, pb, o);
+    // the last warp of the group done with this buffer refills it with slab k + kRing
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence_block();
+      if (atomicAdd(&done_cnt[buf], 1) == kGroupWarps - 1) {
+        __threadfence_block();
+        done_cnt[buf] = 0;
+        const int nk = k + kRing;
+        if (nk < n_off && !abort_flag) {
+          uint8_t* dst = sRing + buf * 2 * kSlabBytes;
+          mbar_arrive_expect_tx(&bar_slab[buf], 2u * kSlabBytes);
+          tma_load_4d(dst, &tk_slab, &bar_slab[buf], 0, hk, q0 - p.large[nk], s);
+          tma_load_4d(dst + kSlabBytes, &tv_slab, &bar_slab[buf], 0, hk, q0 - p.large[nk], s);
+          atomicMax(&n_issued, nk + 1);
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (abort_flag) {
+    // drain this CTA's own copies before exit: the band and the last slab of each buffer
+    if (tid == 0) {
       int never = 0;
-      mbar_wait(&bar_win, 0, &never, &g_offset_err, kErrTimeout);
-      for (int b = 0; b < 2; ++b)
-        if (last_issued[b] >= 0) mbar_wait(&bar_slab[b], (last_issued[b] >> 1) & 1, &never, &g_offset_err, kErrTimeout);
+      mbar_wait(&bar_band, 0, &never, &g_offset_err, kErrTimeout);
+      const int ni = n_issued;
+      for (int j = ni - kRing < 0 ? 0 : ni - kRing; j < ni; ++j)
+        mbar_wait(&bar_slab[j % kRing], (uint32_t)(j / kRing) & 1u, &never, &g_offset_err, kErrTimeout);
     }
-    __syncthreads();
     return;
   }
-  if (i < p.n_tokens) {
-    const float inv = a.l > 0.f ? 1.f / a.l : 0.f;
-    uint4* orow = reinterpret_cast<uint4*>(p.o + (int64_t)s * p.o_sb + (int64_t)i * p.o_sn + (int64_t)h * p.o_sh);
+
+  // ---------------- merge the two groups' partial softmax states (ring buffers are idle now)
+  float4* sO = reinterpret_cast<float4*>(sRing);                        // [wq][nt][lane]
+  float4* sML = reinterpret_cast<float4*>(sRing + kGroupWarps * 8 * 32 * 16);   // [wq][lane]
+  if (grp == 1) {
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      float f[8];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) f2_unpack(a.o[4 * c + e], f[2 * e], f[2 * e + 1]);
-      orow[c] = make_uint4(pack_bf16x2(f[0] * inv, f[1] * inv), pack_bf16x2(f[2] * inv, f[3] * inv),
-                           pack_bf16x2(f[4] * inv, f[5] * inv), pack_bf16x2(f[6] * inv, f[7] * inv));
-    }
-    p.lse[((int64_t)s * p.heads + h) * p.n_tokens + i] =
-        a.l > 0.f ? (a.m + __log2f(a.l)) * 0.69314718055994531f : __int_as_float(0xff800000);
+    for (int nt = 0; nt < 8; ++nt) sO[(wq * 8 + nt) * 32 + lane] = make_float4(o[nt][0], o[nt][1], o[nt][2], o[nt][3]);
+    sML[wq * 32 + lane] = make_float4(m_lo, m_hi, l_lo, l_hi);
   }
+  __syncthreads();
+  if (grp == 1) return;
+  {
+    const float4 ml = sML[wq * 32 + lane];
+    const float mn_lo = fmaxf(m_lo, ml.x), mn_hi = fmaxf(m_hi, ml.y);   // finite: one group kept distance 0
+    const float fa_lo = ex2_approx(m_lo - mn_lo), fb_lo = ex2_approx(ml.x - mn_lo);
+    const float fa_hi = ex2_approx(m_hi - mn_hi), fb_hi = ex2_approx(ml.y - mn_hi);
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      const float4 ob = sO[(wq * 8 + nt) * 32 + lane];
+      o[nt][0] = o[nt][0] * fa_lo + ob.x * fb_lo;
+      o[nt][1] = o[nt][1] * fa_lo + ob.y * fb_lo;
+      o[nt][2] = o[nt][2] * fa_hi + ob.z * fb_hi;
+      o[nt][3] = o[nt][3] * fa_hi + ob.w * fb_hi;
+    }
+    l_lo = l_lo * fa_lo + ml.z * fb_lo;
+    l_hi = l_hi * fa_hi + ml.w * fb_hi;
+    m_lo = mn_lo;
+    m_hi = mn_hi;
+  }
+
+  // ---------------- epilogue: O / l (bf16) and LSE
+  const float inv_lo = 1.f / l_lo, inv_hi = 1.f / l_hi;   // l > 0: every query keeps itself
+  const int i_lo = qw + g, i_hi = qw + g + 8;
+  __nv_bfloat16* orow_lo = p.o + (int64_t)s * p.o_sb + (int64_t)i_lo * p.o_sn + (int64_t)h * p.o_sh;
+  __nv_bfloat16* orow_hi = p.o + (int64_t)s * p.o_sb + (int64_t)i_hi * p.o_sn + (int64_t)h * p.o_sh;
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt) {
+    const int col = 8 * nt + 2 * t;
+    if (i_lo < p.n_tokens)
+      *reinterpret_cast<uint32_t*>(orow_lo + col) = pack_bf16x2(o[nt][0] * inv_lo, o[nt][1] * inv_lo);
+    if (i_hi < p.n_tokens)
+      *reinterpret_cast<uint32_t*>(orow_hi + col) = pack_bf16x2(o[nt][2] * inv_hi, o[nt][3] * inv_hi);
+  }
+  if (t == 0) {
+    float* lrow = p.lse + ((int64_t)s * p.heads + h) * p.n_tokens;
+    if (i_lo < p.n_tokens) lrow[i_lo] = (m_lo + __log2f(l_lo)) * 0.69314718055994531f;
+    if (i_hi < p.n_tokens) lrow[i_hi] = (m_hi + __log2f(l_hi)) * 0.69314718055994531f;
+  }
+}
+
+template <int NKT>
+int launch_nkt(const CUtensorMap& kb, const CUtensorMap& vb, const CUtensorMap& ks, const CUtensorMap& vs,
+               const OffParams& p, int batch, cudaStream_t stream) {
+  const size_t smem = 1024 + 2 * (size_t)kBandBytes + 2 * kRing * (size_t)kSlabBytes;
+  if (cudaFuncSetAttribute(offset_attn_kernel<NKT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
+    return SA_ERR_CUDA;
+  dim3 grid((unsigned)(batch * p.heads), (unsigned)p.ntiles);
+  offset_attn_kernel<NKT><<<grid, kWarps * 32, smem, stream>>>(kb, vb, ks, vs, p);
+  return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
 }  // namespace
 
 int launch_offset_attn_fwd(const OffsetArgs& a, cudaStream_t stream) {
   if (a.head_dim != kD) return SA_ERR_UNSUPPORTED;
-  CUtensorMap kw, vw, ks, vs;
-  const uint32_t win_rows = (uint32_t)(kQ + a.window);
-  if (!encode_bhnd_map(&kw, a.k, a.batch, a.n_tokens, a.kv_heads, kD, a.kv_strides[0], a.kv_strides[1],
-                       a.kv_strides[2], kD, win_rows, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_bhnd_map(&vw, a.v, a.batch, a.n_tokens, a.kv_heads, kD, a.kv_strides[0], a.kv_strides[1],
-                       a.kv_strides[2], kD, win_rows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+  CUtensorMap kb, vb, ks, vs;
+  if (!encode_bhnd_map(&kb, a.k, a.batch, a.n_tokens, a.kv_heads, kD, a.kv_strides[0], a.kv_strides[1],
+                       a.kv_strides[2], kD, kBandRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_bhnd_map(&vb, a.v, a.batch, a.n_tokens, a.kv_heads, kD, a.kv_strides[0], a.kv_strides[1],
+                       a.kv_strides[2], kD, kBandRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_bhnd_map(&ks, a.k, a.batch, a.n_tokens, a.kv_heads, kD, a.kv_strides[0], a.kv_strides[1],
                        a.kv_strides[2], kD, kQ, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_bhnd_map(&vs, a.v, a.batch, a.n_tokens, a.kv_heads, kD, a.kv_strides[0], a.kv_strides[1],
@@ -254,9 +451,37 @@ int launch_offset_attn_fwd(const OffsetArgs& a, cudaStream_t stream) {
   p.n_tokens = a.n_tokens;
   p.heads = a.heads;
   p.heads_per_kv = a.heads / a.kv_heads;
-  p.window = a.window;
-  p.n_offsets = a.n_offsets;
   p.ntiles = (a.n_tokens + kQ - 1) / kQ;
+  // band: the window and every offset <= 64; distances 0..95 as a bit set
+  uint32_t dist_mask[3] = {0u, 0u, 0u};
+  int dmax = a.window;
+  for (int d = 0; d <= a.window; ++d) dist_mask[d >> 5] |= 1u << (d & 31);
+  p.n_large = 0;
+  for (int i = 0; i < a.n_offsets; ++i) {
+    const int d = a.offsets[i];
+    if (d <= kBandMax) {
+      dist_mask[d >> 5] |= 1u << (d & 31);
+      dmax = dmax > d ? dmax : d;
+    } else {
+      p.large[p.n_large++] = d;
+    }
+  }
+  for (int i = p.n_large; i < kMaxLarge; ++i) p.large[i] = 0;
+  p.dr = (dmax + 15) / 16 * 16;
+  const int nkt = (16 + p.dr) / 16;
+  // lane (g, t) holds score elements (row g + 8(e>>1), band column 8 nt + 2t + (e&1));
+  // band column col of row rr is at distance rr + Dr - col
+  for (int lane = 0; lane < 32; ++lane) {
+    const int g = lane >> 2, t = lane & 3;
+    unsigned long long bits = 0ull;
+    for (int nt = 0; nt < 2 * nkt; ++nt)
+      for (int e = 0; e < 4; ++e) {
+        const int rr = g + 8 * (e >> 1), col = 8 * nt + 2 * t + (e & 1);
+        const int dist = rr + p.dr - col;
+        if (dist >= 0 && dist < 96 && ((dist_mask[dist >> 5] >> (dist & 31)) & 1u)) bits |= 1ull << (4 * nt + e);
+      }
+    p.keep[lane] = bits;
+  }
   p.q = static_cast<const __nv_bfloat16*>(a.q);
   p.o = static_cast<__nv_bfloat16*>(a.o);
   p.lse = a.lse;
@@ -267,15 +492,13 @@ int launch_offset_attn_fwd(const OffsetArgs& a, cudaStream_t stream) {
   p.o_sn = a.o_strides[1];
   p.o_sh = a.o_strides[2];
   p.scale_log2 = a.softmax_scale * 1.4426950408889634f;
-  for (int k = 0; k < kMaxOffsets; ++k) p.offsets[k] = k < a.n_offsets ? a.offsets[k] : 0;
-  const int win_bytes = (((kQ + a.window) * kRowBytes) + 1023) & ~1023;
-  const size_t smem = 1024 + 2 * (size_t)win_bytes + 4 * (size_t)kSlabBytes;
-  if (cudaFuncSetAttribute(offset_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-      cudaSuccess)
-    return SA_ERR_CUDA;
-  dim3 grid((unsigned)(a.batch * a.heads), (unsigned)p.ntiles);
-  offset_attn_kernel<<<grid, kQ, smem, stream>>>(kw, vw, ks, vs, p);
-  return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+  switch (nkt) {
+    case 1: return launch_nkt<1>(kb, vb, ks, vs, p, a.batch, stream);
+    case 2: return launch_nkt<2>(kb, vb, ks, vs, p, a.batch, stream);
+    case 3: return launch_nkt<3>(kb, vb, ks, vs, p, a.batch, stream);
+    case 4: return launch_nkt<4>(kb, vb, ks, vs, p, a.batch, stream);
+    default: return launch_nkt<5>(kb, vb, ks, vs, p, a.batch, stream);
+  }
 }
 
 unsigned int offset_read_and_clear_error(cudaStream_t stream) {

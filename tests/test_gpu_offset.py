@@ -70,3 +70,38 @@ def test_fib_8k_one_layer_sampled():
     o_g = np.stack([o_np[s, i, h] for s, i, h in smp])
     l_g = np.array([lse_np[s, h, i] for s, i, h in smp])
     assert_attention_close(o_g, l_g, o_ref, lse_ref, "fib_8k")
+
+
+def _run_offsets(q64, k64, v64, qd, kd, vd, window, offs, what):
+    torch = torch_cuda()
+    o, lse = sa.offset_attn_fwd(qd, kd, vd, window, offs)
+    torch.cuda.synchronize()
+    assert sa.sa_device_status() == 0
+    o_ref, lse_ref = oracle.attention_offsets(q64, k64, v64, window, offs)
+    return assert_attention_close(bf16_to_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref, what)
+
+
+@pytest.mark.parametrize("window,offs", [
+    (8, [9, 31, 32, 33, 63, 64, 65, 79, 80, 96, 127, 128, 129, 500, 777]),   # both sides of the band limit
+    (0, [1, 2, 3, 5, 8, 13, 21, 34, 55, 89, 144, 233, 377, 610]),           # window 0, classic rungs
+    (64, [65, 66, 100, 1000]),                                               # widest window
+    (3, list(range(4, 68)) ),                                                # 64 offsets, all but 3 in the band
+])
+def test_explicit_offset_sets(window, offs):
+    rng = np.random.default_rng(window + len(offs))
+    n = 1100
+    qb = bf16_normal_bits(rng, (2, n, 2, 64), 0.5)
+    kb = bf16_normal_bits(rng, (2, n, 2, 64), 0.5)
+    vb = bf16_normal_bits(rng, (2, n, 2, 64), 0.5)
+    _run_offsets(bf16_bits_to_f64(qb), bf16_bits_to_f64(kb), bf16_bits_to_f64(vb), to_dev(qb), to_dev(kb),
+                 to_dev(vb), window, offs, f"W={window} offsets={offs[:4]}..")
+
+
+def test_packed_strided_inputs():
+    rng = np.random.default_rng(9)
+    bt, n, h = 2, 700, 4
+    packed = bf16_normal_bits(rng, (bt, n, 3, h, 64), 0.5)   # q, k, v interleaved per token
+    t = to_dev(packed)
+    f = bf16_bits_to_f64(packed)
+    _run_offsets(f[:, :, 0], f[:, :, 1], f[:, :, 2], t[:, :, 0], t[:, :, 1], t[:, :, 2], 8,
+                 [9, 13, 21, 34, 55, 89, 144, 233, 377, 610], "packed qkv")
