@@ -1,38 +1,41 @@
 // Block-sparse flash-attention forward for sm_103a (tcgen05 + TMEM + TMA).
 //
-// Work item: 256 consecutive query tokens of one (sequence, head) = two 128-row query
-// tiles A and B, covering 256 / b query blocks. The key blocks the item visits are the
-// sorted union of those blocks' CSR rows; each key block carries one membership bit per
-// query block. Key blocks are packed into key tiles of up to 128 keys; a key tile is
-// "active" for tile A (B) if any of A's (B's) query blocks has it in its row, and the
-// tensor core and the softmax of a query tile only touch its active key tiles.
+// Work item: one 128-row query tile of one (sequence, head), covering 128 / b query
+// blocks. The key blocks the tile visits are the sorted union of those blocks' CSR rows;
+// each key block carries one membership bit per query block of the tile. The union is cut
+// into 32-key chunks, and consecutive chunk pairs form 64-key key tiles.
 //
-// The kernel is persistent: one CTA per SM walks a static list of work items ordered
-// longest first (causal: last query tiles first; BigBird: the global rows first).
+// One CTA per SM runs two independent pipelines x = 0, 1 (one query tile each), so the
+// tensor core always has the other pipeline's work while one waits. Each pipeline has
+// its own Q buffer, K/V ring, meta ring and half of TMEM. The kernel is persistent: the
+// 2 x grid pipelines walk a static list of query tiles ordered longest first (causal: last
+// query tiles first; BigBird: the global rows first).
 //
-// Warp roles (352 threads, one CTA per SM):
-//   warp 0      producer: merges the CSR rows (all lanes, warp-uniform), publishes key-tile
-//               descriptions in a small ring, issues TMA loads of Q and of the K / V blocks.
-//   warps 1, 10 lane 0 of warp 1 (tile A) and of warp 10 (tile B) issue tcgen05 MMAs:
-//                 S_X = Q_X K^T          (A, B from shared memory)
-//                 O_X += P_X V           (A = P_X from TMEM, B = V, MN-major, from shared memory)
-//               QK_X(t+1) as soon as the softmax of X has released tile t, then PV_X(t);
-//               the two query tiles never wait on each other. Warp 1 owns TMEM (512 cols).
-//   warps 2-5   softmax of tile A, warps 6-9 softmax of tile B (warp w reads TMEM lane
-//               quarter w % 4), running concurrently: one query row per thread. One pass over
-//               S per tile, software-pipelined by 32-column chunks (the next chunk's TMEM load
-//               and max overlap this chunk's exponentials); lazily rescaled running max (P
-//               chunks and O are rescaled only when the max grows by more than 2^8); final
-//               normalisation and the O (bf16) / LSE (fp32) stores.
-// TMEM columns (Cfg::col_*): S_A [0,128), S_B [128,256); d <= 64: O_A [256,256+d),
-// O_B [320,320+d), P_A [384,448), P_B [448,512); d = 128: O_A [256,384), O_B [384,512)
-// and P aliases the first 64 columns of S.
+// Warp roles (640 threads):
+//   warps 0, 19  producer of pipeline 0 / 1: builds the union (whole warp), publishes
+//                key-tile descriptions, issues TMA loads of Q and of the K / V chunks.
+//   warps 1, 18  lane 0 issues the tcgen05 MMAs of pipeline 0 / 1:
+//                  S[j % NS] = Q K_j^T        (A, B from shared memory, N = 64 keys)
+//                  O += P_j V_j               (A = P_j from TMEM, B = V_j, MN-major)
+//                QK of the first NS key tiles up front; after each PV_j completes, QK_{j+NS}
+//                into the buffer it frees. The softmax therefore always finds the next S
+//                ready. Warp 1 owns TMEM (512 columns).
+//   warps 2-9, 10-17  softmax of pipeline 0 / 1, two warps per TMEM lane quarter (warp w
+//                reads quarter w % 4): one query row per thread, one 32-key chunk per warp.
+//                The pair agrees on each tile's row max through shared memory, keeps a
+//                lazily rescaled running max (O is rescaled only when the max grows by more
+//                than 2^8), writes P = 2^(s c - m) in bf16 over the first 32 columns of the
+//                tile's own S buffer, and finally normalises and stores its half of O (bf16)
+//                and the LSE (fp32). The exponentials (MUFU, 4 cycles per warp instruction
+//                on each SM sub-partition) bound this stage; four softmax warps per
+//                sub-partition keep that unit busy.
+// TMEM columns of pipeline x: S buffers [256x + 64i, +64), i < NS; O [256x + 64 NS, +d).
 //
 // Token rule: key j of block J is visible to query i of block I iff J is in row(I) and
 // (not causal or j <= i) ("Parameter-free Adaptive Sparse Attention via Compression-Based
 // Content Selection", section 3.4 block-to-token expansion). No token mask is
 // materialised: the per-row column mask comes from the membership bits and, on the
-// diagonal block, from the causal compare.
+// diagonal, from the causal compare.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -47,14 +50,16 @@ namespace {
 
 __device__ unsigned int g_attn_err;
 
-constexpr int kTile = 128;        // query rows per query tile, max keys per key tile
-constexpr int kItemRows = 256;    // query rows per work item (tiles A and B)
-constexpr int kThreads = 352;  // 11 warps: producer, MMA A, 2 x 4 softmax, MMA B
-constexpr int kMetaRing = 4;
-constexpr int kMaxSlots = 4;      // key blocks per key tile (128 / b, b >= 32)
-constexpr int kMaxRows = 8;       // query blocks per work item (256 / b)
+constexpr int kTile = 128;          // query rows per work item
+constexpr int kKeyTile = 64;        // keys per S tile (two 32-key chunks)
+constexpr int kThreads = 640;       // 20 warps
+constexpr int kMetaRing = 8;
+constexpr int kMaxQBlocks = 4;      // query blocks per tile (128 / b, b >= 32)
 constexpr uint32_t kTmemCols = 512;
-constexpr int kMetaConsumers = 10; // 8 softmax warps + the two MMA threads
+constexpr int kSoftmaxWarps = 8;    // per pipeline: two per TMEM lane quarter (one per 32-key chunk)
+constexpr int kMetaConsumers = 1 + kSoftmaxWarps;   // the MMA thread and the softmax warps
+constexpr int kMaxStages = 8;
+constexpr int kMaxSBuf = 3;
 
 template <int D>
 struct Cfg {
@@ -65,29 +70,35 @@ struct Cfg {
   static constexpr CUtensorMapSwizzle TMA_SWZ =
       ROWB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   static constexpr uint32_t ATOM = 8 * ROWB;           // swizzle atom (8 rows)
-  static constexpr int CHUNK = kTile * ROWB;           // one d-chunk of a 128-row tile
-  static constexpr int TILE_BYTES = NCH * CHUNK;       // 128 rows x D bf16
-  static constexpr int STAGES = D == 128 ? 2 : (D == 64 ? 3 : 4);   // K and V ring depth
-  static constexpr int UNION_BYTES = (kMaxRows * kMaxMaskBlocks / 32 + kMaxMaskBlocks) * 4;   // 20 KB
-  static constexpr int SMEM_NEED = 1024 + TILE_BYTES * (2 + 2 * STAGES) + UNION_BYTES;
+  static constexpr int Q_CHUNK = kTile * ROWB;         // one d-chunk of the 128-row Q tile
+  static constexpr int Q_BYTES = NCH * Q_CHUNK;
+  static constexpr int KV_CHUNK = kKeyTile * ROWB;     // one d-chunk of a 64-key K or V tile
+  static constexpr int KV_BYTES = NCH * KV_CHUNK;
+  // d <= 64: each 32-key chunk half of a tile has its own O accumulator (and running max),
+  // so the two softmax warps of a row never synchronise per tile; d = 128: one O.
+  static constexpr bool SPLIT = D <= 64;
+  static constexpr int NO = SPLIT ? 2 : 1;             // O accumulators per pipeline
+  static constexpr int NS = D == 32 ? 3 : 2;           // S buffers per pipeline
+  static constexpr int QB = D > 64 ? 1 : 2;            // Q buffers per pipeline
+  static constexpr int STAGES = D == 128 ? 2 : (D == 64 ? 4 : 6);   // K and V ring depth
+  static constexpr int UNION_BYTES = kMaxQBlocks * (kMaxMaskBlocks / 32) * 4 + kMaxMaskBlocks * 2;   // 10 KB
+  static constexpr int PIPE_BYTES = (QB * Q_BYTES + 2 * STAGES * KV_BYTES + UNION_BYTES + 1023) & ~1023;
+  static constexpr int SMEM_NEED = 1024 + 2 * PIPE_BYTES;
   // at least 120 KB so that only one CTA (512 TMEM columns) is resident per SM
   static constexpr int SMEM = SMEM_NEED > 120 * 1024 ? SMEM_NEED : 120 * 1024;
-  static constexpr bool P_ALIAS = D > 64;              // no room for separate P columns
-  __host__ __device__ static constexpr uint32_t col_s(int x) { return x ? 128u : 0u; }
-  __host__ __device__ static constexpr uint32_t col_o(int x) { return x ? (D > 64 ? 384u : 320u) : 256u; }
-  __host__ __device__ static constexpr uint32_t col_p(int x) {
-    return P_ALIAS ? col_s(x) : (x ? 448u : 384u);
-  }
+  __host__ __device__ static constexpr uint32_t col_s(int x, int i) { return 256u * x + 64u * i; }
+  __host__ __device__ static constexpr uint32_t col_o(int x, int h) { return 256u * x + 64u * NS + (SPLIT ? D * h : 0); }
+  static_assert(64 * NS + NO * D <= 256, "TMEM budget of a pipeline");
+  static_assert(STAGES >= NS && STAGES <= kMaxStages && NS <= kMaxSBuf, "ring sizes");
 };
 
-enum : int { kKeyTile = 0, kEndItem = 1 };
+enum : int { kKindTile = 0, kKindEnd = 1 };
 
 struct Meta {
   int kind;
-  int nslots;
-  int active;                 // bit 0: tile A, bit 1: tile B
-  int jblk[kMaxSlots];
-  int mask[kMaxSlots];        // bit r: query block r of the item has this key block
+  int nch;                    // chunks (1 or 2) in this key tile
+  int tok[2];                 // first key token of each chunk
+  int mask[2];                // bit r: query block r of the tile has the chunk's key block
 };
 
 // Field-wise read of a published ring entry (the producer's mbarrier arrive orders it).
@@ -95,19 +106,17 @@ __device__ __forceinline__ Meta load_meta(const Meta* src) {
   const volatile Meta* vm = src;
   Meta m;
   m.kind = vm->kind;
-  m.nslots = vm->nslots;
-  m.active = vm->active;
-#pragma unroll
-  for (int i = 0; i < kMaxSlots; ++i) {
-    m.jblk[i] = vm->jblk[i];
-    m.mask[i] = vm->mask[i];
-  }
+  m.nch = vm->nch;
+  m.tok[0] = vm->tok[0];
+  m.tok[1] = vm->tok[1];
+  m.mask[0] = vm->mask[0];
+  m.mask[1] = vm->mask[1];
   return m;
 }
 
 struct Params {
   int batch, n_tokens, heads, heads_per_kv, block, log2b, nb, causal, csr_shared;
-  int pairs_per_seq;          // work items per (sequence, head)
+  int tiles_per_seq;          // 128-row query tiles per (sequence, head)
   int n_items;
   const int32_t* row_ptr;
   const int32_t* col_idx;
@@ -117,32 +126,62 @@ struct Params {
   float scale_log2;
 };
 
-struct Bars {
-  uint64_t q_full, q_empty;
-  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+struct PipeBars {
+  uint64_t q_full[2], q_empty[2];
+  uint64_t k_full[kMaxStages], k_empty[kMaxStages], v_full[kMaxStages], v_empty[kMaxStages];
   uint64_t m_full[kMetaRing], m_empty[kMetaRing];
-  uint64_t s_full[2], p_full[2], pv_done[2], o_empty[2];
-  uint64_t drain[2];
+  uint64_t s_full[kMaxSBuf], p_full[kMaxSBuf];
+  uint64_t pv_done[2], o_empty, drain;   // pv_done[j & 1]: PV of key tile j
+  // PVs of this pipeline known complete, written by the MMA thread (which waits for every
+  // PV in order). The epilogue waits on this count: a parity wait on pv_done could be two
+  // phases off there, and one that is a phase ahead of the barrier passes at once.
+  int pv_count;
 };
 
 struct Item {
-  int s, h, pair;
+  int s, h, tile;
 };
 
 // Work item k of the static longest-first order: all (sequence, head) pairs of one
-// query-pair rank before the next rank; causal ranks run from the last query pair.
+// query-tile rank before the next rank; causal ranks run from the last query tile.
 __device__ __forceinline__ Item decode_item(const Params& p, int k) {
   const int bh = k % (p.batch * p.heads);
   const int rank = k / (p.batch * p.heads);
   Item it;
   it.h = bh % p.heads;
   it.s = bh / p.heads;
-  it.pair = p.causal ? (p.pairs_per_seq - 1 - rank) : rank;
+  it.tile = p.causal ? (p.tiles_per_seq - 1 - rank) : rank;
   return it;
 }
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
   return mbar_wait(bar, parity, abort_flag, &g_attn_err, kErrTimeout);
+}
+
+// Bounded wait until *count >= target (a monotonic counter published with release
+// semantics by another thread of the CTA).
+__device__ __forceinline__ bool wait_count(const int* count, int target, volatile int* abort_flag) {
+  const volatile int* c = count;
+  if (*c >= target) {
+    __threadfence_block();
+    return true;
+  }
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(64);                 // leave the issue slots to working warps
+    if (*c >= target) {
+      __threadfence_block();
+      return true;
+    }
+    if ((it & 15u) == 0u) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        atomicOr(&g_attn_err, kErrTimeout);
+        return false;
+      }
+    }
+  }
 }
 
 __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity) {
@@ -168,19 +207,24 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
 
-// ------------------------------------------------------------------ producer (warp 0)
+// ------------------------------------------------------------------ producer (warps 0, 11)
 
-// Per-item key-block union, built by the producer warp in shared memory: one bitmap of
-// nb bits per query block of the item, then an ascending list of (J | membership << 16).
+// Per-tile key-block union, built by the producer warp in shared memory: one bitmap of
+// nb bits per query block of the tile, then an ascending list of (J | membership << 12).
 struct UnionSmem {
-  uint32_t bm[kMaxRows][kMaxMaskBlocks / 32];   // 4 KB
-  uint32_t list[kMaxMaskBlocks];                // 16 KB
+  uint32_t bm[kMaxQBlocks][kMaxMaskBlocks / 32];   // 2 KB
+  uint16_t list[kMaxMaskBlocks];                   // 8 KB
 };
 
 // Builds the union of rows I0 .. I0+nq-1 into u.list; returns its length. Column indices
@@ -192,17 +236,17 @@ __device__ int build_union(const Params& p, UnionSmem& u, const int32_t* rp, int
   for (int r = 0; r < nq; ++r)
     for (int w = lane; w < nw; w += 32) u.bm[r][w] = 0u;
   const int bnd = (lane <= nq) ? rp[I0 + lane] : 0x7fffffff;   // lane r: start of row r
-  int bq[kMaxRows + 1];
+  int bq[kMaxQBlocks + 1];
 #pragma unroll
-  for (int q = 0; q <= kMaxRows; ++q) bq[q] = __shfl_sync(0xffffffffu, bnd, min(q, nq));
+  for (int q = 0; q <= kMaxQBlocks; ++q) bq[q] = __shfl_sync(0xffffffffu, bnd, min(q, nq));
   const int e0 = bq[0];
-  const int e1 = bq[kMaxRows];
+  const int e1 = bq[kMaxQBlocks];
   __syncwarp();
   for (int e = e0 + lane; e < e1; e += 32) {
     const int J = p.col_idx[e];
     int r = 0;
 #pragma unroll
-    for (int q = 1; q < kMaxRows; ++q) r += (q < nq && e >= bq[q]) ? 1 : 0;
+    for (int q = 1; q < kMaxQBlocks; ++q) r += (q < nq && e >= bq[q]) ? 1 : 0;
     if (J < 0 || J >= p.nb) {
       atomicOr(&g_attn_err, kErrBadIndex);
     } else if (!p.causal || J <= I0 + r) {
@@ -213,10 +257,10 @@ __device__ int build_union(const Params& p, UnionSmem& u, const int32_t* rp, int
   int total = 0;
   for (int w0 = 0; w0 < nw; w0 += 32) {
     const int w = w0 + lane;
-    uint32_t word[kMaxRows];
+    uint32_t word[kMaxQBlocks];
     uint32_t un = 0u;
 #pragma unroll
-    for (int r = 0; r < kMaxRows; ++r) {
+    for (int r = 0; r < kMaxQBlocks; ++r) {
       word[r] = (r < nq && w < nw) ? u.bm[r][w] : 0u;
       un |= word[r];
     }
@@ -233,8 +277,8 @@ __device__ int build_union(const Params& p, UnionSmem& u, const int32_t* rp, int
       un &= un - 1u;
       uint32_t mask = 0u;
 #pragma unroll
-      for (int r = 0; r < kMaxRows; ++r) mask |= ((word[r] >> j) & 1u) << r;
-      u.list[pos++] = (uint32_t)(w * 32 + j) | (mask << 16);
+      for (int r = 0; r < kMaxQBlocks; ++r) mask |= ((word[r] >> j) & 1u) << r;
+      u.list[pos++] = (uint16_t)((uint32_t)(w * 32 + j) | (mask << 12));
     }
     total += __shfl_sync(0xffffffffu, incl, 31);
   }
@@ -243,39 +287,36 @@ __device__ int build_union(const Params& p, UnionSmem& u, const int32_t* rp, int
 }
 
 template <int D>
-__device__ void producer(const Params& p, const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
-                         Bars& bars, Meta* meta, UnionSmem& u, uint8_t* sQ, uint8_t* sK, uint8_t* sV,
-                         volatile int* abort_flag) {
+__device__ void producer(const Params& p, int x, const CUtensorMap* tq, const CUtensorMap* tk,
+                         const CUtensorMap* tv, PipeBars& bars, Meta* meta, UnionSmem& u, uint8_t* sQ, uint8_t* sK,
+                         uint8_t* sV, volatile int* abort_flag) {
   using C = Cfg<D>;
   const int lane = threadIdx.x & 31;
   const int b = p.block;
-  const int rows_per_item = kItemRows >> p.log2b;
-  const int slots_per_tile = kTile >> p.log2b;
-  const int maskA = (1 << (kTile >> p.log2b)) - 1;   // query blocks of tile A
+  const int cpb = b >> 5;                            // 32-key chunks per key block
+  const int qb_per_tile = kTile >> p.log2b;
   int mt = 0, kt = 0, item_local = 0;
   int k_issued = 0, v_issued = 0;                    // key tiles whose K / V loads were issued
   int q_last = -1;                                   // item_local of the last Q load
   bool ok = true;
 
-  for (int k = blockIdx.x; k < p.n_items && ok; k += gridDim.x, ++item_local) {
+  for (int k = 2 * blockIdx.x + x; k < p.n_items && ok; k += 2 * gridDim.x, ++item_local) {
     const Item it = decode_item(p, k);
-    const int I0 = it.pair * rows_per_item;
-    const int q0 = it.pair * kItemRows;
+    const int q0 = it.tile * kTile;
+    const int I0 = q0 >> p.log2b;
     const int hk = it.h / p.heads_per_kv;
-    const int nq = min(rows_per_item, p.nb - I0);
+    const int nq = min(qb_per_tile, p.nb - I0);
     const int32_t* rp = p.row_ptr + (size_t)(p.csr_shared ? 0 : it.s) * (p.nb + 1);
 
-    // Q of both tiles (rows beyond the sequence are zero-filled by TMA)
+    // Q into buffer item_local % QB (rows beyond the sequence are zero-filled by TMA)
     if (lane == 0) {
-      if (item_local > 0) ok = wait_bar(&bars.q_empty, (item_local - 1) & 1, abort_flag);
+      const int qb = item_local % C::QB;
+      if (item_local >= C::QB) ok = wait_bar(&bars.q_empty[qb], ((item_local / C::QB) - 1) & 1, abort_flag);
       if (ok) {
-        mbar_arrive_expect_tx(&bars.q_full, 2 * C::TILE_BYTES);
+        mbar_arrive_expect_tx(&bars.q_full[qb], C::Q_BYTES);
 #pragma unroll
-        for (int x = 0; x < 2; ++x)
-#pragma unroll
-          for (int c = 0; c < C::NCH; ++c)
-            tma_load_4d(sQ + x * C::TILE_BYTES + c * C::CHUNK, tq, &bars.q_full, c * C::CH, it.h, q0 + x * kTile,
-                        it.s);
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_4d(sQ + qb * C::Q_BYTES + c * C::Q_CHUNK, tq, &bars.q_full[qb], c * C::CH, it.h, q0, it.s);
         q_last = item_local;
       }
     }
@@ -283,18 +324,18 @@ __device__ void producer(const Params& p, const CUtensorMap* tq, const CUtensorM
     if (!ok) break;
 
     const int n_keys = build_union(p, u, rp, I0, nq);
+    const int n_chunks = n_keys * cpb;
 
-    for (int base = 0;; base += slots_per_tile) {
+    for (int c0 = 0;; c0 += 2) {
       Meta m;
-      m.kind = base < n_keys ? kKeyTile : kEndItem;
-      m.nslots = min(slots_per_tile, n_keys - base);
-      m.active = 0;
+      m.kind = c0 < n_chunks ? kKindTile : kKindEnd;
+      m.nch = min(2, n_chunks - c0);
 #pragma unroll
-      for (int i = 0; i < kMaxSlots; ++i) {
-        const uint32_t e = (i < m.nslots) ? u.list[base + i] : 0u;
-        m.jblk[i] = (int)(e & 0xffffu);
-        m.mask[i] = (int)(e >> 16);
-        m.active |= ((m.mask[i] & maskA) ? 1 : 0) | ((m.mask[i] & ~maskA) ? 2 : 0);
+      for (int i = 0; i < 2; ++i) {
+        const int q = c0 + i;
+        const uint32_t e = (i < m.nch) ? u.list[q / cpb] : 0u;
+        m.tok[i] = (int)(e & 0xfffu) * b + (q % cpb) * 32;
+        m.mask[i] = (i < m.nch) ? (int)(e >> 12) : 0;
       }
       if (lane == 0) {
         const int ms = mt % kMetaRing;
@@ -303,48 +344,44 @@ __device__ void producer(const Params& p, const CUtensorMap* tq, const CUtensorM
           meta[ms] = m;
           mbar_arrive(&bars.m_full[ms]);
         }
-        if (ok && m.kind == kKeyTile) {
+        if (ok && m.kind == kKindTile) {
           const int st = kt % C::STAGES;
           const uint32_t ph = (kt / C::STAGES) & 1;
-          const uint32_t bytes = (uint32_t)(m.nslots * b * D * 2);
+          const uint32_t bytes = (uint32_t)(m.nch * 32 * D * 2);
+          // b = 32: one 32-row box per chunk; b >= 64: the two chunks are one 64-row box
+          const int nbox = b == 32 ? m.nch : 1;
           ok = wait_bar(&bars.k_empty[st], ph ^ 1, abort_flag);
           if (ok) {
             mbar_arrive_expect_tx(&bars.k_full[st], bytes);
+            for (int i = 0; i < nbox; ++i)
 #pragma unroll
-            for (int i = 0; i < kMaxSlots; ++i)
-              if (i < m.nslots) {
-#pragma unroll
-                for (int c = 0; c < C::NCH; ++c)
-                  tma_load_4d(sK + st * C::TILE_BYTES + c * C::CHUNK + i * b * C::ROWB, tk, &bars.k_full[st],
-                              c * C::CH, hk, m.jblk[i] * b, it.s);
-              }
+              for (int c = 0; c < C::NCH; ++c)
+                tma_load_4d(sK + st * C::KV_BYTES + c * C::KV_CHUNK + i * 32 * C::ROWB, tk, &bars.k_full[st],
+                            c * C::CH, hk, m.tok[i], it.s);
             k_issued = kt + 1;
             ok = wait_bar(&bars.v_empty[st], ph ^ 1, abort_flag);
           }
           if (ok) {
             mbar_arrive_expect_tx(&bars.v_full[st], bytes);
+            for (int i = 0; i < nbox; ++i)
 #pragma unroll
-            for (int i = 0; i < kMaxSlots; ++i)
-              if (i < m.nslots) {
-#pragma unroll
-                for (int c = 0; c < C::NCH; ++c)
-                  tma_load_4d(sV + st * C::TILE_BYTES + c * C::CHUNK + i * b * C::ROWB, tv, &bars.v_full[st],
-                              c * C::CH, hk, m.jblk[i] * b, it.s);
-              }
+              for (int c = 0; c < C::NCH; ++c)
+                tma_load_4d(sV + st * C::KV_BYTES + c * C::KV_CHUNK + i * 32 * C::ROWB, tv, &bars.v_full[st],
+                            c * C::CH, hk, m.tok[i], it.s);
             v_issued = kt + 1;
           }
         }
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       ++mt;
-      if (m.kind == kKeyTile) ++kt;
-      if (!ok || m.kind == kEndItem) break;
+      if (m.kind == kKindTile) ++kt;
+      if (!ok || m.kind == kKindEnd) break;
     }
-    __syncwarp();   // the next item's union may overwrite the list
+    __syncwarp();   // the next tile's union may overwrite the list
   }
-  // Drain this CTA's own copies in flight before the CTA may exit.
+  // Drain this pipeline's own copies in flight before the CTA may exit.
   if (lane == 0) {
-    if (q_last >= 0) drain_bar(&bars.q_full, q_last & 1);
+    for (int i = max(0, q_last - C::QB + 1); i <= q_last; ++i) drain_bar(&bars.q_full[i % C::QB], (i / C::QB) & 1);
     // the last tile that used each stage: waiting on it covers every earlier use
     for (int t = max(0, k_issued - C::STAGES); t < k_issued; ++t)
       drain_bar(&bars.k_full[t % C::STAGES], (t / C::STAGES) & 1);
@@ -354,353 +391,315 @@ __device__ void producer(const Params& p, const CUtensorMap* tq, const CUtensorM
   __syncwarp();
 }
 
-// ------------------------------------------------------------------ MMA issuer (warp 1, lane 0)
+// ------------------------------------------------------------------ MMA issuer (warps 1, 10, lane 0)
+
+// Byte offset (>> 4, the descriptor's address unit) of k-step ks inside a K-major tile
+// whose d-chunks are `chunk` bytes apart.
+template <int D>
+__device__ __forceinline__ constexpr uint32_t kmajor_step(int ks, int chunk) {
+  using C = Cfg<D>;
+  return (uint32_t)(((ks * 16) / C::CH) * chunk + ((ks * 16) % C::CH) * 2) >> 4;
+}
 
 template <int D>
 struct MmaState {
   uint32_t tmem;
-  uint64_t qdesc[2];      // descriptors of Q_A, Q_B at k-step 0
-  uint64_t kdesc0, vdesc0;  // descriptors of K / V stage 0 at k-step 0
-  int kt;                 // K/V ring position of the current key tile
-  int cnt[2];             // QK count per query tile (global)
-  int pv[2];              // PV count per query tile (global)
+  uint64_t qdesc, kdesc0, vdesc0;   // Q, K stage 0, V stage 0 at k-step 0
 };
 
-// Byte offset (>> 4, the descriptor's address unit) of k-step ks inside a K-major tile.
 template <int D>
-__device__ __forceinline__ constexpr uint32_t kmajor_step(int ks) {
-  using C = Cfg<D>;
-  return (uint32_t)(((ks * 16) / C::CH) * C::CHUNK + ((ks * 16) % C::CH) * 2) >> 4;
-}
-
-template <int D>
-__device__ __forceinline__ void issue_qk(MmaState<D>& st, int x, int stage, int nkeys) {
+__device__ __forceinline__ void issue_qk(const MmaState<D>& st, int x, int qb, int buf, int stage, int nkeys) {
   using C = Cfg<D>;
   const uint32_t idesc = make_idesc_bf16(128, (uint32_t)nkeys, 0, 0);
-  const uint64_t a0 = st.qdesc[x];
-  const uint64_t b0 = st.kdesc0 + (uint64_t)((stage * C::TILE_BYTES) >> 4);
-  const uint32_t d = st.tmem + C::col_s(x);
+  const uint64_t a0 = st.qdesc + (uint64_t)((qb * C::Q_BYTES) >> 4);
+  const uint64_t b0 = st.kdesc0 + (uint64_t)((stage * C::KV_BYTES) >> 4);
+  const uint32_t d = st.tmem + C::col_s(x, buf);
 #pragma unroll
   for (int ks = 0; ks < D / 16; ++ks)
-    mma_bf16_ss(d, a0 + kmajor_step<D>(ks), b0 + kmajor_step<D>(ks), idesc, ks > 0 ? 1u : 0u);
+    mma_bf16_ss(d, a0 + kmajor_step<D>(ks, C::Q_CHUNK), b0 + kmajor_step<D>(ks, C::KV_CHUNK), idesc,
+                ks > 0 ? 1u : 0u);
 }
 
+// O += P V for one key tile; P of chunk h (keys 32h .. 32h+31) sits in TMEM columns
+// 32h .. 32h+15 of the S buffer. With split accumulators chunk h goes to O_h; `init` says
+// whether O_h already holds this query tile's sum (else it is overwritten), and is updated.
 template <int D>
-__device__ __forceinline__ void issue_pv(MmaState<D>& st, int x, int stage, int nkeys, bool accumulate) {
+__device__ __forceinline__ void issue_pv(const MmaState<D>& st, int x, int buf, int stage, int nkeys, bool (&init)[2]) {
   using C = Cfg<D>;
   const uint32_t idesc = make_idesc_bf16(128, D, 0, 1);
-  const uint64_t b0 = st.vdesc0 + (uint64_t)((stage * C::TILE_BYTES) >> 4);
-  const uint32_t d = st.tmem + C::col_o(x), a = st.tmem + C::col_p(x);
-  const int nks = nkeys >> 4;
-#pragma unroll 8
-  for (int ks = 0; ks < nks; ++ks)
-    mma_bf16_ts(d, a + (uint32_t)(ks * 8), b0 + (uint64_t)((ks * 16 * C::ROWB) >> 4), idesc,
-                (accumulate || ks > 0) ? 1u : 0u);
+  const uint64_t b0 = st.vdesc0 + (uint64_t)((stage * C::KV_BYTES) >> 4);
+  const uint32_t a = st.tmem + C::col_s(x, buf);
+  if (C::SPLIT) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (h == 1 && nkeys <= 32) break;
+      const uint32_t d = st.tmem + C::col_o(x, h);
+      mma_bf16_ts(d, a + 32u * h, b0 + (uint64_t)((32 * h * C::ROWB) >> 4), idesc, init[h] ? 1u : 0u);
+      mma_bf16_ts(d, a + 32u * h + 8u, b0 + (uint64_t)(((32 * h + 16) * C::ROWB) >> 4), idesc, 1u);
+      init[h] = true;
+    }
+  } else {
+    const uint32_t d = st.tmem + C::col_o(x, 0);
+    mma_bf16_ts(d, a, b0, idesc, init[0] ? 1u : 0u);
+    mma_bf16_ts(d, a + 8u, b0 + (uint64_t)((16 * C::ROWB) >> 4), idesc, 1u);
+    if (nkeys > 32) {
+      mma_bf16_ts(d, a + 32u, b0 + (uint64_t)((32 * C::ROWB) >> 4), idesc, 1u);
+      mma_bf16_ts(d, a + 40u, b0 + (uint64_t)((48 * C::ROWB) >> 4), idesc, 1u);
+    }
+    init[0] = true;
+  }
 }
 
-// One MMA-issuing thread per query tile x (warp 1 lane 0: tile A, warp 10 lane 0: tile B).
-// For each key tile active for x: QK_x(t) as soon as the softmax of x has released the
-// previous tile (S_x read, P_x written), then PV_x of that previous tile. With P aliased
-// into S (d = 128) the previous PV goes first and must complete before QK_x(t).
+// Per-S-buffer record of the key tiles whose QK is issued and PV pending (at most NS; kept
+// in scalars selected by buffer index so nothing goes through local memory).
+struct PendRing {
+  int stage0, stage1, stage2, nkeys0, nkeys1, nkeys2;
+  __device__ __forceinline__ void put(int buf, int stage, int nkeys) {
+    if (buf == 0) { stage0 = stage; nkeys0 = nkeys; }
+    else if (buf == 1) { stage1 = stage; nkeys1 = nkeys; }
+    else { stage2 = stage; nkeys2 = nkeys; }
+  }
+  __device__ __forceinline__ void get(int buf, int& stage, int& nkeys) const {
+    stage = buf == 0 ? stage0 : (buf == 1 ? stage1 : stage2);
+    nkeys = buf == 0 ? nkeys0 : (buf == 1 ? nkeys1 : nkeys2);
+  }
+};
+
+// The MMA-issuing thread of pipeline x. Per query tile: QK of the first NS key tiles, then
+// for each key tile j: wait for P_j, PV_j, and once PV_{j+2-NS} has completed (it frees S
+// buffer (j+2-NS) % NS), QK_{j+2} into that buffer. PVs are waited for in order and the
+// completed count is published for the softmax epilogue.
 template <int D>
-__device__ void mma_issuer(const Params& p, Bars& bars, Meta* meta, uint8_t* sQ, uint8_t* sK, uint8_t* sV,
-                           uint32_t tmem, int x, volatile int* abort_flag) {
+__device__ void mma_issuer(const Params& p, int x, PipeBars& bars, Meta* meta, uint8_t* sQ, uint8_t* sK,
+                           uint8_t* sV, uint32_t tmem, volatile int* abort_flag) {
   using C = Cfg<D>;
   MmaState<D> st;
   st.tmem = tmem;
-  st.qdesc[0] = make_smem_desc(smem_u32(sQ), 16, C::ATOM, C::SWZ);
-  st.qdesc[1] = make_smem_desc(smem_u32(sQ) + C::TILE_BYTES, 16, C::ATOM, C::SWZ);
+  st.qdesc = make_smem_desc(smem_u32(sQ), 16, C::ATOM, C::SWZ);
   st.kdesc0 = make_smem_desc(smem_u32(sK), 16, C::ATOM, C::SWZ);
-  st.vdesc0 = make_smem_desc(smem_u32(sV), C::CHUNK, C::ATOM, C::SWZ);
-  int mt = 0, kt = 0;
-  int pvn = 0;              // PVs issued for x (global) == tiles of x released by the softmax
+  st.vdesc0 = make_smem_desc(smem_u32(sV), C::KV_CHUNK, C::ATOM, C::SWZ);
+  int mt = 0;               // metas read
+  int kt = 0;               // key tiles read (K/V ring position)
+  int g0 = 0;               // key tiles of this pipeline before the current query tile
+  int pdone = 0;            // PVs of this pipeline known complete
   bool ok = true;
   int item_local = 0;
-  for (int k = blockIdx.x; k < p.n_items && ok; k += gridDim.x, ++item_local) {
-    if (!(ok = wait_bar(&bars.q_full, item_local & 1, abort_flag))) break;
-    bool first_pv = true;
-    int pend_stage = -1, pend_keys = 0;
-    uint32_t pend_ph = 0;
-    auto issue_pending_pv = [&]() -> bool {
-      if (!wait_bar(&bars.v_full[pend_stage], pend_ph, abort_flag)) return false;
-      if (first_pv && item_local > 0 && !wait_bar(&bars.o_empty[x], (item_local - 1) & 1, abort_flag)) return false;
-      tc_fence_after();
-      issue_pv<D>(st, x, pend_stage, pend_keys, !first_pv);
-      mma_commit(&bars.pv_done[x]);
-      mma_commit(&bars.v_empty[pend_stage]);
-      first_pv = false;
-      ++pvn;
-      pend_stage = -1;
-      return true;
-    };
+  PendRing pend{0, 0, 0, 0, 0, 0};
+  for (int k = 2 * blockIdx.x + x; k < p.n_items && ok; k += 2 * gridDim.x, ++item_local) {
+    const int qb = item_local % C::QB;
+    if (!(ok = wait_bar(&bars.q_full[qb], (item_local / C::QB) & 1, abort_flag))) break;
+    int qi = 0, pi = 0;
+    bool end = false;
+    bool o_init[2] = {false, false};   // O accumulators written in this query tile
+    // Issue QKs while S buffers are free (QK_t needs PV_{t-NS} complete): read the next
+    // key tile's meta, wait for its K, QK into S buffer t % NS.
     for (;;) {
-      const int ms = mt % kMetaRing;
-      if (!(ok = wait_bar(&bars.m_full[ms], (mt / kMetaRing) & 1, abort_flag))) break;
-      const Meta m = load_meta(&meta[ms]);
-      mbar_arrive(&bars.m_empty[ms]);
-      ++mt;
-      if (m.kind != kKeyTile) break;
-      const int stage = kt % C::STAGES;
-      const uint32_t ph = (kt / C::STAGES) & 1;
-      ++kt;
-      const bool act = (m.active & (1 << x)) != 0;
-      if (pend_stage >= 0 && (!act || C::P_ALIAS)) {
-        // resolve the pending PV first: every later release of a K/V stage by this
-        // thread must be ordered after it (and with P aliased into S, so must the QK)
-        if (!(ok = wait_bar(&bars.p_full[x], (pvn & 1), abort_flag))) break;
-        if (!(ok = issue_pending_pv())) break;
-      }
-      if (!act) {
-        // This query tile does not read the stage. Release it only once it has been
-        // filled for this tile: mbarrier arrivals carry no phase, so a consumer must not
-        // run ahead of the producer by a whole ring lap. tcgen05.commit orders the
-        // release behind this thread's earlier MMAs.
+      while (ok && !end && g0 + qi < pdone + C::NS) {
+        const int ms = mt & (kMetaRing - 1);
+        if (!(ok = wait_bar(&bars.m_full[ms], (uint32_t)(mt / kMetaRing) & 1u, abort_flag))) break;
+        const Meta m = load_meta(&meta[ms]);
+        mbar_arrive(&bars.m_empty[ms]);
+        ++mt;
+        if (m.kind != kKindTile) {
+          end = true;
+          break;
+        }
+        const int stage = kt % C::STAGES;
+        const uint32_t ph = (uint32_t)(kt / C::STAGES) & 1u;
+        ++kt;
+        const int t = g0 + qi;
+        const int buf = t % C::NS;
         if (!(ok = wait_bar(&bars.k_full[stage], ph, abort_flag))) break;
+        tc_fence_after();
+        issue_qk<D>(st, x, qb, buf, stage, m.nch * 32);
+        mma_commit(&bars.s_full[buf]);
         mma_commit(&bars.k_empty[stage]);
-        if (!(ok = wait_bar(&bars.v_full[stage], ph, abort_flag))) break;
-        mma_commit(&bars.v_empty[stage]);
-        continue;
+        pend.put(buf, stage, m.nch * 32);
+        ++qi;
       }
-      if (!(ok = wait_bar(&bars.k_full[stage], ph, abort_flag))) break;
-      if (pend_stage >= 0) {
-        // the softmax of x has read S_x and written P_x of the pending tile
-        if (!(ok = wait_bar(&bars.p_full[x], (pvn & 1), abort_flag))) break;
+      if (!ok || pi == qi) break;
+      // PV of the oldest pending key tile
+      const int g = g0 + pi;
+      const int buf = g % C::NS;
+      int stage, nkeys;
+      pend.get(buf, stage, nkeys);
+      // the softmax has read S_j and written P_j
+      if (!(ok = wait_bar(&bars.p_full[buf], (uint32_t)(g / C::NS) & 1u, abort_flag))) break;
+      if (pi == 0 && item_local > 0) {
+        // the previous query tile's epilogue has read O
+        if (!(ok = wait_bar(&bars.o_empty, (uint32_t)(item_local - 1) & 1u, abort_flag))) break;
       }
-      if (C::P_ALIAS && pvn > 0) {
-        // P_x lives in S_x's columns: the last PV reading it must be complete
-        if (!(ok = wait_bar(&bars.pv_done[x], (pvn - 1) & 1, abort_flag))) break;
-      }
+      // V of this key tile: its ring lap is the one its K had
+      const int vkt = kt - (qi - pi);
+      if (!(ok = wait_bar(&bars.v_full[stage], (uint32_t)(vkt / C::STAGES) & 1u, abort_flag))) break;
       tc_fence_after();
-      issue_qk<D>(st, x, stage, m.nslots * p.block);
-      mma_commit(&bars.s_full[x]);
-      mma_commit(&bars.k_empty[stage]);
-      if (pend_stage >= 0 && !(ok = issue_pending_pv())) break;
-      pend_stage = stage;
-      pend_keys = m.nslots * p.block;
-      pend_ph = ph;
+      issue_pv<D>(st, x, buf, stage, nkeys, o_init);
+      mma_commit(&bars.pv_done[g & 1]);
+      mma_commit(&bars.v_empty[stage]);
+      ++pi;
+      // PV_{g+2-NS} completes (in order) before QK_{g+2} takes its S buffer: with two
+      // buffers that is PV_g itself, with three PV_{g-1}, which had a whole key tile to
+      // finish while PV_g waits in the queue.
+      const int j = g + 2 - C::NS;
+      if (j >= pdone) {
+        if (!(ok = wait_bar(&bars.pv_done[j & 1], (uint32_t)(j >> 1) & 1u, abort_flag))) break;
+        pdone = j + 1;
+        __threadfence_block();
+        *reinterpret_cast<volatile int*>(&bars.pv_count) = pdone;
+      }
     }
     if (!ok) break;
-    if (pend_stage >= 0) {
-      if (!(ok = wait_bar(&bars.p_full[x], (pvn & 1), abort_flag))) break;
-      if (!(ok = issue_pending_pv())) break;
+    // the last PVs of the query tile: their completion releases the softmax epilogue
+    while (pdone < g0 + pi) {
+      const int j = pdone;
+      if (!(ok = wait_bar(&bars.pv_done[j & 1], (uint32_t)(j >> 1) & 1u, abort_flag))) break;
+      pdone = j + 1;
+      __threadfence_block();
+      *reinterpret_cast<volatile int*>(&bars.pv_count) = pdone;
     }
-    mma_commit(&bars.q_empty);   // this thread's QKs of the item have been issued; arrives when done
+    if (!ok) break;
+    mma_commit(&bars.q_empty[qb]);   // all QKs of this query tile issued; arrives when they are done
+    g0 += qi;
   }
   // Make sure no MMA of this thread is still writing TMEM when the CTA frees it.
-  mma_commit(&bars.drain[x]);
-  drain_bar(&bars.drain[x], 0);
+  mma_commit(&bars.drain);
+  drain_bar(&bars.drain, 0);
 }
 
 // ------------------------------------------------------------------ softmax + epilogue (warps 2-9)
 
-// Rare path of the online max: multiply the P chunks [0, ch) already written for this
-// tile by alpha (bf16 round trip through TMEM). Kept out of line to spare registers.
-__device__ __noinline__ void rescale_p_chunks(uint32_t tP, int ch, bool u0, bool u1, bool u2, float alpha) {
-  tmem_st_wait();
-  const bool use_pc[3] = {u0, u1, u2};
-#pragma unroll
-  for (int pc = 0; pc < 3; ++pc) {
-    if (pc >= ch || !use_pc[pc]) continue;
-    uint32_t w[16];
-    tmem_ld_x16(tP + pc * 16, w);
-    tmem_ld_wait<16>(w);
-#pragma unroll
-    for (int j = 0; j < 16; ++j)
-      w[j] = pack_bf16x2(__uint_as_float(w[j] << 16) * alpha, __uint_as_float(w[j] & 0xffff0000u) * alpha);
-    tmem_st_x16(tP + pc * 16, w);
+// Visibility of one 32-key chunk (first key token `tok`, membership bits `mask`) for the
+// 32 rows of a warp: `cls` is warp-uniform (0: no row sees a key, 1: every row sees every
+// key, 2: causal diagonal, per-row mask `kp`). `q_warp` is the query token of lane 0.
+__device__ __forceinline__ int chunk_class(const Params& p, int present, int tok, int mask, int sub, int q_warp,
+                                          int lane, uint32_t& kp) {
+  kp = 0u;
+  if (!present || !((mask >> sub) & 1)) return 0;
+  kp = 0xffffffffu;
+  if (!p.causal) return 1;
+  const int lim0 = q_warp - tok;                    // row r sees columns c <= lim0 + r
+  if (lim0 >= 31) return 1;
+  if (lim0 + 31 < 0) {
+    kp = 0u;
+    return 0;
   }
+  const int lim = lim0 + lane;
+  kp = lim >= 31 ? 0xffffffffu : (lim < 0 ? 0u : ((2u << lim) - 1u));
+  return 2;
 }
 
-// One key tile of query tile x for this thread's row, in a single pass over S: per
-// 32-column chunk, the chunk max updates the running max lazily (only when it grows by
-// more than 2^8; then the row sum, the P chunks already written for this tile and,
-// at the end, O are rescaled), p = 2^(s c - m) goes to P_x as bf16. Returns false on abort.
-template <int D>
-__device__ __forceinline__ bool softmax_tile(const Params& p, Bars& bars, const Meta& m, int x, uint32_t tmem,
-                                             uint32_t lane_base, int sub, int qblk, int rloc, float& m_use, float& l,
-                                             int& cnt, int& n_item, volatile int* abort_flag) {
-  using C = Cfg<D>;
-  const int lane = threadIdx.x & 31;
-  const int b = p.block;
-  const float c = p.scale_log2;
+// Max of the visible entries of a 32-column chunk (raw scores; -inf if none). `full` is
+// warp-uniform: every lane of the warp sees the whole chunk.
+__device__ __forceinline__ float chunk_max(const uint32_t* v, uint32_t kp, bool full) {
   const float kNegInf = __int_as_float(0xff800000);
-  const uint32_t tS = tmem + C::col_s(x) + lane_base;
-  const uint32_t tO = tmem + C::col_o(x) + lane_base;
-  const uint32_t tP = tmem + C::col_p(x) + lane_base;
-
-  if (!wait_bar(&bars.s_full[x], cnt & 1, abort_flag)) return false;
-  tc_fence_after();
-  const int nch = (m.nslots * b) >> 5;             // 32-column chunks holding keys
-
-  uint32_t keep[4];
-  bool use[4];
+  float acc[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
+  if (full) {
 #pragma unroll
-  for (int ch = 0; ch < 4; ++ch) {
-    uint32_t kp = 0u;
-    if (ch < nch) {
-      const int slot = (ch * 32) >> p.log2b;
-      // constant-index selects keep the meta fields in registers
-      const int J = slot == 0 ? m.jblk[0] : slot == 1 ? m.jblk[1] : slot == 2 ? m.jblk[2] : m.jblk[3];
-      const int msk = slot == 0 ? m.mask[0] : slot == 1 ? m.mask[1] : slot == 2 ? m.mask[2] : m.mask[3];
-      if ((msk >> sub) & 1) {
-        if (!p.causal || J < qblk) {
-          kp = 0xffffffffu;
-        } else if (J == qblk) {
-          const int lim = rloc - ((ch * 32) & (b - 1));   // visible columns j <= lim
-          kp = lim >= 31 ? 0xffffffffu : (lim < 0 ? 0u : ((2u << lim) - 1u));
-        }
-      }
-    }
-    keep[ch] = kp;
-    use[ch] = __any_sync(0xffffffffu, kp != 0u);   // warp-uniform: this chunk has visible keys
+    for (int j = 0; j < 32; j += 2)
+      acc[(j >> 1) & 3] = max3(acc[(j >> 1) & 3], __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) acc[j & 3] = fmaxf(acc[j & 3], ((kp >> j) & 1u) ? __uint_as_float(v[j]) : kNegInf);
   }
+  return fmaxf(max3(acc[0], acc[1], acc[2]), acc[3]);
+}
 
-  const float m_start = m_use;
-  const uint64_t c2 = f2_pack(c, c);
-  uint64_t rsa[4] = {0ull, 0ull, 0ull, 0ull};     // tile row sum, 4 packed accumulators
-
-  // Software pipeline over 32-column chunks: chunk ch+1 is loaded from TMEM before the
-  // exponentials of chunk ch and its max is taken while they stream through the MUFU.
-  auto chunk_max = [&](const uint32_t* v, uint32_t kp) -> float {
-    float acc[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
-    if (kp == 0xffffffffu) {
+// p = 2^(s c - m) of one chunk into packed bf16 (hidden columns give exactly 0); adds the
+// row sum into rsa. The mask test is hoisted out of the loop (`full` is warp-uniform).
+template <bool FULL>
+__device__ __forceinline__ void chunk_exp_t(const uint32_t* v, uint32_t kp, uint64_t c2, uint64_t negm2, uint32_t* pk,
+                                            uint64_t* rsa) {
+  const float kNegInf = __int_as_float(0xff800000);
 #pragma unroll
-      for (int j = 0; j < 32; j += 2)
-        acc[(j >> 1) & 3] = max3(acc[(j >> 1) & 3], __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) acc[j & 3] = fmaxf(acc[j & 3], ((kp >> j) & 1u) ? __uint_as_float(v[j]) : kNegInf);
+  for (int j = 0; j < 32; j += 2) {
+    float x0, x1;
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), c2, negm2), x0, x1);
+    if (!FULL) {
+      x0 = ((kp >> j) & 1u) ? x0 : kNegInf;
+      x1 = ((kp >> (j + 1)) & 1u) ? x1 : kNegInf;
     }
-    return fmaxf(max3(acc[0], acc[1], acc[2]), acc[3]) * c;   // -inf stays -inf
-  };
-  uint32_t va[32], vb[32];
-  float cm_cur = kNegInf;
-  if (use[0]) {
-    tmem_ld_x32(tS, va);
-    tmem_ld_wait<32>(va);
-    cm_cur = chunk_max(va, keep[0]);
+    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+    rsa[(j >> 1) & 3] = f2_add(rsa[(j >> 1) & 3], f2_pack(p0, p1));
+    pk[j >> 1] = pack_bf16x2(p0, p1);
   }
-#pragma unroll
-  for (int ch = 0; ch < 4; ++ch) {
-    if (ch >= nch) break;
-    uint32_t* vc = (ch & 1) ? vb : va;
-    uint32_t* vn = (ch & 1) ? va : vb;
-    const bool next = ch + 1 < nch && use[ch + 1];
-    if (next) tmem_ld_x32(tS + (ch + 1) * 32, vn);
-    uint32_t pk[16];
-    if (use[ch]) {
-      const uint32_t kp = keep[ch];
-      const float cm = cm_cur;
-      const bool need = cm > m_use + 8.0f;
-      if (__any_sync(0xffffffffu, need)) {
-        // rare: the running max grows; rescale the sums and this tile's P chunks so far
-        float alpha = 1.f;
-        if (need) {
-          alpha = ex2_approx(m_use - cm);          // 0 when m_use = -inf
-          m_use = cm;
-        }
-        l *= alpha;
-        const uint64_t al2 = f2_pack(alpha, alpha);
-#pragma unroll
-        for (int a = 0; a < 4; ++a) {
-          uint64_t r;
-          asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(rsa[a]), "l"(al2));
-          rsa[a] = r;
-        }
-        if (ch > 0) rescale_p_chunks(tP, ch, use[0], use[1], use[2], alpha);
-      }
-      const uint64_t negm2 = f2_pack(-m_use, -m_use);
-#pragma unroll
-      for (int j = 0; j < 32; j += 2) {
-        float x0, x1;
-        f2_unpack(f2_fma(f2_pack(__uint_as_float(vc[j]), __uint_as_float(vc[j + 1])), c2, negm2), x0, x1);
-        if (kp != 0xffffffffu) {                   // hidden columns contribute exactly 0
-          x0 = ((kp >> j) & 1u) ? x0 : kNegInf;
-          x1 = ((kp >> (j + 1)) & 1u) ? x1 : kNegInf;
-        }
-        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-        rsa[(j >> 1) & 3] = f2_add(rsa[(j >> 1) & 3], f2_pack(p0, p1));
-        pk[j >> 1] = pack_bf16x2(p0, p1);
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 16; ++j) pk[j] = 0u;
-    }
-    if (next) {
-      float d0, d1;
-      f2_unpack(rsa[0], d0, d1);
-      tmem_ld_wait_after<32>(vn, d0);              // issued after this chunk's exponentials
-      cm_cur = chunk_max(vn, keep[ch + 1]);
-    } else {
-      cm_cur = kNegInf;
-    }
-    if (ch == 0 && n_item > 0) {
-      // P_x and O_x are free once the previous PV of this query tile has completed
-      const bool ok = wait_bar(&bars.pv_done[x], (cnt - 1) & 1, abort_flag);
-      if (!__all_sync(0xffffffffu, ok)) return false;
-      tc_fence_after();
-    }
-    tmem_st_x16(tP + ch * 16, pk);
-  }
+}
+__device__ __forceinline__ void chunk_exp(const uint32_t* v, uint32_t kp, bool full, uint64_t c2, uint64_t negm2,
+                                          uint32_t* pk, uint64_t* rsa) {
+  if (full) chunk_exp_t<true>(v, kp, c2, negm2, pk, rsa);
+  else chunk_exp_t<false>(v, kp, c2, negm2, pk, rsa);
+}
 
-  // O holds the previous tiles at the old max: rescale once if this tile moved it
-  if (n_item > 0 && __any_sync(0xffffffffu, m_use != m_start)) {
-    const float alpha = (m_use != m_start) ? ex2_approx(m_start - m_use) : 1.f;
-    const uint64_t al2 = f2_pack(alpha, alpha);
-#pragma unroll
-    for (int ch = 0; ch < D / 32; ++ch) {
-      uint32_t ov[32];
+// Rare path of the online max: O *= alpha for this thread's row (O quiescent).
+template <int NC>
+__device__ __noinline__ void rescale_o(uint32_t tO, float alpha) {
+  const uint64_t al2 = f2_pack(alpha, alpha);
+  constexpr int W = NC < 32 ? NC : 32;
+#pragma unroll 1
+  for (int ch = 0; ch < NC / W; ++ch) {
+    uint32_t ov[32];
+    if (W == 32) {
       tmem_ld_x32(tO + ch * 32, ov);
       tmem_ld_wait<32>(ov);
-#pragma unroll
-      for (int j = 0; j < 32; j += 2) {
-        uint64_t r;
-        asm("mul.rn.f32x2 %0, %1, %2;"
-            : "=l"(r)
-            : "l"(f2_pack(__uint_as_float(ov[j]), __uint_as_float(ov[j + 1]))), "l"(al2));
-        float lo, hi;
-        f2_unpack(r, lo, hi);
-        ov[j] = __float_as_uint(lo);
-        ov[j + 1] = __float_as_uint(hi);
-      }
-      tmem_st_x32(tO + ch * 32, ov);
+    } else {
+      tmem_ld_x16(tO, ov);
+      tmem_ld_wait<16>(ov);
     }
+#pragma unroll
+    for (int j = 0; j < W; j += 2) {
+      float lo, hi;
+      f2_unpack(f2_mul(f2_pack(__uint_as_float(ov[j]), __uint_as_float(ov[j + 1])), al2), lo, hi);
+      ov[j] = __float_as_uint(lo);
+      ov[j + 1] = __float_as_uint(hi);
+    }
+    if (W == 32) tmem_st_x32(tO + ch * 32, ov);
+    else tmem_st_x16(tO, ov);
   }
-  const uint64_t rs2 = f2_add(f2_add(rsa[0], rsa[1]), f2_add(rsa[2], rsa[3]));
-  float rs_lo, rs_hi;
-  f2_unpack(rs2, rs_lo, rs_hi);
-  l += rs_lo + rs_hi;
   tmem_st_wait();
-  tc_fence_before();
-  __syncwarp();
-  if (lane == 0) mbar_arrive(&bars.p_full[x]);
-  ++cnt;
-  ++n_item;
-  return true;
 }
 
+// Row-max / row-sum exchange between the two warps that share a TMEM lane quarter.
+struct Exchange {
+  float v[2][2][2][kTile];   // [pipeline][tile parity][chunk][row]
+};
+
+__device__ __forceinline__ void pair_sync(int id) { asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory"); }
+
+// Softmax and epilogue of pipeline x. Warp (quarter q, chunk h) handles rows 32q..32q+31
+// and key columns 32h..32h+31 of every 64-key tile.
+//   d <= 64 (split O): the chunk half has its own running max, row sum and accumulator
+//     O_h, so the two warps of a quarter work independently; their partial results are
+//     merged once per query tile in the epilogue.
+//   d = 128: one O; the pair agrees on each tile's row max through `xc` (named barrier
+//     1 + 4x + q) and each warp rescales its half of the O columns.
 template <int D>
-__device__ void softmax_epilogue(const Params& p, Bars& bars, Meta* meta, uint32_t tmem, volatile int* abort_flag) {
+__device__ void softmax_epilogue(const Params& p, int x, int h, PipeBars& bars, Meta* meta, Exchange& xc,
+                                 uint32_t tmem, volatile int* abort_flag) {
   using C = Cfg<D>;
+  constexpr int DH = D / 2;                          // output columns this warp stores
+  constexpr int RC = C::SPLIT ? D : DH;              // O columns this warp rescales
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int x = (warp - 2) >> 2;                     // warps 2-5: tile A, warps 6-9: tile B
   const int quarter = warp & 3;                      // TMEM lanes this warp may access
   const int row = quarter * 32 + lane;               // query row within the tile
   const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-  const int rows_per_item = kItemRows >> p.log2b;
-  const int sub = (x * kTile + row) >> p.log2b;      // query block within the item
-  const int rloc = row & (p.block - 1);
+  const int sub = row >> p.log2b;                    // query block within the tile (warp-uniform)
+  const int bar_id = 1 + 4 * x + quarter;
   const float kNegInf = __int_as_float(0xff800000);
-  const uint32_t tO = tmem + C::col_o(x) + lane_base;
+  const float c = p.scale_log2;
+  const uint64_t c2 = f2_pack(c, c);
+  // the accumulator columns this warp rescales: all of O_h (split) or its half of O
+  const uint32_t tR = tmem + (C::SPLIT ? C::col_o(x, h) : C::col_o(x, 0) + (uint32_t)(DH * h)) + lane_base;
 
-  int mt = 0, cnt = 0;      // meta position, processed S tiles of this query tile (global)
+  int mt = 0, g = 0;        // meta position, key tiles processed by this pipeline (global)
+  int buf = 0;              // g % NS
+  uint32_t sph = 0;         // (g / NS) & 1
   bool ok = true;
   int item_local = 0;
-  for (int k = blockIdx.x; k < p.n_items && ok; k += gridDim.x, ++item_local) {
+  for (int k = 2 * blockIdx.x + x; k < p.n_items && ok; k += 2 * gridDim.x, ++item_local) {
     const Item it = decode_item(p, k);
-    const int qblk = it.pair * rows_per_item + sub;
+    const int qtok = it.tile * kTile + row;
+    const int q_warp = it.tile * kTile + quarter * 32;
     float m_use = kNegInf;   // running reference max, log2 units
-    float l = 0.f;
+    float l = 0.f;           // row sum over this warp's chunks
     int n_item = 0;
     for (;;) {
       const int ms = mt % kMetaRing;
@@ -709,51 +708,140 @@ __device__ void softmax_epilogue(const Params& p, Bars& bars, Meta* meta, uint32
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.m_empty[ms]);
       ++mt;
-      if (m.kind != kKeyTile) break;
-      if (!(m.active & (1 << x))) continue;
-      if (!(ok = softmax_tile<D>(p, bars, m, x, tmem, lane_base, sub, qblk, rloc, m_use, l, cnt, n_item,
-                                 abort_flag)))
-        break;
+      if (m.kind != kKindTile) break;
+
+      // this warp's chunk of the tile (selects, not an indexed read: keeps Meta in registers)
+      uint32_t kp;
+      const int cls = chunk_class(p, h < m.nch, h ? m.tok[1] : m.tok[0], h ? m.mask[1] : m.mask[0], sub, q_warp,
+                                  lane, kp);
+      const bool u = cls != 0, f = cls == 1;
+      const uint32_t tS = tmem + C::col_s(x, buf) + lane_base;
+      ok = __all_sync(0xffffffffu, wait_bar(&bars.s_full[buf], sph, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+
+      uint32_t va[32];
+      float cm = kNegInf;
+      if (u) {
+        tmem_ld_x32(tS + 32 * h, va);
+        tmem_ld_wait<32>(va);
+        cm = chunk_max(va, kp, f);
+      }
+      float mx = cm * c;                             // -inf stays -inf
+      if (!C::SPLIT) {
+        // tile max of the row over both chunks
+        xc.v[x][g & 1][h][row] = cm;
+        pair_sync(bar_id);
+        mx = fmaxf(cm, xc.v[x][g & 1][h ^ 1][row]) * c;
+      }
+      const bool need = mx > m_use + 8.0f;
+      if (__any_sync(0xffffffffu, need)) {
+        // the running max grows: rescale l and, if earlier tiles contributed, O
+        const float alpha = need ? ex2_approx(m_use - mx) : 1.f;   // 0 when m_use = -inf
+        const bool o_scale = need && m_use != kNegInf;
+        if (n_item > 0 && __any_sync(0xffffffffu, o_scale)) {
+          // O is quiescent once the PV of the previous key tile has completed. S_g exists,
+          // so PV_{g-NS} and every PV before it have completed (QK_g waited for it): the
+          // parity wait on PV_{g-1}'s barrier cannot be two phases off.
+          ok = __all_sync(0xffffffffu, wait_bar(&bars.pv_done[(g - 1) & 1], (uint32_t)((g - 1) >> 1) & 1u, abort_flag));
+          if (!ok) break;
+          tc_fence_after();
+          rescale_o<RC>(tR, alpha);
+        }
+        l *= alpha;
+        if (need) m_use = mx;
+      }
+      uint32_t pk[16];
+      if (u) {
+        const uint64_t negm2 = f2_pack(-m_use, -m_use);
+        uint64_t rsa[4] = {0ull, 0ull, 0ull, 0ull};
+        chunk_exp(va, kp, f, c2, negm2, pk, rsa);
+        const uint64_t rs2 = f2_add(f2_add(rsa[0], rsa[1]), f2_add(rsa[2], rsa[3]));
+        float rs_lo, rs_hi;
+        f2_unpack(rs2, rs_lo, rs_hi);
+        l += rs_lo + rs_hi;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) pk[j] = 0u;
+      }
+      // P of this chunk (bf16 pairs) over the first 16 columns of the chunk's own S
+      // columns 32h..32h+31, which this warp has already read: no other warp's S is touched
+      tmem_st_x16(tS + 32 * h, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.p_full[buf]);
+      ++g;
+      ++n_item;
+      if (++buf == C::NS) {
+        buf = 0;
+        sph ^= 1u;
+      }
     }
     if (!ok) break;
 
-    // epilogue: O / l and LSE of this query tile
+    // epilogue: O / l and LSE of this query tile (this warp: output columns DH*h .. DH*h + DH)
+    float m_fin = m_use, inv = 0.f, a0 = 0.f, a1 = 0.f;
+    float lt;
+    if (C::SPLIT) {
+      xc.v[x][0][h][row] = m_use;
+      xc.v[x][1][h][row] = l;
+      pair_sync(bar_id);
+      const float m0 = xc.v[x][0][0][row], m1 = xc.v[x][0][1][row];
+      const float l0 = xc.v[x][1][0][row], l1 = xc.v[x][1][1][row];
+      pair_sync(bar_id);                             // both read before the next tile reuses xc
+      m_fin = fmaxf(m0, m1);
+      a0 = l0 > 0.f ? ex2_approx(m0 - m_fin) : 0.f;
+      a1 = l1 > 0.f ? ex2_approx(m1 - m_fin) : 0.f;
+      lt = l0 * a0 + l1 * a1;
+    } else {
+      xc.v[x][g & 1][h][row] = l;
+      pair_sync(bar_id);
+      lt = l + xc.v[x][g & 1][h ^ 1][row];
+    }
     if (n_item > 0) {
-      ok = wait_bar(&bars.pv_done[x], (cnt - 1) & 1, abort_flag);
-      ok = __all_sync(0xffffffffu, ok);
+      ok = __all_sync(0xffffffffu, wait_count(&bars.pv_count, g, abort_flag));
       if (!ok) break;
       tc_fence_after();
     }
-    const int qtok = it.pair * kItemRows + x * kTile + row;
     const bool store = qtok < p.n_tokens;
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    __nv_bfloat16* orow = p.o + (int64_t)it.s * p.o_sb + (int64_t)qtok * p.o_sn + (int64_t)it.h * p.o_sh;
+    inv = lt > 0.f ? 1.f / lt : 0.f;
+    __nv_bfloat16* orow =
+        p.o + (int64_t)it.s * p.o_sb + (int64_t)qtok * p.o_sn + (int64_t)it.h * p.o_sh + DH * h;
+#pragma unroll 1
+    for (int ch = 0; ch < DH / 16; ++ch) {            // 16 output columns at a time
+      uint32_t ov[16];
 #pragma unroll
-    for (int ch = 0; ch < D / 32; ++ch) {
-      uint32_t ov[32];
+      for (int j = 0; j < 16; ++j) ov[j] = 0u;
       if (n_item > 0) {
-        tmem_ld_x32(tO + ch * 32, ov);
-        tmem_ld_wait<32>(ov);
-      } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) ov[j] = 0u;
+        for (int part = 0; part < C::NO; ++part) {
+          // split: weight each part by its max correction (a part with no visible key,
+          // whose accumulator may never have been written, contributes nothing)
+          const float wt = C::SPLIT ? (part ? a1 : a0) : 1.f;
+          uint32_t w[16];
+          tmem_ld_x16(tmem + C::col_o(x, part) + (uint32_t)(DH * h + ch * 16) + lane_base, w);
+          tmem_ld_wait<16>(w);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            ov[j] = __float_as_uint(__uint_as_float(ov[j]) + (wt != 0.f ? __uint_as_float(w[j]) * wt : 0.f));
+        }
       }
-      uint32_t pk[16];
-#pragma unroll
-      for (int j = 0; j < 32; j += 2)
-        pk[j >> 1] = pack_bf16x2(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv);
       if (store) {
-        uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+        uint32_t pk[8];
 #pragma unroll
-        for (int v4 = 0; v4 < 4; ++v4)
-          dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+        for (int j = 0; j < 16; j += 2)
+          pk[j >> 1] = pack_bf16x2(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv);
+        uint4* dst = reinterpret_cast<uint4*>(orow + ch * 16);
+        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
       }
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&bars.o_empty[x]);
-    if (store) {
-      const float lse = l > 0.f ? (m_use + __log2f(l)) * 0.69314718055994531f : kNegInf;
+    if (lane == 0) mbar_arrive(&bars.o_empty);
+    if (store && h == 0) {
+      const float lse = lt > 0.f ? (m_fin + __log2f(lt)) * 0.69314718055994531f : kNegInf;
       p.lse[((int64_t)it.s * p.heads + it.h) * p.n_tokens + qtok] = lse;
     }
   }
@@ -767,35 +855,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tv, const Params p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sQ = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sK = sQ + 2 * C::TILE_BYTES;
-  uint8_t* sV = sK + C::STAGES * C::TILE_BYTES;
-  UnionSmem& un = *reinterpret_cast<UnionSmem*>(sV + C::STAGES * C::TILE_BYTES);
-  __shared__ Bars bars;
-  __shared__ Meta meta[kMetaRing];
+  uint8_t* sbase = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ PipeBars bars[2];
+  __shared__ Meta meta[2][kMetaRing];
+  __shared__ Exchange xchg;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
-    mbar_init(&bars.q_full, 1);
-    mbar_init(&bars.q_empty, 2);              // both MMA threads
-    for (int i = 0; i < 4; ++i) {
-      mbar_init(&bars.k_full[i], 1);
-      mbar_init(&bars.k_empty[i], 2);
-      mbar_init(&bars.v_full[i], 1);
-      mbar_init(&bars.v_empty[i], 2);
-    }
-    for (int i = 0; i < kMetaRing; ++i) {
-      mbar_init(&bars.m_full[i], 1);
-      mbar_init(&bars.m_empty[i], kMetaConsumers);
-    }
     for (int x = 0; x < 2; ++x) {
-      mbar_init(&bars.s_full[x], 1);
-      mbar_init(&bars.p_full[x], 4);
-      mbar_init(&bars.pv_done[x], 1);
-      mbar_init(&bars.o_empty[x], 4);
-      mbar_init(&bars.drain[x], 1);
+      PipeBars& b = bars[x];
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&b.q_full[i], 1);
+        mbar_init(&b.q_empty[i], 1);
+      }
+      for (int i = 0; i < C::STAGES; ++i) {
+        mbar_init(&b.k_full[i], 1);
+        mbar_init(&b.k_empty[i], 1);
+        mbar_init(&b.v_full[i], 1);
+        mbar_init(&b.v_empty[i], 1);
+      }
+      for (int i = 0; i < kMetaRing; ++i) {
+        mbar_init(&b.m_full[i], 1);
+        mbar_init(&b.m_empty[i], kMetaConsumers);
+      }
+      for (int i = 0; i < C::NS; ++i) {
+        mbar_init(&b.s_full[i], 1);
+        mbar_init(&b.p_full[i], kSoftmaxWarps);
+      }
+      mbar_init(&b.pv_done[0], 1);
+      mbar_init(&b.pv_done[1], 1);
+      mbar_init(&b.o_empty, kSoftmaxWarps);
+      mbar_init(&b.drain, 1);
+      b.pv_count = 0;
     }
     abort_flag = 0;
     fence_mbar_init();
@@ -812,13 +905,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
-  if (warp == 0) {
-    producer<D>(p, &tq, &tk, &tv, bars, meta, un, sQ, sK, sV, &abort_flag);
-  } else if (warp == 1 || warp == 10) {
-    if ((threadIdx.x & 31) == 0) mma_issuer<D>(p, bars, meta, sQ, sK, sV, tmem, warp == 1 ? 0 : 1, &abort_flag);
+  // pipeline 0: warps 0 (producer), 1 (MMA), 2-9 (softmax); pipeline 1: warps 19, 18, 10-17
+  const int x = (warp <= 9) ? 0 : 1;
+  uint8_t* sQ = sbase + x * C::PIPE_BYTES;
+  uint8_t* sK = sQ + C::QB * C::Q_BYTES;
+  uint8_t* sV = sK + C::STAGES * C::KV_BYTES;
+  UnionSmem& un = *reinterpret_cast<UnionSmem*>(sV + C::STAGES * C::KV_BYTES);
+
+  if (warp == 0 || warp == 19) {
+    producer<D>(p, x, &tq, &tk, &tv, bars[x], meta[x], un, sQ, sK, sV, &abort_flag);
+  } else if (warp == 1 || warp == 18) {
+    if ((threadIdx.x & 31) == 0) mma_issuer<D>(p, x, bars[x], meta[x], sQ, sK, sV, tmem, &abort_flag);
     __syncwarp();
   } else {
-    softmax_epilogue<D>(p, bars, meta, tmem, &abort_flag);
+    // softmax warps 2 + 8x .. 9 + 8x: chunk h = 0 for the first four, 1 for the others
+    const int h = ((warp - 2 - 8 * x) >> 2) & 1;
+    softmax_epilogue<D>(p, x, h, bars[x], meta[x], xchg, tmem, &abort_flag);
   }
 
   tc_fence_before();
@@ -833,12 +935,13 @@ template <int D>
 int launch_d(const AttnArgs& a, cudaStream_t stream) {
   using C = Cfg<D>;
   CUtensorMap tq, tk, tv;
+  const uint32_t kv_rows = a.block == 32 ? 32u : 64u;
   if (!encode_bhnd_map(&tq, a.q, a.batch, a.n_tokens, a.heads, D, a.q_strides[0], a.q_strides[1], a.q_strides[2],
                        C::CH, kTile, C::TMA_SWZ) ||
       !encode_bhnd_map(&tk, a.k, a.batch, a.n_tokens, a.kv_heads, D, a.kv_strides[0], a.kv_strides[1],
-                       a.kv_strides[2], C::CH, (uint32_t)a.block, C::TMA_SWZ) ||
+                       a.kv_strides[2], C::CH, kv_rows, C::TMA_SWZ) ||
       !encode_bhnd_map(&tv, a.v, a.batch, a.n_tokens, a.kv_heads, D, a.kv_strides[0], a.kv_strides[1],
-                       a.kv_strides[2], C::CH, (uint32_t)a.block, C::TMA_SWZ))
+                       a.kv_strides[2], C::CH, kv_rows, C::TMA_SWZ))
     return SA_ERR_UNSUPPORTED;
   Params p;
   p.batch = a.batch;
@@ -850,8 +953,8 @@ int launch_d(const AttnArgs& a, cudaStream_t stream) {
   p.nb = a.n_tokens / a.block;
   p.causal = a.causal;
   p.csr_shared = a.csr_shared;
-  p.pairs_per_seq = (a.n_tokens + kItemRows - 1) / kItemRows;
-  p.n_items = a.batch * a.heads * p.pairs_per_seq;
+  p.tiles_per_seq = (a.n_tokens + kTile - 1) / kTile;
+  p.n_items = a.batch * a.heads * p.tiles_per_seq;
   p.row_ptr = a.row_ptr;
   p.col_idx = a.col_idx;
   p.o = static_cast<__nv_bfloat16*>(a.o);
@@ -870,7 +973,8 @@ int launch_d(const AttnArgs& a, cudaStream_t stream) {
   auto kern = attn_fwd_kernel<D>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return SA_ERR_CUDA;
-  const int grid = p.n_items < sm_count ? p.n_items : sm_count;
+  const int want = (p.n_items + 1) / 2;
+  const int grid = want < sm_count ? want : sm_count;
   kern<<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
