@@ -23,9 +23,10 @@ compression-guided workload (top-64).
 ``--impl reference`` times the CPU oracle (the reference arm of this build) on the
 same workload, each step a bounded sample of query blocks.
 
-Multi-GPU (torchrun): each rank runs its own replica of the workload (weak scaling, no
-collective on the data path); the timed region is bracketed by barriers and the
-maximum over ranks is reported.
+Multi-GPU (torchrun): rank r processes its own shard of a global batch (sequences
+r*B .. r*B+B-1 of the byte stream, its own Q/K/V draw; weak scaling, no collective on
+the data path); the timed region is bracketed by barriers and the maximum over ranks
+is reported.
 """
 from __future__ import annotations
 
@@ -48,6 +49,37 @@ WORKLOAD = "bytelm_topk_8k"
 METRIC = "effective TFLOP/s over mask edges & tokens/s at N=8K; % of BF16 tensor peak"
 UNIT = "TFLOP/s"
 L2_FLUSH_BYTES = 256 << 20
+
+
+# ------------------------------------------------------------------ ranks
+
+def rank_info() -> tuple[int, int, int]:
+    """(rank, world size, local rank) from the torchrun environment (1 process: 0, 1, 0)."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def shard_sequences(rank: int, batch: int) -> range:
+    """Global sequence indices of a rank's shard (weak scaling: `batch` per rank)."""
+    return range(rank * batch, (rank + 1) * batch)
+
+
+def make_max_over_ranks(dist, device):
+    """A float -> float reduction to the maximum over the ranks of the default process
+    group (identity without one)."""
+    def max_over_ranks(x: float) -> float:
+        if dist is None:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+    return max_over_ranks
+
+
+def aggregate_rate(world: int, work_per_rank: float, max_seconds: float) -> float:
+    """Whole-job rate: the work of every rank over the slowest rank's time."""
+    return world * work_per_rank / max_seconds
 
 
 def _peaks() -> dict:
@@ -156,7 +188,7 @@ def _csr_edges(rp, ci, block, causal, heads) -> int:
 class BlockSparseCase:
     """Ratios -> CSR -> attention for one compression-guided / BigBird workload."""
 
-    def __init__(self, name: str, dev, **over):
+    def __init__(self, name: str, dev, shard: int = 0, **over):
         import numpy as np
         import torch
 
@@ -168,7 +200,7 @@ class BlockSparseCase:
         b, n, bt = cfg["block"], cfg["n_tokens"], cfg["batch"]
         self.block, self.causal = b, cfg.get("causal", 1)
         if cfg["kind"] == "topk":
-            self.bytes_host = byte_stream(cfg)
+            self.bytes_host = byte_stream(cfg, seq_offset=shard_sequences(shard, bt).start)
             ratios = sa.sa_block_ratios(self.bytes_host, b)
             self.params = sa.mask_params("topk", b, n, bt, 1, cfg["window_blocks"], cfg["global_blocks"], cfg["topk"])
             self.csr_shared = False
@@ -185,7 +217,7 @@ class BlockSparseCase:
             self.csr_shared = True
         self.ratios_host = ratios
         self.ratios = None if ratios is None else torch.from_numpy(ratios).to(dev)
-        qb, kb, vb = qkv_bits(cfg)
+        qb, kb, vb = qkv_bits(cfg, seed_offset=1000 * shard)
         self.qkv_host = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16) for x in (qb, kb, vb)]
         self.q, self.k, self.v = (t.to(dev) for t in self.qkv_host)
         cap = sa.sa_mask_nnz_bound(self.params)
@@ -341,13 +373,12 @@ def _config_dict(cfg, flush_note: str, world: int) -> dict:
     return {"workload": cfg["name"], "batch": cfg["batch"], "n_tokens": cfg["n_tokens"], "block": cfg["block"],
             "heads": cfg["heads"], "head_dim": cfg["head_dim"], "window_blocks": cfg["window_blocks"],
             "global_blocks": cfg["global_blocks"], "topk": cfg["topk"], "ratio": "zlib level 6 per block",
-            "l2": flush_note, "parallelism": f"replicas x{world} (batch-sharded, no collective)"}
+            "l2": flush_note, "parallelism": f"dp{world}: batch shards of {cfg['batch']} sequences per rank, no collective"}
 
 
 def run_reference(args):
     """The reference arm: the CPU oracle, as it stands, on sampled query blocks."""
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank, world, _ = rank_info()
     if rank != 0:
         return
     from workloads import workload
@@ -383,9 +414,7 @@ def run_ours(args):
 
     import content_adaptive_sparse_gb300 as sa
 
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    rank, world, local = rank_info()
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -405,12 +434,7 @@ def run_ours(args):
         if dist is not None:
             dist.barrier()
 
-    def max_over_ranks(x: float) -> float:
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    max_over_ranks = make_max_over_ranks(dist, dev)
 
     if args.only_row:
         rows = _measure_rows(torch, sa, dev, flush, peaks, max_over_ranks, only=args.only_row,
@@ -419,7 +443,7 @@ def run_ours(args):
             print(json.dumps({"only_row": args.only_row, "rows": rows}), flush=True)
         return
 
-    case = BlockSparseCase(WORKLOAD, dev)
+    case = BlockSparseCase(WORKLOAD, dev, shard=rank)
     cfg = case.cfg
 
     # ---------------- main timed region
@@ -439,7 +463,7 @@ def run_ours(args):
     step_ms = max_over_ranks(step_ms)
     attn_ms = max_over_ranks(seg[1])
     mask_ms = max_over_ranks(seg[0])
-    value = world * case.flops / (step_ms * 1e-3) / 1e12
+    value = aggregate_rate(world, case.flops, step_ms * 1e-3) / 1e12
     attn_tflops = case.flops / (attn_ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
     assert sa.sa_device_status() == 0
@@ -471,7 +495,7 @@ def run_ours(args):
     for _ in range(e2e_steps):
         e2e_step()
     te = max_over_ranks((time.perf_counter() - te0) / e2e_steps)
-    e2e_value = world * case.flops / te / 1e12
+    e2e_value = aggregate_rate(world, case.flops, te) / 1e12
 
     # ---------------- other hot-path rows (kernel time only)
     rows = {}
@@ -493,7 +517,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": _config_dict(cfg, "flushed between timed steps (256 MB write, outside events)", world),
-        "tokens_per_s": world * case.tokens / (step_ms * 1e-3),
+        "tokens_per_s": aggregate_rate(world, case.tokens, step_ms * 1e-3),
         "pct_bf16_peak": 100.0 * value / world / peak,
         "edges_per_step": case.edges,
         "segments_ms": {"sa_build_mask": mask_ms, "sa_attn_fwd": attn_ms},

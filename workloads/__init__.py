@@ -139,10 +139,13 @@ def bytes_zipf_text(seed: int, n: int, p_text: float = 0.6, zipf_s: float = 1.1)
     return out
 
 
-def byte_stream(cfg: dict) -> np.ndarray:
-    """``uint8[batch, n_tokens]`` byte tokens for a compression-guided workload."""
+def byte_stream(cfg: dict, seq_offset: int = 0) -> np.ndarray:
+    """``uint8[batch, n_tokens]`` byte tokens for a compression-guided workload.
+
+    Sequence ``b`` of the result is global sequence ``seq_offset + b``: shards of a larger
+    global batch (one per rank) are generated independently and agree with the whole."""
     gen = {"phrase_random": bytes_phrase_random, "zipf_text": bytes_zipf_text}[cfg["bytes"]]
-    rows = [gen(cfg["seed"] * 1000 + b, cfg["n_tokens"]) for b in range(cfg["batch"])]
+    rows = [gen(cfg["seed"] * 1000 + seq_offset + b, cfg["n_tokens"]) for b in range(cfg["batch"])]
     return np.stack(rows)
 
 
