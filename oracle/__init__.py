@@ -27,15 +27,16 @@ from .ratios import block_ratios, zlib_version
 from .philox import philox4x64_10, philox_word
 from .masks import (MaskParams, build_csr, csr_topk_rows, csr_bigbird_rows, csr_full_rows,
                     csr_literal_mean_rows, csr_to_block_mask, block_mask_to_token_mask,
-                    literal_flags, topk_row_count)
+                    literal_flags, topk_row_count, cas_head_components, LOCAL, LITERAL)
 from .fib import fib_rungs, fib_rungs_upto, alpha_schedule, fib_offsets, offset_key_set
-from .attention import (attention_csr, attention_csr_block, attention_offsets, dense_masked_attention,
-                        attention_rows_csr)
+from .attention import (attention_csr, attention_csr_block, attention_csr_heads, attention_offsets,
+                        dense_masked_attention, attention_rows_csr)
 
 __all__ = [
     "block_ratios", "zlib_version", "philox4x64_10", "philox_word", "MaskParams", "build_csr",
     "csr_topk_rows", "csr_bigbird_rows", "csr_full_rows", "csr_literal_mean_rows",
     "csr_to_block_mask", "block_mask_to_token_mask", "literal_flags", "topk_row_count",
+    "cas_head_components", "LOCAL", "LITERAL", "attention_csr_heads",
     "fib_rungs", "fib_rungs_upto", "alpha_schedule", "fib_offsets", "offset_key_set", "attention_csr",
     "attention_csr_block",
     "attention_offsets", "dense_masked_attention", "attention_rows_csr",

@@ -73,6 +73,24 @@ def attention_csr(q, k, v, row_ptr, col_idx, block: int, causal: int, scale: flo
     return o, lse
 
 
+def attention_csr_heads(q, k, v, csrs, head_mask, block: int, causal: int, scale: float | None = None):
+    """Block-CSR attention where query head h uses CSR ``csrs[head_mask[h]]`` (a list of
+    (row_ptr, col_idx) pairs), as in [CAS] Appendix B "Head-specific mask distribution"
+    (head groups with different parts of the block mask)."""
+    bt, n, h, d = q.shape
+    nb = n // block
+    o = np.zeros((bt, n, h, d), dtype=np.float64)
+    lse = np.full((bt, h, n), -np.inf, dtype=np.float64)
+    for s in range(bt):
+        for I in range(nb):
+            for hh in range(h):
+                row_ptr, col_idx = csrs[head_mask[hh]]
+                ob, lb = attention_csr_block(q, k, v, row_ptr, col_idx, block, causal, s, I, hh, scale)
+                o[s, I * block:(I + 1) * block, hh, :] = ob
+                lse[s, hh, I * block:(I + 1) * block] = lb
+    return o, lse
+
+
 def attention_rows_csr(q, k, v, row_ptr, col_idx, block: int, causal: int, samples,
                        scale: float | None = None, convert=None):
     """The same definition evaluated only at sampled (batch, token, head) triples.

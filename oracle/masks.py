@@ -22,7 +22,9 @@ Modes
   under causality.
 * ``literal_mean``  [CAS] section 3.1 Eq. 2 and section 3.2 Eq. 3 / Algorithm 1:
   l_i = [r_i > mean(r)], M = M_lit u M_local u I with M_lit(i,j) = l_i l_j [|i-j| > w]
-  and M_local(i,j) = [|i-j| <= w]; causal keeps J <= I.
+  and M_local(i,j) = [|i-j| <= w]; causal keeps J <= I. ``components`` selects the
+  parts [CAS] Appendix B "Head-specific mask distribution" hands to head groups:
+  LOCAL (M_local u I), LITERAL (M_lit u I) or both (the full M; 0 means both).
 * ``bigbird``  [BB] section 2: window of w_b consecutive blocks placed as
   [I - w_b//2, I - w_b//2 + w_b - 1] (reading: an even window cannot be centred, this
   placement gives exactly w tokens), g global blocks (global rows attend to every
@@ -54,6 +56,8 @@ class MaskParams:
     topk: int = 0
     random_blocks: int = 0
     seed: int = 0
+    components: int = 0       # literal_mean only: LOCAL | LITERAL, 0 = both
+
 
     @property
     def nb(self) -> int:
@@ -85,6 +89,8 @@ def topk_row_count(I: int, w: int, g: int, k: int) -> int:
 
 # ---------------------------------------------------------------- literal_mean
 
+LOCAL, LITERAL = 1, 2          # components of the [CAS] block mask besides the identity
+
 def literal_flags(ratios) -> list[bool]:
     """[CAS] Eq. 2: l_i = 1 iff r_i > mean(r) (mean over all B blocks)."""
     r = [float(x) for x in ratios]
@@ -92,18 +98,19 @@ def literal_flags(ratios) -> list[bool]:
     return [x > mean for x in r]
 
 
-def csr_literal_mean_rows(ratios, w: int, causal: int) -> list[list[int]]:
+def csr_literal_mean_rows(ratios, w: int, causal: int, components: int = 0) -> list[list[int]]:
     nb = len(ratios)
     lit = literal_flags(ratios)
+    comp = components or (LOCAL | LITERAL)
     rows = []
     for I in range(nb):
         row = []
         for J in range(nb):
             if causal and J > I:
                 continue
-            local = abs(I - J) <= w
+            local = bool(comp & LOCAL) and abs(I - J) <= w
             ident = I == J
-            literal = lit[I] and lit[J] and abs(I - J) > w
+            literal = bool(comp & LITERAL) and lit[I] and lit[J] and abs(I - J) > w
             if local or ident or literal:
                 row.append(J)
         rows.append(row)
@@ -150,7 +157,7 @@ def _rows_for(p: MaskParams, ratios_row):
             raise ValueError("topk mode is causal only")
         return csr_topk_rows(ratios_row, p.window_blocks, p.global_blocks, p.topk)
     if p.mode == "literal_mean":
-        return csr_literal_mean_rows(ratios_row, p.window_blocks, p.causal)
+        return csr_literal_mean_rows(ratios_row, p.window_blocks, p.causal, p.components)
     if p.mode == "bigbird":
         if p.causal:
             raise ValueError("bigbird mode is bidirectional only")
@@ -196,3 +203,16 @@ def block_mask_to_token_mask(block_mask: np.ndarray, block: int, causal: int) ->
         n = tok.shape[0]
         tok &= np.tril(np.ones((n, n), dtype=bool))
     return tok
+
+
+# ---------------------------------------------------------------- head groups
+
+def cas_head_components(heads: int) -> list[int]:
+    """[CAS] Appendix B "Head-specific mask distribution": of 12 heads, heads 0-5 get
+    the local part, heads 6-8 the literal (long-range) part and heads 9-11 the full
+    mask. Reading for other head counts: the same proportions, first half local, next
+    quarter literal, the rest full (12 heads give exactly the page's split)."""
+    n_local = heads // 2
+    n_lit = heads // 4
+    return [LOCAL if h < n_local else LITERAL if h < n_local + n_lit else LOCAL | LITERAL
+            for h in range(heads)]

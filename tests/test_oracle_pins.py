@@ -358,3 +358,98 @@ def test_empty_row_gives_zero_and_minus_inf():
     ci = np.array([0, 2, 3], dtype=np.int32)
     o, lse = oracle.attention_csr(q, k, v, rp, ci, b, 1)
     assert np.all(o[:, 8:16] == 0) and np.all(np.isneginf(lse[:, :, 8:16]))
+
+
+# ------------------------------------------------------------------ head groups ([CAS] App. B)
+
+def _algorithm1_parts(ratios, w):
+    """Algorithm 1's three block-mask components as separate numpy outer products."""
+    B = len(ratios)
+    r = np.asarray(ratios, dtype=np.float64)
+    lit = r > r.mean()
+    i = np.arange(B)[:, None]
+    j = np.arange(B)[None, :]
+    eye = np.eye(B, dtype=bool)
+    local = np.abs(i - j) <= w
+    literal = lit[:, None] & lit[None, :] & (np.abs(i - j) > w)
+    return eye, local, literal
+
+
+@pytest.mark.parametrize("seed,causal,w", [(0, 1, 1), (1, 0, 2), (2, 1, 0)])
+def test_literal_mean_components_match_algorithm1_parts(seed, causal, w):
+    """LOCAL = M_local u I, LITERAL = M_lit u I, both = M, each intersected with the
+    causal triangle at token level ([CAS] Appendix B, Algorithm 1 step 3 and the head
+    distribution paragraph)."""
+    data = bytes_zipf_text(seed, 2048)
+    b = 64
+    r = oracle.block_ratios(data, b)
+    eye, local, literal = _algorithm1_parts(r, w)
+    want = {oracle.LOCAL: eye | local, oracle.LITERAL: eye | literal, 0: eye | local | literal}
+    for comp, M in want.items():
+        p = om.MaskParams("literal_mean", b, 2048, causal, w, components=comp)
+        rp, ci = om.build_csr(p, r[None, :], 1)
+        tok = om.block_mask_to_token_mask(om.csr_to_block_mask(rp, ci, p.nb), b, causal)
+        ref = np.kron(M, np.ones((b, b), dtype=bool))
+        if causal:
+            ref &= ~np.triu(np.ones_like(ref), 1)
+        assert (tok == ref).all()
+
+
+def test_literal_mean_components_partition_rows():
+    """Every row of the full mask is the union of its LOCAL and LITERAL rows, and the two
+    share only the diagonal block (local edges have |I-J| <= w, literal ones > w)."""
+    rng = np.random.default_rng(5)
+    for trial in range(6):
+        nb = int(rng.integers(4, 40))
+        ratios = rng.choice([0.5, 0.75, 1.0, 1.25], size=nb)
+        w = int(rng.integers(0, 4))
+        causal = trial % 2
+        full = om.csr_literal_mean_rows(ratios, w, causal, 0)
+        loc = om.csr_literal_mean_rows(ratios, w, causal, oracle.LOCAL)
+        lit = om.csr_literal_mean_rows(ratios, w, causal, oracle.LITERAL)
+        for I in range(nb):
+            assert set(full[I]) == set(loc[I]) | set(lit[I])
+            assert set(loc[I]) & set(lit[I]) == {I}
+
+
+def test_local_component_is_topk_band_without_literals():
+    """Causal LOCAL (|I-J| <= w, J <= I) is the TOPK mode's window of w+1 blocks with no
+    globals and k = 0; the ratios must not matter."""
+    rng = np.random.default_rng(9)
+    for w in range(0, 5):
+        nb = 37
+        ratios = rng.random(nb)
+        loc = om.csr_literal_mean_rows(ratios, w, 1, oracle.LOCAL)
+        assert loc == om.csr_topk_rows(ratios, w + 1, 0, 0)
+
+
+def test_literal_component_uniform_ratios_is_identity():
+    """Equal ratios: no block exceeds the mean, so LITERAL leaves only the diagonal."""
+    rows = om.csr_literal_mean_rows([0.7] * 20, 2, 0, oracle.LITERAL)
+    assert rows == [[I] for I in range(20)]
+
+
+def test_cas_head_groups_page_split():
+    """12 heads: 0-5 local, 6-8 long-range (literal), 9-11 hybrid (full M)."""
+    comp = oracle.cas_head_components(12)
+    assert comp == [oracle.LOCAL] * 6 + [oracle.LITERAL] * 3 + [oracle.LOCAL | oracle.LITERAL] * 3
+
+
+def test_attention_heads_reduces_to_single_csr_per_head():
+    """Per-head CSR attention equals, head by head, the dense masked route with that
+    head's token mask."""
+    rng = np.random.default_rng(3)
+    bt, n, h, d, b, w = 1, 256, 4, 16, 32, 1
+    q, k, v = (rng.standard_normal((bt, n, h, d)) for _ in range(3))
+    ratios = rng.choice([0.5, 1.0, 1.5], size=(1, n // b))
+    csrs = []
+    for comp in (oracle.LOCAL, oracle.LITERAL, 0):
+        csrs.append(om.build_csr(om.MaskParams("literal_mean", b, n, 1, w, components=comp), ratios, 1))
+    head_mask = [0, 1, 2, 1]
+    o, lse = oracle.attention_csr_heads(q, k, v, csrs, head_mask, b, 1)
+    for hh in range(h):
+        rp, ci = csrs[head_mask[hh]]
+        tok = om.block_mask_to_token_mask(om.csr_to_block_mask(rp, ci, n // b), b, 1)
+        od, ld = oracle.dense_masked_attention(q[:, :, hh:hh + 1], k[:, :, hh:hh + 1], v[:, :, hh:hh + 1], tok)
+        assert np.abs(o[:, :, hh] - od[:, :, 0]).max() < 1e-12
+        assert np.abs(lse[:, hh] - ld[:, 0]).max() < 1e-12
