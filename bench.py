@@ -17,8 +17,9 @@ of the byte stream, pinned host -> device copies of ratios and Q/K/V, mask build
 attention, device -> host copies of O and LSE, all inside the timed region.
 
 ``rows`` times the other hot-path rows once each (kernel time, CUDA events): BigBird
-at N=16384, the 16-layer Fibonacci-offset pass at N=8192 (HBM roofline) and the 64K
-compression-guided workload (top-64).
+at N=16384, the 16-layer Fibonacci-offset pass at N=8192 (HBM roofline), the 64K
+compression-guided workload (top-64) and the mean-threshold mask split over local,
+long-range and hybrid head groups at N=8192.
 
 ``--impl reference`` times the CPU oracle (the reference arm of this build) on the
 same workload, each step a bounded sample of query blocks.
@@ -199,10 +200,21 @@ class BlockSparseCase:
         self.dev = dev
         b, n, bt = cfg["block"], cfg["n_tokens"], cfg["batch"]
         self.block, self.causal = b, cfg.get("causal", 1)
+        self.head_mask = None
         if cfg["kind"] == "topk":
             self.bytes_host = byte_stream(cfg, seq_offset=shard_sequences(shard, bt).start)
             ratios = sa.sa_block_ratios(self.bytes_host, b)
             self.params = sa.mask_params("topk", b, n, bt, 1, cfg["window_blocks"], cfg["global_blocks"], cfg["topk"])
+            self.csr_shared = False
+        elif cfg["kind"] == "literal_heads":
+            # one mean-threshold CSR per mask part; each head reads the part of its group
+            self.bytes_host = byte_stream(cfg, seq_offset=shard_sequences(shard, bt).start)
+            ratios = sa.sa_block_ratios(self.bytes_host, b, cfg["zlib_level"])
+            parts = sorted(set(cfg["head_components"]))
+            self.params_list = [sa.mask_params("literal_mean", b, n, bt, cfg["causal"], cfg["window_blocks"],
+                                               components=c) for c in parts]
+            self.head_mask = [parts.index(c) for c in cfg["head_components"]]
+            self.params = self.params_list[0]
             self.csr_shared = False
         elif cfg["kind"] == "bigbird":
             self.bytes_host = None
@@ -215,30 +227,42 @@ class BlockSparseCase:
             ratios = None
             self.params = sa.mask_params("full", b, n, 1, cfg["causal"])
             self.csr_shared = True
+        if self.head_mask is None:
+            self.params_list = [self.params]
         self.ratios_host = ratios
         self.ratios = None if ratios is None else torch.from_numpy(ratios).to(dev)
         qb, kb, vb = qkv_bits(cfg, seed_offset=1000 * shard)
         self.qkv_host = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16) for x in (qb, kb, vb)]
         self.q, self.k, self.v = (t.to(dev) for t in self.qkv_host)
-        cap = sa.sa_mask_nnz_bound(self.params)
-        self.row_ptr = torch.empty((self.params.batch, n // b + 1), dtype=torch.int32, device=dev)
-        self.col_idx = torch.empty((cap,), dtype=torch.int32, device=dev)
+        self.csrs = []
+        for prm in self.params_list:
+            cap = sa.sa_mask_nnz_bound(prm)
+            self.csrs.append((torch.empty((prm.batch, n // b + 1), dtype=torch.int32, device=dev),
+                              torch.empty((cap,), dtype=torch.int32, device=dev)))
+        self.row_ptr, self.col_idx = self.csrs[0]
         self.o = torch.empty_like(self.q)
         self.lse = torch.empty((bt, cfg["heads"], n), dtype=torch.float32, device=dev)
         self.step()
         torch.cuda.synchronize()
-        rp, ci = self.row_ptr.cpu().numpy(), self.col_idx.cpu().numpy()
-        per_csr = _csr_edges(rp, ci, b, self.causal, cfg["heads"])
+        heads_of = ([cfg["heads"]] if self.head_mask is None else
+                    [self.head_mask.count(m) for m in range(len(self.csrs))])
+        per_csr = sum(_csr_edges(rp.cpu().numpy(), ci.cpu().numpy(), b, self.causal, nh)
+                      for (rp, ci), nh in zip(self.csrs, heads_of))
         self.edges = per_csr * (bt if self.csr_shared else 1)
         self.flops = 4 * self.edges * cfg["head_dim"]
         self.tokens = bt * n
 
     def build(self):
-        self.sa.sa_build_mask(self.params, self.ratios, self.row_ptr, self.col_idx)
+        for prm, (rp, ci) in zip(self.params_list, self.csrs):
+            self.sa.sa_build_mask(prm, self.ratios, rp, ci)
 
     def attend(self):
-        self.sa.sa_attn_fwd(self.q, self.k, self.v, self.row_ptr, self.col_idx, self.block, self.causal, self.o,
-                            self.lse, self.csr_shared)
+        if self.head_mask is None:
+            self.sa.sa_attn_fwd(self.q, self.k, self.v, self.row_ptr, self.col_idx, self.block, self.causal, self.o,
+                                self.lse, self.csr_shared)
+        else:
+            self.sa.sa_attn_fwd_heads(self.q, self.k, self.v, self.csrs, self.head_mask, self.block, self.causal,
+                                      self.o, self.lse, self.csr_shared)
 
     def step(self):
         self.build()
@@ -549,6 +573,8 @@ def _measure_rows(torch, sa, dev, flush, peaks, max_over_ranks, only=None, steps
         rows.update(_row_bigbird(torch, dev, flush, peaks, max_over_ranks, steps, warm))
     if want("long_topk_64k"):
         rows.update(_row_long(torch, dev, flush, peaks, max_over_ranks, steps, warm))
+    if want("cas_heads_8k"):
+        rows.update(_row_block_sparse(torch, dev, flush, peaks, max_over_ranks, steps, warm, "cas_heads_8k"))
     if want("fib_8k_16_layers"):
         rows.update(_row_fib(torch, dev, flush, peaks, max_over_ranks, steps, warm))
     if only == "fib_8k_2_layers":   # same per-layer launch, small device footprint (profiling)
@@ -583,6 +609,16 @@ def _row_long(torch, dev, flush, peaks, max_over_ranks, steps, warm):
     return rows
 
 
+def _row_block_sparse(torch, dev, flush, peaks, max_over_ranks, steps, warm, name):
+    case = BlockSparseCase(name, dev)
+    seg, tot = _time_events(torch, [case.build, case.attend], steps, warm, flush)
+    a = max_over_ranks(seg[1])
+    return {name: {"ms_per_step": max_over_ranks(tot), "attn_ms": a, "mask_ms": seg[0],
+                   "effective_tflops": case.flops / (a * 1e-3) / 1e12,
+                   "frac_bf16_peak": case.flops / (a * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                   "tokens_per_s": case.tokens / (tot * 1e-3), "edges": case.edges}}
+
+
 def _row_fib(torch, dev, flush, peaks, max_over_ranks, steps, warm, layers=16):
     rows = {}
     # 16-layer Fibonacci pass at 8K (HBM roofline)
@@ -605,7 +641,8 @@ def main():
     ap.add_argument("--no-rows", action="store_true", help="skip the other hot-path rows")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--only-row", choices=["bigbird_16k", "long_topk_64k", "fib_8k_16_layers", "fib_8k_2_layers"], default=None,
+    ap.add_argument("--only-row", choices=["bigbird_16k", "long_topk_64k", "cas_heads_8k", "fib_8k_16_layers",
+                                           "fib_8k_2_layers"], default=None,
                     help="time one other hot-path row only (profiling aid; prints that row, not the bench line)")
     args = ap.parse_args()
     if args.warmup < 3:

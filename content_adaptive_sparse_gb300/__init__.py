@@ -5,7 +5,8 @@ current CUDA stream) and calls the C ABI declared in ``include/sa_api.h``; all t
 work of the hot path runs in the library's CUDA kernels. There is no CPU fallback:
 if the library is missing or the device is not an sm_103 GPU, calls raise.
 
-Names follow the C ABI: ``sa_build_mask``, ``sa_attn_fwd``, ``sa_offset_attn_fwd``,
+Names follow the C ABI: ``sa_build_mask``, ``sa_attn_fwd``, ``sa_attn_fwd_heads``,
+``sa_offset_attn_fwd``,
 ``sa_fib_offsets``, ``sa_block_ratios``, ``sa_mask_nnz_bound``, ``sa_device_status``.
 """
 from __future__ import annotations
@@ -18,6 +19,7 @@ import numpy as np
 from .build import LIB, build as build_library
 
 MASK_TOPK, MASK_BIGBIRD, MASK_FULL, MASK_LITERAL_MEAN = 0, 1, 2, 3
+LITERAL_LOCAL, LITERAL_PAIRS = 1, 2          # parts of the LITERAL_MEAN mask (0 = both)
 _MODES = {"topk": MASK_TOPK, "bigbird": MASK_BIGBIRD, "full": MASK_FULL, "literal_mean": MASK_LITERAL_MEAN}
 
 STATUS = {0: "SA_OK", -1: "SA_ERR_INVALID_ARG", -2: "SA_ERR_UNSUPPORTED", -3: "SA_ERR_CAPACITY",
@@ -34,7 +36,7 @@ class MaskParams(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_int32), ("block", ctypes.c_int32), ("n_tokens", ctypes.c_int32),
                 ("batch", ctypes.c_int32), ("causal", ctypes.c_int32), ("window_blocks", ctypes.c_int32),
                 ("global_blocks", ctypes.c_int32), ("topk", ctypes.c_int32), ("random_blocks", ctypes.c_int32),
-                ("reserved", ctypes.c_int32), ("seed", ctypes.c_uint64)]
+                ("components", ctypes.c_int32), ("seed", ctypes.c_uint64)]
 
 
 _lib = None
@@ -59,6 +61,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.sa_attn_fwd.argtypes = [_P, _P, _P, _I64x3, _I64x3, _I64x3, ctypes.c_int32, ctypes.c_int32,
                                 ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                 _P, _P, ctypes.c_int32, ctypes.c_float, _P, _P, _P]
+    lib.sa_attn_fwd_heads.argtypes = [_P, _P, _P, _I64x3, _I64x3, _I64x3, ctypes.c_int32, ctypes.c_int32,
+                                      ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                      ctypes.c_int32, ctypes.c_int32, _P, _P, _P, ctypes.c_int32, ctypes.c_float,
+                                      _P, _P, _P]
     lib.sa_offset_attn_fwd.argtypes = [_P, _P, _P, _I64x3, _I64x3, _I64x3, ctypes.c_int32, ctypes.c_int32,
                                        ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P,
                                        ctypes.c_int32, ctypes.c_float, _P, _P, _P]
@@ -66,8 +72,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.sa_block_ratios.argtypes = [_P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P,
                                     ctypes.c_int32]
     lib.sa_device_status.argtypes = [_P]
-    for name in ("sa_mask_nnz_bound", "sa_build_mask", "sa_attn_fwd", "sa_offset_attn_fwd", "sa_fib_offsets",
-                 "sa_block_ratios", "sa_device_status"):
+    for name in ("sa_mask_nnz_bound", "sa_build_mask", "sa_attn_fwd", "sa_attn_fwd_heads", "sa_offset_attn_fwd",
+                 "sa_fib_offsets", "sa_block_ratios", "sa_device_status"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -92,9 +98,9 @@ def _strides(t) -> _I64x3:
 
 
 def mask_params(mode, block, n_tokens, batch, causal=1, window_blocks=0, global_blocks=0, topk=0,
-                random_blocks=0, seed=0) -> MaskParams:
+                random_blocks=0, seed=0, components=0) -> MaskParams:
     return MaskParams(_MODES.get(mode, mode) if isinstance(mode, str) else mode, block, n_tokens, batch, causal,
-                      window_blocks, global_blocks, topk, random_blocks, 0, seed)
+                      window_blocks, global_blocks, topk, random_blocks, components, seed)
 
 
 # ------------------------------------------------------------------ C ABI, same names
@@ -121,6 +127,25 @@ def sa_attn_fwd(q, k, v, row_ptr, col_idx, block: int, causal: int, o, lse, csr_
         q.data_ptr(), k.data_ptr(), v.data_ptr(), _strides(q), _strides(k), _strides(o), b, n, h, hkv, d, block,
         int(causal), row_ptr.data_ptr(), col_idx.data_ptr(), int(bool(csr_shared)), scale, o.data_ptr(),
         lse.data_ptr(), _stream_ptr(stream)))
+
+
+def sa_attn_fwd_heads(q, k, v, csrs, head_mask, block: int, causal: int, o, lse, csr_shared: bool = False,
+                      softmax_scale: float | None = None, stream=None) -> None:
+    """``csrs``: list of (row_ptr, col_idx) device tensors; query head h uses
+    ``csrs[head_mask[h]]``."""
+    b, n, h, d = q.shape
+    hkv = k.shape[2]
+    nm = len(csrs)
+    rps = (ctypes.c_void_p * nm)(*[rp.data_ptr() for rp, _ in csrs])
+    cis = (ctypes.c_void_p * nm)(*[ci.data_ptr() for _, ci in csrs])
+    hm = np.ascontiguousarray(np.asarray(head_mask, dtype=np.int32))
+    if hm.shape != (h,):
+        raise ValueError("head_mask needs one CSR index per query head")
+    scale = 1.0 / float(np.sqrt(d)) if softmax_scale is None else float(softmax_scale)
+    _check("sa_attn_fwd_heads", load_library().sa_attn_fwd_heads(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), _strides(q), _strides(k), _strides(o), b, n, h, hkv, d, block,
+        int(causal), nm, ctypes.cast(rps, _P), ctypes.cast(cis, _P), hm.ctypes.data, int(bool(csr_shared)), scale,
+        o.data_ptr(), lse.data_ptr(), _stream_ptr(stream)))
 
 
 def sa_offset_attn_fwd(q, k, v, window: int, offsets, o, lse, softmax_scale: float | None = None,
@@ -182,6 +207,16 @@ def attn_fwd(q, k, v, row_ptr, col_idx, block: int, causal: int, csr_shared: boo
     return o, lse
 
 
+def attn_fwd_heads(q, k, v, csrs, head_mask, block: int, causal: int, csr_shared: bool = False,
+                   softmax_scale: float | None = None):
+    import torch
+    b, n, h, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((b, h, n), dtype=torch.float32, device=q.device)
+    sa_attn_fwd_heads(q, k, v, csrs, head_mask, block, causal, o, lse, csr_shared, softmax_scale)
+    return o, lse
+
+
 def offset_attn_fwd(q, k, v, window: int, offsets, softmax_scale: float | None = None):
     import torch
     b, n, h, d = q.shape
@@ -193,6 +228,6 @@ def offset_attn_fwd(q, k, v, window: int, offsets, softmax_scale: float | None =
 
 __all__ = [
     "build_library", "load_library", "SAError", "MaskParams", "mask_params", "sa_mask_nnz_bound", "sa_build_mask",
-    "sa_attn_fwd", "sa_offset_attn_fwd", "sa_fib_offsets", "sa_block_ratios", "sa_device_status", "build_mask",
+    "sa_attn_fwd", "sa_attn_fwd_heads", "attn_fwd_heads", "LITERAL_LOCAL", "LITERAL_PAIRS", "sa_offset_attn_fwd", "sa_fib_offsets", "sa_block_ratios", "sa_device_status", "build_mask",
     "attn_fwd", "offset_attn_fwd", "MASK_TOPK", "MASK_BIGBIRD", "MASK_FULL", "MASK_LITERAL_MEAN",
 ]

@@ -118,8 +118,10 @@ struct Params {
   int batch, n_tokens, heads, heads_per_kv, block, log2b, nb, causal, csr_shared;
   int tiles_per_seq;          // 128-row query tiles per (sequence, head)
   int n_items;
-  const int32_t* row_ptr;
-  const int32_t* col_idx;
+  int n_masks;
+  const int32_t* row_ptr[kMaxMasks];   // one CSR per head group
+  const int32_t* col_idx[kMaxMasks];
+  uint8_t head_mask[kMaxHeadMap];      // query head -> CSR (n_masks > 1)
   __nv_bfloat16* o;
   float* lse;
   int64_t o_sb, o_sn, o_sh;
@@ -230,7 +232,7 @@ struct UnionSmem {
 // Builds the union of rows I0 .. I0+nq-1 into u.list; returns its length. Column indices
 // outside [0, nb) are skipped and reported; under causality a block J > I0 + r is not
 // attached to query block r (its keys are all in the future).
-__device__ int build_union(const Params& p, UnionSmem& u, const int32_t* rp, int I0, int nq) {
+__device__ int build_union(const Params& p, UnionSmem& u, const int32_t* rp, const int32_t* ci, int I0, int nq) {
   const int lane = threadIdx.x & 31;
   const int nw = (p.nb + 31) >> 5;
   for (int r = 0; r < nq; ++r)
@@ -243,7 +245,7 @@ __device__ int build_union(const Params& p, UnionSmem& u, const int32_t* rp, int
   const int e1 = bq[kMaxQBlocks];
   __syncwarp();
   for (int e = e0 + lane; e < e1; e += 32) {
-    const int J = p.col_idx[e];
+    const int J = ci[e];
     int r = 0;
 #pragma unroll
     for (int q = 1; q < kMaxQBlocks; ++q) r += (q < nq && e >= bq[q]) ? 1 : 0;
@@ -306,7 +308,8 @@ __device__ void producer(const Params& p, int x, const CUtensorMap* tq, const CU
     const int I0 = q0 >> p.log2b;
     const int hk = it.h / p.heads_per_kv;
     const int nq = min(qb_per_tile, p.nb - I0);
-    const int32_t* rp = p.row_ptr + (size_t)(p.csr_shared ? 0 : it.s) * (p.nb + 1);
+    const int mi = p.n_masks > 1 ? p.head_mask[it.h] : 0;
+    const int32_t* rp = p.row_ptr[mi] + (size_t)(p.csr_shared ? 0 : it.s) * (p.nb + 1);
 
     // Q into buffer item_local % QB (rows beyond the sequence are zero-filled by TMA)
     if (lane == 0) {
@@ -323,7 +326,7 @@ __device__ void producer(const Params& p, int x, const CUtensorMap* tq, const CU
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     if (!ok) break;
 
-    const int n_keys = build_union(p, u, rp, I0, nq);
+    const int n_keys = build_union(p, u, rp, p.col_idx[mi], I0, nq);
     const int n_chunks = n_keys * cpb;
 
     for (int c0 = 0;; c0 += 2) {
@@ -852,7 +855,7 @@ __device__ void softmax_epilogue(const Params& p, int x, int h, PipeBars& bars, 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                    const __grid_constant__ CUtensorMap tv, const Params p) {
+                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ Params p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sbase = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -955,8 +958,12 @@ int launch_d(const AttnArgs& a, cudaStream_t stream) {
   p.csr_shared = a.csr_shared;
   p.tiles_per_seq = (a.n_tokens + kTile - 1) / kTile;
   p.n_items = a.batch * a.heads * p.tiles_per_seq;
-  p.row_ptr = a.row_ptr;
-  p.col_idx = a.col_idx;
+  p.n_masks = a.n_masks;
+  for (int m = 0; m < kMaxMasks; ++m) {
+    p.row_ptr[m] = a.row_ptr[m];
+    p.col_idx[m] = a.col_idx[m];
+  }
+  for (int h = 0; h < kMaxHeadMap; ++h) p.head_mask[h] = a.head_mask[h];
   p.o = static_cast<__nv_bfloat16*>(a.o);
   p.lse = a.lse;
   p.o_sb = a.o_strides[0];

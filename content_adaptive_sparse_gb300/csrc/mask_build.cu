@@ -21,6 +21,7 @@ constexpr int kWarps = kThreads / 32;
 
 struct MaskArgs {
   int mode, block, nb, batch, causal, w, g, k, r;
+  int local, literal;   // LITERAL_MEAN: which parts besides the identity are kept
   uint64_t seed;
   const float* ratio;
   int32_t* row_ptr;
@@ -196,10 +197,13 @@ __device__ int row_len(const MaskArgs& a, const Smem& s, int I) {
     }
     case SA_MASK_LITERAL_MEAN: {
       const int* lp = s.order;
-      const int lo = max(0, I - a.w);
-      const int hi = a.causal ? I : min(a.nb - 1, I + a.w);
-      int n = hi - lo + 1;
-      if (lit_at(lp, I)) {
+      int n = 1;                                                       // identity
+      if (a.local) {
+        const int lo = max(0, I - a.w);
+        const int hi = a.causal ? I : min(a.nb - 1, I + a.w);
+        n = hi - lo + 1;
+      }
+      if (a.literal && lit_at(lp, I)) {
         if (I - a.w - 1 >= 0) n += lp[I - a.w];                       // literals in [0, I-w-1]
         if (!a.causal && I + a.w + 1 < a.nb) n += lp[a.nb] - lp[I + a.w + 1];
       }
@@ -257,16 +261,17 @@ __device__ void fill_topk(const MaskArgs& a, const Smem& s, int I, int32_t* out,
 __device__ void fill_literal_mean(const MaskArgs& a, const Smem& s, int I, int32_t* out) {
   const int lane = threadIdx.x & 31;
   const int* lp = s.order;
-  const bool lit_i = lit_at(lp, I) != 0;
-  const int lo = lit_i ? 0 : max(0, I - a.w);
-  const int hi = a.causal ? I : (lit_i ? a.nb - 1 : min(a.nb - 1, I + a.w));
+  const bool lit_i = a.literal && lit_at(lp, I) != 0;
+  const int reach = a.local ? a.w : 0;                     // band kept around I
+  const int lo = lit_i ? 0 : max(0, I - reach);
+  const int hi = a.causal ? I : (lit_i ? a.nb - 1 : min(a.nb - 1, I + reach));
   int pos = 0;
   for (int base = lo; base <= hi; base += 32) {
     const int J = base + lane;
     bool sel = false;
     if (J <= hi) {
       const int dist = J > I ? J - I : I - J;
-      sel = dist <= a.w || (lit_i && lit_at(lp, J) && dist > a.w);
+      sel = dist <= reach || (lit_i && lit_at(lp, J) && dist > a.w);
     }
     const unsigned m = __ballot_sync(0xffffffffu, sel);
     if (sel) out[pos + __popc(m & lanemask_lt())] = J;
@@ -404,6 +409,9 @@ int launch_build_mask(const sa_mask_params& p, const float* d_ratio, int32_t* d_
   a.k = p.topk;
   a.r = p.random_blocks;
   a.seed = p.seed;
+  const int comp = p.components ? p.components : (SA_LITERAL_LOCAL | SA_LITERAL_PAIRS);
+  a.local = (comp & SA_LITERAL_LOCAL) != 0;
+  a.literal = (comp & SA_LITERAL_PAIRS) != 0;
   a.ratio = d_ratio;
   a.row_ptr = d_row_ptr;
   a.col_idx = d_col_idx;

@@ -68,7 +68,11 @@ int64_t nnz_bound(const sa_mask_params& p) {
         break;
       }
       case SA_MASK_LITERAL_MEAN:
-        per_seq += p.causal ? I + 1 : nb;   // every block literal
+        if (p.components == SA_LITERAL_LOCAL)   // the band alone
+          per_seq += (p.causal ? I : std::min<int64_t>(nb - 1, I + p.window_blocks)) -
+                     std::max<int64_t>(0, I - p.window_blocks) + 1;
+        else
+          per_seq += p.causal ? I + 1 : nb;     // every block literal
         break;
     }
   }
@@ -79,8 +83,9 @@ int check_mask_params(const sa_mask_params* p) {
   if (!p) return SA_ERR_INVALID_ARG;
   if (p->mode < SA_MASK_TOPK || p->mode > SA_MASK_LITERAL_MEAN) return SA_ERR_INVALID_ARG;
   if (p->block <= 0 || p->n_tokens <= 0 || p->batch <= 0 || p->n_tokens % p->block != 0) return SA_ERR_INVALID_ARG;
-  if (p->window_blocks < 0 || p->global_blocks < 0 || p->topk < 0 || p->random_blocks < 0 || p->reserved != 0)
-    return SA_ERR_INVALID_ARG;
+  if (p->window_blocks < 0 || p->global_blocks < 0 || p->topk < 0 || p->random_blocks < 0) return SA_ERR_INVALID_ARG;
+  if (p->components < 0 || p->components > (SA_LITERAL_LOCAL | SA_LITERAL_PAIRS)) return SA_ERR_INVALID_ARG;
+  if (p->components != 0 && p->mode != SA_MASK_LITERAL_MEAN) return SA_ERR_INVALID_ARG;
   if (p->causal != 0 && p->causal != 1) return SA_ERR_INVALID_ARG;
   if (p->n_tokens / p->block > sa::kMaxMaskBlocks) return SA_ERR_UNSUPPORTED;
   if (p->mode == SA_MASK_TOPK && !p->causal) return SA_ERR_UNSUPPORTED;
@@ -166,13 +171,21 @@ int sa_build_mask(const sa_mask_params* params, const float* d_ratio, int32_t* d
   return sa::launch_build_mask(*params, d_ratio, d_row_ptr, d_col_idx, static_cast<cudaStream_t>(stream));
 }
 
-int sa_attn_fwd(const void* q, const void* k, const void* v, const int64_t q_strides[3], const int64_t kv_strides[3],
-                const int64_t o_strides[3], int32_t batch, int32_t n_tokens, int32_t heads, int32_t kv_heads,
-                int32_t head_dim, int32_t block, int32_t causal, const int32_t* d_row_ptr, const int32_t* d_col_idx,
-                int32_t csr_shared, float softmax_scale, void* o, float* lse, void* stream) {
+int sa_attn_fwd_heads(const void* q, const void* k, const void* v, const int64_t q_strides[3],
+                      const int64_t kv_strides[3], const int64_t o_strides[3], int32_t batch, int32_t n_tokens,
+                      int32_t heads, int32_t kv_heads, int32_t head_dim, int32_t block, int32_t causal,
+                      int32_t n_masks, const int32_t* const* h_row_ptrs, const int32_t* const* h_col_idxs,
+                      const int32_t* h_head_mask, int32_t csr_shared, float softmax_scale, void* o, float* lse,
+                      void* stream) {
   int st = check_attn_common(q, k, v, q_strides, kv_strides, o_strides, batch, n_tokens, heads, kv_heads, o, lse);
   if (st != SA_OK) return st;
-  if (!d_row_ptr || !d_col_idx) return SA_ERR_INVALID_ARG;
+  if (n_masks < 1 || !h_row_ptrs || !h_col_idxs || (n_masks > 1 && !h_head_mask)) return SA_ERR_INVALID_ARG;
+  if (n_masks > sa::kMaxMasks || (n_masks > 1 && heads > sa::kMaxHeadMap)) return SA_ERR_UNSUPPORTED;
+  for (int m = 0; m < n_masks; ++m)
+    if (!h_row_ptrs[m] || !h_col_idxs[m]) return SA_ERR_INVALID_ARG;
+  if (n_masks > 1)
+    for (int h = 0; h < heads; ++h)
+      if (h_head_mask[h] < 0 || h_head_mask[h] >= n_masks) return SA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return SA_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.f)) return SA_ERR_INVALID_ARG;
   if (head_dim != 32 && head_dim != 64 && head_dim != 128) return SA_ERR_UNSUPPORTED;
@@ -200,10 +213,25 @@ int sa_attn_fwd(const void* q, const void* k, const void* v, const int64_t q_str
   a.block = block;
   a.causal = causal;
   a.csr_shared = csr_shared != 0;
-  a.row_ptr = d_row_ptr;
-  a.col_idx = d_col_idx;
+  a.n_masks = n_masks;
+  for (int m = 0; m < sa::kMaxMasks; ++m) {
+    a.row_ptr[m] = m < n_masks ? h_row_ptrs[m] : nullptr;
+    a.col_idx[m] = m < n_masks ? h_col_idxs[m] : nullptr;
+  }
+  for (int h = 0; h < sa::kMaxHeadMap; ++h)
+    a.head_mask[h] = (n_masks > 1 && h < heads) ? (uint8_t)h_head_mask[h] : 0;
   a.softmax_scale = softmax_scale;
   return sa::launch_attn_fwd(a, static_cast<cudaStream_t>(stream));
+}
+
+int sa_attn_fwd(const void* q, const void* k, const void* v, const int64_t q_strides[3], const int64_t kv_strides[3],
+                const int64_t o_strides[3], int32_t batch, int32_t n_tokens, int32_t heads, int32_t kv_heads,
+                int32_t head_dim, int32_t block, int32_t causal, const int32_t* d_row_ptr, const int32_t* d_col_idx,
+                int32_t csr_shared, float softmax_scale, void* o, float* lse, void* stream) {
+  if (!d_row_ptr || !d_col_idx) return SA_ERR_INVALID_ARG;
+  return sa_attn_fwd_heads(q, k, v, q_strides, kv_strides, o_strides, batch, n_tokens, heads, kv_heads, head_dim,
+                           block, causal, 1, &d_row_ptr, &d_col_idx, nullptr, csr_shared, softmax_scale, o, lse,
+                           stream);
 }
 
 int sa_offset_attn_fwd(const void* q, const void* k, const void* v, const int64_t q_strides[3],

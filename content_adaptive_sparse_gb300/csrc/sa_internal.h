@@ -19,6 +19,8 @@ int launch_build_mask(const sa_mask_params& p, const float* d_ratio, int32_t* d_
                       cudaStream_t stream);
 
 // attn_fwd.cu
+constexpr int kMaxMasks = 8;       // CSRs per call (head groups)
+constexpr int kMaxHeadMap = 256;   // heads with a per-head CSR choice
 struct AttnArgs {
   const void* q;
   const void* k;
@@ -29,8 +31,10 @@ struct AttnArgs {
   int64_t kv_strides[3];
   int64_t o_strides[3];
   int32_t batch, n_tokens, heads, kv_heads, head_dim, block, causal, csr_shared;
-  const int32_t* row_ptr;
-  const int32_t* col_idx;
+  int32_t n_masks;
+  const int32_t* row_ptr[kMaxMasks];
+  const int32_t* col_idx[kMaxMasks];
+  uint8_t head_mask[kMaxHeadMap];    // query head -> CSR
   float softmax_scale;
 };
 int launch_attn_fwd(const AttnArgs& a, cudaStream_t stream);

@@ -66,9 +66,14 @@ typedef enum {
   SA_MASK_FULL = 2,
   /* "Parameter-free Adaptive Sparse Attention ...", Eq. 2-3 / Algorithm 1: block i is
    * literal iff r_i > mean(r); M = {|I-J| <= w} u identity u {literal I and J,
-   * |I-J| > w}; causal keeps J <= I. global_blocks must be 0. */
+   * |I-J| > w}; causal keeps J <= I. global_blocks must be 0. sa_mask_params.components
+   * keeps a part of M (Appendix B "Head-specific mask distribution"). */
   SA_MASK_LITERAL_MEAN = 3
 } sa_mask_mode;
+
+/* Parts of the LITERAL_MEAN mask besides the identity (bit flags; 0 = both = full M):
+ * local heads use M_local u I, long-range heads M_lit u I, hybrid heads the full M. */
+enum { SA_LITERAL_LOCAL = 1, SA_LITERAL_PAIRS = 2 };
 
 typedef struct {
   int32_t mode;          /* sa_mask_mode                                               */
@@ -80,13 +85,14 @@ typedef struct {
   int32_t global_blocks; /* g                                                           */
   int32_t topk;          /* k (TOPK)                                                    */
   int32_t random_blocks; /* r (BIGBIRD), <= 64                                          */
-  int32_t reserved;      /* must be 0                                                   */
+  int32_t components;    /* LITERAL_MEAN: SA_LITERAL_* flags, 0 = all; other modes: 0   */
   uint64_t seed;         /* Philox key (BIGBIRD)                                        */
 } sa_mask_params;
 
 /* Upper bound on the number of CSR entries sa_build_mask writes for these parameters
- * (exact for TOPK, BIGBIRD and FULL, whose row lengths do not depend on the ratios;
- * the all-literal worst case for LITERAL_MEAN). Host only; no device work. */
+ * (exact for TOPK, BIGBIRD, FULL and the LOCAL part of LITERAL_MEAN, whose row lengths
+ * do not depend on the ratios; the all-literal worst case for the other LITERAL_MEAN
+ * parts). Host only; no device work. */
 int sa_mask_nnz_bound(const sa_mask_params* params, int64_t* h_nnz);
 
 /* Build the block CSR of every sequence on the GPU.
@@ -121,6 +127,24 @@ int sa_attn_fwd(const void* q, const void* k, const void* v, const int64_t q_str
                 int32_t heads, int32_t kv_heads, int32_t head_dim, int32_t block, int32_t causal,
                 const int32_t* d_row_ptr, const int32_t* d_col_idx, int32_t csr_shared, float softmax_scale,
                 void* o, float* lse, void* stream);
+
+/* sa_attn_fwd with one block CSR per head group ("Parameter-free Adaptive Sparse
+ * Attention ...", Appendix B "Head-specific mask distribution": local, long-range and
+ * hybrid heads read different parts of the block mask).
+ *   n_masks      : number of CSRs, 1 .. 8.
+ *   h_row_ptrs   : host array [n_masks] of device pointers, each a row_ptr as written
+ *                  by sa_build_mask for the same batch, n_tokens and block.
+ *   h_col_idxs   : host array [n_masks] of the matching device col_idx pointers.
+ *   h_head_mask  : host int32 [heads]; query head h uses CSR h_head_mask[h], in
+ *                  [0, n_masks). heads <= 256.
+ * The host arrays are read before the call returns. Every other argument is as in
+ * sa_attn_fwd (csr_shared applies to every CSR). */
+int sa_attn_fwd_heads(const void* q, const void* k, const void* v, const int64_t q_strides[3],
+                      const int64_t kv_strides[3], const int64_t o_strides[3], int32_t batch, int32_t n_tokens,
+                      int32_t heads, int32_t kv_heads, int32_t head_dim, int32_t block, int32_t causal,
+                      int32_t n_masks, const int32_t* const* h_row_ptrs, const int32_t* const* h_col_idxs,
+                      const int32_t* h_head_mask, int32_t csr_shared, float softmax_scale, void* o, float* lse,
+                      void* stream);
 
 /* Token-granular window-plus-offset attention forward ("Depth-Staggered Fibonacci
  * Spacing ...", section 2 "Attended set"): query i attends to keys

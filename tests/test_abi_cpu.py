@@ -31,7 +31,7 @@ def _declared_functions():
 
 def test_header_symbols_exported(lib):
     names = _declared_functions()
-    assert {"sa_build_mask", "sa_attn_fwd", "sa_offset_attn_fwd", "sa_fib_offsets", "sa_block_ratios",
+    assert {"sa_build_mask", "sa_attn_fwd", "sa_attn_fwd_heads", "sa_offset_attn_fwd", "sa_fib_offsets", "sa_block_ratios",
             "sa_mask_nnz_bound", "sa_device_status", "sa_status_string", "sa_version"} <= set(names)
     for n in names:
         assert hasattr(lib, n), n
@@ -63,10 +63,12 @@ def test_fib_offsets_match_oracle(lib):
 def _params(p: om.MaskParams, batch: int):
     mode = {"topk": 0, "bigbird": 1, "full": 2, "literal_mean": 3}[p.mode]
     return sa.mask_params(mode, p.block, p.n_tokens, batch, p.causal, p.window_blocks, p.global_blocks, p.topk,
-                          p.random_blocks, p.seed)
+                          p.random_blocks, p.seed, p.components)
 
 
 @pytest.mark.parametrize("p", [
+    om.MaskParams("literal_mean", 64, 4096, 1, 3, components=1),
+    om.MaskParams("literal_mean", 32, 1024, 0, 2, components=1),
     om.MaskParams("topk", 64, 8192, 1, 4, 1, 16),
     om.MaskParams("topk", 128, 65536, 1, 4, 1, 256),
     om.MaskParams("bigbird", 32, 16384, 0, 8, 1, 0, 1, 45),
@@ -77,7 +79,7 @@ def _params(p: om.MaskParams, batch: int):
 def test_nnz_bound_exact_for_data_independent_modes(lib, p):
     rng = np.random.default_rng(0)
     ratios = rng.random((2, p.nb)).astype(np.float32)
-    _, ci = om.build_csr(p, ratios if p.mode == "topk" else None, 2)
+    _, ci = om.build_csr(p, ratios if p.mode in ("topk", "literal_mean") else None, 2)
     assert sa.sa_mask_nnz_bound(_params(p, 2)) == len(ci)
 
 
@@ -88,8 +90,10 @@ def test_argument_validation_before_any_launch(lib):
         sa.mask_params(0, 64, 1000, 1, window_blocks=4),                   # N % b != 0
         sa.mask_params(3, 64, 1024, 1, global_blocks=1),                   # literal_mean has no globals
         sa.mask_params(0, 1, 8192, 1),                                     # nb > 4096
+        sa.mask_params(3, 64, 1024, 1, components=4),                      # unknown component bit
+        sa.mask_params(0, 64, 8192, 1, window_blocks=4, components=1),     # components: literal_mean only
     ]
-    expect = [-2, -2, -1, -2, -2]
+    expect = [-2, -2, -1, -2, -2, -1, -1]
     for prm, code in zip(bad, expect):
         out = ctypes.c_int64(0)
         assert lib.sa_mask_nnz_bound(ctypes.byref(prm), ctypes.byref(out)) == code
@@ -107,6 +111,16 @@ def test_argument_validation_before_any_launch(lib):
                            ctypes.c_float(0.125), p16, p16, None) == -1
     assert lib.sa_attn_fwd(ctypes.c_void_p(258), p16, p16, s, s, s, 1, 8192, 12, 12, 64, 64, 1, p16, p16, 0,
                            ctypes.c_float(0.125), p16, p16, None) == -2
+    # per-head CSRs: head index out of range invalid, too many CSRs unsupported
+    P2 = ctypes.c_void_p * 2
+    rps, cis = P2(256, 512), P2(256, 512)
+    hm = (ctypes.c_int32 * 12)(*([0] * 11 + [2]))
+    assert lib.sa_attn_fwd_heads(p16, p16, p16, s, s, s, 1, 8192, 12, 12, 64, 64, 1, 2, rps, cis, hm, 0,
+                                 ctypes.c_float(0.125), p16, p16, None) == -1
+    P9 = ctypes.c_void_p * 9
+    rp9 = P9(*([256] * 9))
+    assert lib.sa_attn_fwd_heads(p16, p16, p16, s, s, s, 1, 8192, 12, 12, 64, 64, 1, 9, rp9, rp9, hm, 0,
+                                 ctypes.c_float(0.125), p16, p16, None) == -2
     offs = (ctypes.c_int32 * 2)(5, 9)        # offset inside the window -> invalid
     assert lib.sa_offset_attn_fwd(p16, p16, p16, s, s, s, 1, 8192, 8, 8, 64, 8, offs, 2,
                                   ctypes.c_float(0.125), p16, p16, None) == -1

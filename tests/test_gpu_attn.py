@@ -15,7 +15,7 @@ def _mask_on_gpu(p: om.MaskParams, batch: int, ratios=None):
     torch = torch_cuda()
     mode = {"topk": 0, "bigbird": 1, "full": 2, "literal_mean": 3}[p.mode]
     prm = sa.mask_params(mode, p.block, p.n_tokens, batch, p.causal, p.window_blocks, p.global_blocks, p.topk,
-                         p.random_blocks, p.seed)
+                         p.random_blocks, p.seed, p.components)
     r = None if ratios is None else torch.from_numpy(np.ascontiguousarray(ratios)).cuda()
     return sa.build_mask(prm, r)
 
@@ -217,3 +217,90 @@ def test_long_topk_64k_sampled(topk):
     n = cfg["n_tokens"]
     _full_size(cfg, p, 1, sa.sa_block_ratios(data, cfg["block"]), oracle.block_ratios(data, cfg["block"]),
                [(0, n - 1, 15), (0, 0, 0), (0, 40000, 8)])
+
+
+# ---------------------------------------------------------------- head groups (per-head CSR)
+
+def _head_group_case(bt, n, b, h, hkv, d, w, causal, comps, seed, ratios, qmul=2.0):
+    torch = torch_cuda()
+    rng = np.random.default_rng(seed)
+    qb = bf16_normal_bits(rng, (bt, n, h, d), 0.125 * qmul)
+    kb = bf16_normal_bits(rng, (bt, n, hkv, d), 0.125)
+    vb = bf16_normal_bits(rng, (bt, n, hkv, d), 0.125)
+    parts = sorted(set(comps))
+    head_mask = [parts.index(c) for c in comps]
+    csrs_d, csrs_o = [], []
+    for c in parts:
+        p = om.MaskParams("literal_mean", b, n, causal, w, components=c)
+        csrs_d.append(_mask_on_gpu(p, bt, ratios))
+        csrs_o.append(om.build_csr(p, ratios, bt))
+    o, lse = sa.attn_fwd_heads(to_dev(qb), to_dev(kb), to_dev(vb), csrs_d, head_mask, b, causal)
+    torch.cuda.synchronize()
+    assert sa.sa_device_status() == 0
+    o_ref, lse_ref = oracle.attention_csr_heads(bf16_bits_to_f64(qb), bf16_bits_to_f64(kb), bf16_bits_to_f64(vb),
+                                                csrs_o, head_mask, b, causal)
+    assert_attention_close(bf16_to_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref,
+                           f"head groups b={b} d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("b,d,causal", [(128, 64, 1), (64, 64, 0), (32, 128, 1), (128, 32, 0)])
+def test_head_groups_against_oracle(b, d, causal):
+    """The page's split (6 local, 3 long-range, 3 hybrid heads) with 3 KV heads, so that
+    KV groups straddle head groups (KV head 1 serves local heads 4-5 and literal heads
+    6-7; KV head 2 serves literal head 8 and hybrid heads 9-11)."""
+    n, bt = 1536, 2
+    rng = np.random.default_rng(b + d)
+    ratios = (rng.integers(20, 90, (bt, n // b)) / np.float32(b)).astype(np.float32)
+    comps = oracle.cas_head_components(12)
+    _head_group_case(bt, n, b, 12, 3, d, 1, causal, comps, seed=b * d + causal, ratios=ratios)
+
+
+def test_head_groups_interleaved_and_single_mask():
+    """Heads that alternate between CSRs, and n_masks = 1 through the per-head entry
+    point, which must equal sa_attn_fwd bit for bit."""
+    torch = torch_cuda()
+    n, b, bt = 1024, 64, 1
+    rng = np.random.default_rng(77)
+    ratios = (rng.integers(20, 90, (bt, n // b)) / np.float32(b)).astype(np.float32)
+    _head_group_case(bt, n, b, 5, 5, 64, 2, 1, [2, 1, 0, 1, 2], seed=3, ratios=ratios, qmul=4.0)
+    p = om.MaskParams("literal_mean", b, n, 1, 1)
+    rp, ci = _mask_on_gpu(p, bt, ratios)
+    q, k, v = (to_dev(bf16_normal_bits(rng, (bt, n, 3, 64), 0.25)) for _ in range(3))
+    o1, l1 = sa.attn_fwd(q, k, v, rp, ci, b, 1)
+    o2, l2 = sa.attn_fwd_heads(q, k, v, [(rp, ci)], [0, 0, 0], b, 1)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_cas_heads_8k_sampled():
+    cfg = workload("cas_heads_8k")
+    data = byte_stream(cfg)
+    b, n, bt, h = cfg["block"], cfg["n_tokens"], cfg["batch"], cfg["heads"]
+    r_gpu = sa.sa_block_ratios(data, b, cfg["zlib_level"])
+    r_ora = oracle.block_ratios(data, b, cfg["zlib_level"])
+    comps = list(cfg["head_components"])
+    assert comps == oracle.cas_head_components(h)
+    parts = sorted(set(comps))
+    head_mask = [parts.index(c) for c in comps]
+    qb, kb, vb = qkv_bits(cfg)
+    csrs_d, csrs_o = [], []
+    for c in parts:
+        p = om.MaskParams("literal_mean", b, n, 1, cfg["window_blocks"], components=c)
+        csrs_d.append(_mask_on_gpu(p, bt, r_gpu))
+        csrs_o.append(om.build_csr(p, r_ora, bt))
+    torch = torch_cuda()
+    o, lse = sa.attn_fwd_heads(to_dev(qb), to_dev(kb), to_dev(vb), csrs_d, head_mask, b, 1)
+    torch.cuda.synchronize()
+    assert sa.sa_device_status() == 0
+    o_np, lse_np = bf16_to_f64(o), lse.cpu().numpy().astype(np.float64)
+    rng = np.random.default_rng(4)
+    smp = _samples(rng, bt, n, h, k=36, extra=[(0, 0, 0), (3, n - 1, 11), (1, 130, 7), (2, 4095, 5)])
+    o_g = np.stack([o_np[s, i, hh] for s, i, hh in smp])
+    l_g = np.array([lse_np[s, hh, i] for s, i, hh in smp])
+    o_ref = np.zeros_like(o_g)
+    l_ref = np.zeros_like(l_g)
+    for t, (s, i, hh) in enumerate(smp):
+        rp_o, ci_o = csrs_o[head_mask[hh]]
+        orow, lrow = oracle.attention_rows_csr(qb, kb, vb, rp_o, ci_o, b, 1, [(s, i, hh)], convert=bf16_bits_to_f64)
+        o_ref[t], l_ref[t] = orow[0], lrow[0]
+    assert_attention_close(o_g, l_g, o_ref, l_ref, cfg["name"])

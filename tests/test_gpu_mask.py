@@ -15,7 +15,7 @@ def _gpu_csr(p: om.MaskParams, batch: int, ratios=None):
     torch = torch_cuda()
     mode = {"topk": 0, "bigbird": 1, "full": 2, "literal_mean": 3}[p.mode]
     prm = sa.mask_params(mode, p.block, p.n_tokens, batch, p.causal, p.window_blocks, p.global_blocks, p.topk,
-                         p.random_blocks, p.seed)
+                         p.random_blocks, p.seed, p.components)
     r_dev = None if ratios is None else torch.from_numpy(np.ascontiguousarray(ratios)).cuda()
     rp, ci = sa.build_mask(prm, r_dev)
     torch.cuda.synchronize()
@@ -73,6 +73,15 @@ def test_literal_mean(causal, b, w):
     _compare(p, 3, sa.sa_block_ratios(data, b), oracle.block_ratios(data, b))
 
 
+@pytest.mark.parametrize("components", [1, 2])
+@pytest.mark.parametrize("causal", [1, 0])
+def test_literal_mean_components(causal, components):
+    n, b, w = 8192, 64, 2
+    data = np.stack([bytes_zipf_text(200 + s, n) for s in range(2)])
+    p = om.MaskParams("literal_mean", b, n, causal, w, components=components)
+    _compare(p, 2, sa.sa_block_ratios(data, b), oracle.block_ratios(data, b))
+
+
 def test_random_parameter_sweep():
     rng = np.random.default_rng(2024)
     for trial in range(40):
@@ -91,7 +100,8 @@ def test_random_parameter_sweep():
         elif mode == "full":
             p = om.MaskParams("full", b, n, int(rng.integers(0, 2)))
         else:
-            p = om.MaskParams("literal_mean", b, n, int(rng.integers(0, 2)), int(rng.integers(0, 4)))
+            p = om.MaskParams("literal_mean", b, n, int(rng.integers(0, 2)), int(rng.integers(0, 4)),
+                              components=int(rng.integers(0, 4)))
         needs = mode in ("topk", "literal_mean")
         _compare(p, batch, ratios if needs else None, ratios if needs else None)
 

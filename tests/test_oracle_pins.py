@@ -453,3 +453,10 @@ def test_attention_heads_reduces_to_single_csr_per_head():
         od, ld = oracle.dense_masked_attention(q[:, :, hh:hh + 1], k[:, :, hh:hh + 1], v[:, :, hh:hh + 1], tok)
         assert np.abs(o[:, :, hh] - od[:, :, 0]).max() < 1e-12
         assert np.abs(lse[:, hh] - ld[:, 0]).max() < 1e-12
+
+
+def test_cas_workload_uses_page_head_split():
+    from workloads import workload as _wl
+    cfg = _wl("cas_heads_8k")
+    assert list(cfg["head_components"]) == oracle.cas_head_components(cfg["heads"])
+    assert cfg["block"] == 128 and cfg["window_blocks"] == 1 and cfg["zlib_level"] == 1   # [CAS] Table 8

@@ -19,6 +19,11 @@ Workloads (shapes and pattern parameters as the pages and the task state them):
 * ``fib_2k`` / ``fib_8k`` - 16 layers, 8 sequences, 8 heads of 64, token-granular
                        window plus alpha-scaled Fibonacci offsets (Depth-Staggered
                        Fibonacci Spacing page, sections 2-3).
+* ``cas_heads_8k``   - 4 x 8192 byte tokens, block 128, 12 heads, d_h 64, the mean-threshold
+                       mask with a +-1-block window and zlib level 1, split over head
+                       groups: 6 local, 3 long-range (literal pairs), 3 hybrid (the
+                       Parameter-free Adaptive Sparse Attention page, section 4.1,
+                       Table 8 and Appendix B "Head-specific mask distribution").
 * ``long_topk_64k``  - 1 x 65536 byte tokens, block 128, 16 heads, d_h 128, top-64
                        (top-k swept over 16/64/256), plus ``full_16k``.
 
@@ -58,6 +63,11 @@ WORKLOADS = {
                    window=8, alpha_lo=(1, 2), alpha_hi=(2, 1), n_rungs=15, std=1.0 / 8.0, seed=46),
     "fib_8k": dict(kind="fib", layers=16, batch=8, n_tokens=8192, heads=8, kv_heads=8, head_dim=64,
                    window=8, alpha_lo=(1, 2), alpha_hi=(2, 1), n_rungs=15, std=1.0 / 8.0, seed=46),
+    # head_components: per head, the mask part it reads (1 local, 2 literal pairs, 3 both)
+    "cas_heads_8k": dict(kind="literal_heads", batch=4, n_tokens=8192, block=128, heads=12, kv_heads=12,
+                         head_dim=64, window_blocks=1, causal=1, zlib_level=1,
+                         head_components=(1, 1, 1, 1, 1, 1, 2, 2, 2, 3, 3, 3),
+                         std=1.0 / 8.0, bytes="zipf_text", seed=48),
     "long_topk_64k": dict(kind="topk", batch=1, n_tokens=65536, block=128, heads=16, kv_heads=16,
                           head_dim=128, window_blocks=4, global_blocks=1, topk=64, causal=1,
                           std=1.0 / np.sqrt(128.0), bytes="phrase_random", seed=47),
