@@ -28,7 +28,8 @@ from .philox import philox4x64_10, philox_word
 from .masks import (MaskParams, build_csr, csr_topk_rows, csr_bigbird_rows, csr_full_rows,
                     csr_literal_mean_rows, csr_to_block_mask, block_mask_to_token_mask,
                     literal_flags, topk_row_count, cas_head_components, LOCAL, LITERAL)
-from .fib import fib_rungs, fib_rungs_upto, alpha_schedule, fib_offsets, offset_key_set
+from .fib import (fib_rungs, fib_rungs_upto, pow2_rungs, pow2_rungs_upto, alpha_schedule, fib_offsets,
+                  offset_key_set)
 from .attention import (attention_csr, attention_csr_block, attention_csr_heads, attention_offsets,
                         dense_masked_attention, attention_rows_csr)
 
@@ -37,7 +38,7 @@ __all__ = [
     "csr_topk_rows", "csr_bigbird_rows", "csr_full_rows", "csr_literal_mean_rows",
     "csr_to_block_mask", "block_mask_to_token_mask", "literal_flags", "topk_row_count",
     "cas_head_components", "LOCAL", "LITERAL", "attention_csr_heads",
-    "fib_rungs", "fib_rungs_upto", "alpha_schedule", "fib_offsets", "offset_key_set", "attention_csr",
+    "fib_rungs", "fib_rungs_upto", "pow2_rungs", "pow2_rungs_upto", "alpha_schedule", "fib_offsets", "offset_key_set", "attention_csr",
     "attention_csr_block",
     "attention_offsets", "dense_masked_attention", "attention_rows_csr",
 ]

@@ -9,9 +9,18 @@
   torch ``round``). Ties occur (alpha = 1/2 with odd f).
 * Key set of query i: { i - delta : delta in {0, ..., W} u D, i - delta >= 0 } as a set
   (the union is deduplicated; offsets inside the window add nothing).
+* Coprime stagger ([FIB] section 2 "The per-layer scalar"): the linear ramp's values
+  reassigned to layers by l -> (S l mod L), S = 7. Reading: layer l takes the ramp
+  value at index (S l) mod L. For L = 16, S = 7 is its own inverse (7 * 7 = 49 = 1 mod
+  16), so the other reading (ramp index l goes to layer S l mod L) is the same map.
+* Power-of-2 control base ([FIB] section 2 "Control base"): rungs 1, 2, 4, ..., "reach
+  matched" to the Fibonacci base. Reading: 11 rungs up to 1024, the power of two the
+  page itself equates with f_15 = 987 ("987 ~ 1024"); ``pow2_rungs_upto(N)`` is the
+  every-rung-up-to-N variant.
 """
 from __future__ import annotations
 
+import math
 from fractions import Fraction
 
 
@@ -33,12 +42,33 @@ def fib_rungs_upto(n: int) -> list[int]:
     return out
 
 
-def alpha_schedule(layers: int, lo=(1, 2), hi=(3, 2)) -> list[Fraction]:
+def pow2_rungs(n_rungs: int = 11) -> list[int]:
+    return [2 ** k for k in range(n_rungs)]
+
+
+def pow2_rungs_upto(n: int) -> list[int]:
+    out = []
+    a = 1
+    while a <= n:
+        out.append(a)
+        a *= 2
+    return out
+
+
+def alpha_schedule(layers: int, lo=(1, 2), hi=(3, 2), stride: int = 1) -> list[Fraction]:
+    """Per-layer alpha: the linear ramp lo -> hi over ``layers`` layers; with
+    ``stride`` S > 1 layer l takes the ramp value at index (S l) mod L (coprime
+    stagger; S must be coprime to L)."""
     a_lo = Fraction(*lo)
     a_hi = Fraction(*hi)
     if layers == 1:
         return [a_lo]
-    return [a_lo + (a_hi - a_lo) * Fraction(l, layers - 1) for l in range(layers)]
+    ramp = [a_lo + (a_hi - a_lo) * Fraction(l, layers - 1) for l in range(layers)]
+    if stride == 1:
+        return ramp
+    if math.gcd(stride, layers) != 1:
+        raise ValueError("the stagger stride must be coprime to the layer count")
+    return [ramp[(stride * l) % layers] for l in range(layers)]
 
 
 def fib_offsets(alpha: Fraction, rungs: list[int]) -> list[int]:

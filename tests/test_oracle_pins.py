@@ -237,6 +237,32 @@ def test_fib_offsets_integer_closed_form():
     assert oracle.fib_offsets(Fraction(1, 2), [1, 3, 5]) == [0, 2]
 
 
+def test_coprime_stagger_is_a_permutation_of_the_ramp():
+    """[FIB] section 2: the same multiset of alphas, layer l -> (7 l mod 16); adjacent
+    layers land at least 7 ramp steps apart, and 7 is its own inverse mod 16 (so both
+    directions of the map give the same schedule)."""
+    lin = oracle.alpha_schedule(16, (1, 2), (3, 2))
+    cop = oracle.alpha_schedule(16, (1, 2), (3, 2), stride=7)
+    assert sorted(cop) == sorted(lin) and cop != lin
+    idx = [lin.index(a) for a in cop]
+    assert idx == [0, 7, 14, 5, 12, 3, 10, 1, 8, 15, 6, 13, 4, 11, 2, 9]
+    assert min(abs(idx[l + 1] - idx[l]) for l in range(15)) == 7
+    assert (7 * 7) % 16 == 1 and [idx.index(l) for l in range(16)] == idx
+    with pytest.raises(ValueError):
+        oracle.alpha_schedule(16, (1, 2), (3, 2), stride=4)
+
+
+def test_pow2_rungs_reach_and_offsets():
+    """[FIB] "Control base": powers of two reaching the Fibonacci base's 987 ~ 1024 with
+    fewer rungs; integer offsets follow the same rounding as the Fibonacci ones."""
+    r = oracle.pow2_rungs()
+    assert r == [1 << k for k in range(11)] and len(r) < len(oracle.fib_rungs(15))
+    assert r[-1] == 1024 and r[-2] < 987 < r[-1]
+    assert oracle.pow2_rungs_upto(8192) == [1 << k for k in range(14)]
+    # alpha = 3/4: 3/4 -> 1, 3/2 -> 2, 3 -> 3, 6, 12, ..., 768
+    assert oracle.fib_offsets(Fraction(3, 4), r) == [1, 2, 3, 6, 12, 24, 48, 96, 192, 384, 768]
+
+
 def test_offset_key_set_count_closed_form():
     D = oracle.fib_offsets(Fraction(7, 10), oracle.fib_rungs(15))
     W = 8
