@@ -34,7 +34,6 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
-import math
 import os
 import re
 import statistics
@@ -285,13 +284,10 @@ class OffsetCase:
                                                      "window"))
         self.W = W
         self.layers = []
-        lo, hi = cfg["alpha_lo"], cfg["alpha_hi"]
+        ladder = sa.sa_pow2_offsets if cfg.get("ladder") == "pow2" else sa.sa_fib_offsets
         for l in range(L):
-            # alpha_l = lo + (hi - lo) * l / (L - 1), exact rational
-            num = lo[0] * hi[1] * (L - 1) + (hi[0] * lo[1] - lo[0] * hi[1]) * l
-            den = lo[1] * hi[1] * (L - 1)
-            g = math.gcd(num, den)
-            offs = sa.sa_fib_offsets(num // g, den // g, cfg["n_rungs"], W, n)
+            num, den = sa.sa_layer_alpha(l, L, cfg["alpha_lo"], cfg["alpha_hi"], cfg.get("stride", 1))
+            offs = ladder(num, den, cfg["n_rungs"], W, n)
             qb, kb, vb = qkv_bits(cfg, seed_offset=l)
             q, k, v = (torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev) for x in (qb, kb, vb))
             o = torch.empty_like(q)
@@ -577,6 +573,10 @@ def _measure_rows(torch, sa, dev, flush, peaks, max_over_ranks, only=None, steps
         rows.update(_row_block_sparse(torch, dev, flush, peaks, max_over_ranks, steps, warm, "cas_heads_8k"))
     if want("fib_8k_16_layers"):
         rows.update(_row_fib(torch, dev, flush, peaks, max_over_ranks, steps, warm))
+    if want("fib_8k_coprime_16_layers"):
+        rows.update(_row_fib(torch, dev, flush, peaks, max_over_ranks, steps, warm, name="fib_8k_coprime"))
+    if want("pow2_8k_16_layers"):
+        rows.update(_row_fib(torch, dev, flush, peaks, max_over_ranks, steps, warm, name="pow2_8k"))
     if only == "fib_8k_2_layers":   # same per-layer launch, small device footprint (profiling)
         rows.update(_row_fib(torch, dev, flush, peaks, max_over_ranks, steps, warm, layers=2))
     torch.cuda.empty_cache()
@@ -619,14 +619,14 @@ def _row_block_sparse(torch, dev, flush, peaks, max_over_ranks, steps, warm, nam
                    "tokens_per_s": case.tokens / (tot * 1e-3), "edges": case.edges}}
 
 
-def _row_fib(torch, dev, flush, peaks, max_over_ranks, steps, warm, layers=16):
+def _row_fib(torch, dev, flush, peaks, max_over_ranks, steps, warm, layers=16, name="fib_8k"):
     rows = {}
     # 16-layer Fibonacci pass at 8K (HBM roofline)
-    fb = OffsetCase("fib_8k", dev, layers=layers)
+    fb = OffsetCase(name, dev, layers=layers)
     seg, tot = _time_events(torch, [fb.step], steps, warm, flush)
     t = max_over_ranks(tot)
     gbs = fb.bytes / (t * 1e-3) / 1e9
-    rows[f"fib_8k_{layers}_layers"] = {"ms_per_step": t, "hbm_gbs": gbs, "frac_hbm": gbs / peaks["hbm_gbs"],
+    rows[f"{name}_{layers}_layers"] = {"ms_per_step": t, "hbm_gbs": gbs, "frac_hbm": gbs / peaks["hbm_gbs"],
                                 "algorithmic_bytes": fb.bytes, "effective_tflops": fb.flops / (t * 1e-3) / 1e12,
                                 "tokens_per_s": fb.tokens / (t * 1e-3), "launches_per_step": layers}
     return rows
@@ -642,7 +642,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--only-row", choices=["bigbird_16k", "long_topk_64k", "cas_heads_8k", "fib_8k_16_layers",
-                                           "fib_8k_2_layers"], default=None,
+                                           "fib_8k_coprime_16_layers", "pow2_8k_16_layers", "fib_8k_2_layers"],
+                    default=None,
                     help="time one other hot-path row only (profiling aid; prints that row, not the bench line)")
     args = ap.parse_args()
     if args.warmup < 3:

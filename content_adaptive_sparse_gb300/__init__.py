@@ -6,8 +6,7 @@ work of the hot path runs in the library's CUDA kernels. There is no CPU fallbac
 if the library is missing or the device is not an sm_103 GPU, calls raise.
 
 Names follow the C ABI: ``sa_build_mask``, ``sa_attn_fwd``, ``sa_attn_fwd_heads``,
-``sa_offset_attn_fwd``,
-``sa_fib_offsets``, ``sa_block_ratios``, ``sa_mask_nnz_bound``, ``sa_device_status``.
+``sa_offset_attn_fwd``, ``sa_fib_offsets``, ``sa_pow2_offsets``, ``sa_layer_alpha``, ``sa_block_ratios``, ``sa_mask_nnz_bound``, ``sa_device_status``.
 """
 from __future__ import annotations
 
@@ -69,11 +68,13 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
                                        ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P,
                                        ctypes.c_int32, ctypes.c_float, _P, _P, _P]
     lib.sa_fib_offsets.argtypes = [ctypes.c_int32] * 5 + [_P, ctypes.c_int32, _P]
+    lib.sa_pow2_offsets.argtypes = [ctypes.c_int32] * 5 + [_P, ctypes.c_int32, _P]
+    lib.sa_layer_alpha.argtypes = [ctypes.c_int32] * 7 + [_P, _P]
     lib.sa_block_ratios.argtypes = [_P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P,
                                     ctypes.c_int32]
     lib.sa_device_status.argtypes = [_P]
     for name in ("sa_mask_nnz_bound", "sa_build_mask", "sa_attn_fwd", "sa_attn_fwd_heads", "sa_offset_attn_fwd",
-                 "sa_fib_offsets", "sa_block_ratios", "sa_device_status"):
+                 "sa_fib_offsets", "sa_pow2_offsets", "sa_layer_alpha", "sa_block_ratios", "sa_device_status"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -160,12 +161,28 @@ def sa_offset_attn_fwd(q, k, v, window: int, offsets, o, lse, softmax_scale: flo
         _stream_ptr(stream)))
 
 
-def sa_fib_offsets(alpha_num: int, alpha_den: int, n_rungs: int, window: int, n_tokens: int) -> list[int]:
+def _ladder(fn: str, alpha_num: int, alpha_den: int, n_rungs: int, window: int, n_tokens: int) -> list[int]:
     buf = (ctypes.c_int32 * 128)()
     cnt = ctypes.c_int32(0)
-    _check("sa_fib_offsets", load_library().sa_fib_offsets(alpha_num, alpha_den, n_rungs, window, n_tokens,
-                                                            ctypes.cast(buf, _P), 128, ctypes.byref(cnt)))
+    _check(fn, getattr(load_library(), fn)(alpha_num, alpha_den, n_rungs, window, n_tokens, ctypes.cast(buf, _P), 128,
+                                           ctypes.byref(cnt)))
     return [int(buf[i]) for i in range(cnt.value)]
+
+
+def sa_fib_offsets(alpha_num: int, alpha_den: int, n_rungs: int, window: int, n_tokens: int) -> list[int]:
+    return _ladder("sa_fib_offsets", alpha_num, alpha_den, n_rungs, window, n_tokens)
+
+
+def sa_pow2_offsets(alpha_num: int, alpha_den: int, n_rungs: int, window: int, n_tokens: int) -> list[int]:
+    return _ladder("sa_pow2_offsets", alpha_num, alpha_den, n_rungs, window, n_tokens)
+
+
+def sa_layer_alpha(layer: int, layers: int, lo=(1, 2), hi=(3, 2), stride: int = 1) -> tuple[int, int]:
+    """(numerator, denominator) of the layer's alpha (linear ramp, coprime ``stride``)."""
+    num, den = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check("sa_layer_alpha", load_library().sa_layer_alpha(layer, layers, lo[0], lo[1], hi[0], hi[1], stride,
+                                                            ctypes.byref(num), ctypes.byref(den)))
+    return int(num.value), int(den.value)
 
 
 def sa_block_ratios(data: np.ndarray, block: int, level: int = 6, n_threads: int = 0) -> np.ndarray:
@@ -228,6 +245,6 @@ def offset_attn_fwd(q, k, v, window: int, offsets, softmax_scale: float | None =
 
 __all__ = [
     "build_library", "load_library", "SAError", "MaskParams", "mask_params", "sa_mask_nnz_bound", "sa_build_mask",
-    "sa_attn_fwd", "sa_attn_fwd_heads", "attn_fwd_heads", "LITERAL_LOCAL", "LITERAL_PAIRS", "sa_offset_attn_fwd", "sa_fib_offsets", "sa_block_ratios", "sa_device_status", "build_mask",
+    "sa_attn_fwd", "sa_attn_fwd_heads", "sa_pow2_offsets", "sa_layer_alpha", "attn_fwd_heads", "LITERAL_LOCAL", "LITERAL_PAIRS", "sa_offset_attn_fwd", "sa_fib_offsets", "sa_block_ratios", "sa_device_status", "build_mask",
     "attn_fwd", "offset_attn_fwd", "MASK_TOPK", "MASK_BIGBIRD", "MASK_FULL", "MASK_LITERAL_MEAN",
 ]

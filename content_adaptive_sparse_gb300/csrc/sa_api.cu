@@ -5,6 +5,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <numeric>
 #include <atomic>
 #include <thread>
 #include <vector>
@@ -274,8 +275,14 @@ int sa_offset_attn_fwd(const void* q, const void* k, const void* v, const int64_
   return sa::launch_offset_attn_fwd(a, static_cast<cudaStream_t>(stream));
 }
 
-int sa_fib_offsets(int32_t alpha_num, int32_t alpha_den, int32_t n_rungs, int32_t window, int32_t n_tokens,
-                   int32_t* h_out, int32_t capacity, int32_t* h_count) {
+}  // extern "C"
+
+namespace {
+
+// Distinct round_half_even(alpha * f) over a rung ladder, kept if window < d < n_tokens.
+// ladder 0: Fibonacci 1, 2, 3, 5, ...; ladder 1: powers of two.
+int ladder_offsets(int ladder, int32_t alpha_num, int32_t alpha_den, int32_t n_rungs, int32_t window,
+                   int32_t n_tokens, int32_t* h_out, int32_t capacity, int32_t* h_count) {
   if (alpha_num <= 0 || alpha_den <= 0 || n_rungs < 0 || window < 0 || n_tokens <= 0 || !h_count ||
       capacity < 0 || (capacity > 0 && !h_out))
     return SA_ERR_INVALID_ARG;
@@ -289,15 +296,55 @@ int sa_fib_offsets(int32_t alpha_num, int32_t alpha_den, int32_t n_rungs, int32_
     int64_t q = num / den2;
     if (num % den2 == 0 && (q & 1)) --q;   // exact tie: go to the even neighbour
     if (q > window && q < n_tokens && std::find(out.begin(), out.end(), q) == out.end()) out.push_back(q);
-    const int64_t nxt = a + b;
-    a = b;
-    b = nxt;
+    if (ladder == 0) {
+      const int64_t nxt = a + b;
+      a = b;
+      b = nxt;
+    } else {
+      a *= 2;
+    }
     if (a > (int64_t)1 << 40) break;
   }
   std::sort(out.begin(), out.end());
   *h_count = (int32_t)out.size();
   if ((int64_t)out.size() > capacity) return SA_ERR_CAPACITY;
   for (size_t i = 0; i < out.size(); ++i) h_out[i] = (int32_t)out[i];
+  return SA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int sa_fib_offsets(int32_t alpha_num, int32_t alpha_den, int32_t n_rungs, int32_t window, int32_t n_tokens,
+                   int32_t* h_out, int32_t capacity, int32_t* h_count) {
+  return ladder_offsets(0, alpha_num, alpha_den, n_rungs, window, n_tokens, h_out, capacity, h_count);
+}
+
+int sa_pow2_offsets(int32_t alpha_num, int32_t alpha_den, int32_t n_rungs, int32_t window, int32_t n_tokens,
+                    int32_t* h_out, int32_t capacity, int32_t* h_count) {
+  return ladder_offsets(1, alpha_num, alpha_den, n_rungs, window, n_tokens, h_out, capacity, h_count);
+}
+
+int sa_layer_alpha(int32_t layer, int32_t layers, int32_t lo_num, int32_t lo_den, int32_t hi_num, int32_t hi_den,
+                   int32_t stride, int32_t* h_num, int32_t* h_den) {
+  if (layers <= 0 || layer < 0 || layer >= layers || lo_den <= 0 || hi_den <= 0 || stride <= 0 || !h_num ||
+      !h_den)
+    return SA_ERR_INVALID_ARG;
+  if (std::gcd(stride, layers) != 1) return SA_ERR_INVALID_ARG;
+  const int64_t i = ((int64_t)stride * layer) % layers;
+  // lo + (hi - lo) * i / (L - 1) = (lo_num hi_den (L-1) + (hi_num lo_den - lo_num hi_den) i) / (lo_den hi_den (L-1))
+  const int64_t span = layers > 1 ? layers - 1 : 1;
+  int64_t num = (int64_t)lo_num * hi_den * span + ((int64_t)hi_num * lo_den - (int64_t)lo_num * hi_den) * i;
+  int64_t den = (int64_t)lo_den * hi_den * span;
+  const int64_t g = std::gcd(num < 0 ? -num : num, den);
+  if (g > 1) {
+    num /= g;
+    den /= g;
+  }
+  if (num <= 0 || num > INT32_MAX || den > INT32_MAX) return SA_ERR_UNSUPPORTED;
+  *h_num = (int32_t)num;
+  *h_den = (int32_t)den;
   return SA_OK;
 }
 

@@ -166,6 +166,20 @@ int sa_offset_attn_fwd(const void* q, const void* k, const void* v, const int64_
 int sa_fib_offsets(int32_t alpha_num, int32_t alpha_den, int32_t n_rungs, int32_t window, int32_t n_tokens,
                    int32_t* h_out, int32_t capacity, int32_t* h_count);
 
+/* sa_fib_offsets over the power-of-2 control base f = 1, 2, 4, 8, ... (same section,
+ * "Control base": reach-matched to the Fibonacci base, 11 rungs up to 1024). */
+int sa_pow2_offsets(int32_t alpha_num, int32_t alpha_den, int32_t n_rungs, int32_t window, int32_t n_tokens,
+                    int32_t* h_out, int32_t capacity, int32_t* h_count);
+
+/* Per-layer scale of the staggered schedules (same page, section 2 "The per-layer
+ * scalar"): the linear ramp a_i = lo + (hi - lo) * i / (layers - 1), lo = lo_num/lo_den,
+ * hi = hi_num/hi_den; layer `layer` takes a_i with i = (stride * layer) mod layers
+ * (stride 1: linear stagger; stride 7 with 16 layers: the coprime stagger). Writes the
+ * reduced fraction to *h_num / *h_den. stride must be >= 1 and coprime to layers.
+ * Host only. */
+int sa_layer_alpha(int32_t layer, int32_t layers, int32_t lo_num, int32_t lo_den, int32_t hi_num, int32_t hi_den,
+                   int32_t stride, int32_t* h_num, int32_t* h_den);
+
 /* Per-block compression ratios r_i = |zlib(x[i*b:(i+1)*b], level)| / b of a host byte
  * array h_bytes [batch][n_tokens] ("Parameter-free Adaptive Sparse Attention ...",
  * section 3.1 Eq. 1; zlib framing instead of gzip shifts every length by the same

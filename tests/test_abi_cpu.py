@@ -2,6 +2,7 @@
 symbol include/sa_api.h declares, and its host-only entry points (size bound,
 Fibonacci offsets, zlib ratios, argument validation) agree with the oracle."""
 import ctypes
+import math
 import os
 import re
 from fractions import Fraction
@@ -31,7 +32,8 @@ def _declared_functions():
 
 def test_header_symbols_exported(lib):
     names = _declared_functions()
-    assert {"sa_build_mask", "sa_attn_fwd", "sa_attn_fwd_heads", "sa_offset_attn_fwd", "sa_fib_offsets", "sa_block_ratios",
+    assert {"sa_build_mask", "sa_attn_fwd", "sa_attn_fwd_heads", "sa_offset_attn_fwd", "sa_pow2_offsets",
+            "sa_layer_alpha", "sa_fib_offsets", "sa_block_ratios",
             "sa_mask_nnz_bound", "sa_device_status", "sa_status_string", "sa_version"} <= set(names)
     for n in names:
         assert hasattr(lib, n), n
@@ -58,6 +60,25 @@ def test_fib_offsets_match_oracle(lib):
                     assert got == want
                     want_all = [d for d in oracle.fib_offsets(alpha, oracle.fib_rungs_upto(n)) if W < d < n]
                     assert sa.sa_fib_offsets(alpha.numerator, alpha.denominator, 0, W, n) == want_all
+
+
+def test_pow2_offsets_and_layer_alpha_match_oracle(lib):
+    for lo, hi in (((1, 2), (2, 1)), ((1, 2), (3, 2))):
+        for stride in (1, 7, 3):
+            want_alphas = oracle.alpha_schedule(16, lo, hi, stride=stride)
+            for l in range(16):
+                num, den = sa.sa_layer_alpha(l, 16, lo, hi, stride)
+                assert Fraction(num, den) == want_alphas[l] and math.gcd(num, den) == 1
+        for alpha in oracle.alpha_schedule(16, lo, hi):
+            for W in (6, 8, 12):
+                for n in (2048, 8192):
+                    want = [d for d in oracle.fib_offsets(alpha, oracle.pow2_rungs(11)) if W < d < n]
+                    assert sa.sa_pow2_offsets(alpha.numerator, alpha.denominator, 11, W, n) == want
+                    want_all = [d for d in oracle.fib_offsets(alpha, oracle.pow2_rungs_upto(n)) if W < d < n]
+                    assert sa.sa_pow2_offsets(alpha.numerator, alpha.denominator, 0, W, n) == want_all
+    # a stride sharing a factor with the layer count is refused
+    num, den = ctypes.c_int32(0), ctypes.c_int32(0)
+    assert lib.sa_layer_alpha(0, 16, 1, 2, 3, 2, 4, ctypes.byref(num), ctypes.byref(den)) == -1
 
 
 def _params(p: om.MaskParams, batch: int):

@@ -12,14 +12,18 @@ from gpu_helpers import assert_attention_close, bf16_to_f64, to_dev, torch_cuda
 pytestmark = pytest.mark.gpu
 
 
-def _run(bt, n, h, hkv, window, alpha: Fraction, n_rungs=15, seed=0, qmul=1.0):
+def _run(bt, n, h, hkv, window, alpha: Fraction, n_rungs=15, seed=0, qmul=1.0, ladder="fib"):
     torch = torch_cuda()
     rng = np.random.default_rng(seed)
     qb = bf16_normal_bits(rng, (bt, n, h, 64), 0.125 * qmul)
     kb = bf16_normal_bits(rng, (bt, n, hkv, 64), 0.125)
     vb = bf16_normal_bits(rng, (bt, n, hkv, 64), 0.125)
-    offs = sa.sa_fib_offsets(alpha.numerator, alpha.denominator, n_rungs, window, n)
-    rungs = oracle.fib_rungs(n_rungs) if n_rungs else oracle.fib_rungs_upto(n)
+    if ladder == "fib":
+        offs = sa.sa_fib_offsets(alpha.numerator, alpha.denominator, n_rungs, window, n)
+        rungs = oracle.fib_rungs(n_rungs) if n_rungs else oracle.fib_rungs_upto(n)
+    else:
+        offs = sa.sa_pow2_offsets(alpha.numerator, alpha.denominator, n_rungs, window, n)
+        rungs = oracle.pow2_rungs(n_rungs) if n_rungs else oracle.pow2_rungs_upto(n)
     assert offs == [d for d in oracle.fib_offsets(alpha, rungs) if window < d < n]
     o, lse = sa.offset_attn_fwd(to_dev(qb), to_dev(kb), to_dev(vb), window, offs)
     torch.cuda.synchronize()
@@ -38,6 +42,15 @@ def test_windows_mid_alpha(window):
 @pytest.mark.parametrize("alpha", [Fraction(1, 2), Fraction(1, 1), Fraction(3, 2), Fraction(2, 1)])
 def test_alpha_range_gqa(alpha):
     _run(1, 2048, 4, 2, 8, alpha, seed=3)
+
+
+@pytest.mark.parametrize("layer", [0, 1, 9, 15])
+def test_pow2_base_coprime_stagger(layer):
+    """Power-of-2 control rungs with the coprime-staggered alpha of a layer."""
+    num, den = sa.sa_layer_alpha(layer, 16, (1, 2), (3, 2), 7)
+    alpha = Fraction(num, den)
+    assert alpha == oracle.alpha_schedule(16, (1, 2), (3, 2), stride=7)[layer]
+    _run(1, 2048, 4, 2, 8, alpha, n_rungs=11, seed=20 + layer, qmul=3.0, ladder="pow2")
 
 
 def test_all_rungs_up_to_n_and_ragged_tail():

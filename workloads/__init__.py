@@ -24,6 +24,8 @@ Workloads (shapes and pattern parameters as the pages and the task state them):
                        groups: 6 local, 3 long-range (literal pairs), 3 hybrid (the
                        Parameter-free Adaptive Sparse Attention page, section 4.1,
                        Table 8 and Appendix B "Head-specific mask distribution").
+* ``fib_8k_coprime`` / ``pow2_8k`` - ``fib_8k`` with the coprime stagger of the alpha
+                       ramp, and with the power-of-2 control base (same page, section 2).
 * ``long_topk_64k``  - 1 x 65536 byte tokens, block 128, 16 heads, d_h 128, top-64
                        (top-k swept over 16/64/256), plus ``full_16k``.
 
@@ -68,6 +70,13 @@ WORKLOADS = {
                          head_dim=64, window_blocks=1, causal=1, zlib_level=1,
                          head_components=(1, 1, 1, 1, 1, 1, 2, 2, 2, 3, 3, 3),
                          std=1.0 / 8.0, bytes="zipf_text", seed=48),
+    # schedule variants of fib_8k: coprime alpha stagger (layer l takes ramp index 7l mod 16)
+    # and the power-of-2 control base (11 rungs up to 1024)
+    "fib_8k_coprime": dict(kind="fib", layers=16, batch=8, n_tokens=8192, heads=8, kv_heads=8, head_dim=64,
+                           window=8, alpha_lo=(1, 2), alpha_hi=(2, 1), n_rungs=15, stride=7, std=1.0 / 8.0,
+                           seed=46),
+    "pow2_8k": dict(kind="fib", layers=16, batch=8, n_tokens=8192, heads=8, kv_heads=8, head_dim=64, window=8,
+                    alpha_lo=(1, 2), alpha_hi=(2, 1), n_rungs=11, ladder="pow2", std=1.0 / 8.0, seed=46),
     "long_topk_64k": dict(kind="topk", batch=1, n_tokens=65536, block=128, heads=16, kv_heads=16,
                           head_dim=128, window_blocks=4, global_blocks=1, topk=64, causal=1,
                           std=1.0 / np.sqrt(128.0), bytes="phrase_random", seed=47),
