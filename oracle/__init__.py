@@ -31,7 +31,8 @@ from .masks import (MaskParams, build_csr, csr_topk_rows, csr_bigbird_rows, csr_
 from .fib import (fib_rungs, fib_rungs_upto, pow2_rungs, pow2_rungs_upto, alpha_schedule, fib_offsets,
                   offset_key_set)
 from .attention import (attention_csr, attention_csr_block, attention_csr_heads, attention_offsets,
-                        dense_masked_attention, attention_rows_csr)
+                        dense_masked_attention, attention_rows_csr, attention_csr_backward, attention_rows_dq,
+                        attention_rows_dkdv)
 
 __all__ = [
     "block_ratios", "zlib_version", "philox4x64_10", "philox_word", "MaskParams", "build_csr",
@@ -40,5 +41,6 @@ __all__ = [
     "cas_head_components", "LOCAL", "LITERAL", "attention_csr_heads",
     "fib_rungs", "fib_rungs_upto", "pow2_rungs", "pow2_rungs_upto", "alpha_schedule", "fib_offsets", "offset_key_set", "attention_csr",
     "attention_csr_block",
-    "attention_offsets", "dense_masked_attention", "attention_rows_csr",
+    "attention_offsets", "dense_masked_attention", "attention_rows_csr", "attention_csr_backward",
+    "attention_rows_dq", "attention_rows_dkdv",
 ]

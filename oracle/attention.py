@@ -186,3 +186,114 @@ def dense_masked_attention(q, k, v, token_mask: np.ndarray, scale: float | None 
             o[s, :, hh, :] = p @ v[s, :, hk, :]
             lse[s, hh, :] = l
     return o, lse
+
+
+def attention_csr_backward(q, k, v, d_o, row_ptr, col_idx, block: int, causal: int, scale: float | None = None,
+                           convert=None):
+    """Gradients of L = sum(dO * O) for block-CSR attention, from the definitions.
+
+    For query i with allowed keys S(i) (same token rule as ``attention_csr``):
+        P_ij   = exp(s_ij - LSE_i)
+        dV_j  += sum_i P_ij dO_i
+        dP_ij  = <dO_i, v_j>
+        dS_ij  = P_ij (dP_ij - sum_{l in S(i)} P_il dP_il)
+        dQ_i   = scale * sum_j dS_ij k_j
+        dK_j  += scale * sum_i dS_ij q_i
+    With grouped-query attention, dK / dV of a key/value head sum over the query heads
+    that read it. Returns dq [batch, tokens, heads, d], dk and dv [batch, tokens,
+    kv_heads, d], float64.
+    """
+    cv = convert if convert is not None else (lambda x: x)
+    bt, n, h, d = q.shape
+    hkv = k.shape[2]
+    nb = n // block
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    dq = np.zeros((bt, n, h, d))
+    dk = np.zeros((bt, n, hkv, d))
+    dv = np.zeros((bt, n, hkv, d))
+    for s in range(bt):
+        cs = _csr_batch(row_ptr, s)
+        for I in range(nb):
+            row = col_idx[row_ptr[cs, I]:row_ptr[cs, I + 1]]
+            if len(row) == 0:
+                continue
+            keys = np.concatenate([np.arange(J * block, (J + 1) * block) for J in row])
+            qi = np.arange(I * block, (I + 1) * block)
+            allowed = keys[None, :] <= qi[:, None] if causal else np.ones((block, len(keys)), dtype=bool)
+            for hh in range(h):
+                hk = hh // (h // hkv)
+                Q = cv(q[s, qi, hh, :])
+                K = cv(k[s, keys, hk, :])
+                V = cv(v[s, keys, hk, :])
+                dO = cv(d_o[s, qi, hh, :])
+                sc = np.where(allowed, (Q @ K.T) * scale, -np.inf)
+                P, _ = _softmax_rows(sc)
+                dP = dO @ V.T
+                dS = P * (dP - np.sum(P * dP, axis=1, keepdims=True))
+                dq[s, qi, hh, :] += scale * (dS @ K)
+                np.add.at(dk[s, :, hk, :], keys, scale * (dS.T @ Q))
+                np.add.at(dv[s, :, hk, :], keys, P.T @ dO)
+    return dq, dk, dv
+
+
+def attention_rows_dq(q, k, v, d_o, row_ptr, col_idx, block: int, causal: int, samples,
+                      scale: float | None = None, convert=None):
+    """dQ_i of the backward above at sampled (batch, token, head) triples."""
+    cv = convert if convert is not None else (lambda x: x)
+    d = q.shape[3]
+    h, hkv = q.shape[2], k.shape[2]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    out = np.zeros((len(samples), d))
+    for t, (s, i, hh) in enumerate(samples):
+        cs = _csr_batch(row_ptr, s)
+        I = i // block
+        row = col_idx[row_ptr[cs, I]:row_ptr[cs, I + 1]]
+        keys = [j for J in row for j in range(J * block, (J + 1) * block) if not causal or j <= i]
+        if not keys:
+            continue
+        hk = hh // (h // hkv)
+        K = cv(k[s, keys, hk, :])
+        V = cv(v[s, keys, hk, :])
+        P, _ = _softmax_rows(((K @ cv(q[s, i, hh, :])) * scale)[None, :])
+        dP = V @ cv(d_o[s, i, hh, :])
+        dS = P[0] * (dP - np.sum(P[0] * dP))
+        out[t] = scale * (dS @ K)
+    return out
+
+
+def attention_rows_dkdv(q, k, v, d_o, row_ptr, col_idx, block: int, causal: int, samples,
+                        scale: float | None = None, convert=None):
+    """dK_j and dV_j of the backward above at sampled (batch, token, kv head) triples:
+    sums over every query (of every query head of the group) whose key set holds j."""
+    cv = convert if convert is not None else (lambda x: x)
+    n, h, d = q.shape[1], q.shape[2], q.shape[3]
+    hkv = k.shape[2]
+    nb = n // block
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    dk = np.zeros((len(samples), d))
+    dv = np.zeros((len(samples), d))
+    for t, (s, j, hk) in enumerate(samples):
+        cs = _csr_batch(row_ptr, s)
+        J = j // block
+        q_blocks = [I for I in range(nb) if J in set(col_idx[row_ptr[cs, I]:row_ptr[cs, I + 1]].tolist())]
+        for I in q_blocks:
+            row = col_idx[row_ptr[cs, I]:row_ptr[cs, I + 1]]
+            for i in range(I * block, (I + 1) * block):
+                if causal and j > i:
+                    continue
+                keys = [x for Jr in row for x in range(Jr * block, (Jr + 1) * block) if not causal or x <= i]
+                pos = keys.index(j)
+                for hh in range(hk * (h // hkv), (hk + 1) * (h // hkv)):
+                    K = cv(k[s, keys, hk, :])
+                    V = cv(v[s, keys, hk, :])
+                    qv = cv(q[s, i, hh, :])
+                    dov = cv(d_o[s, i, hh, :])
+                    P, _ = _softmax_rows(((K @ qv) * scale)[None, :])
+                    dP = V @ dov
+                    dS = P[0] * (dP - np.sum(P[0] * dP))
+                    dk[t] += scale * dS[pos] * qv
+                    dv[t] += P[0][pos] * dov
+    return dk, dv

@@ -486,3 +486,86 @@ def test_cas_workload_uses_page_head_split():
     cfg = _wl("cas_heads_8k")
     assert list(cfg["head_components"]) == oracle.cas_head_components(cfg["heads"])
     assert cfg["block"] == 128 and cfg["window_blocks"] == 1 and cfg["zlib_level"] == 1   # [CAS] Table 8
+
+
+# ------------------------------------------------------------------ backward
+
+def _tiny_backward_case(seed, causal, hkv=1):
+    rng = np.random.default_rng(seed)
+    bt, n, h, d, b = 1, 48, 2, 4, 8
+    q, k, v, do = (rng.standard_normal((bt, n, hh, d)) for hh in (h, hkv, hkv, h))
+    rows = [[0], [0, 1], [1, 2], [0, 3], [2, 4], [0, 4, 5]] if causal else \
+        [[0, 3], [1, 5], [0, 1, 2], [4], [2, 4, 5], [0, 5]]
+    rp = np.zeros((1, len(rows) + 1), dtype=np.int32)
+    cols = []
+    for I, r in enumerate(rows):
+        cols += r
+        rp[0, I + 1] = len(cols)
+    return q, k, v, do, rp, np.array(cols, dtype=np.int32), b
+
+
+@pytest.mark.parametrize("causal,hkv", [(1, 1), (0, 2), (1, 2)])
+def test_backward_matches_central_differences(causal, hkv):
+    """dQ, dK, dV of L = sum(dO * O) against central differences of the forward oracle."""
+    q, k, v, do, rp, ci, b = _tiny_backward_case(11 + causal + hkv, causal, hkv)
+    dq, dk, dv = oracle.attention_csr_backward(q, k, v, do, rp, ci, b, causal)
+
+    def loss(qq, kk, vv):
+        o, _ = oracle.attention_csr(qq, kk, vv, rp, ci, b, causal)
+        return float(np.sum(o * do))
+
+    eps = 1e-6
+    rng = np.random.default_rng(0)
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        flat = x.reshape(-1)
+        for idx in rng.choice(flat.size, size=40, replace=False):
+            old = flat[idx]
+            flat[idx] = old + eps
+            lp = loss(q, k, v)
+            flat[idx] = old - eps
+            lm = loss(q, k, v)
+            flat[idx] = old
+            fd = (lp - lm) / (2 * eps)
+            assert abs(fd - g.reshape(-1)[idx]) < 1e-7 * max(1.0, abs(fd)), (name, idx)
+
+
+def test_backward_matches_torch_autograd_dense_route():
+    """The same gradients from torch autograd through a dense N x N masked softmax."""
+    torch = pytest.importorskip("torch")
+    q, k, v, do, rp, ci, b = _tiny_backward_case(5, 1, 1)
+    n, g = q.shape[1], q.shape[2] // k.shape[2]
+    tok = om.block_mask_to_token_mask(om.csr_to_block_mask(rp, ci, n // b), b, 1)
+    dq, dk, dv = oracle.attention_csr_backward(q, k, v, do, rp, ci, b, 1)
+    tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+    kk = tk.repeat_interleave(g, dim=2)
+    vv = tv.repeat_interleave(g, dim=2)
+    s = torch.einsum("bihd,bjhd->bhij", tq, kk) / np.sqrt(q.shape[3])
+    s = s.masked_fill(~torch.tensor(tok), float("-inf"))
+    o = torch.einsum("bhij,bjhd->bihd", torch.softmax(s, dim=-1), vv)
+    o.backward(torch.tensor(do))
+    assert np.abs(tq.grad.numpy() - dq).max() < 1e-12
+    assert np.abs(tk.grad.numpy() - dk).max() < 1e-12
+    assert np.abs(tv.grad.numpy() - dv).max() < 1e-12
+
+
+def test_backward_invariants_and_sampled_forms():
+    """Softmax rows of dS sum to zero, so dK sums to zero over the keys of each
+    (sequence, kv head); dV sums to the sum of dO over queries with a key. The sampled
+    evaluators agree with the full backward."""
+    rng = np.random.default_rng(21)
+    bt, n, h, hkv, d, b = 2, 256, 4, 2, 8, 32
+    q, k, v, do = (rng.standard_normal((bt, n, hh, d)) for hh in (h, hkv, hkv, h))
+    ratios = rng.integers(20, 60, (bt, n // b)) / np.float32(b)
+    p = om.MaskParams("topk", b, n, 1, 2, 1, 2)
+    rp, ci = om.build_csr(p, ratios, bt)
+    dq, dk, dv = oracle.attention_csr_backward(q, k, v, do, rp, ci, b, 1)
+    assert np.abs(dk.sum(axis=1)).max() < 1e-11
+    want_dv = do.reshape(bt, n, hkv, h // hkv, d).sum(axis=(1, 3))
+    assert np.abs(dv.sum(axis=1) - want_dv).max() < 1e-11
+    smp = [(0, 0, 0), (1, 255, 3), (0, 100, 2), (1, 33, 1)]
+    got = oracle.attention_rows_dq(q, k, v, do, rp, ci, b, 1, smp)
+    assert np.abs(got - np.stack([dq[s, i, hh] for s, i, hh in smp])).max() < 1e-12
+    smp_kv = [(0, 0, 0), (1, 255, 1), (0, 70, 1), (1, 31, 0)]
+    gk, gv = oracle.attention_rows_dkdv(q, k, v, do, rp, ci, b, 1, smp_kv)
+    assert np.abs(gk - np.stack([dk[s, j, hk] for s, j, hk in smp_kv])).max() < 1e-12
+    assert np.abs(gv - np.stack([dv[s, j, hk] for s, j, hk in smp_kv])).max() < 1e-12
