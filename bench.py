@@ -571,6 +571,8 @@ def _measure_rows(torch, sa, dev, flush, peaks, max_over_ranks, only=None, steps
         rows.update(_row_long(torch, dev, flush, peaks, max_over_ranks, steps, warm))
     if want("cas_heads_8k"):
         rows.update(_row_block_sparse(torch, dev, flush, peaks, max_over_ranks, steps, warm, "cas_heads_8k"))
+    if want("bwd_bytelm_topk_8k"):
+        rows.update(_row_bwd(torch, dev, flush, peaks, max_over_ranks, steps, warm))
     if want("fib_8k_16_layers"):
         rows.update(_row_fib(torch, dev, flush, peaks, max_over_ranks, steps, warm))
     if want("fib_8k_coprime_16_layers"):
@@ -619,6 +621,35 @@ def _row_block_sparse(torch, dev, flush, peaks, max_over_ranks, steps, warm, nam
                    "tokens_per_s": case.tokens / (tot * 1e-3), "edges": case.edges}}
 
 
+def _row_bwd(torch, dev, flush, peaks, max_over_ranks, steps, warm, name="bytelm_topk_8k"):
+    """Backward of the compression-guided workload: D = rowsum(dO * O), the transposed
+    CSR, dQ and dK / dV (one sa_attn_bwd call). Effective FLOP = 2.5 x the forward's
+    4 * edges * d (five products of edges x d instead of two)."""
+    import numpy as np
+
+    from workloads import bf16_normal_bits
+    case = BlockSparseCase(name, dev)
+    torch.cuda.synchronize()
+    dob = bf16_normal_bits(np.random.default_rng(77), tuple(case.q.shape), case.cfg["std"])
+    d_o = torch.from_numpy(dob.view(np.int16)).view(torch.bfloat16).to(dev)
+    dq, dk, dv = torch.empty_like(case.q), torch.empty_like(case.k), torch.empty_like(case.v)
+    b, n, h, _ = case.q.shape
+    ws_bytes = case.sa.sa_attn_bwd_workspace_size(b, n, h, case.block, case.params.batch, case.col_idx.numel())
+    ws = torch.empty((ws_bytes,), dtype=torch.uint8, device=dev)
+
+    def bwd():
+        case.sa.sa_attn_bwd(case.q, case.k, case.v, case.o, d_o, case.lse, case.row_ptr, case.col_idx, case.block,
+                            case.causal, dq, dk, dv, ws, case.csr_shared)
+
+    seg, tot = _time_events(torch, [bwd], steps, warm, flush)
+    t = max_over_ranks(tot)
+    flops = 2.5 * case.flops
+    return {f"bwd_{name}": {"ms_per_step": t, "effective_tflops": flops / (t * 1e-3) / 1e12,
+                            "frac_bf16_peak": flops / (t * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                            "tokens_per_s": case.tokens / (t * 1e-3), "edges": case.edges,
+                            "launches_per_step": 6}}
+
+
 def _row_fib(torch, dev, flush, peaks, max_over_ranks, steps, warm, layers=16, name="fib_8k"):
     rows = {}
     # 16-layer Fibonacci pass at 8K (HBM roofline)
@@ -641,7 +672,8 @@ def main():
     ap.add_argument("--no-rows", action="store_true", help="skip the other hot-path rows")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--only-row", choices=["bigbird_16k", "long_topk_64k", "cas_heads_8k", "fib_8k_16_layers",
+    ap.add_argument("--only-row", choices=["bigbird_16k", "long_topk_64k", "cas_heads_8k", "bwd_bytelm_topk_8k",
+                                           "fib_8k_16_layers",
                                            "fib_8k_coprime_16_layers", "pow2_8k_16_layers", "fib_8k_2_layers"],
                     default=None,
                     help="time one other hot-path row only (profiling aid; prints that row, not the bench line)")

@@ -64,6 +64,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                       ctypes.c_int32, ctypes.c_int32, _P, _P, _P, ctypes.c_int32, ctypes.c_float,
                                       _P, _P, _P]
+    lib.sa_attn_bwd_workspace_size.argtypes = [ctypes.c_int32] * 5 + [ctypes.c_int64, _P]
+    lib.sa_attn_bwd.argtypes = [_P, _P, _P, _P, _P, _P, _I64x3, _I64x3, _I64x3] + [ctypes.c_int32] * 7 + \
+        [_P, _P, ctypes.c_int32, ctypes.c_float, _P, _P, _P, _P, ctypes.c_size_t, _P]
     lib.sa_offset_attn_fwd.argtypes = [_P, _P, _P, _I64x3, _I64x3, _I64x3, ctypes.c_int32, ctypes.c_int32,
                                        ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P,
                                        ctypes.c_int32, ctypes.c_float, _P, _P, _P]
@@ -73,7 +76,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.sa_block_ratios.argtypes = [_P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P,
                                     ctypes.c_int32]
     lib.sa_device_status.argtypes = [_P]
-    for name in ("sa_mask_nnz_bound", "sa_build_mask", "sa_attn_fwd", "sa_attn_fwd_heads", "sa_offset_attn_fwd",
+    for name in ("sa_mask_nnz_bound", "sa_build_mask", "sa_attn_fwd", "sa_attn_fwd_heads", "sa_attn_bwd",
+                 "sa_attn_bwd_workspace_size", "sa_offset_attn_fwd",
                  "sa_fib_offsets", "sa_pow2_offsets", "sa_layer_alpha", "sa_block_ratios", "sa_device_status"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
@@ -147,6 +151,29 @@ def sa_attn_fwd_heads(q, k, v, csrs, head_mask, block: int, causal: int, o, lse,
         q.data_ptr(), k.data_ptr(), v.data_ptr(), _strides(q), _strides(k), _strides(o), b, n, h, hkv, d, block,
         int(causal), nm, ctypes.cast(rps, _P), ctypes.cast(cis, _P), hm.ctypes.data, int(bool(csr_shared)), scale,
         o.data_ptr(), lse.data_ptr(), _stream_ptr(stream)))
+
+
+def sa_attn_bwd_workspace_size(batch: int, n_tokens: int, heads: int, block: int, csr_batches: int,
+                               col_capacity: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check("sa_attn_bwd_workspace_size", load_library().sa_attn_bwd_workspace_size(
+        batch, n_tokens, heads, block, csr_batches, col_capacity, ctypes.byref(out)))
+    return int(out.value)
+
+
+def sa_attn_bwd(q, k, v, o, d_o, lse, row_ptr, col_idx, block: int, causal: int, dq, dk, dv, workspace,
+                csr_shared: bool = False, softmax_scale: float | None = None, stream=None) -> None:
+    b, n, h, d = q.shape
+    hkv = k.shape[2]
+    scale = 1.0 / float(np.sqrt(d)) if softmax_scale is None else float(softmax_scale)
+    if _strides(d_o)[:] != _strides(o)[:] or _strides(dq)[:] != _strides(q)[:] or \
+            _strides(dk)[:] != _strides(k)[:] or _strides(dv)[:] != _strides(v)[:]:
+        raise ValueError("d_o / dq / dk / dv must have the strides of o / q / k / v")
+    _check("sa_attn_bwd", load_library().sa_attn_bwd(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), d_o.data_ptr(), lse.data_ptr(), _strides(q),
+        _strides(k), _strides(o), b, n, h, hkv, d, block, int(causal), row_ptr.data_ptr(), col_idx.data_ptr(),
+        int(bool(csr_shared)), scale, dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
 
 
 def sa_offset_attn_fwd(q, k, v, window: int, offsets, o, lse, softmax_scale: float | None = None,
@@ -234,6 +261,18 @@ def attn_fwd_heads(q, k, v, csrs, head_mask, block: int, causal: int, csr_shared
     return o, lse
 
 
+def attn_bwd(q, k, v, o, lse, d_o, row_ptr, col_idx, block: int, causal: int, csr_shared: bool = False,
+             softmax_scale: float | None = None):
+    """Allocate dq / dk / dv and the workspace, run the backward; returns (dq, dk, dv)."""
+    import torch
+    b, n, h, d = q.shape
+    ws_bytes = sa_attn_bwd_workspace_size(b, n, h, block, 1 if csr_shared else b, col_idx.numel())
+    ws = torch.empty((ws_bytes,), dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    sa_attn_bwd(q, k, v, o, d_o, lse, row_ptr, col_idx, block, causal, dq, dk, dv, ws, csr_shared, softmax_scale)
+    return dq, dk, dv
+
+
 def offset_attn_fwd(q, k, v, window: int, offsets, softmax_scale: float | None = None):
     import torch
     b, n, h, d = q.shape
@@ -245,6 +284,6 @@ def offset_attn_fwd(q, k, v, window: int, offsets, softmax_scale: float | None =
 
 __all__ = [
     "build_library", "load_library", "SAError", "MaskParams", "mask_params", "sa_mask_nnz_bound", "sa_build_mask",
-    "sa_attn_fwd", "sa_attn_fwd_heads", "sa_pow2_offsets", "sa_layer_alpha", "attn_fwd_heads", "LITERAL_LOCAL", "LITERAL_PAIRS", "sa_offset_attn_fwd", "sa_fib_offsets", "sa_block_ratios", "sa_device_status", "build_mask",
+    "sa_attn_fwd", "sa_attn_fwd_heads", "sa_attn_bwd", "sa_attn_bwd_workspace_size", "attn_bwd", "sa_pow2_offsets", "sa_layer_alpha", "attn_fwd_heads", "LITERAL_LOCAL", "LITERAL_PAIRS", "sa_offset_attn_fwd", "sa_fib_offsets", "sa_block_ratios", "sa_device_status", "build_mask",
     "attn_fwd", "offset_attn_fwd", "MASK_TOPK", "MASK_BIGBIRD", "MASK_FULL", "MASK_LITERAL_MEAN",
 ]

@@ -41,6 +41,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "csr_union.cuh"
 #include "ptx_sm100.cuh"
 #include "sa_internal.h"
 #include "tma_host.h"
@@ -54,7 +55,6 @@ constexpr int kTile = 128;          // query rows per work item
 constexpr int kKeyTile = 64;        // keys per S tile (two 32-key chunks)
 constexpr int kThreads = 640;       // 20 warps
 constexpr int kMetaRing = 8;
-constexpr int kMaxQBlocks = 4;      // query blocks per tile (128 / b, b >= 32)
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSoftmaxWarps = 8;    // per pipeline: two per TMEM lane quarter (one per 32-key chunk)
 constexpr int kMetaConsumers = 1 + kSoftmaxWarps;   // the MMA thread and the softmax warps
@@ -81,7 +81,7 @@ struct Cfg {
   static constexpr int NS = D == 32 ? 3 : 2;           // S buffers per pipeline
   static constexpr int QB = D > 64 ? 1 : 2;            // Q buffers per pipeline
   static constexpr int STAGES = D == 128 ? 2 : (D == 64 ? 4 : 6);   // K and V ring depth
-  static constexpr int UNION_BYTES = kMaxQBlocks * (kMaxMaskBlocks / 32) * 4 + kMaxMaskBlocks * 2;   // 10 KB
+  static constexpr int UNION_BYTES = kMaxTileBlocks * (kMaxMaskBlocks / 32) * 4 + kMaxMaskBlocks * 2;   // 10 KB
   static constexpr int PIPE_BYTES = (QB * Q_BYTES + 2 * STAGES * KV_BYTES + UNION_BYTES + 1023) & ~1023;
   static constexpr int SMEM_NEED = 1024 + 2 * PIPE_BYTES;
   // at least 120 KB so that only one CTA (512 TMEM columns) is resident per SM
@@ -222,72 +222,6 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 
 // ------------------------------------------------------------------ producer (warps 0, 11)
 
-// Per-tile key-block union, built by the producer warp in shared memory: one bitmap of
-// nb bits per query block of the tile, then an ascending list of (J | membership << 12).
-struct UnionSmem {
-  uint32_t bm[kMaxQBlocks][kMaxMaskBlocks / 32];   // 2 KB
-  uint16_t list[kMaxMaskBlocks];                   // 8 KB
-};
-
-// Builds the union of rows I0 .. I0+nq-1 into u.list; returns its length. Column indices
-// outside [0, nb) are skipped and reported; under causality a block J > I0 + r is not
-// attached to query block r (its keys are all in the future).
-__device__ int build_union(const Params& p, UnionSmem& u, const int32_t* rp, const int32_t* ci, int I0, int nq) {
-  const int lane = threadIdx.x & 31;
-  const int nw = (p.nb + 31) >> 5;
-  for (int r = 0; r < nq; ++r)
-    for (int w = lane; w < nw; w += 32) u.bm[r][w] = 0u;
-  const int bnd = (lane <= nq) ? rp[I0 + lane] : 0x7fffffff;   // lane r: start of row r
-  int bq[kMaxQBlocks + 1];
-#pragma unroll
-  for (int q = 0; q <= kMaxQBlocks; ++q) bq[q] = __shfl_sync(0xffffffffu, bnd, min(q, nq));
-  const int e0 = bq[0];
-  const int e1 = bq[kMaxQBlocks];
-  __syncwarp();
-  for (int e = e0 + lane; e < e1; e += 32) {
-    const int J = ci[e];
-    int r = 0;
-#pragma unroll
-    for (int q = 1; q < kMaxQBlocks; ++q) r += (q < nq && e >= bq[q]) ? 1 : 0;
-    if (J < 0 || J >= p.nb) {
-      atomicOr(&g_attn_err, kErrBadIndex);
-    } else if (!p.causal || J <= I0 + r) {
-      atomicOr(&u.bm[r][J >> 5], 1u << (J & 31));
-    }
-  }
-  __syncwarp();
-  int total = 0;
-  for (int w0 = 0; w0 < nw; w0 += 32) {
-    const int w = w0 + lane;
-    uint32_t word[kMaxQBlocks];
-    uint32_t un = 0u;
-#pragma unroll
-    for (int r = 0; r < kMaxQBlocks; ++r) {
-      word[r] = (r < nq && w < nw) ? u.bm[r][w] : 0u;
-      un |= word[r];
-    }
-    const int c = __popc(un);
-    int incl = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    int pos = total + incl - c;
-    while (un) {
-      const int j = __ffs(un) - 1;
-      un &= un - 1u;
-      uint32_t mask = 0u;
-#pragma unroll
-      for (int r = 0; r < kMaxQBlocks; ++r) mask |= ((word[r] >> j) & 1u) << r;
-      u.list[pos++] = (uint16_t)((uint32_t)(w * 32 + j) | (mask << 12));
-    }
-    total += __shfl_sync(0xffffffffu, incl, 31);
-  }
-  __syncwarp();
-  return total;
-}
-
 template <int D>
 __device__ void producer(const Params& p, int x, const CUtensorMap* tq, const CUtensorMap* tk,
                          const CUtensorMap* tv, PipeBars& bars, Meta* meta, UnionSmem& u, uint8_t* sQ, uint8_t* sK,
@@ -326,7 +260,8 @@ __device__ void producer(const Params& p, int x, const CUtensorMap* tq, const CU
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     if (!ok) break;
 
-    const int n_keys = build_union(p, u, rp, p.col_idx[mi], I0, nq);
+    const int n_keys = build_union(p.nb, p.causal ? kKeepLE : kKeepAll, u, rp, p.col_idx[mi], I0, nq, &g_attn_err,
+                                   kErrBadIndex);
     const int n_chunks = n_keys * cpb;
 
     for (int c0 = 0;; c0 += 2) {

@@ -235,6 +235,68 @@ int sa_attn_fwd(const void* q, const void* k, const void* v, const int64_t q_str
                            stream);
 }
 
+int sa_attn_bwd_workspace_size(int32_t batch, int32_t n_tokens, int32_t heads, int32_t block, int32_t csr_batches,
+                               int64_t col_capacity, size_t* h_bytes) {
+  if (batch <= 0 || n_tokens <= 0 || heads <= 0 || block <= 0 || n_tokens % block != 0 || csr_batches <= 0 ||
+      col_capacity < 0 || !h_bytes)
+    return SA_ERR_INVALID_ARG;
+  *h_bytes = sa::bwd_workspace_layout(batch, n_tokens, heads, block, csr_batches, col_capacity).bytes;
+  return SA_OK;
+}
+
+int sa_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* d_o, const float* lse,
+                const int64_t q_strides[3], const int64_t kv_strides[3], const int64_t o_strides[3], int32_t batch,
+                int32_t n_tokens, int32_t heads, int32_t kv_heads, int32_t head_dim, int32_t block, int32_t causal,
+                const int32_t* d_row_ptr, const int32_t* d_col_idx, int32_t csr_shared, float softmax_scale,
+                void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!o || !d_o || !lse || !dk || !dv || !d_row_ptr || !d_col_idx || !workspace) return SA_ERR_INVALID_ARG;
+  const int st = check_attn_common(q, k, v, q_strides, kv_strides, o_strides, batch, n_tokens, heads, kv_heads, dq,
+                                   const_cast<float*>(lse));
+  if (st != SA_OK) return st;
+  if (!aligned16(o) || !aligned16(d_o) || !aligned16(dk) || !aligned16(dv) || !aligned16(lse)) return SA_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SA_ERR_UNSUPPORTED;
+  if (causal != 0 && causal != 1) return SA_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f)) return SA_ERR_INVALID_ARG;
+  if (head_dim != 32 && head_dim != 64 && head_dim != 128) return SA_ERR_UNSUPPORTED;
+  if (block != 32 && block != 64 && block != 128) return SA_ERR_UNSUPPORTED;
+  if (n_tokens % block != 0) return SA_ERR_UNSUPPORTED;
+  if (n_tokens / block > sa::kMaxMaskBlocks) return SA_ERR_UNSUPPORTED;
+  if ((int64_t)batch * heads * ((n_tokens + 127) / 128) > INT32_MAX) return SA_ERR_UNSUPPORTED;
+  const int csr_batches = csr_shared ? 1 : batch;
+  if (workspace_bytes < sa::bwd_workspace_layout(batch, n_tokens, heads, block, csr_batches, 0).bytes)
+    return SA_ERR_CAPACITY;
+  if (!device_ok()) return SA_ERR_CUDA;
+  sa::BwdArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.d_o = d_o;
+  a.lse = lse;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  for (int i = 0; i < 3; ++i) {
+    a.q_strides[i] = q_strides[i];
+    a.kv_strides[i] = kv_strides[i];
+    a.o_strides[i] = o_strides[i];
+  }
+  a.batch = batch;
+  a.n_tokens = n_tokens;
+  a.heads = heads;
+  a.kv_heads = kv_heads;
+  a.head_dim = head_dim;
+  a.block = block;
+  a.causal = causal;
+  a.csr_shared = csr_shared != 0;
+  a.row_ptr = d_row_ptr;
+  a.col_idx = d_col_idx;
+  a.softmax_scale = softmax_scale;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  return sa::launch_attn_bwd(a, static_cast<cudaStream_t>(stream));
+}
+
 int sa_offset_attn_fwd(const void* q, const void* k, const void* v, const int64_t q_strides[3],
                        const int64_t kv_strides[3], const int64_t o_strides[3], int32_t batch, int32_t n_tokens,
                        int32_t heads, int32_t kv_heads, int32_t head_dim, int32_t window, const int32_t* h_offsets,
@@ -390,10 +452,12 @@ int sa_block_ratios(const uint8_t* h_bytes, int32_t batch, int32_t n_tokens, int
 int sa_device_status(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return SA_ERR_CUDA;
-  const unsigned int e = sa::attn_read_and_clear_error(s) | sa::offset_read_and_clear_error(s);
+  const unsigned int e = sa::attn_read_and_clear_error(s) | sa::offset_read_and_clear_error(s) |
+                         sa::bwd_read_and_clear_error(s);
   if (cudaGetLastError() != cudaSuccess) return SA_ERR_CUDA;
   if (e & sa::kErrTimeout) return SA_ERR_TIMEOUT;
   if (e & sa::kErrBadIndex) return SA_ERR_DEVICE;
+  if (e & sa::kErrCapacity) return SA_ERR_CAPACITY;
   return SA_OK;
 }
 

@@ -10,6 +10,7 @@ namespace sa {
 // Device error bits (one error word per translation unit that can raise them).
 constexpr unsigned int kErrTimeout = 1u;     // a bounded wait expired
 constexpr unsigned int kErrBadIndex = 2u;    // CSR column index out of range (skipped)
+constexpr unsigned int kErrCapacity = 4u;    // a device-sized output did not fit its buffer
 
 constexpr int kMaxMaskBlocks = 4096;         // nb limit of the mask builder
 constexpr int kMaxRandomBlocks = 64;
@@ -58,5 +59,37 @@ struct OffsetArgs {
 };
 int launch_offset_attn_fwd(const OffsetArgs& a, cudaStream_t stream);
 unsigned int offset_read_and_clear_error(cudaStream_t stream);
+
+// attn_bwd.cu
+struct BwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const void* d_o;
+  const float* lse;
+  void* dq;
+  void* dk;
+  void* dv;
+  int64_t q_strides[3];    // q and dq
+  int64_t kv_strides[3];   // k, v, dk and dv
+  int64_t o_strides[3];    // o and d_o
+  int32_t batch, n_tokens, heads, kv_heads, head_dim, block, causal, csr_shared;
+  const int32_t* row_ptr;
+  const int32_t* col_idx;
+  float softmax_scale;
+  void* workspace;
+  size_t workspace_bytes;
+};
+// Workspace layout of the backward: D = rowsum(dO * O) fp32 [batch][heads][n_tokens],
+// the transposed CSR's col_ptr int32 [csr_batches][nb + 1] and row_idx int32 [rest].
+struct BwdWorkspace {
+  size_t dvec_off, col_ptr_off, row_idx_off, bytes;
+  int64_t row_idx_capacity;
+};
+BwdWorkspace bwd_workspace_layout(int64_t batch, int64_t n_tokens, int64_t heads, int64_t block,
+                                  int64_t csr_batches, int64_t col_capacity);
+int launch_attn_bwd(const BwdArgs& a, cudaStream_t stream);
+unsigned int bwd_read_and_clear_error(cudaStream_t stream);
 
 }  // namespace sa

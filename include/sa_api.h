@@ -146,6 +146,35 @@ int sa_attn_fwd_heads(const void* q, const void* k, const void* v, const int64_t
                       const int32_t* h_head_mask, int32_t csr_shared, float softmax_scale, void* o, float* lse,
                       void* stream);
 
+/* Workspace bytes of sa_attn_bwd: D = rowsum(dO * O) (fp32 [batch][heads][n_tokens])
+ * and the transposed CSR (int32 [csr_batches][nb + 1] plus col_capacity indices, where
+ * col_capacity >= the number of CSR entries, e.g. sa_mask_nnz_bound). csr_batches is
+ * 1 for a shared CSR, else batch. Host only. */
+int sa_attn_bwd_workspace_size(int32_t batch, int32_t n_tokens, int32_t heads, int32_t block, int32_t csr_batches,
+                               int64_t col_capacity, size_t* h_bytes);
+
+/* Block-sparse attention backward over the block CSR of sa_attn_fwd: the gradients of
+ * sum(dO * O) with respect to q, k and v. With P_ij = exp(s_ij - LSE_i) over the visible
+ * keys and D_i = sum_d dO_id O_id:
+ *   dV_j = sum_i P_ij dO_i,  dS_ij = P_ij (<dO_i, v_j> - D_i),
+ *   dQ_i = softmax_scale * sum_j dS_ij k_j,  dK_j = softmax_scale * sum_i dS_ij q_i
+ * (dK / dV of a key/value head sum over its query heads). The pages train through these
+ * masks ("Parameter-free Adaptive Sparse Attention ...", section 4.1; "Depth-Staggered
+ * Fibonacci Spacing ...", section 3).
+ *   o, lse : the forward's outputs for the same inputs (o with o_strides, lse contiguous
+ *            [batch][heads][n_tokens], 16-byte aligned).
+ *   d_o    : upstream gradient, bf16, layout and strides of o.
+ *   dq     : bf16 with q_strides; dk, dv : bf16 with kv_strides; all written.
+ *   workspace : device memory of at least sa_attn_bwd_workspace_size bytes, 256-byte
+ *            aligned, owned by the caller; its contents on entry do not matter.
+ * Shapes, CSR and error behaviour as in sa_attn_fwd; a CSR with more entries than the
+ * workspace holds is reported by sa_device_status as SA_ERR_CAPACITY. */
+int sa_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* d_o, const float* lse,
+                const int64_t q_strides[3], const int64_t kv_strides[3], const int64_t o_strides[3], int32_t batch,
+                int32_t n_tokens, int32_t heads, int32_t kv_heads, int32_t head_dim, int32_t block, int32_t causal,
+                const int32_t* d_row_ptr, const int32_t* d_col_idx, int32_t csr_shared, float softmax_scale,
+                void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Token-granular window-plus-offset attention forward ("Depth-Staggered Fibonacci
  * Spacing ...", section 2 "Attended set"): query i attends to keys
  *   { i - delta : delta in {0, ..., window} u offsets, i - delta >= 0 }   (a set).
@@ -191,7 +220,8 @@ int sa_block_ratios(const uint8_t* h_bytes, int32_t batch, int32_t n_tokens, int
 
 /* Synchronises `stream`, then reads and clears the library's device error word.
  * Returns SA_OK, SA_ERR_TIMEOUT (a bounded wait expired; the kernel unwound and its
- * outputs are undefined) or SA_ERR_DEVICE (invalid CSR data was skipped). */
+ * outputs are undefined), SA_ERR_DEVICE (invalid CSR data was skipped) or
+ * SA_ERR_CAPACITY (a device-sized structure did not fit the caller's workspace). */
 int sa_device_status(void* stream);
 
 /* Human-readable name of a status code (static string). */

@@ -43,3 +43,26 @@ def assert_attention_close(o_gpu: np.ndarray, lse_gpu: np.ndarray, o_ref: np.nda
     assert err.mean() <= O_MEAN_ABS, msg
     assert lerr.max() <= LSE_MAX_ABS, msg
     return err.max(), err.mean(), lerr.max()
+
+
+# Gradients (dQ, dK, dV) against the float64 oracle, relative to each tensor's scale:
+# max abs error <= 2e-2 * max |ref| and mean abs error <= 5e-3 * mean |ref|. Derivation:
+# the kernel rounds P and dS to bf16 for the tensor core and the outputs to bf16 (unit
+# roundoff u = 2^-9 each), and forms D = rowsum(dO * O) from the bf16 forward output, so
+# each gradient element carries a few u of relative error about its own scale; 2e-2 is
+# about 10 u on the worst element, 5e-3 about 2.5 u on average.
+GRAD_MAX_REL = 2e-2
+GRAD_MEAN_REL = 5e-3
+
+
+def assert_grad_close(g_gpu: np.ndarray, g_ref: np.ndarray, what: str = ""):
+    assert g_gpu.shape == g_ref.shape
+    assert np.all(np.isfinite(g_gpu)), f"{what}: non-finite gradient"
+    err = np.abs(g_gpu - g_ref)
+    scale_max = max(float(np.abs(g_ref).max()), 1e-30)
+    scale_mean = max(float(np.abs(g_ref).mean()), 1e-30)
+    msg = (f"{what}: max err {err.max():.3e} (scale {scale_max:.3e}), mean err {err.mean():.3e} "
+           f"(scale {scale_mean:.3e})")
+    assert err.max() <= GRAD_MAX_REL * scale_max, msg
+    assert err.mean() <= GRAD_MEAN_REL * scale_mean, msg
+    return err.max() / scale_max, err.mean() / scale_mean
