@@ -67,6 +67,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.sa_attn_bwd_workspace_size.argtypes = [ctypes.c_int32] * 5 + [ctypes.c_int64, _P]
     lib.sa_attn_bwd.argtypes = [_P, _P, _P, _P, _P, _P, _I64x3, _I64x3, _I64x3] + [ctypes.c_int32] * 7 + \
         [_P, _P, ctypes.c_int32, ctypes.c_float, _P, _P, _P, _P, ctypes.c_size_t, _P]
+    lib.sa_attn_bwd_noalloc.argtypes = [_P, _P, _P, _P, _P, _P, _I64x3, _I64x3, _I64x3] + \
+        [ctypes.c_int32] * 7 + [_P, _P, ctypes.c_int64, ctypes.c_int32, ctypes.c_float, _P, _P, _P, _P]
     lib.sa_offset_attn_fwd.argtypes = [_P, _P, _P, _I64x3, _I64x3, _I64x3, ctypes.c_int32, ctypes.c_int32,
                                        ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P,
                                        ctypes.c_int32, ctypes.c_float, _P, _P, _P]
@@ -77,6 +79,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
                                     ctypes.c_int32]
     lib.sa_device_status.argtypes = [_P]
     for name in ("sa_mask_nnz_bound", "sa_build_mask", "sa_attn_fwd", "sa_attn_fwd_heads", "sa_attn_bwd",
+                 "sa_attn_bwd_noalloc",
                  "sa_attn_bwd_workspace_size", "sa_offset_attn_fwd",
                  "sa_fib_offsets", "sa_pow2_offsets", "sa_layer_alpha", "sa_block_ratios", "sa_device_status"):
         getattr(lib, name).restype = ctypes.c_int
@@ -174,6 +177,19 @@ def sa_attn_bwd(q, k, v, o, d_o, lse, row_ptr, col_idx, block: int, causal: int,
         _strides(k), _strides(o), b, n, h, hkv, d, block, int(causal), row_ptr.data_ptr(), col_idx.data_ptr(),
         int(bool(csr_shared)), scale, dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
+
+
+def sa_attn_bwd_noalloc(q, k, v, o, d_o, lse, row_ptr, col_idx, block: int, causal: int, dq, dk, dv,
+                        csr_shared: bool = False, softmax_scale: float | None = None, stream=None) -> None:
+    """sa_attn_bwd with the library's own scratch (no workspace argument)."""
+    b, n, h, d = q.shape
+    hkv = k.shape[2]
+    scale = 1.0 / float(np.sqrt(d)) if softmax_scale is None else float(softmax_scale)
+    _check("sa_attn_bwd_noalloc", load_library().sa_attn_bwd_noalloc(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), d_o.data_ptr(), lse.data_ptr(), _strides(q),
+        _strides(k), _strides(o), b, n, h, hkv, d, block, int(causal), row_ptr.data_ptr(), col_idx.data_ptr(),
+        col_idx.numel(), int(bool(csr_shared)), scale, dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+        _stream_ptr(stream)))
 
 
 def sa_offset_attn_fwd(q, k, v, window: int, offsets, o, lse, softmax_scale: float | None = None,
@@ -284,6 +300,7 @@ def offset_attn_fwd(q, k, v, window: int, offsets, softmax_scale: float | None =
 
 __all__ = [
     "build_library", "load_library", "SAError", "MaskParams", "mask_params", "sa_mask_nnz_bound", "sa_build_mask",
-    "sa_attn_fwd", "sa_attn_fwd_heads", "sa_attn_bwd", "sa_attn_bwd_workspace_size", "attn_bwd", "sa_pow2_offsets", "sa_layer_alpha", "attn_fwd_heads", "LITERAL_LOCAL", "LITERAL_PAIRS", "sa_offset_attn_fwd", "sa_fib_offsets", "sa_block_ratios", "sa_device_status", "build_mask",
+    "sa_attn_fwd", "sa_attn_fwd_heads", "sa_attn_bwd", "sa_attn_bwd_workspace_size", "attn_bwd",
+    "sa_attn_bwd_noalloc", "sa_pow2_offsets", "sa_layer_alpha", "attn_fwd_heads", "LITERAL_LOCAL", "LITERAL_PAIRS", "sa_offset_attn_fwd", "sa_fib_offsets", "sa_block_ratios", "sa_device_status", "build_mask",
     "attn_fwd", "offset_attn_fwd", "MASK_TOPK", "MASK_BIGBIRD", "MASK_FULL", "MASK_LITERAL_MEAN",
 ]

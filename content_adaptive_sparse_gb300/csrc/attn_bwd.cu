@@ -69,7 +69,9 @@ struct BCfg {
   // stage: two 64-row tiles (+ 2 x 64 floats for dK / dV), 1 KB aligned for the swizzle
   static constexpr int STAGE_BYTES = (2 * STEP_BYTES + 512 + 1023) & ~1023;
   static constexpr int UNION_BYTES = (int)sizeof(UnionSmem);
-  static constexpr int SMEM = 1024 + 2 * BIG_BYTES + STAGES * STAGE_BYTES + UNION_BYTES;
+  static constexpr int SMEM_NEED = 1024 + 2 * BIG_BYTES + STAGES * STAGE_BYTES + UNION_BYTES;
+  // at least 80 KB: at most two CTAs per SM, whose TMEM (256 columns each) then always fits
+  static constexpr int SMEM = SMEM_NEED > 80 * 1024 ? SMEM_NEED : 80 * 1024;
   static constexpr uint32_t TMEM_DQ = 256;
   static constexpr uint32_t TMEM_DKDV = 128 + 2 * D <= 256 ? 256 : 512;
   static_assert(STAGES <= kMaxStages, "ring size");
@@ -374,13 +376,10 @@ __device__ void dq_compute(const BParams& p, const Item& it, int h, Bars& bars, 
     ok = __all_sync(0xffffffffu, wait_bar(&bars.s_full, t & 1, abort_flag));
     if (!ok) break;
     tc_fence_after();
-    uint32_t pk[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) pk[j] = 0u;
     if (cls != 0) {
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        uint32_t sv[16], dv[16];
+        uint32_t sv[16], dv[16], pk[8];
         tmem_ld_x16(tS + 16 * half, sv);
         tmem_ld_x16(tP + 16 * half, dv);
         tmem_ld_wait<16>(sv);
@@ -397,12 +396,18 @@ __device__ void dq_compute(const BParams& p, const Item& it, int h, Bars& bars, 
           const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
           const float d0 = p0 * (__uint_as_float(dv[j]) - dval);
           const float d1 = p1 * (__uint_as_float(dv[j + 1]) - dval);
-          pk[8 * half + (j >> 1)] = pack_bf16x2(d0, d1);
+          pk[j >> 1] = pack_bf16x2(d0, d1);
         }
+        // dS (bf16 pairs) of this half over columns 8 half .. 8 half + 7 of the warp's own
+        // S chunk (already read; the S columns of half 1 are not among them)
+        tmem_st_x8(tS + 8 * half, pk);
       }
+    } else {
+      uint32_t z[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) z[j] = 0u;
+      tmem_st_x16(tS, z);
     }
-    // dS (bf16 pairs) over the first 16 columns of this warp's own S chunk
-    tmem_st_x16(tS, pk);
     tmem_st_wait();
     tc_fence_before();
     __syncwarp();
@@ -433,7 +438,7 @@ __device__ void dq_compute(const BParams& p, const Item& it, int h, Bars& bars, 
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
                   const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                   const __grid_constant__ BParams p) {
@@ -641,9 +646,6 @@ __device__ void dkdv_compute(const BParams& p, const Item& it, int h, Bars& bars
     ok = __all_sync(0xffffffffu, wait_bar(&bars.s_full, t & 1, abort_flag));
     if (!ok) break;
     tc_fence_after();
-    uint32_t pp[16], pd[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) pp[j] = pd[j] = 0u;
     if (any) {
       // LSE and D of the step's query rows (landed with the stage; this wait is complete)
       ok = __all_sync(0xffffffffu, wait_bar(&bars.st_full[st], (t / C::STAGES) & 1, abort_flag));
@@ -653,7 +655,7 @@ __device__ void dkdv_compute(const BParams& p, const Item& it, int h, Bars& bars
       const float4* d4 = reinterpret_cast<const float4*>(vec + 64 + 32 * h);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        uint32_t sv[16], dv[16];
+        uint32_t sv[16], dv[16], pp[8], pd[8];
         tmem_ld_x16(tS + 16 * half, sv);
         tmem_ld_x16(tP + 16 * half, dv);
         tmem_ld_wait<16>(sv);
@@ -675,15 +677,22 @@ __device__ void dkdv_compute(const BParams& p, const Item& it, int h, Bars& bars
             const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
             const float d0 = p0 * (__uint_as_float(dv[j]) - Dv[e]);
             const float d1 = p1 * (__uint_as_float(dv[j + 1]) - Dv[e + 1]);
-            pp[8 * half + (j >> 1)] = pack_bf16x2(p0, p1);
-            pd[8 * half + (j >> 1)] = pack_bf16x2(d0, d1);
+            pp[j >> 1] = pack_bf16x2(p0, p1);
+            pd[j >> 1] = pack_bf16x2(d0, d1);
           }
         }
+        // P^T over this warp's S^T chunk, dS^T over its dP^T chunk: the 8 columns of this
+        // half (the S / dP columns of half 1 are not among them)
+        tmem_st_x8(tS + 8 * half, pp);
+        tmem_st_x8(tP + 8 * half, pd);
       }
+    } else {
+      uint32_t z[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) z[j] = 0u;
+      tmem_st_x16(tS, z);
+      tmem_st_x16(tP, z);
     }
-    // P^T over this warp's S^T chunk, dS^T over its dP^T chunk (first 16 columns each)
-    tmem_st_x16(tS, pp);
-    tmem_st_x16(tP, pd);
     tmem_st_wait();
     tc_fence_before();
     __syncwarp();
@@ -719,7 +728,7 @@ __device__ void dkdv_compute(const BParams& p, const Item& it, int h, Bars& bars
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                     const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
                     const __grid_constant__ BParams p) {
@@ -1055,6 +1064,13 @@ int launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
     case 128: return launch_attention<128>(a, ws, stream);
   }
   return SA_ERR_UNSUPPORTED;
+}
+
+// Scratch of the no-allocation entry point: D and the transposed CSR of one call at a time.
+static __device__ __align__(256) uint8_t g_bwd_static_scratch[kBwdStaticScratchBytes];
+
+int bwd_static_scratch(void** ptr) {
+  return cudaGetSymbolAddress(ptr, g_bwd_static_scratch) == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
 unsigned int bwd_read_and_clear_error(cudaStream_t stream) {

@@ -297,6 +297,25 @@ int sa_attn_bwd(const void* q, const void* k, const void* v, const void* o, cons
   return sa::launch_attn_bwd(a, static_cast<cudaStream_t>(stream));
 }
 
+int sa_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* d_o, const float* lse,
+                        const int64_t q_strides[3], const int64_t kv_strides[3], const int64_t o_strides[3],
+                        int32_t batch, int32_t n_tokens, int32_t heads, int32_t kv_heads, int32_t head_dim,
+                        int32_t block, int32_t causal, const int32_t* d_row_ptr, const int32_t* d_col_idx,
+                        int64_t col_capacity, int32_t csr_shared, float softmax_scale, void* dq, void* dk, void* dv,
+                        void* stream) {
+  if (batch <= 0 || n_tokens <= 0 || heads <= 0 || block <= 0 || n_tokens % block != 0 || col_capacity < 0)
+    return SA_ERR_INVALID_ARG;
+  const int64_t csr_batches = csr_shared ? 1 : batch;
+  const size_t need = sa::bwd_workspace_layout(batch, n_tokens, heads, block, csr_batches, col_capacity).bytes;
+  if (need > sa::kBwdStaticScratchBytes) return SA_ERR_CAPACITY;
+  if (!device_ok()) return SA_ERR_CUDA;
+  void* scratch = nullptr;
+  if (sa::bwd_static_scratch(&scratch) != SA_OK) return SA_ERR_CUDA;
+  return sa_attn_bwd(q, k, v, o, d_o, lse, q_strides, kv_strides, o_strides, batch, n_tokens, heads, kv_heads,
+                     head_dim, block, causal, d_row_ptr, d_col_idx, csr_shared, softmax_scale, dq, dk, dv, scratch,
+                     need, stream);
+}
+
 int sa_offset_attn_fwd(const void* q, const void* k, const void* v, const int64_t q_strides[3],
                        const int64_t kv_strides[3], const int64_t o_strides[3], int32_t batch, int32_t n_tokens,
                        int32_t heads, int32_t kv_heads, int32_t head_dim, int32_t window, const int32_t* h_offsets,

@@ -90,6 +90,10 @@ struct BwdWorkspace {
 BwdWorkspace bwd_workspace_layout(int64_t batch, int64_t n_tokens, int64_t heads, int64_t block,
                                   int64_t csr_batches, int64_t col_capacity);
 int launch_attn_bwd(const BwdArgs& a, cudaStream_t stream);
+// Device address of the library's own backward scratch (kBwdStaticScratchBytes, 256-byte
+// aligned), used by sa_attn_bwd_noalloc.
+constexpr size_t kBwdStaticScratchBytes = size_t(16) << 20;
+int bwd_static_scratch(void** ptr);
 unsigned int bwd_read_and_clear_error(cudaStream_t stream);
 
 }  // namespace sa

@@ -175,6 +175,18 @@ int sa_attn_bwd(const void* q, const void* k, const void* v, const void* o, cons
                 const int32_t* d_row_ptr, const int32_t* d_col_idx, int32_t csr_shared, float softmax_scale,
                 void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, void* stream);
 
+/* sa_attn_bwd without a caller workspace: the scratch lives in a 16 MiB array inside the
+ * library (one per device), so the call allocates nothing. col_capacity bounds the CSR's
+ * entries as in sa_attn_bwd_workspace_size; if the scratch that needs exceeds 16 MiB the
+ * call returns SA_ERR_CAPACITY before any launch. The scratch is shared: calls must not
+ * overlap in time (serialise them on one stream, or synchronise between streams). */
+int sa_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* d_o, const float* lse,
+                        const int64_t q_strides[3], const int64_t kv_strides[3], const int64_t o_strides[3],
+                        int32_t batch, int32_t n_tokens, int32_t heads, int32_t kv_heads, int32_t head_dim,
+                        int32_t block, int32_t causal, const int32_t* d_row_ptr, const int32_t* d_col_idx,
+                        int64_t col_capacity, int32_t csr_shared, float softmax_scale, void* dq, void* dk, void* dv,
+                        void* stream);
+
 /* Token-granular window-plus-offset attention forward ("Depth-Staggered Fibonacci
  * Spacing ...", section 2 "Attended set"): query i attends to keys
  *   { i - delta : delta in {0, ..., window} u offsets, i - delta >= 0 }   (a set).

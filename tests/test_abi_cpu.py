@@ -33,6 +33,7 @@ def _declared_functions():
 def test_header_symbols_exported(lib):
     names = _declared_functions()
     assert {"sa_build_mask", "sa_attn_fwd", "sa_attn_fwd_heads", "sa_offset_attn_fwd", "sa_pow2_offsets",
+            "sa_attn_bwd", "sa_attn_bwd_workspace_size", "sa_attn_bwd_noalloc",
             "sa_layer_alpha", "sa_fib_offsets", "sa_block_ratios",
             "sa_mask_nnz_bound", "sa_device_status", "sa_status_string", "sa_version"} <= set(names)
     for n in names:
@@ -154,6 +155,23 @@ def test_compute_entry_points_refuse_without_gpu(lib):
     ok = sa.mask_params(0, 64, 8192, 1, window_blocks=4, global_blocks=1, topk=16)
     dummy = ctypes.c_void_p(16)
     assert lib.sa_build_mask(ctypes.byref(ok), dummy, dummy, dummy, 10**6, None) == -4   # SA_ERR_CUDA
+
+
+def test_bwd_noalloc_capacity_is_checked_on_the_host(lib):
+    """The no-allocation backward refuses shapes whose scratch exceeds its 16 MiB before
+    touching a device; shapes that fit get as far as the device check."""
+    I3 = ctypes.c_int64 * 3
+    s = I3(8192 * 12 * 64, 12 * 64, 64)
+    p16 = ctypes.c_void_p(256)
+    args = lambda batch, cap: (p16, p16, p16, p16, p16, p16, s, s, s, batch, 8192, 12, 12, 64, 64, 1, p16, p16,
+                               ctypes.c_int64(cap), 0, ctypes.c_float(0.125), p16, p16, p16, None)
+    assert lib.sa_attn_bwd_noalloc(*args(64, 10**5)) == -3        # 64 x 12 x 8192 x 4 B of D alone > 16 MiB
+    ws = ctypes.c_size_t(0)
+    assert lib.sa_attn_bwd_workspace_size(4, 8192, 12, 64, 4, 10**4, ctypes.byref(ws)) == 0
+    assert ws.value < 16 << 20
+    import torch
+    if not torch.cuda.is_available():
+        assert lib.sa_attn_bwd_noalloc(*args(4, 10**4)) == -4     # fits; no device here
 
 
 def test_ratio_threads_are_deterministic(lib):
