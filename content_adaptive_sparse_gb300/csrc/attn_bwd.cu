@@ -143,6 +143,16 @@ __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
   return d;
 }
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 
 // Work item k, longest first. dQ: query tiles, causal ranks from the last tile. dK / dV:
 // key tiles from the first (the first key blocks are seen by the most query blocks).
@@ -359,6 +369,7 @@ __device__ void dq_compute(const BParams& p, const Item& it, int h, Bars& bars, 
   const float nl2 = lse == kNegInf ? kNegInf : -lse * kLog2e;
   const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
   const uint64_t nl22 = f2_pack(nl2, nl2);
+  const uint64_t negd2 = f2_pack(-dval, -dval);
   const uint32_t tS = tmem + kColS + 32u * h + lane_base;
   const uint32_t tP = tmem + kColP + 32u * h + lane_base;
   bool ok = true;
@@ -394,8 +405,9 @@ __device__ void dq_compute(const BParams& p, const Item& it, int h, Bars& bars, 
             x1 = ((kp >> (cj + 1)) & 1u) ? x1 : kNegInf;
           }
           const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-          const float d0 = p0 * (__uint_as_float(dv[j]) - dval);
-          const float d1 = p1 * (__uint_as_float(dv[j + 1]) - dval);
+          float d0, d1;
+          f2_unpack(f2_mul(f2_pack(p0, p1), f2_add(f2_pack(__uint_as_float(dv[j]), __uint_as_float(dv[j + 1])), negd2)),
+                    d0, d1);
           pk[j >> 1] = pack_bf16x2(d0, d1);
         }
         // dS (bf16 pairs) of this half over columns 8 half .. 8 half + 7 of the warp's own
@@ -620,7 +632,9 @@ __device__ void dkdv_compute(const BParams& p, const Item& it, int h, Bars& bars
   const int jl = row >> p.log2b;                       // key block within the tile
   const bool valid = ktok < p.n_tokens;
   const float kNegInf = __int_as_float(0xff800000);
-  const float c = p.scale_log2;
+  const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
+  const uint64_t neg_log2e2 = f2_pack(-kLog2e, -kLog2e);
+  const uint64_t minus_one2 = f2_pack(-1.f, -1.f);
   const uint32_t tS = tmem + kColS + 32u * h + lane_base;
   const uint32_t tP = tmem + kColP + 32u * h + lane_base;
   bool ok = true;
@@ -643,6 +657,7 @@ __device__ void dkdv_compute(const BParams& p, const Item& it, int h, Bars& bars
       kp = (!p.causal || lim <= 0) ? 0xffffffffu : (lim >= 32 ? 0u : (0xffffffffu << lim));
     }
     const bool any = __any_sync(0xffffffffu, kp != 0u);
+    const bool full = __all_sync(0xffffffffu, kp == 0xffffffffu);   // no masked column in the warp
     ok = __all_sync(0xffffffffu, wait_bar(&bars.s_full, t & 1, abort_flag));
     if (!ok) break;
     tc_fence_after();
@@ -664,19 +679,24 @@ __device__ void dkdv_compute(const BParams& p, const Item& it, int h, Bars& bars
         for (int q4 = 0; q4 < 4; ++q4) {
           const float4 L = lse4[4 * half + q4];
           const float4 Dq = d4[4 * half + q4];
-          const float Lv[4] = {L.x, L.y, L.z, L.w};
-          const float Dv[4] = {Dq.x, Dq.y, Dq.z, Dq.w};
 #pragma unroll
           for (int e = 0; e < 4; e += 2) {
             const int j = 4 * q4 + e;                  // column within this half
             const int cj = 16 * half + j;              // column within the chunk
-            float x0 = __uint_as_float(sv[j]) * c - Lv[e] * kLog2e;
-            float x1 = __uint_as_float(sv[j + 1]) * c - Lv[e + 1] * kLog2e;
-            x0 = ((kp >> cj) & 1u) ? x0 : kNegInf;
-            x1 = ((kp >> (cj + 1)) & 1u) ? x1 : kNegInf;
+            // x = s c - LSE log2(e); p = 2^x; dS = p (dP - D), two columns at a time
+            const uint64_t nl2 = f2_mul(e ? f2_pack(L.z, L.w) : f2_pack(L.x, L.y), neg_log2e2);
+            const uint64_t d2 = e ? f2_pack(Dq.z, Dq.w) : f2_pack(Dq.x, Dq.y);
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[j]), __uint_as_float(sv[j + 1])), c2, nl2), x0, x1);
+            if (!full) {
+              x0 = ((kp >> cj) & 1u) ? x0 : kNegInf;
+              x1 = ((kp >> (cj + 1)) & 1u) ? x1 : kNegInf;
+            }
             const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-            const float d0 = p0 * (__uint_as_float(dv[j]) - Dv[e]);
-            const float d1 = p1 * (__uint_as_float(dv[j + 1]) - Dv[e + 1]);
+            const uint64_t p2 = f2_pack(p0, p1);
+            const uint64_t t2 = f2_fma(d2, minus_one2, f2_pack(__uint_as_float(dv[j]), __uint_as_float(dv[j + 1])));
+            float d0, d1;
+            f2_unpack(f2_mul(p2, t2), d0, d1);
             pp[j >> 1] = pack_bf16x2(p0, p1);
             pd[j >> 1] = pack_bf16x2(d0, d1);
           }
