@@ -29,10 +29,10 @@ from .masks import (MaskParams, build_csr, csr_topk_rows, csr_bigbird_rows, csr_
                     csr_literal_mean_rows, csr_to_block_mask, block_mask_to_token_mask,
                     literal_flags, topk_row_count, cas_head_components, LOCAL, LITERAL)
 from .fib import (fib_rungs, fib_rungs_upto, pow2_rungs, pow2_rungs_upto, alpha_schedule, fib_offsets,
-                  offset_key_set)
+                  offset_key_set, interp_rungs)
 from .attention import (attention_csr, attention_csr_block, attention_csr_heads, attention_offsets,
                         dense_masked_attention, attention_rows_csr, attention_csr_backward, attention_rows_dq,
-                        attention_rows_dkdv)
+                        attention_rows_dkdv, attention_offsets_interp)
 
 __all__ = [
     "block_ratios", "zlib_version", "philox4x64_10", "philox_word", "MaskParams", "build_csr",
@@ -42,5 +42,5 @@ __all__ = [
     "fib_rungs", "fib_rungs_upto", "pow2_rungs", "pow2_rungs_upto", "alpha_schedule", "fib_offsets", "offset_key_set", "attention_csr",
     "attention_csr_block",
     "attention_offsets", "dense_masked_attention", "attention_rows_csr", "attention_csr_backward",
-    "attention_rows_dq", "attention_rows_dkdv",
+    "attention_rows_dq", "attention_rows_dkdv", "attention_offsets_interp", "interp_rungs",
 ]

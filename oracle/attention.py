@@ -297,3 +297,53 @@ def attention_rows_dkdv(q, k, v, d_o, row_ptr, col_idx, block: int, causal: int,
                     dk[t] += scale * dS[pos] * qv
                     dv[t] += P[0][pos] * dov
     return dk, dv
+
+
+def attention_offsets_interp(q, k, v, window: int, rungs_lo_t, scale: float | None = None, samples=None,
+                             convert=None):
+    """Window plus interpolated-rung attention ([FIB] section 2, the interpolated gather).
+
+    Entries of query i: the window rows i - delta (delta = 0..W, i - delta >= 0) and, for
+    every rung (lo, t) with i - lo - t >= 0, the interpolated key and value
+        k~ = (1 - t) k[i - lo] + t k[i - lo - 1],   v~ likewise (t = 0: row i - lo).
+    Softmax over all entries with s = scale <q_i, k~>. ``rungs_lo_t`` as returned by
+    ``fib.interp_rungs``. If ``samples`` (list of (batch, token, head)) is given only those
+    queries are evaluated; returns o [len, d], lse [len]; else o [B, N, H, d], lse [B, H, N].
+    """
+    cv = convert if convert is not None else (lambda x: x)
+    bt, n, h, d = q.shape
+    hkv = k.shape[2]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    if samples is None:
+        samples = [(s, i, hh) for s in range(bt) for i in range(n) for hh in range(h)]
+        full = True
+    else:
+        full = False
+    o = np.zeros((len(samples), d))
+    lse = np.full(len(samples), -np.inf)
+    for t_idx, (s, i, hh) in enumerate(samples):
+        hk = hh // (h // hkv)
+        keys, vals = [], []
+        for delta in range(window + 1):
+            if i - delta >= 0:
+                keys.append(cv(k[s, i - delta, hk, :]))
+                vals.append(cv(v[s, i - delta, hk, :]))
+        for lo, t in rungs_lo_t:
+            if i - lo - t < 0:
+                continue
+            if t == 0.0:
+                keys.append(cv(k[s, i - lo, hk, :]))
+                vals.append(cv(v[s, i - lo, hk, :]))
+            else:
+                keys.append((1.0 - t) * cv(k[s, i - lo, hk, :]) + t * cv(k[s, i - lo - 1, hk, :]))
+                vals.append((1.0 - t) * cv(v[s, i - lo, hk, :]) + t * cv(v[s, i - lo - 1, hk, :]))
+        K = np.stack(keys)
+        V = np.stack(vals)
+        sc = (K @ cv(q[s, i, hh, :])) * scale
+        p, l = _softmax_rows(sc[None, :])
+        o[t_idx] = p[0] @ V
+        lse[t_idx] = l[0]
+    if not full:
+        return o, lse
+    return o.reshape(bt, n, h, d), lse.reshape(bt, n, h).transpose(0, 2, 1)

@@ -79,3 +79,23 @@ def fib_offsets(alpha: Fraction, rungs: list[int]) -> list[int]:
 def offset_key_set(i: int, window: int, offsets: list[int]) -> list[int]:
     deltas = set(range(window + 1)) | set(offsets)
     return sorted({i - d for d in deltas if i - d >= 0})
+
+
+def interp_rungs(alpha: float, rungs: list[int], window: int) -> list[tuple[int, float]]:
+    """Rungs of the interpolated gather ([FIB] section 2 "Attended set"): the distance
+    d_k = alpha * f_k is continuous (the IEEE double product), and the gathered key and
+    value are the linear interpolation between rows i - floor(d_k) and i - floor(d_k) - 1
+    with weight t_k = d_k - floor(d_k) on the farther row. Returns (floor(d_k), t_k) per
+    rung kept. Reading: a rung whose distance is an integer inside the window is the same
+    key as a window row and is dropped, so that integer alphas give exactly the
+    integer-offset key set (the page states the gather and the boolean-mask paths agree
+    for integer offsets, section 2 "Implementation note")."""
+    out = []
+    for f in rungs:
+        d = float(alpha) * float(f)
+        lo = math.floor(d)
+        t = d - lo
+        if t == 0.0 and lo <= window:
+            continue
+        out.append((int(lo), float(t)))
+    return out

@@ -569,3 +569,51 @@ def test_backward_invariants_and_sampled_forms():
     gk, gv = oracle.attention_rows_dkdv(q, k, v, do, rp, ci, b, 1, smp_kv)
     assert np.abs(gk - np.stack([dk[s, j, hk] for s, j, hk in smp_kv])).max() < 1e-12
     assert np.abs(gv - np.stack([dv[s, j, hk] for s, j, hk in smp_kv])).max() < 1e-12
+
+
+# ------------------------------------------------------------------ interpolated gather
+
+@pytest.mark.parametrize("alpha", [1, 2, 3])
+def test_interp_integer_alpha_is_the_integer_offset_set(alpha):
+    """Integer alpha: every rung is an exact row; the result is the integer-offset
+    attention of the same rungs (window duplicates removed)."""
+    rng = np.random.default_rng(alpha)
+    q, k, v = (rng.standard_normal((1, 300, 2, 8)) for _ in range(3))
+    W = 6
+    rungs = oracle.fib_rungs(15)
+    lt = oracle.interp_rungs(alpha, rungs, W)
+    assert all(t == 0.0 for _, t in lt)
+    o1, l1 = oracle.attention_offsets_interp(q, k, v, W, lt)
+    o2, l2 = oracle.attention_offsets(q, k, v, W, oracle.fib_offsets(Fraction(alpha), rungs))
+    assert np.abs(o1 - o2).max() < 1e-12 and np.abs(l1 - l2).max() < 1e-12
+
+
+def test_interp_linear_rows_give_keys_at_continuous_positions():
+    """Keys and values linear in the position, K[j] = A + j B: the interpolated rung of
+    query i is exactly the key at the continuous position i - alpha f_k, so attention
+    equals a softmax over the closed-form keys A + (i - d) B."""
+    rng = np.random.default_rng(3)
+    n, d, W = 400, 8, 4
+    A, B, C, E = (rng.standard_normal(d) for _ in range(4))
+    pos = np.arange(n, dtype=np.float64)
+    k = (A[None, :] + pos[:, None] * B[None, :] / n)[None, :, None, :]
+    v = (C[None, :] + pos[:, None] * E[None, :] / n)[None, :, None, :]
+    q = rng.standard_normal((1, n, 1, d))
+    alpha = 0.8317
+    lt = oracle.interp_rungs(alpha, oracle.fib_rungs(15), W)
+    assert any(t > 0 for _, t in lt)
+    smp = [(0, i, 0) for i in (0, 5, 37, 120, 399)]
+    o, lse = oracle.attention_offsets_interp(q, k, v, W, lt, samples=smp)
+    scale = 1.0 / np.sqrt(d)
+    for t_idx, (_, i, _) in enumerate(smp):
+        ps = [i - dl for dl in range(W + 1) if i - dl >= 0]
+        ps += [i - alpha * f for f in oracle.fib_rungs(15)
+               if i - alpha * f >= 0 and not (float(alpha * f).is_integer() and alpha * f <= W)]
+        ps = np.array(ps)
+        keys = A[None, :] + ps[:, None] * B[None, :] / n
+        vals = C[None, :] + ps[:, None] * E[None, :] / n
+        sc = keys @ q[0, i, 0] * scale
+        m = sc.max()
+        p = np.exp(sc - m)
+        assert abs(lse[t_idx] - (m + np.log(p.sum()))) < 1e-12
+        assert np.abs(o[t_idx] - (p / p.sum()) @ vals).max() < 1e-12
