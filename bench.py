@@ -34,6 +34,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import re
 import statistics
@@ -268,6 +269,14 @@ class BlockSparseCase:
         self.attend()
 
 
+def _fib_rungs(k: int) -> list[int]:
+    out, a, b = [], 1, 2
+    for _ in range(k):
+        out.append(a)
+        a, b = b, a + b
+    return out
+
+
 class OffsetCase:
     """16-layer window + Fibonacci-offset pass (one launch per layer, own Q/K/V each)."""
 
@@ -285,8 +294,11 @@ class OffsetCase:
         self.W = W
         self.layers = []
         ladder = sa.sa_pow2_offsets if cfg.get("ladder") == "pow2" else sa.sa_fib_offsets
+        self.interp = bool(cfg.get("interp", False))
+        self.alphas = []
         for l in range(L):
             num, den = sa.sa_layer_alpha(l, L, cfg["alpha_lo"], cfg["alpha_hi"], cfg.get("stride", 1))
+            self.alphas.append(num / den)
             offs = ladder(num, den, cfg["n_rungs"], W, n)
             qb, kb, vb = qkv_bits(cfg, seed_offset=l)
             q, k, v = (torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev) for x in (qb, kb, vb))
@@ -296,14 +308,25 @@ class OffsetCase:
         # algorithmic bytes: Q, K, V read once, O and LSE written once, per layer
         self.bytes = L * (bt * n * (2 * h * d * 2 + 2 * hkv * d * 2) + bt * h * n * 4)
         keys = 0
-        for *_, offs in self.layers:
+        for (*_, offs), alpha in zip(self.layers, self.alphas):
             i = np.arange(n)
-            keys += int(np.sum(np.minimum(W, i) + 1)) + sum(int(max(0, n - dd)) for dd in offs)
+            keys += int(np.sum(np.minimum(W, i) + 1))
+            if self.interp:   # rung k is one entry for every query i >= alpha f_k (two rows when fractional)
+                for f in _fib_rungs(cfg["n_rungs"]):
+                    dd = alpha * f
+                    if not (float(dd).is_integer() and dd <= W):
+                        keys += max(0, n - int(math.ceil(dd)))
+            else:
+                keys += sum(int(max(0, n - dd)) for dd in offs)
         self.edges = keys * bt * h
         self.flops = 4 * self.edges * d
         self.tokens = bt * n
 
     def step(self):
+        if self.interp:
+            for (q, k, v, o, lse, _), alpha in zip(self.layers, self.alphas):
+                self.sa.sa_offset_attn_interp_fwd(q, k, v, self.W, alpha, o, lse, self.cfg["n_rungs"])
+            return
         for q, k, v, o, lse, offs in self.layers:
             self.sa.sa_offset_attn_fwd(q, k, v, self.W, offs, o, lse)
 
@@ -577,6 +600,8 @@ def _measure_rows(torch, sa, dev, flush, peaks, max_over_ranks, only=None, steps
         rows.update(_row_fib(torch, dev, flush, peaks, max_over_ranks, steps, warm))
     if want("fib_8k_coprime_16_layers"):
         rows.update(_row_fib(torch, dev, flush, peaks, max_over_ranks, steps, warm, name="fib_8k_coprime"))
+    if want("fib_interp_8k_16_layers"):
+        rows.update(_row_fib(torch, dev, flush, peaks, max_over_ranks, steps, warm, name="fib_interp_8k"))
     if want("pow2_8k_16_layers"):
         rows.update(_row_fib(torch, dev, flush, peaks, max_over_ranks, steps, warm, name="pow2_8k"))
     if only == "fib_8k_2_layers":   # same per-layer launch, small device footprint (profiling)
@@ -674,7 +699,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--only-row", choices=["bigbird_16k", "long_topk_64k", "cas_heads_8k", "bwd_bytelm_topk_8k",
                                            "fib_8k_16_layers",
-                                           "fib_8k_coprime_16_layers", "pow2_8k_16_layers", "fib_8k_2_layers"],
+                                           "fib_8k_coprime_16_layers", "pow2_8k_16_layers", "fib_interp_8k_16_layers",
+                                           "fib_8k_2_layers"],
                     default=None,
                     help="time one other hot-path row only (profiling aid; prints that row, not the bench line)")
     args = ap.parse_args()

@@ -72,6 +72,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.sa_offset_attn_fwd.argtypes = [_P, _P, _P, _I64x3, _I64x3, _I64x3, ctypes.c_int32, ctypes.c_int32,
                                        ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P,
                                        ctypes.c_int32, ctypes.c_float, _P, _P, _P]
+    lib.sa_offset_attn_interp_fwd.argtypes = [_P, _P, _P, _I64x3, _I64x3, _I64x3] + [ctypes.c_int32] * 6 + \
+        [ctypes.c_double, ctypes.c_int32, ctypes.c_int32, ctypes.c_float, _P, _P, _P]
     lib.sa_fib_offsets.argtypes = [ctypes.c_int32] * 5 + [_P, ctypes.c_int32, _P]
     lib.sa_pow2_offsets.argtypes = [ctypes.c_int32] * 5 + [_P, ctypes.c_int32, _P]
     lib.sa_layer_alpha.argtypes = [ctypes.c_int32] * 7 + [_P, _P]
@@ -79,9 +81,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
                                     ctypes.c_int32]
     lib.sa_device_status.argtypes = [_P]
     for name in ("sa_mask_nnz_bound", "sa_build_mask", "sa_attn_fwd", "sa_attn_fwd_heads", "sa_attn_bwd",
-                 "sa_attn_bwd_noalloc",
-                 "sa_attn_bwd_workspace_size", "sa_offset_attn_fwd",
-                 "sa_fib_offsets", "sa_pow2_offsets", "sa_layer_alpha", "sa_block_ratios", "sa_device_status"):
+                 "sa_attn_bwd_noalloc", "sa_attn_bwd_workspace_size", "sa_offset_attn_fwd",
+                 "sa_offset_attn_interp_fwd", "sa_fib_offsets", "sa_pow2_offsets", "sa_layer_alpha", "sa_block_ratios",
+                 "sa_device_status"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -212,6 +214,26 @@ def _ladder(fn: str, alpha_num: int, alpha_den: int, n_rungs: int, window: int, 
     return [int(buf[i]) for i in range(cnt.value)]
 
 
+def sa_offset_attn_interp_fwd(q, k, v, window: int, alpha: float, o, lse, n_rungs: int = 15, ladder: int = 0,
+                              softmax_scale: float | None = None, stream=None) -> None:
+    b, n, h, d = q.shape
+    hkv = k.shape[2]
+    scale = 1.0 / float(np.sqrt(d)) if softmax_scale is None else float(softmax_scale)
+    _check("sa_offset_attn_interp_fwd", load_library().sa_offset_attn_interp_fwd(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), _strides(q), _strides(k), _strides(o), b, n, h, hkv, d, window,
+        float(alpha), n_rungs, ladder, scale, o.data_ptr(), lse.data_ptr(), _stream_ptr(stream)))
+
+
+def offset_attn_interp_fwd(q, k, v, window: int, alpha: float, n_rungs: int = 15, ladder: int = 0,
+                           softmax_scale: float | None = None):
+    import torch
+    b, n, h, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((b, h, n), dtype=torch.float32, device=q.device)
+    sa_offset_attn_interp_fwd(q, k, v, window, alpha, o, lse, n_rungs, ladder, softmax_scale)
+    return o, lse
+
+
 def sa_fib_offsets(alpha_num: int, alpha_den: int, n_rungs: int, window: int, n_tokens: int) -> list[int]:
     return _ladder("sa_fib_offsets", alpha_num, alpha_den, n_rungs, window, n_tokens)
 
@@ -299,8 +321,13 @@ def offset_attn_fwd(q, k, v, window: int, offsets, softmax_scale: float | None =
 
 
 __all__ = [
-    "build_library", "load_library", "SAError", "MaskParams", "mask_params", "sa_mask_nnz_bound", "sa_build_mask",
-    "sa_attn_fwd", "sa_attn_fwd_heads", "sa_attn_bwd", "sa_attn_bwd_workspace_size", "attn_bwd",
-    "sa_attn_bwd_noalloc", "sa_pow2_offsets", "sa_layer_alpha", "attn_fwd_heads", "LITERAL_LOCAL", "LITERAL_PAIRS", "sa_offset_attn_fwd", "sa_fib_offsets", "sa_block_ratios", "sa_device_status", "build_mask",
-    "attn_fwd", "offset_attn_fwd", "MASK_TOPK", "MASK_BIGBIRD", "MASK_FULL", "MASK_LITERAL_MEAN",
+    "build_library", "load_library", "SAError", "MaskParams", "mask_params",
+    # C ABI
+    "sa_mask_nnz_bound", "sa_build_mask", "sa_attn_fwd", "sa_attn_fwd_heads", "sa_attn_bwd",
+    "sa_attn_bwd_workspace_size", "sa_attn_bwd_noalloc", "sa_offset_attn_fwd", "sa_offset_attn_interp_fwd",
+    "sa_fib_offsets", "sa_pow2_offsets", "sa_layer_alpha", "sa_block_ratios", "sa_device_status",
+    # allocating conveniences
+    "build_mask", "attn_fwd", "attn_fwd_heads", "attn_bwd", "offset_attn_fwd", "offset_attn_interp_fwd",
+    # constants
+    "MASK_TOPK", "MASK_BIGBIRD", "MASK_FULL", "MASK_LITERAL_MEAN", "LITERAL_LOCAL", "LITERAL_PAIRS",
 ]

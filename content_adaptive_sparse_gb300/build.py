@@ -1,6 +1,6 @@
 """Compile libsa.so in-tree for sm_103a with nvcc (no cmake, no torch extension).
 
-The five translation units are compiled in parallel and linked against the shared
+The translation units are compiled in parallel and linked against the shared
 CUDA runtime. The result is ``content_adaptive_sparse_gb300/lib/libsa.so``. A rebuild
 happens only when a source or header is newer than the library.
 """
@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libsa.so")
-SOURCES = ["sa_api.cu", "mask_build.cu", "attn_fwd.cu", "attn_bwd.cu", "offset_attn.cu"]
+SOURCES = ["sa_api.cu", "mask_build.cu", "attn_fwd.cu", "attn_bwd.cu", "offset_attn.cu", "offset_interp.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

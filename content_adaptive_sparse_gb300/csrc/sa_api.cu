@@ -5,6 +5,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <cmath>
 #include <numeric>
 #include <atomic>
 #include <thread>
@@ -396,6 +397,63 @@ int ladder_offsets(int ladder, int32_t alpha_num, int32_t alpha_den, int32_t n_r
 }  // namespace
 
 extern "C" {
+
+int sa_offset_attn_interp_fwd(const void* q, const void* k, const void* v, const int64_t q_strides[3],
+                              const int64_t kv_strides[3], const int64_t o_strides[3], int32_t batch,
+                              int32_t n_tokens, int32_t heads, int32_t kv_heads, int32_t head_dim, int32_t window,
+                              double alpha, int32_t n_rungs, int32_t ladder, float softmax_scale, void* o, float* lse,
+                              void* stream) {
+  int st = check_attn_common(q, k, v, q_strides, kv_strides, o_strides, batch, n_tokens, heads, kv_heads, o, lse);
+  if (st != SA_OK) return st;
+  if (!(softmax_scale > 0.f) || !(alpha > 0.0) || !std::isfinite(alpha)) return SA_ERR_INVALID_ARG;
+  if (window < 0 || n_rungs < 0 || (ladder != 0 && ladder != 1)) return SA_ERR_INVALID_ARG;
+  if (window > sa::kMaxWindow || head_dim != 64) return SA_ERR_UNSUPPORTED;
+  sa::InterpArgs a;
+  a.n_rungs = 0;
+  int64_t f = 1, g = 2;   // rung ladder
+  for (int r = 0;; ++r) {
+    if (n_rungs > 0 ? r >= n_rungs : f > n_tokens) break;
+    const double d = alpha * (double)f;
+    if (d >= (double)n_tokens) {                 // never reached by any query
+    } else {
+      const double lo = std::floor(d);
+      const double t = d - lo;
+      if (!(t == 0.0 && lo <= (double)window)) {
+        if (a.n_rungs >= sa::kMaxInterpRungs) return SA_ERR_UNSUPPORTED;
+        a.lo[a.n_rungs] = (int32_t)lo;
+        a.t[a.n_rungs] = (float)t;
+        ++a.n_rungs;
+      }
+    }
+    if (ladder == 0) {
+      const int64_t nxt = f + g;
+      f = g;
+      g = nxt;
+    } else {
+      f *= 2;
+    }
+    if (f > ((int64_t)1 << 40)) break;
+  }
+  if ((int64_t)batch * heads * ((n_tokens + 31) / 32) > (int64_t)INT32_MAX * 4) return SA_ERR_UNSUPPORTED;
+  if (!device_ok()) return SA_ERR_CUDA;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  for (int i = 0; i < 3; ++i) {
+    a.q_strides[i] = q_strides[i];
+    a.kv_strides[i] = kv_strides[i];
+    a.o_strides[i] = o_strides[i];
+  }
+  a.batch = batch;
+  a.n_tokens = n_tokens;
+  a.heads = heads;
+  a.kv_heads = kv_heads;
+  a.window = window;
+  a.softmax_scale = softmax_scale;
+  return sa::launch_offset_interp_fwd(a, static_cast<cudaStream_t>(stream));
+}
 
 int sa_fib_offsets(int32_t alpha_num, int32_t alpha_den, int32_t n_rungs, int32_t window, int32_t n_tokens,
                    int32_t* h_out, int32_t capacity, int32_t* h_count) {

@@ -60,6 +60,24 @@ struct OffsetArgs {
 int launch_offset_attn_fwd(const OffsetArgs& a, cudaStream_t stream);
 unsigned int offset_read_and_clear_error(cudaStream_t stream);
 
+// offset_interp.cu
+constexpr int kMaxInterpRungs = 64;
+struct InterpArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  int64_t q_strides[3];
+  int64_t kv_strides[3];
+  int64_t o_strides[3];
+  int32_t batch, n_tokens, heads, kv_heads, window, n_rungs;
+  int32_t lo[kMaxInterpRungs];   // floor of the rung distance
+  float t[kMaxInterpRungs];      // weight of the farther row
+  float softmax_scale;
+};
+int launch_offset_interp_fwd(const InterpArgs& a, cudaStream_t stream);
+
 // attn_bwd.cu
 struct BwdArgs {
   const void* q;

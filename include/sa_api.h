@@ -198,6 +198,23 @@ int sa_offset_attn_fwd(const void* q, const void* k, const void* v, const int64_
                        int32_t heads, int32_t kv_heads, int32_t head_dim, int32_t window, const int32_t* h_offsets,
                        int32_t n_offsets, float softmax_scale, void* o, float* lse, void* stream);
 
+/* Window plus interpolated-rung attention forward ("Depth-Staggered Fibonacci Spacing ...",
+ * section 2 "Attended set"; the interpolated gather of a continuous alpha). Rung k has the
+ * distance d_k = alpha * f_k (IEEE double product) over the Fibonacci rungs (ladder 0) or
+ * the power-of-2 rungs (ladder 1), the first n_rungs of them (n_rungs > 0) or every rung
+ * f_k <= n_tokens (n_rungs == 0). With lo = floor(d_k) and t = d_k - lo, query i sees
+ *   the window rows i - delta, delta = 0..window, i - delta >= 0, and
+ *   for every rung with i - d_k >= 0 the key (1 - t) k[i - lo] + t k[i - lo - 1] and the
+ *   value (1 - t) v[i - lo] + t v[i - lo - 1]
+ * (a rung with an integer distance inside the window is the window row itself and is not
+ * counted twice). head_dim == 64; window in [0, 64]; at most 64 rungs remain; other
+ * arguments as in sa_offset_attn_fwd. alpha must be finite and > 0. */
+int sa_offset_attn_interp_fwd(const void* q, const void* k, const void* v, const int64_t q_strides[3],
+                              const int64_t kv_strides[3], const int64_t o_strides[3], int32_t batch,
+                              int32_t n_tokens, int32_t heads, int32_t kv_heads, int32_t head_dim, int32_t window,
+                              double alpha, int32_t n_rungs, int32_t ladder, float softmax_scale, void* o, float* lse,
+                              void* stream);
+
 /* Distinct offsets d_k = round_half_even(alpha * f_k), alpha = alpha_num / alpha_den > 0,
  * over Fibonacci rungs f = 1, 2, 3, 5, 8, ... ("Depth-Staggered Fibonacci Spacing ...",
  * section 2: K = 15 rungs up to 987). n_rungs > 0 takes the first n_rungs rungs;

@@ -33,7 +33,7 @@ def _declared_functions():
 def test_header_symbols_exported(lib):
     names = _declared_functions()
     assert {"sa_build_mask", "sa_attn_fwd", "sa_attn_fwd_heads", "sa_offset_attn_fwd", "sa_pow2_offsets",
-            "sa_attn_bwd", "sa_attn_bwd_workspace_size", "sa_attn_bwd_noalloc",
+            "sa_attn_bwd", "sa_attn_bwd_workspace_size", "sa_attn_bwd_noalloc", "sa_offset_attn_interp_fwd",
             "sa_layer_alpha", "sa_fib_offsets", "sa_block_ratios",
             "sa_mask_nnz_bound", "sa_device_status", "sa_status_string", "sa_version"} <= set(names)
     for n in names:
@@ -143,6 +143,11 @@ def test_argument_validation_before_any_launch(lib):
     rp9 = P9(*([256] * 9))
     assert lib.sa_attn_fwd_heads(p16, p16, p16, s, s, s, 1, 8192, 12, 12, 64, 64, 1, 9, rp9, rp9, hm, 0,
                                  ctypes.c_float(0.125), p16, p16, None) == -2
+    # interpolated gather: alpha must be positive, head_dim 64 only
+    assert lib.sa_offset_attn_interp_fwd(p16, p16, p16, s, s, s, 1, 8192, 8, 8, 64, 8, ctypes.c_double(-0.5), 15, 0,
+                                         ctypes.c_float(0.125), p16, p16, None) == -1
+    assert lib.sa_offset_attn_interp_fwd(p16, p16, p16, s, s, s, 1, 8192, 8, 8, 32, 8, ctypes.c_double(0.8), 15, 0,
+                                         ctypes.c_float(0.125), p16, p16, None) == -2
     offs = (ctypes.c_int32 * 2)(5, 9)        # offset inside the window -> invalid
     assert lib.sa_offset_attn_fwd(p16, p16, p16, s, s, s, 1, 8192, 8, 8, 64, 8, offs, 2,
                                   ctypes.c_float(0.125), p16, p16, None) == -1

@@ -7,7 +7,7 @@ import pytest
 import content_adaptive_sparse_gb300 as sa
 import oracle
 from workloads import bf16_bits_to_f64, bf16_normal_bits, qkv_bits, workload
-from gpu_helpers import assert_attention_close, bf16_to_f64, to_dev, torch_cuda
+from gpu_helpers import LSE_MAX_ABS, O_MAX_ABS, assert_attention_close, bf16_to_f64, to_dev, torch_cuda
 
 pytestmark = pytest.mark.gpu
 
@@ -118,3 +118,75 @@ def test_packed_strided_inputs():
     f = bf16_bits_to_f64(packed)
     _run_offsets(f[:, :, 0], f[:, :, 1], f[:, :, 2], t[:, :, 0], t[:, :, 1], t[:, :, 2], 8,
                  [9, 13, 21, 34, 55, 89, 144, 233, 377, 610], "packed qkv")
+
+
+# ---------------------------------------------------------------- interpolated gather (continuous alpha)
+
+def _run_interp(bt, n, h, hkv, window, alpha, n_rungs=15, ladder=0, seed=0, qmul=1.0):
+    torch = torch_cuda()
+    rng = np.random.default_rng(seed)
+    qb = bf16_normal_bits(rng, (bt, n, h, 64), 0.125 * qmul)
+    kb = bf16_normal_bits(rng, (bt, n, hkv, 64), 0.125)
+    vb = bf16_normal_bits(rng, (bt, n, hkv, 64), 0.125)
+    o, lse = sa.offset_attn_interp_fwd(to_dev(qb), to_dev(kb), to_dev(vb), window, alpha, n_rungs, ladder)
+    torch.cuda.synchronize()
+    assert sa.sa_device_status() == 0
+    if ladder == 0:
+        rungs = oracle.fib_rungs(n_rungs) if n_rungs else oracle.fib_rungs_upto(n)
+    else:
+        rungs = oracle.pow2_rungs(n_rungs) if n_rungs else oracle.pow2_rungs_upto(n)
+    lt = oracle.interp_rungs(alpha, rungs, window)
+    o_ref, lse_ref = oracle.attention_offsets_interp(bf16_bits_to_f64(qb), bf16_bits_to_f64(kb),
+                                                     bf16_bits_to_f64(vb), window, lt)
+    return assert_attention_close(bf16_to_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref,
+                                  f"interp W={window} alpha={alpha}")
+
+
+@pytest.mark.parametrize("alpha", [0.8317, 1.2345, 0.5, 1.5])
+def test_interp_alphas_gqa(alpha):
+    _run_interp(1, 1000, 4, 2, 8, alpha, seed=int(alpha * 1000), qmul=3.0)
+
+
+def test_interp_windows_pow2_and_all_rungs():
+    _run_interp(2, 520, 2, 2, 0, 0.777, seed=1)                  # window 0: self plus rungs
+    _run_interp(1, 700, 2, 1, 12, 1.1, ladder=1, n_rungs=11, seed=2, qmul=2.0)
+    _run_interp(1, 900, 2, 2, 6, 0.9, n_rungs=0, seed=3)         # every rung up to N
+
+
+def test_interp_integer_alpha_matches_integer_offset_kernel():
+    """alpha = 1 and 2: the interpolated path and the integer-offset kernel see the same
+    key set; both match the oracle, and each other to the combined tolerance."""
+    torch = torch_cuda()
+    rng = np.random.default_rng(12)
+    n = 1024
+    qb, kb, vb = (bf16_normal_bits(rng, (1, n, 2, 64), 0.3) for _ in range(3))
+    q, k, v = to_dev(qb), to_dev(kb), to_dev(vb)
+    for alpha in (1, 2):
+        o1, l1 = sa.offset_attn_interp_fwd(q, k, v, 8, float(alpha))
+        offs = sa.sa_fib_offsets(alpha, 1, 15, 8, n)
+        o2, l2 = sa.offset_attn_fwd(q, k, v, 8, offs)
+        torch.cuda.synchronize()
+        assert (o1.float() - o2.float()).abs().max().item() < 2 * O_MAX_ABS
+        assert (l1 - l2).abs().max().item() < 2 * LSE_MAX_ABS
+
+
+def test_interp_fib_8k_sampled():
+    torch = torch_cuda()
+    cfg = workload("fib_8k", layers=1)
+    qb, kb, vb = qkv_bits(cfg)
+    alpha = 0.5 + 1.0 / (1.0 + np.exp(-0.37))            # a learned-style alpha in (0.5, 1.5)
+    o, lse = sa.offset_attn_interp_fwd(to_dev(qb), to_dev(kb), to_dev(vb), cfg["window"], alpha)
+    torch.cuda.synchronize()
+    assert sa.sa_device_status() == 0
+    rng = np.random.default_rng(2)
+    bt, n, h = cfg["batch"], cfg["n_tokens"], cfg["heads"]
+    smp = [(int(rng.integers(bt)), int(rng.integers(n)), int(rng.integers(h))) for _ in range(40)]
+    smp += [(0, 0, 0), (7, n - 1, 7), (3, 1, 2), (5, 987, 4)]
+    lt = oracle.interp_rungs(alpha, oracle.fib_rungs(15), cfg["window"])
+    o_ref, lse_ref = oracle.attention_offsets_interp(qb, kb, vb, cfg["window"], lt, samples=smp,
+                                                     convert=bf16_bits_to_f64)
+    o_np = bf16_to_f64(o)
+    lse_np = lse.cpu().numpy().astype(np.float64)
+    o_g = np.stack([o_np[s, i, hh] for s, i, hh in smp])
+    l_g = np.array([lse_np[s, hh, i] for s, i, hh in smp])
+    assert_attention_close(o_g, l_g, o_ref, lse_ref, "interp fib 8k")

@@ -26,6 +26,8 @@ Workloads (shapes and pattern parameters as the pages and the task state them):
                        Table 8 and Appendix B "Head-specific mask distribution").
 * ``fib_8k_coprime`` / ``pow2_8k`` - ``fib_8k`` with the coprime stagger of the alpha
                        ramp, and with the power-of-2 control base (same page, section 2).
+* ``fib_interp_8k``  - ``fib_8k`` through the interpolated gather of a continuous alpha
+                       (the same page, section 2 "Attended set").
 * ``long_topk_64k``  - 1 x 65536 byte tokens, block 128, 16 heads, d_h 128, top-64
                        (top-k swept over 16/64/256), plus ``full_16k``.
 
@@ -77,6 +79,11 @@ WORKLOADS = {
                            seed=46),
     "pow2_8k": dict(kind="fib", layers=16, batch=8, n_tokens=8192, heads=8, kv_heads=8, head_dim=64, window=8,
                     alpha_lo=(1, 2), alpha_hi=(2, 1), n_rungs=11, ladder="pow2", std=1.0 / 8.0, seed=46),
+    # interpolated gather: the page's ramp alpha_l = 0.5 + l / 15 taken as real numbers
+    # (continuous distances alpha f_k, interpolated between neighbouring rows)
+    "fib_interp_8k": dict(kind="fib", layers=16, batch=8, n_tokens=8192, heads=8, kv_heads=8, head_dim=64,
+                          window=8, alpha_lo=(1, 2), alpha_hi=(3, 2), n_rungs=15, interp=True, std=1.0 / 8.0,
+                          seed=46),
     "long_topk_64k": dict(kind="topk", batch=1, n_tokens=65536, block=128, heads=16, kv_heads=16,
                           head_dim=128, window_blocks=4, global_blocks=1, topk=64, causal=1,
                           std=1.0 / np.sqrt(128.0), bytes="phrase_random", seed=47),
