@@ -32,7 +32,7 @@ from .fib import (fib_rungs, fib_rungs_upto, pow2_rungs, pow2_rungs_upto, alpha_
                   offset_key_set, interp_rungs)
 from .attention import (attention_csr, attention_csr_block, attention_csr_heads, attention_offsets,
                         dense_masked_attention, attention_rows_csr, attention_csr_backward, attention_rows_dq,
-                        attention_rows_dkdv, attention_offsets_interp)
+                        attention_rows_dkdv, attention_offsets_interp, attention_csr_backward_heads)
 
 __all__ = [
     "block_ratios", "zlib_version", "philox4x64_10", "philox_word", "MaskParams", "build_csr",
@@ -43,4 +43,5 @@ __all__ = [
     "attention_csr_block",
     "attention_offsets", "dense_masked_attention", "attention_rows_csr", "attention_csr_backward",
     "attention_rows_dq", "attention_rows_dkdv", "attention_offsets_interp", "interp_rungs",
+    "attention_csr_backward_heads",
 ]

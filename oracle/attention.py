@@ -347,3 +347,24 @@ def attention_offsets_interp(q, k, v, window: int, rungs_lo_t, scale: float | No
     if not full:
         return o, lse
     return o.reshape(bt, n, h, d), lse.reshape(bt, n, h).transpose(0, 2, 1)
+
+
+def attention_csr_backward_heads(q, k, v, d_o, csrs, head_mask, block: int, causal: int,
+                                 scale: float | None = None):
+    """Backward of ``attention_csr_heads``: query head h uses CSR ``csrs[head_mask[h]]``;
+    dK / dV of a key/value head sum over its query heads (each with its own CSR)."""
+    bt, n, h, d = q.shape
+    hkv = k.shape[2]
+    g = h // hkv
+    dq = np.zeros((bt, n, h, d))
+    dk = np.zeros((bt, n, hkv, d))
+    dv = np.zeros((bt, n, hkv, d))
+    for hh in range(h):
+        hk = hh // g
+        rp, ci = csrs[head_mask[hh]]
+        a, b_, c = attention_csr_backward(q[:, :, hh:hh + 1], k[:, :, hk:hk + 1], v[:, :, hk:hk + 1],
+                                          d_o[:, :, hh:hh + 1], rp, ci, block, causal, scale)
+        dq[:, :, hh] = a[:, :, 0]
+        dk[:, :, hk] += b_[:, :, 0]
+        dv[:, :, hk] += c[:, :, 0]
+    return dq, dk, dv

@@ -617,3 +617,31 @@ def test_interp_linear_rows_give_keys_at_continuous_positions():
         p = np.exp(sc - m)
         assert abs(lse[t_idx] - (m + np.log(p.sum()))) < 1e-12
         assert np.abs(o[t_idx] - (p / p.sum()) @ vals).max() < 1e-12
+
+
+def test_backward_heads_matches_central_differences():
+    """Per-head CSRs with a KV group shared by heads of different groups: the per-head
+    backward against central differences of the per-head forward oracle."""
+    rng = np.random.default_rng(17)
+    bt, n, h, hkv, d, b = 1, 64, 4, 2, 4, 8
+    q, k, v, do = (rng.standard_normal((bt, n, hh, d)) for hh in (h, hkv, hkv, h))
+    ratios = rng.choice([0.5, 1.0, 1.5], size=(1, n // b))
+    csrs = [om.build_csr(om.MaskParams("literal_mean", b, n, 1, 1, components=c), ratios, 1) for c in (1, 2, 3)]
+    head_mask = [0, 2, 1, 0]                      # KV head 0: local + full; KV head 1: literal + local
+    dq, dk, dv = oracle.attention_csr_backward_heads(q, k, v, do, csrs, head_mask, b, 1)
+
+    def loss(qq, kk, vv):
+        o, _ = oracle.attention_csr_heads(qq, kk, vv, csrs, head_mask, b, 1)
+        return float(np.sum(o * do))
+
+    eps = 1e-6
+    for x, g in ((q, dq), (k, dk), (v, dv)):
+        flat = x.reshape(-1)
+        for idx in rng.choice(flat.size, size=30, replace=False):
+            old = flat[idx]
+            flat[idx] = old + eps
+            lp = loss(q, k, v)
+            flat[idx] = old - eps
+            lm = loss(q, k, v)
+            flat[idx] = old
+            assert abs((lp - lm) / (2 * eps) - g.reshape(-1)[idx]) < 1e-7 * max(1.0, abs(g.reshape(-1)[idx]))
