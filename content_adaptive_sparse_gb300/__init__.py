@@ -67,6 +67,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.sa_attn_bwd_workspace_size.argtypes = [ctypes.c_int32] * 5 + [ctypes.c_int64, _P]
     lib.sa_attn_bwd.argtypes = [_P, _P, _P, _P, _P, _P, _I64x3, _I64x3, _I64x3] + [ctypes.c_int32] * 7 + \
         [_P, _P, ctypes.c_int32, ctypes.c_float, _P, _P, _P, _P, ctypes.c_size_t, _P]
+    lib.sa_attn_bwd_heads.argtypes = [_P, _P, _P, _P, _P, _P, _I64x3, _I64x3, _I64x3] + [ctypes.c_int32] * 8 + \
+        [_P, _P, _P, _P, ctypes.c_int32, ctypes.c_float, _P, _P, _P, _P, ctypes.c_size_t, _P]
     lib.sa_attn_bwd_noalloc.argtypes = [_P, _P, _P, _P, _P, _P, _I64x3, _I64x3, _I64x3] + \
         [ctypes.c_int32] * 7 + [_P, _P, ctypes.c_int64, ctypes.c_int32, ctypes.c_float, _P, _P, _P, _P]
     lib.sa_offset_attn_fwd.argtypes = [_P, _P, _P, _I64x3, _I64x3, _I64x3, ctypes.c_int32, ctypes.c_int32,
@@ -81,7 +83,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
                                     ctypes.c_int32]
     lib.sa_device_status.argtypes = [_P]
     for name in ("sa_mask_nnz_bound", "sa_build_mask", "sa_attn_fwd", "sa_attn_fwd_heads", "sa_attn_bwd",
-                 "sa_attn_bwd_noalloc", "sa_attn_bwd_workspace_size", "sa_offset_attn_fwd",
+                 "sa_attn_bwd_noalloc", "sa_attn_bwd_heads", "sa_attn_bwd_workspace_size", "sa_offset_attn_fwd",
                  "sa_offset_attn_interp_fwd", "sa_fib_offsets", "sa_pow2_offsets", "sa_layer_alpha", "sa_block_ratios",
                  "sa_device_status"):
         getattr(lib, name).restype = ctypes.c_int
@@ -179,6 +181,41 @@ def sa_attn_bwd(q, k, v, o, d_o, lse, row_ptr, col_idx, block: int, causal: int,
         _strides(k), _strides(o), b, n, h, hkv, d, block, int(causal), row_ptr.data_ptr(), col_idx.data_ptr(),
         int(bool(csr_shared)), scale, dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
+
+
+def sa_attn_bwd_heads(q, k, v, o, d_o, lse, csrs, head_mask, block: int, causal: int, dq, dk, dv, workspace,
+                      csr_shared: bool = False, softmax_scale: float | None = None, stream=None) -> None:
+    """``csrs``: list of (row_ptr, col_idx) device tensors; query head h uses
+    ``csrs[head_mask[h]]``; each col_idx's size is its capacity."""
+    b, n, h, d = q.shape
+    hkv = k.shape[2]
+    nm = len(csrs)
+    rps = (ctypes.c_void_p * nm)(*[rp.data_ptr() for rp, _ in csrs])
+    cis = (ctypes.c_void_p * nm)(*[ci.data_ptr() for _, ci in csrs])
+    caps = (ctypes.c_int64 * nm)(*[ci.numel() for _, ci in csrs])
+    hm = np.ascontiguousarray(np.asarray(head_mask, dtype=np.int32))
+    if hm.shape != (h,):
+        raise ValueError("head_mask needs one CSR index per query head")
+    scale = 1.0 / float(np.sqrt(d)) if softmax_scale is None else float(softmax_scale)
+    _check("sa_attn_bwd_heads", load_library().sa_attn_bwd_heads(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), d_o.data_ptr(), lse.data_ptr(), _strides(q),
+        _strides(k), _strides(o), b, n, h, hkv, d, block, int(causal), nm, ctypes.cast(rps, _P), ctypes.cast(cis, _P),
+        ctypes.cast(caps, _P), hm.ctypes.data, int(bool(csr_shared)), scale, dq.data_ptr(), dk.data_ptr(),
+        dv.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
+
+
+def attn_bwd_heads(q, k, v, o, lse, d_o, csrs, head_mask, block: int, causal: int, csr_shared: bool = False,
+                   softmax_scale: float | None = None):
+    """Allocate dq / dk / dv and the workspace, run the head-group backward."""
+    import torch
+    b, n, h, d = q.shape
+    cap = sum(ci.numel() for _, ci in csrs)
+    ws_bytes = sa_attn_bwd_workspace_size(b, n, h, block, (1 if csr_shared else b) * len(csrs), cap)
+    ws = torch.empty((ws_bytes,), dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    sa_attn_bwd_heads(q, k, v, o, d_o, lse, csrs, head_mask, block, causal, dq, dk, dv, ws, csr_shared,
+                      softmax_scale)
+    return dq, dk, dv
 
 
 def sa_attn_bwd_noalloc(q, k, v, o, d_o, lse, row_ptr, col_idx, block: int, causal: int, dq, dk, dv,
@@ -324,10 +361,10 @@ __all__ = [
     "build_library", "load_library", "SAError", "MaskParams", "mask_params",
     # C ABI
     "sa_mask_nnz_bound", "sa_build_mask", "sa_attn_fwd", "sa_attn_fwd_heads", "sa_attn_bwd",
-    "sa_attn_bwd_workspace_size", "sa_attn_bwd_noalloc", "sa_offset_attn_fwd", "sa_offset_attn_interp_fwd",
+    "sa_attn_bwd_workspace_size", "sa_attn_bwd_noalloc", "sa_attn_bwd_heads", "sa_offset_attn_fwd", "sa_offset_attn_interp_fwd",
     "sa_fib_offsets", "sa_pow2_offsets", "sa_layer_alpha", "sa_block_ratios", "sa_device_status",
     # allocating conveniences
-    "build_mask", "attn_fwd", "attn_fwd_heads", "attn_bwd", "offset_attn_fwd", "offset_attn_interp_fwd",
+    "build_mask", "attn_fwd", "attn_fwd_heads", "attn_bwd", "attn_bwd_heads", "offset_attn_fwd", "offset_attn_interp_fwd",
     # constants
     "MASK_TOPK", "MASK_BIGBIRD", "MASK_FULL", "MASK_LITERAL_MEAN", "LITERAL_LOCAL", "LITERAL_PAIRS",
 ]

@@ -104,8 +104,10 @@ struct BParams {
   int batch, n_tokens, heads, heads_per_kv, kv_heads, block, log2b, nb, causal, csr_shared;
   int tiles;                        // 128-row tiles per sequence
   int n_items;
-  const int32_t* rp;                // CSR (dQ) or CSC (dK / dV) row pointers
-  const int32_t* ci;                // CSR column / CSC row indices
+  int n_masks;                      // head groups: query head h uses CSR head_mask[h]
+  const int32_t* rp[kMaxMasks];     // CSR (dQ) or transposed CSR (dK / dV) row pointers
+  const int32_t* ci[kMaxMasks];     // CSR column / transposed CSR row indices
+  uint8_t head_mask[kMaxHeadMap];
   const float* lse;                 // [batch][heads][n_tokens]
   const float* dvec;                // D, same layout
   __nv_bfloat16* out0;              // dQ, or dK
@@ -256,8 +258,10 @@ __device__ void dq_producer(const BParams& p, const Item& it, const CUtensorMap*
       tma_load_4d(sFix + C::BIG_BYTES + c * C::BIG_CHUNK, tdo, &bars.fixed_full, c * C::CH, it.h, q0, it.s);
     }
   }
-  const int32_t* rp = p.rp + (size_t)(p.csr_shared ? 0 : it.s) * (p.nb + 1);
-  const int n_keys = build_union(p.nb, p.causal ? kKeepLE : kKeepAll, u, rp, p.ci, I0, nq, &g_bwd_err, kErrBadIndex);
+  const int mi = p.n_masks > 1 ? p.head_mask[it.h] : 0;
+  const int32_t* rp = p.rp[mi] + (size_t)(p.csr_shared ? 0 : it.s) * (p.nb + 1);
+  const int n_keys =
+      build_union(p.nb, p.causal ? kKeepLE : kKeepAll, u, rp, p.ci[mi], I0, nq, &g_bwd_err, kErrBadIndex);
   const int n_chunks = n_keys * cpb;
   int kt = 0;
   bool ok = true;
@@ -533,14 +537,23 @@ __device__ void dkdv_producer(const BParams& p, const Item& it, const CUtensorMa
       tma_load_4d(sFix + C::BIG_BYTES + c * C::BIG_CHUNK, tv, &bars.fixed_full, c * C::CH, it.h, k0, it.s);
     }
   }
-  const int32_t* rp = p.rp + (size_t)(p.csr_shared ? 0 : it.s) * (p.nb + 1);
-  const int n_q = build_union(p.nb, p.causal ? kKeepGE : kKeepAll, u, rp, p.ci, J0, nk, &g_bwd_err, kErrBadIndex);
-  const int n_chunks = n_q * cpb;
+  int cur_mask = -1, n_chunks = 0;
   int kt = 0, mt = 0;
   bool ok = true;
-  // every query head of the group, then the end marker
+  // every query head of the group, then the end marker; the union of the transposed CSR's
+  // rows is rebuilt when the head's CSR differs from the previous head's
   for (int hh = 0; hh <= p.heads_per_kv && ok; ++hh) {
     const int head = it.h * p.heads_per_kv + hh;
+    if (hh < p.heads_per_kv) {
+      const int mi = p.n_masks > 1 ? p.head_mask[head] : 0;
+      if (mi != cur_mask) {
+        const int32_t* rp = p.rp[mi] + (size_t)(p.csr_shared ? 0 : it.s) * (p.nb + 1);
+        const int n_q =
+            build_union(p.nb, p.causal ? kKeepGE : kKeepAll, u, rp, p.ci[mi], J0, nk, &g_bwd_err, kErrBadIndex);
+        n_chunks = n_q * cpb;
+        cur_mask = mi;
+      }
+    }
     for (int c0 = (hh < p.heads_per_kv ? 0 : n_chunks);; c0 += 2, ++mt) {
       const Meta m = step_meta(u, c0, n_chunks, cpb, b, head);
       if (m.kind == kKindEnd && hh < p.heads_per_kv) break;   // next head
@@ -946,7 +959,8 @@ __global__ void __launch_bounds__(1024) csc_scan_kernel(const int32_t* rp_all, i
 // ------------------------------------------------------------------ launch
 
 template <int D>
-int launch_attention(const BwdArgs& a, const BwdWorkspace& ws, cudaStream_t stream) {
+int launch_attention(const BwdArgs& a, const BwdWorkspace& ws, const int32_t* const* csc_ptr,
+                     const int32_t* const* csc_idx, cudaStream_t stream) {
   using C = BCfg<D>;
   const uint32_t mrows = a.block == 32 ? 32u : 64u;
   uint8_t* wsb = static_cast<uint8_t*>(a.workspace);
@@ -966,6 +980,8 @@ int launch_attention(const BwdArgs& a, const BwdWorkspace& ws, cudaStream_t stre
   p.dvec = reinterpret_cast<const float*>(wsb + ws.dvec_off);
   p.scale = a.softmax_scale;
   p.scale_log2 = a.softmax_scale * kLog2e;
+  p.n_masks = a.n_masks;
+  for (int h = 0; h < kMaxHeadMap; ++h) p.head_mask[h] = a.head_mask[h];
 
   // dQ: query-stationary over the CSR
   {
@@ -980,8 +996,10 @@ int launch_attention(const BwdArgs& a, const BwdWorkspace& ws, cudaStream_t stre
                          a.kv_strides[2], C::CH, mrows, C::TMA_SWZ))
       return SA_ERR_UNSUPPORTED;
     BParams pq = p;
-    pq.rp = a.row_ptr;
-    pq.ci = a.col_idx;
+    for (int m = 0; m < kMaxMasks; ++m) {
+      pq.rp[m] = m < a.n_masks ? a.row_ptr[m] : nullptr;
+      pq.ci[m] = m < a.n_masks ? a.col_idx[m] : nullptr;
+    }
     pq.n_items = a.batch * a.heads * p.tiles;
     pq.out0 = static_cast<__nv_bfloat16*>(a.dq);
     pq.out1 = nullptr;
@@ -1007,8 +1025,10 @@ int launch_attention(const BwdArgs& a, const BwdWorkspace& ws, cudaStream_t stre
                          a.o_strides[2], C::CH, mrows, C::TMA_SWZ))
       return SA_ERR_UNSUPPORTED;
     BParams pk = p;
-    pk.rp = reinterpret_cast<const int32_t*>(wsb + ws.col_ptr_off);
-    pk.ci = reinterpret_cast<const int32_t*>(wsb + ws.row_idx_off);
+    for (int m = 0; m < kMaxMasks; ++m) {
+      pk.rp[m] = m < a.n_masks ? csc_ptr[m] : nullptr;
+      pk.ci[m] = m < a.n_masks ? csc_idx[m] : nullptr;
+    }
     pk.n_items = a.batch * a.kv_heads * p.tiles;
     pk.out0 = static_cast<__nv_bfloat16*>(a.dk);
     pk.out1 = static_cast<__nv_bfloat16*>(a.dv);
@@ -1042,7 +1062,12 @@ BwdWorkspace bwd_workspace_layout(int64_t batch, int64_t n_tokens, int64_t heads
 int launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
   const int csr_batches = a.csr_shared ? 1 : a.batch;
   const int nb = a.n_tokens / a.block;
-  BwdWorkspace ws = bwd_workspace_layout(a.batch, a.n_tokens, a.heads, a.block, csr_batches, 0);
+  // one transposed CSR per mask: col_ptr regions of csr_batches x (nb + 1), row_idx regions of
+  // each mask's capacity (one mask: whatever the workspace holds after the fixed parts)
+  int64_t cap_total = 0;
+  for (int m = 0; m < a.n_masks; ++m) cap_total += a.n_masks > 1 ? a.col_capacity[m] : 0;
+  BwdWorkspace ws =
+      bwd_workspace_layout(a.batch, a.n_tokens, a.heads, a.block, (int64_t)csr_batches * a.n_masks, cap_total);
   if (a.workspace_bytes < ws.bytes) return SA_ERR_CAPACITY;
   ws.row_idx_capacity = (int64_t)((a.workspace_bytes - ws.row_idx_off) / 4);
   uint8_t* wsb = static_cast<uint8_t*>(a.workspace);
@@ -1068,20 +1093,27 @@ int launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
     }
     if (cudaGetLastError() != cudaSuccess) return SA_ERR_CUDA;
   }
-  // transposed CSR
-  {
+  // transposed CSRs
+  const int32_t* csc_ptr[kMaxMasks];
+  const int32_t* csc_idx[kMaxMasks];
+  int64_t base = 0;
+  for (int m = 0; m < a.n_masks; ++m) {
+    int32_t* cp = col_ptr + (size_t)m * csr_batches * (nb + 1);
+    int32_t* ri = row_idx + base;
+    const int64_t cap = a.n_masks > 1 ? a.col_capacity[m] : ws.row_idx_capacity;
+    base += cap;
     const dim3 grid((unsigned)((nb + 7) / 8), (unsigned)csr_batches);
-    csc_pass_kernel<<<grid, 256, 0, stream>>>(a.row_ptr, a.col_idx, nb, a.causal, col_ptr, row_idx,
-                                              ws.row_idx_capacity, 0);
-    csc_scan_kernel<<<csr_batches, 1024, 0, stream>>>(a.row_ptr, nb, col_ptr, ws.row_idx_capacity);
-    csc_pass_kernel<<<grid, 256, 0, stream>>>(a.row_ptr, a.col_idx, nb, a.causal, col_ptr, row_idx,
-                                              ws.row_idx_capacity, 1);
+    csc_pass_kernel<<<grid, 256, 0, stream>>>(a.row_ptr[m], a.col_idx[m], nb, a.causal, cp, ri, cap, 0);
+    csc_scan_kernel<<<csr_batches, 1024, 0, stream>>>(a.row_ptr[m], nb, cp, cap);
+    csc_pass_kernel<<<grid, 256, 0, stream>>>(a.row_ptr[m], a.col_idx[m], nb, a.causal, cp, ri, cap, 1);
     if (cudaGetLastError() != cudaSuccess) return SA_ERR_CUDA;
+    csc_ptr[m] = cp;
+    csc_idx[m] = ri;
   }
   switch (a.head_dim) {
-    case 32: return launch_attention<32>(a, ws, stream);
-    case 64: return launch_attention<64>(a, ws, stream);
-    case 128: return launch_attention<128>(a, ws, stream);
+    case 32: return launch_attention<32>(a, ws, csc_ptr, csc_idx, stream);
+    case 64: return launch_attention<64>(a, ws, csc_ptr, csc_idx, stream);
+    case 128: return launch_attention<128>(a, ws, csc_ptr, csc_idx, stream);
   }
   return SA_ERR_UNSUPPORTED;
 }

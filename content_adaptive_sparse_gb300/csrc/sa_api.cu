@@ -245,12 +245,23 @@ int sa_attn_bwd_workspace_size(int32_t batch, int32_t n_tokens, int32_t heads, i
   return SA_OK;
 }
 
-int sa_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* d_o, const float* lse,
-                const int64_t q_strides[3], const int64_t kv_strides[3], const int64_t o_strides[3], int32_t batch,
-                int32_t n_tokens, int32_t heads, int32_t kv_heads, int32_t head_dim, int32_t block, int32_t causal,
-                const int32_t* d_row_ptr, const int32_t* d_col_idx, int32_t csr_shared, float softmax_scale,
-                void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, void* stream) {
-  if (!o || !d_o || !lse || !dk || !dv || !d_row_ptr || !d_col_idx || !workspace) return SA_ERR_INVALID_ARG;
+int sa_attn_bwd_heads(const void* q, const void* k, const void* v, const void* o, const void* d_o, const float* lse,
+                      const int64_t q_strides[3], const int64_t kv_strides[3], const int64_t o_strides[3],
+                      int32_t batch, int32_t n_tokens, int32_t heads, int32_t kv_heads, int32_t head_dim,
+                      int32_t block, int32_t causal, int32_t n_masks, const int32_t* const* h_row_ptrs,
+                      const int32_t* const* h_col_idxs, const int64_t* h_col_capacities,
+                      const int32_t* h_head_mask, int32_t csr_shared, float softmax_scale, void* dq, void* dk,
+                      void* dv, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!o || !d_o || !lse || !dk || !dv || !workspace || !h_row_ptrs || !h_col_idxs) return SA_ERR_INVALID_ARG;
+  if (n_masks < 1 || (n_masks > 1 && (!h_head_mask || !h_col_capacities))) return SA_ERR_INVALID_ARG;
+  if (n_masks > sa::kMaxMasks || (n_masks > 1 && heads > sa::kMaxHeadMap)) return SA_ERR_UNSUPPORTED;
+  for (int m = 0; m < n_masks; ++m) {
+    if (!h_row_ptrs[m] || !h_col_idxs[m]) return SA_ERR_INVALID_ARG;
+    if (n_masks > 1 && h_col_capacities[m] < 0) return SA_ERR_INVALID_ARG;
+  }
+  if (n_masks > 1)
+    for (int h = 0; h < heads; ++h)
+      if (h_head_mask[h] < 0 || h_head_mask[h] >= n_masks) return SA_ERR_INVALID_ARG;
   const int st = check_attn_common(q, k, v, q_strides, kv_strides, o_strides, batch, n_tokens, heads, kv_heads, dq,
                                    const_cast<float*>(lse));
   if (st != SA_OK) return st;
@@ -263,8 +274,11 @@ int sa_attn_bwd(const void* q, const void* k, const void* v, const void* o, cons
   if (n_tokens % block != 0) return SA_ERR_UNSUPPORTED;
   if (n_tokens / block > sa::kMaxMaskBlocks) return SA_ERR_UNSUPPORTED;
   if ((int64_t)batch * heads * ((n_tokens + 127) / 128) > INT32_MAX) return SA_ERR_UNSUPPORTED;
-  const int csr_batches = csr_shared ? 1 : batch;
-  if (workspace_bytes < sa::bwd_workspace_layout(batch, n_tokens, heads, block, csr_batches, 0).bytes)
+  const int64_t csr_batches = csr_shared ? 1 : batch;
+  int64_t cap_total = 0;
+  for (int m = 0; m < n_masks; ++m) cap_total += n_masks > 1 ? h_col_capacities[m] : 0;
+  if (workspace_bytes <
+      sa::bwd_workspace_layout(batch, n_tokens, heads, block, csr_batches * n_masks, cap_total).bytes)
     return SA_ERR_CAPACITY;
   if (!device_ok()) return SA_ERR_CUDA;
   sa::BwdArgs a;
@@ -290,12 +304,28 @@ int sa_attn_bwd(const void* q, const void* k, const void* v, const void* o, cons
   a.block = block;
   a.causal = causal;
   a.csr_shared = csr_shared != 0;
-  a.row_ptr = d_row_ptr;
-  a.col_idx = d_col_idx;
+  a.n_masks = n_masks;
+  for (int m = 0; m < sa::kMaxMasks; ++m) {
+    a.row_ptr[m] = m < n_masks ? h_row_ptrs[m] : nullptr;
+    a.col_idx[m] = m < n_masks ? h_col_idxs[m] : nullptr;
+    a.col_capacity[m] = (m < n_masks && n_masks > 1) ? h_col_capacities[m] : 0;
+  }
+  for (int h = 0; h < sa::kMaxHeadMap; ++h) a.head_mask[h] = (n_masks > 1 && h < heads) ? (uint8_t)h_head_mask[h] : 0;
   a.softmax_scale = softmax_scale;
   a.workspace = workspace;
   a.workspace_bytes = workspace_bytes;
   return sa::launch_attn_bwd(a, static_cast<cudaStream_t>(stream));
+}
+
+int sa_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* d_o, const float* lse,
+                const int64_t q_strides[3], const int64_t kv_strides[3], const int64_t o_strides[3], int32_t batch,
+                int32_t n_tokens, int32_t heads, int32_t kv_heads, int32_t head_dim, int32_t block, int32_t causal,
+                const int32_t* d_row_ptr, const int32_t* d_col_idx, int32_t csr_shared, float softmax_scale,
+                void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!d_row_ptr || !d_col_idx) return SA_ERR_INVALID_ARG;
+  return sa_attn_bwd_heads(q, k, v, o, d_o, lse, q_strides, kv_strides, o_strides, batch, n_tokens, heads, kv_heads,
+                           head_dim, block, causal, 1, &d_row_ptr, &d_col_idx, nullptr, nullptr, csr_shared,
+                           softmax_scale, dq, dk, dv, workspace, workspace_bytes, stream);
 }
 
 int sa_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* d_o, const float* lse,

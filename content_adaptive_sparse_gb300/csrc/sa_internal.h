@@ -93,14 +93,18 @@ struct BwdArgs {
   int64_t kv_strides[3];   // k, v, dk and dv
   int64_t o_strides[3];    // o and d_o
   int32_t batch, n_tokens, heads, kv_heads, head_dim, block, causal, csr_shared;
-  const int32_t* row_ptr;
-  const int32_t* col_idx;
+  int32_t n_masks;                       // CSRs (head groups); query head h uses head_mask[h]
+  const int32_t* row_ptr[kMaxMasks];
+  const int32_t* col_idx[kMaxMasks];
+  int64_t col_capacity[kMaxMasks];       // entries each CSR may hold (n_masks > 1)
+  uint8_t head_mask[kMaxHeadMap];
   float softmax_scale;
   void* workspace;
   size_t workspace_bytes;
 };
 // Workspace layout of the backward: D = rowsum(dO * O) fp32 [batch][heads][n_tokens],
-// the transposed CSR's col_ptr int32 [csr_batches][nb + 1] and row_idx int32 [rest].
+// the transposed CSRs' col_ptr int32 [n_masks][csr_batches][nb + 1] (csr_batches below counts
+// all masks) and row_idx int32 [rest], mask m's entries after those of masks < m.
 struct BwdWorkspace {
   size_t dvec_off, col_ptr_off, row_idx_off, bytes;
   int64_t row_idx_capacity;

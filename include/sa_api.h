@@ -175,6 +175,21 @@ int sa_attn_bwd(const void* q, const void* k, const void* v, const void* o, cons
                 const int32_t* d_row_ptr, const int32_t* d_col_idx, int32_t csr_shared, float softmax_scale,
                 void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, void* stream);
 
+/* sa_attn_bwd with one block CSR per head group, the backward of sa_attn_fwd_heads.
+ *   n_masks, h_row_ptrs, h_col_idxs, h_head_mask : as in sa_attn_fwd_heads.
+ *   h_col_capacities : host int64 [n_masks], entries each CSR may hold (its col_idx size);
+ *                      read only when n_masks > 1.
+ * The workspace is sa_attn_bwd_workspace_size(batch, n_tokens, heads, block,
+ * csr_batches * n_masks, sum of h_col_capacities) bytes. Every other argument is as in
+ * sa_attn_bwd, which is this call with one CSR. */
+int sa_attn_bwd_heads(const void* q, const void* k, const void* v, const void* o, const void* d_o, const float* lse,
+                      const int64_t q_strides[3], const int64_t kv_strides[3], const int64_t o_strides[3],
+                      int32_t batch, int32_t n_tokens, int32_t heads, int32_t kv_heads, int32_t head_dim,
+                      int32_t block, int32_t causal, int32_t n_masks, const int32_t* const* h_row_ptrs,
+                      const int32_t* const* h_col_idxs, const int64_t* h_col_capacities,
+                      const int32_t* h_head_mask, int32_t csr_shared, float softmax_scale, void* dq, void* dk,
+                      void* dv, void* workspace, size_t workspace_bytes, void* stream);
+
 /* sa_attn_bwd without a caller workspace: the scratch lives in a 16 MiB array inside the
  * library (one per device), so the call allocates nothing. col_capacity bounds the CSR's
  * entries as in sa_attn_bwd_workspace_size; if the scratch that needs exceeds 16 MiB the

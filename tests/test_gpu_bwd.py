@@ -194,3 +194,36 @@ def test_bytelm_topk_8k_sampled_and_invariants():
     want_dv = do_f.sum(axis=1)
     assert np.abs(sum_dv - want_dv).max() <= 2e-2 * np.abs(want_dv).max()
     assert np.abs(dk_np.sum(axis=1)).max() <= 2e-2 * np.abs(dk_np).max() * np.sqrt(n)
+
+
+# ---------------------------------------------------------------- head groups
+
+@pytest.mark.parametrize("b,d,causal", [(128, 64, 1), (64, 64, 0), (32, 128, 1)])
+def test_head_group_backward(b, d, causal):
+    """The page's 6/3/3 split with 3 KV heads (KV groups straddle head groups)."""
+    n, bt, h, hkv = 1024, 2, 12, 3
+    rng = np.random.default_rng(b + d + causal)
+    ratios = (rng.integers(20, 90, (bt, n // b)) / np.float32(b)).astype(np.float32)
+    comps = oracle.cas_head_components(h)
+    parts = sorted(set(comps))
+    head_mask = [parts.index(c) for c in comps]
+    qb = bf16_normal_bits(rng, (bt, n, h, d), 0.5)
+    kb, vb = (bf16_normal_bits(rng, (bt, n, hkv, d), 0.25) for _ in range(2))
+    dob = bf16_normal_bits(rng, (bt, n, h, d), 0.25)
+    csrs_d, csrs_o = [], []
+    for c in parts:
+        p = om.MaskParams("literal_mean", b, n, causal, 1, components=c)
+        csrs_d.append(_mask_on_gpu(p, bt, ratios))
+        csrs_o.append(om.build_csr(p, ratios, bt))
+    torch = torch_cuda()
+    q, k, v, do = (to_dev(x) for x in (qb, kb, vb, dob))
+    o, lse = sa.attn_fwd_heads(q, k, v, csrs_d, head_mask, b, causal)
+    dq, dk, dv = sa.attn_bwd_heads(q, k, v, o, lse, do, csrs_d, head_mask, b, causal)
+    torch.cuda.synchronize()
+    assert sa.sa_device_status() == 0
+    f = bf16_bits_to_f64
+    rq, rk, rv = oracle.attention_csr_backward_heads(f(qb), f(kb), f(vb), f(dob), csrs_o, head_mask, b, causal)
+    what = f"head groups b={b} d={d} causal={causal}"
+    assert_grad_close(bf16_to_f64(dq), rq, "dQ " + what)
+    assert_grad_close(bf16_to_f64(dk), rk, "dK " + what)
+    assert_grad_close(bf16_to_f64(dv), rv, "dV " + what)
