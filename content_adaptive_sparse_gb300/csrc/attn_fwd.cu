@@ -7,9 +7,10 @@
 //
 // One CTA per SM runs two independent pipelines x = 0, 1 (one query tile each), so the
 // tensor core always has the other pipeline's work while one waits. Each pipeline has
-// its own Q buffer, K/V ring, meta ring and half of TMEM. The kernel is persistent: the
-// 2 x grid pipelines walk a static list of query tiles ordered longest first (causal: last
-// query tiles first; BigBird: the global rows first).
+// its own Q buffer, K/V ring, meta ring and half of TMEM. The kernel is persistent: each
+// pipeline's producer takes the next query tile from a launch-wide counter over a list
+// ordered longest first (causal: last query tiles first; BigBird: the global rows first),
+// so a pipeline that drew a long tile takes fewer of the rest.
 //
 // Warp roles (640 threads):
 //   warps 0, 19  producer of pipeline 0 / 1: builds the union (whole warp), publishes
@@ -41,6 +42,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "csr_union.cuh"
 #include "ptx_sm100.cuh"
 #include "sa_internal.h"
@@ -50,6 +53,11 @@ namespace sa {
 namespace {
 
 __device__ unsigned int g_attn_err;
+
+// Work counters of the persistent kernel: each launch takes one slot (round robin) and zeroes
+// it on its stream, so up to kWorkSlots launches may be in flight at once on any streams.
+constexpr int kWorkSlots = 64;
+__device__ unsigned int g_work_counters[kWorkSlots];
 
 constexpr int kTile = 128;          // query rows per work item
 constexpr int kKeyTile = 64;        // keys per S tile (two 32-key chunks)
@@ -92,7 +100,9 @@ struct Cfg {
   static_assert(STAGES >= NS && STAGES <= kMaxStages && NS <= kMaxSBuf, "ring sizes");
 };
 
-enum : int { kKindTile = 0, kKindEnd = 1 };
+// Meta kinds: a key tile of the current item, the end of the item, the header of the next
+// item (tok[0] = item index), no more items.
+enum : int { kKindTile = 0, kKindEnd = 1, kKindItem = 2, kKindDone = 3 };
 
 struct Meta {
   int kind;
@@ -118,6 +128,7 @@ struct Params {
   int batch, n_tokens, heads, heads_per_kv, block, log2b, nb, causal, csr_shared;
   int tiles_per_seq;          // 128-row query tiles per (sequence, head)
   int n_items;
+  unsigned int* work_counter;          // next item index (zeroed before the launch)
   int n_masks;
   const int32_t* row_ptr[kMaxMasks];   // one CSR per head group
   const int32_t* col_idx[kMaxMasks];
@@ -236,7 +247,31 @@ __device__ void producer(const Params& p, int x, const CUtensorMap* tq, const CU
   int q_last = -1;                                   // item_local of the last Q load
   bool ok = true;
 
-  for (int k = 2 * blockIdx.x + x; k < p.n_items && ok; k += 2 * gridDim.x, ++item_local) {
+  for (;; ++item_local) {
+    // the next item of the launch-wide longest-first list, announced to the MMA thread and
+    // the softmax warps of this pipeline through the meta ring
+    int k = 0;
+    if (lane == 0) k = (int)atomicAdd(p.work_counter, 1u);
+    k = __shfl_sync(0xffffffffu, k, 0);
+    {
+      Meta hm;
+      hm.kind = k < p.n_items ? kKindItem : kKindDone;
+      hm.nch = 0;
+      hm.tok[0] = k;
+      hm.tok[1] = 0;
+      hm.mask[0] = hm.mask[1] = 0;
+      if (lane == 0) {
+        const int ms = mt % kMetaRing;
+        ok = wait_bar(&bars.m_empty[ms], ((mt / kMetaRing) & 1) ^ 1, abort_flag);
+        if (ok) {
+          meta[ms] = hm;
+          mbar_arrive(&bars.m_full[ms]);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      ++mt;
+      if (!ok || hm.kind == kKindDone) break;
+    }
     const Item it = decode_item(p, k);
     const int q0 = it.tile * kTile;
     const int I0 = q0 >> p.log2b;
@@ -423,7 +458,15 @@ __device__ void mma_issuer(const Params& p, int x, PipeBars& bars, Meta* meta, u
   bool ok = true;
   int item_local = 0;
   PendRing pend{0, 0, 0, 0, 0, 0};
-  for (int k = 2 * blockIdx.x + x; k < p.n_items && ok; k += 2 * gridDim.x, ++item_local) {
+  for (; ok; ++item_local) {
+    {
+      const int ms = mt & (kMetaRing - 1);
+      if (!(ok = wait_bar(&bars.m_full[ms], (uint32_t)(mt / kMetaRing) & 1u, abort_flag))) break;
+      const Meta hm = load_meta(&meta[ms]);
+      mbar_arrive(&bars.m_empty[ms]);
+      ++mt;
+      if (hm.kind == kKindDone) break;
+    }
     const int qb = item_local % C::QB;
     if (!(ok = wait_bar(&bars.q_full[qb], (item_local / C::QB) & 1, abort_flag))) break;
     int qi = 0, pi = 0;
@@ -632,7 +675,18 @@ __device__ void softmax_epilogue(const Params& p, int x, int h, PipeBars& bars, 
   uint32_t sph = 0;         // (g / NS) & 1
   bool ok = true;
   int item_local = 0;
-  for (int k = 2 * blockIdx.x + x; k < p.n_items && ok; k += 2 * gridDim.x, ++item_local) {
+  for (; ok; ++item_local) {
+    int k;
+    {
+      const int ms = mt % kMetaRing;
+      if (!(ok = wait_bar(&bars.m_full[ms], (mt / kMetaRing) & 1, abort_flag))) break;
+      const Meta hm = load_meta(&meta[ms]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.m_empty[ms]);
+      ++mt;
+      if (hm.kind == kKindDone) break;
+      k = hm.tok[0];
+    }
     const Item it = decode_item(p, k);
     const int qtok = it.tile * kTile + row;
     const int q_warp = it.tile * kTile + quarter * 32;
@@ -905,6 +959,14 @@ int launch_d(const AttnArgs& a, cudaStream_t stream) {
   p.o_sn = a.o_strides[1];
   p.o_sh = a.o_strides[2];
   p.scale_log2 = a.softmax_scale * 1.4426950408889634f;
+  // a work counter of its own for this launch: slot (ticket mod kWorkSlots), zeroed on the
+  // launch's stream first
+  static unsigned int* counters = nullptr;
+  if (!counters && cudaGetSymbolAddress(reinterpret_cast<void**>(&counters), g_work_counters) != cudaSuccess)
+    return SA_ERR_CUDA;
+  static std::atomic<unsigned int> ticket{0};
+  p.work_counter = counters + (ticket.fetch_add(1u) % kWorkSlots);
+  if (cudaMemsetAsync(p.work_counter, 0, sizeof(unsigned int), stream) != cudaSuccess) return SA_ERR_CUDA;
   static int sm_count = 0;
   if (sm_count == 0) {
     int dev = 0;
