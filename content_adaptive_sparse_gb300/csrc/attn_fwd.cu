@@ -82,11 +82,12 @@ struct Cfg {
   static constexpr int Q_BYTES = NCH * Q_CHUNK;
   static constexpr int KV_CHUNK = kKeyTile * ROWB;     // one d-chunk of a 64-key K or V tile
   static constexpr int KV_BYTES = NCH * KV_CHUNK;
-  // d <= 64: each 32-key chunk half of a tile has its own O accumulator (and running max),
-  // so the two softmax warps of a row never synchronise per tile; d = 128: one O.
-  static constexpr bool SPLIT = D <= 64;
+  // d = 32: each 32-key chunk half of a tile has its own O accumulator (and running max),
+  // so the two softmax warps of a row never synchronise per tile; d >= 64: one O, which
+  // leaves TMEM for three S buffers at d = 64 (measured 4 % faster than split O with two).
+  static constexpr bool SPLIT = D < 64;
   static constexpr int NO = SPLIT ? 2 : 1;             // O accumulators per pipeline
-  static constexpr int NS = D == 32 ? 3 : 2;           // S buffers per pipeline
+  static constexpr int NS = D <= 64 ? 3 : 2;           // S buffers per pipeline
   static constexpr int QB = D > 64 ? 1 : 2;            // Q buffers per pipeline
   static constexpr int STAGES = D == 128 ? 2 : (D == 64 ? 4 : 6);   // K and V ring depth
   static constexpr int UNION_BYTES = kMaxTileBlocks * (kMaxMaskBlocks / 32) * 4 + kMaxMaskBlocks * 2;   // 10 KB
@@ -647,10 +648,10 @@ __device__ __forceinline__ void pair_sync(int id) { asm volatile("bar.sync %0, 6
 
 // Softmax and epilogue of pipeline x. Warp (quarter q, chunk h) handles rows 32q..32q+31
 // and key columns 32h..32h+31 of every 64-key tile.
-//   d <= 64 (split O): the chunk half has its own running max, row sum and accumulator
+//   d = 32 (split O): the chunk half has its own running max, row sum and accumulator
 //     O_h, so the two warps of a quarter work independently; their partial results are
 //     merged once per query tile in the epilogue.
-//   d = 128: one O; the pair agrees on each tile's row max through `xc` (named barrier
+//   d >= 64: one O; the pair agrees on each tile's row max through `xc` (named barrier
 //     1 + 4x + q) and each warp rescales its half of the O columns.
 template <int D>
 __device__ void softmax_epilogue(const Params& p, int x, int h, PipeBars& bars, Meta* meta, Exchange& xc,
