@@ -1,14 +1,16 @@
 // GPU block-CSR builder: per-block ratios and pattern parameters -> row_ptr / col_idx.
 //
-// One CTA (1024 threads) per sequence. The CTA
+// CTAs of 1024 threads, a few per sequence (grid.y splits the rows). Each CTA
 //   1. computes the per-sequence state the mode needs (ratio rank order for TOPK,
 //      literal flags from the mean threshold for LITERAL_MEAN),
 //   2. computes every row length and an exclusive scan of them (row_ptr), offset by the
 //      entries of the sequences before it,
-//   3. fills the rows, one warp per row, in ascending block order.
+//   3. fills its share of the rows, one warp per row, in ascending block order.
 // All decisions are integer or exact float compares, so the output is bit-identical
 // to the definitions in include/sa_api.h on every run.
 #include <cuda_runtime.h>
+
+#include <algorithm>
 #include <stdint.h>
 
 #include "sa_internal.h"
@@ -144,16 +146,25 @@ __device__ void load_ratios(const MaskArgs& a, const Smem& s, int seq) {
   __syncthreads();
 }
 
-// TOPK: rank by (ratio desc, index asc) over all blocks; order[rank] = block.
+// TOPK: rank by (ratio desc, index asc) over all blocks; order[rank] = block. Eight
+// consecutive lanes share a block j and count over interleaved eighths of the blocks.
 __device__ void topk_order(const MaskArgs& a, const Smem& s) {
-  for (int j = threadIdx.x; j < a.nb; j += kThreads) {
+  const int part = threadIdx.x & 7;
+  constexpr int kGroups = kThreads >> 3;
+  const int iters = (a.nb + kGroups - 1) / kGroups;   // the same for every thread: the
+  for (int it = 0; it < iters; ++it) {                // whole warp reaches the shuffles
+    const int j0 = (threadIdx.x >> 3) + kGroups * it;
+    const int j = j0 < a.nb ? j0 : a.nb - 1;
     const float rj = s.r[j];
     int rank = 0;
-    for (int t = 0; t < a.nb; ++t) {
+    for (int t = part; t < a.nb; t += 8) {
       const float rt = s.r[t];
       rank += (rt > rj) || (rt == rj && t < j);
     }
-    s.order[rank] = j;
+    rank += __shfl_xor_sync(0xffffffffu, rank, 1);
+    rank += __shfl_xor_sync(0xffffffffu, rank, 2);
+    rank += __shfl_xor_sync(0xffffffffu, rank, 4);
+    if (part == 0 && j0 < a.nb) s.order[rank] = j;
   }
   __syncthreads();
 }
@@ -368,18 +379,22 @@ __global__ void __launch_bounds__(kThreads) build_mask_kernel(MaskArgs a) {
   if (needs_ratio) load_ratios(a, s, seq);
   if (a.mode == SA_MASK_TOPK) topk_order(a, s);
   if (a.mode == SA_MASK_LITERAL_MEAN) literal_prefix(a, s);
-  if (a.mode != SA_MASK_LITERAL_MEAN) base = (int64_t)seq * seq_total(a, s);
 
   for (int I = threadIdx.x; I < a.nb; I += kThreads) s.cnt[I] = row_len(a, s, I);
   __syncthreads();
   const int total = block_exclusive_scan(s.cnt, a.nb, s.scan_tmp);
+  // row lengths of the other modes do not depend on the data: every sequence has `total`
+  if (a.mode != SA_MASK_LITERAL_MEAN) base = (int64_t)seq * total;
+  // this CTA's share of the rows: every CTA of the sequence holds the same state and offsets
+  const int per = (a.nb + gridDim.y - 1) / gridDim.y;
+  const int row_lo = blockIdx.y * per, row_hi = min(a.nb, row_lo + per);
   int32_t* rp = a.row_ptr + (size_t)seq * (a.nb + 1);
-  for (int I = threadIdx.x; I < a.nb; I += kThreads) rp[I] = (int32_t)(base + s.cnt[I]);
-  if (threadIdx.x == 0) rp[a.nb] = (int32_t)(base + total);
+  for (int I = row_lo + threadIdx.x; I < row_hi; I += kThreads) rp[I] = (int32_t)(base + s.cnt[I]);
+  if (blockIdx.y == 0 && threadIdx.x == 0) rp[a.nb] = (int32_t)(base + total);
 
   const int wid = threadIdx.x >> 5;
   uint32_t* bm = s.bm + (size_t)wid * s.words;
-  for (int I = wid; I < a.nb; I += kWarps) {
+  for (int I = row_lo + wid; I < row_hi; I += kWarps) {
     int32_t* out = a.col_idx + base + s.cnt[I];
     switch (a.mode) {
       case SA_MASK_TOPK: fill_topk(a, s, I, out, bm); break;
@@ -420,7 +435,17 @@ int launch_build_mask(const sa_mask_params& p, const float* d_ratio, int32_t* d_
   if (cudaFuncSetAttribute(build_mask_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return SA_ERR_CUDA;
-  build_mask_kernel<<<a.batch, kThreads, smem, stream>>>(a);
+  // rows of a sequence split over up to nb / 32 CTAs (one row per warp), enough CTAs in all
+  // to cover the GPU twice; each CTA rebuilds the sequence's state, which is cheap
+  static int sm_count = 0;
+  if (sm_count == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (sm_count <= 0) sm_count = 148;
+  }
+  const int groups = std::max(1, std::min((a.nb + kWarps - 1) / kWarps, (2 * sm_count + a.batch - 1) / a.batch));
+  build_mask_kernel<<<dim3((unsigned)a.batch, (unsigned)groups), kThreads, smem, stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
