@@ -18,8 +18,7 @@ against the pages it follows:
 * [FIB] "Depth-Staggered Fibonacci Spacing for Sparse Attention" (arXiv 2606.28560,
   section 2 "Method"): dense window {0..W} plus offsets d_k = alpha * f_k.
 
-Readings taken where the pages are silent or disagree are listed in the design doc and at
-each function. Parity status: every function here is pinned by ``tests/test_oracle_*``
+Readings taken where the pages are silent or disagree are stated at each function. Parity status: every function here is pinned by ``tests/test_oracle_*``
 against closed forms, brute force from the token-level definitions, library routines
 (numpy's Philox, gzip framing) or an independent dense route.
 """

@@ -3,8 +3,8 @@ numbers: as easy as 1, 2, 3", SC'11), used for the BigBird random blocks.
 
 The BigBird page (section 2, "Random attention G_R") draws r keys per query uniformly;
 its sketch (section 3) uses torch.randperm. To make the draw reproducible on two
-independent implementations, the random stream is fixed as follows (a reading; see
-DESIGN.md):
+independent implementations, the random stream is fixed as follows (a reading of the
+page, which names no generator):
 
   word(p) = Philox4x64_10(counter = (p // 4 + 1, 0, 0, 0), key = (seed, 0))[p % 4]
 
