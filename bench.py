@@ -22,7 +22,7 @@ at N=16384, the 16-layer Fibonacci-offset pass at N=8192 (HBM roofline), the 64K
 compression-guided workload (top-64) and the mean-threshold mask split over local,
 long-range and hybrid head groups at N=8192.
 
-``--impl reference`` times the CPU oracle (the reference arm of this build) on the
+``--impl reference`` times the CPU oracle (the reference arm) on the
 same workload, each step a bounded sample of query blocks.
 
 Multi-GPU (torchrun): rank r processes its own shard of a global batch (sequences
