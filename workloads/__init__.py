@@ -5,7 +5,7 @@ bf16 bit patterns from seeded generators and names the workload shapes. Both the
 oracle (``oracle/``) and the GPU tests / bench consume exactly these arrays, so
 parity is always checked on identical bits.
 
-Workloads (shapes and pattern parameters as the pages and the task state them):
+Workloads (shapes and pattern parameters as the pages and the workload statement give them):
 
 * ``tiny_topk``      - 1 x 512 byte tokens, block 32, 2 heads, d_h 32, top-2
                        compression-guided causal mask (correctness size).
