@@ -304,3 +304,27 @@ def test_cas_heads_8k_sampled():
         orow, lrow = oracle.attention_rows_csr(qb, kb, vb, rp_o, ci_o, b, 1, [(s, i, hh)], convert=bf16_bits_to_f64)
         o_ref[t], l_ref[t] = orow[0], lrow[0]
     assert_attention_close(o_g, l_g, o_ref, l_ref, cfg["name"])
+
+
+def test_head_groups_eight_masks_sixteen_heads():
+    """The maximum of 8 CSRs, 16 query heads over 4 KV heads, two masks unused, heads of
+    one KV group spread over several masks."""
+    torch = torch_cuda()
+    n, b, bt, h, hkv = 1024, 64, 2, 16, 4
+    rng = np.random.default_rng(88)
+    ratios = (rng.integers(20, 90, (bt, n // b)) / np.float32(b)).astype(np.float32)
+    params = [om.MaskParams("topk", b, n, 1, 2, 1, 3), om.MaskParams("topk", b, n, 1, 1, 0, 6),
+              om.MaskParams("full", b, n, 1), om.MaskParams("literal_mean", b, n, 1, 1, components=1),
+              om.MaskParams("literal_mean", b, n, 1, 1, components=2), om.MaskParams("literal_mean", b, n, 1, 2),
+              om.MaskParams("topk", b, n, 1, 4, 2, 1), om.MaskParams("full", b, n, 1)]
+    head_mask = [int(x) for x in rng.integers(0, 6, h)]          # masks 6 and 7 unused
+    qb = bf16_normal_bits(rng, (bt, n, h, 64), 0.4)
+    kb, vb = (bf16_normal_bits(rng, (bt, n, hkv, 64), 0.25) for _ in range(2))
+    csrs_d = [_mask_on_gpu(p, bt, ratios) for p in params]
+    csrs_o = [om.build_csr(p, ratios, bt) for p in params]
+    o, lse = sa.attn_fwd_heads(to_dev(qb), to_dev(kb), to_dev(vb), csrs_d, head_mask, b, 1)
+    torch.cuda.synchronize()
+    assert sa.sa_device_status() == 0
+    o_ref, lse_ref = oracle.attention_csr_heads(bf16_bits_to_f64(qb), bf16_bits_to_f64(kb), bf16_bits_to_f64(vb),
+                                                csrs_o, head_mask, b, 1)
+    assert_attention_close(bf16_to_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref, "8 masks")

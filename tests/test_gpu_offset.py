@@ -190,3 +190,11 @@ def test_interp_fib_8k_sampled():
     o_g = np.stack([o_np[s, i, hh] for s, i, hh in smp])
     l_g = np.array([lse_np[s, hh, i] for s, i, hh in smp])
     assert_attention_close(o_g, l_g, o_ref, lse_ref, "interp fib 8k")
+
+
+def test_interp_ragged_length_and_tiny_sequences():
+    """Lengths that are not multiples of the 8-query warp tile, and sequences shorter than
+    the first rung."""
+    _run_interp(2, 1003, 2, 1, 8, 0.6180, seed=31, qmul=2.0)
+    _run_interp(1, 7, 1, 1, 3, 1.7, seed=32)
+    _run_interp(1, 1, 1, 1, 0, 0.9, seed=33)
