@@ -961,20 +961,13 @@ int launch_d(const AttnArgs& a, cudaStream_t stream) {
   p.o_sh = a.o_strides[2];
   p.scale_log2 = a.softmax_scale * 1.4426950408889634f;
   // a work counter of its own for this launch: slot (ticket mod kWorkSlots), zeroed on the
-  // launch's stream first
-  static unsigned int* counters = nullptr;
-  if (!counters && cudaGetSymbolAddress(reinterpret_cast<void**>(&counters), g_work_counters) != cudaSuccess)
-    return SA_ERR_CUDA;
+  // launch's stream first (the slots' address differs per device: looked up on every call)
+  unsigned int* counters = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&counters), g_work_counters) != cudaSuccess) return SA_ERR_CUDA;
   static std::atomic<unsigned int> ticket{0};
   p.work_counter = counters + (ticket.fetch_add(1u) % kWorkSlots);
   if (cudaMemsetAsync(p.work_counter, 0, sizeof(unsigned int), stream) != cudaSuccess) return SA_ERR_CUDA;
-  static int sm_count = 0;
-  if (sm_count == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
-    if (sm_count <= 0) sm_count = 148;
-  }
+  const int sm_count = current_sm_count();
   auto kern = attn_fwd_kernel<D>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return SA_ERR_CUDA;

@@ -437,13 +437,7 @@ int launch_build_mask(const sa_mask_params& p, const float* d_ratio, int32_t* d_
     return SA_ERR_CUDA;
   // rows of a sequence split over up to nb / 32 CTAs (one row per warp), enough CTAs in all
   // to cover the GPU twice; each CTA rebuilds the sequence's state, which is cheap
-  static int sm_count = 0;
-  if (sm_count == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
-    if (sm_count <= 0) sm_count = 148;
-  }
+  const int sm_count = current_sm_count();
   const int groups = std::max(1, std::min((a.nb + kWarps - 1) / kWarps, (2 * sm_count + a.batch - 1) / a.batch));
   build_mask_kernel<<<dim3((unsigned)a.batch, (unsigned)groups), kThreads, smem, stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;

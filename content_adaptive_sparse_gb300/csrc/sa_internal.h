@@ -15,6 +15,16 @@ constexpr unsigned int kErrCapacity = 4u;    // a device-sized output did not fi
 constexpr int kMaxMaskBlocks = 4096;         // nb limit of the mask builder
 constexpr int kMaxRandomBlocks = 64;
 
+// Streaming multiprocessors of the current device (queried per call: a process may drive
+// several devices).
+inline int current_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      n <= 0)
+    n = 1;
+  return n;
+}
+
 // mask_build.cu
 int launch_build_mask(const sa_mask_params& p, const float* d_ratio, int32_t* d_row_ptr, int32_t* d_col_idx,
                       cudaStream_t stream);
