@@ -18,8 +18,10 @@
 // the keys (group 0 the first half of the band steps and the even offset slabs, group 1
 // the rest) and merge their partial softmax states through shared memory at the end.
 // K/V arrive by TMA: the band (rows [q0 - 64, q0 + 64)) once, the offset slabs (64 rows
-// each) through a ring of four buffers that the last warp done with a buffer refills,
-// so loads are issued from many warps (one issuing thread streams boxes slowly).
+// each) through a ring of two buffers (one per group) that the last warp done with a
+// buffer refills, so loads are issued from many warps (one issuing thread streams boxes
+// slowly). At 66.5 KB of shared memory three CTAs share an SM (a four-buffer ring allowed
+// two and was 1.5 % slower).
 // Softmax: exact max over the band part, then the offsets with a lazily rescaled
 // running max (threshold 2^8).
 #include <cuda.h>
@@ -39,7 +41,7 @@ __device__ unsigned int g_offset_err;
 constexpr int kQ = 64;                   // queries per CTA
 constexpr int kGroupWarps = 4;           // 16 queries per warp: one group covers the tile
 constexpr int kWarps = 2 * kGroupWarps;  // two groups split the keys of the tile
-constexpr int kRing = 4;                 // offset slabs in flight per CTA (two per group)
+constexpr int kRing = 2;                 // offset slabs in flight per CTA (one per group)
 constexpr int kD = 64;                   // head dim supported by this kernel
 constexpr int kRowBytes = kD * 2;        // 128 B per K/V row
 constexpr int kBandMax = 64;             // deltas up to this go through the band
@@ -155,7 +157,7 @@ __device__ __forceinline__ void diag_pv(uint32_t vt, int wq, int lane, bool hold
 }
 
 template <int NKT>
-__global__ void __launch_bounds__(kWarps * 32, 2)
+__global__ void __launch_bounds__(kWarps * 32, 3)
     offset_attn_kernel(const __grid_constant__ CUtensorMap tk_band, const __grid_constant__ CUtensorMap tv_band,
                        const __grid_constant__ CUtensorMap tk_slab, const __grid_constant__ CUtensorMap tv_slab,
                        const __grid_constant__ OffParams p) {
@@ -163,7 +165,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sKb = sm;                        // band K, 16 KB
   uint8_t* sVb = sKb + kBandBytes;          // band V, 16 KB
-  uint8_t* sRing = sVb + kBandBytes;        // kRing x (K slab, V slab), 64 KB; merge buffer at the end
+  uint8_t* sRing = sVb + kBandBytes;        // kRing x (K slab, V slab), 32 KB; merge buffer at the end
   __shared__ uint64_t bar_band, bar_slab[kRing];
   __shared__ int done_cnt[kRing];           // warps finished with the slab in each buffer
   __shared__ int n_issued;                  // slabs issued so far
