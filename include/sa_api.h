@@ -12,8 +12,11 @@
  *
  * Conventions (all entry points):
  *   - Device pointers are marked d_*, host pointers h_*; q/k/v/o/lse are device memory.
- *   - The caller owns all memory. The library allocates no device memory and keeps no
- *     state besides a per-library device error word (see sa_device_status).
+ *   - The caller owns all memory. The library allocates no device memory; its only
+ *     device state is static arrays in the module: the device error words (see
+ *     sa_device_status), 64 work-counter slots of the block-sparse forward (each launch
+ *     takes the next slot and zeroes it on its stream, so at most 64 launches may be in
+ *     flight at once across streams) and the 16 MiB scratch of sa_attn_bwd_noalloc.
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = legacy default
  *     stream). Argument errors are returned synchronously before anything is launched.
  *   - Tensors q, k, v, o are bf16 with layout [batch, tokens, heads, head_dim]:
