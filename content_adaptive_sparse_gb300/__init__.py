@@ -82,10 +82,11 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.sa_block_ratios.argtypes = [_P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P,
                                     ctypes.c_int32]
     lib.sa_device_status.argtypes = [_P]
+    lib.sa_selftest_bounded_wait.argtypes = [_P]
     for name in ("sa_mask_nnz_bound", "sa_build_mask", "sa_attn_fwd", "sa_attn_fwd_heads", "sa_attn_bwd",
                  "sa_attn_bwd_noalloc", "sa_attn_bwd_heads", "sa_attn_bwd_workspace_size", "sa_offset_attn_fwd",
                  "sa_offset_attn_interp_fwd", "sa_fib_offsets", "sa_pow2_offsets", "sa_layer_alpha", "sa_block_ratios",
-                 "sa_device_status"):
+                 "sa_device_status", "sa_selftest_bounded_wait"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -298,6 +299,11 @@ def sa_block_ratios(data: np.ndarray, block: int, level: int = 6, n_threads: int
     return out
 
 
+def sa_selftest_bounded_wait(stream=None) -> None:
+    """Launch the failure-path self-test (a wait that times out after 1 s)."""
+    _check("sa_selftest_bounded_wait", load_library().sa_selftest_bounded_wait(_stream_ptr(stream)))
+
+
 def sa_device_status(stream=None) -> int:
     """Synchronises the stream and returns (and clears) the device error status code."""
     return int(load_library().sa_device_status(_stream_ptr(stream)))
@@ -363,6 +369,7 @@ __all__ = [
     "sa_mask_nnz_bound", "sa_build_mask", "sa_attn_fwd", "sa_attn_fwd_heads", "sa_attn_bwd",
     "sa_attn_bwd_workspace_size", "sa_attn_bwd_noalloc", "sa_attn_bwd_heads", "sa_offset_attn_fwd", "sa_offset_attn_interp_fwd",
     "sa_fib_offsets", "sa_pow2_offsets", "sa_layer_alpha", "sa_block_ratios", "sa_device_status",
+    "sa_selftest_bounded_wait",
     # allocating conveniences
     "build_mask", "attn_fwd", "attn_fwd_heads", "attn_bwd", "attn_bwd_heads", "offset_attn_fwd", "offset_attn_interp_fwd",
     # constants

@@ -14,6 +14,7 @@
 #include <cuda_runtime.h>
 
 #include "sa_api.h"
+#include "ptx_sm100.cuh"
 #include "sa_internal.h"
 
 namespace {
@@ -95,6 +96,22 @@ int check_mask_params(const sa_mask_params* p) {
   if (p->mode == SA_MASK_BIGBIRD && p->random_blocks > sa::kMaxRandomBlocks) return SA_ERR_UNSUPPORTED;
   if (p->mode == SA_MASK_LITERAL_MEAN && p->global_blocks != 0) return SA_ERR_UNSUPPORTED;
   return SA_OK;
+}
+
+// Self-test of the bounded waits: one thread waits on an mbarrier that nothing arrives on.
+// After the wait limit the wait gives up, sets the CTA's abort flag and the timeout bit.
+__device__ unsigned int g_selftest_err;
+
+__global__ void bounded_wait_selftest_kernel() {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    sa::mbar_init(&bar, 1);
+    abort_flag = 0;
+    sa::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) sa::mbar_wait(&bar, 0, &abort_flag, &g_selftest_err, sa::kErrTimeout);
 }
 
 int check_attn_common(const void* q, const void* k, const void* v, const int64_t qs[3], const int64_t kvs[3],
@@ -556,11 +573,20 @@ int sa_block_ratios(const uint8_t* h_bytes, int32_t batch, int32_t n_tokens, int
   return failed ? SA_ERR_UNSUPPORTED : SA_OK;
 }
 
+int sa_selftest_bounded_wait(void* stream) {
+  if (!device_ok()) return SA_ERR_CUDA;
+  bounded_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>();
+  return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+}
+
 int sa_device_status(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return SA_ERR_CUDA;
+  unsigned int self = 0, zero = 0;
+  cudaMemcpyFromSymbolAsync(&self, g_selftest_err, sizeof(self), 0, cudaMemcpyDeviceToHost, s);
+  cudaMemcpyToSymbolAsync(g_selftest_err, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, s);
   const unsigned int e = sa::attn_read_and_clear_error(s) | sa::offset_read_and_clear_error(s) |
-                         sa::bwd_read_and_clear_error(s);
+                         sa::bwd_read_and_clear_error(s) | self;
   if (cudaGetLastError() != cudaSuccess) return SA_ERR_CUDA;
   if (e & sa::kErrTimeout) return SA_ERR_TIMEOUT;
   if (e & sa::kErrBadIndex) return SA_ERR_DEVICE;

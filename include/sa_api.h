@@ -271,6 +271,12 @@ int sa_block_ratios(const uint8_t* h_bytes, int32_t batch, int32_t n_tokens, int
  * SA_ERR_CAPACITY (a device-sized structure did not fit the caller's workspace). */
 int sa_device_status(void* stream);
 
+/* Self-test of the failure path: launches a one-thread kernel that waits on a barrier
+ * nothing completes. The wait gives up after the library's wait limit (1 s), records a
+ * timeout and the kernel exits; the next sa_device_status returns SA_ERR_TIMEOUT, and the
+ * context stays usable. No memory is touched. */
+int sa_selftest_bounded_wait(void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* sa_status_string(int status);
 

@@ -34,7 +34,7 @@ def test_header_symbols_exported(lib):
     names = _declared_functions()
     assert {"sa_build_mask", "sa_attn_fwd", "sa_attn_fwd_heads", "sa_offset_attn_fwd", "sa_pow2_offsets",
             "sa_attn_bwd", "sa_attn_bwd_workspace_size", "sa_attn_bwd_noalloc", "sa_offset_attn_interp_fwd",
-            "sa_attn_bwd_heads",
+            "sa_attn_bwd_heads", "sa_selftest_bounded_wait",
             "sa_layer_alpha", "sa_fib_offsets", "sa_block_ratios",
             "sa_mask_nnz_bound", "sa_device_status", "sa_status_string", "sa_version"} <= set(names)
     for n in names:

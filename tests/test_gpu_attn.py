@@ -150,6 +150,16 @@ def test_running_max_rescale_paths(d, b):
                                f"rescale {mode} d={d} b={b}")
 
 
+def test_bounded_wait_times_out_and_context_survives():
+    """A wait on a barrier nothing completes gives up after the wait limit and reports
+    SA_ERR_TIMEOUT; the status is cleared by the read and the device keeps working."""
+    torch = torch_cuda()
+    sa.sa_selftest_bounded_wait()
+    assert sa.sa_device_status() == -5
+    assert sa.sa_device_status() == 0
+    _run_case(om.MaskParams("full", 64, 256, 1), 1, 2, 2, 64, seed=12)
+
+
 def test_bad_csr_index_is_reported():
     torch = torch_cuda()
     bt, n, h, d, b = 1, 256, 1, 64, 64
