@@ -1,0 +1,797 @@
+// Block-sparse flash-attention forward for head dimensions 32 and 64 on sm_103a, with
+// 128-key score tiles and one full score row per softmax thread.
+//
+// Work item: one 128-row query tile of one (sequence, head), as in attn_fwd.cu: the tile's
+// key list is the sorted union of its query blocks' CSR rows, each key block tagged with one
+// membership bit per query block. The list is cut into 32-key chunks and four consecutive
+// chunks form one key tile (128 keys; the last tile of an item may be shorter).
+//
+// Why a second design for small d: at d <= 64 every per-tile step of the softmax (waits,
+// arrivals, TMEM round trips, the online-max bookkeeping) is paid per 32 x 32 chunk when a
+// 64-key tile is split over two warps, and that overhead, not the tensor core or the
+// exponential unit, bounds the 64-key kernel. Here each softmax thread owns a whole 128-key
+// row of S, so the same fixed cost covers four times as many scores and no two warps ever
+// exchange a row maximum.
+//
+// TMEM of pipeline x (256 columns each, two pipelines per CTA):
+//   S [256x, +128)        fp32 scores of the current key tile
+//   P [256x + 128, +64)   bf16 probabilities of the current key tile (two per column)
+//   O [256x + 192, +d)    fp32 output accumulator
+// P has columns of its own, so the QK of key tile j+1 may overwrite S as soon as the softmax
+// has loaded S_j into registers; the exponentials of tile j then overlap with QK_{j+1}.
+//
+// Warp roles (384 threads, 12 warps; warp w runs on SM sub-partition w % 4):
+//   warps 0-3   softmax of pipeline 0, warp w reads TMEM lane quarter w (query rows 32w ..)
+//   warps 4-7   softmax of pipeline 1
+//   warps 8, 11 producers of pipeline 0 / 1: union, key-tile metas, TMA loads of Q, K, V
+//   warps 9, 10 lane 0 issues the tcgen05 MMAs of pipeline 0 / 1:
+//                 S = Q K_j^T   (N = keys of the tile, up to 128)
+//                 O += P_j V_j  (A = P_j from TMEM, B = V_j MN-major; K = 16 keys per MMA)
+//               in the order QK_j, PV_{j-1}: the next tile's scores are requested as soon as
+//               S is free, before the previous tile's probabilities are ready.
+//
+// Token rule: key j of block J is visible to query i of block I iff J is in row(I) and
+// (not causal or j <= i) ("Parameter-free Adaptive Sparse Attention via Compression-Based
+// Content Selection", section 3.4 block-to-token expansion). No token mask is materialised.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "csr_union.cuh"
+#include "ptx_sm100.cuh"
+#include "sa_internal.h"
+#include "tma_host.h"
+
+namespace sa {
+namespace {
+
+__device__ unsigned int g_wide_err;
+
+// Work counters (one slot per launch in flight, round robin, zeroed on the launch's stream).
+constexpr int kWorkSlots = 64;
+__device__ unsigned int g_wide_counters[kWorkSlots];
+
+constexpr int kTile = 128;            // query rows per work item
+constexpr int kKeys = 128;            // keys per S tile (four 32-key chunks)
+constexpr int kThreads = 384;         // 12 warps
+constexpr int kMetaRing = 8;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kSoftmaxWarps = 4;      // per pipeline: one per TMEM lane quarter
+constexpr int kMetaConsumers = 1 + kSoftmaxWarps;
+constexpr int kMaxStages = 4;
+
+template <int D>
+struct Cfg {
+  static_assert(D == 32 || D == 64, "head dimension");
+  static constexpr int ROWB = D * 2;                   // bytes per swizzled row (one d-chunk)
+  static constexpr uint32_t SWZ = ROWB == 128 ? kSwizzle128B : kSwizzle64B;
+  static constexpr CUtensorMapSwizzle TMA_SWZ =
+      ROWB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  static constexpr uint32_t ATOM = 8 * ROWB;           // swizzle atom (8 rows)
+  static constexpr int Q_BYTES = kTile * ROWB;
+  static constexpr int KV_BYTES = kKeys * ROWB;        // one K or V tile
+  static constexpr int QB = 2;                         // Q buffers per pipeline
+  static constexpr int STAGES = D == 64 ? 2 : 4;       // K and V ring depth
+  static constexpr int UNION_BYTES = kMaxTileBlocks * (kMaxMaskBlocks / 32) * 4 + kMaxMaskBlocks * 2;
+  static constexpr int PIPE_BYTES = (QB * Q_BYTES + 2 * STAGES * KV_BYTES + UNION_BYTES + 1023) & ~1023;
+  static constexpr int SMEM = 1024 + 2 * PIPE_BYTES;
+  __host__ __device__ static constexpr uint32_t col_s(int x) { return 256u * x; }
+  __host__ __device__ static constexpr uint32_t col_p(int x) { return 256u * x + 128u; }
+  __host__ __device__ static constexpr uint32_t col_o(int x) { return 256u * x + 192u; }
+  static_assert(STAGES <= kMaxStages, "ring size");
+  static_assert(SMEM <= 227 * 1024, "shared memory");
+};
+
+// Meta kinds: a key tile of the current item, the end of the item, the header of the next
+// item (tm[0] = item index), no more items.
+enum : int { kKindTile = 0, kKindEnd = 1, kKindItem = 2, kKindDone = 3 };
+
+// One ring entry, read by the consumers as two 16-byte loads.
+struct __align__(16) Meta {
+  int kind;
+  int nch;                    // 32-key chunks (1 .. 4) in this key tile
+  int pad[2];
+  int tm[4];                  // chunk c: first key token << 4 | membership bits (bit r: query block r)
+};
+
+__device__ __forceinline__ int4 ld_shared_v4(const void* ptr) {
+  int4 r;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "r"(smem_u32(ptr))
+               : "memory");
+  return r;
+}
+
+struct MetaRegs {
+  int kind, nch;
+  int tm[4];
+};
+
+__device__ __forceinline__ MetaRegs load_meta(const Meta* src) {
+  const int4 a = ld_shared_v4(src);
+  const int4 b = ld_shared_v4(reinterpret_cast<const uint8_t*>(src) + 16);
+  MetaRegs m;
+  m.kind = a.x;
+  m.nch = a.y;
+  m.tm[0] = b.x;
+  m.tm[1] = b.y;
+  m.tm[2] = b.z;
+  m.tm[3] = b.w;
+  return m;
+}
+
+struct Params {
+  int batch, n_tokens, heads, heads_per_kv, block, log2b, nb, causal, csr_shared;
+  int tiles_per_seq;          // 128-row query tiles per (sequence, head)
+  int n_items;
+  unsigned int* work_counter;          // next item index (zeroed before the launch)
+  int n_masks;
+  const int32_t* row_ptr[kMaxMasks];   // one CSR per head group
+  const int32_t* col_idx[kMaxMasks];
+  uint8_t head_mask[kMaxHeadMap];      // query head -> CSR (n_masks > 1)
+  __nv_bfloat16* o;
+  float* lse;
+  int64_t o_sb, o_sn, o_sh;
+  float scale_log2;
+};
+
+struct PipeBars {
+  uint64_t q_full[2], q_empty[2];
+  uint64_t k_full[kMaxStages], k_empty[kMaxStages], v_full[kMaxStages], v_empty[kMaxStages];
+  uint64_t m_full[kMetaRing], m_empty[kMetaRing];
+  uint64_t s_full;            // QK_j complete (phase j)
+  uint64_t s_free;            // the softmax has loaded S_j (phase j)
+  uint64_t p_full;            // the softmax has stored P_j (phase j)
+  uint64_t pv_done[2];        // pv_done[j & 1]: PV_j complete
+  uint64_t drain;
+};
+
+struct Item {
+  int s, h, tile;
+};
+
+// Work item k of the longest-first order: all (sequence, head) pairs of one query-tile rank
+// before the next rank; causal ranks run from the last query tile.
+__device__ __forceinline__ Item decode_item(const Params& p, int k) {
+  const int bh = k % (p.batch * p.heads);
+  const int rank = k / (p.batch * p.heads);
+  Item it;
+  it.h = bh % p.heads;
+  it.s = bh / p.heads;
+  it.tile = p.causal ? (p.tiles_per_seq - 1 - rank) : rank;
+  return it;
+}
+
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  return mbar_wait(bar, parity, abort_flag, &g_wide_err, kErrTimeout);
+}
+
+__device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity) {
+  int never = 0;
+  mbar_wait(bar, parity, &never, &g_wide_err, kErrTimeout);
+}
+
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Publishes one meta entry (lane 0 of the producer warp); returns false on abort.
+__device__ __forceinline__ bool put_meta(PipeBars& bars, Meta* meta, int mt, const Meta& m, volatile int* abort_flag) {
+  const int ms = mt % kMetaRing;
+  if (!wait_bar(&bars.m_empty[ms], ((mt / kMetaRing) & 1) ^ 1, abort_flag)) return false;
+  meta[ms] = m;
+  mbar_arrive(&bars.m_full[ms]);
+  return true;
+}
+
+// ------------------------------------------------------------------ producer (warps 8, 11)
+
+template <int D>
+__device__ void producer(const Params& p, const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
+                         PipeBars& bars, Meta* meta, UnionSmem& u, uint8_t* sQ, uint8_t* sK, uint8_t* sV,
+                         volatile int* abort_flag) {
+  using C = Cfg<D>;
+  const int lane = threadIdx.x & 31;
+  const int b = p.block;
+  const int cpb = b >> 5;                            // 32-key chunks per key block
+  const int qb_per_tile = kTile >> p.log2b;
+  int mt = 0, kt = 0;
+  int k_issued = 0, v_issued = 0;                    // key tiles whose K / V loads were issued
+  int q_last = -1;                                   // item_local of the last Q load
+  bool ok = true;
+
+  for (int item_local = 0;; ++item_local) {
+    int k = 0;
+    if (lane == 0) k = (int)atomicAdd(p.work_counter, 1u);
+    k = __shfl_sync(0xffffffffu, k, 0);
+    {
+      Meta hm;
+      hm.kind = k < p.n_items ? kKindItem : kKindDone;
+      hm.nch = 0;
+      hm.pad[0] = hm.pad[1] = 0;
+      hm.tm[0] = k;
+      hm.tm[1] = hm.tm[2] = hm.tm[3] = 0;
+      if (lane == 0) ok = put_meta(bars, meta, mt, hm, abort_flag);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      ++mt;
+      if (!ok || hm.kind == kKindDone) break;
+    }
+    const Item it = decode_item(p, k);
+    const int q0 = it.tile * kTile;
+    const int I0 = q0 >> p.log2b;
+    const int hk = it.h / p.heads_per_kv;
+    const int nq = min(qb_per_tile, p.nb - I0);
+    const int mi = p.n_masks > 1 ? p.head_mask[it.h] : 0;
+    const int32_t* rp = p.row_ptr[mi] + (size_t)(p.csr_shared ? 0 : it.s) * (p.nb + 1);
+
+    // Q into buffer item_local % QB (rows beyond the sequence are zero-filled by TMA)
+    if (lane == 0) {
+      const int qb = item_local % C::QB;
+      if (item_local >= C::QB) ok = wait_bar(&bars.q_empty[qb], ((item_local / C::QB) - 1) & 1, abort_flag);
+      if (ok) {
+        mbar_arrive_expect_tx(&bars.q_full[qb], C::Q_BYTES);
+        tma_load_4d(sQ + qb * C::Q_BYTES, tq, &bars.q_full[qb], 0, it.h, q0, it.s);
+        q_last = item_local;
+      }
+    }
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    if (!ok) break;
+
+    const int n_keys = build_union(p.nb, p.causal ? kKeepLE : kKeepAll, u, rp, p.col_idx[mi], I0, nq, &g_wide_err,
+                                   kErrBadIndex);
+    const int n_chunks = n_keys * cpb;
+
+    for (int c0 = 0;; c0 += 4) {
+      Meta m;
+      m.kind = c0 < n_chunks ? kKindTile : kKindEnd;
+      m.nch = min(4, n_chunks - c0);
+      m.pad[0] = m.pad[1] = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int q = c0 + i;
+        const uint32_t e = (i < m.nch) ? u.list[q / cpb] : 0u;
+        const int tok = (int)(e & 0xfffu) * b + (q % cpb) * 32;
+        m.tm[i] = (i < m.nch) ? ((tok << 4) | (int)(e >> 12)) : 0;
+      }
+      if (lane == 0) {
+        ok = put_meta(bars, meta, mt, m, abort_flag);
+        if (ok && m.kind == kKindTile) {
+          const int st = kt % C::STAGES;
+          const uint32_t ph = (kt / C::STAGES) & 1;
+          const uint32_t bytes = (uint32_t)(m.nch * 32 * D * 2);
+          // b = 32: one 32-row box per chunk; b >= 64: one 64-row box per chunk pair
+          const int rows = b == 32 ? 32 : 64;
+          const int nbox = (m.nch * 32 + rows - 1) / rows;
+          ok = wait_bar(&bars.k_empty[st], ph ^ 1, abort_flag);
+          if (ok) {
+            mbar_arrive_expect_tx(&bars.k_full[st], bytes);
+            for (int i = 0; i < nbox; ++i)
+              tma_load_4d(sK + st * C::KV_BYTES + i * rows * C::ROWB, tk, &bars.k_full[st], 0, hk,
+                          m.tm[i * rows / 32] >> 4, it.s);
+            k_issued = kt + 1;
+            ok = wait_bar(&bars.v_empty[st], ph ^ 1, abort_flag);
+          }
+          if (ok) {
+            mbar_arrive_expect_tx(&bars.v_full[st], bytes);
+            for (int i = 0; i < nbox; ++i)
+              tma_load_4d(sV + st * C::KV_BYTES + i * rows * C::ROWB, tv, &bars.v_full[st], 0, hk,
+                          m.tm[i * rows / 32] >> 4, it.s);
+            v_issued = kt + 1;
+          }
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      ++mt;
+      if (m.kind == kKindTile) ++kt;
+      if (!ok || m.kind == kKindEnd) break;
+    }
+    __syncwarp();   // the next tile's union may overwrite the list
+  }
+  // Drain this pipeline's own copies in flight before the CTA may exit.
+  if (lane == 0) {
+    for (int i = max(0, q_last - C::QB + 1); i <= q_last; ++i) drain_bar(&bars.q_full[i % C::QB], (i / C::QB) & 1);
+    for (int t = max(0, k_issued - C::STAGES); t < k_issued; ++t)
+      drain_bar(&bars.k_full[t % C::STAGES], (t / C::STAGES) & 1);
+    for (int t = max(0, v_issued - C::STAGES); t < v_issued; ++t)
+      drain_bar(&bars.v_full[t % C::STAGES], (t / C::STAGES) & 1);
+  }
+  __syncwarp();
+}
+
+// ------------------------------------------------------------------ MMA issuer (warps 9, 10, lane 0)
+
+// O += P_j V_j for the key tile held in ring stage `stage` (its V load was the kt-th),
+// after P_j is stored. `o_init` says whether O already holds this item's sum.
+template <int D>
+__device__ __forceinline__ bool issue_pv(PipeBars& bars, uint32_t tP, uint32_t tO, uint64_t vdesc0, int j, int stage,
+                                         int vkt, int nkeys, bool& o_init, volatile int* abort_flag) {
+  using C = Cfg<D>;
+  if (!wait_bar(&bars.p_full, (uint32_t)j & 1u, abort_flag)) return false;
+  if (!wait_bar(&bars.v_full[stage], (uint32_t)(vkt / C::STAGES) & 1u, abort_flag)) return false;
+  tc_fence_after();
+  constexpr uint32_t idesc = make_idesc_bf16(128, D, 0, 1);
+  const uint64_t b0 = vdesc0 + (uint64_t)((stage * C::KV_BYTES) >> 4);
+  for (int ks = 0; ks < nkeys / 16; ++ks)
+    mma_bf16_ts(tO, tP + 8u * ks, b0 + (uint64_t)((16 * ks * C::ROWB) >> 4), idesc, (o_init || ks > 0) ? 1u : 0u);
+  o_init = true;
+  mma_commit(&bars.pv_done[j & 1]);
+  mma_commit(&bars.v_empty[stage]);
+  return true;
+}
+
+template <int D>
+__device__ void mma_issuer(int x, PipeBars& bars, Meta* meta, uint8_t* sQ, uint8_t* sK, uint8_t* sV, uint32_t tmem,
+                           volatile int* abort_flag) {
+  using C = Cfg<D>;
+  const uint64_t qdesc = make_smem_desc(smem_u32(sQ), 16, C::ATOM, C::SWZ);
+  const uint64_t kdesc0 = make_smem_desc(smem_u32(sK), 16, C::ATOM, C::SWZ);
+  const uint64_t vdesc0 = make_smem_desc(smem_u32(sV), C::KV_BYTES, C::ATOM, C::SWZ);
+  const uint32_t tS = tmem + C::col_s(x), tP = tmem + C::col_p(x), tO = tmem + C::col_o(x);
+  int mt = 0;               // metas read
+  int kt = 0;               // key tiles read (K/V ring position)
+  int g = 0;                // key tiles of this pipeline whose QK is issued
+  bool ok = true;
+  for (int item_local = 0; ok; ++item_local) {
+    {
+      const int ms = mt & (kMetaRing - 1);
+      if (!(ok = wait_bar(&bars.m_full[ms], (uint32_t)(mt / kMetaRing) & 1u, abort_flag))) break;
+      const MetaRegs hm = load_meta(&meta[ms]);
+      mbar_arrive(&bars.m_empty[ms]);
+      ++mt;
+      if (hm.kind == kKindDone) break;
+    }
+    const int qb = item_local % C::QB;
+    if (!(ok = wait_bar(&bars.q_full[qb], (item_local / C::QB) & 1, abort_flag))) break;
+    const uint64_t a0 = qdesc + (uint64_t)((qb * C::Q_BYTES) >> 4);
+    bool o_init = false;
+    bool pend = false;        // PV of the previous key tile of this item not yet issued
+    int p_stage = 0, p_vkt = 0, p_nkeys = 0;
+    for (;;) {
+      const int ms = mt & (kMetaRing - 1);
+      if (!(ok = wait_bar(&bars.m_full[ms], (uint32_t)(mt / kMetaRing) & 1u, abort_flag))) break;
+      const MetaRegs m = load_meta(&meta[ms]);
+      mbar_arrive(&bars.m_empty[ms]);
+      ++mt;
+      if (m.kind != kKindTile) break;
+      const int stage = kt % C::STAGES;
+      const int nkeys = m.nch * 32;
+      if (!(ok = wait_bar(&bars.k_full[stage], (uint32_t)(kt / C::STAGES) & 1u, abort_flag))) break;
+      // S is free once the softmax has loaded S_{g-1}
+      if (g > 0 && !(ok = wait_bar(&bars.s_free, (uint32_t)(g - 1) & 1u, abort_flag))) break;
+      tc_fence_after();
+      const uint32_t idesc = make_idesc_bf16(128, (uint32_t)nkeys, 0, 0);
+      const uint64_t b0 = kdesc0 + (uint64_t)((stage * C::KV_BYTES) >> 4);
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks)
+        mma_bf16_ss(tS, a0 + (uint64_t)((ks * 32) >> 4), b0 + (uint64_t)((ks * 32) >> 4), idesc, ks > 0 ? 1u : 0u);
+      mma_commit(&bars.s_full);
+      mma_commit(&bars.k_empty[stage]);
+      if (pend && !(ok = issue_pv<D>(bars, tP, tO, vdesc0, g - 1, p_stage, p_vkt, p_nkeys, o_init, abort_flag)))
+        break;
+      pend = true;
+      p_stage = stage;
+      p_vkt = kt;
+      p_nkeys = nkeys;
+      ++kt;
+      ++g;
+    }
+    if (!ok) break;
+    // the item's last PV: its completion releases the softmax epilogue
+    if (pend && !(ok = issue_pv<D>(bars, tP, tO, vdesc0, g - 1, p_stage, p_vkt, p_nkeys, o_init, abort_flag))) break;
+    mma_commit(&bars.q_empty[qb]);   // all QKs of this item issued; arrives when they are done
+  }
+  // Make sure no MMA of this thread is still writing TMEM when the CTA frees it.
+  mma_commit(&bars.drain);
+  drain_bar(&bars.drain, 0);
+}
+
+// ------------------------------------------------------------------ softmax + epilogue (warps 0-7)
+
+// Max of the 32 scores of one chunk, folded into acc.
+__device__ __forceinline__ float chunk_max(const uint32_t* v, float acc) {
+  const float kNegInf = __int_as_float(0xff800000);
+  float a[4] = {acc, kNegInf, kNegInf, kNegInf};
+#pragma unroll
+  for (int j = 0; j < 32; j += 2)
+    a[(j >> 1) & 3] = max3(a[(j >> 1) & 3], __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
+  return fmaxf(max3(a[0], a[1], a[2]), a[3]);
+}
+
+// Causal diagonal chunk: scores of columns this row may not see become -inf (bit j of kp:
+// column j visible), so the unmasked max and exponential paths below handle the chunk.
+__device__ __forceinline__ void mask_chunk(uint32_t* v, uint32_t kp) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = ((kp >> j) & 1u) ? v[j] : 0xff800000u;
+}
+
+// p = 2^(s c - m) of one chunk into packed bf16 (a score of -inf gives exactly 0); adds the
+// row sum into rs.
+__device__ __forceinline__ void chunk_exp(const uint32_t* v, uint64_t c2, uint64_t negm2, uint32_t* pk, uint64_t* rs) {
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    float x0, x1;
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), c2, negm2), x0, x1);
+    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+    rs[(j >> 1) & 1] = f2_add(rs[(j >> 1) & 1], f2_pack(p0, p1));
+    pk[j >> 1] = pack_bf16x2(p0, p1);
+  }
+}
+
+// Rare path of the online max: O *= alpha for this thread's row (O quiescent).
+template <int D>
+__device__ __forceinline__ void rescale_o(uint32_t tO, float alpha) {
+  const uint64_t al2 = f2_pack(alpha, alpha);
+#pragma unroll 1
+  for (int ch = 0; ch < D / 32; ++ch) {
+    uint32_t ov[32];
+    tmem_ld_x32(tO + ch * 32, ov);
+    tmem_ld_wait<32>(ov);
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+      float lo, hi;
+      f2_unpack(f2_mul(f2_pack(__uint_as_float(ov[j]), __uint_as_float(ov[j + 1])), al2), lo, hi);
+      ov[j] = __float_as_uint(lo);
+      ov[j + 1] = __float_as_uint(hi);
+    }
+    tmem_st_x32(tO + ch * 32, ov);
+  }
+  tmem_st_wait();
+}
+
+// Softmax and epilogue of pipeline x; this warp handles query rows 32q .. 32q+31 of every
+// item (q = its TMEM lane quarter) and all 128 keys of every key tile.
+template <int D>
+__device__ void softmax_epilogue(const Params& p, int x, PipeBars& bars, Meta* meta, uint32_t tmem,
+                                 volatile int* abort_flag) {
+  using C = Cfg<D>;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quarter = warp & 3;
+  const int row = quarter * 32 + lane;               // query row within the tile
+  const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+  const int sub = (quarter * 32) >> p.log2b;         // query block within the tile (warp-uniform)
+  const float kNegInf = __int_as_float(0xff800000);
+  const float c = p.scale_log2;
+  const uint64_t c2 = f2_pack(c, c);
+  const uint32_t tS = tmem + C::col_s(x) + lane_base;
+  const uint32_t tP = tmem + C::col_p(x) + lane_base;
+  const uint32_t tO = tmem + C::col_o(x) + lane_base;
+
+  int mt = 0, g = 0;        // meta position, key tiles processed by this pipeline
+  bool ok = true;
+  for (;;) {
+    int k;
+    {
+      const int ms = mt % kMetaRing;
+      if (!(ok = wait_bar(&bars.m_full[ms], (mt / kMetaRing) & 1, abort_flag))) break;
+      const MetaRegs hm = load_meta(&meta[ms]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.m_empty[ms]);
+      ++mt;
+      if (hm.kind == kKindDone) break;
+      k = hm.tm[0];
+    }
+    const Item it = decode_item(p, k);
+    const int qtok = it.tile * kTile + row;
+    const int q_warp = it.tile * kTile + quarter * 32;
+    float m_use = kNegInf;   // running reference max, log2 units
+    float l = 0.f;           // row sum
+    int n_item = 0;
+    for (;;) {
+      const int ms = mt % kMetaRing;
+      if (!(ok = wait_bar(&bars.m_full[ms], (mt / kMetaRing) & 1, abort_flag))) break;
+      const MetaRegs m = load_meta(&meta[ms]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.m_empty[ms]);
+      ++mt;
+      if (m.kind != kKindTile) break;
+
+      // Visibility of each 32-key chunk for this warp's 32 rows (warp-uniform): bit ch of
+      // vis: some row sees some key of chunk ch. Query and key chunks start at multiples of
+      // 32, so under causality at most one chunk (the one starting at this warp's first
+      // query) is the diagonal, where row r sees columns 0 .. r.
+      int vis = 0, dch = -1;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        const int tm = m.tm[ch];
+        if (ch < m.nch && ((tm >> sub) & 1)) {
+          const int lim0 = q_warp - (tm >> 4);       // row r sees columns c <= lim0 + r
+          if (!p.causal || lim0 >= 31) {
+            vis |= 1 << ch;
+          } else if (lim0 + 31 >= 0) {
+            vis |= 1 << ch;
+            dch = ch;
+          }
+        }
+      }
+
+      ok = __all_sync(0xffffffffu, wait_bar(&bars.s_full, (uint32_t)g & 1u, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t v[128];
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) tmem_ld_x32(tS + 32 * ch, v + 32 * ch);
+      tmem_ld_wait<128>(v);
+      // S may now be overwritten by the next QK
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.s_free);
+
+      if (dch >= 0) {
+        const int lim = q_warp - (m.tm[dch] >> 4) + lane;
+        const uint32_t kp = lim >= 31 ? 0xffffffffu : (lim < 0 ? 0u : ((2u << lim) - 1u));
+        switch (dch) {
+          case 0: mask_chunk(v, kp); break;
+          case 1: mask_chunk(v + 32, kp); break;
+          case 2: mask_chunk(v + 64, kp); break;
+          default: mask_chunk(v + 96, kp); break;
+        }
+      }
+      float cm = kNegInf;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch)
+        if ((vis >> ch) & 1) cm = chunk_max(v + 32 * ch, cm);
+      const float mx = cm * c;                       // -inf stays -inf
+      const bool need = mx > m_use + 8.0f;
+      float alpha = 1.f;
+      bool o_scale = false;
+      if (__any_sync(0xffffffffu, need)) {
+        // the running max grows by more than 2^8: rescale l now and O before this tile's PV
+        alpha = need ? ex2_approx(m_use - mx) : 1.f;   // 0 when m_use = -inf
+        o_scale = need && m_use != kNegInf && n_item > 0;
+        l *= alpha;
+        if (need) m_use = mx;
+      }
+      const uint64_t negm2 = f2_pack(-m_use, -m_use);
+      uint64_t rs[2] = {0ull, 0ull};
+      uint32_t pk[16];
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        if ((vis >> ch) & 1) {
+          chunk_exp(v + 32 * ch, c2, negm2, pk, rs);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) pk[j] = 0u;
+        }
+        if (ch == 0) {
+          // PV_{g-1} has read P and finished writing O
+          if (g > 0) {
+            ok = __all_sync(0xffffffffu,
+                            wait_bar(&bars.pv_done[(g - 1) & 1], (uint32_t)((g - 1) >> 1) & 1u, abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+          }
+          if (__any_sync(0xffffffffu, o_scale)) rescale_o<D>(tO, alpha);
+        }
+        if (ch < m.nch) tmem_st_x16(tP + 16 * ch, pk);
+      }
+      if (!ok) break;
+      {
+        const uint64_t rs2 = f2_add(rs[0], rs[1]);
+        float rs_lo, rs_hi;
+        f2_unpack(rs2, rs_lo, rs_hi);
+        l += rs_lo + rs_hi;
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.p_full);
+      ++g;
+      ++n_item;
+    }
+    if (!ok) break;
+
+    // epilogue: O / l and LSE of this query tile's rows
+    if (n_item > 0) {
+      ok = __all_sync(0xffffffffu, wait_bar(&bars.pv_done[(g - 1) & 1], (uint32_t)((g - 1) >> 1) & 1u, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+    }
+    const bool store = qtok < p.n_tokens;
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    __nv_bfloat16* orow = p.o + (int64_t)it.s * p.o_sb + (int64_t)qtok * p.o_sn + (int64_t)it.h * p.o_sh;
+#pragma unroll
+    for (int ch = 0; ch < D / 32; ++ch) {
+      uint32_t ov[32];
+      if (n_item > 0) {
+        tmem_ld_x32(tO + 32 * ch, ov);
+        tmem_ld_wait<32>(ov);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) ov[j] = 0u;
+      }
+      if (store) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 32; j += 2)
+          pk[j >> 1] = pack_bf16x2(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv);
+        uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+      }
+    }
+    if (store) {
+      const float lse = l > 0.f ? (m_use + __log2f(l)) * 0.69314718055994531f : kNegInf;
+      p.lse[((int64_t)it.s * p.heads + it.h) * p.n_tokens + qtok] = lse;
+    }
+    // The next item's first P store follows these O loads in program order, and the MMA
+    // thread issues that item's first PV only after the P store: O is not overwritten early.
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                         const __grid_constant__ CUtensorMap tv, const __grid_constant__ Params p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sbase = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ PipeBars bars[2];
+  __shared__ Meta meta[2][kMetaRing];
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    for (int x = 0; x < 2; ++x) {
+      PipeBars& b = bars[x];
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&b.q_full[i], 1);
+        mbar_init(&b.q_empty[i], 1);
+      }
+      for (int i = 0; i < C::STAGES; ++i) {
+        mbar_init(&b.k_full[i], 1);
+        mbar_init(&b.k_empty[i], 1);
+        mbar_init(&b.v_full[i], 1);
+        mbar_init(&b.v_empty[i], 1);
+      }
+      for (int i = 0; i < kMetaRing; ++i) {
+        mbar_init(&b.m_full[i], 1);
+        mbar_init(&b.m_empty[i], kMetaConsumers);
+      }
+      mbar_init(&b.s_full, 1);
+      mbar_init(&b.s_free, kSoftmaxWarps);
+      mbar_init(&b.p_full, kSoftmaxWarps);
+      mbar_init(&b.pv_done[0], 1);
+      mbar_init(&b.pv_done[1], 1);
+      mbar_init(&b.drain, 1);
+    }
+    abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tq);
+    tma_prefetch_desc(&tk);
+    tma_prefetch_desc(&tv);
+  }
+  if (warp == 9) {
+    tmem_alloc(&tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  // pipeline 0: softmax warps 0-3, producer 8, MMA 9; pipeline 1: softmax 4-7, MMA 10, producer 11
+  const int x = warp < 8 ? (warp >> 2) : (warp == 8 || warp == 9 ? 0 : 1);
+  uint8_t* sQ = sbase + x * C::PIPE_BYTES;
+  uint8_t* sK = sQ + C::QB * C::Q_BYTES;
+  uint8_t* sV = sK + C::STAGES * C::KV_BYTES;
+  UnionSmem& un = *reinterpret_cast<UnionSmem*>(sV + C::STAGES * C::KV_BYTES);
+
+  if (warp < 8) {
+    softmax_epilogue<D>(p, x, bars[x], meta[x], tmem, &abort_flag);
+  } else if (warp == 8 || warp == 11) {
+    producer<D>(p, &tq, &tk, &tv, bars[x], meta[x], un, sQ, sK, sV, &abort_flag);
+  } else {
+    if ((threadIdx.x & 31) == 0) mma_issuer<D>(x, bars[x], meta[x], sQ, sK, sV, tmem, &abort_flag);
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D>
+int launch_d(const AttnArgs& a, cudaStream_t stream) {
+  using C = Cfg<D>;
+  CUtensorMap tq, tk, tv;
+  const uint32_t kv_rows = a.block == 32 ? 32u : 64u;
+  if (!encode_bhnd_map(&tq, a.q, a.batch, a.n_tokens, a.heads, D, a.q_strides[0], a.q_strides[1], a.q_strides[2], D,
+                       kTile, C::TMA_SWZ) ||
+      !encode_bhnd_map(&tk, a.k, a.batch, a.n_tokens, a.kv_heads, D, a.kv_strides[0], a.kv_strides[1],
+                       a.kv_strides[2], D, kv_rows, C::TMA_SWZ) ||
+      !encode_bhnd_map(&tv, a.v, a.batch, a.n_tokens, a.kv_heads, D, a.kv_strides[0], a.kv_strides[1],
+                       a.kv_strides[2], D, kv_rows, C::TMA_SWZ))
+    return SA_ERR_UNSUPPORTED;
+  Params p;
+  p.batch = a.batch;
+  p.n_tokens = a.n_tokens;
+  p.heads = a.heads;
+  p.heads_per_kv = a.heads / a.kv_heads;
+  p.block = a.block;
+  p.log2b = __builtin_ctz((unsigned)a.block);
+  p.nb = a.n_tokens / a.block;
+  p.causal = a.causal;
+  p.csr_shared = a.csr_shared;
+  p.tiles_per_seq = (a.n_tokens + kTile - 1) / kTile;
+  p.n_items = a.batch * a.heads * p.tiles_per_seq;
+  p.n_masks = a.n_masks;
+  for (int m = 0; m < kMaxMasks; ++m) {
+    p.row_ptr[m] = a.row_ptr[m];
+    p.col_idx[m] = a.col_idx[m];
+  }
+  for (int h = 0; h < kMaxHeadMap; ++h) p.head_mask[h] = a.head_mask[h];
+  p.o = static_cast<__nv_bfloat16*>(a.o);
+  p.lse = a.lse;
+  p.o_sb = a.o_strides[0];
+  p.o_sn = a.o_strides[1];
+  p.o_sh = a.o_strides[2];
+  p.scale_log2 = a.softmax_scale * 1.4426950408889634f;
+  unsigned int* counters = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&counters), g_wide_counters) != cudaSuccess) return SA_ERR_CUDA;
+  static std::atomic<unsigned int> ticket{0};
+  p.work_counter = counters + (ticket.fetch_add(1u) % kWorkSlots);
+  if (cudaMemsetAsync(p.work_counter, 0, sizeof(unsigned int), stream) != cudaSuccess) return SA_ERR_CUDA;
+  const int sm_count = current_sm_count();
+  auto kern = attn_fwd_wide_kernel<D>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+    return SA_ERR_CUDA;
+  const int want = (p.n_items + 1) / 2;
+  const int grid = want < sm_count ? want : sm_count;
+  kern<<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_attn_fwd_wide(const AttnArgs& a, cudaStream_t stream) {
+  switch (a.head_dim) {
+    case 32: return launch_d<32>(a, stream);
+    case 64: return launch_d<64>(a, stream);
+  }
+  return SA_ERR_UNSUPPORTED;
+}
+
+unsigned int attn_wide_read_and_clear_error(cudaStream_t stream) {
+  unsigned int v = 0, zero = 0;
+  cudaMemcpyFromSymbolAsync(&v, g_wide_err, sizeof(v), 0, cudaMemcpyDeviceToHost, stream);
+  cudaMemcpyToSymbolAsync(g_wide_err, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, stream);
+  cudaStreamSynchronize(stream);
+  return v;
+}
+
+}  // namespace sa
