@@ -20,10 +20,12 @@
 // P has columns of its own, so the QK of key tile j+1 may overwrite S as soon as the softmax
 // has loaded S_j into registers; the exponentials of tile j then overlap with QK_{j+1}.
 //
-// Warp roles (384 threads, 12 warps; warp w runs on SM sub-partition w % 4):
+// Warp roles (512 threads, 16 warps; warp w runs on SM sub-partition w % 4):
 //   warps 0-3   softmax of pipeline 0, warp w reads TMEM lane quarter w (query rows 32w ..)
 //   warps 4-7   softmax of pipeline 1
-//   warps 8, 11 producers of pipeline 0 / 1: union, key-tile metas, TMA loads of Q, K, V
+//   warps 12, 13 planners of pipeline 0 / 1: claim items, build the key-block union, publish
+//               the item's key tiles into a 32-entry meta ring (an item or more ahead)
+//   warps 8, 11 lane 0 loads Q, K and V of pipeline 0 / 1 by TMA as the metas arrive
 //   warps 9, 10 lane 0 issues the tcgen05 MMAs of pipeline 0 / 1:
 //                 S = Q K_j^T   (N = keys of the tile, up to 128)
 //                 O += P_j V_j  (A = P_j from TMEM, B = V_j MN-major; K = 16 keys per MMA)
@@ -56,11 +58,18 @@ __device__ unsigned int g_wide_counters[kWorkSlots];
 
 constexpr int kTile = 128;            // query rows per work item
 constexpr int kKeys = 128;            // keys per S tile (four 32-key chunks)
-constexpr int kThreads = 384;         // 12 warps
-constexpr int kMetaRing = 8;
+constexpr int kThreads = 512;         // 16 warps, four warpgroups
+constexpr int kMetaRing = 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSoftmaxWarps = 4;      // per pipeline: one per TMEM lane quarter
-constexpr int kMetaConsumers = 1 + kSoftmaxWarps;
+constexpr int kMetaConsumers = 2 + kSoftmaxWarps;   // MMA thread, loader, softmax warps
+// Register split (setmaxnreg): the launch gives every thread 128 registers; the two
+// warpgroups of control warps drop to kCtrlRegs so that the softmax warpgroups can hold a
+// whole 128-key score row: 8 warps x 184 + 8 warps x 72 = 16 warps x 128 per thread.
+constexpr int kLaunchRegs = 128;
+constexpr int kSoftmaxRegs = 184;
+constexpr int kCtrlRegs = 72;
+static_assert(8 * kSoftmaxRegs + 8 * kCtrlRegs == 16 * kLaunchRegs, "register split");
 constexpr int kMaxStages = 4;
 
 template <int D>
@@ -73,15 +82,17 @@ struct Cfg {
   static constexpr uint32_t ATOM = 8 * ROWB;           // swizzle atom (8 rows)
   static constexpr int Q_BYTES = kTile * ROWB;
   static constexpr int KV_BYTES = kKeys * ROWB;        // one K or V tile
+  // Ring depths. V is loaded one key tile behind K (it is needed one softmax later).
   static constexpr int QB = 2;                         // Q buffers per pipeline
-  static constexpr int STAGES = D == 64 ? 2 : 4;       // K and V ring depth
+  static constexpr int KS = D == 64 ? 2 : 4;           // K ring depth
+  static constexpr int VS = D == 64 ? 2 : 4;           // V ring depth
   static constexpr int UNION_BYTES = kMaxTileBlocks * (kMaxMaskBlocks / 32) * 4 + kMaxMaskBlocks * 2;
-  static constexpr int PIPE_BYTES = (QB * Q_BYTES + 2 * STAGES * KV_BYTES + UNION_BYTES + 1023) & ~1023;
+  static constexpr int PIPE_BYTES = (QB * Q_BYTES + (KS + VS) * KV_BYTES + UNION_BYTES + 1023) & ~1023;
   static constexpr int SMEM = 1024 + 2 * PIPE_BYTES;
   __host__ __device__ static constexpr uint32_t col_s(int x) { return 256u * x; }
   __host__ __device__ static constexpr uint32_t col_p(int x) { return 256u * x + 128u; }
   __host__ __device__ static constexpr uint32_t col_o(int x) { return 256u * x + 192u; }
-  static_assert(STAGES <= kMaxStages, "ring size");
+  static_assert(KS <= kMaxStages && VS <= kMaxStages, "ring size");
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
@@ -204,7 +215,7 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return d;
 }
 
-// Publishes one meta entry (lane 0 of the producer warp); returns false on abort.
+// Publishes one meta entry (lane 0 of the planner warp); returns false on abort.
 __device__ __forceinline__ bool put_meta(PipeBars& bars, Meta* meta, int mt, const Meta& m, volatile int* abort_flag) {
   const int ms = mt % kMetaRing;
   if (!wait_bar(&bars.m_empty[ms], ((mt / kMetaRing) & 1) ^ 1, abort_flag)) return false;
@@ -213,29 +224,63 @@ __device__ __forceinline__ bool put_meta(PipeBars& bars, Meta* meta, int mt, con
   return true;
 }
 
-// ------------------------------------------------------------------ producer (warps 8, 11)
+// ------------------------------------------------------------------ tile loads
 
+// The TMA boxes of one key tile (b = 32: one 32-row box per chunk; b >= 64: one 64-row box
+// per chunk pair) and where they go. V is loaded one key tile behind K, so the boxes of the
+// tile whose V is pending are kept here: the union list may already hold the next item.
+struct TileLoad {
+  int t;                      // key tile index within this pipeline (ring position)
+  int nbox, rows, s, hk;
+  uint32_t bytes;
+  int tok[4];
+};
+
+// Lane 0: waits for ring stage t % S of (full, empty) and issues the tile's boxes into it.
+template <int S, int ROWB>
+__device__ __forceinline__ bool load_tile(const TileLoad& L, const CUtensorMap* map, uint8_t* ring, int stage_bytes,
+                                          uint64_t* full, uint64_t* empty, volatile int* abort_flag) {
+  const int st = L.t % S;
+  if (!wait_bar(&empty[st], ((L.t / S) & 1) ^ 1, abort_flag)) return false;
+  mbar_arrive_expect_tx(&full[st], L.bytes);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    if (i < L.nbox) tma_load_4d(ring + st * stage_bytes + i * L.rows * ROWB, map, &full[st], 0, L.hk, L.tok[i], L.s);
+  return true;
+}
+
+// ------------------------------------------------------------------ planner (warps 12, 13)
+
+// Claims work items from the launch-wide counter, builds each item's key-block union and
+// publishes the item (header, key tiles, end) into the meta ring. The ring holds more than
+// an item, so the union of the next item is built while the consumers still work on the
+// current one.
 template <int D>
-__device__ void producer(const Params& p, const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
-                         PipeBars& bars, Meta* meta, UnionSmem& u, uint8_t* sQ, uint8_t* sK, uint8_t* sV,
-                         volatile int* abort_flag) {
-  using C = Cfg<D>;
+__device__ void planner(const Params& p, PipeBars& bars, Meta* meta, UnionSmem& u, volatile int* abort_flag) {
   const int lane = threadIdx.x & 31;
   const int b = p.block;
   const int cpb = b >> 5;                            // 32-key chunks per key block
   const int qb_per_tile = kTile >> p.log2b;
-  int mt = 0, kt = 0;
-  int k_issued = 0, v_issued = 0;                    // key tiles whose K / V loads were issued
-  int q_last = -1;                                   // item_local of the last Q load
+  int mt = 0;
   bool ok = true;
-
-  for (int item_local = 0;; ++item_local) {
+  for (;;) {
     int k = 0;
     if (lane == 0) k = (int)atomicAdd(p.work_counter, 1u);
     k = __shfl_sync(0xffffffffu, k, 0);
+    const bool done = k >= p.n_items;
+    int n_chunks = 0;
+    if (!done) {
+      const Item it = decode_item(p, k);
+      const int I0 = (it.tile * kTile) >> p.log2b;
+      const int nq = min(qb_per_tile, p.nb - I0);
+      const int mi = p.n_masks > 1 ? p.head_mask[it.h] : 0;
+      const int32_t* rp = p.row_ptr[mi] + (size_t)(p.csr_shared ? 0 : it.s) * (p.nb + 1);
+      n_chunks = cpb * build_union(p.nb, p.causal ? kKeepLE : kKeepAll, u, rp, p.col_idx[mi], I0, nq, &g_wide_err,
+                                   kErrBadIndex);
+    }
     {
       Meta hm;
-      hm.kind = k < p.n_items ? kKindItem : kKindDone;
+      hm.kind = done ? kKindDone : kKindItem;
       hm.nch = 0;
       hm.pad[0] = hm.pad[1] = 0;
       hm.tm[0] = k;
@@ -243,33 +288,8 @@ __device__ void producer(const Params& p, const CUtensorMap* tq, const CUtensorM
       if (lane == 0) ok = put_meta(bars, meta, mt, hm, abort_flag);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       ++mt;
-      if (!ok || hm.kind == kKindDone) break;
+      if (!ok || done) break;
     }
-    const Item it = decode_item(p, k);
-    const int q0 = it.tile * kTile;
-    const int I0 = q0 >> p.log2b;
-    const int hk = it.h / p.heads_per_kv;
-    const int nq = min(qb_per_tile, p.nb - I0);
-    const int mi = p.n_masks > 1 ? p.head_mask[it.h] : 0;
-    const int32_t* rp = p.row_ptr[mi] + (size_t)(p.csr_shared ? 0 : it.s) * (p.nb + 1);
-
-    // Q into buffer item_local % QB (rows beyond the sequence are zero-filled by TMA)
-    if (lane == 0) {
-      const int qb = item_local % C::QB;
-      if (item_local >= C::QB) ok = wait_bar(&bars.q_empty[qb], ((item_local / C::QB) - 1) & 1, abort_flag);
-      if (ok) {
-        mbar_arrive_expect_tx(&bars.q_full[qb], C::Q_BYTES);
-        tma_load_4d(sQ + qb * C::Q_BYTES, tq, &bars.q_full[qb], 0, it.h, q0, it.s);
-        q_last = item_local;
-      }
-    }
-    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    if (!ok) break;
-
-    const int n_keys = build_union(p.nb, p.causal ? kKeepLE : kKeepAll, u, rp, p.col_idx[mi], I0, nq, &g_wide_err,
-                                   kErrBadIndex);
-    const int n_chunks = n_keys * cpb;
-
     for (int c0 = 0;; c0 += 4) {
       Meta m;
       m.kind = c0 < n_chunks ? kKindTile : kKindEnd;
@@ -282,49 +302,80 @@ __device__ void producer(const Params& p, const CUtensorMap* tq, const CUtensorM
         const int tok = (int)(e & 0xfffu) * b + (q % cpb) * 32;
         m.tm[i] = (i < m.nch) ? ((tok << 4) | (int)(e >> 12)) : 0;
       }
-      if (lane == 0) {
-        ok = put_meta(bars, meta, mt, m, abort_flag);
-        if (ok && m.kind == kKindTile) {
-          const int st = kt % C::STAGES;
-          const uint32_t ph = (kt / C::STAGES) & 1;
-          const uint32_t bytes = (uint32_t)(m.nch * 32 * D * 2);
-          // b = 32: one 32-row box per chunk; b >= 64: one 64-row box per chunk pair
-          const int rows = b == 32 ? 32 : 64;
-          const int nbox = (m.nch * 32 + rows - 1) / rows;
-          ok = wait_bar(&bars.k_empty[st], ph ^ 1, abort_flag);
-          if (ok) {
-            mbar_arrive_expect_tx(&bars.k_full[st], bytes);
-            for (int i = 0; i < nbox; ++i)
-              tma_load_4d(sK + st * C::KV_BYTES + i * rows * C::ROWB, tk, &bars.k_full[st], 0, hk,
-                          m.tm[i * rows / 32] >> 4, it.s);
-            k_issued = kt + 1;
-            ok = wait_bar(&bars.v_empty[st], ph ^ 1, abort_flag);
-          }
-          if (ok) {
-            mbar_arrive_expect_tx(&bars.v_full[st], bytes);
-            for (int i = 0; i < nbox; ++i)
-              tma_load_4d(sV + st * C::KV_BYTES + i * rows * C::ROWB, tv, &bars.v_full[st], 0, hk,
-                          m.tm[i * rows / 32] >> 4, it.s);
-            v_issued = kt + 1;
-          }
-        }
-      }
+      if (lane == 0) ok = put_meta(bars, meta, mt, m, abort_flag);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       ++mt;
-      if (m.kind == kKindTile) ++kt;
       if (!ok || m.kind == kKindEnd) break;
     }
-    __syncwarp();   // the next tile's union may overwrite the list
+    __syncwarp();   // the next item's union may overwrite the list
   }
-  // Drain this pipeline's own copies in flight before the CTA may exit.
-  if (lane == 0) {
-    for (int i = max(0, q_last - C::QB + 1); i <= q_last; ++i) drain_bar(&bars.q_full[i % C::QB], (i / C::QB) & 1);
-    for (int t = max(0, k_issued - C::STAGES); t < k_issued; ++t)
-      drain_bar(&bars.k_full[t % C::STAGES], (t / C::STAGES) & 1);
-    for (int t = max(0, v_issued - C::STAGES); t < v_issued; ++t)
-      drain_bar(&bars.v_full[t % C::STAGES], (t / C::STAGES) & 1);
+}
+
+// ------------------------------------------------------------------ loader (warps 8, 11, lane 0)
+
+// Reads the meta ring and issues the TMA loads: Q at each item header (Q_BYTES into buffer
+// item % QB), K of each key tile, and V one key tile later (the V of an item's last tile at
+// the item's end). Copies still in flight are drained before return.
+template <int D>
+__device__ void loader(const Params& p, const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
+                       PipeBars& bars, Meta* meta, uint8_t* sQ, uint8_t* sK, uint8_t* sV, volatile int* abort_flag) {
+  using C = Cfg<D>;
+  const int rows = p.block == 32 ? 32 : 64;          // rows per TMA box
+  int mt = 0, kt = 0, item_local = -1;
+  int k_issued = 0, v_issued = 0, q_last = -1;       // loads issued (drained at the end)
+  int cur_s = 0, cur_hk = 0;
+  bool ok = true;
+  bool v_pending = false;                            // the V of tile `pend` is not yet issued
+  TileLoad pend;
+  pend.t = 0;
+  for (;;) {
+    const int ms = mt % kMetaRing;
+    if (!(ok = wait_bar(&bars.m_full[ms], (mt / kMetaRing) & 1, abort_flag))) break;
+    const MetaRegs m = load_meta(&meta[ms]);
+    mbar_arrive(&bars.m_empty[ms]);
+    ++mt;
+    if (m.kind == kKindDone) break;
+    if (m.kind == kKindItem) {
+      ++item_local;
+      const Item it = decode_item(p, m.tm[0]);
+      cur_s = it.s;
+      cur_hk = it.h / p.heads_per_kv;
+      const int qb = item_local % C::QB;
+      if (item_local >= C::QB && !(ok = wait_bar(&bars.q_empty[qb], ((item_local / C::QB) - 1) & 1, abort_flag)))
+        break;
+      // rows beyond the sequence are zero-filled by TMA
+      mbar_arrive_expect_tx(&bars.q_full[qb], C::Q_BYTES);
+      tma_load_4d(sQ + qb * C::Q_BYTES, tq, &bars.q_full[qb], 0, it.h, it.tile * kTile, it.s);
+      q_last = item_local;
+    } else if (m.kind == kKindTile) {
+      TileLoad L;
+      L.t = kt;
+      L.rows = rows;
+      L.nbox = (m.nch * 32 + rows - 1) / rows;
+      L.s = cur_s;
+      L.hk = cur_hk;
+      L.bytes = (uint32_t)(m.nch * 32 * D * 2);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) L.tok[i] = m.tm[min(3, i * rows / 32)] >> 4;
+      if (!(ok = load_tile<C::KS, C::ROWB>(L, tk, sK, C::KV_BYTES, bars.k_full, bars.k_empty, abort_flag))) break;
+      k_issued = ++kt;
+      if (v_pending) {
+        if (!(ok = load_tile<C::VS, C::ROWB>(pend, tv, sV, C::KV_BYTES, bars.v_full, bars.v_empty, abort_flag))) break;
+        v_issued = pend.t + 1;
+      }
+      pend = L;
+      v_pending = true;
+    } else if (v_pending) {
+      // end of the item: its last V cannot wait for the next item's first K
+      if (!(ok = load_tile<C::VS, C::ROWB>(pend, tv, sV, C::KV_BYTES, bars.v_full, bars.v_empty, abort_flag))) break;
+      v_issued = pend.t + 1;
+      v_pending = false;
+    }
   }
-  __syncwarp();
+  // Drain this pipeline's copies in flight before the CTA may exit.
+  for (int i = max(0, q_last - C::QB + 1); i <= q_last; ++i) drain_bar(&bars.q_full[i % C::QB], (i / C::QB) & 1);
+  for (int t = max(0, k_issued - C::KS); t < k_issued; ++t) drain_bar(&bars.k_full[t % C::KS], (t / C::KS) & 1);
+  for (int t = max(0, v_issued - C::VS); t < v_issued; ++t) drain_bar(&bars.v_full[t % C::VS], (t / C::VS) & 1);
 }
 
 // ------------------------------------------------------------------ MMA issuer (warps 9, 10, lane 0)
@@ -336,7 +387,7 @@ __device__ __forceinline__ bool issue_pv(PipeBars& bars, uint32_t tP, uint32_t t
                                          int vkt, int nkeys, bool& o_init, volatile int* abort_flag) {
   using C = Cfg<D>;
   if (!wait_bar(&bars.p_full, (uint32_t)j & 1u, abort_flag)) return false;
-  if (!wait_bar(&bars.v_full[stage], (uint32_t)(vkt / C::STAGES) & 1u, abort_flag)) return false;
+  if (!wait_bar(&bars.v_full[stage], (uint32_t)(vkt / C::VS) & 1u, abort_flag)) return false;
   tc_fence_after();
   constexpr uint32_t idesc = make_idesc_bf16(128, D, 0, 1);
   const uint64_t b0 = vdesc0 + (uint64_t)((stage * C::KV_BYTES) >> 4);
@@ -382,9 +433,9 @@ __device__ void mma_issuer(int x, PipeBars& bars, Meta* meta, uint8_t* sQ, uint8
       mbar_arrive(&bars.m_empty[ms]);
       ++mt;
       if (m.kind != kKindTile) break;
-      const int stage = kt % C::STAGES;
+      const int stage = kt % C::KS;
       const int nkeys = m.nch * 32;
-      if (!(ok = wait_bar(&bars.k_full[stage], (uint32_t)(kt / C::STAGES) & 1u, abort_flag))) break;
+      if (!(ok = wait_bar(&bars.k_full[stage], (uint32_t)(kt / C::KS) & 1u, abort_flag))) break;
       // S is free once the softmax has loaded S_{g-1}
       if (g > 0 && !(ok = wait_bar(&bars.s_free, (uint32_t)(g - 1) & 1u, abort_flag))) break;
       tc_fence_after();
@@ -398,7 +449,7 @@ __device__ void mma_issuer(int x, PipeBars& bars, Meta* meta, uint8_t* sQ, uint8
       if (pend && !(ok = issue_pv<D>(bars, tP, tO, vdesc0, g - 1, p_stage, p_vkt, p_nkeys, o_init, abort_flag)))
         break;
       pend = true;
-      p_stage = stage;
+      p_stage = kt % C::VS;
       p_vkt = kt;
       p_nkeys = nkeys;
       ++kt;
@@ -669,7 +720,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&b.q_full[i], 1);
         mbar_init(&b.q_empty[i], 1);
       }
-      for (int i = 0; i < C::STAGES; ++i) {
+      for (int i = 0; i < kMaxStages; ++i) {
         mbar_init(&b.k_full[i], 1);
         mbar_init(&b.k_empty[i], 1);
         mbar_init(&b.v_full[i], 1);
@@ -701,20 +752,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
-  // pipeline 0: softmax warps 0-3, producer 8, MMA 9; pipeline 1: softmax 4-7, MMA 10, producer 11
-  const int x = warp < 8 ? (warp >> 2) : (warp == 8 || warp == 9 ? 0 : 1);
+  // Register split: warpgroups 0-1 (softmax) grow, warpgroups 2-3 (control) shrink, at the
+  // top of their branches (the compiler budgets the code that follows by it); the sum equals
+  // the launch allocation (checked on the host), so the growth always completes.
+  static_assert(kSoftmaxRegs == 184 && kCtrlRegs == 72, "register split literals");
+
+  // pipeline 0: softmax warps 0-3, loader 8, MMA 9, planner 12;
+  // pipeline 1: softmax warps 4-7, MMA 10, loader 11, planner 13; warps 14, 15 idle
+  const int x = warp < 8 ? (warp >> 2) : ((warp == 8 || warp == 9 || warp == 12) ? 0 : 1);
   uint8_t* sQ = sbase + x * C::PIPE_BYTES;
   uint8_t* sK = sQ + C::QB * C::Q_BYTES;
-  uint8_t* sV = sK + C::STAGES * C::KV_BYTES;
-  UnionSmem& un = *reinterpret_cast<UnionSmem*>(sV + C::STAGES * C::KV_BYTES);
+  uint8_t* sV = sK + C::KS * C::KV_BYTES;
+  UnionSmem& un = *reinterpret_cast<UnionSmem*>(sV + C::VS * C::KV_BYTES);
 
   if (warp < 8) {
+    // warpgroups 0 and 1: one setmaxnreg instruction for both
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 184;" ::: "memory");
     softmax_epilogue<D>(p, x, bars[x], meta[x], tmem, &abort_flag);
-  } else if (warp == 8 || warp == 11) {
-    producer<D>(p, &tq, &tk, &tv, bars[x], meta[x], un, sQ, sK, sV, &abort_flag);
   } else {
-    if ((threadIdx.x & 31) == 0) mma_issuer<D>(x, bars[x], meta[x], sQ, sK, sV, tmem, &abort_flag);
-    __syncwarp();
+    // warpgroups 2 and 3: one setmaxnreg instruction for both, then the roles
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;" ::: "memory");
+    if (warp == 8 || warp == 11) {
+      if ((threadIdx.x & 31) == 0) loader<D>(p, &tq, &tk, &tv, bars[x], meta[x], sQ, sK, sV, &abort_flag);
+      __syncwarp();
+    } else if (warp == 9 || warp == 10) {
+      if ((threadIdx.x & 31) == 0) mma_issuer<D>(x, bars[x], meta[x], sQ, sK, sV, tmem, &abort_flag);
+      __syncwarp();
+    } else if (warp == 12 || warp == 13) {
+      planner<D>(p, bars[x], meta[x], un, &abort_flag);
+    }
   }
 
   tc_fence_before();
@@ -768,6 +834,11 @@ int launch_d(const AttnArgs& a, cudaStream_t stream) {
   if (cudaMemsetAsync(p.work_counter, 0, sizeof(unsigned int), stream) != cudaSuccess) return SA_ERR_CUDA;
   const int sm_count = current_sm_count();
   auto kern = attn_fwd_wide_kernel<D>;
+  // The register split in the kernel hands out exactly the launch allocation: refuse to
+  // launch a build whose per-thread register count differs from it.
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return SA_ERR_CUDA;
+  if (fa.numRegs != kLaunchRegs) return SA_ERR_UNSUPPORTED;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return SA_ERR_CUDA;
   const int want = (p.n_items + 1) / 2;
