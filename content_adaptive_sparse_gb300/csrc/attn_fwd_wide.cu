@@ -59,7 +59,7 @@ __device__ unsigned int g_wide_counters[kWorkSlots];
 constexpr int kTile = 128;            // query rows per work item
 constexpr int kKeys = 128;            // keys per S tile (four 32-key chunks)
 constexpr int kThreads = 512;         // 16 warps, four warpgroups
-constexpr int kMetaRing = 32;
+constexpr int kMetaRing = 8;          // batch entries (up to 64 key tiles)
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSoftmaxWarps = 4;      // per pipeline: one per TMEM lane quarter
 constexpr int kMetaConsumers = 2 + kSoftmaxWarps;   // MMA thread, loader, softmax warps
@@ -96,16 +96,21 @@ struct Cfg {
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
-// Meta kinds: a key tile of the current item, the end of the item, the header of the next
-// item (tm[0] = item index), no more items.
-enum : int { kKindTile = 0, kKindEnd = 1, kKindItem = 2, kKindDone = 3 };
+// The planner hands work to the other roles through a ring of batches: each entry carries up
+// to kBatch key tiles of one item, so every consumer pays one barrier round trip per batch,
+// not per tile. An item is one or more consecutive entries (the first and last flagged; an
+// item without key tiles is one entry with no tiles); a Done entry ends the launch.
+constexpr int kBatch = 8;
+enum : int { kKindItem = 0, kKindDone = 1 };
+enum : int { kFirst = 1, kLast = 2 };
 
-// One ring entry, read by the consumers as two 16-byte loads.
-struct __align__(16) Meta {
+struct __align__(16) Batch {
   int kind;
-  int nch;                    // 32-key chunks (1 .. 4) in this key tile
-  int pad[2];
-  int tm[4];                  // chunk c: first key token << 4 | membership bits (bit r: query block r)
+  int ntiles;                 // key tiles in this entry (0 .. kBatch)
+  int item;                   // work item index
+  int flags;                  // kFirst | kLast
+  int4 tile[kBatch];          // per key tile and 32-key chunk c (x, y, z, w): first key token
+                              // << 4 | membership bits (bit r: query block r); 0 = no chunk
 };
 
 __device__ __forceinline__ int4 ld_shared_v4(const void* ptr) {
@@ -117,22 +122,15 @@ __device__ __forceinline__ int4 ld_shared_v4(const void* ptr) {
   return r;
 }
 
-struct MetaRegs {
-  int kind, nch;
+struct TileDesc {
+  int nch;                    // 32-key chunks (1 .. 4)
   int tm[4];
 };
 
-__device__ __forceinline__ MetaRegs load_meta(const Meta* src) {
-  const int4 a = ld_shared_v4(src);
-  const int4 b = ld_shared_v4(reinterpret_cast<const uint8_t*>(src) + 16);
-  MetaRegs m;
-  m.kind = a.x;
-  m.nch = a.y;
-  m.tm[0] = b.x;
-  m.tm[1] = b.y;
-  m.tm[2] = b.z;
-  m.tm[3] = b.w;
-  return m;
+// Chunks present in a key tile (they fill positions 0 .. n-1; a present chunk always has at
+// least one membership bit, so its entry is nonzero).
+__device__ __forceinline__ int tile_chunks(const int4& t) {
+  return (t.x != 0) + (t.y != 0) + (t.z != 0) + (t.w != 0);
 }
 
 struct Params {
@@ -153,7 +151,7 @@ struct Params {
 struct PipeBars {
   uint64_t q_full[2], q_empty[2];
   uint64_t k_full[kMaxStages], k_empty[kMaxStages], v_full[kMaxStages], v_empty[kMaxStages];
-  uint64_t m_full[kMetaRing], m_empty[kMetaRing];
+  uint64_t m_full[kMetaRing], m_empty[kMetaRing];     // batch ring
   uint64_t s_full;            // QK_j complete (phase j)
   uint64_t s_free;            // the softmax has loaded S_j (phase j)
   uint64_t p_full;            // the softmax has stored P_j (phase j)
@@ -215,12 +213,13 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return d;
 }
 
-// Publishes one meta entry (lane 0 of the planner warp); returns false on abort.
-__device__ __forceinline__ bool put_meta(PipeBars& bars, Meta* meta, int mt, const Meta& m, volatile int* abort_flag) {
+// Waits (one thread) until ring entry mt is published and returns its header (kind, ntiles,
+// item, flags); false on abort.
+__device__ __forceinline__ bool wait_batch(PipeBars& bars, const Batch* ring, int mt, int4& hdr,
+                                           volatile int* abort_flag) {
   const int ms = mt % kMetaRing;
-  if (!wait_bar(&bars.m_empty[ms], ((mt / kMetaRing) & 1) ^ 1, abort_flag)) return false;
-  meta[ms] = m;
-  mbar_arrive(&bars.m_full[ms]);
+  if (!wait_bar(&bars.m_full[ms], (uint32_t)(mt / kMetaRing) & 1u, abort_flag)) return false;
+  hdr = ld_shared_v4(&ring[ms]);
   return true;
 }
 
@@ -252,11 +251,10 @@ __device__ __forceinline__ bool load_tile(const TileLoad& L, const CUtensorMap* 
 // ------------------------------------------------------------------ planner (warps 12, 13)
 
 // Claims work items from the launch-wide counter, builds each item's key-block union and
-// publishes the item (header, key tiles, end) into the meta ring. The ring holds more than
-// an item, so the union of the next item is built while the consumers still work on the
-// current one.
+// publishes the item's key tiles in batches. The ring holds several items' worth of tiles,
+// so the next item's union is built while the consumers still work on the current one.
 template <int D>
-__device__ void planner(const Params& p, PipeBars& bars, Meta* meta, UnionSmem& u, volatile int* abort_flag) {
+__device__ void planner(const Params& p, PipeBars& bars, Batch* ring, UnionSmem& u, volatile int* abort_flag) {
   const int lane = threadIdx.x & 31;
   const int b = p.block;
   const int cpb = b >> 5;                            // 32-key chunks per key block
@@ -278,66 +276,66 @@ __device__ void planner(const Params& p, PipeBars& bars, Meta* meta, UnionSmem& 
       n_chunks = cpb * build_union(p.nb, p.causal ? kKeepLE : kKeepAll, u, rp, p.col_idx[mi], I0, nq, &g_wide_err,
                                    kErrBadIndex);
     }
-    {
-      Meta hm;
-      hm.kind = done ? kKindDone : kKindItem;
-      hm.nch = 0;
-      hm.pad[0] = hm.pad[1] = 0;
-      hm.tm[0] = k;
-      hm.tm[1] = hm.tm[2] = hm.tm[3] = 0;
-      if (lane == 0) ok = put_meta(bars, meta, mt, hm, abort_flag);
+    const int n_tiles = (n_chunks + 3) >> 2;
+    for (int t0 = 0;; t0 += kBatch) {
+      const int ms = mt % kMetaRing;
+      if (lane == 0) ok = wait_bar(&bars.m_empty[ms], ((mt / kMetaRing) & 1) ^ 1, abort_flag);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      ++mt;
-      if (!ok || done) break;
-    }
-    for (int c0 = 0;; c0 += 4) {
-      Meta m;
-      m.kind = c0 < n_chunks ? kKindTile : kKindEnd;
-      m.nch = min(4, n_chunks - c0);
-      m.pad[0] = m.pad[1] = 0;
+      if (!ok) break;
+      const int nt = done ? 0 : min(kBatch, n_tiles - t0);
+      // lane i < nt describes key tile t0 + i
+      if (lane < nt) {
+        int tm[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int q = c0 + i;
-        const uint32_t e = (i < m.nch) ? u.list[q / cpb] : 0u;
-        const int tok = (int)(e & 0xfffu) * b + (q % cpb) * 32;
-        m.tm[i] = (i < m.nch) ? ((tok << 4) | (int)(e >> 12)) : 0;
+        for (int c = 0; c < 4; ++c) {
+          const int q = 4 * (t0 + lane) + c;         // chunk index within the item
+          const uint32_t e = q < n_chunks ? u.list[q / cpb] : 0u;
+          tm[c] = q < n_chunks ? ((((int)(e & 0xfffu) * b + (q % cpb) * 32) << 4) | (int)(e >> 12)) : 0;
+        }
+        ring[ms].tile[lane] = make_int4(tm[0], tm[1], tm[2], tm[3]);
       }
-      if (lane == 0) ok = put_meta(bars, meta, mt, m, abort_flag);
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (lane == 0)
+        *reinterpret_cast<int4*>(&ring[ms]) = make_int4(done ? kKindDone : kKindItem, nt, k,
+                                                        (t0 == 0 ? kFirst : 0) | (t0 + kBatch >= n_tiles ? kLast : 0));
+      __syncwarp();                                  // every lane's entry is written before the release
+      if (lane == 0) mbar_arrive(&bars.m_full[ms]);
       ++mt;
-      if (!ok || m.kind == kKindEnd) break;
+      if (done || t0 + kBatch >= n_tiles) break;
     }
+    if (!ok || done) break;
     __syncwarp();   // the next item's union may overwrite the list
   }
 }
 
 // ------------------------------------------------------------------ loader (warps 8, 11, lane 0)
 
-// Reads the meta ring and issues the TMA loads: Q at each item header (Q_BYTES into buffer
+// Reads the batch ring and issues the TMA loads: Q at each item's start (Q_BYTES into buffer
 // item % QB), K of each key tile, and V one key tile later (the V of an item's last tile at
 // the item's end). Copies still in flight are drained before return.
 template <int D>
 __device__ void loader(const Params& p, const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
-                       PipeBars& bars, Meta* meta, uint8_t* sQ, uint8_t* sK, uint8_t* sV, volatile int* abort_flag) {
+                       PipeBars& bars, const Batch* ring, uint8_t* sQ, uint8_t* sK, uint8_t* sV,
+                       volatile int* abort_flag) {
   using C = Cfg<D>;
   const int rows = p.block == 32 ? 32 : 64;          // rows per TMA box
-  int mt = 0, kt = 0, item_local = -1;
+  int kt = 0, item_local = -1;
   int k_issued = 0, v_issued = 0, q_last = -1;       // loads issued (drained at the end)
   int cur_s = 0, cur_hk = 0;
   bool ok = true;
   bool v_pending = false;                            // the V of tile `pend` is not yet issued
   TileLoad pend;
   pend.t = 0;
-  for (;;) {
-    const int ms = mt % kMetaRing;
-    if (!(ok = wait_bar(&bars.m_full[ms], (mt / kMetaRing) & 1, abort_flag))) break;
-    const MetaRegs m = load_meta(&meta[ms]);
-    mbar_arrive(&bars.m_empty[ms]);
-    ++mt;
-    if (m.kind == kKindDone) break;
-    if (m.kind == kKindItem) {
+  for (int mt = 0;; ++mt) {
+    int4 hdr;
+    if (!(ok = wait_batch(bars, ring, mt, hdr, abort_flag))) break;
+    const Batch& e = ring[mt % kMetaRing];
+    if (hdr.x == kKindDone) {
+      mbar_arrive(&bars.m_empty[mt % kMetaRing]);
+      break;
+    }
+    if (hdr.w & kFirst) {
       ++item_local;
-      const Item it = decode_item(p, m.tm[0]);
+      const Item it = decode_item(p, hdr.z);
       cur_s = it.s;
       cur_hk = it.h / p.heads_per_kv;
       const int qb = item_local % C::QB;
@@ -347,16 +345,21 @@ __device__ void loader(const Params& p, const CUtensorMap* tq, const CUtensorMap
       mbar_arrive_expect_tx(&bars.q_full[qb], C::Q_BYTES);
       tma_load_4d(sQ + qb * C::Q_BYTES, tq, &bars.q_full[qb], 0, it.h, it.tile * kTile, it.s);
       q_last = item_local;
-    } else if (m.kind == kKindTile) {
+    }
+    for (int i = 0; i < hdr.y && ok; ++i) {
+      const int4 tm = ld_shared_v4(&e.tile[i]);
+      const int nch = tile_chunks(tm);
       TileLoad L;
       L.t = kt;
       L.rows = rows;
-      L.nbox = (m.nch * 32 + rows - 1) / rows;
+      L.nbox = (nch * 32 + rows - 1) / rows;
       L.s = cur_s;
       L.hk = cur_hk;
-      L.bytes = (uint32_t)(m.nch * 32 * D * 2);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) L.tok[i] = m.tm[min(3, i * rows / 32)] >> 4;
+      L.bytes = (uint32_t)(nch * 32 * D * 2);
+      L.tok[0] = tm.x >> 4;
+      L.tok[1] = (rows == 32 ? tm.y : tm.z) >> 4;
+      L.tok[2] = tm.z >> 4;
+      L.tok[3] = tm.w >> 4;
       if (!(ok = load_tile<C::KS, C::ROWB>(L, tk, sK, C::KV_BYTES, bars.k_full, bars.k_empty, abort_flag))) break;
       k_issued = ++kt;
       if (v_pending) {
@@ -365,7 +368,10 @@ __device__ void loader(const Params& p, const CUtensorMap* tq, const CUtensorMap
       }
       pend = L;
       v_pending = true;
-    } else if (v_pending) {
+    }
+    if (!ok) break;
+    mbar_arrive(&bars.m_empty[mt % kMetaRing]);
+    if ((hdr.w & kLast) && v_pending) {
       // end of the item: its last V cannot wait for the next item's first K
       if (!(ok = load_tile<C::VS, C::ROWB>(pend, tv, sV, C::KV_BYTES, bars.v_full, bars.v_empty, abort_flag))) break;
       v_issued = pend.t + 1;
@@ -400,42 +406,41 @@ __device__ __forceinline__ bool issue_pv(PipeBars& bars, uint32_t tP, uint32_t t
 }
 
 template <int D>
-__device__ void mma_issuer(int x, PipeBars& bars, Meta* meta, uint8_t* sQ, uint8_t* sK, uint8_t* sV, uint32_t tmem,
-                           volatile int* abort_flag) {
+__device__ void mma_issuer(int x, PipeBars& bars, const Batch* ring, uint8_t* sQ, uint8_t* sK, uint8_t* sV,
+                           uint32_t tmem, volatile int* abort_flag) {
   using C = Cfg<D>;
   const uint64_t qdesc = make_smem_desc(smem_u32(sQ), 16, C::ATOM, C::SWZ);
   const uint64_t kdesc0 = make_smem_desc(smem_u32(sK), 16, C::ATOM, C::SWZ);
   const uint64_t vdesc0 = make_smem_desc(smem_u32(sV), C::KV_BYTES, C::ATOM, C::SWZ);
   const uint32_t tS = tmem + C::col_s(x), tP = tmem + C::col_p(x), tO = tmem + C::col_o(x);
-  int mt = 0;               // metas read
-  int kt = 0;               // key tiles read (K/V ring position)
-  int g = 0;                // key tiles of this pipeline whose QK is issued
+  int g = 0;                // key tiles of this pipeline whose QK is issued (K / V ring position)
+  int item_local = -1;
+  int qb = 0;
+  uint64_t a0 = qdesc;
   bool ok = true;
-  for (int item_local = 0; ok; ++item_local) {
-    {
-      const int ms = mt & (kMetaRing - 1);
-      if (!(ok = wait_bar(&bars.m_full[ms], (uint32_t)(mt / kMetaRing) & 1u, abort_flag))) break;
-      const MetaRegs hm = load_meta(&meta[ms]);
-      mbar_arrive(&bars.m_empty[ms]);
-      ++mt;
-      if (hm.kind == kKindDone) break;
+  bool o_init = false;
+  bool pend = false;        // PV of the previous key tile of this item not yet issued
+  int p_nkeys = 0;
+  for (int mt = 0;; ++mt) {
+    int4 hdr;
+    if (!(ok = wait_batch(bars, ring, mt, hdr, abort_flag))) break;
+    const Batch& e = ring[mt % kMetaRing];
+    if (hdr.x == kKindDone) {
+      mbar_arrive(&bars.m_empty[mt % kMetaRing]);
+      break;
     }
-    const int qb = item_local % C::QB;
-    if (!(ok = wait_bar(&bars.q_full[qb], (item_local / C::QB) & 1, abort_flag))) break;
-    const uint64_t a0 = qdesc + (uint64_t)((qb * C::Q_BYTES) >> 4);
-    bool o_init = false;
-    bool pend = false;        // PV of the previous key tile of this item not yet issued
-    int p_stage = 0, p_vkt = 0, p_nkeys = 0;
-    for (;;) {
-      const int ms = mt & (kMetaRing - 1);
-      if (!(ok = wait_bar(&bars.m_full[ms], (uint32_t)(mt / kMetaRing) & 1u, abort_flag))) break;
-      const MetaRegs m = load_meta(&meta[ms]);
-      mbar_arrive(&bars.m_empty[ms]);
-      ++mt;
-      if (m.kind != kKindTile) break;
-      const int stage = kt % C::KS;
-      const int nkeys = m.nch * 32;
-      if (!(ok = wait_bar(&bars.k_full[stage], (uint32_t)(kt / C::KS) & 1u, abort_flag))) break;
+    if (hdr.w & kFirst) {
+      ++item_local;
+      qb = item_local % C::QB;
+      if (!(ok = wait_bar(&bars.q_full[qb], (item_local / C::QB) & 1, abort_flag))) break;
+      a0 = qdesc + (uint64_t)((qb * C::Q_BYTES) >> 4);
+      o_init = false;
+      pend = false;
+    }
+    for (int i = 0; i < hdr.y; ++i) {
+      const int nkeys = 32 * tile_chunks(ld_shared_v4(&e.tile[i]));
+      const int stage = g % C::KS;
+      if (!(ok = wait_bar(&bars.k_full[stage], (uint32_t)(g / C::KS) & 1u, abort_flag))) break;
       // S is free once the softmax has loaded S_{g-1}
       if (g > 0 && !(ok = wait_bar(&bars.s_free, (uint32_t)(g - 1) & 1u, abort_flag))) break;
       tc_fence_after();
@@ -446,19 +451,23 @@ __device__ void mma_issuer(int x, PipeBars& bars, Meta* meta, uint8_t* sQ, uint8
         mma_bf16_ss(tS, a0 + (uint64_t)((ks * 32) >> 4), b0 + (uint64_t)((ks * 32) >> 4), idesc, ks > 0 ? 1u : 0u);
       mma_commit(&bars.s_full);
       mma_commit(&bars.k_empty[stage]);
-      if (pend && !(ok = issue_pv<D>(bars, tP, tO, vdesc0, g - 1, p_stage, p_vkt, p_nkeys, o_init, abort_flag)))
+      if (pend && !(ok = issue_pv<D>(bars, tP, tO, vdesc0, g - 1, (g - 1) % C::VS, g - 1, p_nkeys, o_init,
+                                     abort_flag)))
         break;
       pend = true;
-      p_stage = kt % C::VS;
-      p_vkt = kt;
       p_nkeys = nkeys;
-      ++kt;
       ++g;
     }
     if (!ok) break;
-    // the item's last PV: its completion releases the softmax epilogue
-    if (pend && !(ok = issue_pv<D>(bars, tP, tO, vdesc0, g - 1, p_stage, p_vkt, p_nkeys, o_init, abort_flag))) break;
-    mma_commit(&bars.q_empty[qb]);   // all QKs of this item issued; arrives when they are done
+    mbar_arrive(&bars.m_empty[mt % kMetaRing]);
+    if (hdr.w & kLast) {
+      mma_commit(&bars.q_empty[qb]);   // all QKs of this item issued; arrives when they are done
+      // the item's last PV: its completion releases the softmax epilogue
+      if (pend && !(ok = issue_pv<D>(bars, tP, tO, vdesc0, g - 1, (g - 1) % C::VS, g - 1, p_nkeys, o_init,
+                                     abort_flag)))
+        break;
+      pend = false;
+    }
   }
   // Make sure no MMA of this thread is still writing TMEM when the CTA frees it.
   mma_commit(&bars.drain);
@@ -521,7 +530,7 @@ __device__ __forceinline__ void rescale_o(uint32_t tO, float alpha) {
 // Softmax and epilogue of pipeline x; this warp handles query rows 32q .. 32q+31 of every
 // item (q = its TMEM lane quarter) and all 128 keys of every key tile.
 template <int D>
-__device__ void softmax_epilogue(const Params& p, int x, PipeBars& bars, Meta* meta, uint32_t tmem,
+__device__ void softmax_epilogue(const Params& p, int x, PipeBars& bars, const Batch* ring, uint32_t tmem,
                                  volatile int* abort_flag) {
   using C = Cfg<D>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -536,34 +545,42 @@ __device__ void softmax_epilogue(const Params& p, int x, PipeBars& bars, Meta* m
   const uint32_t tP = tmem + C::col_p(x) + lane_base;
   const uint32_t tO = tmem + C::col_o(x) + lane_base;
 
-  int mt = 0, g = 0;        // meta position, key tiles processed by this pipeline
+  int g = 0;                // key tiles processed by this pipeline
   bool ok = true;
-  for (;;) {
-    int k;
-    {
-      const int ms = mt % kMetaRing;
-      if (!(ok = wait_bar(&bars.m_full[ms], (mt / kMetaRing) & 1, abort_flag))) break;
-      const MetaRegs hm = load_meta(&meta[ms]);
+  Item it;
+  it.s = it.h = it.tile = 0;
+  int qtok = 0, q_warp = 0;
+  float m_use = kNegInf;    // running reference max, log2 units
+  float l = 0.f;            // row sum
+  int n_item = 0;           // key tiles of the current item
+  for (int mt = 0;; ++mt) {
+    int4 hdr;
+    ok = __all_sync(0xffffffffu, wait_batch(bars, ring, mt, hdr, abort_flag));
+    if (!ok) break;
+    const Batch& e = ring[mt % kMetaRing];
+    if (hdr.x == kKindDone) {
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.m_empty[ms]);
-      ++mt;
-      if (hm.kind == kKindDone) break;
-      k = hm.tm[0];
+      if (lane == 0) mbar_arrive(&bars.m_empty[mt % kMetaRing]);
+      break;
     }
-    const Item it = decode_item(p, k);
-    const int qtok = it.tile * kTile + row;
-    const int q_warp = it.tile * kTile + quarter * 32;
-    float m_use = kNegInf;   // running reference max, log2 units
-    float l = 0.f;           // row sum
-    int n_item = 0;
-    for (;;) {
-      const int ms = mt % kMetaRing;
-      if (!(ok = wait_bar(&bars.m_full[ms], (mt / kMetaRing) & 1, abort_flag))) break;
-      const MetaRegs m = load_meta(&meta[ms]);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.m_empty[ms]);
-      ++mt;
-      if (m.kind != kKindTile) break;
+    if (hdr.w & kFirst) {
+      it = decode_item(p, hdr.z);
+      qtok = it.tile * kTile + row;
+      q_warp = it.tile * kTile + quarter * 32;
+      m_use = kNegInf;
+      l = 0.f;
+      n_item = 0;
+    }
+    for (int i = 0; i < hdr.y; ++i) {
+      TileDesc m;
+      {
+        const int4 t4 = ld_shared_v4(&e.tile[i]);
+        m.tm[0] = t4.x;
+        m.tm[1] = t4.y;
+        m.tm[2] = t4.z;
+        m.tm[3] = t4.w;
+        m.nch = tile_chunks(t4);
+      }
 
       // Visibility of each 32-key chunk for this warp's 32 rows (warp-uniform): bit ch of
       // vis: some row sees some key of chunk ch. Query and key chunks start at multiples of
@@ -659,6 +676,9 @@ __device__ void softmax_epilogue(const Params& p, int x, PipeBars& bars, Meta* m
       ++n_item;
     }
     if (!ok) break;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars.m_empty[mt % kMetaRing]);
+    if (!(hdr.w & kLast)) continue;
 
     // epilogue: O / l and LSE of this query tile's rows
     if (n_item > 0) {
@@ -708,7 +728,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sbase = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ PipeBars bars[2];
-  __shared__ Meta meta[2][kMetaRing];
+  __shared__ Batch ring[2][kMetaRing];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -768,18 +788,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 8) {
     // warpgroups 0 and 1: one setmaxnreg instruction for both
     asm volatile("setmaxnreg.inc.sync.aligned.u32 184;" ::: "memory");
-    softmax_epilogue<D>(p, x, bars[x], meta[x], tmem, &abort_flag);
+    softmax_epilogue<D>(p, x, bars[x], ring[x], tmem, &abort_flag);
   } else {
     // warpgroups 2 and 3: one setmaxnreg instruction for both, then the roles
     asm volatile("setmaxnreg.dec.sync.aligned.u32 72;" ::: "memory");
     if (warp == 8 || warp == 11) {
-      if ((threadIdx.x & 31) == 0) loader<D>(p, &tq, &tk, &tv, bars[x], meta[x], sQ, sK, sV, &abort_flag);
+      if ((threadIdx.x & 31) == 0) loader<D>(p, &tq, &tk, &tv, bars[x], ring[x], sQ, sK, sV, &abort_flag);
       __syncwarp();
     } else if (warp == 9 || warp == 10) {
-      if ((threadIdx.x & 31) == 0) mma_issuer<D>(x, bars[x], meta[x], sQ, sK, sV, tmem, &abort_flag);
+      if ((threadIdx.x & 31) == 0) mma_issuer<D>(x, bars[x], ring[x], sQ, sK, sV, tmem, &abort_flag);
       __syncwarp();
     } else if (warp == 12 || warp == 13) {
-      planner<D>(p, bars[x], meta[x], un, &abort_flag);
+      planner<D>(p, bars[x], ring[x], un, &abort_flag);
     }
   }
 
