@@ -111,7 +111,38 @@ struct __align__(16) Batch {
   int flags;                  // kFirst | kLast
   int4 tile[kBatch];          // per key tile and 32-key chunk c (x, y, z, w): first key token
                               // << 4 | membership bits (bit r: query block r); 0 = no chunk
+  uint8_t nch[kBatch];        // per key tile: 32-key chunks (1 .. 4)
+  uint8_t vq[4][kBatch];      // per TMEM lane quarter and key tile: bits 0-3, chunk c visible
+                              // to some row of the quarter; bits 4-6, 1 + the causal-diagonal
+                              // chunk (0: none)
 };
+
+// Visibility byte of one key tile for the 32 query rows of lane quarter q (rows 32q ..
+// 32q+31 of the item's query tile, first query token q_warp; query block sub). Query and key
+// chunks start at multiples of 32, so under causality at most one chunk (the one starting at
+// q_warp) is the diagonal, where row r sees columns 0 .. r.
+__device__ __forceinline__ int quarter_vis(const int (&tm)[4], int nch, int sub, int q_warp, int causal) {
+  int vis = 0, dch = -1;
+#pragma unroll
+  for (int ch = 0; ch < 4; ++ch) {
+    if (ch < nch && ((tm[ch] >> sub) & 1)) {
+      const int lim0 = q_warp - (tm[ch] >> 4);     // row r sees columns c <= lim0 + r
+      if (!causal || lim0 >= 31) {
+        vis |= 1 << ch;
+      } else if (lim0 + 31 >= 0) {
+        vis |= 1 << ch;
+        dch = ch;
+      }
+    }
+  }
+  return vis | ((dch + 1) << 4);
+}
+
+__device__ __forceinline__ uint2 ld_shared_v2(const void* ptr) {
+  uint2 r;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(smem_u32(ptr)) : "memory");
+  return r;
+}
 
 __device__ __forceinline__ int4 ld_shared_v4(const void* ptr) {
   int4 r;
@@ -121,11 +152,6 @@ __device__ __forceinline__ int4 ld_shared_v4(const void* ptr) {
                : "memory");
   return r;
 }
-
-struct TileDesc {
-  int nch;                    // 32-key chunks (1 .. 4)
-  int tm[4];
-};
 
 // Chunks present in a key tile (they fill positions 0 .. n-1; a present chunk always has at
 // least one membership bit, so its entry is nonzero).
@@ -293,6 +319,12 @@ __device__ void planner(const Params& p, PipeBars& bars, Batch* ring, UnionSmem&
           tm[c] = q < n_chunks ? ((((int)(e & 0xfffu) * b + (q % cpb) * 32) << 4) | (int)(e >> 12)) : 0;
         }
         ring[ms].tile[lane] = make_int4(tm[0], tm[1], tm[2], tm[3]);
+        const int nch = min(4, n_chunks - 4 * (t0 + lane));
+        ring[ms].nch[lane] = (uint8_t)nch;
+        const int tile0 = decode_item(p, k).tile * kTile;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          ring[ms].vq[q][lane] = (uint8_t)quarter_vis(tm, nch, (32 * q) >> p.log2b, tile0 + 32 * q, p.causal);
       }
       if (lane == 0)
         *reinterpret_cast<int4*>(&ring[ms]) = make_int4(done ? kKindDone : kKindItem, nt, k,
@@ -437,8 +469,9 @@ __device__ void mma_issuer(int x, PipeBars& bars, const Batch* ring, uint8_t* sQ
       o_init = false;
       pend = false;
     }
+    const uint2 ncw = ld_shared_v2(&e.nch[0]);
     for (int i = 0; i < hdr.y; ++i) {
-      const int nkeys = 32 * tile_chunks(ld_shared_v4(&e.tile[i]));
+      const int nkeys = 32 * (int)(((i < 4 ? ncw.x : ncw.y) >> (8 * (i & 3))) & 0xffu);
       const int stage = g % C::KS;
       if (!(ok = wait_bar(&bars.k_full[stage], (uint32_t)(g / C::KS) & 1u, abort_flag))) break;
       // S is free once the softmax has loaded S_{g-1}
@@ -537,7 +570,6 @@ __device__ void softmax_epilogue(const Params& p, int x, PipeBars& bars, const B
   const int quarter = warp & 3;
   const int row = quarter * 32 + lane;               // query row within the tile
   const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-  const int sub = (quarter * 32) >> p.log2b;         // query block within the tile (warp-uniform)
   const float kNegInf = __int_as_float(0xff800000);
   const float c = p.scale_log2;
   const uint64_t c2 = f2_pack(c, c);
@@ -549,7 +581,7 @@ __device__ void softmax_epilogue(const Params& p, int x, PipeBars& bars, const B
   bool ok = true;
   Item it;
   it.s = it.h = it.tile = 0;
-  int qtok = 0, q_warp = 0;
+  int qtok = 0;
   float m_use = kNegInf;    // running reference max, log2 units
   float l = 0.f;            // row sum
   int n_item = 0;           // key tiles of the current item
@@ -566,40 +598,18 @@ __device__ void softmax_epilogue(const Params& p, int x, PipeBars& bars, const B
     if (hdr.w & kFirst) {
       it = decode_item(p, hdr.z);
       qtok = it.tile * kTile + row;
-      q_warp = it.tile * kTile + quarter * 32;
       m_use = kNegInf;
       l = 0.f;
       n_item = 0;
     }
+    // this quarter's visibility bytes and the chunk counts of the batch's tiles
+    const uint2 vqw = ld_shared_v2(&e.vq[quarter][0]);
+    const uint2 ncw = ld_shared_v2(&e.nch[0]);
     for (int i = 0; i < hdr.y; ++i) {
-      TileDesc m;
-      {
-        const int4 t4 = ld_shared_v4(&e.tile[i]);
-        m.tm[0] = t4.x;
-        m.tm[1] = t4.y;
-        m.tm[2] = t4.z;
-        m.tm[3] = t4.w;
-        m.nch = tile_chunks(t4);
-      }
-
-      // Visibility of each 32-key chunk for this warp's 32 rows (warp-uniform): bit ch of
-      // vis: some row sees some key of chunk ch. Query and key chunks start at multiples of
-      // 32, so under causality at most one chunk (the one starting at this warp's first
-      // query) is the diagonal, where row r sees columns 0 .. r.
-      int vis = 0, dch = -1;
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        const int tm = m.tm[ch];
-        if (ch < m.nch && ((tm >> sub) & 1)) {
-          const int lim0 = q_warp - (tm >> 4);       // row r sees columns c <= lim0 + r
-          if (!p.causal || lim0 >= 31) {
-            vis |= 1 << ch;
-          } else if (lim0 + 31 >= 0) {
-            vis |= 1 << ch;
-            dch = ch;
-          }
-        }
-      }
+      const int sh = 8 * (i & 3);
+      const int vb = (int)(((i < 4 ? vqw.x : vqw.y) >> sh) & 0xffu);
+      const int nch = (int)(((i < 4 ? ncw.x : ncw.y) >> sh) & 0xffu);
+      const int vis = vb & 15, dch = (vb >> 4) - 1;
 
       ok = __all_sync(0xffffffffu, wait_bar(&bars.s_full, (uint32_t)g & 1u, abort_flag));
       if (!ok) break;
@@ -614,8 +624,8 @@ __device__ void softmax_epilogue(const Params& p, int x, PipeBars& bars, const B
       if (lane == 0) mbar_arrive(&bars.s_free);
 
       if (dch >= 0) {
-        const int lim = q_warp - (m.tm[dch] >> 4) + lane;
-        const uint32_t kp = lim >= 31 ? 0xffffffffu : (lim < 0 ? 0u : ((2u << lim) - 1u));
+        // the diagonal chunk starts at this warp's first query: row r sees columns 0 .. r
+        const uint32_t kp = (2u << lane) - 1u;       // lane 31: all 32 columns
         switch (dch) {
           case 0: mask_chunk(v, kp); break;
           case 1: mask_chunk(v + 32, kp); break;
@@ -659,7 +669,7 @@ __device__ void softmax_epilogue(const Params& p, int x, PipeBars& bars, const B
           }
           if (__any_sync(0xffffffffu, o_scale)) rescale_o<D>(tO, alpha);
         }
-        if (ch < m.nch) tmem_st_x16(tP + 16 * ch, pk);
+        if (ch < nch) tmem_st_x16(tP + 16 * ch, pk);
       }
       if (!ok) break;
       {
