@@ -1,4 +1,9 @@
-// Block-sparse flash-attention forward for sm_103a (tcgen05 + TMEM + TMA).
+// Block-sparse flash-attention forward for sm_103a (tcgen05 + TMEM + TMA), 64-key tiles.
+//
+// The library runs this kernel for head dimension 128. Head dimensions 32 and 64 go to
+// attn_fwd_wide.cu (128-key tiles, one full score row per softmax thread), which is faster
+// there; the template below still compiles for d = 32 and 64 (split accumulators at d = 32)
+// and is kept as the measured baseline of that design.
 //
 // Work item: one 128-row query tile of one (sequence, head), covering 128 / b query
 // blocks. The key blocks the tile visits are the sorted union of those blocks' CSR rows;

@@ -117,14 +117,17 @@ def test_empty_rows_and_strided_inputs():
     assert np.all(bf16_to_f64(o)[:, 32:64] == 0)
 
 
-@pytest.mark.parametrize("d,b", [(64, 64), (128, 128), (64, 32)])
-def test_running_max_rescale_paths(d, b):
+@pytest.mark.parametrize("steep", [6.0, 2.0])
+@pytest.mark.parametrize("d,b", [(64, 64), (128, 128), (64, 32), (32, 32)])
+def test_running_max_rescale_paths(d, b, steep):
     """Logits that grow along the sequence (and jump inside a key tile) force the
-    lazy running-max updates: in-tile P rescale, O rescale, and first-tile init."""
+    running-max updates: first-tile init, O rescale, and (steep = 2: the logits of each
+    128-key tile exceed the running max by far more than 2^32 / 128) a tile recomputed
+    against its exact max."""
     torch = torch_cuda()
     rng = np.random.default_rng(d + b)
     n, h = 768, 2
-    base = np.arange(n, dtype=np.float32)[None, :, None, None] / 6.0
+    base = np.arange(n, dtype=np.float32)[None, :, None, None] / np.float32(steep)
     sign = np.where(rng.random((1, n, h, 1)) < 0.5, -1.0, 1.0).astype(np.float32)
     qf = np.ones((1, n, h, d), np.float32) * 0.5 + 0.05 * rng.standard_normal((1, n, h, d), dtype=np.float32)
     kf = (base * (1.0 + 0.3 * sign)) * np.ones((1, n, h, d), np.float32) / np.float32(np.sqrt(d))
