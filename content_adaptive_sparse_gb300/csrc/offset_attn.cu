@@ -18,10 +18,11 @@
 // the keys (group 0 the first half of the band steps and the even offset slabs, group 1
 // the rest) and merge their partial softmax states through shared memory at the end.
 // K/V arrive by TMA: the band (rows [q0 - 64, q0 + 64)) once, the offset slabs (64 rows
-// each) through a ring of two buffers (one per group) that the last warp done with a
+// each) through a ring of four buffers (two per group) that the last warp done with a
 // buffer refills, so loads are issued from many warps (one issuing thread streams boxes
-// slowly). At 66.5 KB of shared memory three CTAs share an SM (a four-buffer ring allowed
-// two and was 1.5 % slower).
+// slowly). Buffers 2 and 3 reuse the band's memory once every warp is past the band, so at
+// 66.5 KB of shared memory three CTAs still share an SM (3 % faster than two buffers; four
+// buffers of their own allowed only two CTAs per SM and were 1.5 % slower than two).
 // Softmax: exact max over the band part, then the offsets with a lazily rescaled
 // running max (threshold 2^8).
 #include <cuda.h>
@@ -41,7 +42,8 @@ __device__ unsigned int g_offset_err;
 constexpr int kQ = 64;                   // queries per CTA
 constexpr int kGroupWarps = 4;           // 16 queries per warp: one group covers the tile
 constexpr int kWarps = 2 * kGroupWarps;  // two groups split the keys of the tile
-constexpr int kRing = 2;                 // offset slabs in flight per CTA (one per group)
+constexpr int kRing = 4;                 // offset slab buffers per CTA (two per group)
+constexpr int kRingMem = 2;              // of which own memory; buffers 2, 3 reuse the band's
 constexpr int kD = 64;                   // head dim supported by this kernel
 constexpr int kRowBytes = kD * 2;        // 128 B per K/V row
 constexpr int kBandMax = 64;             // deltas up to this go through the band
@@ -165,7 +167,9 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sKb = sm;                        // band K, 16 KB
   uint8_t* sVb = sKb + kBandBytes;          // band V, 16 KB
-  uint8_t* sRing = sVb + kBandBytes;        // kRing x (K slab, V slab), 32 KB; merge buffer at the end
+  uint8_t* sRing = sVb + kBandBytes;        // slab buffers 0, 1 (K slab, V slab), 32 KB; merge buffer at the end
+  // slab buffer b: 0, 1 in the ring memory, 2, 3 over the band (free once the band is done)
+  auto slab_buf = [&](int b) -> uint8_t* { return b < kRingMem ? sRing + b * 2 * kSlabBytes : sKb + (b - kRingMem) * kBandBytes; };
   __shared__ uint64_t bar_band, bar_slab[kRing];
   __shared__ int done_cnt[kRing];           // warps finished with the slab in each buffer
   __shared__ int n_issued;                  // slabs issued so far
@@ -190,18 +194,18 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
       done_cnt[b] = 0;
     }
     abort_flag = 0;
-    n_issued = n_off < kRing ? n_off : kRing;
+    n_issued = n_off < kRingMem ? n_off : kRingMem;
     fence_mbar_init();
     mbar_arrive_expect_tx(&bar_band, (uint32_t)(2 * kBandBytes));
   }
   __syncthreads();
   // A single thread streams TMA boxes at a limited rate, so several warps issue loads:
-  // warp w < kRing the first slab of buffer w, warps 4 and 5 the band.
+  // warp w < kRingMem the first slab of buffer w, warps 4 and 5 the band.
   if (lane == 0) {
     if (warp == 4) tma_load_4d(sKb, &tk_band, &bar_band, 0, hk, q0 - kBandMax, s);
     if (warp == 5) tma_load_4d(sVb, &tv_band, &bar_band, 0, hk, q0 - kBandMax, s);
-    if (warp < kRing && warp < n_off) {
-      uint8_t* dst = sRing + warp * 2 * kSlabBytes;
+    if (warp < kRingMem && warp < n_off) {
+      uint8_t* dst = slab_buf(warp);
       mbar_arrive_expect_tx(&bar_slab[warp], 2u * kSlabBytes);
       tma_load_4d(dst, &tk_slab, &bar_slab[warp], 0, hk, q0 - p.large[warp], s);
       tma_load_4d(dst + kSlabBytes, &tv_slab, &bar_slab[warp], 0, hk, q0 - p.large[warp], s);
@@ -306,6 +310,20 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
     l_hi = lsum[2];
   }
 
+  // The band is read: its memory becomes slab buffers 2 and 3 (slabs 2 and 3 of the tile),
+  // so each group has two slabs in flight while it works on one.
+  __syncthreads();
+  if (tid == 0 && !abort_flag) {
+    for (int k = kRingMem; k < kRing && k < n_off; ++k) {
+      uint8_t* dst = slab_buf(k);
+      mbar_arrive_expect_tx(&bar_slab[k], 2u * kSlabBytes);
+      tma_load_4d(dst, &tk_slab, &bar_slab[k], 0, hk, q0 - p.large[k], s);
+      tma_load_4d(dst + kSlabBytes, &tv_slab, &bar_slab[k], 0, hk, q0 - p.large[k], s);
+      n_issued = k + 1;
+    }
+  }
+  ok = ok && !abort_flag;
+
   // ---------------- larger offsets: group 0 takes slabs 0, 2, 4, ..., group 1 slabs 1, 3, ...
   // (buffers {0, 2} and {1, 3}); one diagonal 16 x 16 block per slab
   const int hl = (lane & ~3) | (g >> 1);     // lane of this quad that holds the diagonal
@@ -316,7 +334,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
     ok = __all_sync(0xffffffffu, mbar_wait(&bar_slab[buf], (uint32_t)(k / kRing) & 1u, &abort_flag,
                                            &g_offset_err, kErrTimeout));
     if (!ok) break;
-    const uint32_t kt = smem_u32(sRing + buf * 2 * kSlabBytes);
+    const uint32_t kt = smem_u32(slab_buf(buf));
     float s_lo, s_hi;
     diag_scores(kt, wq, g, t, hl, e_sel, qa, s_lo, s_hi);
     const int delta = p.large[k];
@@ -352,7 +370,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
         done_cnt[buf] = 0;
         const int nk = k + kRing;
         if (nk < n_off && !abort_flag) {
-          uint8_t* dst = sRing + buf * 2 * kSlabBytes;
+          uint8_t* dst = slab_buf(buf);
           mbar_arrive_expect_tx(&bar_slab[buf], 2u * kSlabBytes);
           tma_load_4d(dst, &tk_slab, &bar_slab[buf], 0, hk, q0 - p.large[nk], s);
           tma_load_4d(dst + kSlabBytes, &tv_slab, &bar_slab[buf], 0, hk, q0 - p.large[nk], s);
@@ -426,7 +444,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
 template <int NKT>
 int launch_nkt(const CUtensorMap& kb, const CUtensorMap& vb, const CUtensorMap& ks, const CUtensorMap& vs,
                const OffParams& p, int batch, cudaStream_t stream) {
-  const size_t smem = 1024 + 2 * (size_t)kBandBytes + 2 * kRing * (size_t)kSlabBytes;
+  const size_t smem = 1024 + 2 * (size_t)kBandBytes + 2 * kRingMem * (size_t)kSlabBytes;
   if (cudaFuncSetAttribute(offset_attn_kernel<NKT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return SA_ERR_CUDA;
