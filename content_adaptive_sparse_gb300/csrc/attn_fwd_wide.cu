@@ -59,7 +59,7 @@ __device__ unsigned int g_wide_counters[kWorkSlots];
 constexpr int kTile = 128;            // query rows per work item
 constexpr int kKeys = 128;            // keys per S tile (four 32-key chunks)
 constexpr int kThreads = 512;         // 16 warps, four warpgroups
-constexpr int kMetaRing = 8;          // batch entries (up to 64 key tiles)
+constexpr int kMetaRing = 8;          // batch entries (up to 128 key tiles)
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSoftmaxWarps = 4;      // per pipeline: one per TMEM lane quarter
 constexpr int kMetaConsumers = 2 + kSoftmaxWarps;   // MMA thread, loader, softmax warps
@@ -100,7 +100,7 @@ struct Cfg {
 // to kBatch key tiles of one item, so every consumer pays one barrier round trip per batch,
 // not per tile. An item is one or more consecutive entries (the first and last flagged; an
 // item without key tiles is one entry with no tiles); a Done entry ends the launch.
-constexpr int kBatch = 8;
+constexpr int kBatch = 16;
 enum : int { kKindItem = 0, kKindDone = 1 };
 enum : int { kFirst = 1, kLast = 2 };
 
@@ -111,7 +111,7 @@ struct __align__(16) Batch {
   int flags;                  // kFirst | kLast
   int4 tile[kBatch];          // per key tile and 32-key chunk c (x, y, z, w): first key token
                               // << 4 | membership bits (bit r: query block r); 0 = no chunk
-  uint8_t nch[kBatch];        // per key tile: 32-key chunks (1 .. 4)
+  uint8_t nch[kBatch];        // per key tile: 32-key chunks (1 .. 4); 16-byte aligned
   uint8_t vq[4][kBatch];      // per TMEM lane quarter and key tile: bits 0-3, chunk c visible
                               // to some row of the quarter; bits 4-6, 1 + the causal-diagonal
                               // chunk (0: none)
@@ -138,10 +138,18 @@ __device__ __forceinline__ int quarter_vis(const int (&tm)[4], int nch, int sub,
   return vis | ((dch + 1) << 4);
 }
 
-__device__ __forceinline__ uint2 ld_shared_v2(const void* ptr) {
-  uint2 r;
-  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(smem_u32(ptr)) : "memory");
+__device__ __forceinline__ uint4 ld_shared_u4(const void* ptr) {
+  uint4 r;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "r"(smem_u32(ptr))
+               : "memory");
   return r;
+}
+
+// Word w (0 .. 3) of a 16-byte value (selects, not an indexed read: stays in registers).
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int w) {
+  return w == 0 ? v.x : (w == 1 ? v.y : (w == 2 ? v.z : v.w));
 }
 
 __device__ __forceinline__ int4 ld_shared_v4(const void* ptr) {
@@ -469,9 +477,9 @@ __device__ void mma_issuer(int x, PipeBars& bars, const Batch* ring, uint8_t* sQ
       o_init = false;
       pend = false;
     }
-    const uint2 ncw = ld_shared_v2(&e.nch[0]);
+    const uint4 ncw = ld_shared_u4(&e.nch[0]);
     for (int i = 0; i < hdr.y; ++i) {
-      const int nkeys = 32 * (int)(((i < 4 ? ncw.x : ncw.y) >> (8 * (i & 3))) & 0xffu);
+      const int nkeys = 32 * (int)((word_of(ncw, i >> 2) >> (8 * (i & 3))) & 0xffu);
       const int stage = g % C::KS;
       if (!(ok = wait_bar(&bars.k_full[stage], (uint32_t)(g / C::KS) & 1u, abort_flag))) break;
       // S is free once the softmax has loaded S_{g-1}
@@ -603,12 +611,12 @@ __device__ void softmax_epilogue(const Params& p, int x, PipeBars& bars, const B
       n_item = 0;
     }
     // this quarter's visibility bytes and the chunk counts of the batch's tiles
-    const uint2 vqw = ld_shared_v2(&e.vq[quarter][0]);
-    const uint2 ncw = ld_shared_v2(&e.nch[0]);
+    const uint4 vqw = ld_shared_u4(&e.vq[quarter][0]);
+    const uint4 ncw = ld_shared_u4(&e.nch[0]);
     for (int i = 0; i < hdr.y; ++i) {
       const int sh = 8 * (i & 3);
-      const int vb = (int)(((i < 4 ? vqw.x : vqw.y) >> sh) & 0xffu);
-      const int nch = (int)(((i < 4 ? ncw.x : ncw.y) >> sh) & 0xffu);
+      const int vb = (int)((word_of(vqw, i >> 2) >> sh) & 0xffu);
+      const int nch = (int)((word_of(ncw, i >> 2) >> sh) & 0xffu);
       const int vis = vb & 15, dch = (vb >> 4) - 1;
 
       ok = __all_sync(0xffffffffu, wait_bar(&bars.s_full, (uint32_t)g & 1u, abort_flag));
