@@ -24,13 +24,17 @@
 //   warps 0-3   softmax of pipeline 0, warp w reads TMEM lane quarter w (query rows 32w ..)
 //   warps 4-7   softmax of pipeline 1
 //   warps 12, 13 planners of pipeline 0 / 1: claim items, build the key-block union, publish
-//               the item's key tiles into a 32-entry meta ring (an item or more ahead)
-//   warps 8, 11 lane 0 loads Q, K and V of pipeline 0 / 1 by TMA as the metas arrive
+//               the item's key tiles into a ring of batches (up to 16 tiles per entry, 128
+//               tiles in the ring: an item or more ahead)
+//   warps 8, 11 lane 0 loads Q, K and V of pipeline 0 / 1 by TMA as the batches arrive
+//   warps 14, 15 idle (the fourth warpgroup's remainder)
 //   warps 9, 10 lane 0 issues the tcgen05 MMAs of pipeline 0 / 1:
 //                 S = Q K_j^T   (N = keys of the tile, up to 128)
 //                 O += P_j V_j  (A = P_j from TMEM, B = V_j MN-major; K = 16 keys per MMA)
 //               in the order QK_j, PV_{j-1}: the next tile's scores are requested as soon as
-//               S is free, before the previous tile's probabilities are ready.
+//               S is free, before the previous tile's probabilities are ready. The commit that
+//               frees a K stage also tells the softmax that S is ready, and the one that frees
+//               a V stage tells it that P has been read and O written.
 //
 // Token rule: key j of block J is visible to query i of block I iff J is in row(I) and
 // (not causal or j <= i) ("Parameter-free Adaptive Sparse Attention via Compression-Based
@@ -186,10 +190,8 @@ struct PipeBars {
   uint64_t q_full[2], q_empty[2];
   uint64_t k_full[kMaxStages], k_empty[kMaxStages], v_full[kMaxStages], v_empty[kMaxStages];
   uint64_t m_full[kMetaRing], m_empty[kMetaRing];     // batch ring
-  uint64_t s_full;            // QK_j complete (phase j)
   uint64_t s_free;            // the softmax has loaded S_j (phase j)
   uint64_t p_full;            // the softmax has stored P_j (phase j)
-  uint64_t pv_done[2];        // pv_done[j & 1]: PV_j complete
   uint64_t drain;
 };
 
@@ -437,10 +439,16 @@ __device__ __forceinline__ bool issue_pv(PipeBars& bars, uint32_t tP, uint32_t t
   tc_fence_after();
   constexpr uint32_t idesc = make_idesc_bf16(128, D, 0, 1);
   const uint64_t b0 = vdesc0 + (uint64_t)((stage * C::KV_BYTES) >> 4);
-  for (int ks = 0; ks < nkeys / 16; ++ks)
-    mma_bf16_ts(tO, tP + 8u * ks, b0 + (uint64_t)((16 * ks * C::ROWB) >> 4), idesc, (o_init || ks > 0) ? 1u : 0u);
+  if (nkeys == kKeys) {
+#pragma unroll
+    for (int ks = 0; ks < kKeys / 16; ++ks)
+      mma_bf16_ts(tO, tP + 8u * ks, b0 + (uint64_t)((16 * ks * C::ROWB) >> 4), idesc, (o_init || ks > 0) ? 1u : 0u);
+  } else {
+    for (int ks = 0; ks < nkeys / 16; ++ks)
+      mma_bf16_ts(tO, tP + 8u * ks, b0 + (uint64_t)((16 * ks * C::ROWB) >> 4), idesc, (o_init || ks > 0) ? 1u : 0u);
+  }
   o_init = true;
-  mma_commit(&bars.pv_done[j & 1]);
+  // frees the V stage and tells the softmax that P_j is read and O is written
   mma_commit(&bars.v_empty[stage]);
   return true;
 }
@@ -490,7 +498,7 @@ __device__ void mma_issuer(int x, PipeBars& bars, const Batch* ring, uint8_t* sQ
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks)
         mma_bf16_ss(tS, a0 + (uint64_t)((ks * 32) >> 4), b0 + (uint64_t)((ks * 32) >> 4), idesc, ks > 0 ? 1u : 0u);
-      mma_commit(&bars.s_full);
+      // frees the K stage and tells the softmax that S_g is ready
       mma_commit(&bars.k_empty[stage]);
       if (pend && !(ok = issue_pv<D>(bars, tP, tO, vdesc0, g - 1, (g - 1) % C::VS, g - 1, p_nkeys, o_init,
                                      abort_flag)))
@@ -619,7 +627,8 @@ __device__ void softmax_epilogue(const Params& p, int x, PipeBars& bars, const B
       const int nch = (int)((word_of(ncw, i >> 2) >> sh) & 0xffu);
       const int vis = vb & 15, dch = (vb >> 4) - 1;
 
-      ok = __all_sync(0xffffffffu, wait_bar(&bars.s_full, (uint32_t)g & 1u, abort_flag));
+      // QK_g done: its commit is the (g / KS)-th completion of K stage g % KS
+      ok = __all_sync(0xffffffffu, wait_bar(&bars.k_empty[g % C::KS], (uint32_t)(g / C::KS) & 1u, abort_flag));
       if (!ok) break;
       tc_fence_after();
       uint32_t v[128];
@@ -671,7 +680,7 @@ __device__ void softmax_epilogue(const Params& p, int x, PipeBars& bars, const B
           // PV_{g-1} has read P and finished writing O
           if (g > 0) {
             ok = __all_sync(0xffffffffu,
-                            wait_bar(&bars.pv_done[(g - 1) & 1], (uint32_t)((g - 1) >> 1) & 1u, abort_flag));
+                            wait_bar(&bars.v_empty[(g - 1) % C::VS], (uint32_t)((g - 1) / C::VS) & 1u, abort_flag));
             if (!ok) break;
             tc_fence_after();
           }
@@ -700,7 +709,7 @@ __device__ void softmax_epilogue(const Params& p, int x, PipeBars& bars, const B
 
     // epilogue: O / l and LSE of this query tile's rows
     if (n_item > 0) {
-      ok = __all_sync(0xffffffffu, wait_bar(&bars.pv_done[(g - 1) & 1], (uint32_t)((g - 1) >> 1) & 1u, abort_flag));
+      ok = __all_sync(0xffffffffu, wait_bar(&bars.v_empty[(g - 1) % C::VS], (uint32_t)((g - 1) / C::VS) & 1u, abort_flag));
       if (!ok) break;
       tc_fence_after();
     }
@@ -768,11 +777,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&b.m_full[i], 1);
         mbar_init(&b.m_empty[i], kMetaConsumers);
       }
-      mbar_init(&b.s_full, 1);
       mbar_init(&b.s_free, kSoftmaxWarps);
       mbar_init(&b.p_full, kSoftmaxWarps);
-      mbar_init(&b.pv_done[0], 1);
-      mbar_init(&b.pv_done[1], 1);
       mbar_init(&b.drain, 1);
     }
     abort_flag = 0;
