@@ -341,3 +341,34 @@ def test_head_groups_eight_masks_sixteen_heads():
     o_ref, lse_ref = oracle.attention_csr_heads(bf16_bits_to_f64(qb), bf16_bits_to_f64(kb), bf16_bits_to_f64(vb),
                                                 csrs_o, head_mask, b, 1)
     assert_attention_close(bf16_to_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref, "8 masks")
+
+
+def test_concurrent_launches_on_four_streams():
+    """Four forward launches in flight at once on four streams (each launch takes a work
+    counter slot of its own; both forward kernels and both head-dimension paths); every
+    result matches the oracle."""
+    torch = torch_cuda()
+    shapes = [(64, 64, 1), (32, 32, 1), (64, 128, 0), (128, 64, 1)]   # (d, b, causal)
+    n, bt, h = 1024, 2, 2
+    cases = []
+    for i, (d, b, causal) in enumerate(shapes):
+        rng = np.random.default_rng(300 + i)
+        p = om.MaskParams("full", b, n, causal)
+        bits = [bf16_normal_bits(rng, (bt, n, h, d), 0.25) for _ in range(3)]
+        rp_d, ci_d = _mask_on_gpu(p, bt)
+        cases.append((p, bits, rp_d, ci_d))
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in shapes]
+    outs = []
+    for s, (p, bits, rp_d, ci_d) in zip(streams, cases):
+        with torch.cuda.stream(s):
+            q, k, v = (to_dev(x) for x in bits)
+            outs.append(sa.attn_fwd(q, k, v, rp_d, ci_d, p.block, p.causal))
+    torch.cuda.synchronize()
+    assert sa.sa_device_status() == 0
+    for (p, bits, _, _), (o, lse), (d, _, _) in zip(cases, outs, shapes):
+        rp_o, ci_o = om.build_csr(p, None, bt)
+        f = [bf16_bits_to_f64(x) for x in bits]
+        o_ref, lse_ref = oracle.attention_csr(f[0], f[1], f[2], rp_o, ci_o, p.block, p.causal)
+        assert_attention_close(bf16_to_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref,
+                               f"stream case d={d} b={p.block} causal={p.causal}")
