@@ -24,8 +24,9 @@
 //   warps 0-3   softmax of pipeline 0, warp w reads TMEM lane quarter w (query rows 32w ..)
 //   warps 4-7   softmax of pipeline 1
 //   warps 12, 13 planners of pipeline 0 / 1: claim items, build the key-block union, publish
-//               the item's key tiles into a ring of batches (up to 16 tiles per entry, 128
-//               tiles in the ring: an item or more ahead)
+//               the item's key tiles into a ring of two batches (up to 16 tiles per entry):
+//               the next item's union is built under the current item, and a planner never
+//               claims many items ahead of its pipeline
 //   warps 8, 11 lane 0 loads Q, K and V of pipeline 0 / 1 by TMA as the batches arrive
 //   warps 14, 15 idle (the fourth warpgroup's remainder)
 //   warps 9, 10 lane 0 issues the tcgen05 MMAs of pipeline 0 / 1:
@@ -63,7 +64,7 @@ __device__ unsigned int g_wide_counters[kWorkSlots];
 constexpr int kTile = 128;            // query rows per work item
 constexpr int kKeys = 128;            // keys per S tile (four 32-key chunks)
 constexpr int kThreads = 512;         // 16 warps, four warpgroups
-constexpr int kMetaRing = 8;          // batch entries (up to 128 key tiles)
+constexpr int kMetaRing = 2;          // batch entries: items claimed ahead of the consumers
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSoftmaxWarps = 4;      // per pipeline: one per TMEM lane quarter
 constexpr int kMetaConsumers = 2 + kSoftmaxWarps;   // MMA thread, loader, softmax warps
