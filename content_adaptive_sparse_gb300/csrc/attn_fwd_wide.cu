@@ -288,8 +288,9 @@ __device__ __forceinline__ bool load_tile(const TileLoad& L, const CUtensorMap* 
 // ------------------------------------------------------------------ planner (warps 12, 13)
 
 // Claims work items from the launch-wide counter, builds each item's key-block union and
-// publishes the item's key tiles in batches. The ring holds several items' worth of tiles,
-// so the next item's union is built while the consumers still work on the current one.
+// publishes the item's key tiles in batches. With two ring entries the next item's union is
+// built while the consumers still work on the current one, and no more than about two items
+// are claimed ahead of this pipeline.
 template <int D>
 __device__ void planner(const Params& p, PipeBars& bars, Batch* ring, UnionSmem& u, volatile int* abort_flag) {
   const int lane = threadIdx.x & 31;
