@@ -372,3 +372,11 @@ def test_concurrent_launches_on_four_streams():
         o_ref, lse_ref = oracle.attention_csr(f[0], f[1], f[2], rp_o, ci_o, p.block, p.causal)
         assert_attention_close(bf16_to_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref,
                                f"stream case d={d} b={p.block} causal={p.causal}")
+
+
+@pytest.mark.parametrize("d", [32, 64])
+def test_items_spanning_several_tile_batches(d):
+    """Full causal mask at 4096 tokens with 32-token blocks: the last query tiles' key lists
+    hold 128 blocks = 32 key tiles of 128 keys, published in more than one batch of tiles;
+    the item's output must not depend on where the batches split it."""
+    _run_case(om.MaskParams("full", 32, 4096, 1), 1, 1, 1, d, seed=40 + d, qmul=2.0)
