@@ -987,8 +987,8 @@ int launch_d(const AttnArgs& a, cudaStream_t stream) {
 int launch_attn_fwd(const AttnArgs& a, cudaStream_t stream) {
   switch (a.head_dim) {
     case 32:
-    case 64: return launch_attn_fwd_wide(a, stream);
-    case 128: return launch_d<128>(a, stream);
+    case 64:
+    case 128: return launch_attn_fwd_wide(a, stream);
   }
   return SA_ERR_UNSUPPORTED;
 }

@@ -79,24 +79,34 @@ constexpr int kMaxStages = 4;
 
 template <int D>
 struct Cfg {
-  static_assert(D == 32 || D == 64, "head dimension");
-  static constexpr int ROWB = D * 2;                   // bytes per swizzled row (one d-chunk)
+  static_assert(D == 32 || D == 64 || D == 128, "head dimension");
+  static constexpr int CH = D >= 64 ? 64 : 32;         // head-dimension elements per swizzled row
+  static constexpr int NCH = D / CH;                   // d-chunks of a row
+  static constexpr int ROWB = CH * 2;                  // bytes per swizzled row
   static constexpr uint32_t SWZ = ROWB == 128 ? kSwizzle128B : kSwizzle64B;
   static constexpr CUtensorMapSwizzle TMA_SWZ =
       ROWB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   static constexpr uint32_t ATOM = 8 * ROWB;           // swizzle atom (8 rows)
-  static constexpr int Q_BYTES = kTile * ROWB;
-  static constexpr int KV_BYTES = kKeys * ROWB;        // one K or V tile
+  static constexpr int Q_CHUNK = kTile * ROWB;         // one d-chunk of the Q tile
+  static constexpr int Q_BYTES = NCH * Q_CHUNK;
+  static constexpr int KV_CHUNK = kKeys * ROWB;        // one d-chunk of a K or V tile
+  static constexpr int KV_BYTES = NCH * KV_CHUNK;      // one K or V tile
+  // d = 128: P is written over S's own columns (S and O fill the pipeline's 256 columns),
+  // so QK of tile j+1 waits until PV of tile j has read P; the two pipelines of the CTA keep
+  // the tensor core busy in turn, and one K, V and Q buffer per pipeline are enough (a K load
+  // has a whole softmax to land, a V load a QK and a softmax).
+  static constexpr bool ALIAS = D == 128;
   // Ring depths. V is loaded one key tile behind K (it is needed one softmax later).
-  static constexpr int QB = 2;                         // Q buffers per pipeline
-  static constexpr int KS = D == 64 ? 2 : 4;           // K ring depth
-  static constexpr int VS = D == 64 ? 2 : 4;           // V ring depth
+  static constexpr int QB = ALIAS ? 1 : 2;             // Q buffers per pipeline
+  static constexpr int KS = ALIAS ? 1 : (D == 64 ? 2 : 4);   // K ring depth
+  static constexpr int VS = ALIAS ? 1 : (D == 64 ? 2 : 4);   // V ring depth
   static constexpr int UNION_BYTES = kMaxTileBlocks * (kMaxMaskBlocks / 32) * 4 + kMaxMaskBlocks * 2;
   static constexpr int PIPE_BYTES = (QB * Q_BYTES + (KS + VS) * KV_BYTES + UNION_BYTES + 1023) & ~1023;
   static constexpr int SMEM = 1024 + 2 * PIPE_BYTES;
   __host__ __device__ static constexpr uint32_t col_s(int x) { return 256u * x; }
-  __host__ __device__ static constexpr uint32_t col_p(int x) { return 256u * x + 128u; }
-  __host__ __device__ static constexpr uint32_t col_o(int x) { return 256u * x + 192u; }
+  __host__ __device__ static constexpr uint32_t col_p(int x) { return ALIAS ? 256u * x : 256u * x + 128u; }
+  __host__ __device__ static constexpr uint32_t col_o(int x) { return ALIAS ? 256u * x + 128u : 256u * x + 192u; }
+  static_assert((ALIAS ? 128 : 192) + D <= 256, "TMEM columns of a pipeline");
   static_assert(KS <= kMaxStages && VS <= kMaxStages, "ring size");
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
@@ -272,16 +282,22 @@ struct TileLoad {
   int tok[4];
 };
 
-// Lane 0: waits for ring stage t % S of (full, empty) and issues the tile's boxes into it.
-template <int S, int ROWB>
-__device__ __forceinline__ bool load_tile(const TileLoad& L, const CUtensorMap* map, uint8_t* ring, int stage_bytes,
-                                          uint64_t* full, uint64_t* empty, volatile int* abort_flag) {
+// Lane 0: waits for ring stage t % S of (full, empty) and issues the tile's boxes into it
+// (each box once per d-chunk; chunk c of a stage starts KV_CHUNK * c bytes in).
+template <int D, int S>
+__device__ __forceinline__ bool load_tile(const TileLoad& L, const CUtensorMap* map, uint8_t* ring, uint64_t* full,
+                                          uint64_t* empty, volatile int* abort_flag) {
+  using C = Cfg<D>;
   const int st = L.t % S;
   if (!wait_bar(&empty[st], ((L.t / S) & 1) ^ 1, abort_flag)) return false;
   mbar_arrive_expect_tx(&full[st], L.bytes);
 #pragma unroll
   for (int i = 0; i < 4; ++i)
-    if (i < L.nbox) tma_load_4d(ring + st * stage_bytes + i * L.rows * ROWB, map, &full[st], 0, L.hk, L.tok[i], L.s);
+    if (i < L.nbox)
+#pragma unroll
+      for (int c = 0; c < C::NCH; ++c)
+        tma_load_4d(ring + st * C::KV_BYTES + c * C::KV_CHUNK + i * L.rows * C::ROWB, map, &full[st], c * C::CH,
+                    L.hk, L.tok[i], L.s);
   return true;
 }
 
@@ -387,7 +403,9 @@ __device__ void loader(const Params& p, const CUtensorMap* tq, const CUtensorMap
         break;
       // rows beyond the sequence are zero-filled by TMA
       mbar_arrive_expect_tx(&bars.q_full[qb], C::Q_BYTES);
-      tma_load_4d(sQ + qb * C::Q_BYTES, tq, &bars.q_full[qb], 0, it.h, it.tile * kTile, it.s);
+#pragma unroll
+      for (int c = 0; c < C::NCH; ++c)
+        tma_load_4d(sQ + qb * C::Q_BYTES + c * C::Q_CHUNK, tq, &bars.q_full[qb], c * C::CH, it.h, it.tile * kTile, it.s);
       q_last = item_local;
     }
     for (int i = 0; i < hdr.y && ok; ++i) {
@@ -404,10 +422,17 @@ __device__ void loader(const Params& p, const CUtensorMap* tq, const CUtensorMap
       L.tok[1] = (rows == 32 ? tm.y : tm.z) >> 4;
       L.tok[2] = tm.z >> 4;
       L.tok[3] = tm.w >> 4;
-      if (!(ok = load_tile<C::KS, C::ROWB>(L, tk, sK, C::KV_BYTES, bars.k_full, bars.k_empty, abort_flag))) break;
+      if (!(ok = load_tile<D, C::KS>(L, tk, sK, bars.k_full, bars.k_empty, abort_flag))) break;
       k_issued = ++kt;
+      if (C::ALIAS) {
+        // P over S: QK of the next tile waits for this tile's PV anyway, so V goes right
+        // after K (its stage frees when the previous PV completes)
+        if (!(ok = load_tile<D, C::VS>(L, tv, sV, bars.v_full, bars.v_empty, abort_flag))) break;
+        v_issued = L.t + 1;
+        continue;
+      }
       if (v_pending) {
-        if (!(ok = load_tile<C::VS, C::ROWB>(pend, tv, sV, C::KV_BYTES, bars.v_full, bars.v_empty, abort_flag))) break;
+        if (!(ok = load_tile<D, C::VS>(pend, tv, sV, bars.v_full, bars.v_empty, abort_flag))) break;
         v_issued = pend.t + 1;
       }
       pend = L;
@@ -417,7 +442,7 @@ __device__ void loader(const Params& p, const CUtensorMap* tq, const CUtensorMap
     mbar_arrive(&bars.m_empty[mt % kMetaRing]);
     if ((hdr.w & kLast) && v_pending) {
       // end of the item: its last V cannot wait for the next item's first K
-      if (!(ok = load_tile<C::VS, C::ROWB>(pend, tv, sV, C::KV_BYTES, bars.v_full, bars.v_empty, abort_flag))) break;
+      if (!(ok = load_tile<D, C::VS>(pend, tv, sV, bars.v_full, bars.v_empty, abort_flag))) break;
       v_issued = pend.t + 1;
       v_pending = false;
     }
@@ -429,6 +454,14 @@ __device__ void loader(const Params& p, const CUtensorMap* tq, const CUtensorMap
 }
 
 // ------------------------------------------------------------------ MMA issuer (warps 9, 10, lane 0)
+
+// Descriptor offset (bytes >> 4) of k-step ks (16 head-dimension elements) inside a K-major
+// tile whose d-chunks are `chunk` bytes apart.
+template <int D>
+__device__ __forceinline__ constexpr uint64_t kmajor_step(int ks, int chunk) {
+  using C = Cfg<D>;
+  return (uint64_t)((((ks * 16) / C::CH) * chunk + ((ks * 16) % C::CH) * 2) >> 4);
+}
 
 // O += P_j V_j for the key tile held in ring stage `stage` (its V load was the kt-th),
 // after P_j is stored. `o_init` says whether O already holds this item's sum.
@@ -461,7 +494,8 @@ __device__ void mma_issuer(int x, PipeBars& bars, const Batch* ring, uint8_t* sQ
   using C = Cfg<D>;
   const uint64_t qdesc = make_smem_desc(smem_u32(sQ), 16, C::ATOM, C::SWZ);
   const uint64_t kdesc0 = make_smem_desc(smem_u32(sK), 16, C::ATOM, C::SWZ);
-  const uint64_t vdesc0 = make_smem_desc(smem_u32(sV), C::KV_BYTES, C::ATOM, C::SWZ);
+  // V is the MN-major B operand of PV: N = d runs across the d-chunks (KV_CHUNK apart)
+  const uint64_t vdesc0 = make_smem_desc(smem_u32(sV), C::KV_CHUNK, C::ATOM, C::SWZ);
   const uint32_t tS = tmem + C::col_s(x), tP = tmem + C::col_p(x), tO = tmem + C::col_o(x);
   int g = 0;                // key tiles of this pipeline whose QK is issued (K / V ring position)
   int item_local = -1;
@@ -492,21 +526,33 @@ __device__ void mma_issuer(int x, PipeBars& bars, const Batch* ring, uint8_t* sQ
       const int nkeys = 32 * (int)((word_of(ncw, i >> 2) >> (8 * (i & 3))) & 0xffu);
       const int stage = g % C::KS;
       if (!(ok = wait_bar(&bars.k_full[stage], (uint32_t)(g / C::KS) & 1u, abort_flag))) break;
-      // S is free once the softmax has loaded S_{g-1}
-      if (g > 0 && !(ok = wait_bar(&bars.s_free, (uint32_t)(g - 1) & 1u, abort_flag))) break;
+      if (C::ALIAS) {
+        // S holds P_{g-1} until PV_{g-1} has read it (the commit that frees its V stage)
+        if (g > 0 && !(ok = wait_bar(&bars.v_empty[(g - 1) % C::VS], (uint32_t)((g - 1) / C::VS) & 1u, abort_flag)))
+          break;
+      } else {
+        // S is free once the softmax has loaded S_{g-1}
+        if (g > 0 && !(ok = wait_bar(&bars.s_free, (uint32_t)(g - 1) & 1u, abort_flag))) break;
+      }
       tc_fence_after();
       const uint32_t idesc = make_idesc_bf16(128, (uint32_t)nkeys, 0, 0);
       const uint64_t b0 = kdesc0 + (uint64_t)((stage * C::KV_BYTES) >> 4);
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks)
-        mma_bf16_ss(tS, a0 + (uint64_t)((ks * 32) >> 4), b0 + (uint64_t)((ks * 32) >> 4), idesc, ks > 0 ? 1u : 0u);
+        mma_bf16_ss(tS, a0 + kmajor_step<D>(ks, C::Q_CHUNK), b0 + kmajor_step<D>(ks, C::KV_CHUNK), idesc,
+                    ks > 0 ? 1u : 0u);
       // frees the K stage and tells the softmax that S_g is ready
       mma_commit(&bars.k_empty[stage]);
-      if (pend && !(ok = issue_pv<D>(bars, tP, tO, vdesc0, g - 1, (g - 1) % C::VS, g - 1, p_nkeys, o_init,
-                                     abort_flag)))
-        break;
-      pend = true;
-      p_nkeys = nkeys;
+      if (C::ALIAS) {
+        // nothing else of this pipeline can go ahead of PV_g
+        if (!(ok = issue_pv<D>(bars, tP, tO, vdesc0, g, g % C::VS, g, nkeys, o_init, abort_flag))) break;
+      } else {
+        if (pend && !(ok = issue_pv<D>(bars, tP, tO, vdesc0, g - 1, (g - 1) % C::VS, g - 1, p_nkeys, o_init,
+                                       abort_flag)))
+          break;
+        pend = true;
+        p_nkeys = nkeys;
+      }
       ++g;
     }
     if (!ok) break;
@@ -637,10 +683,12 @@ __device__ void softmax_epilogue(const Params& p, int x, PipeBars& bars, const B
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) tmem_ld_x32(tS + 32 * ch, v + 32 * ch);
       tmem_ld_wait<128>(v);
-      // S may now be overwritten by the next QK
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.s_free);
+      if (!C::ALIAS) {
+        // S may now be overwritten by the next QK
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.s_free);
+      }
 
       if (dch >= 0) {
         // the diagonal chunk starts at this warp's first query: row r sees columns 0 .. r
@@ -679,8 +727,9 @@ __device__ void softmax_epilogue(const Params& p, int x, PipeBars& bars, const B
           for (int j = 0; j < 16; ++j) pk[j] = 0u;
         }
         if (ch == 0) {
-          // PV_{g-1} has read P and finished writing O
-          if (g > 0) {
+          // PV_{g-1} has read P and finished writing O (with P over S this holds already:
+          // QK_g was issued after PV_{g-1} completed, and S_g is here)
+          if (!C::ALIAS && g > 0) {
             ok = __all_sync(0xffffffffu,
                             wait_bar(&bars.v_empty[(g - 1) % C::VS], (uint32_t)((g - 1) / C::VS) & 1u, abort_flag));
             if (!ok) break;
@@ -842,12 +891,12 @@ int launch_d(const AttnArgs& a, cudaStream_t stream) {
   using C = Cfg<D>;
   CUtensorMap tq, tk, tv;
   const uint32_t kv_rows = a.block == 32 ? 32u : 64u;
-  if (!encode_bhnd_map(&tq, a.q, a.batch, a.n_tokens, a.heads, D, a.q_strides[0], a.q_strides[1], a.q_strides[2], D,
-                       kTile, C::TMA_SWZ) ||
+  if (!encode_bhnd_map(&tq, a.q, a.batch, a.n_tokens, a.heads, D, a.q_strides[0], a.q_strides[1], a.q_strides[2],
+                       C::CH, kTile, C::TMA_SWZ) ||
       !encode_bhnd_map(&tk, a.k, a.batch, a.n_tokens, a.kv_heads, D, a.kv_strides[0], a.kv_strides[1],
-                       a.kv_strides[2], D, kv_rows, C::TMA_SWZ) ||
+                       a.kv_strides[2], C::CH, kv_rows, C::TMA_SWZ) ||
       !encode_bhnd_map(&tv, a.v, a.batch, a.n_tokens, a.kv_heads, D, a.kv_strides[0], a.kv_strides[1],
-                       a.kv_strides[2], D, kv_rows, C::TMA_SWZ))
+                       a.kv_strides[2], C::CH, kv_rows, C::TMA_SWZ))
     return SA_ERR_UNSUPPORTED;
   Params p;
   p.batch = a.batch;
@@ -899,6 +948,7 @@ int launch_attn_fwd_wide(const AttnArgs& a, cudaStream_t stream) {
   switch (a.head_dim) {
     case 32: return launch_d<32>(a, stream);
     case 64: return launch_d<64>(a, stream);
+    case 128: return launch_d<128>(a, stream);
   }
   return SA_ERR_UNSUPPORTED;
 }
