@@ -605,7 +605,7 @@ def run_ours(args):
                "sample": f"{res['units']} random (sequence, query block, head) units of the same workload "
                          f"({res['seconds']:.1f} s, numpy float64, 1 BLAS thread)"}
 
-    traffic = _profile_traffic("attn_fwd_bytelm_topk_8k.md", ["attn_fwd.cu", "attn_fwd_wide.cu", "ptx_sm100.cuh", "csr_union.cuh"])
+    traffic = _profile_traffic("attn_fwd_bytelm_topk_8k.md", ["attn_fwd.cu", "ptx_sm100.cuh", "csr_union.cuh"])
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
@@ -617,7 +617,7 @@ def run_ours(args):
         "segments_ms": {"sa_build_mask": mask_ms, "sa_attn_fwd": attn_ms},
         "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": peak, "unit": "TFLOP/s",
                      "frac": attn_tflops / peak, "traffic": traffic,
-                     "kernel": "attn_fwd_wide_kernel<64> (sa_attn_fwd)",
+                     "kernel": "attn_fwd_kernel<64> (sa_attn_fwd)",
                      "peak_source": f"{peaks['source']} bf16 burst (kernel timed alone)",
                      "algorithmic_flops_per_launch": case.flops,
                      "frac_of_sustained": attn_tflops / peaks["bf16_tflops_sustained"]

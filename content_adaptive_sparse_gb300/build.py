@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libsa.so")
-SOURCES = ["sa_api.cu", "mask_build.cu", "attn_fwd.cu", "attn_fwd_wide.cu", "attn_bwd.cu", "offset_attn.cu", "offset_interp.cu"]
+SOURCES = ["sa_api.cu", "mask_build.cu", "attn_fwd.cu", "attn_bwd.cu", "offset_attn.cu", "offset_interp.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

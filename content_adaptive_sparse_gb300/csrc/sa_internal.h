@@ -51,10 +51,6 @@ struct AttnArgs {
 int launch_attn_fwd(const AttnArgs& a, cudaStream_t stream);
 unsigned int attn_read_and_clear_error(cudaStream_t stream);
 
-// attn_fwd_wide.cu (head dimensions 32 and 64)
-int launch_attn_fwd_wide(const AttnArgs& a, cudaStream_t stream);
-unsigned int attn_wide_read_and_clear_error(cudaStream_t stream);
-
 // offset_attn.cu
 constexpr int kMaxOffsets = 64;
 constexpr int kMaxWindow = 64;

@@ -14,9 +14,8 @@
  *   - Device pointers are marked d_*, host pointers h_*; q/k/v/o/lse are device memory.
  *   - The caller owns all memory. The library allocates no device memory; its only
  *     device state is static arrays in the module: the device error words (see
- *     sa_device_status), 64 work-counter slots for each of the two block-sparse forward
- *     kernels (head_dim <= 64 and head_dim = 128; each launch takes the next slot of its
- *     kernel and zeroes it on its stream, so at most 64 launches of one kernel may be in
+ *     sa_device_status), 64 work-counter slots of the block-sparse forward (each launch
+ *     takes the next slot and zeroes it on its stream, so at most 64 launches may be in
  *     flight at once across streams) and the 16 MiB scratch of sa_attn_bwd_noalloc.
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = legacy default
  *     stream). Argument errors are returned synchronously before anything is launched.
