@@ -13,18 +13,16 @@
 //     uses only key r: the diagonal of a 16 x 16 block. Computed with 8 mma.sync for QK
 //     and 8 for PV; the zero off-diagonal P entries cost tensor work, not memory traffic.
 //
-// Work item: one CTA of 8 warps per (sequence, head, 64-query tile). Warps 4g..4g+3 form
-// group g; warp w of a group owns queries q0 + 16w .. q0 + 16w + 15. The two groups split
-// the keys (group 0 the first half of the band steps and the even offset slabs, group 1
-// the rest) and merge their partial softmax states through shared memory at the end.
-// K/V arrive by TMA: the band (rows [q0 - 64, q0 + 64)) once, the offset slabs (64 rows
-// each) through a ring of four buffers (two per group) that the last warp done with a
-// buffer refills, so loads are issued from many warps (one issuing thread streams boxes
-// slowly). Buffers 2 and 3 reuse the band's memory once every warp is past the band, so at
-// 66.5 KB of shared memory three CTAs still share an SM (3 % faster than two buffers; four
-// buffers of their own allowed only two CTAs per SM and were 1.5 % slower than two).
-// Softmax: exact max over the band part, then the offsets with a lazily rescaled
-// running max (threshold 2^8).
+// Work item: one CTA of 4 warps per (sequence, head, 64-query tile); warp w owns queries
+// q0 + 16w .. q0 + 16w + 15 and takes every key of them (band steps and offsets), so no
+// two warps merge softmax states. The band (K/V rows [q0 - 64, q0 + 64)) arrives by TMA
+// once per CTA and is shared by the four warps. Once every warp is past the band, its
+// 32 KB become four per-warp slab rings of two buffers: a warp streams the 16 K and V rows
+// of each larger offset that its own queries use (4 KB) two offsets ahead, and waits on
+// nothing but its own copies (no cross-warp release of a buffer, no CTA barrier between
+// offsets). At 33 KB of shared memory and <= 80 registers six CTAs (24 warps) share an SM.
+// Softmax: exact max over the band part, then the offsets with a lazily rescaled running
+// max (threshold 2^8).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -40,15 +38,15 @@ namespace {
 __device__ unsigned int g_offset_err;
 
 constexpr int kQ = 64;                   // queries per CTA
-constexpr int kGroupWarps = 4;           // 16 queries per warp: one group covers the tile
-constexpr int kWarps = 2 * kGroupWarps;  // two groups split the keys of the tile
-constexpr int kRing = 4;                 // offset slab buffers per CTA (two per group)
-constexpr int kRingMem = 2;              // of which own memory; buffers 2, 3 reuse the band's
+constexpr int kWarps = 4;                // 16 queries per warp
+constexpr int kCtasPerSm = 6;            // 33 KB of shared memory and <= 80 registers per thread
+constexpr int kRing = 2;                 // slab buffers per warp
 constexpr int kD = 64;                   // head dim supported by this kernel
 constexpr int kRowBytes = kD * 2;        // 128 B per K/V row
 constexpr int kBandMax = 64;             // deltas up to this go through the band
 constexpr int kBandRows = kQ + kBandMax; // band slab rows [q0 - 64, q0 + 64)
-constexpr int kSlabBytes = kQ * kRowBytes;
+constexpr int kWarpSlabBytes = 2 * 16 * kRowBytes;   // K and V rows of one warp's 16 queries
+static_assert(kWarps * kRing * kWarpSlabBytes == 2 * kBandRows * kRowBytes, "warp rings fill the band's memory");
 constexpr int kBandBytes = kBandRows * kRowBytes;
 constexpr int kMaxLarge = kMaxOffsets;
 constexpr uint32_t kOnesBf16x2 = 0x3f803f80u;   // (1.0, 1.0) in bf16
@@ -159,7 +157,7 @@ __device__ __forceinline__ void diag_pv(uint32_t vt, int wq, int lane, bool hold
 }
 
 template <int NKT>
-__global__ void __launch_bounds__(kWarps * 32, 3)
+__global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
     offset_attn_kernel(const __grid_constant__ CUtensorMap tk_band, const __grid_constant__ CUtensorMap tv_band,
                        const __grid_constant__ CUtensorMap tk_slab, const __grid_constant__ CUtensorMap tv_slab,
                        const __grid_constant__ OffParams p) {
@@ -167,53 +165,40 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sKb = sm;                        // band K, 16 KB
   uint8_t* sVb = sKb + kBandBytes;          // band V, 16 KB
-  uint8_t* sRing = sVb + kBandBytes;        // slab buffers 0, 1 (K slab, V slab), 32 KB; merge buffer at the end
-  // slab buffer b: 0, 1 in the ring memory, 2, 3 over the band (free once the band is done)
-  auto slab_buf = [&](int b) -> uint8_t* { return b < kRingMem ? sRing + b * 2 * kSlabBytes : sKb + (b - kRingMem) * kBandBytes; };
-  __shared__ uint64_t bar_band, bar_slab[kRing];
-  __shared__ int done_cnt[kRing];           // warps finished with the slab in each buffer
-  __shared__ int n_issued;                  // slabs issued so far
+  // once every warp is past the band, warp w's slab ring occupies [w * 8 KB, w * 8 KB + 8 KB)
+  // of the band's memory: buffer b at + b * 4 KB, K rows at + 0, V rows at + 2 KB
+  __shared__ uint64_t bar_band, bar_slab[kWarps][kRing];
   __shared__ int abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int grp = warp / kGroupWarps, wq = warp % kGroupWarps;
+  const int wq = warp;
   const int h = blockIdx.x % p.heads;
   const int s = blockIdx.x / p.heads;
   const int tile = p.ntiles - 1 - (int)blockIdx.y;   // later tiles reach more offsets: start them first
   const int q0 = tile * kQ;
   const int hk = h / p.heads_per_kv;
-  // larger offsets that reach at least one query of this tile
+  // larger offsets that reach at least one query of this warp
+  const int qw = q0 + 16 * wq;               // first query of this warp
   int n_off = 0;
-  while (n_off < p.n_large && p.large[n_off] <= q0 + kQ - 1) ++n_off;
+  while (n_off < p.n_large && p.large[n_off] <= qw + 15) ++n_off;
 
   if (tid == 0) {
     mbar_init(&bar_band, 1);
 #pragma unroll
-    for (int b = 0; b < kRing; ++b) {
-      mbar_init(&bar_slab[b], 1);
-      done_cnt[b] = 0;
-    }
+    for (int w = 0; w < kWarps; ++w)
+#pragma unroll
+      for (int b = 0; b < kRing; ++b) mbar_init(&bar_slab[w][b], 1);
     abort_flag = 0;
-    n_issued = n_off < kRingMem ? n_off : kRingMem;
     fence_mbar_init();
     mbar_arrive_expect_tx(&bar_band, (uint32_t)(2 * kBandBytes));
   }
   __syncthreads();
-  // A single thread streams TMA boxes at a limited rate, so several warps issue loads:
-  // warp w < kRingMem the first slab of buffer w, warps 4 and 5 the band.
   if (lane == 0) {
-    if (warp == 4) tma_load_4d(sKb, &tk_band, &bar_band, 0, hk, q0 - kBandMax, s);
-    if (warp == 5) tma_load_4d(sVb, &tv_band, &bar_band, 0, hk, q0 - kBandMax, s);
-    if (warp < kRingMem && warp < n_off) {
-      uint8_t* dst = slab_buf(warp);
-      mbar_arrive_expect_tx(&bar_slab[warp], 2u * kSlabBytes);
-      tma_load_4d(dst, &tk_slab, &bar_slab[warp], 0, hk, q0 - p.large[warp], s);
-      tma_load_4d(dst + kSlabBytes, &tv_slab, &bar_slab[warp], 0, hk, q0 - p.large[warp], s);
-    }
+    if (warp == 0) tma_load_4d(sKb, &tk_band, &bar_band, 0, hk, q0 - kBandMax, s);
+    if (warp == 1) tma_load_4d(sVb, &tv_band, &bar_band, 0, hk, q0 - kBandMax, s);
   }
 
   const int g = lane >> 2, t = lane & 3;     // mma fragment coordinates: rows g, g+8; cols 2t, 2t+1
-  const int qw = q0 + 16 * wq;               // first query of this warp
   const float c = p.scale_log2;
   const float kNegInf = __int_as_float(0xff800000);
 
@@ -243,14 +228,12 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
   float o[8][4];                             // O fragments: d n-tiles 0..7
 #pragma unroll
   for (int nt = 0; nt < 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-  // running max of rows g, g+8 (log2 units); -inf until this group has seen a kept key
+  // running max of rows g, g+8 (log2 units)
   float m_lo = kNegInf, m_hi = kNegInf;
   float l_lo = 0.f, l_hi = 0.f;
 
   if (ok) {
-    // ---------------- band: keys [qw - Dr, qw + 16), band slab row = key - (q0 - 64);
-    // group 0 takes the first (NKT + 1) / 2 16-key steps, group 1 the rest
-    constexpr int kSplit = (NKT + 1) / 2;
+    // ---------------- band: keys [qw - Dr, qw + 16), band slab row = key - (q0 - 64)
     uint64_t keep = p.keep[lane];
     const int lim = p.dr - qw;               // band columns below lim are keys < 0 (first tile only)
     if (lim > 0) {
@@ -266,77 +249,73 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
     float mx_lo = kNegInf, mx_hi = kNegInf;
 #pragma unroll
     for (int nt = 0; nt < 2 * NKT; ++nt) {
-      if ((nt / 2 < kSplit) == (grp == 0)) {
-        uint32_t u[8];
-        load_kfrag(kb_tile, row0 + 8 * nt + g, t, u);
-        sb[nt][0] = sb[nt][1] = sb[nt][2] = sb[nt][3] = 0.f;
-        qk_ntile(sb[nt], qa, u);
+      uint32_t u[8];
+      load_kfrag(kb_tile, row0 + 8 * nt + g, t, u);
+      sb[nt][0] = sb[nt][1] = sb[nt][2] = sb[nt][3] = 0.f;
+      qk_ntile(sb[nt], qa, u);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float v = (keep >> (4 * nt + e)) & 1ull ? sb[nt][e] : kNegInf;
-          sb[nt][e] = v;
-          if (e < 2) mx_lo = fmaxf(mx_lo, v);
-          else mx_hi = fmaxf(mx_hi, v);
-        }
+      for (int e = 0; e < 4; ++e) {
+        const float v = (keep >> (4 * nt + e)) & 1ull ? sb[nt][e] : kNegInf;
+        sb[nt][e] = v;
+        if (e < 2) mx_lo = fmaxf(mx_lo, v);
+        else mx_hi = fmaxf(mx_hi, v);
       }
     }
     mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
     mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
     mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
     mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
-    m_lo = mx_lo * c;                        // -inf * c stays -inf
+    m_lo = mx_lo * c;                        // finite: distance 0 is always kept
     m_hi = mx_hi * c;
-    const float e_lo = m_lo == kNegInf ? 0.f : m_lo, e_hi = m_hi == kNegInf ? 0.f : m_hi;
     // P = exp2(s c - m); row sums of the bf16 P the PV product uses come from one more
     // MMA against a ones matrix
     float lsum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < NKT; ++j) {
-      if ((j < kSplit) == (grp == 0)) {
-        uint32_t pa[4];
-        pa[0] = pack_bf16x2(ex2_approx(fmaf(sb[2 * j][0], c, -e_lo)), ex2_approx(fmaf(sb[2 * j][1], c, -e_lo)));
-        pa[1] = pack_bf16x2(ex2_approx(fmaf(sb[2 * j][2], c, -e_hi)), ex2_approx(fmaf(sb[2 * j][3], c, -e_hi)));
-        pa[2] = pack_bf16x2(ex2_approx(fmaf(sb[2 * j + 1][0], c, -e_lo)),
-                            ex2_approx(fmaf(sb[2 * j + 1][1], c, -e_lo)));
-        pa[3] = pack_bf16x2(ex2_approx(fmaf(sb[2 * j + 1][2], c, -e_hi)),
-                            ex2_approx(fmaf(sb[2 * j + 1][3], c, -e_hi)));
-        mma16816(lsum, pa, kOnesBf16x2, kOnesBf16x2);
-        uint32_t vb[4][4];
-        load_v16(vb_tile, row0 + 16 * j, lane, vb);
-        pv_16(o, pa, vb);
-      }
+      uint32_t pa[4];
+      pa[0] = pack_bf16x2(ex2_approx(fmaf(sb[2 * j][0], c, -m_lo)), ex2_approx(fmaf(sb[2 * j][1], c, -m_lo)));
+      pa[1] = pack_bf16x2(ex2_approx(fmaf(sb[2 * j][2], c, -m_hi)), ex2_approx(fmaf(sb[2 * j][3], c, -m_hi)));
+      pa[2] = pack_bf16x2(ex2_approx(fmaf(sb[2 * j + 1][0], c, -m_lo)),
+                          ex2_approx(fmaf(sb[2 * j + 1][1], c, -m_lo)));
+      pa[3] = pack_bf16x2(ex2_approx(fmaf(sb[2 * j + 1][2], c, -m_hi)),
+                          ex2_approx(fmaf(sb[2 * j + 1][3], c, -m_hi)));
+      mma16816(lsum, pa, kOnesBf16x2, kOnesBf16x2);
+      uint32_t vb[4][4];
+      load_v16(vb_tile, row0 + 16 * j, lane, vb);
+      pv_16(o, pa, vb);
     }
     l_lo = lsum[0];
     l_hi = lsum[2];
   }
 
-  // The band is read: its memory becomes slab buffers 2 and 3 (slabs 2 and 3 of the tile),
-  // so each group has two slabs in flight while it works on one.
+  // The band is read: its memory becomes the warps' slab rings. Each warp streams the 16
+  // key rows of each larger offset that its own queries use, two slabs ahead, and waits
+  // on nothing but its own copies.
   __syncthreads();
-  if (tid == 0 && !abort_flag) {
-    for (int k = kRingMem; k < kRing && k < n_off; ++k) {
-      uint8_t* dst = slab_buf(k);
-      mbar_arrive_expect_tx(&bar_slab[k], 2u * kSlabBytes);
-      tma_load_4d(dst, &tk_slab, &bar_slab[k], 0, hk, q0 - p.large[k], s);
-      tma_load_4d(dst + kSlabBytes, &tv_slab, &bar_slab[k], 0, hk, q0 - p.large[k], s);
-      n_issued = k + 1;
+  uint8_t* ring = sm + wq * (kRing * kWarpSlabBytes);
+  int issued = 0;
+  if (lane == 0 && !abort_flag) {
+    for (; issued < kRing && issued < n_off; ++issued) {
+      uint8_t* dst = ring + issued * kWarpSlabBytes;
+      mbar_arrive_expect_tx(&bar_slab[wq][issued], (uint32_t)kWarpSlabBytes);
+      tma_load_4d(dst, &tk_slab, &bar_slab[wq][issued], 0, hk, qw - p.large[issued], s);
+      tma_load_4d(dst + kWarpSlabBytes / 2, &tv_slab, &bar_slab[wq][issued], 0, hk, qw - p.large[issued], s);
     }
   }
   ok = ok && !abort_flag;
 
-  // ---------------- larger offsets: group 0 takes slabs 0, 2, 4, ..., group 1 slabs 1, 3, ...
-  // (buffers {0, 2} and {1, 3}); one diagonal 16 x 16 block per slab
+  // ---------------- larger offsets: one diagonal 16 x 16 block per slab
   const int hl = (lane & ~3) | (g >> 1);     // lane of this quad that holds the diagonal
   const bool holder = (t == (g >> 1));
   const int e_sel = g & 1;                   // which of the two fragment columns is diagonal
-  for (int k = grp; k < n_off && ok; k += 2) {
-    const int buf = k % kRing;
-    ok = __all_sync(0xffffffffu, mbar_wait(&bar_slab[buf], (uint32_t)(k / kRing) & 1u, &abort_flag,
+  for (int k = 0; k < n_off && ok; ++k) {
+    const int b = k % kRing;
+    ok = __all_sync(0xffffffffu, mbar_wait(&bar_slab[wq][b], (uint32_t)(k / kRing) & 1u, &abort_flag,
                                            &g_offset_err, kErrTimeout));
     if (!ok) break;
-    const uint32_t kt = smem_u32(slab_buf(buf));
+    const uint32_t kt = smem_u32(ring + b * kWarpSlabBytes);
     float s_lo, s_hi;
-    diag_scores(kt, wq, g, t, hl, e_sel, qa, s_lo, s_hi);
+    diag_scores(kt, 0, g, t, hl, e_sel, qa, s_lo, s_hi);
     const int delta = p.large[k];
     if (qw + g - delta < 0) s_lo = kNegInf;
     if (qw + g + 8 - delta < 0) s_hi = kNegInf;
@@ -356,95 +335,56 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
       l_lo *= a_lo;
       l_hi *= a_hi;
     }
-    const float e_lo = m_lo == kNegInf ? 0.f : m_lo, e_hi = m_hi == kNegInf ? 0.f : m_hi;
-    const uint32_t pb = pack_bf16x2(ex2_approx(fmaf(s_lo, c, -e_lo)), ex2_approx(fmaf(s_hi, c, -e_hi)));
+    const uint32_t pb = pack_bf16x2(ex2_approx(fmaf(s_lo, c, -m_lo)), ex2_approx(fmaf(s_hi, c, -m_hi)));
     l_lo += __uint_as_float(pb << 16);
     l_hi += __uint_as_float(pb & 0xffff0000u);
-    diag_pv(kt + kSlabBytes, wq, lane, holder, e_sel, pb, o);
-    // the last warp of the group done with this buffer refills it with slab k + kRing
+    diag_pv(kt + kWarpSlabBytes / 2, 0, lane, holder, e_sel, pb, o);
+    // every lane has read the buffer: refill it with the slab kRing ahead
     __syncwarp();
-    if (lane == 0) {
-      __threadfence_block();
-      if (atomicAdd(&done_cnt[buf], 1) == kGroupWarps - 1) {
-        __threadfence_block();
-        done_cnt[buf] = 0;
-        const int nk = k + kRing;
-        if (nk < n_off && !abort_flag) {
-          uint8_t* dst = slab_buf(buf);
-          mbar_arrive_expect_tx(&bar_slab[buf], 2u * kSlabBytes);
-          tma_load_4d(dst, &tk_slab, &bar_slab[buf], 0, hk, q0 - p.large[nk], s);
-          tma_load_4d(dst + kSlabBytes, &tv_slab, &bar_slab[buf], 0, hk, q0 - p.large[nk], s);
-          atomicMax(&n_issued, nk + 1);
-        }
-      }
+    if (lane == 0 && issued < n_off && !abort_flag) {
+      uint8_t* dst = ring + b * kWarpSlabBytes;
+      mbar_arrive_expect_tx(&bar_slab[wq][b], (uint32_t)kWarpSlabBytes);
+      tma_load_4d(dst, &tk_slab, &bar_slab[wq][b], 0, hk, qw - p.large[issued], s);
+      tma_load_4d(dst + kWarpSlabBytes / 2, &tv_slab, &bar_slab[wq][b], 0, hk, qw - p.large[issued], s);
+      ++issued;
     }
-  }
-  __syncthreads();
-  if (abort_flag) {
-    // drain this CTA's own copies before exit: the band and the last slab of each buffer
-    if (tid == 0) {
-      int never = 0;
-      mbar_wait(&bar_band, 0, &never, &g_offset_err, kErrTimeout);
-      const int ni = n_issued;
-      for (int j = ni - kRing < 0 ? 0 : ni - kRing; j < ni; ++j)
-        mbar_wait(&bar_slab[j % kRing], (uint32_t)(j / kRing) & 1u, &never, &g_offset_err, kErrTimeout);
-    }
-    return;
   }
 
-  // ---------------- merge the two groups' partial softmax states (ring buffers are idle now)
-  float4* sO = reinterpret_cast<float4*>(sRing);                        // [wq][nt][lane]
-  float4* sML = reinterpret_cast<float4*>(sRing + kGroupWarps * 8 * 32 * 16);   // [wq][lane]
-  if (grp == 1) {
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) sO[(wq * 8 + nt) * 32 + lane] = make_float4(o[nt][0], o[nt][1], o[nt][2], o[nt][3]);
-    sML[wq * 32 + lane] = make_float4(m_lo, m_hi, l_lo, l_hi);
-  }
-  __syncthreads();
-  if (grp == 1) return;
-  {
-    const float4 ml = sML[wq * 32 + lane];
-    const float mn_lo = fmaxf(m_lo, ml.x), mn_hi = fmaxf(m_hi, ml.y);   // finite: one group kept distance 0
-    const float fa_lo = ex2_approx(m_lo - mn_lo), fb_lo = ex2_approx(ml.x - mn_lo);
-    const float fa_hi = ex2_approx(m_hi - mn_hi), fb_hi = ex2_approx(ml.y - mn_hi);
+  if (ok && !abort_flag) {
+    // ---------------- epilogue: O / l (bf16) and LSE
+    const float inv_lo = 1.f / l_lo, inv_hi = 1.f / l_hi;   // l > 0: every query keeps itself
+    const int i_lo = qw + g, i_hi = qw + g + 8;
+    __nv_bfloat16* orow_lo = p.o + (int64_t)s * p.o_sb + (int64_t)i_lo * p.o_sn + (int64_t)h * p.o_sh;
+    __nv_bfloat16* orow_hi = p.o + (int64_t)s * p.o_sb + (int64_t)i_hi * p.o_sn + (int64_t)h * p.o_sh;
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
-      const float4 ob = sO[(wq * 8 + nt) * 32 + lane];
-      o[nt][0] = o[nt][0] * fa_lo + ob.x * fb_lo;
-      o[nt][1] = o[nt][1] * fa_lo + ob.y * fb_lo;
-      o[nt][2] = o[nt][2] * fa_hi + ob.z * fb_hi;
-      o[nt][3] = o[nt][3] * fa_hi + ob.w * fb_hi;
+      const int col = 8 * nt + 2 * t;
+      if (i_lo < p.n_tokens)
+        *reinterpret_cast<uint32_t*>(orow_lo + col) = pack_bf16x2(o[nt][0] * inv_lo, o[nt][1] * inv_lo);
+      if (i_hi < p.n_tokens)
+        *reinterpret_cast<uint32_t*>(orow_hi + col) = pack_bf16x2(o[nt][2] * inv_hi, o[nt][3] * inv_hi);
     }
-    l_lo = l_lo * fa_lo + ml.z * fb_lo;
-    l_hi = l_hi * fa_hi + ml.w * fb_hi;
-    m_lo = mn_lo;
-    m_hi = mn_hi;
+    if (t == 0) {
+      float* lrow = p.lse + ((int64_t)s * p.heads + h) * p.n_tokens;
+      if (i_lo < p.n_tokens) lrow[i_lo] = (m_lo + __log2f(l_lo)) * 0.69314718055994531f;
+      if (i_hi < p.n_tokens) lrow[i_hi] = (m_hi + __log2f(l_hi)) * 0.69314718055994531f;
+    }
   }
-
-  // ---------------- epilogue: O / l (bf16) and LSE
-  const float inv_lo = 1.f / l_lo, inv_hi = 1.f / l_hi;   // l > 0: every query keeps itself
-  const int i_lo = qw + g, i_hi = qw + g + 8;
-  __nv_bfloat16* orow_lo = p.o + (int64_t)s * p.o_sb + (int64_t)i_lo * p.o_sn + (int64_t)h * p.o_sh;
-  __nv_bfloat16* orow_hi = p.o + (int64_t)s * p.o_sb + (int64_t)i_hi * p.o_sn + (int64_t)h * p.o_sh;
-#pragma unroll
-  for (int nt = 0; nt < 8; ++nt) {
-    const int col = 8 * nt + 2 * t;
-    if (i_lo < p.n_tokens)
-      *reinterpret_cast<uint32_t*>(orow_lo + col) = pack_bf16x2(o[nt][0] * inv_lo, o[nt][1] * inv_lo);
-    if (i_hi < p.n_tokens)
-      *reinterpret_cast<uint32_t*>(orow_hi + col) = pack_bf16x2(o[nt][2] * inv_hi, o[nt][3] * inv_hi);
-  }
-  if (t == 0) {
-    float* lrow = p.lse + ((int64_t)s * p.heads + h) * p.n_tokens;
-    if (i_lo < p.n_tokens) lrow[i_lo] = (m_lo + __log2f(l_lo)) * 0.69314718055994531f;
-    if (i_hi < p.n_tokens) lrow[i_hi] = (m_hi + __log2f(l_hi)) * 0.69314718055994531f;
+  // A CTA leaves only with none of its copies in flight: after an abort each warp drains
+  // the slabs it issued and has not waited for, warp 0 the band.
+  __syncthreads();
+  if (abort_flag && lane == 0) {
+    int never = 0;
+    if (warp == 0) mbar_wait(&bar_band, 0, &never, &g_offset_err, kErrTimeout);
+    for (int j = issued - kRing < 0 ? 0 : issued - kRing; j < issued; ++j)
+      mbar_wait(&bar_slab[wq][j % kRing], (uint32_t)(j / kRing) & 1u, &never, &g_offset_err, kErrTimeout);
   }
 }
 
 template <int NKT>
 int launch_nkt(const CUtensorMap& kb, const CUtensorMap& vb, const CUtensorMap& ks, const CUtensorMap& vs,
                const OffParams& p, int batch, cudaStream_t stream) {
-  const size_t smem = 1024 + 2 * (size_t)kBandBytes + 2 * kRingMem * (size_t)kSlabBytes;
+  const size_t smem = 1024 + 2 * (size_t)kBandBytes;
   if (cudaFuncSetAttribute(offset_attn_kernel<NKT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return SA_ERR_CUDA;
@@ -463,9 +403,9 @@ int launch_offset_attn_fwd(const OffsetArgs& a, cudaStream_t stream) {
       !encode_bhnd_map(&vb, a.v, a.batch, a.n_tokens, a.kv_heads, kD, a.kv_strides[0], a.kv_strides[1],
                        a.kv_strides[2], kD, kBandRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_bhnd_map(&ks, a.k, a.batch, a.n_tokens, a.kv_heads, kD, a.kv_strides[0], a.kv_strides[1],
-                       a.kv_strides[2], kD, kQ, CU_TENSOR_MAP_SWIZZLE_128B) ||
+                       a.kv_strides[2], kD, 16, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_bhnd_map(&vs, a.v, a.batch, a.n_tokens, a.kv_heads, kD, a.kv_strides[0], a.kv_strides[1],
-                       a.kv_strides[2], kD, kQ, CU_TENSOR_MAP_SWIZZLE_128B))
+                       a.kv_strides[2], kD, 16, CU_TENSOR_MAP_SWIZZLE_128B))
     return SA_ERR_UNSUPPORTED;
   OffParams p;
   p.n_tokens = a.n_tokens;
