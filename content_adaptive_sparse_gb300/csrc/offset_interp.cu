@@ -3,255 +3,427 @@
 // distance d_k = alpha f_k interpolates between rows i - floor(d_k) and i - floor(d_k) - 1).
 //
 // Entries of query i: window rows i - delta (delta = 0..W) and, for each rung (lo, t) with
-// i - lo - t >= 0, the interpolated key / value (1 - t) x[i - lo] + t x[i - lo - 1]. Since
-// the score is linear in the key, the rung's score is (1 - t) s_lo + t s_lo+1, and its
-// value enters O with weights p (1 - t) and p t.
+// i >= lo + t, the interpolated key / value (1 - t) x[i - lo] + t x[i - lo - 1]. The score is
+// linear in the key, so a rung's score is (1 - t) s_lo + t s_lo+1 with s_delta = q_i . k_{i-delta},
+// and its value enters O with the weights p (1 - t) and p t.
 //
-// The work per entry is a 64-wide dot product and a 64-wide update of O, so the kernel runs
-// on the CUDA cores (paired f32x2 FMAs): four lanes per query row (each lane holds 16 of the
-// 64 head-dimension elements of q and O; two shuffles complete a dot product), 8 consecutive
-// queries of one (sequence, head) per warp, so that the lanes of a warp read neighbouring
-// rows at the same offset. The running max is rescaled lazily (only when it grows by more
-// than 2^8). The rung table (floor distance, weight) is computed on the host from alpha.
+// For 16 consecutive queries each distance is the diagonal of a 16 x 16 block, so the kernel
+// is the integer-offset kernel's design with two diagonals per rung (mma.sync m16n8k16,
+// bf16 -> f32):
+//   * window: the dense 16 x (16 + Dr) block of keys [i0 - Dr, i0 + 16) (Dr = W rounded up
+//     to 16) with a per-lane bit mask of the window distances, from a band of K/V rows
+//     [q0 - 64, q0 + 64) that one TMA load brings in per CTA;
+//   * rungs with lo + 1 <= 64: both diagonals read straight from the band;
+//   * farther rungs: a 17-row K/V slab per warp (rows i0 - lo - 1 .. i0 - lo + 15; query r
+//     takes rows r + 1 and r), streamed by TMA through a two-buffer ring per warp that
+//     reuses the band's memory once every warp is past the band.
+// One CTA of 4 warps per (sequence, head, 64-query tile); warp w owns queries q0 + 16w ..
+// q0 + 16w + 15 and waits on nothing but the band and its own slabs. Softmax: exact max over
+// the window block, then the rungs with a lazily rescaled running max (threshold 2^8).
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "mma_frag.cuh"
+#include "ptx_sm100.cuh"
 #include "sa_internal.h"
+#include "tma_host.h"
 
 namespace sa {
 namespace {
 
+using namespace frag;
+
+__device__ unsigned int g_interp_err;
+
+constexpr int kQ = 64;                     // queries per CTA
+constexpr int kWarps = 4;                  // 16 queries per warp
 constexpr int kD = 64;
-constexpr int kLanesPerQuery = 4;                   // lanes sharing one query row (8 measured slower)
-constexpr int kHalf = kD / kLanesPerQuery;          // head-dimension elements per lane
-constexpr int kQueriesPerWarp = 32 / kLanesPerQuery;
-constexpr int kWarpsPerBlock = 4;
+constexpr int kRowBytes = kD * 2;
+constexpr int kBandMax = 64;               // rungs with lo + 1 <= 64 are read from the band
+constexpr int kBandRows = kQ + kBandMax;   // band rows [q0 - 64, q0 + 64)
+constexpr int kBandBytes = kBandRows * kRowBytes;
+constexpr int kSlabRows = 17;              // rows i0 - lo - 1 .. i0 - lo + 15
+constexpr int kSlabBoxBytes = kSlabRows * kRowBytes;
+constexpr int kSlotBytes = 3072;           // one 17-row K or V slab, 1024-byte aligned slots
+constexpr int kBufBytes = 2 * kSlotBytes;  // K slot, then V slot
+constexpr int kRing = 2;                   // slab buffers per warp
+constexpr int kRingsBytes = kWarps * kRing * kBufBytes;
+constexpr int kSmemMain = kRingsBytes > 2 * kBandBytes ? kRingsBytes : 2 * kBandBytes;
+constexpr int kCtasPerSm = 4;              // 49 KB of shared memory per CTA
+static_assert(kSlabBoxBytes <= kSlotBytes && kSlotBytes % 1024 == 0, "slab slots");
 
 struct InterpParams {
-  int batch, n_tokens, heads, heads_per_kv, window, n_rungs;
-  int lo[kMaxInterpRungs];
-  float t[kMaxInterpRungs];
+  int n_tokens, heads, heads_per_kv, ntiles;
+  int dr;                          // window reach Dr (multiple of 16, <= 64)
+  int n_small;                     // rungs [0, n_small) have lo + 1 <= 64
+  int n_rungs;                     // rungs by ascending distance
+  int lo[kMaxInterpRungs];         // floor of the rung distance
+  float t[kMaxInterpRungs];        // weight of the farther row
+  // per lane: bit 4*nt + e set if score fragment element e of window n-tile nt is at a
+  // distance 0..W (the same for every warp and tile)
+  unsigned long long keep[32];
   const __nv_bfloat16* q;
-  const __nv_bfloat16* k;
-  const __nv_bfloat16* v;
   __nv_bfloat16* o;
   float* lse;
-  int64_t q_sb, q_sn, q_sh, kv_sb, kv_sn, kv_sh, o_sb, o_sn, o_sh;
+  int64_t q_sb, q_sn, q_sh, o_sb, o_sn, o_sh;
   float scale_log2;
-  int tiles;                       // 16-query tiles per (sequence, head)
 };
 
-__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ void f2_unpack(uint64_t v, float& a, float& b) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-// bf16 pair (low element first) -> two floats, exactly
-__device__ __forceinline__ uint64_t bf2_to_f2(uint32_t x) {
-  return f2_pack(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
-}
-__device__ __forceinline__ float ex2_approx(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
+// Online-softmax state of one warp: O fragments, running max (log2 units) and row sums of
+// query rows g and g + 8.
+struct RungState {
+  float o[8][4];
+  float m_lo, m_hi, l_lo, l_hi;
+};
 
-// <q, row> over this lane's half of the head dimension (q held as 16 float pairs), then
-// completed with the partner lane's half
-__device__ __forceinline__ float row_dot(const uint64_t (&q2)[kHalf / 2], const __nv_bfloat16* half_row) {
-  const uint4* r4 = reinterpret_cast<const uint4*>(half_row);
-  uint64_t acc0 = 0ull, acc1 = 0ull;
+// Softmax and PV of one rung from the raw diagonal scores (sa: distance lo, sb: lo + 1) of
+// query rows g and g + 8; va / vb = the value rows of query row 0 at distance lo / lo + 1 in
+// the swizzled tile vt; ok_* = the rung reaches the row.
+__device__ __forceinline__ void enter_rung(RungState& st, float sa_lo, float sa_hi, float sb_lo, float sb_hi,
+                                           float t, bool two, bool ok_lo, bool ok_hi, float c, uint32_t vt,
+                                           int va, int vb, int lane, bool holder, int e_sel) {
+  const float kNegInf = __int_as_float(0xff800000);
+  const float x_lo = ok_lo ? ((1.f - t) * sa_lo + t * sb_lo) * c : kNegInf;
+  const float x_hi = ok_hi ? ((1.f - t) * sa_hi + t * sb_hi) * c : kNegInf;
+  // lazy running max (log2 units): rescale only when a score passes the max by 2^8
+  float a_lo = 1.f, a_hi = 1.f;
+  if (x_lo > st.m_lo + 8.f) { a_lo = ex2_approx(st.m_lo - x_lo); st.m_lo = x_lo; }
+  if (x_hi > st.m_hi + 8.f) { a_hi = ex2_approx(st.m_hi - x_hi); st.m_hi = x_hi; }
+  if (__any_sync(0xffffffffu, a_lo != 1.f || a_hi != 1.f)) {
 #pragma unroll
-  for (int c = 0; c < kHalf / 8; ++c) {
-    const uint4 w = __ldg(r4 + c);
-    acc0 = f2_fma(q2[4 * c + 0], bf2_to_f2(w.x), acc0);
-    acc1 = f2_fma(q2[4 * c + 1], bf2_to_f2(w.y), acc1);
-    acc0 = f2_fma(q2[4 * c + 2], bf2_to_f2(w.z), acc0);
-    acc1 = f2_fma(q2[4 * c + 3], bf2_to_f2(w.w), acc1);
+    for (int nt = 0; nt < 8; ++nt) {
+      st.o[nt][0] *= a_lo;
+      st.o[nt][1] *= a_lo;
+      st.o[nt][2] *= a_hi;
+      st.o[nt][3] *= a_hi;
+    }
+    st.l_lo *= a_lo;
+    st.l_hi *= a_hi;
   }
-  float a, b, c2, d;
-  f2_unpack(acc0, a, b);
-  f2_unpack(acc1, c2, d);
-  float part = (a + b) + (c2 + d);
-#pragma unroll
-  for (int o = 1; o < kLanesPerQuery; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-  return part;
-}
-
-// o += w * row over this lane's half of the head dimension
-__device__ __forceinline__ void row_axpy(uint64_t (&o2)[kHalf / 2], float w, const __nv_bfloat16* half_row) {
-  const uint4* r4 = reinterpret_cast<const uint4*>(half_row);
-  const uint64_t w2 = f2_pack(w, w);
-#pragma unroll
-  for (int c = 0; c < kHalf / 8; ++c) {
-    const uint4 x = __ldg(r4 + c);
-    o2[4 * c + 0] = f2_fma(w2, bf2_to_f2(x.x), o2[4 * c + 0]);
-    o2[4 * c + 1] = f2_fma(w2, bf2_to_f2(x.y), o2[4 * c + 1]);
-    o2[4 * c + 2] = f2_fma(w2, bf2_to_f2(x.z), o2[4 * c + 2]);
-    o2[4 * c + 3] = f2_fma(w2, bf2_to_f2(x.w), o2[4 * c + 3]);
+  const float p_lo = ex2_approx(x_lo - st.m_lo), p_hi = ex2_approx(x_hi - st.m_hi);
+  const uint32_t wa = pack_bf16x2(p_lo * (1.f - t), p_hi * (1.f - t));
+  st.l_lo += __uint_as_float(wa << 16);
+  st.l_hi += __uint_as_float(wa & 0xffff0000u);
+  diag_pv(vt, va, lane, holder, e_sel, wa, st.o);
+  if (two) {
+    const uint32_t wb = pack_bf16x2(p_lo * t, p_hi * t);
+    st.l_lo += __uint_as_float(wb << 16);
+    st.l_hi += __uint_as_float(wb & 0xffff0000u);
+    diag_pv(vt, vb, lane, holder, e_sel, wb, st.o);
   }
 }
 
-__global__ void __launch_bounds__(32 * kWarpsPerBlock) offset_interp_kernel(const __grid_constant__ InterpParams p) {
-  const int warp_global = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  const int part = lane % kLanesPerQuery;          // which part of the head dimension
-  const int per_seq = p.heads * p.tiles;
-  if (warp_global >= p.batch * per_seq) return;    // whole warp
-  const int s = warp_global / per_seq;
-  const int rem = warp_global % per_seq;
-  const int h = rem / p.tiles;
-  const int i_raw = (rem % p.tiles) * kQueriesPerWarp + lane / kLanesPerQuery;
-  // rows past the end repeat the last query (the shuffles need every lane of a group);
-  // they are not stored
-  const bool store = i_raw < p.n_tokens;
-  const int i = store ? i_raw : p.n_tokens - 1;
+template <int NKT>
+__global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
+    offset_interp_kernel(const __grid_constant__ CUtensorMap tk_band, const __grid_constant__ CUtensorMap tv_band,
+                         const __grid_constant__ CUtensorMap tk_slab, const __grid_constant__ CUtensorMap tv_slab,
+                         const __grid_constant__ InterpParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sKb = sm;                        // band K, 16 KB
+  uint8_t* sVb = sKb + kBandBytes;          // band V, 16 KB
+  // once every warp is past the band, warp w's slab ring occupies [w * 12 KB, w * 12 KB + 12 KB):
+  // buffer b at + b * 6 KB, K rows at + 0, V rows at + 3 KB
+  __shared__ uint64_t bar_band, bar_slab[kWarps][kRing];
+  __shared__ int abort_flag;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int wq = warp;
+  const int h = blockIdx.x % p.heads;
+  const int s = blockIdx.x / p.heads;
+  const int tile = p.ntiles - 1 - (int)blockIdx.y;   // later tiles reach more rungs: start them first
+  const int q0 = tile * kQ;
   const int hk = h / p.heads_per_kv;
-  const __nv_bfloat16* kb = p.k + (int64_t)s * p.kv_sb + (int64_t)hk * p.kv_sh + kHalf * part;
-  const __nv_bfloat16* vb = p.v + (int64_t)s * p.kv_sb + (int64_t)hk * p.kv_sh + kHalf * part;
+  const int qw = q0 + 16 * wq;               // first query of this warp
+  // rungs that reach at least one query of this warp (query i needs i >= lo + t, i.e.
+  // i >= lo + 1 when t > 0); the reach is nondecreasing along the ascending rung list
+  int n_reach = 0;
+  while (n_reach < p.n_rungs && p.lo[n_reach] + (p.t[n_reach] > 0.f ? 1 : 0) <= qw + 15) ++n_reach;
+  const int n_small = n_reach < p.n_small ? n_reach : p.n_small;
+  const int n_large = n_reach - n_small;     // slabs of this warp: rungs n_small .. n_reach - 1
 
-  // q pre-scaled by softmax_scale * log2(e): scores come out in log2 units
-  uint64_t q2[kHalf / 2];
+  if (tid == 0) {
+    mbar_init(&bar_band, 1);
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w)
+#pragma unroll
+      for (int b = 0; b < kRing; ++b) mbar_init(&bar_slab[w][b], 1);
+    abort_flag = 0;
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&bar_band, (uint32_t)(2 * kBandBytes));
+  }
+  __syncthreads();
+  if (lane == 0) {
+    if (warp == 0) tma_load_4d(sKb, &tk_band, &bar_band, 0, hk, q0 - kBandMax, s);
+    if (warp == 1) tma_load_4d(sVb, &tv_band, &bar_band, 0, hk, q0 - kBandMax, s);
+  }
+
+  const int g = lane >> 2, t4 = lane & 3;    // mma fragment coordinates: rows g, g+8; cols 2t, 2t+1
+  const float c = p.scale_log2;
+  const float kNegInf = __int_as_float(0xff800000);
+
+  // Q operand straight from global memory (rows past the end read the last row; never stored)
+  uint32_t qa[4][4];
   {
-    const uint4* qr = reinterpret_cast<const uint4*>(p.q + (int64_t)s * p.q_sb + (int64_t)i * p.q_sn +
-                                                     (int64_t)h * p.q_sh + kHalf * part);
-    const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
+    const int last = p.n_tokens - 1;
+    const int i_lo = qw + g < last ? qw + g : last, i_hi = qw + g + 8 < last ? qw + g + 8 : last;
+    const __nv_bfloat16* base = p.q + (int64_t)s * p.q_sb + (int64_t)h * p.q_sh + 16 * t4;
+    const uint4* lo = reinterpret_cast<const uint4*>(base + (int64_t)i_lo * p.q_sn);
+    const uint4* hi = reinterpret_cast<const uint4*>(base + (int64_t)i_hi * p.q_sn);
+    const uint4 a = __ldg(lo), b = __ldg(lo + 1), x = __ldg(hi), y = __ldg(hi + 1);
+    const uint32_t wl[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    const uint32_t wh[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
 #pragma unroll
-    for (int c = 0; c < kHalf / 8; ++c) {
-      const uint4 w = __ldg(qr + c);
-      q2[4 * c + 0] = f2_mul(bf2_to_f2(w.x), sc2);
-      q2[4 * c + 1] = f2_mul(bf2_to_f2(w.y), sc2);
-      q2[4 * c + 2] = f2_mul(bf2_to_f2(w.z), sc2);
-      q2[4 * c + 3] = f2_mul(bf2_to_f2(w.w), sc2);
+    for (int ks = 0; ks < 4; ++ks) {
+      qa[ks][0] = wl[2 * ks];
+      qa[ks][1] = wh[2 * ks];
+      qa[ks][2] = wl[2 * ks + 1];
+      qa[ks][3] = wh[2 * ks + 1];
     }
   }
-  uint64_t o2[kHalf / 2];
-#pragma unroll
-  for (int c = 0; c < kHalf / 2; ++c) o2[c] = 0ull;
-  float m = __int_as_float(0xff800000);   // reference max (log2 units), equal in both lanes
-  float l = 0.f;
 
-  // One entry with score x (log2 units): lazily rescaled online softmax.
-  auto enter = [&](float x) -> float {
-    if (x > m + 8.f) {
-      const float a = ex2_approx(m - x);    // 0 when m = -inf
-      const uint64_t a2 = f2_pack(a, a);
-#pragma unroll
-      for (int c = 0; c < kHalf / 2; ++c) o2[c] = f2_mul(o2[c], a2);
-      l *= a;
-      m = x;
-    }
-    const float pe = ex2_approx(x - m);
-    l += pe;
-    return pe;
-  };
+  // warp-uniform wait results: the fragment code below uses full-warp shuffles
+  bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_band, 0, &abort_flag, &g_interp_err, kErrTimeout));
 
-  // The pair shuffle in row_dot names the whole warp, so every lane must reach it together:
-  // both loops below have warp-uniform trip counts, and entries out of a query's range are
-  // computed on a valid row and then skipped.
-  // window rows i - delta, delta = 0..W (uniform count W + 1; rows below 0 skipped)
-  for (int delta = 0; delta <= p.window; ++delta) {
-    const int j = i - delta;
-    const bool ok = j >= 0;
-    const int jj = ok ? j : 0;
-    const float x = row_dot(q2, kb + (int64_t)jj * p.kv_sn);
-    if (ok) {
-      const float pe = enter(x);
-      row_axpy(o2, pe, vb + (int64_t)jj * p.kv_sn);
+  RungState st;
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt) st.o[nt][0] = st.o[nt][1] = st.o[nt][2] = st.o[nt][3] = 0.f;
+  st.m_lo = st.m_hi = kNegInf;
+  st.l_lo = st.l_hi = 0.f;
+  const int hl = (lane & ~3) | (g >> 1);     // lane of this quad that holds the diagonal
+  const bool holder = (t4 == (g >> 1));
+  const int e_sel = g & 1;                   // which of the two fragment columns is diagonal
+  const int i_lo = qw + g, i_hi = qw + g + 8;
+
+  if (ok) {
+    // ---------------- window: keys [qw - Dr, qw + 16), band row = key - (q0 - 64)
+    uint64_t keep = p.keep[lane];
+    const int lim = p.dr - qw;               // window columns below lim are keys < 0 (first tile only)
+    if (lim > 0) {
+#pragma unroll
+      for (int nt = 0; nt < 2 * NKT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (8 * nt + 2 * t4 + (e & 1) < lim) keep &= ~(1ull << (4 * nt + e));
     }
-  }
-  // interpolated rungs
-  for (int r = 0; r < p.n_rungs; ++r) {
-    const int lo = p.lo[r];
-    const float t = p.t[r];
-    const int far = t > 0.f ? lo + 1 : lo;            // both rows exist iff i >= far
-    const bool ok = i >= far;
-    if (!__any_sync(0xffffffffu, ok)) continue;       // no query of the warp reaches this rung
-    const int64_t r0 = (int64_t)(ok ? i - lo : 0) * p.kv_sn;
-    if (t > 0.f) {
-      const int64_t r1 = (int64_t)(ok ? i - lo - 1 : 0) * p.kv_sn;
-      const float x = (1.f - t) * row_dot(q2, kb + r0) + t * row_dot(q2, kb + r1);
-      if (ok) {
-        const float pe = enter(x);
-        row_axpy(o2, pe * (1.f - t), vb + r0);
-        row_axpy(o2, pe * t, vb + r1);
-      }
-    } else {
-      const float x = row_dot(q2, kb + r0);
-      if (ok) {
-        const float pe = enter(x);
-        row_axpy(o2, pe, vb + r0);
+    const int row0 = 16 * wq + kBandMax - p.dr;
+    const uint32_t kb_tile = smem_u32(sKb), vb_tile = smem_u32(sVb);
+    float sb[2 * NKT][4];
+    float mx_lo = kNegInf, mx_hi = kNegInf;
+#pragma unroll
+    for (int nt = 0; nt < 2 * NKT; ++nt) {
+      uint32_t u[8];
+      load_kfrag(kb_tile, row0 + 8 * nt + g, t4, u);
+      sb[nt][0] = sb[nt][1] = sb[nt][2] = sb[nt][3] = 0.f;
+      qk_ntile(sb[nt], qa, u);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float v = (keep >> (4 * nt + e)) & 1ull ? sb[nt][e] : kNegInf;
+        sb[nt][e] = v;
+        if (e < 2) mx_lo = fmaxf(mx_lo, v);
+        else mx_hi = fmaxf(mx_hi, v);
       }
     }
+    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+    st.m_lo = mx_lo * c;                     // finite: distance 0 is always kept
+    st.m_hi = mx_hi * c;
+    // P = exp2(s c - m); row sums of the bf16 P come from one more MMA against a ones matrix
+    float lsum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < NKT; ++j) {
+      uint32_t pa[4];
+      pa[0] = pack_bf16x2(ex2_approx(fmaf(sb[2 * j][0], c, -st.m_lo)), ex2_approx(fmaf(sb[2 * j][1], c, -st.m_lo)));
+      pa[1] = pack_bf16x2(ex2_approx(fmaf(sb[2 * j][2], c, -st.m_hi)), ex2_approx(fmaf(sb[2 * j][3], c, -st.m_hi)));
+      pa[2] = pack_bf16x2(ex2_approx(fmaf(sb[2 * j + 1][0], c, -st.m_lo)),
+                          ex2_approx(fmaf(sb[2 * j + 1][1], c, -st.m_lo)));
+      pa[3] = pack_bf16x2(ex2_approx(fmaf(sb[2 * j + 1][2], c, -st.m_hi)),
+                          ex2_approx(fmaf(sb[2 * j + 1][3], c, -st.m_hi)));
+      mma16816(lsum, pa, kOnesBf16x2, kOnesBf16x2);
+      uint32_t vbf[4][4];
+      load_v16(vb_tile, row0 + 16 * j, lane, vbf);
+      pv_16(st.o, pa, vbf);
+    }
+    st.l_lo = lsum[0];
+    st.l_hi = lsum[2];
+
+    // ---------------- near rungs: both rows in the band (query r: band rows ra + r, ra - 1 + r)
+    for (int k = 0; k < n_small; ++k) {
+      const int lo = p.lo[k];
+      const float t = p.t[k];
+      const bool two = t > 0.f;                // warp-uniform
+      const int far = lo + (two ? 1 : 0);
+      const int ra = 16 * wq + kBandMax - lo;  // >= 1 since lo <= 63
+      float sa_lo, sa_hi, sb_lo = 0.f, sb_hi = 0.f;
+      diag_scores(kb_tile, ra, g, t4, hl, e_sel, qa, sa_lo, sa_hi);
+      if (two) diag_scores(kb_tile, ra - 1, g, t4, hl, e_sel, qa, sb_lo, sb_hi);
+      enter_rung(st, sa_lo, sa_hi, sb_lo, sb_hi, t, two, i_lo >= far, i_hi >= far, c, vb_tile, ra, ra - 1, lane,
+                 holder, e_sel);
+    }
   }
 
-  // the self row is always an entry, so l > 0
-  const float inv = 1.f / l;
-  uint32_t pk[kHalf / 2];
-#pragma unroll
-  for (int c = 0; c < kHalf / 2; ++c) {
-    float a, b;
-    f2_unpack(o2[c], a, b);
-    __nv_bfloat162 hv = __floats2bfloat162_rn(a * inv, b * inv);
-    pk[c] = *reinterpret_cast<uint32_t*>(&hv);
+  // The band is read: its memory becomes the warps' slab rings.
+  __syncthreads();
+  uint8_t* ring = sm + wq * (kRing * kBufBytes);
+  int issued = 0;
+  if (lane == 0 && !abort_flag) {
+    for (; issued < kRing && issued < n_large; ++issued) {
+      const int lo = p.lo[n_small + issued];
+      uint8_t* dst = ring + issued * kBufBytes;
+      mbar_arrive_expect_tx(&bar_slab[wq][issued], (uint32_t)(2 * kSlabBoxBytes));
+      tma_load_4d(dst, &tk_slab, &bar_slab[wq][issued], 0, hk, qw - lo - 1, s);
+      tma_load_4d(dst + kSlotBytes, &tv_slab, &bar_slab[wq][issued], 0, hk, qw - lo - 1, s);
+    }
   }
-  if (!store) return;
-  uint4* orow = reinterpret_cast<uint4*>(p.o + (int64_t)s * p.o_sb + (int64_t)i * p.o_sn + (int64_t)h * p.o_sh +
-                                         kHalf * part);
+  ok = ok && !abort_flag;
+
+  // ---------------- far rungs: slab row r + 1 is distance lo of query r, slab row r distance lo + 1
+  for (int j = 0; j < n_large && ok; ++j) {
+    const int b = j % kRing;
+    ok = __all_sync(0xffffffffu, mbar_wait(&bar_slab[wq][b], (uint32_t)(j / kRing) & 1u, &abort_flag,
+                                           &g_interp_err, kErrTimeout));
+    if (!ok) break;
+    const int k = n_small + j;
+    const int lo = p.lo[k];
+    const float t = p.t[k];
+    const bool two = t > 0.f;
+    const int far = lo + (two ? 1 : 0);
+    const uint32_t kt = smem_u32(ring + b * kBufBytes);
+    float sa_lo, sa_hi, sb_lo = 0.f, sb_hi = 0.f;
+    diag_scores(kt, 1, g, t4, hl, e_sel, qa, sa_lo, sa_hi);
+    if (two) diag_scores(kt, 0, g, t4, hl, e_sel, qa, sb_lo, sb_hi);
+    enter_rung(st, sa_lo, sa_hi, sb_lo, sb_hi, t, two, i_lo >= far, i_hi >= far, c, kt + kSlotBytes, 1, 0, lane,
+               holder, e_sel);
+    // every lane has read the buffer: refill it with the slab kRing ahead
+    __syncwarp();
+    if (lane == 0 && issued < n_large && !abort_flag) {
+      const int lo2 = p.lo[n_small + issued];
+      uint8_t* dst = ring + b * kBufBytes;
+      mbar_arrive_expect_tx(&bar_slab[wq][b], (uint32_t)(2 * kSlabBoxBytes));
+      tma_load_4d(dst, &tk_slab, &bar_slab[wq][b], 0, hk, qw - lo2 - 1, s);
+      tma_load_4d(dst + kSlotBytes, &tv_slab, &bar_slab[wq][b], 0, hk, qw - lo2 - 1, s);
+      ++issued;
+    }
+  }
+
+  if (ok && !abort_flag) {
+    // ---------------- epilogue: O / l (bf16) and LSE
+    const float inv_lo = 1.f / st.l_lo, inv_hi = 1.f / st.l_hi;   // l > 0: every query keeps itself
+    __nv_bfloat16* orow_lo = p.o + (int64_t)s * p.o_sb + (int64_t)i_lo * p.o_sn + (int64_t)h * p.o_sh;
+    __nv_bfloat16* orow_hi = p.o + (int64_t)s * p.o_sb + (int64_t)i_hi * p.o_sn + (int64_t)h * p.o_sh;
 #pragma unroll
-  for (int c = 0; c < kHalf / 8; ++c) orow[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-  if (part == 0) p.lse[((int64_t)s * p.heads + h) * p.n_tokens + i] = (m + __log2f(l)) * 0.69314718055994531f;
+    for (int nt = 0; nt < 8; ++nt) {
+      const int col = 8 * nt + 2 * t4;
+      if (i_lo < p.n_tokens)
+        *reinterpret_cast<uint32_t*>(orow_lo + col) = pack_bf16x2(st.o[nt][0] * inv_lo, st.o[nt][1] * inv_lo);
+      if (i_hi < p.n_tokens)
+        *reinterpret_cast<uint32_t*>(orow_hi + col) = pack_bf16x2(st.o[nt][2] * inv_hi, st.o[nt][3] * inv_hi);
+    }
+    if (t4 == 0) {
+      float* lrow = p.lse + ((int64_t)s * p.heads + h) * p.n_tokens;
+      if (i_lo < p.n_tokens) lrow[i_lo] = (st.m_lo + __log2f(st.l_lo)) * 0.69314718055994531f;
+      if (i_hi < p.n_tokens) lrow[i_hi] = (st.m_hi + __log2f(st.l_hi)) * 0.69314718055994531f;
+    }
+  }
+  // A CTA leaves only with none of its copies in flight: after an abort each warp drains
+  // the slabs it issued and has not waited for, warp 0 the band.
+  __syncthreads();
+  if (abort_flag && lane == 0) {
+    int never = 0;
+    if (warp == 0) mbar_wait(&bar_band, 0, &never, &g_interp_err, kErrTimeout);
+    for (int j = issued - kRing < 0 ? 0 : issued - kRing; j < issued; ++j)
+      mbar_wait(&bar_slab[wq][j % kRing], (uint32_t)(j / kRing) & 1u, &never, &g_interp_err, kErrTimeout);
+  }
+}
+
+template <int NKT>
+int launch_nkt(const CUtensorMap& kb, const CUtensorMap& vb, const CUtensorMap& ks, const CUtensorMap& vs,
+               const InterpParams& p, int batch, cudaStream_t stream) {
+  const size_t smem = 1024 + (size_t)kSmemMain;
+  if (cudaFuncSetAttribute(offset_interp_kernel<NKT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
+    return SA_ERR_CUDA;
+  dim3 grid((unsigned)(batch * p.heads), (unsigned)p.ntiles);
+  offset_interp_kernel<NKT><<<grid, kWarps * 32, smem, stream>>>(kb, vb, ks, vs, p);
+  return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
 }  // namespace
 
 int launch_offset_interp_fwd(const InterpArgs& a, cudaStream_t stream) {
+  if (a.window < 0 || a.window > kBandMax || a.n_rungs < 0 || a.n_rungs > kMaxInterpRungs) return SA_ERR_UNSUPPORTED;
+  if ((int64_t)a.batch * a.heads > 0x7fffffff || (a.n_tokens + kQ - 1) / kQ > 65535) return SA_ERR_UNSUPPORTED;
+  CUtensorMap kb, vb, ks, vs;
+  if (!encode_bhnd_map(&kb, a.k, a.batch, a.n_tokens, a.kv_heads, kD, a.kv_strides[0], a.kv_strides[1],
+                       a.kv_strides[2], kD, kBandRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_bhnd_map(&vb, a.v, a.batch, a.n_tokens, a.kv_heads, kD, a.kv_strides[0], a.kv_strides[1],
+                       a.kv_strides[2], kD, kBandRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_bhnd_map(&ks, a.k, a.batch, a.n_tokens, a.kv_heads, kD, a.kv_strides[0], a.kv_strides[1],
+                       a.kv_strides[2], kD, kSlabRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_bhnd_map(&vs, a.v, a.batch, a.n_tokens, a.kv_heads, kD, a.kv_strides[0], a.kv_strides[1],
+                       a.kv_strides[2], kD, kSlabRows, CU_TENSOR_MAP_SWIZZLE_128B))
+    return SA_ERR_UNSUPPORTED;
   InterpParams p;
-  p.batch = a.batch;
   p.n_tokens = a.n_tokens;
   p.heads = a.heads;
   p.heads_per_kv = a.heads / a.kv_heads;
-  p.window = a.window;
+  p.ntiles = (a.n_tokens + kQ - 1) / kQ;
+  p.dr = (a.window + 15) / 16 * 16;
+  const int nkt = (16 + p.dr) / 16;
+  // rungs: ascending distance, the near ones (lo + 1 <= 64) first
   p.n_rungs = a.n_rungs;
+  p.n_small = 0;
   for (int r = 0; r < kMaxInterpRungs; ++r) {
     p.lo[r] = r < a.n_rungs ? a.lo[r] : 0;
     p.t[r] = r < a.n_rungs ? a.t[r] : 0.f;
   }
+  for (int r = 0; r < a.n_rungs; ++r) {
+    if (r > 0 && (a.lo[r] < a.lo[r - 1] || (a.lo[r] == a.lo[r - 1] && a.t[r] < a.t[r - 1]))) return SA_ERR_UNSUPPORTED;
+    if (a.lo[r] < 0 || !(a.t[r] >= 0.f && a.t[r] <= 1.f)) return SA_ERR_INVALID_ARG;
+    if (a.lo[r] + 1 <= kBandMax) p.n_small = r + 1;
+  }
+  // lane (g, t) holds score elements (row g + 8(e>>1), window column 8 nt + 2t + (e&1));
+  // window column col of row rr is at distance rr + Dr - col
+  for (int lane = 0; lane < 32; ++lane) {
+    const int g = lane >> 2, t = lane & 3;
+    unsigned long long bits = 0ull;
+    for (int nt = 0; nt < 2 * nkt; ++nt)
+      for (int e = 0; e < 4; ++e) {
+        const int rr = g + 8 * (e >> 1), col = 8 * nt + 2 * t + (e & 1);
+        const int dist = rr + p.dr - col;
+        if (dist >= 0 && dist <= a.window) bits |= 1ull << (4 * nt + e);
+      }
+    p.keep[lane] = bits;
+  }
   p.q = static_cast<const __nv_bfloat16*>(a.q);
-  p.k = static_cast<const __nv_bfloat16*>(a.k);
-  p.v = static_cast<const __nv_bfloat16*>(a.v);
   p.o = static_cast<__nv_bfloat16*>(a.o);
   p.lse = a.lse;
   p.q_sb = a.q_strides[0];
   p.q_sn = a.q_strides[1];
   p.q_sh = a.q_strides[2];
-  p.kv_sb = a.kv_strides[0];
-  p.kv_sn = a.kv_strides[1];
-  p.kv_sh = a.kv_strides[2];
   p.o_sb = a.o_strides[0];
   p.o_sn = a.o_strides[1];
   p.o_sh = a.o_strides[2];
   p.scale_log2 = a.softmax_scale * 1.4426950408889634f;
-  p.tiles = (a.n_tokens + kQueriesPerWarp - 1) / kQueriesPerWarp;
-  const int64_t warps = (int64_t)a.batch * a.heads * p.tiles;
-  const int64_t blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
-  if (blocks > INT32_MAX) return SA_ERR_UNSUPPORTED;
-  offset_interp_kernel<<<(unsigned)blocks, 32 * kWarpsPerBlock, 0, stream>>>(p);
-  return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+  switch (nkt) {
+    case 1: return launch_nkt<1>(kb, vb, ks, vs, p, a.batch, stream);
+    case 2: return launch_nkt<2>(kb, vb, ks, vs, p, a.batch, stream);
+    case 3: return launch_nkt<3>(kb, vb, ks, vs, p, a.batch, stream);
+    case 4: return launch_nkt<4>(kb, vb, ks, vs, p, a.batch, stream);
+    default: return launch_nkt<5>(kb, vb, ks, vs, p, a.batch, stream);
+  }
+}
+
+unsigned int interp_read_and_clear_error(cudaStream_t stream) {
+  unsigned int v = 0, zero = 0;
+  cudaMemcpyFromSymbolAsync(&v, g_interp_err, sizeof(v), 0, cudaMemcpyDeviceToHost, stream);
+  cudaMemcpyToSymbolAsync(g_interp_err, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, stream);
+  cudaStreamSynchronize(stream);
+  return v;
 }
 
 }  // namespace sa

@@ -586,7 +586,7 @@ int sa_device_status(void* stream) {
   cudaMemcpyFromSymbolAsync(&self, g_selftest_err, sizeof(self), 0, cudaMemcpyDeviceToHost, s);
   cudaMemcpyToSymbolAsync(g_selftest_err, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, s);
   const unsigned int e = sa::attn_read_and_clear_error(s) | sa::offset_read_and_clear_error(s) |
-                         sa::bwd_read_and_clear_error(s) | self;
+                         sa::interp_read_and_clear_error(s) | sa::bwd_read_and_clear_error(s) | self;
   if (cudaGetLastError() != cudaSuccess) return SA_ERR_CUDA;
   if (e & sa::kErrTimeout) return SA_ERR_TIMEOUT;
   if (e & sa::kErrBadIndex) return SA_ERR_DEVICE;

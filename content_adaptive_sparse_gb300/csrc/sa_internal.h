@@ -87,6 +87,7 @@ struct InterpArgs {
   float softmax_scale;
 };
 int launch_offset_interp_fwd(const InterpArgs& a, cudaStream_t stream);
+unsigned int interp_read_and_clear_error(cudaStream_t stream);
 
 // attn_bwd.cu
 struct BwdArgs {
