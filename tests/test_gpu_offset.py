@@ -192,9 +192,20 @@ def test_interp_fib_8k_sampled():
     assert_attention_close(o_g, l_g, o_ref, lse_ref, "interp fib 8k")
 
 
+def test_interp_band_boundary_and_wide_windows():
+    """Rungs just inside and just past the 64-row band (floor distance 63 and 64, with and
+    without a fractional part), and windows that need three to five 16-key steps."""
+    _run_interp(1, 600, 2, 2, 8, 0.99, ladder=1, n_rungs=8, seed=41)      # 64 x 0.99 = 63.36
+    _run_interp(1, 600, 2, 2, 8, 1.01, ladder=1, n_rungs=8, seed=42)      # 64.64
+    _run_interp(1, 600, 2, 1, 8, 63 / 64, ladder=1, n_rungs=8, seed=43)   # 63.0 and 126.0
+    _run_interp(1, 600, 2, 2, 8, 1.0, ladder=1, n_rungs=9, seed=44)       # 64.0, 128.0, 256.0
+    _run_interp(1, 777, 2, 2, 40, 0.73, seed=45, qmul=2.0)
+    _run_interp(2, 500, 2, 1, 64, 1.3, n_rungs=0, seed=46)
+
+
 def test_interp_ragged_length_and_tiny_sequences():
-    """Lengths that are not multiples of the 8-query warp tile, and sequences shorter than
-    the first rung."""
+    """Lengths that are not multiples of the 16-query warp tile or the 64-query CTA tile, and
+    sequences shorter than the first rung."""
     _run_interp(2, 1003, 2, 1, 8, 0.6180, seed=31, qmul=2.0)
     _run_interp(1, 7, 1, 1, 3, 1.7, seed=32)
     _run_interp(1, 1, 1, 1, 0, 0.9, seed=33)
