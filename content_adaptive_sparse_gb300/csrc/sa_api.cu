@@ -379,7 +379,8 @@ int sa_offset_attn_fwd(const void* q, const void* k, const void* v, const int64_
     if (h_offsets[i] <= window || h_offsets[i] >= n_tokens) return SA_ERR_INVALID_ARG;
     if (i > 0 && h_offsets[i] <= h_offsets[i - 1]) return SA_ERR_INVALID_ARG;
   }
-  if ((int64_t)batch * heads > 65535 * 32 || (n_tokens + 127) / 128 > 65535) return SA_ERR_UNSUPPORTED;
+  // grid: (batch x heads, 64-query tiles)
+  if ((int64_t)batch * heads > 0x7fffffff || (n_tokens + 63) / 64 > 65535) return SA_ERR_UNSUPPORTED;
   if (!device_ok()) return SA_ERR_CUDA;
   sa::OffsetArgs a;
   a.q = q;
@@ -481,7 +482,8 @@ int sa_offset_attn_interp_fwd(const void* q, const void* k, const void* v, const
     }
     if (f > ((int64_t)1 << 40)) break;
   }
-  if ((int64_t)batch * heads * ((n_tokens + 31) / 32) > (int64_t)INT32_MAX * 4) return SA_ERR_UNSUPPORTED;
+  // grid: (batch x heads, 64-query tiles)
+  if ((int64_t)batch * heads > 0x7fffffff || (n_tokens + 63) / 64 > 65535) return SA_ERR_UNSUPPORTED;
   if (!device_ok()) return SA_ERR_CUDA;
   a.q = q;
   a.k = k;
