@@ -210,7 +210,10 @@ int sa_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void*
  *   { i - delta : delta in {0, ..., window} u offsets, i - delta >= 0 }   (a set).
  *   h_offsets : host int32[n_offsets], strictly ascending, each > window and
  *               < n_tokens (see sa_fib_offsets); n_offsets <= 64.
- *   window in [0, 64]; head_dim == 64; other arguments as in sa_attn_fwd. */
+ *   window in [0, 64]; head_dim == 64; n_tokens <= 65535 * 64 and batch * heads < 2^31
+ *   (else SA_ERR_UNSUPPORTED); other arguments as in sa_attn_fwd. The kernel's copy waits
+ *   are bounded: an expired wait leaves O and LSE incomplete and is reported by
+ *   sa_device_status as SA_ERR_TIMEOUT. */
 int sa_offset_attn_fwd(const void* q, const void* k, const void* v, const int64_t q_strides[3],
                        const int64_t kv_strides[3], const int64_t o_strides[3], int32_t batch, int32_t n_tokens,
                        int32_t heads, int32_t kv_heads, int32_t head_dim, int32_t window, const int32_t* h_offsets,
@@ -226,7 +229,8 @@ int sa_offset_attn_fwd(const void* q, const void* k, const void* v, const int64_
  *   value (1 - t) v[i - lo] + t v[i - lo - 1]
  * (a rung with an integer distance inside the window is the window row itself and is not
  * counted twice). head_dim == 64; window in [0, 64]; at most 64 rungs remain; other
- * arguments as in sa_offset_attn_fwd. alpha must be finite and > 0. */
+ * arguments, size limits and the bounded-wait report as in sa_offset_attn_fwd. alpha must
+ * be finite and > 0. */
 int sa_offset_attn_interp_fwd(const void* q, const void* k, const void* v, const int64_t q_strides[3],
                               const int64_t kv_strides[3], const int64_t o_strides[3], int32_t batch,
                               int32_t n_tokens, int32_t heads, int32_t kv_heads, int32_t head_dim, int32_t window,
