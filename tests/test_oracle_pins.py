@@ -204,6 +204,60 @@ def test_bigbird_random_draws_distinct_and_valid():
             assert len(row) == len(set(om.bigbird_window(I, wb, nb)) | set(range(gb))) + rb
 
 
+def _chi2_sf(stat: float, dof: int) -> float:
+    scipy_stats = pytest.importorskip("scipy.stats")
+    return float(scipy_stats.chi2.sf(stat, dof))
+
+
+@pytest.mark.parametrize("seed,rb", [(45, 1), (7, 1), (45, 3)])
+def test_bigbird_random_draws_are_uniform(seed, rb):
+    """[BB] section 2: the random blocks are drawn uniformly among the blocks outside the
+    window and the globals. Over 4096 rows the position of every drawn block within its
+    row's candidate list A(I), scaled to [0, 1), must be uniform (a chi-square test on 20
+    bins), and so must the drawn block indices themselves, against the expected count
+    sum_I |A(I) n bin| / |A(I)| of each of 16 index bins. A biased index map (a shift too
+    many, a modulo of the low word, the draw taken from the full row) fails one of them."""
+    nb, wb, gb = 4096, 8, 1
+    rows = om.csr_bigbird_rows(nb, wb, gb, rb, seed)
+    pos_bins = np.zeros(20)
+    idx_obs = np.zeros(16)
+    idx_exp = np.zeros(16)
+    edges = np.linspace(0, nb, 17)
+    for I in range(gb, nb):
+        W = set(om.bigbird_window(I, wb, nb))
+        A = [J for J in range(nb) if J not in W and J >= gb]
+        drawn = [J for J in rows[I] if J not in W and J >= gb]
+        assert len(drawn) == rb
+        for J in drawn:
+            u = A.index(J) / len(A)
+            pos_bins[min(19, int(u * 20))] += 1
+            idx_obs[min(15, int(J * 16 // nb))] += 1
+        counts, _ = np.histogram(A, bins=edges)
+        idx_exp += rb * counts / len(A)
+    exp_pos = pos_bins.sum() / 20
+    stat_pos = float(((pos_bins - exp_pos) ** 2 / exp_pos).sum())
+    stat_idx = float(((idx_obs - idx_exp) ** 2 / idx_exp).sum())
+    assert _chi2_sf(stat_pos, 19) > 1e-3, (stat_pos, pos_bins)
+    assert _chi2_sf(stat_idx, 15) > 1e-3, (stat_idx, idx_obs, idx_exp)
+
+
+def test_bigbird_uniformity_test_rejects_a_biased_draw(monkeypatch):
+    """The chi-square statistic above does detect a plausible mistake: an index map that
+    drops one bit (draws only from the first half of A) is rejected."""
+    nb, wb, gb = 4096, 8, 1
+    real = om.philox_word
+    monkeypatch.setattr(om, "philox_word", lambda seed, p: real(seed, p) >> 1)
+    rows = om.csr_bigbird_rows(nb, wb, gb, 1, 45)
+    pos_bins = np.zeros(20)
+    for I in range(gb, nb):
+        W = set(om.bigbird_window(I, wb, nb))
+        A = [J for J in range(nb) if J not in W and J >= gb]
+        J = [J for J in rows[I] if J not in W and J >= gb][0]
+        pos_bins[min(19, int(A.index(J) / len(A) * 20))] += 1
+    exp_pos = pos_bins.sum() / 20
+    assert _chi2_sf(float(((pos_bins - exp_pos) ** 2 / exp_pos).sum()), 19) < 1e-6
+
+
 def test_bigbird_dense_special_case():
     nb = 10
     rows = om.csr_bigbird_rows(nb, 2 * nb, 1, 2, seed=1)
