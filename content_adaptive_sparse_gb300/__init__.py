@@ -220,16 +220,18 @@ def attn_bwd_heads(q, k, v, o, lse, d_o, csrs, head_mask, block: int, causal: in
 
 
 def sa_attn_bwd_noalloc(q, k, v, o, d_o, lse, row_ptr, col_idx, block: int, causal: int, dq, dk, dv,
-                        csr_shared: bool = False, softmax_scale: float | None = None, stream=None) -> None:
-    """sa_attn_bwd with the library's own scratch (no workspace argument)."""
+                        csr_shared: bool = False, softmax_scale: float | None = None, stream=None,
+                        col_capacity: int | None = None) -> None:
+    """sa_attn_bwd for callers that cannot allocate: the scratch is the library's own
+    (no workspace argument). ``col_capacity`` defaults to the size of ``col_idx``."""
     b, n, h, d = q.shape
     hkv = k.shape[2]
     scale = 1.0 / float(np.sqrt(d)) if softmax_scale is None else float(softmax_scale)
+    cap = col_idx.numel() if col_capacity is None else int(col_capacity)
     _check("sa_attn_bwd_noalloc", load_library().sa_attn_bwd_noalloc(
         q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), d_o.data_ptr(), lse.data_ptr(), _strides(q),
         _strides(k), _strides(o), b, n, h, hkv, d, block, int(causal), row_ptr.data_ptr(), col_idx.data_ptr(),
-        col_idx.numel(), int(bool(csr_shared)), scale, dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-        _stream_ptr(stream)))
+        cap, int(bool(csr_shared)), scale, dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), _stream_ptr(stream)))
 
 
 def sa_offset_attn_fwd(q, k, v, window: int, offsets, o, lse, softmax_scale: float | None = None,

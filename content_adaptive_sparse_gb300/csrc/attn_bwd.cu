@@ -32,6 +32,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "csr_union.cuh"
 #include "ptx_sm100.cuh"
 #include "sa_internal.h"
@@ -74,6 +76,10 @@ struct BCfg {
   static constexpr int SMEM = SMEM_NEED > 80 * 1024 ? SMEM_NEED : 80 * 1024;
   static constexpr uint32_t TMEM_DQ = 256;
   static constexpr uint32_t TMEM_DKDV = 128 + 2 * D <= 256 ? 256 : 512;
+  // Occupancy: at d <= 64 two CTAs share an SM (256 TMEM columns each). At d = 128 the dK/dV
+  // kernel takes all 512 columns, and its shared memory alone already keeps a second CTA off
+  // the SM, so no CTA ever waits in tcgen05.alloc for another one's columns.
+  static_assert(TMEM_DKDV == 256 || 2 * SMEM > 227 * 1024, "a 512-column CTA must have the SM to itself");
   static_assert(STAGES <= kMaxStages, "ring size");
 };
 
@@ -1119,10 +1125,24 @@ int launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
 }
 
 // Scratch of the no-allocation entry point: D and the transposed CSR of one call at a time.
+// Every device that loads the library holds one copy of it until the process exits.
 static __device__ __align__(256) uint8_t g_bwd_static_scratch[kBwdStaticScratchBytes];
 
+// The array's name is only a host-side stand-in for it; the device address of each device's
+// copy is looked up once, by the first call made with that device current, and kept here.
+constexpr int kMaxScratchDevices = 64;
+std::atomic<void*> g_bwd_scratch_addr[kMaxScratchDevices];
+
 int bwd_static_scratch(void** ptr) {
-  return cudaGetSymbolAddress(ptr, g_bwd_static_scratch) == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxScratchDevices) return SA_ERR_CUDA;
+  void* addr = g_bwd_scratch_addr[dev].load(std::memory_order_acquire);
+  if (addr == nullptr) {
+    if (cudaGetSymbolAddress(&addr, g_bwd_static_scratch) != cudaSuccess || addr == nullptr) return SA_ERR_CUDA;
+    g_bwd_scratch_addr[dev].store(addr, std::memory_order_release);
+  }
+  *ptr = addr;
+  return SA_OK;
 }
 
 unsigned int bwd_read_and_clear_error(cudaStream_t stream) {

@@ -193,11 +193,26 @@ int sa_attn_bwd_heads(const void* q, const void* k, const void* v, const void* o
                       const int32_t* h_head_mask, int32_t csr_shared, float softmax_scale, void* dq, void* dk,
                       void* dv, void* workspace, size_t workspace_bytes, void* stream);
 
-/* sa_attn_bwd without a caller workspace: the scratch lives in a 16 MiB array inside the
- * library (one per device), so the call allocates nothing. col_capacity bounds the CSR's
- * entries as in sa_attn_bwd_workspace_size; if the scratch that needs exceeds 16 MiB the
- * call returns SA_ERR_CAPACITY before any launch. The scratch is shared: calls must not
- * overlap in time (serialise them on one stream, or synchronise between streams). */
+/* sa_attn_bwd for callers that cannot allocate device memory. The pages have no
+ * counterpart of this call; it exists for the library's users. Some callers must not call
+ * cudaMalloc at this point: a plugin whose host application owns every device allocation,
+ * a service that allocates only at start-up so that its memory use stays fixed, or a
+ * latency-bound caller for whom cudaMalloc's implicit device synchronisation is too costly.
+ * This call needs no workspace from them: its scratch (D and the transposed CSR) is a
+ * 16 MiB array inside the library, of which every device that loads the library holds one
+ * copy until the process exits. The call itself allocates nothing.
+ *   col_capacity : entries the CSR may hold, as in sa_attn_bwd_workspace_size. If the
+ *                  scratch for these shapes exceeds 16 MiB the call returns
+ *                  SA_ERR_CAPACITY before any launch. A col_capacity below the CSR's real
+ *                  entry count is not seen on the host: the kernels clamp the transposed
+ *                  lists to it (dK and dV are then incomplete) and only sa_device_status
+ *                  reports it, as SA_ERR_CAPACITY.
+ *   The first call on a device looks up that device's copy of the array (with the device
+ *   current) and keeps its address; make that first call before any stream capture.
+ *   Every call shares the one array, which keeps the previous call's contents (the call
+ *   rewrites every part it reads). Calls that overlap on the GPU race on it: serialise
+ *   them on one stream, or synchronise between streams.
+ * Every other argument, and the outputs, as in sa_attn_bwd. */
 int sa_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* d_o, const float* lse,
                         const int64_t q_strides[3], const int64_t kv_strides[3], const int64_t o_strides[3],
                         int32_t batch, int32_t n_tokens, int32_t heads, int32_t kv_heads, int32_t head_dim,
@@ -269,10 +284,14 @@ int sa_layer_alpha(int32_t layer, int32_t layers, int32_t lo_num, int32_t lo_den
 int sa_block_ratios(const uint8_t* h_bytes, int32_t batch, int32_t n_tokens, int32_t block, int32_t level,
                     float* h_ratio, int32_t n_threads);
 
-/* Synchronises `stream`, then reads and clears the library's device error word.
+/* Synchronises `stream`, then reads and clears the library's device error words.
  * Returns SA_OK, SA_ERR_TIMEOUT (a bounded wait expired; the kernel unwound and its
  * outputs are undefined), SA_ERR_DEVICE (invalid CSR data was skipped) or
- * SA_ERR_CAPACITY (a device-sized structure did not fit the caller's workspace). */
+ * SA_ERR_CAPACITY (a device-sized structure did not fit the caller's workspace).
+ * The error words belong to the current device, not to a stream: every launch on any
+ * stream of the device sets them, and this call clears them. To attribute an error to
+ * the right calls, synchronise every stream that launched library work before calling
+ * it. */
 int sa_device_status(void* stream);
 
 /* Self-test of the failure path: launches a one-thread kernel that waits on a barrier

@@ -136,32 +136,6 @@ def test_backward_is_deterministic():
         assert torch.equal(x, y)
 
 
-def test_noalloc_entry_point_matches_workspace_call():
-    """sa_attn_bwd_noalloc (library scratch) gives the same bits as sa_attn_bwd with a
-    caller workspace, and both match the oracle."""
-    torch = torch_cuda()
-    n, b, bt, h = 1024, 64, 2, 4
-    rng = np.random.default_rng(31)
-    ratios = (rng.integers(20, 80, (bt, n // b)) / np.float32(b)).astype(np.float32)
-    p = om.MaskParams("topk", b, n, 1, 2, 1, 3)
-    qb, kb, vb, dob = (bf16_normal_bits(rng, (bt, n, h, 64), 0.3) for _ in range(4))
-    rp_d, ci_d = _mask_on_gpu(p, bt, ratios)
-    q, k, v, do = (to_dev(x) for x in (qb, kb, vb, dob))
-    o, lse = sa.attn_fwd(q, k, v, rp_d, ci_d, b, 1)
-    dq1, dk1, dv1 = sa.attn_bwd(q, k, v, o, lse, do, rp_d, ci_d, b, 1)
-    dq2, dk2, dv2 = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    sa.sa_attn_bwd_noalloc(q, k, v, o, do, lse, rp_d, ci_d, b, 1, dq2, dk2, dv2)
-    torch.cuda.synchronize()
-    assert sa.sa_device_status() == 0
-    assert torch.equal(dq1, dq2) and torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
-    rp_o, ci_o = om.build_csr(p, ratios, bt)
-    f = bf16_bits_to_f64
-    rq, rk, rv = oracle.attention_csr_backward(f(qb), f(kb), f(vb), f(dob), rp_o, ci_o, b, 1)
-    assert_grad_close(bf16_to_f64(dq2), rq, "dQ noalloc")
-    assert_grad_close(bf16_to_f64(dk2), rk, "dK noalloc")
-    assert_grad_close(bf16_to_f64(dv2), rv, "dV noalloc")
-
-
 # ---------------------------------------------------------------- full-size workload, sampled rows
 
 def test_bytelm_topk_8k_sampled_and_invariants():
