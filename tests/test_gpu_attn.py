@@ -174,62 +174,7 @@ def test_bad_csr_index_is_reported():
     assert sa.sa_device_status() == 0          # the status word was cleared
 
 
-# ---------------------------------------------------------------- full-size workloads, sampled outputs
-
-def _samples(rng, bt, n, h, k=48, extra=()):
-    out = [(int(rng.integers(bt)), int(rng.integers(n)), int(rng.integers(h))) for _ in range(k)]
-    return out + list(extra)
-
-
-def _full_size(cfg, p, csr_batch, ratios_gpu, ratios_oracle, samples_extra=()):
-    torch = torch_cuda()
-    qb, kb, vb = qkv_bits(cfg)
-    rp_d, ci_d = _mask_on_gpu(p, csr_batch, ratios_gpu)
-    o, lse = sa.attn_fwd(to_dev(qb), to_dev(kb), to_dev(vb), rp_d, ci_d, p.block, p.causal,
-                         csr_shared=(csr_batch == 1 and cfg["batch"] > 1))
-    torch.cuda.synchronize()
-    assert sa.sa_device_status() == 0
-    o_np = bf16_to_f64(o)
-    lse_np = lse.cpu().numpy().astype(np.float64)
-    assert np.all(np.isfinite(o_np)) and np.all(np.isfinite(lse_np))   # no row is empty in these graphs
-    rp_o, ci_o = om.build_csr(p, ratios_oracle, csr_batch)
-    rng = np.random.default_rng(1)
-    bt, n, h = cfg["batch"], cfg["n_tokens"], cfg["heads"]
-    smp = _samples(rng, bt, n, h, extra=samples_extra)
-    o_ref, lse_ref = oracle.attention_rows_csr(qb, kb, vb, rp_o, ci_o, p.block, p.causal, smp,
-                                               convert=bf16_bits_to_f64)
-    o_g = np.stack([o_np[s, i, hh] for s, i, hh in smp])
-    l_g = np.array([lse_np[s, hh, i] for s, i, hh in smp])
-    assert_attention_close(o_g, l_g, o_ref, lse_ref, cfg["name"])
-
-
-def test_bytelm_topk_8k_sampled():
-    cfg = workload("bytelm_topk_8k")
-    data = byte_stream(cfg)
-    p = om.MaskParams("topk", cfg["block"], cfg["n_tokens"], 1, cfg["window_blocks"], cfg["global_blocks"],
-                      cfg["topk"])
-    n = cfg["n_tokens"]
-    _full_size(cfg, p, cfg["batch"], sa.sa_block_ratios(data, cfg["block"]), oracle.block_ratios(data, cfg["block"]),
-               [(0, 0, 0), (3, n - 1, 11), (1, 127, 5), (2, 128, 6), (0, 4095, 3)])
-
-
-def test_bigbird_16k_sampled():
-    cfg = workload("bigbird_16k")
-    b = cfg["block"]
-    p = om.MaskParams("bigbird", b, cfg["n_tokens"], 0, cfg["window_tokens"] // b, cfg["global_tokens"] // b, 0,
-                      cfg["random_tokens"] // b, cfg["seed"])
-    n = cfg["n_tokens"]
-    _full_size(cfg, p, 1, None, None, [(0, 0, 0), (7, 31, 11), (3, 32, 2), (5, n - 1, 4), (1, 100, 7)])
-
-
-@pytest.mark.parametrize("topk", [64])
-def test_long_topk_64k_sampled(topk):
-    cfg = workload("long_topk_64k", topk=topk)
-    data = byte_stream(cfg)
-    p = om.MaskParams("topk", cfg["block"], cfg["n_tokens"], 1, cfg["window_blocks"], cfg["global_blocks"], topk)
-    n = cfg["n_tokens"]
-    _full_size(cfg, p, 1, sa.sa_block_ratios(data, cfg["block"]), oracle.block_ratios(data, cfg["block"]),
-               [(0, n - 1, 15), (0, 0, 0), (0, 40000, 8)])
+# Full-size workloads (whole query tiles of every head) are in test_gpu_fullsize.py.
 
 
 # ---------------------------------------------------------------- head groups (per-head CSR)
@@ -283,40 +228,6 @@ def test_head_groups_interleaved_and_single_mask():
     o2, l2 = sa.attn_fwd_heads(q, k, v, [(rp, ci)], [0, 0, 0], b, 1)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
-
-
-def test_cas_heads_8k_sampled():
-    cfg = workload("cas_heads_8k")
-    data = byte_stream(cfg)
-    b, n, bt, h = cfg["block"], cfg["n_tokens"], cfg["batch"], cfg["heads"]
-    r_gpu = sa.sa_block_ratios(data, b, cfg["zlib_level"])
-    r_ora = oracle.block_ratios(data, b, cfg["zlib_level"])
-    comps = list(cfg["head_components"])
-    assert comps == oracle.cas_head_components(h)
-    parts = sorted(set(comps))
-    head_mask = [parts.index(c) for c in comps]
-    qb, kb, vb = qkv_bits(cfg)
-    csrs_d, csrs_o = [], []
-    for c in parts:
-        p = om.MaskParams("literal_mean", b, n, 1, cfg["window_blocks"], components=c)
-        csrs_d.append(_mask_on_gpu(p, bt, r_gpu))
-        csrs_o.append(om.build_csr(p, r_ora, bt))
-    torch = torch_cuda()
-    o, lse = sa.attn_fwd_heads(to_dev(qb), to_dev(kb), to_dev(vb), csrs_d, head_mask, b, 1)
-    torch.cuda.synchronize()
-    assert sa.sa_device_status() == 0
-    o_np, lse_np = bf16_to_f64(o), lse.cpu().numpy().astype(np.float64)
-    rng = np.random.default_rng(4)
-    smp = _samples(rng, bt, n, h, k=36, extra=[(0, 0, 0), (3, n - 1, 11), (1, 130, 7), (2, 4095, 5)])
-    o_g = np.stack([o_np[s, i, hh] for s, i, hh in smp])
-    l_g = np.array([lse_np[s, hh, i] for s, i, hh in smp])
-    o_ref = np.zeros_like(o_g)
-    l_ref = np.zeros_like(l_g)
-    for t, (s, i, hh) in enumerate(smp):
-        rp_o, ci_o = csrs_o[head_mask[hh]]
-        orow, lrow = oracle.attention_rows_csr(qb, kb, vb, rp_o, ci_o, b, 1, [(s, i, hh)], convert=bf16_bits_to_f64)
-        o_ref[t], l_ref[t] = orow[0], lrow[0]
-    assert_attention_close(o_g, l_g, o_ref, l_ref, cfg["name"])
 
 
 def test_head_groups_eight_masks_sixteen_heads():

@@ -62,27 +62,55 @@ def test_small_edge_cases():
     _run(1, 64, 1, 1, 64, Fraction(1, 2), seed=6)          # window covers everything: dense causal
 
 
-def test_fib_8k_one_layer_sampled():
+@pytest.mark.parametrize("window,hkv", [(6, 2), (8, 8), (8, 2), (10, 2), (12, 8), (12, 2)])
+def test_fib_2k_full_layers(window, hkv):
+    """The 2048-token Fibonacci workload (8 sequences, 8 heads of 64) in full, through the
+    entry point that takes the page's parameters (W, alpha as a fraction, 15 rungs), for
+    the first, a middle and the last layer of the 0.5 -> 2.0 ramp and of the page's own
+    0.5 -> 1.5 ramp ("Depth-Staggered Fibonacci Spacing ...", section 3 "Run matrix": windows
+    6 to 12, grouped-query attention with 2 KV heads)."""
     torch = torch_cuda()
-    cfg = workload("fib_8k")
-    qb, kb, vb = qkv_bits(cfg)
-    alpha = oracle.alpha_schedule(16, cfg["alpha_lo"], cfg["alpha_hi"])[11]
-    W, n = cfg["window"], cfg["n_tokens"]
-    offs = sa.sa_fib_offsets(alpha.numerator, alpha.denominator, cfg["n_rungs"], W, n)
-    o, lse = sa.offset_attn_fwd(to_dev(qb), to_dev(kb), to_dev(vb), W, offs)
+    cfg = workload("fib_2k", window=window, kv_heads=hkv)
+    for lo, hi in ((cfg["alpha_lo"], cfg["alpha_hi"]), ((1, 2), (3, 2))):
+        for layer in (0, 7, 15):
+            num, den = sa.sa_layer_alpha(layer, 16, lo, hi)
+            alpha = Fraction(num, den)
+            assert alpha == oracle.alpha_schedule(16, lo, hi)[layer]
+            qb, kb, vb = qkv_bits(cfg, seed_offset=layer)
+            o, lse = sa.fib_offset_attn_fwd(to_dev(qb), to_dev(kb), to_dev(vb), window, num, den, 15)
+            torch.cuda.synchronize()
+            assert sa.sa_device_status() == 0
+            f = bf16_bits_to_f64
+            o_ref, lse_ref = oracle.attention_offsets(f(qb), f(kb), f(vb), window,
+                                                      oracle.fib_offsets(alpha, oracle.fib_rungs(15)))
+            assert_attention_close(bf16_to_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref,
+                                   f"fib 2k W={window} Hkv={hkv} layer {layer} alpha={alpha}")
+
+
+@pytest.mark.parametrize("window,hkv,layer", [(8, 8, 11), (6, 2, 0), (10, 2, 15), (12, 8, 5)])
+def test_fib_8k_whole_tiles(window, hkv, layer):
+    """The 8192-token workload (4x the training length): every row of eight 128-query slices
+    (the first, the last, others spread over the sequences) for every head."""
+    torch = torch_cuda()
+    cfg = workload("fib_8k", window=window, kv_heads=hkv)
+    qb, kb, vb = qkv_bits(cfg, seed_offset=layer)
+    num, den = sa.sa_layer_alpha(layer, 16, cfg["alpha_lo"], cfg["alpha_hi"])
+    alpha = Fraction(num, den)
+    n, bt, h = cfg["n_tokens"], cfg["batch"], cfg["heads"]
+    o, lse = sa.fib_offset_attn_fwd(to_dev(qb), to_dev(kb), to_dev(vb), window, num, den, cfg["n_rungs"])
     torch.cuda.synchronize()
     assert sa.sa_device_status() == 0
-    rng = np.random.default_rng(2)
-    smp = [(int(rng.integers(8)), int(rng.integers(n)), int(rng.integers(8))) for _ in range(64)]
-    smp += [(0, 0, 0), (7, n - 1, 7), (3, 127, 1), (4, 128, 2)]
-    o_ref, lse_ref = oracle.attention_offsets(qb, kb, vb, W, oracle.fib_offsets(alpha, oracle.fib_rungs(15)),
-                                              samples=smp, convert=bf16_bits_to_f64)
     o_np = bf16_to_f64(o)
     lse_np = lse.cpu().numpy().astype(np.float64)
     assert np.all(np.isfinite(o_np)) and np.all(np.isfinite(lse_np))
-    o_g = np.stack([o_np[s, i, h] for s, i, h in smp])
-    l_g = np.array([lse_np[s, h, i] for s, i, h in smp])
-    assert_attention_close(o_g, l_g, o_ref, lse_ref, "fib_8k")
+    slices = [(0, 0), (bt - 1, n - 128), (1, 128), (2, 1024), (3, 4096 - 64), (4, 6000), (5, 8000 - 128),
+              (6, 987 - 60)]
+    smp = [(s, i, hh) for s, i0 in slices for i in range(i0, i0 + 128) for hh in range(h)]
+    o_ref, lse_ref = oracle.attention_offsets(qb, kb, vb, window, oracle.fib_offsets(alpha, oracle.fib_rungs(15)),
+                                              samples=smp, convert=bf16_bits_to_f64)
+    o_g = np.stack([o_np[s, i, hh] for s, i, hh in smp])
+    l_g = np.array([lse_np[s, hh, i] for s, i, hh in smp])
+    assert_attention_close(o_g, l_g, o_ref, lse_ref, f"fib_8k W={window} Hkv={hkv} layer {layer}")
 
 
 def _run_offsets(q64, k64, v64, qd, kd, vd, window, offs, what):
@@ -170,7 +198,7 @@ def test_interp_integer_alpha_matches_integer_offset_kernel():
         assert (l1 - l2).abs().max().item() < 2 * LSE_MAX_ABS
 
 
-def test_interp_fib_8k_sampled():
+def test_interp_fib_8k_whole_slices():
     torch = torch_cuda()
     cfg = workload("fib_8k", layers=1)
     qb, kb, vb = qkv_bits(cfg)
@@ -178,10 +206,10 @@ def test_interp_fib_8k_sampled():
     o, lse = sa.offset_attn_interp_fwd(to_dev(qb), to_dev(kb), to_dev(vb), cfg["window"], alpha)
     torch.cuda.synchronize()
     assert sa.sa_device_status() == 0
-    rng = np.random.default_rng(2)
     bt, n, h = cfg["batch"], cfg["n_tokens"], cfg["heads"]
-    smp = [(int(rng.integers(bt)), int(rng.integers(n)), int(rng.integers(h))) for _ in range(40)]
-    smp += [(0, 0, 0), (7, n - 1, 7), (3, 1, 2), (5, 987, 4)]
+    # every row of eight 128-query slices, every head
+    slices = [(0, 0), (bt - 1, n - 128), (3, 1), (5, 987 - 64), (1, 2048), (2, 4000), (4, 6100), (6, 7777)]
+    smp = [(s, i, hh) for s, i0 in slices for i in range(i0, min(n, i0 + 128)) for hh in range(h)]
     lt = oracle.interp_rungs(alpha, oracle.fib_rungs(15), cfg["window"])
     o_ref, lse_ref = oracle.attention_offsets_interp(qb, kb, vb, cfg["window"], lt, samples=smp,
                                                      convert=bf16_bits_to_f64)
