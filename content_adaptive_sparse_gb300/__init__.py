@@ -6,7 +6,7 @@ work of the hot path runs in the library's CUDA kernels. There is no CPU fallbac
 if the library is missing or the device is not an sm_103 GPU, calls raise.
 
 Names follow the C ABI: ``sa_build_mask``, ``sa_attn_fwd``, ``sa_attn_fwd_heads``,
-``sa_offset_attn_fwd``, ``sa_fib_offsets``, ``sa_pow2_offsets``, ``sa_layer_alpha``, ``sa_block_ratios``, ``sa_mask_nnz_bound``, ``sa_device_status``.
+``sa_offset_attn_fwd``, ``sa_offset_attn_fwd_list``, ``sa_fib_offsets``, ``sa_pow2_offsets``, ``sa_layer_alpha``, ``sa_block_ratios``, ``sa_mask_nnz_bound``, ``sa_device_status``.
 """
 from __future__ import annotations
 
@@ -71,9 +71,11 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         [_P, _P, _P, _P, ctypes.c_int32, ctypes.c_float, _P, _P, _P, _P, ctypes.c_size_t, _P]
     lib.sa_attn_bwd_noalloc.argtypes = [_P, _P, _P, _P, _P, _P, _I64x3, _I64x3, _I64x3] + \
         [ctypes.c_int32] * 7 + [_P, _P, ctypes.c_int64, ctypes.c_int32, ctypes.c_float, _P, _P, _P, _P]
-    lib.sa_offset_attn_fwd.argtypes = [_P, _P, _P, _I64x3, _I64x3, _I64x3, ctypes.c_int32, ctypes.c_int32,
-                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P,
-                                       ctypes.c_int32, ctypes.c_float, _P, _P, _P]
+    lib.sa_offset_attn_fwd.argtypes = [_P, _P, _P, _I64x3, _I64x3, _I64x3] + [ctypes.c_int32] * 9 + \
+        [ctypes.c_float, _P, _P, _P]
+    lib.sa_offset_attn_fwd_list.argtypes = [_P, _P, _P, _I64x3, _I64x3, _I64x3, ctypes.c_int32, ctypes.c_int32,
+                                            ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P,
+                                            ctypes.c_int32, ctypes.c_float, _P, _P, _P]
     lib.sa_offset_attn_interp_fwd.argtypes = [_P, _P, _P, _I64x3, _I64x3, _I64x3] + [ctypes.c_int32] * 6 + \
         [ctypes.c_double, ctypes.c_int32, ctypes.c_int32, ctypes.c_float, _P, _P, _P]
     lib.sa_fib_offsets.argtypes = [ctypes.c_int32] * 5 + [_P, ctypes.c_int32, _P]
@@ -81,12 +83,14 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.sa_layer_alpha.argtypes = [ctypes.c_int32] * 7 + [_P, _P]
     lib.sa_block_ratios.argtypes = [_P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P,
                                     ctypes.c_int32]
+    lib.sa_build_mask_from_bytes.argtypes = [ctypes.POINTER(MaskParams), _P, ctypes.c_int32, ctypes.c_int32, _P, _P,
+                                             _P, _P, ctypes.c_int64, _P]
     lib.sa_device_status.argtypes = [_P]
     lib.sa_selftest_bounded_wait.argtypes = [_P]
     for name in ("sa_mask_nnz_bound", "sa_build_mask", "sa_attn_fwd", "sa_attn_fwd_heads", "sa_attn_bwd",
-                 "sa_attn_bwd_noalloc", "sa_attn_bwd_heads", "sa_attn_bwd_workspace_size", "sa_offset_attn_fwd",
+                 "sa_attn_bwd_noalloc", "sa_attn_bwd_heads", "sa_attn_bwd_workspace_size", "sa_offset_attn_fwd", "sa_offset_attn_fwd_list",
                  "sa_offset_attn_interp_fwd", "sa_fib_offsets", "sa_pow2_offsets", "sa_layer_alpha", "sa_block_ratios",
-                 "sa_device_status", "sa_selftest_bounded_wait"):
+                 "sa_device_status", "sa_selftest_bounded_wait", "sa_build_mask_from_bytes"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -234,13 +238,24 @@ def sa_attn_bwd_noalloc(q, k, v, o, d_o, lse, row_ptr, col_idx, block: int, caus
         cap, int(bool(csr_shared)), scale, dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), _stream_ptr(stream)))
 
 
-def sa_offset_attn_fwd(q, k, v, window: int, offsets, o, lse, softmax_scale: float | None = None,
-                       stream=None) -> None:
+def sa_offset_attn_fwd(q, k, v, window: int, alpha_num: int, alpha_den: int, n_rungs: int, o, lse,
+                       softmax_scale: float | None = None, stream=None) -> None:
+    """Window plus the Fibonacci offsets round_half_even(alpha * f_k), alpha = num / den."""
+    b, n, h, d = q.shape
+    hkv = k.shape[2]
+    scale = 1.0 / float(np.sqrt(d)) if softmax_scale is None else float(softmax_scale)
+    _check("sa_offset_attn_fwd", load_library().sa_offset_attn_fwd(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), _strides(q), _strides(k), _strides(o), b, n, h, hkv, d, window,
+        int(alpha_num), int(alpha_den), int(n_rungs), scale, o.data_ptr(), lse.data_ptr(), _stream_ptr(stream)))
+
+
+def sa_offset_attn_fwd_list(q, k, v, window: int, offsets, o, lse, softmax_scale: float | None = None,
+                            stream=None) -> None:
     b, n, h, d = q.shape
     hkv = k.shape[2]
     offs = np.ascontiguousarray(np.asarray(offsets, dtype=np.int32))
     scale = 1.0 / float(np.sqrt(d)) if softmax_scale is None else float(softmax_scale)
-    _check("sa_offset_attn_fwd", load_library().sa_offset_attn_fwd(
+    _check("sa_offset_attn_fwd_list", load_library().sa_offset_attn_fwd_list(
         q.data_ptr(), k.data_ptr(), v.data_ptr(), _strides(q), _strides(k), _strides(o), b, n, h, hkv, d, window,
         offs.ctypes.data if offs.size else None, int(offs.size), scale, o.data_ptr(), lse.data_ptr(),
         _stream_ptr(stream)))
@@ -299,6 +314,17 @@ def sa_block_ratios(data: np.ndarray, block: int, level: int = 6, n_threads: int
     _check("sa_block_ratios", load_library().sa_block_ratios(arr.ctypes.data, arr.shape[0], arr.shape[1], block,
                                                               level, out.ctypes.data, n_threads))
     return out
+
+
+def sa_build_mask_from_bytes(params: MaskParams, data, h_ratio, d_ratio, row_ptr, col_idx, level: int = 6,
+                             n_threads: int = 0, stream=None) -> None:
+    """Host ratios of ``data`` (uint8 [batch, n_tokens], host) into ``h_ratio`` (float32 host
+    tensor, pinned for an asynchronous upload), then their upload into ``d_ratio`` and the
+    mask build, enqueued on the stream."""
+    arr = np.ascontiguousarray(np.asarray(data, dtype=np.uint8))
+    _check("sa_build_mask_from_bytes", load_library().sa_build_mask_from_bytes(
+        ctypes.byref(params), arr.ctypes.data, level, n_threads, h_ratio.data_ptr(), d_ratio.data_ptr(),
+        row_ptr.data_ptr(), col_idx.data_ptr(), col_idx.numel(), _stream_ptr(stream)))
 
 
 def sa_selftest_bounded_wait(stream=None) -> None:
@@ -361,7 +387,18 @@ def offset_attn_fwd(q, k, v, window: int, offsets, softmax_scale: float | None =
     b, n, h, d = q.shape
     o = torch.empty_like(q)
     lse = torch.empty((b, h, n), dtype=torch.float32, device=q.device)
-    sa_offset_attn_fwd(q, k, v, window, offsets, o, lse, softmax_scale)
+    sa_offset_attn_fwd_list(q, k, v, window, offsets, o, lse, softmax_scale)
+    return o, lse
+
+
+def fib_offset_attn_fwd(q, k, v, window: int, alpha_num: int, alpha_den: int, n_rungs: int = 15,
+                        softmax_scale: float | None = None):
+    """Allocate O / LSE and run sa_offset_attn_fwd (Fibonacci offsets of alpha = num / den)."""
+    import torch
+    b, n, h, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((b, h, n), dtype=torch.float32, device=q.device)
+    sa_offset_attn_fwd(q, k, v, window, alpha_num, alpha_den, n_rungs, o, lse, softmax_scale)
     return o, lse
 
 

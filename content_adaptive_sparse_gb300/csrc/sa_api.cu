@@ -364,10 +364,11 @@ int sa_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void*
                      need, stream);
 }
 
-int sa_offset_attn_fwd(const void* q, const void* k, const void* v, const int64_t q_strides[3],
-                       const int64_t kv_strides[3], const int64_t o_strides[3], int32_t batch, int32_t n_tokens,
-                       int32_t heads, int32_t kv_heads, int32_t head_dim, int32_t window, const int32_t* h_offsets,
-                       int32_t n_offsets, float softmax_scale, void* o, float* lse, void* stream) {
+int sa_offset_attn_fwd_list(const void* q, const void* k, const void* v, const int64_t q_strides[3],
+                            const int64_t kv_strides[3], const int64_t o_strides[3], int32_t batch,
+                            int32_t n_tokens, int32_t heads, int32_t kv_heads, int32_t head_dim, int32_t window,
+                            const int32_t* h_offsets, int32_t n_offsets, float softmax_scale, void* o, float* lse,
+                            void* stream) {
   int st = check_attn_common(q, k, v, q_strides, kv_strides, o_strides, batch, n_tokens, heads, kv_heads, o, lse);
   if (st != SA_OK) return st;
   if (n_offsets < 0 || (n_offsets > 0 && !h_offsets)) return SA_ERR_INVALID_ARG;
@@ -403,6 +404,19 @@ int sa_offset_attn_fwd(const void* q, const void* k, const void* v, const int64_
   for (int i = 0; i < sa::kMaxOffsets; ++i) a.offsets[i] = i < n_offsets ? h_offsets[i] : 0;
   a.softmax_scale = softmax_scale;
   return sa::launch_offset_attn_fwd(a, static_cast<cudaStream_t>(stream));
+}
+
+int sa_offset_attn_fwd(const void* q, const void* k, const void* v, const int64_t q_strides[3],
+                       const int64_t kv_strides[3], const int64_t o_strides[3], int32_t batch, int32_t n_tokens,
+                       int32_t heads, int32_t kv_heads, int32_t head_dim, int32_t window, int32_t alpha_num,
+                       int32_t alpha_den, int32_t n_rungs, float softmax_scale, void* o, float* lse, void* stream) {
+  int32_t offs[sa::kMaxOffsets];
+  int32_t count = 0;
+  const int st = sa_fib_offsets(alpha_num, alpha_den, n_rungs, window, n_tokens, offs, sa::kMaxOffsets, &count);
+  if (st == SA_ERR_CAPACITY) return SA_ERR_UNSUPPORTED;   // more distinct offsets than the kernel takes
+  if (st != SA_OK) return st;
+  return sa_offset_attn_fwd_list(q, k, v, q_strides, kv_strides, o_strides, batch, n_tokens, heads, kv_heads,
+                                 head_dim, window, offs, count, softmax_scale, o, lse, stream);
 }
 
 }  // extern "C"
@@ -573,6 +587,28 @@ int sa_block_ratios(const uint8_t* h_bytes, int32_t batch, int32_t n_tokens, int
     for (auto& th : pool) th.join();
   }
   return failed ? SA_ERR_UNSUPPORTED : SA_OK;
+}
+
+int sa_build_mask_from_bytes(const sa_mask_params* params, const uint8_t* h_bytes, int32_t zlib_level,
+                             int32_t n_threads, float* h_ratio, float* d_ratio, int32_t* d_row_ptr,
+                             int32_t* d_col_idx, int64_t col_capacity, void* stream) {
+  const int st = check_mask_params(params);
+  if (st != SA_OK) return st;
+  if (params->mode != SA_MASK_TOPK && params->mode != SA_MASK_LITERAL_MEAN) return SA_ERR_INVALID_ARG;
+  if (!h_bytes || !h_ratio || !d_ratio || !d_row_ptr || !d_col_idx) return SA_ERR_INVALID_ARG;
+  const int64_t need = nnz_bound(*params);
+  if (need > INT32_MAX) return SA_ERR_UNSUPPORTED;
+  if (col_capacity < need) return SA_ERR_CAPACITY;
+  if (!device_ok()) return SA_ERR_CUDA;
+  // host part: the ratios, on host threads, while the GPU works through what the caller
+  // enqueued before this call (e.g. the Q/K/V uploads and the previous step's attention)
+  const int r = sa_block_ratios(h_bytes, params->batch, params->n_tokens, params->block, zlib_level, h_ratio,
+                                n_threads);
+  if (r != SA_OK) return r;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t bytes = sizeof(float) * (size_t)params->batch * (size_t)(params->n_tokens / params->block);
+  if (cudaMemcpyAsync(d_ratio, h_ratio, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return SA_ERR_CUDA;
+  return sa::launch_build_mask(*params, d_ratio, d_row_ptr, d_col_idx, s);
 }
 
 int sa_selftest_bounded_wait(void* stream) {

@@ -220,19 +220,35 @@ int sa_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void*
                         int64_t col_capacity, int32_t csr_shared, float softmax_scale, void* dq, void* dk, void* dv,
                         void* stream);
 
-/* Token-granular window-plus-offset attention forward ("Depth-Staggered Fibonacci
- * Spacing ...", section 2 "Attended set"): query i attends to keys
- *   { i - delta : delta in {0, ..., window} u offsets, i - delta >= 0 }   (a set).
- *   h_offsets : host int32[n_offsets], strictly ascending, each > window and
- *               < n_tokens (see sa_fib_offsets); n_offsets <= 64.
- *   window in [0, 64]; head_dim == 64; n_tokens <= 65535 * 64 and batch * heads < 2^31
+/* Token-granular window-plus-Fibonacci-offset attention forward ("Depth-Staggered
+ * Fibonacci Spacing for Sparse Attention", section 2 "Method" and "Attended set"): query i
+ * attends to keys
+ *   { i - delta : delta in {0, ..., window} u D, i - delta >= 0 }   (a set),
+ * where D = { round_half_even(alpha * f_k) } over the Fibonacci rungs f = 1, 2, 3, 5, ...
+ * (the first n_rungs of them; n_rungs == 0: every f_k <= n_tokens; the page uses 15) and
+ * alpha = alpha_num / alpha_den > 0 is the layer's scale as an exact fraction (the page's
+ * per-layer linear stagger, see sa_layer_alpha). D is computed on the host exactly as
+ * sa_fib_offsets returns it.
+ *   head_dim == 64 (the page's model: 8 heads of 64); window in [0, 64]; at most 64
+ *   distinct offsets beyond the window; n_tokens <= 65535 * 64 and batch * heads < 2^31
  *   (else SA_ERR_UNSUPPORTED); other arguments as in sa_attn_fwd. The kernel's copy waits
  *   are bounded: an expired wait leaves O and LSE incomplete and is reported by
  *   sa_device_status as SA_ERR_TIMEOUT. */
 int sa_offset_attn_fwd(const void* q, const void* k, const void* v, const int64_t q_strides[3],
                        const int64_t kv_strides[3], const int64_t o_strides[3], int32_t batch, int32_t n_tokens,
-                       int32_t heads, int32_t kv_heads, int32_t head_dim, int32_t window, const int32_t* h_offsets,
-                       int32_t n_offsets, float softmax_scale, void* o, float* lse, void* stream);
+                       int32_t heads, int32_t kv_heads, int32_t head_dim, int32_t window, int32_t alpha_num,
+                       int32_t alpha_den, int32_t n_rungs, float softmax_scale, void* o, float* lse, void* stream);
+
+/* sa_offset_attn_fwd over an explicit offset set (any ladder, e.g. sa_pow2_offsets):
+ * query i attends to { i - delta : delta in {0, ..., window} u h_offsets, i - delta >= 0 }.
+ *   h_offsets : host int32[n_offsets], strictly ascending, each > window and
+ *               < n_tokens; n_offsets <= 64. Read before the call returns.
+ * Every other argument, limit and error as in sa_offset_attn_fwd. */
+int sa_offset_attn_fwd_list(const void* q, const void* k, const void* v, const int64_t q_strides[3],
+                            const int64_t kv_strides[3], const int64_t o_strides[3], int32_t batch,
+                            int32_t n_tokens, int32_t heads, int32_t kv_heads, int32_t head_dim, int32_t window,
+                            const int32_t* h_offsets, int32_t n_offsets, float softmax_scale, void* o, float* lse,
+                            void* stream);
 
 /* Window plus interpolated-rung attention forward ("Depth-Staggered Fibonacci Spacing ...",
  * section 2 "Attended set"; the interpolated gather of a continuous alpha). Rung k has the
@@ -283,6 +299,22 @@ int sa_layer_alpha(int32_t layer, int32_t layers, int32_t lo_num, int32_t lo_den
  * run time; returns SA_ERR_UNSUPPORTED if it cannot be loaded. Host only. */
 int sa_block_ratios(const uint8_t* h_bytes, int32_t batch, int32_t n_tokens, int32_t block, int32_t level,
                     float* h_ratio, int32_t n_threads);
+
+/* The whole mask step of one batch from host bytes ("Parameter-free Adaptive Sparse
+ * Attention ...", section 3.1 Eq. 1 and section 3.4: the ratios of one 8192-byte sequence
+ * take well under a millisecond on the host): the per-block ratios of h_bytes
+ * [batch][n_tokens] are computed on up to n_threads host threads (0 = hardware
+ * concurrency) into h_ratio [batch][nb] (as sa_block_ratios), then the upload of h_ratio
+ * into d_ratio and the mask build (as sa_build_mask) are enqueued on `stream`.
+ * The host part runs in the calling thread before the call returns, so GPU work that the
+ * caller enqueued earlier (for example the uploads of Q, K and V on another stream, or the
+ * previous batch's attention) overlaps it. TOPK and LITERAL_MEAN modes only (the modes
+ * that read ratios). h_ratio must stay unchanged until the upload has run (use pinned
+ * memory for an asynchronous copy; a pageable buffer is copied before the call returns).
+ * Errors as in sa_block_ratios and sa_build_mask. */
+int sa_build_mask_from_bytes(const sa_mask_params* params, const uint8_t* h_bytes, int32_t zlib_level,
+                             int32_t n_threads, float* h_ratio, float* d_ratio, int32_t* d_row_ptr,
+                             int32_t* d_col_idx, int64_t col_capacity, void* stream);
 
 /* Synchronises `stream`, then reads and clears the library's device error words.
  * Returns SA_OK, SA_ERR_TIMEOUT (a bounded wait expired; the kernel unwound and its

@@ -33,6 +33,7 @@ def _declared_functions():
 def test_header_symbols_exported(lib):
     names = _declared_functions()
     assert {"sa_build_mask", "sa_attn_fwd", "sa_attn_fwd_heads", "sa_offset_attn_fwd", "sa_pow2_offsets",
+            "sa_offset_attn_fwd_list",
             "sa_attn_bwd", "sa_attn_bwd_workspace_size", "sa_attn_bwd_noalloc", "sa_offset_attn_interp_fwd",
             "sa_attn_bwd_heads", "sa_selftest_bounded_wait",
             "sa_layer_alpha", "sa_fib_offsets", "sa_block_ratios",
@@ -150,8 +151,15 @@ def test_argument_validation_before_any_launch(lib):
     assert lib.sa_offset_attn_interp_fwd(p16, p16, p16, s, s, s, 1, 8192, 8, 8, 32, 8, ctypes.c_double(0.8), 15, 0,
                                          ctypes.c_float(0.125), p16, p16, None) == -2
     offs = (ctypes.c_int32 * 2)(5, 9)        # offset inside the window -> invalid
-    assert lib.sa_offset_attn_fwd(p16, p16, p16, s, s, s, 1, 8192, 8, 8, 64, 8, offs, 2,
+    assert lib.sa_offset_attn_fwd_list(p16, p16, p16, s, s, s, 1, 8192, 8, 8, 64, 8, offs, 2,
+                                       ctypes.c_float(0.125), p16, p16, None) == -1
+    # the page's parameters: alpha must be a positive fraction; d != 64 is not supported
+    assert lib.sa_offset_attn_fwd(p16, p16, p16, s, s, s, 1, 8192, 8, 8, 64, 8, 1, 0, 15,
                                   ctypes.c_float(0.125), p16, p16, None) == -1
+    assert lib.sa_offset_attn_fwd(p16, p16, p16, s, s, s, 1, 8192, 8, 8, 64, 8, -3, 2, 15,
+                                  ctypes.c_float(0.125), p16, p16, None) == -1
+    assert lib.sa_offset_attn_fwd(p16, p16, p16, s, s, s, 1, 8192, 8, 8, 32, 8, 1, 1, 15,
+                                  ctypes.c_float(0.125), p16, p16, None) == -2
 
 
 def test_compute_entry_points_refuse_without_gpu(lib):

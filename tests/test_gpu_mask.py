@@ -111,3 +111,34 @@ def test_mask_is_deterministic():
     a = _gpu_csr(p, batch, rg)
     b = _gpu_csr(p, batch, rg)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("name,mode", [("bytelm_topk_8k", "topk"), ("cas_heads_8k", "literal_mean")])
+def test_mask_from_host_bytes(name, mode):
+    """sa_build_mask_from_bytes (host ratios, their upload and the mask build in one call)
+    writes the oracle's CSR bit for bit, and the host ratios it returns equal the oracle's."""
+    torch = torch_cuda()
+    cfg = workload(name)
+    data = byte_stream(cfg)
+    b, n, bt = cfg["block"], cfg["n_tokens"], cfg["batch"]
+    level = cfg.get("zlib_level", 6)
+    if mode == "topk":
+        p = om.MaskParams("topk", b, n, 1, cfg["window_blocks"], cfg["global_blocks"], cfg["topk"])
+    else:
+        p = om.MaskParams("literal_mean", b, n, 1, cfg["window_blocks"])
+    prm = sa.mask_params(mode, b, n, bt, p.causal, p.window_blocks, p.global_blocks, p.topk, 0, 0, 0)
+    cap = sa.sa_mask_nnz_bound(prm)
+    h_ratio = torch.empty((bt, n // b), dtype=torch.float32).pin_memory()
+    d_ratio = torch.empty((bt, n // b), dtype=torch.float32, device="cuda")
+    rp = torch.empty((bt, n // b + 1), dtype=torch.int32, device="cuda")
+    ci = torch.empty((cap,), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.Stream()
+    sa.sa_build_mask_from_bytes(prm, data, h_ratio, d_ratio, rp, ci, level=level, stream=stream)
+    stream.synchronize()
+    assert sa.sa_device_status() == 0
+    r_ora = oracle.block_ratios(data, b, level)
+    assert np.array_equal(h_ratio.numpy(), r_ora)
+    assert np.array_equal(d_ratio.cpu().numpy(), r_ora)
+    rp_o, ci_o = om.build_csr(p, r_ora, bt)
+    assert np.array_equal(rp.cpu().numpy(), rp_o)
+    assert np.array_equal(ci.cpu().numpy()[:len(ci_o)], ci_o)
