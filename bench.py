@@ -33,11 +33,10 @@ is reported.
 from __future__ import annotations
 
 import argparse
-import hashlib
 import json
+import platform
 import math
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -92,28 +91,6 @@ def _peaks() -> dict:
         return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
                 "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
-
-
-def _kernel_source_hash(files) -> str:
-    h = hashlib.sha256()
-    for f in files:
-        with open(os.path.join(ROOT, "content_adaptive_sparse_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
-    return h.hexdigest()[:16]
-
-
-def _profile_traffic(profile_md: str, src_files) -> float | None:
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
-    current kernel source (the summary records the source hash)."""
-    path = os.path.join(ROOT, "profiles", profile_md)
-    if not os.path.exists(path):
-        return None
-    text = open(path).read()
-    m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
-    m_bytes = re.search(r"dram_bytes_per_launch_full_workload:\s*([0-9.eE+]+)", text)
-    if not m_hash or not m_bytes or m_hash.group(1) != _kernel_source_hash(src_files):
-        return None
-    return float(m_bytes.group(1))
 
 
 # ------------------------------------------------------------------ clocks
@@ -297,9 +274,12 @@ class OffsetCase:
         ladder = sa.sa_pow2_offsets if cfg.get("ladder") == "pow2" else sa.sa_fib_offsets
         self.interp = bool(cfg.get("interp", False))
         self.alphas = []
+        self.fracs = []
+        self.pow2 = cfg.get("ladder") == "pow2"
         for l in range(L):
             num, den = sa.sa_layer_alpha(l, L, cfg["alpha_lo"], cfg["alpha_hi"], cfg.get("stride", 1))
             self.alphas.append(num / den)
+            self.fracs.append((num, den))
             offs = ladder(num, den, cfg["n_rungs"], W, n)
             qb, kb, vb = qkv_bits(cfg, seed_offset=l)
             q, k, v = (torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev) for x in (qb, kb, vb))
@@ -328,8 +308,13 @@ class OffsetCase:
             for (q, k, v, o, lse, _), alpha in zip(self.layers, self.alphas):
                 self.sa.sa_offset_attn_interp_fwd(q, k, v, self.W, alpha, o, lse, self.cfg["n_rungs"])
             return
-        for q, k, v, o, lse, offs in self.layers:
-            self.sa.sa_offset_attn_fwd(q, k, v, self.W, offs, o, lse)
+        if self.pow2:
+            for q, k, v, o, lse, offs in self.layers:
+                self.sa.sa_offset_attn_fwd_list(q, k, v, self.W, offs, o, lse)
+            return
+        # the Fibonacci ladder through the entry point that takes the page's parameters
+        for (q, k, v, o, lse, _), (num, den) in zip(self.layers, self.fracs):
+            self.sa.sa_offset_attn_fwd(q, k, v, self.W, num, den, self.cfg["n_rungs"], o, lse)
 
 
 def _time_events(torch, fn_pairs, steps: int, warmup: int, flush):
@@ -400,6 +385,122 @@ def _oracle_sample_child(budget_s: float, units_per_step: int, steps: int) -> di
             k += 1
         out["steps"].append({"flops": flops, "seconds": time.perf_counter() - t0})
     return out
+
+
+# The workloads of the oracle timing (the hot path's configurations): name, overrides,
+# how the oracle is sampled.
+ORACLE_CONFIGS = [
+    ("tiny_topk", {}, "full"),
+    ("bytelm_topk_8k", {}, "sampled"),
+    ("bigbird_4k", {}, "sampled"),
+    ("bigbird_16k", {}, "sampled"),
+    ("fib_2k", {}, "sampled"),
+    ("fib_8k", {}, "sampled"),
+    ("long_topk_64k", {"topk": 16}, "sampled"),
+    ("long_topk_64k", {"topk": 64}, "sampled"),
+    ("long_topk_64k", {"topk": 256}, "extrapolated"),
+    ("full_16k", {}, "sampled"),
+]
+
+
+def _oracle_configs_child(budget_s: float) -> dict:
+    """Run in a fresh single-threaded process: the oracle, as it stands, on every workload of
+    the hot path, each for about ``budget_s`` seconds of work (the tiny one in full; the
+    others on random (sequence, query block, head) units, or random queries for the offset
+    workloads; top-256 at 64K on a fixed 64-block sample, extrapolated linearly in edges).
+    Returns attended edges per second per workload."""
+    from fractions import Fraction
+
+    import numpy as np
+
+    import oracle
+    from oracle import masks as om
+    from workloads import bf16_bits_to_f64, byte_stream, qkv_bits, workload
+    out = {}
+    data_cache = {}
+    for name, over, kind in ORACLE_CONFIGS:
+        cfg = workload(name, **over)
+        key = name + "".join(f"_{k}{v}" for k, v in over.items())
+        rng = np.random.default_rng(0)
+        if name not in data_cache:
+            data_cache.clear()
+            data_cache[name] = qkv_bits(cfg)
+        qb, kb, vb = data_cache[name]
+        if cfg["kind"] == "fib":
+            W = cfg["window"]
+            alpha = Fraction(*cfg["alpha_lo"])
+            offs = oracle.fib_offsets(alpha, oracle.fib_rungs(cfg["n_rungs"]))
+            deltas = sorted(set(range(W + 1)) | set(offs))
+            bt, n, h = cfg["batch"], cfg["n_tokens"], cfg["heads"]
+            edges, t0, k = 0, time.perf_counter(), 0
+            while time.perf_counter() - t0 < budget_s:
+                smp = [(int(rng.integers(bt)), int(rng.integers(n)), int(rng.integers(h))) for _ in range(64)]
+                oracle.attention_offsets(qb, kb, vb, W, offs, samples=smp, convert=bf16_bits_to_f64)
+                edges += sum(sum(1 for dd in deltas if dd <= i) for _, i, _ in smp)
+                k += len(smp)
+            secs = time.perf_counter() - t0
+            out[key] = {"edges_per_s": edges / secs, "tflops": 4 * edges * cfg["head_dim"] / secs / 1e12,
+                        "kind": kind, "units": k, "unit": "query (one head)", "seconds": secs}
+            continue
+        b, n, h, d, bt = cfg["block"], cfg["n_tokens"], cfg["heads"], cfg["head_dim"], cfg["batch"]
+        causal = cfg.get("causal", 1)
+        if cfg["kind"] == "topk":
+            p = om.MaskParams("topk", b, n, 1, cfg["window_blocks"], cfg["global_blocks"], cfg["topk"])
+            ratios = oracle.block_ratios(byte_stream(cfg), b)
+            rp, ci = om.build_csr(p, ratios, bt)
+        elif cfg["kind"] == "bigbird":
+            p = om.MaskParams("bigbird", b, n, 0, cfg["window_tokens"] // b, cfg["global_tokens"] // b, 0,
+                              cfg["random_tokens"] // b, cfg["seed"])
+            rp, ci = om.build_csr(p, None, 1)
+        else:
+            p = om.MaskParams("full", b, n, causal)
+            rp, ci = om.build_csr(p, None, 1)
+        nb = n // b
+
+        def unit_edges(s, I):
+            cs = s if rp.shape[0] > 1 else 0
+            row = ci[rp[cs, I]:rp[cs, I + 1]]
+            if causal:
+                return int(np.sum(row < I)) * b * b + int(np.sum(row == I)) * b * (b + 1) // 2
+            return len(row) * b * b
+
+        if kind == "full":
+            t0 = time.perf_counter()
+            oracle.attention_csr(bf16_bits_to_f64(qb), bf16_bits_to_f64(kb), bf16_bits_to_f64(vb), rp, ci, b, causal)
+            secs = time.perf_counter() - t0
+            edges = sum(unit_edges(s, I) for s in range(bt) for I in range(nb)) * h
+            out[key] = {"edges_per_s": edges / secs, "tflops": 4 * edges * d / secs / 1e12, "kind": kind,
+                        "units": bt * nb * h, "unit": "whole workload", "seconds": secs}
+            continue
+        units = [(int(rng.integers(bt)), int(rng.integers(nb)), int(rng.integers(h))) for _ in range(4096)]
+        if kind == "extrapolated":
+            units = units[:64]
+        edges, t0, k = 0, time.perf_counter(), 0
+        while k < len(units) and (kind == "extrapolated" or time.perf_counter() - t0 < budget_s):
+            s_, I, hh = units[k]
+            oracle.attention_csr_block(qb, kb, vb, rp, ci, b, causal, s_, I, hh, convert=bf16_bits_to_f64)
+            edges += unit_edges(s_, I)
+            k += 1
+        secs = time.perf_counter() - t0
+        rate = edges / secs
+        entry = {"edges_per_s": rate, "tflops": 4 * rate * d / 1e12, "kind": kind, "units": k,
+                 "unit": "(sequence, query block, head)", "seconds": secs}
+        if kind == "extrapolated":
+            total_edges = sum(unit_edges(s, I) for s in range(bt) for I in range(nb)) * h
+            entry["whole_workload_seconds_extrapolated"] = total_edges / rate
+        out[key] = entry
+    return out
+
+
+def _run_oracle_configs_child(budget_s: float) -> dict:
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    code = ("import json,sys; sys.path.insert(0, %r); import bench; "
+            "print(json.dumps(bench._oracle_configs_child(%r)))" % (ROOT, budget_s))
+    res = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=1800)
+    if res.returncode != 0:
+        raise RuntimeError("oracle child failed:\n" + res.stderr[-2000:])
+    return json.loads(res.stdout.strip().splitlines()[-1])
 
 
 def _run_oracle_child(budget_s: float, units_per_step: int, steps: int) -> dict:
@@ -513,73 +614,7 @@ def run_ours(args):
     assert sa.sa_device_status() == 0
 
     # ---------------- end to end through the C ABI from host buffers
-    # Steps are pipelined over three streams with two device buffer sets: the uploads of
-    # step i + 1 (and the host ratios) overlap the kernels of step i and the download of step
-    # i - 1. Each step still uploads its Q/K/V and ratios from pinned host memory and reads
-    # its O and LSE back; the time per step is the whole run divided by the steps.
-    pinned = [t.pin_memory() for t in case.qkv_host]
-    nbk = cfg["n_tokens"] // cfg["block"]
-    ratios_pinned = [torch.empty((cfg["batch"], nbk), dtype=torch.float32).pin_memory() for _ in range(2)]
-    o_host = [torch.empty(case.o.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    lse_host = [torch.empty(case.lse.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
-    h2d = sum(t.numel() * t.element_size() for t in pinned) + ratios_pinned[0].numel() * 4
-    d2h = o_host[0].numel() * 2 + lse_host[0].numel() * 4
-    bufs = []
-    for bi in range(2):
-        if bi == 0:
-            bq, bk, bv, br, brp, bci, bo, bl = (case.q, case.k, case.v, case.ratios, case.row_ptr, case.col_idx,
-                                               case.o, case.lse)
-        else:
-            bq, bk, bv, br = (torch.empty_like(x) for x in (case.q, case.k, case.v, case.ratios))
-            brp, bci, bo, bl = (torch.empty_like(x) for x in (case.row_ptr, case.col_idx, case.o, case.lse))
-        bufs.append((bq, bk, bv, br, brp, bci, bo, bl))
-    s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-    ev_in = [torch.cuda.Event() for _ in range(2)]
-    ev_comp = [torch.cuda.Event() for _ in range(2)]
-    ev_out = [torch.cuda.Event() for _ in range(2)]
-    started = [False, False]
-
-    def e2e_step(i):
-        b = i & 1
-        bq, bk, bv, br, brp, bci, bo, bl = bufs[b]
-        if started[b]:
-            ev_in[b].synchronize()           # the previous upload from ratios_pinned[b] is done
-        ratios_pinned[b].numpy()[...] = sa.sa_block_ratios(case.bytes_host, cfg["block"])
-        with torch.cuda.stream(s_in):
-            if started[b]:
-                s_in.wait_event(ev_comp[b])  # step i - 2 has finished reading buffer set b
-            bq.copy_(pinned[0], non_blocking=True)
-            bk.copy_(pinned[1], non_blocking=True)
-            bv.copy_(pinned[2], non_blocking=True)
-            br.copy_(ratios_pinned[b], non_blocking=True)
-            ev_in[b].record(s_in)
-        with torch.cuda.stream(s_comp):
-            s_comp.wait_event(ev_in[b])
-            if started[b]:
-                s_comp.wait_event(ev_out[b])  # O / LSE of step i - 2 have been read back
-            sa.sa_build_mask(case.params, br, brp, bci)
-            sa.sa_attn_fwd(bq, bk, bv, brp, bci, case.block, case.causal, bo, bl, case.csr_shared)
-            ev_comp[b].record(s_comp)
-        with torch.cuda.stream(s_out):
-            if started[b]:
-                ev_out[b].synchronize()        # the host may reuse o_host[b] / lse_host[b]
-            s_out.wait_event(ev_comp[b])
-            o_host[b].copy_(bo, non_blocking=True)
-            lse_host[b].copy_(bl, non_blocking=True)
-            ev_out[b].record(s_out)
-        started[b] = True
-
-    e2e_steps = max(6, min(50, args.steps // 10))
-    for i in range(4):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    barrier()
-    te0 = time.perf_counter()
-    for i in range(e2e_steps):
-        e2e_step(i)
-    torch.cuda.synchronize()                   # every step's O and LSE are on the host
-    te = max_over_ranks((time.perf_counter() - te0) / e2e_steps)
-    e2e_value = aggregate_rate(world, case.flops, te) / 1e12
+    e2e = _measure_e2e(torch, sa, case, cfg, barrier, max_over_ranks, world)
     # host ratio pass alone, one 8192-byte sequence: the workload's blocks (64 bytes, zlib
     # level 6) and the compression paper's (128 bytes, level 1; "< 1 ms for N = 8192")
     one_seq = case.bytes_host[:1]
@@ -594,7 +629,6 @@ def run_ours(args):
     # ---------------- other hot-path rows (kernel time only)
     rows = {}
     if not args.no_rows:
-        del pinned, o_host, lse_host, bufs
         rows = _measure_rows(torch, sa, dev, flush, peaks, max_over_ranks)
 
     # ---------------- CPU baseline (rank 0, N = 1 only)
@@ -603,9 +637,12 @@ def run_ours(args):
         res = _run_oracle_child(args.cpu_seconds, 0, 0)["single"]
         cpu = {"value": res["flops"] / res["seconds"] / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": f"{res['units']} random (sequence, query block, head) units of the same workload "
-                         f"({res['seconds']:.1f} s, numpy float64, 1 BLAS thread)"}
+                         f"({res['seconds']:.1f} s, numpy float64, 1 BLAS thread)",
+               "host_cpu_count": os.cpu_count(), "blas_threads": 1}
+        if not args.no_cpu_configs:
+            cpu["per_workload"] = _run_oracle_configs_child(args.cpu_config_seconds)
 
-    traffic = _profile_traffic("attn_fwd_bytelm_topk_8k.md", ["attn_fwd.cu", "ptx_sm100.cuh", "csr_union.cuh"])
+    traffic = None   # DRAM bytes come from an ncu capture, which this timed run does not take
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
@@ -622,11 +659,7 @@ def run_ours(args):
                      "algorithmic_flops_per_launch": case.flops,
                      "frac_of_sustained": attn_tflops / peaks["bf16_tflops_sustained"]
                      if peaks.get("bf16_tflops_sustained") else None},
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": te * 1e3, "includes": "per step: host zlib ratios, H2D Q+K+V+ratios, mask, "
-                                                      "attention, D2H O+LSE; steps pipelined over three streams "
-                                                      "with two buffer sets",
-                "host_ratio_ms_per_8k_sequence": ratio_ms},
+        "e2e": dict(e2e, host_ratio_ms_per_8k_sequence=ratio_ms),
         "gpu_launches": 2 * args.steps,
         "clocks": clk,
         "rows": rows,
@@ -636,6 +669,111 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+E2E_STEPS = 60      # timed end-to-end steps, whatever --steps says (a fixed, long enough sample)
+E2E_WARM = 6
+
+
+def _measure_e2e(torch, sa, case, cfg, barrier, max_over_ranks, world) -> dict:
+    """The headline workload end to end through the C ABI from host buffers.
+
+    Each step uploads its Q, K, V from pinned host memory, runs the mask step from the host
+    bytes (sa_build_mask_from_bytes: host zlib ratios on the library's threads, their upload
+    and the CSR build), the attention, and reads O and LSE back into pinned host memory.
+    Steps are pipelined over three streams (uploads, compute, downloads) with two device
+    buffer sets, so the uploads of step i + 1 and the host ratios overlap the kernels of step
+    i and the downloads of step i - 1. Reported: the mean time per step over E2E_STEPS steps
+    (wall clock, from the first enqueue to the last download), and per stage the median of
+    the per-step durations (CUDA events on each stream; host time for the ratio call)."""
+    import numpy as np
+
+    nbk = cfg["n_tokens"] // cfg["block"]
+    pinned = [t.pin_memory() for t in case.qkv_host]
+    ratios_pinned = [torch.empty((cfg["batch"], nbk), dtype=torch.float32).pin_memory() for _ in range(2)]
+    o_host = [torch.empty(case.o.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    lse_host = [torch.empty(case.lse.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in pinned) + ratios_pinned[0].numel() * 4
+    d2h = o_host[0].numel() * 2 + lse_host[0].numel() * 4
+    bufs = []
+    for bi in range(2):
+        if bi == 0:
+            bufs.append((case.q, case.k, case.v, case.ratios, case.row_ptr, case.col_idx, case.o, case.lse))
+        else:
+            bufs.append(tuple(torch.empty_like(x) for x in (case.q, case.k, case.v, case.ratios, case.row_ptr,
+                                                             case.col_idx, case.o, case.lse)))
+    s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    total = E2E_WARM + E2E_STEPS
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(total)]
+    host_ratio_s = []
+    started = [False, False]
+
+    def step(i):
+        b = i & 1
+        bq, bk, bv, br, brp, bci, bo, bl = bufs[b]
+        m = marks[i]
+        with torch.cuda.stream(s_in):
+            if started[b]:
+                s_in.wait_event(ev_comp[b])   # step i - 2 has finished reading buffer set b
+            m[0].record(s_in)
+            bq.copy_(pinned[0], non_blocking=True)
+            bk.copy_(pinned[1], non_blocking=True)
+            bv.copy_(pinned[2], non_blocking=True)
+            m[1].record(s_in)
+            ev_in[b].record(s_in)
+        if started[b]:
+            ev_comp[b].synchronize()          # step i - 2's ratio upload from ratios_pinned[b] is done
+        with torch.cuda.stream(s_comp):
+            if started[b]:
+                s_comp.wait_event(ev_out[b])  # O / LSE of step i - 2 have been read back
+            m[2].record(s_comp)
+            r0 = time.perf_counter()
+            sa.sa_build_mask_from_bytes(case.params, case.bytes_host, ratios_pinned[b], br, brp, bci)
+            host_ratio_s.append(time.perf_counter() - r0)
+            s_comp.wait_event(ev_in[b])
+            sa.sa_attn_fwd(bq, bk, bv, brp, bci, case.block, case.causal, bo, bl, case.csr_shared)
+            m[3].record(s_comp)
+            ev_comp[b].record(s_comp)
+        with torch.cuda.stream(s_out):
+            if started[b]:
+                ev_out[b].synchronize()       # the host may reuse o_host[b] / lse_host[b]
+            s_out.wait_event(ev_comp[b])
+            m[4].record(s_out)
+            o_host[b].copy_(bo, non_blocking=True)
+            lse_host[b].copy_(bl, non_blocking=True)
+            m[5].record(s_out)
+            ev_out[b].record(s_out)
+        started[b] = True
+
+    for i in range(E2E_WARM):
+        step(i)
+    torch.cuda.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    for i in range(E2E_WARM, total):
+        step(i)
+    torch.cuda.synchronize()                  # every step's O and LSE are on the host
+    te = max_over_ranks((time.perf_counter() - t0) / E2E_STEPS)
+    timed = marks[E2E_WARM:]
+    stage = {
+        "h2d_qkv_ms": float(np.median([m[0].elapsed_time(m[1]) for m in timed])),
+        "mask_and_attention_ms": float(np.median([m[2].elapsed_time(m[3]) for m in timed])),
+        "d2h_o_lse_ms": float(np.median([m[4].elapsed_time(m[5]) for m in timed])),
+        "host_ratio_call_ms": float(np.median(host_ratio_s[E2E_WARM:]) * 1e3),
+    }
+    bound = max(stage, key=stage.get)
+    return {"value": aggregate_rate(world, case.flops, te) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": te * 1e3, "steps": E2E_STEPS, "warmup": E2E_WARM,
+            "stages_median_ms": stage, "slowest_stage": bound,
+            "h2d_gbs": h2d / 1e9 / (stage["h2d_qkv_ms"] * 1e-3), "d2h_gbs": d2h / 1e9 / (stage["d2h_o_lse_ms"] * 1e-3),
+            "host": {"os_cpu_count": os.cpu_count(), "ratio_threads": "hardware concurrency",
+                     "platform": platform.machine()},
+            "includes": "per step: H2D Q+K+V (pinned), host zlib ratios + their H2D + mask build "
+                        "(sa_build_mask_from_bytes), attention, D2H O+LSE (pinned); three streams, two "
+                        "buffer sets"}
 
 
 def _measure_rows(torch, sa, dev, flush, peaks, max_over_ranks, only=None, steps=10, warm=3) -> dict:
@@ -750,6 +888,9 @@ def main():
     ap.add_argument("--no-rows", action="store_true", help="skip the other hot-path rows")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-configs", action="store_true", help="skip the oracle timing of the other workloads")
+    ap.add_argument("--cpu-config-seconds", type=float, default=1.5,
+                    help="oracle seconds per workload in the per-workload CPU timing")
     ap.add_argument("--only-row", choices=["bigbird_16k", "long_topk_64k", "cas_heads_8k", "bwd_bytelm_topk_8k",
                                            "fib_8k_16_layers",
                                            "fib_8k_coprime_16_layers", "pow2_8k_16_layers", "fib_interp_8k_16_layers",

@@ -718,29 +718,49 @@ __device__ void softmax_epilogue(const Params& p, int x, PipeBars& bars, const B
       }
       const uint64_t negm2 = f2_pack(-m_use, -m_use);
       uint64_t rs[2] = {0ull, 0ull};
-      uint32_t pk[16];
+      if constexpr (C::ALIAS) {
+        // P over S: QK_g was issued after PV_{g-1} completed, so P may be stored chunk by
+        // chunk as it is computed (fewer live registers at d = 128)
+        uint32_t pk[16];
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        if ((vis >> ch) & 1) {
-          chunk_exp(v + 32 * ch, c2, negm2, pk, rs);
-        } else {
+        for (int ch = 0; ch < 4; ++ch) {
+          if ((vis >> ch) & 1) {
+            chunk_exp(v + 32 * ch, c2, negm2, pk, rs);
+          } else {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) pk[j] = 0u;
-        }
-        if (ch == 0) {
-          // PV_{g-1} has read P and finished writing O (with P over S this holds already:
-          // QK_g was issued after PV_{g-1} completed, and S_g is here)
-          if (!C::ALIAS && g > 0) {
-            ok = __all_sync(0xffffffffu,
-                            wait_bar(&bars.v_empty[(g - 1) % C::VS], (uint32_t)((g - 1) / C::VS) & 1u, abort_flag));
-            if (!ok) break;
-            tc_fence_after();
+            for (int j = 0; j < 16; ++j) pk[j] = 0u;
           }
-          if (__any_sync(0xffffffffu, o_scale)) rescale_o<D>(tO, alpha);
+          // the rare O rescale once chunk 0's scores are consumed (registers for O's chunk)
+          if (ch == 0 && __any_sync(0xffffffffu, o_scale)) rescale_o<D>(tO, alpha);
+          if (ch < nch) tmem_st_x16(tP + 16 * ch, pk);
         }
-        if (ch < nch) tmem_st_x16(tP + 16 * ch, pk);
+      } else {
+        // All exponentials of the tile first (P_j packed in registers; the scores' registers
+        // are reused as they die): only the stores of P wait for PV_{j-1}, so the tensor
+        // core's PV and the next QK run under this tile's exponentials instead of in series
+        // with them.
+        uint32_t pk[64];
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          if ((vis >> ch) & 1) {
+            chunk_exp(v + 32 * ch, c2, negm2, pk + 16 * ch, rs);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) pk[16 * ch + j] = 0u;
+          }
+        }
+        // PV_{g-1} has read P and finished writing O
+        if (g > 0) {
+          ok = __all_sync(0xffffffffu,
+                          wait_bar(&bars.v_empty[(g - 1) % C::VS], (uint32_t)((g - 1) / C::VS) & 1u, abort_flag));
+          if (!ok) break;
+          tc_fence_after();
+        }
+        if (__any_sync(0xffffffffu, o_scale)) rescale_o<D>(tO, alpha);
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch)
+          if (ch < nch) tmem_st_x16(tP + 16 * ch, pk + 16 * ch);
       }
-      if (!ok) break;
       {
         const uint64_t rs2 = f2_add(rs[0], rs[1]);
         float rs_lo, rs_hi;
