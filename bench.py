@@ -220,6 +220,8 @@ class BlockSparseCase:
         self.row_ptr, self.col_idx = self.csrs[0]
         self.o = torch.empty_like(self.q)
         self.lse = torch.empty((bt, cfg["heads"], n), dtype=torch.float32, device=dev)
+        # the forward's workspace (work counter, split plan and partial results), allocated once
+        self.ws = sa.fwd_workspace(self.q, b, self.csr_shared, len(self.csrs))
         self.step()
         torch.cuda.synchronize()
         heads_of = ([cfg["heads"]] if self.head_mask is None else
@@ -237,10 +239,10 @@ class BlockSparseCase:
     def attend(self):
         if self.head_mask is None:
             self.sa.sa_attn_fwd(self.q, self.k, self.v, self.row_ptr, self.col_idx, self.block, self.causal, self.o,
-                                self.lse, self.csr_shared)
+                                self.lse, self.csr_shared, workspace=self.ws)
         else:
             self.sa.sa_attn_fwd_heads(self.q, self.k, self.v, self.csrs, self.head_mask, self.block, self.causal,
-                                      self.o, self.lse, self.csr_shared)
+                                      self.o, self.lse, self.csr_shared, workspace=self.ws)
 
     def step(self):
         self.build()
@@ -698,10 +700,10 @@ def _measure_e2e(torch, sa, case, cfg, barrier, max_over_ranks, world) -> dict:
     bufs = []
     for bi in range(2):
         if bi == 0:
-            bufs.append((case.q, case.k, case.v, case.ratios, case.row_ptr, case.col_idx, case.o, case.lse))
+            bufs.append((case.q, case.k, case.v, case.ratios, case.row_ptr, case.col_idx, case.o, case.lse, case.ws))
         else:
             bufs.append(tuple(torch.empty_like(x) for x in (case.q, case.k, case.v, case.ratios, case.row_ptr,
-                                                             case.col_idx, case.o, case.lse)))
+                                                             case.col_idx, case.o, case.lse, case.ws)))
     s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_comp = [torch.cuda.Event() for _ in range(2)]
@@ -713,7 +715,7 @@ def _measure_e2e(torch, sa, case, cfg, barrier, max_over_ranks, world) -> dict:
 
     def step(i):
         b = i & 1
-        bq, bk, bv, br, brp, bci, bo, bl = bufs[b]
+        bq, bk, bv, br, brp, bci, bo, bl, bws = bufs[b]
         m = marks[i]
         with torch.cuda.stream(s_in):
             if started[b]:
@@ -734,7 +736,7 @@ def _measure_e2e(torch, sa, case, cfg, barrier, max_over_ranks, world) -> dict:
             sa.sa_build_mask_from_bytes(case.params, case.bytes_host, ratios_pinned[b], br, brp, bci)
             host_ratio_s.append(time.perf_counter() - r0)
             s_comp.wait_event(ev_in[b])
-            sa.sa_attn_fwd(bq, bk, bv, brp, bci, case.block, case.causal, bo, bl, case.csr_shared)
+            sa.sa_attn_fwd(bq, bk, bv, brp, bci, case.block, case.causal, bo, bl, case.csr_shared, workspace=bws)
             m[3].record(s_comp)
             ev_comp[b].record(s_comp)
         with torch.cuda.stream(s_out):

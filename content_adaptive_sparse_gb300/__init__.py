@@ -59,11 +59,12 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.sa_build_mask.argtypes = [ctypes.POINTER(MaskParams), _P, _P, _P, ctypes.c_int64, _P]
     lib.sa_attn_fwd.argtypes = [_P, _P, _P, _I64x3, _I64x3, _I64x3, ctypes.c_int32, ctypes.c_int32,
                                 ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-                                _P, _P, ctypes.c_int32, ctypes.c_float, _P, _P, _P]
+                                _P, _P, ctypes.c_int32, ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P]
     lib.sa_attn_fwd_heads.argtypes = [_P, _P, _P, _I64x3, _I64x3, _I64x3, ctypes.c_int32, ctypes.c_int32,
                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                       ctypes.c_int32, ctypes.c_int32, _P, _P, _P, ctypes.c_int32, ctypes.c_float,
-                                      _P, _P, _P]
+                                      _P, _P, _P, ctypes.c_size_t, _P]
+    lib.sa_attn_fwd_workspace_size.argtypes = [ctypes.c_int32] * 7 + [_P]
     lib.sa_attn_bwd_workspace_size.argtypes = [ctypes.c_int32] * 5 + [ctypes.c_int64, _P]
     lib.sa_attn_bwd.argtypes = [_P, _P, _P, _P, _P, _P, _I64x3, _I64x3, _I64x3] + [ctypes.c_int32] * 7 + \
         [_P, _P, ctypes.c_int32, ctypes.c_float, _P, _P, _P, _P, ctypes.c_size_t, _P]
@@ -87,7 +88,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
                                              _P, _P, ctypes.c_int64, _P]
     lib.sa_device_status.argtypes = [_P]
     lib.sa_selftest_bounded_wait.argtypes = [_P]
-    for name in ("sa_mask_nnz_bound", "sa_build_mask", "sa_attn_fwd", "sa_attn_fwd_heads", "sa_attn_bwd",
+    for name in ("sa_mask_nnz_bound", "sa_build_mask", "sa_attn_fwd", "sa_attn_fwd_heads", "sa_attn_fwd_workspace_size",
+                 "sa_attn_bwd",
                  "sa_attn_bwd_noalloc", "sa_attn_bwd_heads", "sa_attn_bwd_workspace_size", "sa_offset_attn_fwd", "sa_offset_attn_fwd_list",
                  "sa_offset_attn_interp_fwd", "sa_fib_offsets", "sa_pow2_offsets", "sa_layer_alpha", "sa_block_ratios",
                  "sa_device_status", "sa_selftest_bounded_wait", "sa_build_mask_from_bytes"):
@@ -135,19 +137,38 @@ def sa_build_mask(params: MaskParams, ratio, row_ptr, col_idx, stream=None) -> N
                                                           col_idx.data_ptr(), col_idx.numel(), _stream_ptr(stream)))
 
 
+def sa_attn_fwd_workspace_size(batch: int, n_tokens: int, heads: int, head_dim: int, block: int,
+                               csr_batches: int, n_masks: int = 1) -> int:
+    out = ctypes.c_size_t(0)
+    _check("sa_attn_fwd_workspace_size", load_library().sa_attn_fwd_workspace_size(
+        batch, n_tokens, heads, head_dim, block, csr_batches, n_masks, ctypes.byref(out)))
+    return int(out.value)
+
+
+def fwd_workspace(q, block: int, csr_shared: bool = False, n_masks: int = 1):
+    """A device workspace of sa_attn_fwd_workspace_size bytes for q's shape (uint8 tensor)."""
+    import torch
+    b, n, h, d = q.shape
+    nbytes = sa_attn_fwd_workspace_size(b, n, h, d, block, 1 if csr_shared else b, n_masks)
+    return torch.empty((nbytes,), dtype=torch.uint8, device=q.device)
+
+
 def sa_attn_fwd(q, k, v, row_ptr, col_idx, block: int, causal: int, o, lse, csr_shared: bool = False,
-                softmax_scale: float | None = None, stream=None) -> None:
+                softmax_scale: float | None = None, stream=None, workspace=None) -> None:
+    """``workspace``: a uint8 device tensor (see fwd_workspace); one is allocated on the current
+    stream when omitted."""
     b, n, h, d = q.shape
     hkv = k.shape[2]
     scale = 1.0 / float(np.sqrt(d)) if softmax_scale is None else float(softmax_scale)
+    ws = fwd_workspace(q, block, csr_shared) if workspace is None else workspace
     _check("sa_attn_fwd", load_library().sa_attn_fwd(
         q.data_ptr(), k.data_ptr(), v.data_ptr(), _strides(q), _strides(k), _strides(o), b, n, h, hkv, d, block,
         int(causal), row_ptr.data_ptr(), col_idx.data_ptr(), int(bool(csr_shared)), scale, o.data_ptr(),
-        lse.data_ptr(), _stream_ptr(stream)))
+        lse.data_ptr(), ws.data_ptr(), ws.numel() * ws.element_size(), _stream_ptr(stream)))
 
 
 def sa_attn_fwd_heads(q, k, v, csrs, head_mask, block: int, causal: int, o, lse, csr_shared: bool = False,
-                      softmax_scale: float | None = None, stream=None) -> None:
+                      softmax_scale: float | None = None, stream=None, workspace=None) -> None:
     """``csrs``: list of (row_ptr, col_idx) device tensors; query head h uses
     ``csrs[head_mask[h]]``."""
     b, n, h, d = q.shape
@@ -159,10 +180,11 @@ def sa_attn_fwd_heads(q, k, v, csrs, head_mask, block: int, causal: int, o, lse,
     if hm.shape != (h,):
         raise ValueError("head_mask needs one CSR index per query head")
     scale = 1.0 / float(np.sqrt(d)) if softmax_scale is None else float(softmax_scale)
+    ws = fwd_workspace(q, block, csr_shared, nm) if workspace is None else workspace
     _check("sa_attn_fwd_heads", load_library().sa_attn_fwd_heads(
         q.data_ptr(), k.data_ptr(), v.data_ptr(), _strides(q), _strides(k), _strides(o), b, n, h, hkv, d, block,
         int(causal), nm, ctypes.cast(rps, _P), ctypes.cast(cis, _P), hm.ctypes.data, int(bool(csr_shared)), scale,
-        o.data_ptr(), lse.data_ptr(), _stream_ptr(stream)))
+        o.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel() * ws.element_size(), _stream_ptr(stream)))
 
 
 def sa_attn_bwd_workspace_size(batch: int, n_tokens: int, heads: int, block: int, csr_batches: int,

@@ -58,10 +58,6 @@ namespace {
 
 __device__ unsigned int g_attn_err;
 
-// Work counters (one slot per launch in flight, round robin, zeroed on the launch's stream).
-constexpr int kWorkSlots = 64;
-__device__ unsigned int g_work_counters[kWorkSlots];
-
 constexpr int kTile = 128;            // query rows per work item
 constexpr int kKeys = 128;            // keys per S tile (four 32-key chunks)
 constexpr int kThreads = 512;         // 16 warps, four warpgroups
@@ -125,6 +121,8 @@ struct __align__(16) Batch {
   int ntiles;                 // key tiles in this entry (0 .. kBatch)
   int item;                   // work item index
   int flags;                  // kFirst | kLast
+  int slot;                   // partial-result slot of a split item's part (-1: the whole item)
+  int pad[3];
   int4 tile[kBatch];          // per key tile and 32-key chunk c (x, y, z, w): first key token
                               // << 4 | membership bits (bit r: query block r); 0 = no chunk
   uint8_t nch[kBatch];        // per key tile: 32-key chunks (1 .. 4); 16-byte aligned
@@ -187,7 +185,14 @@ struct Params {
   int batch, n_tokens, heads, heads_per_kv, block, log2b, nb, causal, csr_shared;
   int tiles_per_seq;          // 128-row query tiles per (sequence, head)
   int n_items;
-  unsigned int* work_counter;          // next item index (zeroed before the launch)
+  unsigned int* work_counter;          // next work-list entry (in the workspace, zeroed before the launch)
+  // Split mode (work_list != nullptr): the schedule kernel's list of (item, part) entries, split
+  // parts first; entry i < n_split is part y of item x, whose key tiles [y T, (y + 1) T) go
+  // to partial-result slot i. Header: list length, n_split, T.
+  const int2* work_list;
+  const int* list_hdr;
+  float* partial;                      // slots of 128 x (d + 1) floats: O rows, then LSE
+  int csr_batches;
   int n_masks;
   const int32_t* row_ptr[kMaxMasks];   // one CSR per head group
   const int32_t* col_idx[kMaxMasks];
@@ -316,11 +321,22 @@ __device__ void planner(const Params& p, PipeBars& bars, Batch* ring, UnionSmem&
   const int qb_per_tile = kTile >> p.log2b;
   int mt = 0;
   bool ok = true;
+  const bool split_mode = p.work_list != nullptr;
+  const int list_len = split_mode ? p.list_hdr[0] : p.n_items;
+  const int n_split = split_mode ? p.list_hdr[1] : 0;
+  const int part_tiles = split_mode ? p.list_hdr[2] : 0;
   for (;;) {
-    int k = 0;
-    if (lane == 0) k = (int)atomicAdd(p.work_counter, 1u);
-    k = __shfl_sync(0xffffffffu, k, 0);
-    const bool done = k >= p.n_items;
+    int idx = 0;
+    if (lane == 0) idx = (int)atomicAdd(p.work_counter, 1u);
+    idx = __shfl_sync(0xffffffffu, idx, 0);
+    const bool done = idx >= list_len;
+    int k = idx, part = 0;
+    if (split_mode && !done) {
+      const int2 ent = p.work_list[idx];
+      k = ent.x;
+      part = ent.y;
+    }
+    const int slot = (split_mode && idx < n_split) ? idx : -1;
     int n_chunks = 0;
     if (!done) {
       const Item it = decode_item(p, k);
@@ -331,8 +347,11 @@ __device__ void planner(const Params& p, PipeBars& bars, Batch* ring, UnionSmem&
       n_chunks = cpb * build_union(p.nb, p.causal ? kKeepLE : kKeepAll, u, rp, p.col_idx[mi], I0, nq, &g_attn_err,
                                    kErrBadIndex);
     }
-    const int n_tiles = (n_chunks + 3) >> 2;
-    for (int t0 = 0;; t0 += kBatch) {
+    const int n_all = (n_chunks + 3) >> 2;
+    // key tiles of this entry: all of the item's, or a split part's range
+    const int t_begin = slot >= 0 ? min(n_all, part * part_tiles) : 0;
+    const int n_tiles = slot >= 0 ? min(n_all, t_begin + part_tiles) : n_all;
+    for (int t0 = t_begin;; t0 += kBatch) {
       const int ms = mt % kMetaRing;
       if (lane == 0) ok = wait_bar(&bars.m_empty[ms], ((mt / kMetaRing) & 1) ^ 1, abort_flag);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -355,9 +374,11 @@ __device__ void planner(const Params& p, PipeBars& bars, Batch* ring, UnionSmem&
         for (int q = 0; q < 4; ++q)
           ring[ms].vq[q][lane] = (uint8_t)quarter_vis(tm, nch, (32 * q) >> p.log2b, tile0 + 32 * q, p.causal);
       }
-      if (lane == 0)
+      if (lane == 0) {
         *reinterpret_cast<int4*>(&ring[ms]) = make_int4(done ? kKindDone : kKindItem, nt, k,
-                                                        (t0 == 0 ? kFirst : 0) | (t0 + kBatch >= n_tiles ? kLast : 0));
+                                                        (t0 == t_begin ? kFirst : 0) | (t0 + kBatch >= n_tiles ? kLast : 0));
+        ring[ms].slot = slot;
+      }
       __syncwarp();                                  // every lane's entry is written before the release
       if (lane == 0) mbar_arrive(&bars.m_full[ms]);
       ++mt;
@@ -650,6 +671,7 @@ __device__ void softmax_epilogue(const Params& p, int x, PipeBars& bars, const B
   float m_use = kNegInf;    // running reference max, log2 units
   float l = 0.f;            // row sum
   int n_item = 0;           // key tiles of the current item
+  int slot = -1;            // partial-result slot of a split item's part (-1: write O and LSE)
   for (int mt = 0;; ++mt) {
     int4 hdr;
     ok = __all_sync(0xffffffffu, wait_batch(bars, ring, mt, hdr, abort_flag));
@@ -666,6 +688,7 @@ __device__ void softmax_epilogue(const Params& p, int x, PipeBars& bars, const B
       m_use = kNegInf;
       l = 0.f;
       n_item = 0;
+      slot = e.slot;
     }
     // this quarter's visibility bytes and the chunk counts of the batch's tiles
     const uint4 vqw = ld_shared_u4(&e.vq[quarter][0]);
@@ -785,8 +808,31 @@ __device__ void softmax_epilogue(const Params& p, int x, PipeBars& bars, const B
       if (!ok) break;
       tc_fence_after();
     }
-    const bool store = qtok < p.n_tokens;
     const float inv = l > 0.f ? 1.f / l : 0.f;
+    if (slot >= 0) {
+      // a part of a split item: O / l of its key range (fp32) and its LSE, merged later
+      float* po = p.partial + (size_t)slot * (kTile * (D + 1)) + (size_t)row * D;
+#pragma unroll
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t ov[32];
+        if (n_item > 0) {
+          tmem_ld_x32(tO + 32 * ch, ov);
+          tmem_ld_wait<32>(ov);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) ov[j] = 0u;
+        }
+        float4* dst = reinterpret_cast<float4*>(po + ch * 32);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          dst[j] = make_float4(__uint_as_float(ov[4 * j]) * inv, __uint_as_float(ov[4 * j + 1]) * inv,
+                               __uint_as_float(ov[4 * j + 2]) * inv, __uint_as_float(ov[4 * j + 3]) * inv);
+      }
+      p.partial[(size_t)slot * (kTile * (D + 1)) + (size_t)kTile * D + row] =
+          l > 0.f ? (m_use + __log2f(l)) * 0.69314718055994531f : kNegInf;
+      continue;
+    }
+    const bool store = qtok < p.n_tokens;
     __nv_bfloat16* orow = p.o + (int64_t)it.s * p.o_sb + (int64_t)qtok * p.o_sn + (int64_t)it.h * p.o_sh;
 #pragma unroll
     for (int ch = 0; ch < D / 32; ++ch) {
@@ -907,6 +953,247 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ------------------------------------------------------------------ split-row combine (K9)
+//
+// Used when a launch has fewer work items than twice the pipelines of the GPU: a few long key
+// lists would then leave SMs idle. fwd_plan_kernel counts the key tiles of every query tile's
+// union (one warp per (mask, CSR sequence, query tile)), fwd_schedule_kernel (one CTA) cuts the
+// items whose lists are longer than T tiles into parts of T tiles, each with a slot for its
+// partial result, and lists the parts first, then the other items; attn_fwd_kernel runs the
+// list; fwd_merge_kernel combines the parts of each split item:
+//   LSE = ln sum_p exp(LSE_p),  O = sum_p exp(LSE_p - LSE) O_p.
+
+struct SplitHdr {
+  int list_len, n_split, part_tiles, n_split_items;
+};
+
+constexpr int kPlanWarps = 8;
+constexpr int kMinPartTiles = 4;
+
+__global__ void __launch_bounds__(32 * kPlanWarps) fwd_plan_kernel(const __grid_constant__ Params p, int n_groups,
+                                                                    int* tiles) {
+  __shared__ uint32_t bm[kPlanWarps][kMaxMaskBlocks / 32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = blockIdx.x * kPlanWarps + warp;
+  if (g >= n_groups) return;                         // the whole warp leaves
+  const int t = g % p.tiles_per_seq;
+  const int cs = (g / p.tiles_per_seq) % p.csr_batches;
+  const int m = g / (p.tiles_per_seq * p.csr_batches);
+  const int nb = p.nb, nw = (nb + 31) >> 5;
+  const int32_t* rp = p.row_ptr[m] + (size_t)cs * (nb + 1);
+  const int32_t* ci = p.col_idx[m];
+  const int I0 = (t * kTile) >> p.log2b;
+  const int nq = min(kTile >> p.log2b, nb - I0);
+  for (int w = lane; w < nw; w += 32) bm[warp][w] = 0u;
+  __syncwarp();
+  for (int r = 0; r < nq; ++r) {
+    const int e1 = rp[I0 + r + 1];
+    for (int e = rp[I0 + r] + lane; e < e1; e += 32) {
+      const int X = ci[e];
+      if (X >= 0 && X < nb && (!p.causal || X <= I0 + r)) atomicOr(&bm[warp][X >> 5], 1u << (X & 31));
+    }
+  }
+  __syncwarp();
+  int cnt = 0;
+  for (int w = lane; w < nw; w += 32) cnt += __popc(bm[warp][w]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+  if (lane == 0) tiles[g] = (cnt * (p.block >> 5) + 3) >> 2;   // 32-key chunks, four per key tile
+}
+
+// Block-wide exclusive scan of one int per thread (1024 threads); returns the total too.
+__device__ __forceinline__ int block_scan_excl(int v, int* warp_sums, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  __syncthreads();
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_sums[lane] = w;
+  }
+  __syncthreads();
+  total = warp_sums[31];
+  return (warp > 0 ? warp_sums[warp - 1] : 0) + incl - v;
+}
+
+// Key tiles of work item k (its query tile's union, from the plan).
+__device__ __forceinline__ int item_tiles(const Params& p, const int* tiles, int k) {
+  const Item it = decode_item(p, k);
+  const int m = p.n_masks > 1 ? p.head_mask[it.h] : 0;
+  const int cs = p.csr_shared ? 0 : it.s;
+  return tiles[(m * p.csr_batches + cs) * p.tiles_per_seq + it.tile];
+}
+
+__global__ void __launch_bounds__(1024) fwd_schedule_kernel(const __grid_constant__ Params p, const int* tiles,
+                                                             int slot_cap, int n_pipes, int2* list, int4* split_items,
+                                                             SplitHdr* hdr) {
+  __shared__ int warp_sums[32];
+  __shared__ int s_T;
+  const int n = p.n_items;
+  const int per = (n + 1023) / 1024;
+  const int k0 = min(n, (int)threadIdx.x * per), k1 = min(n, k0 + per);
+  // total work, longest item
+  long long tot = 0;
+  int mx = 0;
+  for (int k = k0; k < k1; ++k) {
+    const int t = item_tiles(p, tiles, k);
+    tot += t;
+    mx = max(mx, t);
+  }
+  // reduce (sum as int: a launch holds far fewer than 2^31 key tiles)
+  int total = 0;
+  block_scan_excl((int)tot, warp_sums, total);
+  int big = mx;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) big = max(big, __shfl_xor_sync(0xffffffffu, big, o));
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) warp_sums[threadIdx.x >> 5] = big;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int b = 0;
+    for (int w = 0; w < 32; ++w) b = max(b, warp_sums[w]);
+    // about two parts of work per pipeline; parts of at least kMinPartTiles key tiles
+    int T = max(kMinPartTiles, (total + 2 * n_pipes - 1) / (2 * n_pipes));
+    s_T = T;
+    warp_sums[0] = b;
+  }
+  __syncthreads();
+  const int longest = warp_sums[0];
+  int T = s_T;
+  __syncthreads();
+  // the smallest T (doubling) whose parts fit the slots
+  for (;;) {
+    int need = 0;
+    for (int k = k0; k < k1; ++k) {
+      const int t = item_tiles(p, tiles, k);
+      if (t > T) need += (t + T - 1) / T;
+    }
+    int need_tot = 0;
+    block_scan_excl(need, warp_sums, need_tot);
+    if (need_tot <= slot_cap || T >= longest) break;
+    T *= 2;
+  }
+  // positions: split parts first (slot = list position), then the unsplit items
+  int n_parts = 0, n_whole = 0, n_si = 0;
+  for (int k = k0; k < k1; ++k) {
+    const int t = item_tiles(p, tiles, k);
+    if (t > T) {
+      n_parts += (t + T - 1) / T;
+      ++n_si;
+    } else {
+      ++n_whole;
+    }
+  }
+  int tot_parts = 0, tot_whole = 0, tot_si = 0;
+  int pos_p = block_scan_excl(n_parts, warp_sums, tot_parts);
+  int pos_w = block_scan_excl(n_whole, warp_sums, tot_whole);
+  int pos_s = block_scan_excl(n_si, warp_sums, tot_si);
+  pos_w += tot_parts;
+  for (int k = k0; k < k1; ++k) {
+    const int t = item_tiles(p, tiles, k);
+    if (t > T) {
+      const int parts = (t + T - 1) / T;
+      split_items[pos_s++] = make_int4(k, parts, pos_p, 0);
+      for (int q = 0; q < parts; ++q) list[pos_p++] = make_int2(k, q);
+    } else {
+      list[pos_w++] = make_int2(k, 0);
+    }
+  }
+  if (threadIdx.x == 0) {
+    hdr->list_len = tot_parts + tot_whole;
+    hdr->n_split = tot_parts;
+    hdr->part_tiles = T;
+    hdr->n_split_items = tot_si;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kTile) fwd_merge_kernel(const __grid_constant__ Params p, const int4* split_items,
+                                                           const SplitHdr* hdr) {
+  const float kNegInf = __int_as_float(0xff800000);
+  const int n_si = hdr->n_split_items;
+  const int r = threadIdx.x;
+  for (int j = blockIdx.x; j < n_si; j += gridDim.x) {
+    const int4 si = split_items[j];
+    const Item it = decode_item(p, si.x);
+    const int qtok = it.tile * kTile + r;
+    if (qtok >= p.n_tokens) continue;
+    const float* base = p.partial + (size_t)si.z * (kTile * (D + 1));
+    float mx = kNegInf;
+    for (int q = 0; q < si.y; ++q) mx = fmaxf(mx, base[(size_t)q * (kTile * (D + 1)) + kTile * D + r]);
+    __nv_bfloat16* orow = p.o + (int64_t)it.s * p.o_sb + (int64_t)qtok * p.o_sn + (int64_t)it.h * p.o_sh;
+    float lse = kNegInf;
+    float acc[D];
+#pragma unroll
+    for (int c = 0; c < D; ++c) acc[c] = 0.f;
+    if (mx != kNegInf) {
+      float wsum = 0.f;
+      for (int q = 0; q < si.y; ++q) {
+        const float* part = base + (size_t)q * (kTile * (D + 1));
+        const float lq = part[kTile * D + r];
+        if (lq == kNegInf) continue;
+        const float w = __expf(lq - mx);
+        wsum += w;
+        const float4* row = reinterpret_cast<const float4*>(part + (size_t)r * D);
+#pragma unroll
+        for (int c = 0; c < D / 4; ++c) {
+          const float4 v = row[c];
+          acc[4 * c] += w * v.x;
+          acc[4 * c + 1] += w * v.y;
+          acc[4 * c + 2] += w * v.z;
+          acc[4 * c + 3] += w * v.w;
+        }
+      }
+      const float inv = 1.f / wsum;
+#pragma unroll
+      for (int c = 0; c < D; ++c) acc[c] *= inv;
+      lse = mx + __logf(wsum);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c)
+      dst[c] = make_uint4(pack_bf16x2(acc[8 * c], acc[8 * c + 1]), pack_bf16x2(acc[8 * c + 2], acc[8 * c + 3]),
+                          pack_bf16x2(acc[8 * c + 4], acc[8 * c + 5]), pack_bf16x2(acc[8 * c + 6], acc[8 * c + 7]));
+    p.lse[((int64_t)it.s * p.heads + it.h) * p.n_tokens + qtok] = lse;
+  }
+}
+
+// Workspace of the forward: the work counter, then (split mode) the split header, the plan's
+// key-tile counts, the work list, the split items and the partial-result slots, each section
+// 256-byte aligned. slot_cap is the number of slots that fit in `bytes`.
+struct FwdWorkspace {
+  size_t counter_off, hdr_off, tiles_off, list_off, items_off, partial_off, min_bytes, slot_cap;
+};
+
+inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+FwdWorkspace fwd_workspace_layout(int64_t n_items, int64_t n_groups, int d, size_t bytes) {
+  FwdWorkspace w;
+  w.counter_off = 0;
+  w.hdr_off = 64;
+  w.min_bytes = 256;
+  w.tiles_off = 256;
+  w.list_off = w.tiles_off + up256((size_t)n_groups * 4);
+  const size_t slot_bytes = (size_t)kTile * (d + 1) * 4;
+  const size_t fixed = w.list_off + up256((size_t)n_items * 8) + 3 * 256;
+  // per slot: one list entry (8 B), at most one split item (16 B), the partial (slot_bytes)
+  w.slot_cap = bytes > fixed ? (bytes - fixed) / (8 + 16 + slot_bytes) : 0;
+  w.items_off = w.list_off + up256((size_t)(n_items + (int64_t)w.slot_cap) * 8);
+  w.partial_off = w.items_off + up256(w.slot_cap * 16);
+  return w;
+}
+
 template <int D>
 int launch_d(const AttnArgs& a, cudaStream_t stream) {
   using C = Cfg<D>;
@@ -943,10 +1230,15 @@ int launch_d(const AttnArgs& a, cudaStream_t stream) {
   p.o_sn = a.o_strides[1];
   p.o_sh = a.o_strides[2];
   p.scale_log2 = a.softmax_scale * 1.4426950408889634f;
-  unsigned int* counters = nullptr;
-  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&counters), g_work_counters) != cudaSuccess) return SA_ERR_CUDA;
-  static std::atomic<unsigned int> ticket{0};
-  p.work_counter = counters + (ticket.fetch_add(1u) % kWorkSlots);
+  p.csr_batches = a.csr_shared ? 1 : a.batch;
+  const int n_groups = a.n_masks * p.csr_batches * p.tiles_per_seq;
+  const FwdWorkspace ws = fwd_workspace_layout(p.n_items, n_groups, D, a.workspace_bytes);
+  if (a.workspace == nullptr || a.workspace_bytes < ws.min_bytes) return SA_ERR_CAPACITY;
+  uint8_t* wsb = static_cast<uint8_t*>(a.workspace);
+  p.work_counter = reinterpret_cast<unsigned int*>(wsb + ws.counter_off);
+  p.work_list = nullptr;
+  p.list_hdr = nullptr;
+  p.partial = nullptr;
   if (cudaMemsetAsync(p.work_counter, 0, sizeof(unsigned int), stream) != cudaSuccess) return SA_ERR_CUDA;
   const int sm_count = current_sm_count();
   auto kern = attn_fwd_kernel<D>;
@@ -957,13 +1249,45 @@ int launch_d(const AttnArgs& a, cudaStream_t stream) {
   if (fa.numRegs != kLaunchRegs) return SA_ERR_UNSUPPORTED;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return SA_ERR_CUDA;
-  const int want = (p.n_items + 1) / 2;
-  const int grid = want < sm_count ? want : sm_count;
+  // Split mode when the items are few for the GPU's pipelines (two per SM) and the workspace
+  // holds partial-result slots: long key lists are then cut into parts (K9).
+  const int n_pipes = 2 * sm_count;
+  const bool split = ws.slot_cap >= 2 && p.n_items < 2 * n_pipes;
+  int grid = (p.n_items + 1) / 2 < sm_count ? (p.n_items + 1) / 2 : sm_count;
+  if (split) {
+    int* tiles = reinterpret_cast<int*>(wsb + ws.tiles_off);
+    int2* list = reinterpret_cast<int2*>(wsb + ws.list_off);
+    int4* split_items = reinterpret_cast<int4*>(wsb + ws.items_off);
+    SplitHdr* hdr = reinterpret_cast<SplitHdr*>(wsb + ws.hdr_off);
+    p.partial = reinterpret_cast<float*>(wsb + ws.partial_off);
+    fwd_plan_kernel<<<(n_groups + kPlanWarps - 1) / kPlanWarps, 32 * kPlanWarps, 0, stream>>>(p, n_groups, tiles);
+    fwd_schedule_kernel<<<1, 1024, 0, stream>>>(p, tiles, (int)ws.slot_cap, n_pipes, list, split_items, hdr);
+    if (cudaGetLastError() != cudaSuccess) return SA_ERR_CUDA;
+    p.work_list = list;
+    p.list_hdr = &hdr->list_len;
+    grid = sm_count;   // the list is at most n_items + slot_cap entries long
+    kern<<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, p);
+    if (cudaGetLastError() != cudaSuccess) return SA_ERR_CUDA;
+    const int mgrid = (int)(ws.slot_cap < (size_t)(2 * sm_count) ? ws.slot_cap : (size_t)(2 * sm_count));
+    fwd_merge_kernel<D><<<mgrid, kTile, 0, stream>>>(p, split_items, hdr);
+    return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+  }
   kern<<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
 }  // namespace
+
+size_t attn_fwd_workspace_bytes(int64_t batch, int64_t n_tokens, int64_t heads, int head_dim, int64_t csr_batches,
+                                int64_t n_masks) {
+  const int64_t tiles_per_seq = (n_tokens + kTile - 1) / kTile;
+  const int64_t n_items = batch * heads * tiles_per_seq;
+  const FwdWorkspace w = fwd_workspace_layout(n_items, n_masks * csr_batches * tiles_per_seq, head_dim, 0);
+  const size_t slot_bytes = (size_t)kTile * (head_dim + 1) * 4;
+  // room for the default number of split parts (about four per SM of a GB300)
+  return w.list_off + up256((size_t)(n_items + kFwdDefaultSlots) * 8) + up256((size_t)kFwdDefaultSlots * 16) +
+         (size_t)kFwdDefaultSlots * slot_bytes + 3 * 256;
+}
 
 int launch_attn_fwd(const AttnArgs& a, cudaStream_t stream) {
   switch (a.head_dim) {

@@ -195,7 +195,7 @@ int sa_attn_fwd_heads(const void* q, const void* k, const void* v, const int64_t
                       int32_t heads, int32_t kv_heads, int32_t head_dim, int32_t block, int32_t causal,
                       int32_t n_masks, const int32_t* const* h_row_ptrs, const int32_t* const* h_col_idxs,
                       const int32_t* h_head_mask, int32_t csr_shared, float softmax_scale, void* o, float* lse,
-                      void* stream) {
+                      void* workspace, size_t workspace_bytes, void* stream) {
   int st = check_attn_common(q, k, v, q_strides, kv_strides, o_strides, batch, n_tokens, heads, kv_heads, o, lse);
   if (st != SA_OK) return st;
   if (n_masks < 1 || !h_row_ptrs || !h_col_idxs || (n_masks > 1 && !h_head_mask)) return SA_ERR_INVALID_ARG;
@@ -212,6 +212,9 @@ int sa_attn_fwd_heads(const void* q, const void* k, const void* v, const int64_t
   if (n_tokens % block != 0) return SA_ERR_UNSUPPORTED;
   if (n_tokens / block > sa::kMaxMaskBlocks) return SA_ERR_UNSUPPORTED;
   if ((int64_t)batch * heads > 65535 * 32 || (n_tokens + 127) / 128 > 65535) return SA_ERR_UNSUPPORTED;
+  if (!workspace) return SA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SA_ERR_UNSUPPORTED;
+  if (workspace_bytes < 256) return SA_ERR_CAPACITY;
   if (!device_ok()) return SA_ERR_CUDA;
   sa::AttnArgs a;
   a.q = q;
@@ -240,17 +243,30 @@ int sa_attn_fwd_heads(const void* q, const void* k, const void* v, const int64_t
   for (int h = 0; h < sa::kMaxHeadMap; ++h)
     a.head_mask[h] = (n_masks > 1 && h < heads) ? (uint8_t)h_head_mask[h] : 0;
   a.softmax_scale = softmax_scale;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
   return sa::launch_attn_fwd(a, static_cast<cudaStream_t>(stream));
 }
 
 int sa_attn_fwd(const void* q, const void* k, const void* v, const int64_t q_strides[3], const int64_t kv_strides[3],
                 const int64_t o_strides[3], int32_t batch, int32_t n_tokens, int32_t heads, int32_t kv_heads,
                 int32_t head_dim, int32_t block, int32_t causal, const int32_t* d_row_ptr, const int32_t* d_col_idx,
-                int32_t csr_shared, float softmax_scale, void* o, float* lse, void* stream) {
+                int32_t csr_shared, float softmax_scale, void* o, float* lse, void* workspace,
+                size_t workspace_bytes, void* stream) {
   if (!d_row_ptr || !d_col_idx) return SA_ERR_INVALID_ARG;
   return sa_attn_fwd_heads(q, k, v, q_strides, kv_strides, o_strides, batch, n_tokens, heads, kv_heads, head_dim,
                            block, causal, 1, &d_row_ptr, &d_col_idx, nullptr, csr_shared, softmax_scale, o, lse,
-                           stream);
+                           workspace, workspace_bytes, stream);
+}
+
+int sa_attn_fwd_workspace_size(int32_t batch, int32_t n_tokens, int32_t heads, int32_t head_dim, int32_t block,
+                               int32_t csr_batches, int32_t n_masks, size_t* h_bytes) {
+  if (batch <= 0 || n_tokens <= 0 || heads <= 0 || block <= 0 || n_tokens % block != 0 || csr_batches <= 0 ||
+      n_masks <= 0 || !h_bytes)
+    return SA_ERR_INVALID_ARG;
+  if (head_dim != 32 && head_dim != 64 && head_dim != 128) return SA_ERR_UNSUPPORTED;
+  *h_bytes = sa::attn_fwd_workspace_bytes(batch, n_tokens, heads, head_dim, csr_batches, n_masks);
+  return SA_OK;
 }
 
 int sa_attn_bwd_workspace_size(int32_t batch, int32_t n_tokens, int32_t heads, int32_t block, int32_t csr_batches,

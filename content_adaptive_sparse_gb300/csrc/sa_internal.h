@@ -47,8 +47,14 @@ struct AttnArgs {
   const int32_t* col_idx[kMaxMasks];
   uint8_t head_mask[kMaxHeadMap];    // query head -> CSR
   float softmax_scale;
+  void* workspace;                   // caller-owned, 256-byte aligned
+  size_t workspace_bytes;
 };
 int launch_attn_fwd(const AttnArgs& a, cudaStream_t stream);
+// Workspace bytes of the forward with room for kFwdDefaultSlots split parts (split-row combine).
+constexpr int kFwdDefaultSlots = 608;
+size_t attn_fwd_workspace_bytes(int64_t batch, int64_t n_tokens, int64_t heads, int head_dim, int64_t csr_batches,
+                                int64_t n_masks);
 unsigned int attn_read_and_clear_error(cudaStream_t stream);
 
 // offset_attn.cu

@@ -14,9 +14,8 @@
  *   - Device pointers are marked d_*, host pointers h_*; q/k/v/o/lse are device memory.
  *   - The caller owns all memory. The library allocates no device memory; its only
  *     device state is static arrays in the module: the device error words (see
- *     sa_device_status), 64 work-counter slots of the block-sparse forward (each launch
- *     takes the next slot and zeroes it on its stream, so at most 64 launches may be in
- *     flight at once across streams) and the 16 MiB scratch of sa_attn_bwd_noalloc.
+ *     sa_device_status) and the 16 MiB scratch of sa_attn_bwd_noalloc. Calls that need
+ *     scratch take a caller workspace (sa_attn_fwd, sa_attn_bwd).
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = legacy default
  *     stream). Argument errors are returned synchronously before anything is launched.
  *   - Tensors q, k, v, o are bf16 with layout [batch, tokens, heads, head_dim]:
@@ -110,6 +109,13 @@ int sa_mask_nnz_bound(const sa_mask_params* params, int64_t* h_nnz);
 int sa_build_mask(const sa_mask_params* params, const float* d_ratio, int32_t* d_row_ptr, int32_t* d_col_idx,
                   int64_t col_capacity, void* stream);
 
+/* Workspace bytes of sa_attn_fwd / sa_attn_fwd_heads for these shapes: the launch's work
+ * counter, the split plan and room for 608 partial results of split items (about 33 KB each
+ * at head_dim 64, 66 KB at 128). csr_batches is 1 for a shared CSR, else batch; n_masks is
+ * the number of CSRs (1 for sa_attn_fwd). Host only. */
+int sa_attn_fwd_workspace_size(int32_t batch, int32_t n_tokens, int32_t heads, int32_t head_dim, int32_t block,
+                               int32_t csr_batches, int32_t n_masks, size_t* h_bytes);
+
 /* Block-sparse attention forward over a block CSR (tcgen05 / TMEM / TMA kernel).
  * Token pair (i, j) is attended iff blk(j) is in row(blk(i)) and, if causal, j <= i
  * ("Parameter-free Adaptive Sparse Attention ...", section 3.4 "Block-to-token
@@ -124,12 +130,20 @@ int sa_build_mask(const sa_mask_params* params, const float* d_ratio, int32_t* d
  *   Column indices must lie in [0, nb); rows must be ascending without duplicates.
  *   An out-of-range index is skipped and reported as SA_ERR_DEVICE by
  *   sa_device_status.
- *   o : bf16 output, lse : fp32 [batch, heads, n_tokens]. */
+ *   o : bf16 output, lse : fp32 [batch, heads, n_tokens].
+ *   workspace : caller-owned device memory, 256-byte aligned, at least 256 bytes; its
+ *   contents on entry do not matter. It holds the launch's work counter, so launches in
+ *   flight at the same time need separate workspaces. With
+ *   sa_attn_fwd_workspace_size bytes, a launch with fewer work items (128-row query tiles
+ *   x heads x sequences) than four per SM splits the items whose key lists are longest
+ *   into parts of equal key-tile counts, writes each part's O and LSE to the workspace and
+ *   merges them (LSE = ln sum exp LSE_p, O = sum exp(LSE_p - LSE) O_p), so that a few long
+ *   rows do not leave SMs idle; a smaller workspace (>= 256 bytes) never splits. */
 int sa_attn_fwd(const void* q, const void* k, const void* v, const int64_t q_strides[3],
                 const int64_t kv_strides[3], const int64_t o_strides[3], int32_t batch, int32_t n_tokens,
                 int32_t heads, int32_t kv_heads, int32_t head_dim, int32_t block, int32_t causal,
                 const int32_t* d_row_ptr, const int32_t* d_col_idx, int32_t csr_shared, float softmax_scale,
-                void* o, float* lse, void* stream);
+                void* o, float* lse, void* workspace, size_t workspace_bytes, void* stream);
 
 /* sa_attn_fwd with one block CSR per head group ("Parameter-free Adaptive Sparse
  * Attention ...", Appendix B "Head-specific mask distribution": local, long-range and
@@ -141,13 +155,13 @@ int sa_attn_fwd(const void* q, const void* k, const void* v, const int64_t q_str
  *   h_head_mask  : host int32 [heads]; query head h uses CSR h_head_mask[h], in
  *                  [0, n_masks). heads <= 256.
  * The host arrays are read before the call returns. Every other argument is as in
- * sa_attn_fwd (csr_shared applies to every CSR). */
+ * sa_attn_fwd (csr_shared applies to every CSR; the workspace size query takes n_masks). */
 int sa_attn_fwd_heads(const void* q, const void* k, const void* v, const int64_t q_strides[3],
                       const int64_t kv_strides[3], const int64_t o_strides[3], int32_t batch, int32_t n_tokens,
                       int32_t heads, int32_t kv_heads, int32_t head_dim, int32_t block, int32_t causal,
                       int32_t n_masks, const int32_t* const* h_row_ptrs, const int32_t* const* h_col_idxs,
                       const int32_t* h_head_mask, int32_t csr_shared, float softmax_scale, void* o, float* lse,
-                      void* stream);
+                      void* workspace, size_t workspace_bytes, void* stream);
 
 /* Workspace bytes of sa_attn_bwd: D = rowsum(dO * O) (fp32 [batch][heads][n_tokens])
  * and the transposed CSR (int32 [csr_batches][nb + 1] plus col_capacity indices, where

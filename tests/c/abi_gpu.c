@@ -68,7 +68,10 @@ int main(int argc, char** argv) {
 
   float *d_ratio = NULL, *d_lse = NULL;
   int32_t *d_row_ptr = NULL, *d_col_idx = NULL;
-  void *d_q = NULL, *d_k = NULL, *d_v = NULL, *d_o = NULL;
+  void *d_q = NULL, *d_k = NULL, *d_v = NULL, *d_o = NULL, *d_ws = NULL;
+  size_t ws_bytes = 0;
+  TRY(sa_attn_fwd_workspace_size(batch, n, heads, d, b, batch, 1, &ws_bytes));
+  TRY(cudaMalloc(&d_ws, ws_bytes));
   TRY(cudaMalloc((void**)&d_ratio, sizeof(float) * batch * nb));
   TRY(cudaMalloc((void**)&d_row_ptr, sizeof(int32_t) * batch * (nb + 1)));
   TRY(cudaMalloc((void**)&d_col_idx, sizeof(int32_t) * (size_t)(cap > 0 ? cap : 1)));
@@ -88,7 +91,7 @@ int main(int argc, char** argv) {
   const int64_t qs[3] = {(int64_t)n * heads * d, (int64_t)heads * d, d};
   const int64_t kvs[3] = {(int64_t)n * kv_heads * d, (int64_t)kv_heads * d, d};
   TRY(sa_attn_fwd(d_q, d_k, d_v, qs, kvs, qs, batch, n, heads, kv_heads, d, b, 1, d_row_ptr, d_col_idx, 0,
-                  1.0f / sqrtf((float)d), d_o, d_lse, stream));
+                  1.0f / sqrtf((float)d), d_o, d_lse, d_ws, ws_bytes, stream));
   TRY(sa_device_status(stream));
 
   int32_t* h_row_ptr = (int32_t*)malloc(sizeof(int32_t) * batch * (nb + 1));
@@ -119,6 +122,7 @@ int main(int argc, char** argv) {
   cudaFree(d_v);
   cudaFree(d_o);
   cudaFree(d_lse);
+  cudaFree(d_ws);
   cudaStreamDestroy(stream);
   printf("c gpu ok\n");
   return 0;

@@ -63,8 +63,14 @@ int main(void) {
   /* a compute call with a misaligned pointer is refused before any launch */
   const int64_t st[3] = {8192 * 12 * 64, 12 * 64, 64};
   CHECK(sa_attn_fwd((const void*)258, (const void*)256, (const void*)256, st, st, st, 1, 8192, 12, 12, 64, 64, 1,
-                    (const int32_t*)256, (const int32_t*)256, 0, 0.125f, (void*)256, (float*)256, NULL) ==
-        SA_ERR_UNSUPPORTED);
+                    (const int32_t*)256, (const int32_t*)256, 0, 0.125f, (void*)256, (float*)256, (void*)256, 4096,
+                    NULL) == SA_ERR_UNSUPPORTED);
+  /* the forward's workspace holds its work counter: at least 256 bytes */
+  CHECK(sa_attn_fwd((const void*)256, (const void*)256, (const void*)256, st, st, st, 1, 8192, 12, 12, 64, 64, 1,
+                    (const int32_t*)256, (const int32_t*)256, 0, 0.125f, (void*)256, (float*)256, (void*)256, 64,
+                    NULL) == SA_ERR_CAPACITY);
+  size_t fws = 0;
+  CHECK(sa_attn_fwd_workspace_size(4, 8192, 12, 64, 64, 4, 1, &fws) == SA_OK && fws > 608 * 128 * 65 * 4);
 
   if (fails == 0) printf("c abi ok\n");
   return fails == 0 ? 0 : 1;

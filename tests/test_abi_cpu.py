@@ -35,7 +35,7 @@ def test_header_symbols_exported(lib):
     assert {"sa_build_mask", "sa_attn_fwd", "sa_attn_fwd_heads", "sa_offset_attn_fwd", "sa_pow2_offsets",
             "sa_offset_attn_fwd_list",
             "sa_attn_bwd", "sa_attn_bwd_workspace_size", "sa_attn_bwd_noalloc", "sa_offset_attn_interp_fwd",
-            "sa_attn_bwd_heads", "sa_selftest_bounded_wait",
+            "sa_attn_bwd_heads", "sa_selftest_bounded_wait", "sa_attn_fwd_workspace_size", "sa_build_mask_from_bytes",
             "sa_layer_alpha", "sa_fib_offsets", "sa_block_ratios",
             "sa_mask_nnz_bound", "sa_device_status", "sa_status_string", "sa_version"} <= set(names)
     for n in names:
@@ -130,21 +130,33 @@ def test_argument_validation_before_any_launch(lib):
     p16 = ctypes.c_void_p(256)
     # head_dim 48 unsupported, heads % kv_heads != 0 invalid, misaligned pointer unsupported
     assert lib.sa_attn_fwd(p16, p16, p16, s, s, s, 1, 8192, 12, 12, 48, 64, 1, p16, p16, 0,
-                           ctypes.c_float(0.125), p16, p16, None) == -2
+                           ctypes.c_float(0.125), p16, p16, p16, 4096, None) == -2
     assert lib.sa_attn_fwd(p16, p16, p16, s, s, s, 1, 8192, 12, 5, 64, 64, 1, p16, p16, 0,
-                           ctypes.c_float(0.125), p16, p16, None) == -1
+                           ctypes.c_float(0.125), p16, p16, p16, 4096, None) == -1
     assert lib.sa_attn_fwd(ctypes.c_void_p(258), p16, p16, s, s, s, 1, 8192, 12, 12, 64, 64, 1, p16, p16, 0,
-                           ctypes.c_float(0.125), p16, p16, None) == -2
+                           ctypes.c_float(0.125), p16, p16, p16, 4096, None) == -2
+    # the workspace: required, 256-byte aligned, at least 256 bytes
+    assert lib.sa_attn_fwd(p16, p16, p16, s, s, s, 1, 8192, 12, 12, 64, 64, 1, p16, p16, 0,
+                           ctypes.c_float(0.125), p16, p16, None, 4096, None) == -1
+    assert lib.sa_attn_fwd(p16, p16, p16, s, s, s, 1, 8192, 12, 12, 64, 64, 1, p16, p16, 0,
+                           ctypes.c_float(0.125), p16, p16, ctypes.c_void_p(272), 4096, None) == -2
+    assert lib.sa_attn_fwd(p16, p16, p16, s, s, s, 1, 8192, 12, 12, 64, 64, 1, p16, p16, 0,
+                           ctypes.c_float(0.125), p16, p16, p16, 128, None) == -3
+    nbytes = ctypes.c_size_t(0)
+    assert lib.sa_attn_fwd_workspace_size(4, 8192, 12, 64, 64, 4, 1, ctypes.byref(nbytes)) == 0
+    # counter + plan (3072 items, 256 query-tile groups) + 608 slots of 128 x 65 floats
+    assert 608 * 128 * 65 * 4 < nbytes.value < 608 * 128 * 65 * 4 + 3072 * 8 + 608 * 24 + 256 * 16
+    assert lib.sa_attn_fwd_workspace_size(4, 8192, 12, 48, 64, 4, 1, ctypes.byref(nbytes)) == -2
     # per-head CSRs: head index out of range invalid, too many CSRs unsupported
     P2 = ctypes.c_void_p * 2
     rps, cis = P2(256, 512), P2(256, 512)
     hm = (ctypes.c_int32 * 12)(*([0] * 11 + [2]))
     assert lib.sa_attn_fwd_heads(p16, p16, p16, s, s, s, 1, 8192, 12, 12, 64, 64, 1, 2, rps, cis, hm, 0,
-                                 ctypes.c_float(0.125), p16, p16, None) == -1
+                                 ctypes.c_float(0.125), p16, p16, p16, 4096, None) == -1
     P9 = ctypes.c_void_p * 9
     rp9 = P9(*([256] * 9))
     assert lib.sa_attn_fwd_heads(p16, p16, p16, s, s, s, 1, 8192, 12, 12, 64, 64, 1, 9, rp9, rp9, hm, 0,
-                                 ctypes.c_float(0.125), p16, p16, None) == -2
+                                 ctypes.c_float(0.125), p16, p16, p16, 4096, None) == -2
     # interpolated gather: alpha must be positive, head_dim 64 only
     assert lib.sa_offset_attn_interp_fwd(p16, p16, p16, s, s, s, 1, 8192, 8, 8, 64, 8, ctypes.c_double(-0.5), 15, 0,
                                          ctypes.c_float(0.125), p16, p16, None) == -1
