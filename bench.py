@@ -785,6 +785,8 @@ def _measure_rows(torch, sa, dev, flush, peaks, max_over_ranks, only=None, steps
         rows.update(_row_bigbird(torch, dev, flush, peaks, max_over_ranks, steps, warm))
     if want("long_topk_64k"):
         rows.update(_row_long(torch, dev, flush, peaks, max_over_ranks, steps, warm))
+    if want("full_32k_one_head_split"):
+        rows.update(_row_split(torch, dev, flush, peaks, max_over_ranks, steps, warm))
     if want("cas_heads_8k"):
         rows.update(_row_block_sparse(torch, dev, flush, peaks, max_over_ranks, steps, warm, "cas_heads_8k"))
     if want("bwd_bytelm_topk_8k"):
@@ -827,6 +829,25 @@ def _row_long(torch, dev, flush, peaks, max_over_ranks, steps, warm):
                              "frac_bf16_peak": lc.flops / (a * 1e-3) / 1e12 / peaks["bf16_tflops"],
                              "tokens_per_s": lc.tokens / (tot * 1e-3), "edges": lc.edges}
     return rows
+
+
+def _row_split(torch, dev, flush, peaks, max_over_ranks, steps, warm):
+    """Few work items with long key lists (full causal 32K, one sequence and head): the
+    forward with its workspace (long items split into parts and merged) and with a 256-byte
+    workspace (no split)."""
+    case = BlockSparseCase("full_32k_one_head", dev)
+    seg, _ = _time_events(torch, [case.attend], steps, warm, flush)
+    a = max_over_ranks(seg[0])
+    full_ws = case.ws
+    case.ws = torch.empty((256,), dtype=torch.uint8, device=dev)
+    seg2, _ = _time_events(torch, [case.attend], steps, warm, flush)
+    case.ws = full_ws
+    b = max_over_ranks(seg2[0])
+    return {"full_32k_one_head_split": {"attn_ms": a, "attn_ms_without_split": b,
+                                        "effective_tflops": case.flops / (a * 1e-3) / 1e12,
+                                        "frac_bf16_peak": case.flops / (a * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                                        "effective_tflops_without_split": case.flops / (b * 1e-3) / 1e12,
+                                        "edges": case.edges, "launches_per_step": 4}}
 
 
 def _row_block_sparse(torch, dev, flush, peaks, max_over_ranks, steps, warm, name):
@@ -893,7 +914,8 @@ def main():
     ap.add_argument("--no-cpu-configs", action="store_true", help="skip the oracle timing of the other workloads")
     ap.add_argument("--cpu-config-seconds", type=float, default=1.5,
                     help="oracle seconds per workload in the per-workload CPU timing")
-    ap.add_argument("--only-row", choices=["bigbird_16k", "long_topk_64k", "cas_heads_8k", "bwd_bytelm_topk_8k",
+    ap.add_argument("--only-row", choices=["bigbird_16k", "long_topk_64k", "full_32k_one_head_split", "cas_heads_8k",
+                                           "bwd_bytelm_topk_8k",
                                            "fib_8k_16_layers",
                                            "fib_8k_coprime_16_layers", "pow2_8k_16_layers", "fib_interp_8k_16_layers",
                                            "fib_8k_2_layers"],

@@ -30,6 +30,8 @@ Workloads (shapes and pattern parameters as the pages and the workload statement
                        (the same page, section 2 "Attended set").
 * ``long_topk_64k``  - 1 x 65536 byte tokens, block 128, 16 heads, d_h 128, top-64
                        (top-k swept over 16/64/256), plus ``full_16k``.
+* ``full_32k_one_head`` - the full causal mask over 32768 tokens for one sequence and one
+                       head of 128: few work items with long key lists.
 
 Stand-in data: the pages measure on PG-19 and FineWeb-Edu style corpora, which are
 not available here. The byte generators below reproduce the properties the mask
@@ -89,6 +91,9 @@ WORKLOADS = {
                           std=1.0 / np.sqrt(128.0), bytes="phrase_random", seed=47),
     "full_16k": dict(kind="full", batch=1, n_tokens=16384, block=128, heads=16, kv_heads=16,
                      head_dim=128, causal=1, std=1.0 / np.sqrt(128.0), seed=47),
+    # few work items with long key lists (one sequence, one head): the forward's split path
+    "full_32k_one_head": dict(kind="full", batch=1, n_tokens=32768, block=128, heads=1, kv_heads=1,
+                              head_dim=128, causal=1, std=1.0 / np.sqrt(128.0), seed=49),
 }
 
 
