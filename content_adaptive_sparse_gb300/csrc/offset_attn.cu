@@ -13,14 +13,16 @@
 //     uses only key r: the diagonal of a 16 x 16 block. Computed with 8 mma.sync for QK
 //     and 8 for PV; the zero off-diagonal P entries cost tensor work, not memory traffic.
 //
-// Work item: one CTA of 4 warps per (sequence, head, 64-query tile); warp w owns queries
-// q0 + 16w .. q0 + 16w + 15 and takes every key of them (band steps and offsets), so no
-// two warps merge softmax states. The band (K/V rows [q0 - 64, q0 + 64)) arrives by TMA
-// once per CTA and is shared by the four warps. Once every warp is past the band, its
-// 32 KB become four per-warp slab rings of two buffers: a warp streams the 16 K and V rows
-// of each larger offset that its own queries use (4 KB) two offsets ahead, and waits on
-// nothing but its own copies (no cross-warp release of a buffer, no CTA barrier between
-// offsets). At 33 KB of shared memory and <= 80 registers six CTAs (24 warps) share an SM.
+// Work item: one CTA of 4 warps per (sequence, head, 128-query tile); warp w owns queries
+// q0 + 32w .. q0 + 32w + 31 as two 16-query m-tiles and takes every key of them (band steps
+// and offsets), so no two warps merge softmax states. The band (K/V rows [q0 - 64, q0 + 128),
+// 48 KB) arrives by TMA once per CTA and is shared by the four warps. Once every warp is past
+// the band, its memory becomes four per-warp slab rings of two buffers: a warp streams the 32
+// K and V rows of each larger offset that its own queries use (8 KB) two offsets ahead, and
+// waits on nothing but its own copies (no cross-warp release of a buffer, no CTA barrier
+// between offsets). One slab, one wait and one refill serve two m-tiles, and the band's
+// over-fetch is 1.5x instead of 2x. At 65 KB of shared memory and <= 168 registers three CTAs
+// (12 warps, 384 queries in flight) share an SM.
 // Softmax: exact max over the band part, then the offsets with a lazily rescaled running
 // max (threshold 2^8).
 #include <cuda.h>
@@ -40,17 +42,22 @@ using namespace frag;
 
 __device__ unsigned int g_offset_err;
 
-constexpr int kQ = 64;                   // queries per CTA
-constexpr int kWarps = 4;                // 16 queries per warp
-constexpr int kCtasPerSm = 6;            // 33 KB of shared memory and <= 80 registers per thread
+constexpr int kMT = 2;                   // 16-query m-tiles per warp
+constexpr int kWarps = 4;
+constexpr int kQ = 16 * kMT * kWarps;    // queries per CTA (128)
+constexpr int kCtasPerSm = kMT == 1 ? 6 : 3;   // shared memory per CTA (33 / 65 KB), <= 170 registers
 constexpr int kRing = 2;                 // slab buffers per warp
 constexpr int kD = 64;                   // head dim supported by this kernel
 constexpr int kRowBytes = kD * 2;        // 128 B per K/V row
 constexpr int kBandMax = 64;             // deltas up to this go through the band
-constexpr int kBandRows = kQ + kBandMax; // band slab rows [q0 - 64, q0 + 64)
-constexpr int kWarpSlabBytes = 2 * 16 * kRowBytes;   // K and V rows of one warp's 16 queries
-static_assert(kWarps * kRing * kWarpSlabBytes == 2 * kBandRows * kRowBytes, "warp rings fill the band's memory");
+constexpr int kBandRows = kQ + kBandMax; // band slab rows [q0 - 64, q0 + kQ)
+constexpr int kSlabRows = 16 * kMT;      // K (then V) rows of one warp's slab
+constexpr int kWarpSlabBytes = 2 * kSlabRows * kRowBytes;   // K and V rows of one warp's queries
 constexpr int kBandBytes = kBandRows * kRowBytes;
+constexpr int kRingBytes = kWarps * kRing * kWarpSlabBytes;
+constexpr int kSmemBytes = (2 * kBandBytes > kRingBytes ? 2 * kBandBytes : kRingBytes);
+static_assert(kBandRows <= 256 && kSlabRows <= 256, "TMA box rows");
+static_assert(kCtasPerSm * (1024 + kSmemBytes) <= 227 * 1024, "shared memory per SM");
 constexpr int kMaxLarge = kMaxOffsets;
 
 struct OffParams {
@@ -75,10 +82,10 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
                        const __grid_constant__ OffParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sKb = sm;                        // band K, 16 KB
-  uint8_t* sVb = sKb + kBandBytes;          // band V, 16 KB
-  // once every warp is past the band, warp w's slab ring occupies [w * 8 KB, w * 8 KB + 8 KB)
-  // of the band's memory: buffer b at + b * 4 KB, K rows at + 0, V rows at + 2 KB
+  uint8_t* sKb = sm;                        // band K
+  uint8_t* sVb = sKb + kBandBytes;          // band V
+  // once every warp is past the band, warp w's slab ring occupies its own kRing slabs of the
+  // same memory: buffer b at + b * kWarpSlabBytes, K rows first, then V rows
   __shared__ uint64_t bar_band, bar_slab[kWarps][kRing];
   __shared__ int abort_flag;
 
@@ -90,9 +97,9 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
   const int q0 = tile * kQ;
   const int hk = h / p.heads_per_kv;
   // larger offsets that reach at least one query of this warp
-  const int qw = q0 + 16 * wq;               // first query of this warp
+  const int qw = q0 + kSlabRows * wq;        // first query of this warp (m-tile m: qw + 16 m)
   int n_off = 0;
-  while (n_off < p.n_large && p.large[n_off] <= qw + 15) ++n_off;
+  while (n_off < p.n_large && p.large[n_off] <= qw + kSlabRows - 1) ++n_off;
 
   if (tid == 0) {
     mbar_init(&bar_band, 1);
@@ -114,11 +121,13 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
   const float c = p.scale_log2;
   const float kNegInf = __int_as_float(0xff800000);
 
-  // Q operand straight from global memory (rows past the end read the last row; never stored)
-  uint32_t qa[4][4];
-  {
+  // Q operands straight from global memory (rows past the end read the last row; never stored)
+  uint32_t qa[kMT][4][4];
+#pragma unroll
+  for (int m = 0; m < kMT; ++m) {
+    const int qm = qw + 16 * m;
     const int last = p.n_tokens - 1;
-    const int i_lo = qw + g < last ? qw + g : last, i_hi = qw + g + 8 < last ? qw + g + 8 : last;
+    const int i_lo = qm + g < last ? qm + g : last, i_hi = qm + g + 8 < last ? qm + g + 8 : last;
     const __nv_bfloat16* base = p.q + (int64_t)s * p.q_sb + (int64_t)h * p.q_sh + 16 * t;
     const uint4* lo = reinterpret_cast<const uint4*>(base + (int64_t)i_lo * p.q_sn);
     const uint4* hi = reinterpret_cast<const uint4*>(base + (int64_t)i_hi * p.q_sn);
@@ -127,82 +136,92 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
     const uint32_t wh[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {
-      qa[ks][0] = wl[2 * ks];
-      qa[ks][1] = wh[2 * ks];
-      qa[ks][2] = wl[2 * ks + 1];
-      qa[ks][3] = wh[2 * ks + 1];
+      qa[m][ks][0] = wl[2 * ks];
+      qa[m][ks][1] = wh[2 * ks];
+      qa[m][ks][2] = wl[2 * ks + 1];
+      qa[m][ks][3] = wh[2 * ks + 1];
     }
   }
 
   // warp-uniform wait results: the fragment code below uses full-warp shuffles
   bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_band, 0, &abort_flag, &g_offset_err, kErrTimeout));
 
-  float o[8][4];                             // O fragments: d n-tiles 0..7
+  float o[kMT][8][4];                        // O fragments per m-tile: d n-tiles 0..7
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-  // running max of rows g, g+8 (log2 units)
-  float m_lo = kNegInf, m_hi = kNegInf;
-  float l_lo = 0.f, l_hi = 0.f;
-
-  if (ok) {
-    // ---------------- band: keys [qw - Dr, qw + 16), band slab row = key - (q0 - 64)
-    uint64_t keep = p.keep[lane];
-    const int lim = p.dr - qw;               // band columns below lim are keys < 0 (first tile only)
-    if (lim > 0) {
+  for (int m = 0; m < kMT; ++m)
 #pragma unroll
-      for (int nt = 0; nt < 2 * NKT; ++nt)
+    for (int nt = 0; nt < 8; ++nt) o[m][nt][0] = o[m][nt][1] = o[m][nt][2] = o[m][nt][3] = 0.f;
+  // running max of rows g, g+8 of each m-tile (log2 units) and the row sums
+  float m_lo[kMT], m_hi[kMT], l_lo[kMT], l_hi[kMT];
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (8 * nt + 2 * t + (e & 1) < lim) keep &= ~(1ull << (4 * nt + e));
-    }
-    const int row0 = 16 * wq + kBandMax - p.dr;
-    const uint32_t kb_tile = smem_u32(sKb), vb_tile = smem_u32(sVb);
-    float sb[2 * NKT][4];
-    float mx_lo = kNegInf, mx_hi = kNegInf;
-#pragma unroll
-    for (int nt = 0; nt < 2 * NKT; ++nt) {
-      uint32_t u[8];
-      load_kfrag(kb_tile, row0 + 8 * nt + g, t, u);
-      sb[nt][0] = sb[nt][1] = sb[nt][2] = sb[nt][3] = 0.f;
-      qk_ntile(sb[nt], qa, u);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float v = (keep >> (4 * nt + e)) & 1ull ? sb[nt][e] : kNegInf;
-        sb[nt][e] = v;
-        if (e < 2) mx_lo = fmaxf(mx_lo, v);
-        else mx_hi = fmaxf(mx_hi, v);
-      }
-    }
-    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
-    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
-    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
-    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
-    m_lo = mx_lo * c;                        // finite: distance 0 is always kept
-    m_hi = mx_hi * c;
-    // P = exp2(s c - m); row sums of the bf16 P the PV product uses come from one more
-    // MMA against a ones matrix
-    float lsum[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int j = 0; j < NKT; ++j) {
-      uint32_t pa[4];
-      pa[0] = pack_bf16x2(ex2_approx(fmaf(sb[2 * j][0], c, -m_lo)), ex2_approx(fmaf(sb[2 * j][1], c, -m_lo)));
-      pa[1] = pack_bf16x2(ex2_approx(fmaf(sb[2 * j][2], c, -m_hi)), ex2_approx(fmaf(sb[2 * j][3], c, -m_hi)));
-      pa[2] = pack_bf16x2(ex2_approx(fmaf(sb[2 * j + 1][0], c, -m_lo)),
-                          ex2_approx(fmaf(sb[2 * j + 1][1], c, -m_lo)));
-      pa[3] = pack_bf16x2(ex2_approx(fmaf(sb[2 * j + 1][2], c, -m_hi)),
-                          ex2_approx(fmaf(sb[2 * j + 1][3], c, -m_hi)));
-      mma16816(lsum, pa, kOnesBf16x2, kOnesBf16x2);
-      uint32_t vb[4][4];
-      load_v16(vb_tile, row0 + 16 * j, lane, vb);
-      pv_16(o, pa, vb);
-    }
-    l_lo = lsum[0];
-    l_hi = lsum[2];
+  for (int m = 0; m < kMT; ++m) {
+    m_lo[m] = m_hi[m] = kNegInf;
+    l_lo[m] = l_hi[m] = 0.f;
   }
 
-  // The band is read: its memory becomes the warps' slab rings. Each warp streams the 16
-  // key rows of each larger offset that its own queries use, two slabs ahead, and waits
-  // on nothing but its own copies.
+  if (ok) {
+    const uint32_t kb_tile = smem_u32(sKb), vb_tile = smem_u32(sVb);
+#pragma unroll
+    for (int m = 0; m < kMT; ++m) {
+      // ---------------- band: keys [qm - Dr, qm + 16), band slab row = key - (q0 - 64)
+      const int qm = qw + 16 * m;
+      uint64_t keep = p.keep[lane];
+      const int lim = p.dr - qm;             // band columns below lim are keys < 0 (first tile only)
+      if (lim > 0) {
+#pragma unroll
+        for (int nt = 0; nt < 2 * NKT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (8 * nt + 2 * t + (e & 1) < lim) keep &= ~(1ull << (4 * nt + e));
+      }
+      const int row0 = qm - q0 + kBandMax - p.dr;
+      float sb[2 * NKT][4];
+      float mx_lo = kNegInf, mx_hi = kNegInf;
+#pragma unroll
+      for (int nt = 0; nt < 2 * NKT; ++nt) {
+        uint32_t u[8];
+        load_kfrag(kb_tile, row0 + 8 * nt + g, t, u);
+        sb[nt][0] = sb[nt][1] = sb[nt][2] = sb[nt][3] = 0.f;
+        qk_ntile(sb[nt], qa[m], u);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float v = (keep >> (4 * nt + e)) & 1ull ? sb[nt][e] : kNegInf;
+          sb[nt][e] = v;
+          if (e < 2) mx_lo = fmaxf(mx_lo, v);
+          else mx_hi = fmaxf(mx_hi, v);
+        }
+      }
+      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+      m_lo[m] = mx_lo * c;                   // finite: distance 0 is always kept
+      m_hi[m] = mx_hi * c;
+      // P = exp2(s c - m); row sums of the bf16 P the PV product uses come from one more
+      // MMA against a ones matrix
+      float lsum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < NKT; ++j) {
+        uint32_t pa[4];
+        pa[0] = pack_bf16x2(ex2_approx(fmaf(sb[2 * j][0], c, -m_lo[m])), ex2_approx(fmaf(sb[2 * j][1], c, -m_lo[m])));
+        pa[1] = pack_bf16x2(ex2_approx(fmaf(sb[2 * j][2], c, -m_hi[m])), ex2_approx(fmaf(sb[2 * j][3], c, -m_hi[m])));
+        pa[2] = pack_bf16x2(ex2_approx(fmaf(sb[2 * j + 1][0], c, -m_lo[m])),
+                            ex2_approx(fmaf(sb[2 * j + 1][1], c, -m_lo[m])));
+        pa[3] = pack_bf16x2(ex2_approx(fmaf(sb[2 * j + 1][2], c, -m_hi[m])),
+                            ex2_approx(fmaf(sb[2 * j + 1][3], c, -m_hi[m])));
+        mma16816(lsum, pa, kOnesBf16x2, kOnesBf16x2);
+        uint32_t vb[4][4];
+        load_v16(vb_tile, row0 + 16 * j, lane, vb);
+        pv_16(o[m], pa, vb);
+      }
+      l_lo[m] = lsum[0];
+      l_hi[m] = lsum[2];
+    }
+  }
+
+  // The band is read: its memory becomes the warps' slab rings. Each warp streams the
+  // kSlabRows key and value rows of each larger offset that its own queries use, two slabs
+  // ahead, and waits on nothing but its own copies.
   __syncthreads();
   uint8_t* ring = sm + wq * (kRing * kWarpSlabBytes);
   int issued = 0;
@@ -216,7 +235,7 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
   }
   ok = ok && !abort_flag;
 
-  // ---------------- larger offsets: one diagonal 16 x 16 block per slab
+  // ---------------- larger offsets: per m-tile, one diagonal 16 x 16 block of the slab
   const int hl = (lane & ~3) | (g >> 1);     // lane of this quad that holds the diagonal
   const bool holder = (t == (g >> 1));
   const int e_sel = g & 1;                   // which of the two fragment columns is diagonal
@@ -226,31 +245,35 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
                                            &g_offset_err, kErrTimeout));
     if (!ok) break;
     const uint32_t kt = smem_u32(ring + b * kWarpSlabBytes);
-    float s_lo, s_hi;
-    diag_scores(kt, 0, g, t, hl, e_sel, qa, s_lo, s_hi);
     const int delta = p.large[k];
-    if (qw + g - delta < 0) s_lo = kNegInf;
-    if (qw + g + 8 - delta < 0) s_hi = kNegInf;
-    // lazy running max (log2 units): rescale only when a score passes the max by 2^8
-    const float x_lo = s_lo * c, x_hi = s_hi * c;
-    float a_lo = 1.f, a_hi = 1.f;
-    if (x_lo > m_lo + 8.f) { a_lo = ex2_approx(m_lo - x_lo); m_lo = x_lo; }
-    if (x_hi > m_hi + 8.f) { a_hi = ex2_approx(m_hi - x_hi); m_hi = x_hi; }
-    if (__any_sync(0xffffffffu, a_lo != 1.f || a_hi != 1.f)) {
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        o[nt][0] *= a_lo;
-        o[nt][1] *= a_lo;
-        o[nt][2] *= a_hi;
-        o[nt][3] *= a_hi;
+    for (int m = 0; m < kMT; ++m) {
+      const int qm = qw + 16 * m;
+      float s_lo, s_hi;
+      diag_scores(kt, 16 * m, g, t, hl, e_sel, qa[m], s_lo, s_hi);
+      if (qm + g - delta < 0) s_lo = kNegInf;
+      if (qm + g + 8 - delta < 0) s_hi = kNegInf;
+      // lazy running max (log2 units): rescale only when a score passes the max by 2^8
+      const float x_lo = s_lo * c, x_hi = s_hi * c;
+      float a_lo = 1.f, a_hi = 1.f;
+      if (x_lo > m_lo[m] + 8.f) { a_lo = ex2_approx(m_lo[m] - x_lo); m_lo[m] = x_lo; }
+      if (x_hi > m_hi[m] + 8.f) { a_hi = ex2_approx(m_hi[m] - x_hi); m_hi[m] = x_hi; }
+      if (__any_sync(0xffffffffu, a_lo != 1.f || a_hi != 1.f)) {
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+          o[m][nt][0] *= a_lo;
+          o[m][nt][1] *= a_lo;
+          o[m][nt][2] *= a_hi;
+          o[m][nt][3] *= a_hi;
+        }
+        l_lo[m] *= a_lo;
+        l_hi[m] *= a_hi;
       }
-      l_lo *= a_lo;
-      l_hi *= a_hi;
+      const uint32_t pb = pack_bf16x2(ex2_approx(fmaf(s_lo, c, -m_lo[m])), ex2_approx(fmaf(s_hi, c, -m_hi[m])));
+      l_lo[m] += __uint_as_float(pb << 16);
+      l_hi[m] += __uint_as_float(pb & 0xffff0000u);
+      diag_pv(kt + kWarpSlabBytes / 2, 16 * m, lane, holder, e_sel, pb, o[m]);
     }
-    const uint32_t pb = pack_bf16x2(ex2_approx(fmaf(s_lo, c, -m_lo)), ex2_approx(fmaf(s_hi, c, -m_hi)));
-    l_lo += __uint_as_float(pb << 16);
-    l_hi += __uint_as_float(pb & 0xffff0000u);
-    diag_pv(kt + kWarpSlabBytes / 2, 0, lane, holder, e_sel, pb, o);
     // every lane has read the buffer: refill it with the slab kRing ahead
     __syncwarp();
     if (lane == 0 && issued < n_off && !abort_flag) {
@@ -264,22 +287,25 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
 
   if (ok && !abort_flag) {
     // ---------------- epilogue: O / l (bf16) and LSE
-    const float inv_lo = 1.f / l_lo, inv_hi = 1.f / l_hi;   // l > 0: every query keeps itself
-    const int i_lo = qw + g, i_hi = qw + g + 8;
-    __nv_bfloat16* orow_lo = p.o + (int64_t)s * p.o_sb + (int64_t)i_lo * p.o_sn + (int64_t)h * p.o_sh;
-    __nv_bfloat16* orow_hi = p.o + (int64_t)s * p.o_sb + (int64_t)i_hi * p.o_sn + (int64_t)h * p.o_sh;
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      const int col = 8 * nt + 2 * t;
-      if (i_lo < p.n_tokens)
-        *reinterpret_cast<uint32_t*>(orow_lo + col) = pack_bf16x2(o[nt][0] * inv_lo, o[nt][1] * inv_lo);
-      if (i_hi < p.n_tokens)
-        *reinterpret_cast<uint32_t*>(orow_hi + col) = pack_bf16x2(o[nt][2] * inv_hi, o[nt][3] * inv_hi);
-    }
-    if (t == 0) {
-      float* lrow = p.lse + ((int64_t)s * p.heads + h) * p.n_tokens;
-      if (i_lo < p.n_tokens) lrow[i_lo] = (m_lo + __log2f(l_lo)) * 0.69314718055994531f;
-      if (i_hi < p.n_tokens) lrow[i_hi] = (m_hi + __log2f(l_hi)) * 0.69314718055994531f;
+    for (int m = 0; m < kMT; ++m) {
+      const float inv_lo = 1.f / l_lo[m], inv_hi = 1.f / l_hi[m];   // l > 0: every query keeps itself
+      const int i_lo = qw + 16 * m + g, i_hi = qw + 16 * m + g + 8;
+      __nv_bfloat16* orow_lo = p.o + (int64_t)s * p.o_sb + (int64_t)i_lo * p.o_sn + (int64_t)h * p.o_sh;
+      __nv_bfloat16* orow_hi = p.o + (int64_t)s * p.o_sb + (int64_t)i_hi * p.o_sn + (int64_t)h * p.o_sh;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        const int col = 8 * nt + 2 * t;
+        if (i_lo < p.n_tokens)
+          *reinterpret_cast<uint32_t*>(orow_lo + col) = pack_bf16x2(o[m][nt][0] * inv_lo, o[m][nt][1] * inv_lo);
+        if (i_hi < p.n_tokens)
+          *reinterpret_cast<uint32_t*>(orow_hi + col) = pack_bf16x2(o[m][nt][2] * inv_hi, o[m][nt][3] * inv_hi);
+      }
+      if (t == 0) {
+        float* lrow = p.lse + ((int64_t)s * p.heads + h) * p.n_tokens;
+        if (i_lo < p.n_tokens) lrow[i_lo] = (m_lo[m] + __log2f(l_lo[m])) * 0.69314718055994531f;
+        if (i_hi < p.n_tokens) lrow[i_hi] = (m_hi[m] + __log2f(l_hi[m])) * 0.69314718055994531f;
+      }
     }
   }
   // A CTA leaves only with none of its copies in flight: after an abort each warp drains
@@ -296,7 +322,7 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
 template <int NKT>
 int launch_nkt(const CUtensorMap& kb, const CUtensorMap& vb, const CUtensorMap& ks, const CUtensorMap& vs,
                const OffParams& p, int batch, cudaStream_t stream) {
-  const size_t smem = 1024 + 2 * (size_t)kBandBytes;
+  const size_t smem = 1024 + (size_t)kSmemBytes;
   if (cudaFuncSetAttribute(offset_attn_kernel<NKT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return SA_ERR_CUDA;
@@ -315,9 +341,9 @@ int launch_offset_attn_fwd(const OffsetArgs& a, cudaStream_t stream) {
       !encode_bhnd_map(&vb, a.v, a.batch, a.n_tokens, a.kv_heads, kD, a.kv_strides[0], a.kv_strides[1],
                        a.kv_strides[2], kD, kBandRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_bhnd_map(&ks, a.k, a.batch, a.n_tokens, a.kv_heads, kD, a.kv_strides[0], a.kv_strides[1],
-                       a.kv_strides[2], kD, 16, CU_TENSOR_MAP_SWIZZLE_128B) ||
+                       a.kv_strides[2], kD, kSlabRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_bhnd_map(&vs, a.v, a.batch, a.n_tokens, a.kv_heads, kD, a.kv_strides[0], a.kv_strides[1],
-                       a.kv_strides[2], kD, 16, CU_TENSOR_MAP_SWIZZLE_128B))
+                       a.kv_strides[2], kD, kSlabRows, CU_TENSOR_MAP_SWIZZLE_128B))
     return SA_ERR_UNSUPPORTED;
   OffParams p;
   p.n_tokens = a.n_tokens;

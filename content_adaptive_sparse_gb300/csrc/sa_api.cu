@@ -396,8 +396,8 @@ int sa_offset_attn_fwd_list(const void* q, const void* k, const void* v, const i
     if (h_offsets[i] <= window || h_offsets[i] >= n_tokens) return SA_ERR_INVALID_ARG;
     if (i > 0 && h_offsets[i] <= h_offsets[i - 1]) return SA_ERR_INVALID_ARG;
   }
-  // grid: (batch x heads, 64-query tiles)
-  if ((int64_t)batch * heads > 0x7fffffff || (n_tokens + 63) / 64 > 65535) return SA_ERR_UNSUPPORTED;
+  // grid: (batch x heads, 128-query tiles)
+  if ((int64_t)batch * heads > 0x7fffffff || (n_tokens + 127) / 128 > 65535) return SA_ERR_UNSUPPORTED;
   if (!device_ok()) return SA_ERR_CUDA;
   sa::OffsetArgs a;
   a.q = q;
