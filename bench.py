@@ -833,21 +833,29 @@ def _row_long(torch, dev, flush, peaks, max_over_ranks, steps, warm):
 
 def _row_split(torch, dev, flush, peaks, max_over_ranks, steps, warm):
     """Few work items with long key lists (full causal 32K, one sequence and head): the
-    forward with its workspace (long items split into parts and merged) and with a 256-byte
-    workspace (no split)."""
-    case = BlockSparseCase("full_32k_one_head", dev)
-    seg, _ = _time_events(torch, [case.attend], steps, warm, flush)
-    a = max_over_ranks(seg[0])
-    full_ws = case.ws
-    case.ws = torch.empty((256,), dtype=torch.uint8, device=dev)
-    seg2, _ = _time_events(torch, [case.attend], steps, warm, flush)
-    case.ws = full_ws
-    b = max_over_ranks(seg2[0])
-    return {"full_32k_one_head_split": {"attn_ms": a, "attn_ms_without_split": b,
-                                        "effective_tflops": case.flops / (a * 1e-3) / 1e12,
-                                        "frac_bf16_peak": case.flops / (a * 1e-3) / 1e12 / peaks["bf16_tflops"],
-                                        "effective_tflops_without_split": case.flops / (b * 1e-3) / 1e12,
-                                        "edges": case.edges, "launches_per_step": 4}}
+    forward with its workspace (the schedule kernel splits long items into parts and merges
+    them when the longest item exceeds 1.25x a stream's share) and with a 256-byte workspace
+    (no split), at d = 64 (two-pipeline kernel: the items are split) and d = 128 (one-stream
+    kernel: the items stay whole)."""
+    out = {}
+    for d in (64, 128):
+        case = BlockSparseCase("full_32k_one_head", dev, head_dim=d, std=1.0 / (d ** 0.5))
+        seg, _ = _time_events(torch, [case.attend], steps, warm, flush)
+        a = max_over_ranks(seg[0])
+        full_ws = case.ws
+        case.ws = torch.empty((256,), dtype=torch.uint8, device=dev)
+        seg2, _ = _time_events(torch, [case.attend], steps, warm, flush)
+        case.ws = full_ws
+        b = max_over_ranks(seg2[0])
+        hdr = full_ws[64:80].cpu().numpy().view("int32")
+        out[f"d{d}"] = {"attn_ms": a, "attn_ms_without_split": b,
+                        "effective_tflops": case.flops / (a * 1e-3) / 1e12,
+                        "frac_bf16_peak": case.flops / (a * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                        "effective_tflops_without_split": case.flops / (b * 1e-3) / 1e12,
+                        "split_items": int(hdr[3]), "part_tiles": int(hdr[2]), "edges": case.edges}
+        del case
+        torch.cuda.empty_cache()
+    return {"full_32k_one_head_split": out}
 
 
 def _row_block_sparse(torch, dev, flush, peaks, max_over_ranks, steps, warm, name):

@@ -28,6 +28,8 @@
 //               tile's probabilities are ready. The commit that frees a K stage also tells the
 //               softmax that S is ready, and the one that frees a V stage tells it that P has
 //               been read and O written.
+#include <string.h>
+
 #include <atomic>
 
 #include "attn_fwd_common.cuh"
@@ -37,6 +39,7 @@ namespace sa {
 namespace {
 
 constexpr int kSoftmaxWarps = 4;      // per pipeline: one per TMEM lane quarter
+constexpr int kTmaStoreTiles = 4;     // d = 64: items of at least this many key tiles store O by TMA
 constexpr int kMetaConsumers = 2 + kSoftmaxWarps;   // MMA thread, loader, softmax warps
 __host__ __device__ constexpr uint32_t col_s(int x) { return 256u * x; }
 __host__ __device__ constexpr uint32_t col_p(int x) { return 256u * x + 128u; }
@@ -174,10 +177,13 @@ __device__ __forceinline__ void rescale_o(uint32_t tO, float alpha) {
 }
 
 // Softmax and epilogue of pipeline x; this warp handles query rows 32q .. 32q+31 of every
-// item (q = its TMEM lane quarter) and all 128 keys of every key tile.
+// item (q = its TMEM lane quarter) and all 128 keys of every key tile. At d = 64 (with an
+// output tensor map, to) an item's O / l rows are staged, 128B-swizzled, in the item's own Q
+// buffer (its QKs are complete) and written by one TMA store per warp; the Q buffer is
+// released to the loader (q_empty) once that store has read it.
 template <int D>
 __device__ void softmax_epilogue(const Params& p, int x, PipeBars& bars, const Batch* ring, uint32_t tmem,
-                                 volatile int* abort_flag) {
+                                 uint8_t* sQ, const CUtensorMap* to, volatile int* abort_flag) {
   using C = Cfg<D>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;
@@ -191,6 +197,7 @@ __device__ void softmax_epilogue(const Params& p, int x, PipeBars& bars, const B
   const uint32_t tO = tmem + col_o(x) + lane_base;
 
   int g = 0;                // key tiles processed by this pipeline
+  int item_local = -1;      // items of this pipeline (Q buffer item_local % QB)
   bool ok = true;
   Item it;
   it.s = it.h = it.tile = 0;
@@ -210,12 +217,22 @@ __device__ void softmax_epilogue(const Params& p, int x, PipeBars& bars, const B
       break;
     }
     if (hdr.w & kFirst) {
+      ++item_local;
       it = decode_item(p, hdr.z);
       qtok = it.tile * kTile + row;
       m_use = kNegInf;
       l = 0.f;
       n_item = 0;
       slot = e.slot;
+      // Items of at least kTmaStoreTiles key tiles (d = 64, whole items) stage their output in
+      // their Q buffer; the others give the buffer up now (its release then waits only for the
+      // item's QKs), so the loader can fetch the Q two items ahead early when items are short.
+      // An item's first batch holds min(16, its key tiles) tiles, so this test and the one at
+      // the item's end, on its tile count, agree.
+      if (!(D == 64 && p.o_tma && slot < 0 && hdr.y >= kTmaStoreTiles)) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.q_empty[item_local % C::QB]);
+      }
     }
     // this quarter's visibility bytes and the chunk counts of the batch's tiles
     const uint4 vqw = ld_shared_u4(&e.vq[quarter][0]);
@@ -316,6 +333,7 @@ __device__ void softmax_epilogue(const Params& p, int x, PipeBars& bars, const B
       tc_fence_after();
     }
     const float inv = l > 0.f ? 1.f / l : 0.f;
+    const float lse = l > 0.f ? (m_use + __log2f(l)) * 0.69314718055994531f : kNegInf;
     if (slot >= 0) {
       // a part of a split item: O / l of its key range (fp32) and its LSE, merged later
       float* po = p.partial + (size_t)slot * (kTile * (D + 1)) + (size_t)row * D;
@@ -335,39 +353,76 @@ __device__ void softmax_epilogue(const Params& p, int x, PipeBars& bars, const B
           dst[j] = make_float4(__uint_as_float(ov[4 * j]) * inv, __uint_as_float(ov[4 * j + 1]) * inv,
                                __uint_as_float(ov[4 * j + 2]) * inv, __uint_as_float(ov[4 * j + 3]) * inv);
       }
-      p.partial[(size_t)slot * (kTile * (D + 1)) + (size_t)kTile * D + row] =
-          l > 0.f ? (m_use + __log2f(l)) * 0.69314718055994531f : kNegInf;
-      continue;
-    }
-    const bool store = qtok < p.n_tokens;
-    __nv_bfloat16* orow = p.o + (int64_t)it.s * p.o_sb + (int64_t)qtok * p.o_sn + (int64_t)it.h * p.o_sh;
+      p.partial[(size_t)slot * (kTile * (D + 1)) + (size_t)kTile * D + row] = lse;
+    } else if (D == 64 && p.o_tma && n_item >= kTmaStoreTiles) {
+      // Staged in the item's Q buffer (its QKs are complete: the last PV has been waited for):
+      // rows of this warp, 128 bytes each, 128B-swizzled (16-byte chunk c of row r at
+      // r * 128 + (c ^ (r & 7)) * 16) as the output map's box expects; rows past the sequence
+      // end are dropped by the TMA store
+      const int qb = item_local % C::QB;
+      uint8_t* stg = sQ + qb * C::Q_BYTES + quarter * 32 * 128;
+      const uint32_t srow = smem_u32(stg) + (uint32_t)lane * 128u;
 #pragma unroll
-    for (int ch = 0; ch < D / 32; ++ch) {
-      uint32_t ov[32];
-      if (n_item > 0) {
-        tmem_ld_x32(tO + 32 * ch, ov);
-        tmem_ld_wait<32>(ov);
-      } else {
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t ov[32];
+        if (n_item > 0) {
+          tmem_ld_x32(tO + 32 * ch, ov);
+          tmem_ld_wait<32>(ov);
+        } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) ov[j] = 0u;
-      }
-      if (store) {
+          for (int j = 0; j < 32; ++j) ov[j] = 0u;
+        }
         uint32_t pk[16];
 #pragma unroll
         for (int j = 0; j < 32; j += 2)
           pk[j >> 1] = pack_bf16x2(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv);
-        uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        for (int j = 0; j < 4; ++j)
+          st_shared_v4(srow + (uint32_t)(((4 * ch + j) ^ (lane & 7)) << 4), pk[4 * j], pk[4 * j + 1], pk[4 * j + 2],
+                       pk[4 * j + 3]);
       }
-    }
-    if (store) {
-      const float lse = l > 0.f ? (m_use + __log2f(l)) * 0.69314718055994531f : kNegInf;
-      p.lse[((int64_t)it.s * p.heads + it.h) * p.n_tokens + qtok] = lse;
+      fence_proxy_async_smem();                      // the staged rows are visible to the TMA store
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_4d(to, stg, 0, it.h, it.tile * kTile + quarter * 32, it.s);
+        bulk_commit_group();
+      }
+      if (qtok < p.n_tokens) p.lse[((int64_t)it.s * p.heads + it.h) * p.n_tokens + qtok] = lse;
+      // the buffer goes back to the loader once the store has read it
+      if (lane == 0) bulk_wait_group_read<0>();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.q_empty[qb]);
+    } else {
+      const bool store = qtok < p.n_tokens;
+      __nv_bfloat16* orow = p.o + (int64_t)it.s * p.o_sb + (int64_t)qtok * p.o_sn + (int64_t)it.h * p.o_sh;
+#pragma unroll
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t ov[32];
+        if (n_item > 0) {
+          tmem_ld_x32(tO + 32 * ch, ov);
+          tmem_ld_wait<32>(ov);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) ov[j] = 0u;
+        }
+        if (store) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 32; j += 2)
+            pk[j >> 1] = pack_bf16x2(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv);
+          uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        }
+      }
+      if (store) p.lse[((int64_t)it.s * p.heads + it.h) * p.n_tokens + qtok] = lse;
     }
     // The next item's first P store follows these O loads in program order, and the MMA
     // thread issues that item's first PV only after the P store: O is not overwritten early.
   }
+  // every TMA store of this warp has completed before the CTA may exit
+  if (lane == 0) bulk_wait_group<0>();
+  __syncwarp();
 }
 
 // ------------------------------------------------------------------ kernel
@@ -375,7 +430,8 @@ __device__ void softmax_epilogue(const Params& p, int x, PipeBars& bars, const B
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ Params p) {
+                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
+                    const __grid_constant__ Params p) {
   using C = Cfg<D>;
   static_assert(!C::WIDE && 192 + D <= 256, "two-pipeline kernel: head dimension 32 or 64");
   extern __shared__ uint8_t smem_raw[];
@@ -391,7 +447,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       PipeBars& b = bars[x];
       for (int i = 0; i < 2; ++i) {
         mbar_init(&b.q_full[i], 1);
-        mbar_init(&b.q_empty[i], 1);
+        // released by the MMA thread (the item's QKs are done) and the softmax warps (at the
+        // item's start, or once the item's output store has read the buffer)
+        mbar_init(&b.q_empty[i], 1 + kSoftmaxWarps);
       }
       for (int i = 0; i < kMaxStages; ++i) {
         mbar_init(&b.k_full[i], 1);
@@ -438,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 8) {
     // warpgroups 0 and 1: one setmaxnreg instruction for both
     asm volatile("setmaxnreg.inc.sync.aligned.u32 184;" ::: "memory");
-    softmax_epilogue<D>(p, x, bars[x], ring[x], tmem, &abort_flag);
+    softmax_epilogue<D>(p, x, bars[x], ring[x], tmem, sQ, &to, &abort_flag);
   } else {
     // warpgroups 2 and 3: one setmaxnreg instruction for both, then the roles
     asm volatile("setmaxnreg.dec.sync.aligned.u32 72;" ::: "memory");
@@ -574,6 +632,11 @@ __global__ void __launch_bounds__(1024) fwd_schedule_kernel(const __grid_constan
     // about two parts of work per item stream (n_pipes: streams of the launch); parts of at
     // least kMinPartTiles key tiles
     int T = max(kMinPartTiles, (total + 2 * n_pipes - 1) / (2 * n_pipes));
+    // No split when the longest item is within 1.25x of a stream's even share: the
+    // longest-first order then balances the streams about as well, without the partial
+    // results and the merge.
+    const int share = (total + n_pipes - 1) / n_pipes;
+    if (4 * b <= 5 * share) T = max(T, b);
     s_T = T;
     warp_sums[0] = b;
   }
@@ -713,7 +776,7 @@ constexpr auto fwd_kernel() {
 template <int D>
 int launch_d(const AttnArgs& a, cudaStream_t stream) {
   using C = Cfg<D>;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   const uint32_t kv_rows = a.block == 32 ? 32u : 64u;
   if (!encode_bhnd_map(&tq, a.q, a.batch, a.n_tokens, a.heads, D, a.q_strides[0], a.q_strides[1], a.q_strides[2],
                        C::CH, kTile, C::TMA_SWZ) ||
@@ -741,6 +804,13 @@ int launch_d(const AttnArgs& a, cudaStream_t stream) {
   }
   for (int h = 0; h < kMaxHeadMap; ++h) p.head_mask[h] = a.head_mask[h];
   p.o = static_cast<__nv_bfloat16*>(a.o);
+  // d = 64: O leaves through TMA stores of 32-row boxes when its layout allows a tensor map
+  // (16-byte aligned base and strides); otherwise, and at other d, through plain stores
+  memset(&to, 0, sizeof(to));
+  p.o_tma = D == 64 && encode_bhnd_map(&to, a.o, a.batch, a.n_tokens, a.heads, D, a.o_strides[0], a.o_strides[1],
+                                       a.o_strides[2], C::CH, 32, C::TMA_SWZ)
+                ? 1
+                : 0;
   p.lse = a.lse;
   p.o_sb = a.o_strides[0];
   p.o_sn = a.o_strides[1];
@@ -785,13 +855,13 @@ int launch_d(const AttnArgs& a, cudaStream_t stream) {
     p.work_list = list;
     p.list_hdr = &hdr->list_len;
     grid = sm_count;   // the list is at most n_items + slot_cap entries long
-    kern<<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, p);
+    kern<<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, to, p);
     if (cudaGetLastError() != cudaSuccess) return SA_ERR_CUDA;
     const int mgrid = (int)(ws.slot_cap < (size_t)(2 * sm_count) ? ws.slot_cap : (size_t)(2 * sm_count));
     fwd_merge_kernel<D><<<mgrid, kTile, 0, stream>>>(p, split_items, hdr);
     return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;
   }
-  kern<<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, p);
+  kern<<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, to, p);
   return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 

@@ -163,6 +163,7 @@ struct Params {
   const int32_t* col_idx[kMaxMasks];
   uint8_t head_mask[kMaxHeadMap];      // query head -> CSR (n_masks > 1)
   __nv_bfloat16* o;
+  int o_tma;                           // the kernel's output tensor map describes o (TMA stores)
   float* lse;
   int64_t o_sb, o_sn, o_sh;
   float scale_log2;

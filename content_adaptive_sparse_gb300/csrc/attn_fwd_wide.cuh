@@ -476,7 +476,9 @@ __device__ void epilogue(const Params& p, StreamBars& bars, const EpiEntry* epi,
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ Params p) {
+                         const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
+                         const __grid_constant__ Params p) {
+  // `to` (the output map) is not used here: the epilogue warps write O with plain stores
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sbase = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));

@@ -285,9 +285,53 @@ def test_concurrent_launches_on_four_streams():
                                f"stream case d={d} b={p.block} causal={p.causal}")
 
 
-@pytest.mark.parametrize("d", [32, 64])
+@pytest.mark.parametrize("d", [32, 64, 128])
 def test_items_spanning_several_tile_batches(d):
     """Full causal mask at 4096 tokens with 32-token blocks: the last query tiles' key lists
     hold 128 blocks = 32 key tiles of 128 keys, published in more than one batch of tiles;
     the item's output must not depend on where the batches split it."""
     _run_case(om.MaskParams("full", 32, 4096, 1), 1, 1, 1, d, seed=40 + d, qmul=2.0)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_many_items_per_cta_with_keyless_items(d):
+    """640 work items (more than four per SM, so no split and each CTA runs a stream of
+    several items) over a random causal CSR in which about a third of the query blocks have
+    no key block at all: items without key tiles interleave with items of one to eight key
+    tiles, so the hand-over of each item's output, and of O to the next item, happens many
+    times per CTA (at d = 128 through the epilogue warps)."""
+    torch = torch_cuda()
+    rng = np.random.default_rng(70 + d)
+    bt, n, h, hkv, b = 4, 2048, 10, 5, 128
+    nb = n // b
+    rp = np.zeros((bt, nb + 1), dtype=np.int32)
+    cols = []
+    for s in range(bt):
+        rp[s, 0] = len(cols)
+        for I in range(nb):
+            row = []
+            if rng.random() >= 0.35:
+                picks = set(rng.integers(0, I + 1, size=int(rng.integers(1, 9))).tolist())
+                if rng.random() < 0.5:
+                    picks.add(I)
+                row = sorted(picks)
+            cols += row
+            rp[s, I + 1] = len(cols)
+    ci = np.array(cols, dtype=np.int32)
+    qb = bf16_normal_bits(rng, (bt, n, h, d), 0.25)
+    kb = bf16_normal_bits(rng, (bt, n, hkv, d), 0.25)
+    vb = bf16_normal_bits(rng, (bt, n, hkv, d), 0.25)
+    o, lse = sa.attn_fwd(to_dev(qb), to_dev(kb), to_dev(vb), torch.from_numpy(rp).cuda(),
+                         torch.from_numpy(ci).cuda(), b, 1)
+    torch.cuda.synchronize()
+    assert sa.sa_device_status() == 0
+    f = bf16_bits_to_f64
+    o_ref, lse_ref = oracle.attention_csr(f(qb), f(kb), f(vb), rp, ci, b, 1)
+    assert_attention_close(bf16_to_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref,
+                           f"many items d={d}")
+    # rows of key-less query blocks: O = 0 and LSE = -inf
+    empty = [(s, I) for s in range(bt) for I in range(nb) if rp[s, I + 1] == rp[s, I]]
+    assert empty
+    oh, lh = bf16_to_f64(o), lse.cpu().numpy()
+    for s, I in empty[:8]:
+        assert np.all(oh[s, I * b:(I + 1) * b] == 0) and np.all(np.isneginf(lh[s, :, I * b:(I + 1) * b]))
