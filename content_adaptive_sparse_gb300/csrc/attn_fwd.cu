@@ -521,8 +521,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ split-row combine (K9)
 //
-// Used when a launch has fewer work items than four per SM of the GPU: a few long key
-// lists would then leave SMs idle. fwd_plan_kernel counts the key tiles of every query tile's
+// Used when a launch has few work items for the GPU's item streams (see launch_d): a few long
+// key lists would then leave SMs idle. fwd_plan_kernel counts the key tiles of every query tile's
 // union (one warp per (mask, CSR sequence, query tile)), fwd_schedule_kernel (one CTA) cuts the
 // items whose lists are longer than T tiles into parts of T tiles, each with a slot for its
 // partial result, and lists the parts first, then the other items; attn_fwd_kernel runs the
@@ -836,12 +836,15 @@ int launch_d(const AttnArgs& a, cudaStream_t stream) {
   if (fa.numRegs != kLaunchRegs) return SA_ERR_UNSUPPORTED;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return SA_ERR_CUDA;
-  // Split mode when the items are few for the GPU (fewer than four per SM) and the workspace
-  // holds partial-result slots: long key lists are then cut into parts (K9), about two per
-  // item stream (two streams per SM at d <= 64, one at d = 128).
+  // Split mode when the items are few for the GPU's item streams and the workspace holds
+  // partial-result slots: long key lists are then cut into parts (K9), about two per stream.
+  // d <= 64 (two streams per SM, each at about half an SM's speed): fewer than two items per
+  // stream. d = 128 (one stream per SM at a whole SM's speed, which balances a few long items
+  // well in longest-first order): fewer items than SMs. The schedule kernel still keeps the
+  // items whole when the longest is within 1.25x of a stream's share.
   const int per_cta = C::WIDE ? 1 : 2;
   const int n_pipes = per_cta * sm_count;
-  const bool split = ws.slot_cap >= 2 && p.n_items < 4 * sm_count;
+  const bool split = ws.slot_cap >= 2 && p.n_items < (C::WIDE ? 1 : 2) * n_pipes;
   int grid = (p.n_items + per_cta - 1) / per_cta < sm_count ? (p.n_items + per_cta - 1) / per_cta : sm_count;
   if (split) {
     int* tiles = reinterpret_cast<int*>(wsb + ws.tiles_off);

@@ -134,11 +134,13 @@ int sa_attn_fwd_workspace_size(int32_t batch, int32_t n_tokens, int32_t heads, i
  *   workspace : caller-owned device memory, 256-byte aligned, at least 256 bytes; its
  *   contents on entry do not matter. It holds the launch's work counter, so launches in
  *   flight at the same time need separate workspaces. With
- *   sa_attn_fwd_workspace_size bytes, a launch with fewer work items (128-row query tiles
- *   x heads x sequences) than four per SM splits the items whose key lists are longest
- *   into parts of equal key-tile counts, writes each part's O and LSE to the workspace and
- *   merges them (LSE = ln sum exp LSE_p, O = sum exp(LSE_p - LSE) O_p), so that a few long
- *   rows do not leave SMs idle; a smaller workspace (>= 256 bytes) never splits. */
+ *   sa_attn_fwd_workspace_size bytes, a launch with few work items (128-row query tiles
+ *   x heads x sequences: fewer than four per SM at head_dim 32 or 64, fewer than one per SM
+ *   at 128) whose longest key list exceeds 1.25x an even share splits the items whose key
+ *   lists are longest into parts of equal key-tile counts, writes each part's O and LSE to
+ *   the workspace and merges them (LSE = ln sum exp LSE_p, O = sum exp(LSE_p - LSE) O_p), so
+ *   that a few long rows do not leave SMs idle; a smaller workspace (>= 256 bytes) never
+ *   splits. */
 int sa_attn_fwd(const void* q, const void* k, const void* v, const int64_t q_strides[3],
                 const int64_t kv_strides[3], const int64_t o_strides[3], int32_t batch, int32_t n_tokens,
                 int32_t heads, int32_t kv_heads, int32_t head_dim, int32_t block, int32_t causal,

@@ -1,9 +1,10 @@
 """Split-row combine of the block-sparse forward: long key lists cut into parts that write
 partial (O, LSE) to the workspace and are merged by log-sum-exp.
 
-A launch splits when it has fewer work items (query tiles x heads x sequences) than four
-per SM and its workspace has room for partial results; the shapes below are chosen so that
-it does (one or two sequences and heads with long rows: the full causal mask, BigBird's
+A launch splits when it has few work items (query tiles x heads x sequences: fewer than
+four per SM at d = 32 or 64, fewer than one per SM at d = 128), its longest key list exceeds
+1.25x an even share and its workspace has room for partial results; the shapes below are
+chosen so that it does (one or two sequences and heads with long rows: the full causal mask, BigBird's
 global rows that attend to every key). Each case is compared with the float64 oracle on
 every row, and the workspace's split header (list length, split entries, key tiles per part,
 split items; 16 bytes at offset 64) must show that items were split. The same call with a
