@@ -40,6 +40,11 @@ namespace {
 
 constexpr int kSoftmaxWarps = 4;      // per pipeline: one per TMEM lane quarter
 constexpr int kTmaStoreTiles = 4;     // d = 64: items of at least this many key tiles store O by TMA
+// Of every 16 exponential pairs, these many on the FMA pipe (exp2_fma2). Measured on the 8K
+// top-16 workload at 0 / 1 / 2 / 3 / 4 pairs: 193-195 / 197-199 / 199-200 / 211 / 213-215 us:
+// in this kernel the exponentials are not held up by the MUFU pipe but by issue slots and
+// latency, so the polynomial's extra instructions only add time.
+constexpr int kPolyPairs = 0;
 constexpr int kMetaConsumers = 2 + kSoftmaxWarps;   // MMA thread, loader, softmax warps
 __host__ __device__ constexpr uint32_t col_s(int x) { return 256u * x; }
 __host__ __device__ constexpr uint32_t col_p(int x) { return 256u * x + 128u; }
@@ -291,7 +296,7 @@ __device__ void softmax_epilogue(const Params& p, int x, PipeBars& bars, const B
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
         if ((vis >> ch) & 1) {
-          chunk_exp(v + 32 * ch, c2, negm2, pk + 16 * ch, rs);
+          chunk_exp<kPolyPairs>(v + 32 * ch, c2, negm2, pk + 16 * ch, rs);
         } else {
 #pragma unroll
           for (int j = 0; j < 16; ++j) pk[16 * ch + j] = 0u;

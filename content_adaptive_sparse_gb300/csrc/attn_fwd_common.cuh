@@ -450,14 +450,50 @@ __device__ __forceinline__ void mask_chunk(uint32_t* v, uint32_t kp) {
   for (int j = 0; j < 32; ++j) v[j] = ((kp >> j) & 1u) ? v[j] : 0xff800000u;
 }
 
+// 2^x of two values on the FMA pipe: Cody-Waite range reduction 2^x = 2^n * 2^f with
+// n = floor(x) (rounding x + 1.5 * 2^23 toward minus infinity leaves n in the low mantissa bits)
+// and f = x - n in [0, 1), then a cubic fitted to 2^f on [0, 1] for this kernel (least squares,
+// largest relative error 7.5e-5, far below the bf16 rounding of P); 2^n enters as n added to the
+// exponent field. x is at most 8 here (the lazily rescaled running max); x below -126 (masked
+// scores included) gives exactly 0.
+__device__ __forceinline__ uint64_t exp2_fma2(uint64_t x2) {
+  float a, b;
+  f2_unpack(x2, a, b);
+  const float ac = fmaxf(a, -127.f), bc = fmaxf(b, -127.f);
+  const uint64_t x = f2_pack(ac, bc);
+  const uint64_t magic = f2_pack(12582912.f, 12582912.f);
+  uint64_t t, n, f;
+  asm("add.rm.f32x2 %0, %1, %2;" : "=l"(t) : "l"(x), "l"(magic));
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(n) : "l"(t), "l"(magic));
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(f) : "l"(x), "l"(n));
+  uint64_t q = f2_fma(f, f2_pack(0.07802403f, 0.07802403f), f2_pack(0.22606707f, 0.22606707f));
+  q = f2_fma(f, q, f2_pack(0.695834f, 0.695834f));
+  q = f2_fma(f, q, f2_pack(0.99992514f, 0.99992514f));
+  float q0, q1, t0, t1;
+  f2_unpack(q, q0, q1);
+  f2_unpack(t, t0, t1);
+  const float r0 = a < -126.f ? 0.f : __uint_as_float(__float_as_uint(q0) + (__float_as_uint(t0) << 23));
+  const float r1 = b < -126.f ? 0.f : __uint_as_float(__float_as_uint(q1) + (__float_as_uint(t1) << 23));
+  return f2_pack(r0, r1);
+}
+
 // p = 2^(s c - m) of one chunk into packed bf16 (a score of -inf gives exactly 0); adds the
-// row sum into rs.
+// row sum into rs. The first POLY of the chunk's 16 pairs take 2^x on the FMA pipe, the rest
+// on the MUFU pipe (ex2.approx), so that the two pipes share the exponentials.
+template <int POLY = 0>
 __device__ __forceinline__ void chunk_exp(const uint32_t* v, uint64_t c2, uint64_t negm2, uint32_t* pk, uint64_t* rs) {
 #pragma unroll
   for (int j = 0; j < 32; j += 2) {
-    float x0, x1;
-    f2_unpack(f2_fma(f2_pack(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), c2, negm2), x0, x1);
-    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+    const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), c2, negm2);
+    float p0, p1;
+    if ((j >> 1) < POLY) {
+      f2_unpack(exp2_fma2(x2), p0, p1);
+    } else {
+      float x0, x1;
+      f2_unpack(x2, x0, x1);
+      p0 = ex2_approx(x0);
+      p1 = ex2_approx(x1);
+    }
     rs[(j >> 1) & 1] = f2_add(rs[(j >> 1) & 1], f2_pack(p0, p1));
     pk[j >> 1] = pack_bf16x2(p0, p1);
   }
