@@ -1,6 +1,7 @@
 // GPU block-CSR builder: per-block ratios and pattern parameters -> row_ptr / col_idx.
 //
-// CTAs of 1024 threads, a few per sequence (grid.y splits the rows). Each CTA
+// CTAs of 256 threads (short sequences) or 1024, a few per sequence (grid.y splits the rows).
+// Each CTA
 //   1. computes the per-sequence state the mode needs (ratio rank order for TOPK,
 //      literal flags from the mean threshold for LITERAL_MEAN),
 //   2. computes every row length and an exclusive scan of them (row_ptr), offset by the
@@ -11,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <stdint.h>
 
 #include "sa_internal.h"
@@ -18,8 +20,10 @@
 namespace sa {
 namespace {
 
-constexpr int kThreads = 1024;
-constexpr int kWarps = kThreads / 32;
+constexpr int kMaxThreads = 1024;     // CTA size for long sequences (256 when nb <= 1024)
+constexpr int kMaxWarps = kMaxThreads / 32;
+__device__ __forceinline__ int n_threads() { return (int)blockDim.x; }
+__device__ __forceinline__ int n_warps() { return (int)(blockDim.x >> 5); }
 
 struct MaskArgs {
   int mode, block, nb, batch, causal, w, g, k, r;
@@ -69,7 +73,7 @@ __device__ int64_t block_sum(int64_t v, int64_t* red) {
   if (lane == 0) red[wid] = v;
   __syncthreads();
   int64_t t = 0;
-  for (int i = 0; i < kWarps; ++i) t += red[i];
+  for (int i = 0; i < n_warps(); ++i) t += red[i];
   __syncthreads();
   return t;
 }
@@ -81,15 +85,15 @@ __device__ double block_sum_f64(double v, double* red) {
   if (lane == 0) red[wid] = v;
   __syncthreads();
   double t = 0.0;
-  for (int i = 0; i < kWarps; ++i) t += red[i];
+  for (int i = 0; i < n_warps(); ++i) t += red[i];
   __syncthreads();
   return t;
 }
 
-// In-place exclusive scan of a[0..n), n <= 4 * kThreads. Returns the total.
+// In-place exclusive scan of a[0..n), n <= 4 * blockDim.x. Returns the total.
 __device__ int block_exclusive_scan(int* a, int n, int* tmp) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int per = (n + kThreads - 1) / kThreads;
+  const int per = (n + n_threads() - 1) / n_threads();
   const int base = tid * per;
   int local[4];
   int s = 0;
@@ -108,7 +112,7 @@ __device__ int block_exclusive_scan(int* a, int n, int* tmp) {
   if (lane == 31) tmp[wid] = x;
   __syncthreads();
   if (wid == 0) {
-    const int w = tmp[lane];
+    const int w = lane < n_warps() ? tmp[lane] : 0;
     int wx = w;
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, wx, o);
@@ -134,7 +138,7 @@ struct Smem {
   float* r;        // [nb] ratios of the current sequence
   int* order;      // [nb] TOPK: blocks by (ratio desc, index asc); LITERAL_MEAN: literal prefix [nb+1]
   int* cnt;        // [nb] row lengths, scanned in place into row offsets
-  uint32_t* bm;    // [kWarps][words] per-warp bitmaps
+  uint32_t* bm;    // [warps][words] per-warp bitmaps
   int words;
   int64_t* red;
   double* redf;
@@ -142,7 +146,7 @@ struct Smem {
 };
 
 __device__ void load_ratios(const MaskArgs& a, const Smem& s, int seq) {
-  for (int j = threadIdx.x; j < a.nb; j += kThreads) s.r[j] = a.ratio[(size_t)seq * a.nb + j];
+  for (int j = threadIdx.x; j < a.nb; j += n_threads()) s.r[j] = a.ratio[(size_t)seq * a.nb + j];
   __syncthreads();
 }
 
@@ -150,7 +154,7 @@ __device__ void load_ratios(const MaskArgs& a, const Smem& s, int seq) {
 // consecutive lanes share a block j and count over interleaved eighths of the blocks.
 __device__ void topk_order(const MaskArgs& a, const Smem& s) {
   const int part = threadIdx.x & 7;
-  constexpr int kGroups = kThreads >> 3;
+  const int kGroups = n_threads() >> 3;
   const int iters = (a.nb + kGroups - 1) / kGroups;   // the same for every thread: the
   for (int it = 0; it < iters; ++it) {                // whole warp reaches the shuffles
     const int j0 = (threadIdx.x >> 3) + kGroups * it;
@@ -172,10 +176,10 @@ __device__ void topk_order(const MaskArgs& a, const Smem& s) {
 // LITERAL_MEAN: literal flag l_j = (r_j > mean r); stored as prefix counts lit[0..nb].
 __device__ void literal_prefix(const MaskArgs& a, const Smem& s) {
   double part = 0.0;
-  for (int j = threadIdx.x; j < a.nb; j += kThreads) part += (double)s.r[j];
+  for (int j = threadIdx.x; j < a.nb; j += n_threads()) part += (double)s.r[j];
   const double mean = block_sum_f64(part, s.redf) / (double)a.nb;
   int* lit = s.order;
-  for (int j = threadIdx.x; j < a.nb; j += kThreads) lit[j] = ((double)s.r[j] > mean) ? 1 : 0;
+  for (int j = threadIdx.x; j < a.nb; j += n_threads()) lit[j] = ((double)s.r[j] > mean) ? 1 : 0;
   __syncthreads();
   const int total = block_exclusive_scan(lit, a.nb, s.scan_tmp);
   if (threadIdx.x == 0) lit[a.nb] = total;
@@ -227,7 +231,7 @@ __device__ int row_len(const MaskArgs& a, const Smem& s, int I) {
 // Total entries of one sequence (state for that sequence already in smem).
 __device__ int64_t seq_total(const MaskArgs& a, const Smem& s) {
   int64_t part = 0;
-  for (int I = threadIdx.x; I < a.nb; I += kThreads) part += row_len(a, s, I);
+  for (int I = threadIdx.x; I < a.nb; I += n_threads()) part += row_len(a, s, I);
   return block_sum(part, s.red);
 }
 
@@ -349,12 +353,12 @@ __device__ void fill_bigbird(const MaskArgs& a, int I, int32_t* out, int* picks)
   __syncwarp();
 }
 
-__global__ void __launch_bounds__(kThreads) build_mask_kernel(MaskArgs a) {
+__global__ void __launch_bounds__(kMaxThreads) build_mask_kernel(MaskArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
-  __shared__ int64_t red[kWarps];
-  __shared__ double redf[kWarps];
+  __shared__ int64_t red[kMaxWarps];
+  __shared__ double redf[kMaxWarps];
   __shared__ int scan_tmp[33];
-  __shared__ int picks_all[kWarps][kMaxRandomBlocks];
+  __shared__ int picks_all[kMaxWarps][kMaxRandomBlocks];
   const int seq = blockIdx.x;
   Smem s;
   s.words = (a.nb + 31) / 32;
@@ -380,7 +384,7 @@ __global__ void __launch_bounds__(kThreads) build_mask_kernel(MaskArgs a) {
   if (a.mode == SA_MASK_TOPK) topk_order(a, s);
   if (a.mode == SA_MASK_LITERAL_MEAN) literal_prefix(a, s);
 
-  for (int I = threadIdx.x; I < a.nb; I += kThreads) s.cnt[I] = row_len(a, s, I);
+  for (int I = threadIdx.x; I < a.nb; I += n_threads()) s.cnt[I] = row_len(a, s, I);
   __syncthreads();
   const int total = block_exclusive_scan(s.cnt, a.nb, s.scan_tmp);
   // row lengths of the other modes do not depend on the data: every sequence has `total`
@@ -389,12 +393,12 @@ __global__ void __launch_bounds__(kThreads) build_mask_kernel(MaskArgs a) {
   const int per = (a.nb + gridDim.y - 1) / gridDim.y;
   const int row_lo = blockIdx.y * per, row_hi = min(a.nb, row_lo + per);
   int32_t* rp = a.row_ptr + (size_t)seq * (a.nb + 1);
-  for (int I = row_lo + threadIdx.x; I < row_hi; I += kThreads) rp[I] = (int32_t)(base + s.cnt[I]);
+  for (int I = row_lo + threadIdx.x; I < row_hi; I += n_threads()) rp[I] = (int32_t)(base + s.cnt[I]);
   if (blockIdx.y == 0 && threadIdx.x == 0) rp[a.nb] = (int32_t)(base + total);
 
   const int wid = threadIdx.x >> 5;
   uint32_t* bm = s.bm + (size_t)wid * s.words;
-  for (int I = row_lo + wid; I < row_hi; I += kWarps) {
+  for (int I = row_lo + wid; I < row_hi; I += n_warps()) {
     int32_t* out = a.col_idx + base + s.cnt[I];
     switch (a.mode) {
       case SA_MASK_TOPK: fill_topk(a, s, I, out, bm); break;
@@ -407,6 +411,24 @@ __global__ void __launch_bounds__(kThreads) build_mask_kernel(MaskArgs a) {
       }
     }
   }
+}
+
+// The kernel's dynamic shared-memory limit, raised on the current device only when a launch
+// needs more than it was last raised to (the attribute call costs host time on every launch).
+bool mask_smem_ready(size_t smem) {
+  static std::atomic<size_t> raised[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::atomic<size_t>* r = dev >= 0 && dev < 64 ? &raised[dev] : nullptr;
+  if (r != nullptr && smem <= r->load()) return true;
+  if (cudaFuncSetAttribute(build_mask_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return false;
+  if (r != nullptr) {
+    size_t cur = r->load();
+    while (cur < smem && !r->compare_exchange_weak(cur, smem)) {
+    }
+  }
+  return true;
 }
 
 }  // namespace
@@ -431,15 +453,20 @@ int launch_build_mask(const sa_mask_params& p, const float* d_ratio, int32_t* d_
   a.row_ptr = d_row_ptr;
   a.col_idx = d_col_idx;
   const int words = (a.nb + 31) / 32;
-  const size_t smem = (size_t)a.nb * 4 + (size_t)(a.nb + 1) * 4 + (size_t)a.nb * 4 + (size_t)kWarps * words * 4;
-  if (cudaFuncSetAttribute(build_mask_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-      cudaSuccess)
-    return SA_ERR_CUDA;
-  // rows of a sequence split over up to nb / 32 CTAs (one row per warp), enough CTAs in all
-  // to cover the GPU twice; each CTA rebuilds the sequence's state, which is cheap
+  // 256-thread CTAs (more, shorter CTAs: the per-sequence state is cheap to rebuild) while
+  // the scan's four entries per thread cover the sequence's blocks and, for TOPK, the rank
+  // pass (nb^2 / threads compares per thread) stays short; else 1024. Measured: 8K top-16
+  // (128 blocks) 10.9 -> 8.9 us, the three head-group masks 200 -> 52 us; 64K top-64 (512
+  // blocks) is faster with 1024 threads (19 against 23 us).
+  const int threads = (a.nb <= 4 * 256 && (a.mode != SA_MASK_TOPK || a.nb <= 256)) ? 256 : kMaxThreads;
+  const int warps = threads / 32;
+  const size_t smem = (size_t)a.nb * 4 + (size_t)(a.nb + 1) * 4 + (size_t)a.nb * 4 + (size_t)warps * words * 4;
+  if (!mask_smem_ready(smem)) return SA_ERR_CUDA;
+  // rows of a sequence split over up to nb / warps CTAs (one row per warp), enough CTAs in
+  // all to cover the GPU twice; each CTA rebuilds the sequence's state, which is cheap
   const int sm_count = current_sm_count();
-  const int groups = std::max(1, std::min((a.nb + kWarps - 1) / kWarps, (2 * sm_count + a.batch - 1) / a.batch));
-  build_mask_kernel<<<dim3((unsigned)a.batch, (unsigned)groups), kThreads, smem, stream>>>(a);
+  const int groups = std::max(1, std::min((a.nb + warps - 1) / warps, (2 * sm_count + a.batch - 1) / a.batch));
+  build_mask_kernel<<<dim3((unsigned)a.batch, (unsigned)groups), threads, smem, stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
