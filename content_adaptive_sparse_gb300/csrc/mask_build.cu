@@ -78,18 +78,6 @@ __device__ int64_t block_sum(int64_t v, int64_t* red) {
   return t;
 }
 
-__device__ double block_sum_f64(double v, double* red) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  __syncthreads();
-  if (lane == 0) red[wid] = v;
-  __syncthreads();
-  double t = 0.0;
-  for (int i = 0; i < n_warps(); ++i) t += red[i];
-  __syncthreads();
-  return t;
-}
-
 // In-place exclusive scan of a[0..n), n <= 4 * blockDim.x. Returns the total.
 __device__ int block_exclusive_scan(int* a, int n, int* tmp) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -134,11 +122,16 @@ __device__ int block_exclusive_scan(int* a, int n, int* tmp) {
 
 // ---------------------------------------------------------------- per-mode pieces
 
+constexpr int kPriorWarps = 8;          // warps that derive earlier sequences' entry counts
+constexpr int kPriorMaxBlocks = 1024;   // ... when their literal prefixes fit in shared memory
+
 struct Smem {
   float* r;        // [nb] ratios of the current sequence
   int* order;      // [nb] TOPK: blocks by (ratio desc, index asc); LITERAL_MEAN: literal prefix [nb+1]
   int* cnt;        // [nb] row lengths, scanned in place into row offsets
   uint32_t* bm;    // [warps][words] per-warp bitmaps
+  int* lscr;       // LITERAL_MEAN, nb <= kPriorMaxBlocks: [kPriorWarps][nb+1] literal prefixes of
+                   // earlier sequences (nullptr: derive them one after another)
   int words;
   int64_t* red;
   double* redf;
@@ -174,10 +167,26 @@ __device__ void topk_order(const MaskArgs& a, const Smem& s) {
 }
 
 // LITERAL_MEAN: literal flag l_j = (r_j > mean r); stored as prefix counts lit[0..nb].
-__device__ void literal_prefix(const MaskArgs& a, const Smem& s) {
+// Mean of one sequence's ratios (r: nb values), computed by one warp with the same arithmetic
+// wherever it runs: lane-strided partial sums in double, then a butterfly over the warp (every
+// lane ends with the same bits, as each step adds the same two values). Every CTA that derives
+// a sequence's literal flags therefore agrees with every other on them.
+__device__ double warp_seq_mean(const MaskArgs& a, const float* r) {
+  const int lane = threadIdx.x & 31;
   double part = 0.0;
-  for (int j = threadIdx.x; j < a.nb; j += n_threads()) part += (double)s.r[j];
-  const double mean = block_sum_f64(part, s.redf) / (double)a.nb;
+  for (int j = lane; j < a.nb; j += 32) part += (double)r[j];
+  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+  return part / (double)a.nb;
+}
+
+__device__ void literal_prefix(const MaskArgs& a, const Smem& s) {
+  if ((threadIdx.x >> 5) == 0) {
+    const double m = warp_seq_mean(a, s.r);
+    if (threadIdx.x == 0) s.redf[0] = m;
+  }
+  __syncthreads();
+  const double mean = s.redf[0];
+  __syncthreads();
   int* lit = s.order;
   for (int j = threadIdx.x; j < a.nb; j += n_threads()) lit[j] = ((double)s.r[j] > mean) ? 1 : 0;
   __syncthreads();
@@ -191,6 +200,52 @@ __device__ __forceinline__ int lit_at(const int* litpre, int j) { return litpre[
 __device__ __forceinline__ int bigbird_wlo(const MaskArgs& a, int I) { return I - a.w / 2; }
 
 // Length of row I.
+// LITERAL_MEAN row length of block row I from the literal prefix lp[0..nb].
+__device__ int literal_row_len(const MaskArgs& a, const int* lp, int I) {
+  int n = 1;                                                         // identity
+  if (a.local) {
+    const int lo = max(0, I - a.w);
+    const int hi = a.causal ? I : min(a.nb - 1, I + a.w);
+    n = hi - lo + 1;
+  }
+  if (a.literal && lit_at(lp, I)) {
+    if (I - a.w - 1 >= 0) n += lp[I - a.w];                         // literals in [0, I-w-1]
+    if (!a.causal && I + a.w + 1 < a.nb) n += lp[a.nb] - lp[I + a.w + 1];
+  }
+  return n;
+}
+
+// LITERAL_MEAN: CSR entries of the sequences before `seq`, warp w < kPriorWarps taking
+// sequences w, w + kPriorWarps, ... (mean, literal prefix in its own scratch, row lengths).
+__device__ int64_t literal_prior_entries(const MaskArgs& a, int seq, int* scratch, int64_t* red) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int nw = min(n_warps(), kPriorWarps);
+  int64_t mine = 0;
+  if (wid < nw) {
+    int* lp = scratch + (size_t)wid * (a.nb + 1);
+    for (int p = wid; p < seq; p += nw) {
+      const float* r = a.ratio + (size_t)p * a.nb;
+      const double mean = warp_seq_mean(a, r);
+      int run = 0;
+      for (int j0 = 0; j0 < a.nb; j0 += 32) {
+        const int j = j0 + lane;
+        const bool f = j < a.nb && (double)r[j] > mean;
+        const unsigned m = __ballot_sync(0xffffffffu, f);
+        if (j < a.nb) lp[j] = run + __popc(m & lanemask_lt());
+        run += __popc(m);
+      }
+      if (lane == 0) lp[a.nb] = run;
+      __syncwarp();
+      int64_t tot = 0;
+      for (int I = lane; I < a.nb; I += 32) tot += literal_row_len(a, lp, I);
+      for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+      mine += tot;
+      __syncwarp();                                  // lp is this warp's again for its next sequence
+    }
+  }
+  return block_sum(lane == 0 ? mine : 0, red);
+}
+
 __device__ int row_len(const MaskArgs& a, const Smem& s, int I) {
   switch (a.mode) {
     case SA_MASK_TOPK: {
@@ -210,20 +265,8 @@ __device__ int row_len(const MaskArgs& a, const Smem& s, int I) {
       const int n_union = n_w + g - n_wg;
       return n_union + min(a.r, a.nb - n_union);
     }
-    case SA_MASK_LITERAL_MEAN: {
-      const int* lp = s.order;
-      int n = 1;                                                       // identity
-      if (a.local) {
-        const int lo = max(0, I - a.w);
-        const int hi = a.causal ? I : min(a.nb - 1, I + a.w);
-        n = hi - lo + 1;
-      }
-      if (a.literal && lit_at(lp, I)) {
-        if (I - a.w - 1 >= 0) n += lp[I - a.w];                       // literals in [0, I-w-1]
-        if (!a.causal && I + a.w + 1 < a.nb) n += lp[a.nb] - lp[I + a.w + 1];
-      }
-      return n;
-    }
+    case SA_MASK_LITERAL_MEAN:
+      return literal_row_len(a, s.order, I);
   }
   return 0;
 }
@@ -366,6 +409,9 @@ __global__ void __launch_bounds__(kMaxThreads) build_mask_kernel(MaskArgs a) {
   s.order = reinterpret_cast<int*>(s.r + a.nb);
   s.cnt = s.order + (a.nb + 1);
   s.bm = reinterpret_cast<uint32_t*>(s.cnt + a.nb);
+  s.lscr = (a.mode == SA_MASK_LITERAL_MEAN && a.nb <= kPriorMaxBlocks)
+               ? reinterpret_cast<int*>(s.bm + (size_t)n_warps() * s.words)
+               : nullptr;
   s.red = red;
   s.redf = redf;
   s.scan_tmp = scan_tmp;
@@ -373,10 +419,14 @@ __global__ void __launch_bounds__(kMaxThreads) build_mask_kernel(MaskArgs a) {
   // Entries of the sequences before this one.
   int64_t base = 0;
   if (a.mode == SA_MASK_LITERAL_MEAN) {
-    for (int p = 0; p < seq; ++p) {
-      load_ratios(a, s, p);
-      literal_prefix(a, s);
-      base += seq_total(a, s);
+    if (s.lscr != nullptr) {
+      base = literal_prior_entries(a, seq, s.lscr, red);
+    } else {
+      for (int p = 0; p < seq; ++p) {
+        load_ratios(a, s, p);
+        literal_prefix(a, s);
+        base += seq_total(a, s);
+      }
     }
   }
   const bool needs_ratio = a.mode == SA_MASK_TOPK || a.mode == SA_MASK_LITERAL_MEAN;
@@ -460,7 +510,8 @@ int launch_build_mask(const sa_mask_params& p, const float* d_ratio, int32_t* d_
   // blocks) is faster with 1024 threads (19 against 23 us).
   const int threads = (a.nb <= 4 * 256 && (a.mode != SA_MASK_TOPK || a.nb <= 256)) ? 256 : kMaxThreads;
   const int warps = threads / 32;
-  const size_t smem = (size_t)a.nb * 4 + (size_t)(a.nb + 1) * 4 + (size_t)a.nb * 4 + (size_t)warps * words * 4;
+  size_t smem = (size_t)a.nb * 4 + (size_t)(a.nb + 1) * 4 + (size_t)a.nb * 4 + (size_t)warps * words * 4;
+  if (a.mode == SA_MASK_LITERAL_MEAN && a.nb <= kPriorMaxBlocks) smem += (size_t)kPriorWarps * (a.nb + 1) * 4;
   if (!mask_smem_ready(smem)) return SA_ERR_CUDA;
   // rows of a sequence split over up to nb / warps CTAs (one row per warp), enough CTAs in
   // all to cover the GPU twice; each CTA rebuilds the sequence's state, which is cheap

@@ -73,6 +73,17 @@ def test_literal_mean(causal, b, w):
     _compare(p, 3, sa.sa_block_ratios(data, b), oracle.block_ratios(data, b))
 
 
+@pytest.mark.parametrize("causal", [1, 0])
+def test_literal_mean_long_sequences(causal):
+    """1280 blocks per sequence (more than the 1024 whose literal prefixes the CTAs keep in
+    shared memory for the entry counts of earlier sequences), three sequences: the CTAs of later
+    sequences derive the earlier ones' counts one after another."""
+    n, b = 40960, 32
+    data = np.stack([bytes_zipf_text(300 + s, n) for s in range(3)])
+    p = om.MaskParams("literal_mean", b, n, causal, 1)
+    _compare(p, 3, sa.sa_block_ratios(data, b), oracle.block_ratios(data, b))
+
+
 @pytest.mark.parametrize("components", [1, 2])
 @pytest.mark.parametrize("causal", [1, 0])
 def test_literal_mean_components(causal, components):
