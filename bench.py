@@ -840,6 +840,7 @@ def _row_split(torch, dev, flush, peaks, max_over_ranks, steps, warm):
     out = {}
     for d in (64, 128):
         case = BlockSparseCase("full_32k_one_head", dev, head_dim=d, std=1.0 / (d ** 0.5))
+        case.ws[64:80].zero_()                       # split header: stays zero unless a launch splits
         seg, _ = _time_events(torch, [case.attend], steps, warm, flush)
         a = max_over_ranks(seg[0])
         full_ws = case.ws

@@ -146,6 +146,15 @@ def test_guard_empty_rows_causal():
     _case(1, 256, 2, 2, 64, 32, rows=rows, causal=1, seed=8)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_guard_keyless_query_tile(d):
+    """The second 128-row query tile of every (sequence, head) has no key block at all (its
+    four 32-token query blocks have empty rows): those items write zeros and -inf without key
+    tiles, next to items that do have some (at d = 128 through the epilogue warps)."""
+    rows = [[0], [0, 1], [], [2, 3], [], [], [], []]
+    _case(2, 256, 4, 2, d, 32, rows=rows, causal=1, seed=11 + d)
+
+
 @pytest.mark.parametrize("interp", [False, True])
 def test_guard_offset_kernels(interp):
     """The window-plus-offset kernels (integer and interpolated): O and LSE guarded, a
