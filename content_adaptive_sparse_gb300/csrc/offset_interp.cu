@@ -53,6 +53,9 @@ constexpr int kRingsBytes = kWarps * kRing * kBufBytes;
 constexpr int kSmemMain = kRingsBytes > 2 * kBandBytes ? kRingsBytes : 2 * kBandBytes;
 constexpr int kCtasPerSm = 4;              // 49 KB of shared memory per CTA
 static_assert(kSlabBoxBytes <= kSlotBytes && kSlotBytes % 1024 == 0, "slab slots");
+// the 16 x 24 score block of a rung pair reads key rows r0 .. r0 + 23: inside a slot, and at
+// most 6 rows past the K band (into the V band)
+static_assert(24 * kRowBytes <= kSlotBytes && (kBandRows + 6) * kRowBytes <= 2 * kBandBytes, "rung pair rows");
 
 struct InterpParams {
   int n_tokens, heads, heads_per_kv, ntiles;
@@ -70,6 +73,38 @@ struct InterpParams {
   int64_t q_sb, q_sn, q_sh, o_sb, o_sn, o_sh;
   float scale_log2;
 };
+
+// Raw scores of both distances of a rung for query rows g and g + 8 from one 16 x 24 block:
+// key rows r0 .. r0 + 23 of a swizzled tile, where r0 + r is distance lo + 1 of query r (the
+// diagonal, sb) and r0 + r + 1 distance lo (the superdiagonal, sa). Three 8-key n-tiles, 12
+// mma.sync, instead of two 16 x 16 blocks (16); of the third n-tile only column 0 (query 15's
+// distance lo) is read, so its other rows may hold anything. All lanes of a quad receive the
+// scores of their rows.
+__device__ __forceinline__ void diag_scores_pair(uint32_t kt, int r0, int g, int t, const uint32_t (&qa)[4][4],
+                                                 float& sa_lo, float& sa_hi, float& sb_lo, float& sb_hi) {
+  uint32_t u0[8], u1[8], u2[8];
+  load_kfrag(kt, r0 + g, t, u0);
+  load_kfrag(kt, r0 + 8 + g, t, u1);
+  load_kfrag(kt, r0 + 16 + g, t, u2);
+  float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f}, d2[4] = {0.f, 0.f, 0.f, 0.f};
+  qk_ntile(d0, qa, u0);
+  qk_ntile(d1, qa, u1);
+  qk_ntile(d2, qa, u2);
+  // fragment (row R, column C) of an n-tile: lane 4 (R % 8) + C / 2, element 2 (R / 8) + C % 2.
+  // Diagonal of query row g: column g of n-tile 0 (row g) / n-tile 1 (row g + 8). Superdiagonal:
+  // column g + 1, which for g = 7 is column 0 of the next n-tile. The lane holding either value
+  // has the same g as the lane asking for it, so each lane offers the elements its g selects.
+  const int e_a = g & 1, e_b = (g + 1) & 1;
+  const float diag_lo = e_a ? d0[1] : d0[0], diag_hi = e_a ? d1[3] : d1[2];
+  const float sup_lo = g < 7 ? (e_b ? d0[1] : d0[0]) : d1[0];
+  const float sup_hi = g < 7 ? (e_b ? d1[3] : d1[2]) : d2[2];
+  const int src_diag = 4 * g + (g >> 1);
+  const int src_sup = g < 7 ? 4 * g + ((g + 1) >> 1) : 28;
+  sb_lo = __shfl_sync(0xffffffffu, diag_lo, src_diag);
+  sb_hi = __shfl_sync(0xffffffffu, diag_hi, src_diag);
+  sa_lo = __shfl_sync(0xffffffffu, sup_lo, src_sup);
+  sa_hi = __shfl_sync(0xffffffffu, sup_hi, src_sup);
+}
 
 // Online-softmax state of one warp: O fragments, running max (log2 units) and row sums of
 // query rows g and g + 8.
@@ -259,8 +294,9 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
       const int far = lo + (two ? 1 : 0);
       const int ra = 16 * wq + kBandMax - lo;  // >= 1 since lo <= 63
       float sa_lo, sa_hi, sb_lo = 0.f, sb_hi = 0.f;
-      diag_scores(kb_tile, ra, g, t4, hl, e_sel, qa, sa_lo, sa_hi);
-      if (two) diag_scores(kb_tile, ra - 1, g, t4, hl, e_sel, qa, sb_lo, sb_hi);
+      // (the pair's block reads up to 7 rows past the K band, into the V band: unused values)
+      if (two) diag_scores_pair(kb_tile, ra - 1, g, t4, qa, sa_lo, sa_hi, sb_lo, sb_hi);
+      else diag_scores(kb_tile, ra, g, t4, hl, e_sel, qa, sa_lo, sa_hi);
       enter_rung(st, sa_lo, sa_hi, sb_lo, sb_hi, t, two, i_lo >= far, i_hi >= far, c, vb_tile, ra, ra - 1, lane,
                  holder, e_sel);
     }
@@ -294,8 +330,9 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
     const int far = lo + (two ? 1 : 0);
     const uint32_t kt = smem_u32(ring + b * kBufBytes);
     float sa_lo, sa_hi, sb_lo = 0.f, sb_hi = 0.f;
-    diag_scores(kt, 1, g, t4, hl, e_sel, qa, sa_lo, sa_hi);
-    if (two) diag_scores(kt, 0, g, t4, hl, e_sel, qa, sb_lo, sb_hi);
+    // (the pair's block reads rows 17 .. 23 of the 24-row slot: unused values)
+    if (two) diag_scores_pair(kt, 0, g, t4, qa, sa_lo, sa_hi, sb_lo, sb_hi);
+    else diag_scores(kt, 1, g, t4, hl, e_sel, qa, sa_lo, sa_hi);
     enter_rung(st, sa_lo, sa_hi, sb_lo, sb_hi, t, two, i_lo >= far, i_hi >= far, c, kt + kSlotBytes, 1, 0, lane,
                holder, e_sel);
     // every lane has read the buffer: refill it with the slab kRing ahead
