@@ -1,7 +1,7 @@
 // GPU block-CSR builder: per-block ratios and pattern parameters -> row_ptr / col_idx.
 //
-// CTAs of 256 threads (short sequences) or 1024, a few per sequence (grid.y splits the rows).
-// Each CTA
+// CTAs of 1024 threads (256 for mean-threshold masks of up to 1024 blocks), a few per sequence
+// (grid.y splits the rows). Each CTA
 //   1. computes the per-sequence state the mode needs (ratio rank order for TOPK,
 //      literal flags from the mean threshold for LITERAL_MEAN),
 //   2. computes every row length and an exclusive scan of them (row_ptr), offset by the
@@ -22,8 +22,7 @@ namespace {
 
 constexpr int kMaxThreads = 1024;     // CTA size for long sequences (256 when nb <= 1024)
 constexpr int kMaxWarps = kMaxThreads / 32;
-__device__ __forceinline__ int n_threads() { return (int)blockDim.x; }
-__device__ __forceinline__ int n_warps() { return (int)(blockDim.x >> 5); }
+
 
 struct MaskArgs {
   int mode, block, nb, batch, causal, w, g, k, r;
@@ -66,6 +65,7 @@ __device__ __forceinline__ unsigned lanemask_lt() {
 }
 
 // Sum of one int64 per thread over the CTA.
+template <int T>  // threads per CTA
 __device__ int64_t block_sum(int64_t v, int64_t* red) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -73,15 +73,16 @@ __device__ int64_t block_sum(int64_t v, int64_t* red) {
   if (lane == 0) red[wid] = v;
   __syncthreads();
   int64_t t = 0;
-  for (int i = 0; i < n_warps(); ++i) t += red[i];
+  for (int i = 0; i < (T / 32); ++i) t += red[i];
   __syncthreads();
   return t;
 }
 
 // In-place exclusive scan of a[0..n), n <= 4 * blockDim.x. Returns the total.
+template <int T>  // threads per CTA
 __device__ int block_exclusive_scan(int* a, int n, int* tmp) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int per = (n + n_threads() - 1) / n_threads();
+  const int per = (n + T - 1) / T;
   const int base = tid * per;
   int local[4];
   int s = 0;
@@ -100,7 +101,7 @@ __device__ int block_exclusive_scan(int* a, int n, int* tmp) {
   if (lane == 31) tmp[wid] = x;
   __syncthreads();
   if (wid == 0) {
-    const int w = lane < n_warps() ? tmp[lane] : 0;
+    const int w = lane < (T / 32) ? tmp[lane] : 0;
     int wx = w;
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, wx, o);
@@ -138,16 +139,18 @@ struct Smem {
   int* scan_tmp;   // [33]
 };
 
+template <int T>  // threads per CTA
 __device__ void load_ratios(const MaskArgs& a, const Smem& s, int seq) {
-  for (int j = threadIdx.x; j < a.nb; j += n_threads()) s.r[j] = a.ratio[(size_t)seq * a.nb + j];
+  for (int j = threadIdx.x; j < a.nb; j += T) s.r[j] = a.ratio[(size_t)seq * a.nb + j];
   __syncthreads();
 }
 
 // TOPK: rank by (ratio desc, index asc) over all blocks; order[rank] = block. Eight
 // consecutive lanes share a block j and count over interleaved eighths of the blocks.
+template <int T>  // threads per CTA
 __device__ void topk_order(const MaskArgs& a, const Smem& s) {
   const int part = threadIdx.x & 7;
-  const int kGroups = n_threads() >> 3;
+  const int kGroups = T >> 3;
   const int iters = (a.nb + kGroups - 1) / kGroups;   // the same for every thread: the
   for (int it = 0; it < iters; ++it) {                // whole warp reaches the shuffles
     const int j0 = (threadIdx.x >> 3) + kGroups * it;
@@ -179,6 +182,7 @@ __device__ double warp_seq_mean(const MaskArgs& a, const float* r) {
   return part / (double)a.nb;
 }
 
+template <int T>  // threads per CTA
 __device__ void literal_prefix(const MaskArgs& a, const Smem& s) {
   if ((threadIdx.x >> 5) == 0) {
     const double m = warp_seq_mean(a, s.r);
@@ -188,9 +192,9 @@ __device__ void literal_prefix(const MaskArgs& a, const Smem& s) {
   const double mean = s.redf[0];
   __syncthreads();
   int* lit = s.order;
-  for (int j = threadIdx.x; j < a.nb; j += n_threads()) lit[j] = ((double)s.r[j] > mean) ? 1 : 0;
+  for (int j = threadIdx.x; j < a.nb; j += T) lit[j] = ((double)s.r[j] > mean) ? 1 : 0;
   __syncthreads();
-  const int total = block_exclusive_scan(lit, a.nb, s.scan_tmp);
+  const int total = block_exclusive_scan<T>(lit, a.nb, s.scan_tmp);
   if (threadIdx.x == 0) lit[a.nb] = total;
   __syncthreads();
 }
@@ -217,9 +221,10 @@ __device__ int literal_row_len(const MaskArgs& a, const int* lp, int I) {
 
 // LITERAL_MEAN: CSR entries of the sequences before `seq`, warp w < kPriorWarps taking
 // sequences w, w + kPriorWarps, ... (mean, literal prefix in its own scratch, row lengths).
+template <int T>  // threads per CTA
 __device__ int64_t literal_prior_entries(const MaskArgs& a, int seq, int* scratch, int64_t* red) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int nw = min(n_warps(), kPriorWarps);
+  const int nw = min((T / 32), kPriorWarps);
   int64_t mine = 0;
   if (wid < nw) {
     int* lp = scratch + (size_t)wid * (a.nb + 1);
@@ -243,7 +248,7 @@ __device__ int64_t literal_prior_entries(const MaskArgs& a, int seq, int* scratc
       __syncwarp();                                  // lp is this warp's again for its next sequence
     }
   }
-  return block_sum(lane == 0 ? mine : 0, red);
+  return block_sum<T>(lane == 0 ? mine : 0, red);
 }
 
 __device__ int row_len(const MaskArgs& a, const Smem& s, int I) {
@@ -272,10 +277,11 @@ __device__ int row_len(const MaskArgs& a, const Smem& s, int I) {
 }
 
 // Total entries of one sequence (state for that sequence already in smem).
+template <int T>  // threads per CTA
 __device__ int64_t seq_total(const MaskArgs& a, const Smem& s) {
   int64_t part = 0;
-  for (int I = threadIdx.x; I < a.nb; I += n_threads()) part += row_len(a, s, I);
-  return block_sum(part, s.red);
+  for (int I = threadIdx.x; I < a.nb; I += T) part += row_len(a, s, I);
+  return block_sum<T>(part, s.red);
 }
 
 // ---------------------------------------------------------------- row fills (one warp)
@@ -396,7 +402,8 @@ __device__ void fill_bigbird(const MaskArgs& a, int I, int32_t* out, int* picks)
   __syncwarp();
 }
 
-__global__ void __launch_bounds__(kMaxThreads) build_mask_kernel(MaskArgs a) {
+template <int T>  // threads per CTA: 256 or 1024
+__global__ void __launch_bounds__(T) build_mask_kernel(MaskArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __shared__ int64_t red[kMaxWarps];
   __shared__ double redf[kMaxWarps];
@@ -410,7 +417,7 @@ __global__ void __launch_bounds__(kMaxThreads) build_mask_kernel(MaskArgs a) {
   s.cnt = s.order + (a.nb + 1);
   s.bm = reinterpret_cast<uint32_t*>(s.cnt + a.nb);
   s.lscr = (a.mode == SA_MASK_LITERAL_MEAN && a.nb <= kPriorMaxBlocks)
-               ? reinterpret_cast<int*>(s.bm + (size_t)n_warps() * s.words)
+               ? reinterpret_cast<int*>(s.bm + (size_t)(T / 32) * s.words)
                : nullptr;
   s.red = red;
   s.redf = redf;
@@ -420,35 +427,35 @@ __global__ void __launch_bounds__(kMaxThreads) build_mask_kernel(MaskArgs a) {
   int64_t base = 0;
   if (a.mode == SA_MASK_LITERAL_MEAN) {
     if (s.lscr != nullptr) {
-      base = literal_prior_entries(a, seq, s.lscr, red);
+      base = literal_prior_entries<T>(a, seq, s.lscr, red);
     } else {
       for (int p = 0; p < seq; ++p) {
-        load_ratios(a, s, p);
-        literal_prefix(a, s);
-        base += seq_total(a, s);
+        load_ratios<T>(a, s, p);
+        literal_prefix<T>(a, s);
+        base += seq_total<T>(a, s);
       }
     }
   }
   const bool needs_ratio = a.mode == SA_MASK_TOPK || a.mode == SA_MASK_LITERAL_MEAN;
-  if (needs_ratio) load_ratios(a, s, seq);
-  if (a.mode == SA_MASK_TOPK) topk_order(a, s);
-  if (a.mode == SA_MASK_LITERAL_MEAN) literal_prefix(a, s);
+  if (needs_ratio) load_ratios<T>(a, s, seq);
+  if (a.mode == SA_MASK_TOPK) topk_order<T>(a, s);
+  if (a.mode == SA_MASK_LITERAL_MEAN) literal_prefix<T>(a, s);
 
-  for (int I = threadIdx.x; I < a.nb; I += n_threads()) s.cnt[I] = row_len(a, s, I);
+  for (int I = threadIdx.x; I < a.nb; I += T) s.cnt[I] = row_len(a, s, I);
   __syncthreads();
-  const int total = block_exclusive_scan(s.cnt, a.nb, s.scan_tmp);
+  const int total = block_exclusive_scan<T>(s.cnt, a.nb, s.scan_tmp);
   // row lengths of the other modes do not depend on the data: every sequence has `total`
   if (a.mode != SA_MASK_LITERAL_MEAN) base = (int64_t)seq * total;
   // this CTA's share of the rows: every CTA of the sequence holds the same state and offsets
   const int per = (a.nb + gridDim.y - 1) / gridDim.y;
   const int row_lo = blockIdx.y * per, row_hi = min(a.nb, row_lo + per);
   int32_t* rp = a.row_ptr + (size_t)seq * (a.nb + 1);
-  for (int I = row_lo + threadIdx.x; I < row_hi; I += n_threads()) rp[I] = (int32_t)(base + s.cnt[I]);
+  for (int I = row_lo + threadIdx.x; I < row_hi; I += T) rp[I] = (int32_t)(base + s.cnt[I]);
   if (blockIdx.y == 0 && threadIdx.x == 0) rp[a.nb] = (int32_t)(base + total);
 
   const int wid = threadIdx.x >> 5;
   uint32_t* bm = s.bm + (size_t)wid * s.words;
-  for (int I = row_lo + wid; I < row_hi; I += n_warps()) {
+  for (int I = row_lo + wid; I < row_hi; I += (T / 32)) {
     int32_t* out = a.col_idx + base + s.cnt[I];
     switch (a.mode) {
       case SA_MASK_TOPK: fill_topk(a, s, I, out, bm); break;
@@ -465,13 +472,15 @@ __global__ void __launch_bounds__(kMaxThreads) build_mask_kernel(MaskArgs a) {
 
 // The kernel's dynamic shared-memory limit, raised on the current device only when a launch
 // needs more than it was last raised to (the attribute call costs host time on every launch).
+template <int T>
 bool mask_smem_ready(size_t smem) {
-  static std::atomic<size_t> raised[64];
+  static std::atomic<size_t> raised[64];             // one table per CTA size (T)
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
   std::atomic<size_t>* r = dev >= 0 && dev < 64 ? &raised[dev] : nullptr;
   if (r != nullptr && smem <= r->load()) return true;
-  if (cudaFuncSetAttribute(build_mask_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+  if (cudaFuncSetAttribute(build_mask_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
     return false;
   if (r != nullptr) {
     size_t cur = r->load();
@@ -503,21 +512,27 @@ int launch_build_mask(const sa_mask_params& p, const float* d_ratio, int32_t* d_
   a.row_ptr = d_row_ptr;
   a.col_idx = d_col_idx;
   const int words = (a.nb + 31) / 32;
-  // 256-thread CTAs (more, shorter CTAs: the per-sequence state is cheap to rebuild) while
-  // the scan's four entries per thread cover the sequence's blocks and, for TOPK, the rank
-  // pass (nb^2 / threads compares per thread) stays short; else 1024. Measured: 8K top-16
-  // (128 blocks) 10.9 -> 8.9 us, the three head-group masks 200 -> 52 us; 64K top-64 (512
-  // blocks) is faster with 1024 threads (19 against 23 us).
-  const int threads = (a.nb <= 4 * 256 && (a.mode != SA_MASK_TOPK || a.nb <= 256)) ? 256 : kMaxThreads;
+  // LITERAL_MEAN with up to 1024 blocks: 256-thread CTAs (more, shorter CTAs; the scan's four
+  // entries per thread cover the blocks). Measured on the three head-group masks of the 4 x 8K
+  // workload: 200 -> 52 us (28 us with the earlier sequences' counts in parallel). The other
+  // modes keep 1024 threads: the 8K top-16 mask took 12.4 us with 256 against 9.3 us with 1024
+  // (ncu), and BigBird 16K was the same either way. The CTA size is a template parameter, so
+  // every loop bound and stride in the kernel is a constant (with blockDim instead, the 8K
+  // top-16 mask took 11.7 us).
+  const int threads = (a.mode == SA_MASK_LITERAL_MEAN && a.nb <= 4 * 256) ? 256 : kMaxThreads;
   const int warps = threads / 32;
   size_t smem = (size_t)a.nb * 4 + (size_t)(a.nb + 1) * 4 + (size_t)a.nb * 4 + (size_t)warps * words * 4;
   if (a.mode == SA_MASK_LITERAL_MEAN && a.nb <= kPriorMaxBlocks) smem += (size_t)kPriorWarps * (a.nb + 1) * 4;
-  if (!mask_smem_ready(smem)) return SA_ERR_CUDA;
+  if (!(threads == 256 ? mask_smem_ready<256>(smem) : mask_smem_ready<kMaxThreads>(smem))) return SA_ERR_CUDA;
   // rows of a sequence split over up to nb / warps CTAs (one row per warp), enough CTAs in
   // all to cover the GPU twice; each CTA rebuilds the sequence's state, which is cheap
   const int sm_count = current_sm_count();
   const int groups = std::max(1, std::min((a.nb + warps - 1) / warps, (2 * sm_count + a.batch - 1) / a.batch));
-  build_mask_kernel<<<dim3((unsigned)a.batch, (unsigned)groups), threads, smem, stream>>>(a);
+  const dim3 grid((unsigned)a.batch, (unsigned)groups);
+  if (threads == 256)
+    build_mask_kernel<256><<<grid, 256, smem, stream>>>(a);
+  else
+    build_mask_kernel<kMaxThreads><<<grid, kMaxThreads, smem, stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
