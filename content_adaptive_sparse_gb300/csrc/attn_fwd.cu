@@ -39,7 +39,9 @@ namespace sa {
 namespace {
 
 constexpr int kSoftmaxWarps = 4;      // per pipeline: one per TMEM lane quarter
-constexpr int kTmaStoreTiles = 4;     // d = 64: items of at least this many key tiles store O by TMA
+// d = 64: items of at least this many key tiles store O by TMA (measured at 1, 2, 4 and 8:
+// 1-4 equal within noise, 8 slower on BigBird 16K; 1 = every item with key tiles)
+constexpr int kTmaStoreTiles = 1;
 // Of every 16 exponential pairs, these many on the FMA pipe (exp2_fma2). Measured on the 8K
 // top-16 workload at 0 / 1 / 2 / 3 / 4 pairs: 193-195 / 197-199 / 199-200 / 211 / 213-215 us:
 // in this kernel the exponentials are not held up by the MUFU pipe but by issue slots and
@@ -230,8 +232,8 @@ __device__ void softmax_epilogue(const Params& p, int x, PipeBars& bars, const B
       n_item = 0;
       slot = e.slot;
       // Items of at least kTmaStoreTiles key tiles (d = 64, whole items) stage their output in
-      // their Q buffer; the others give the buffer up now (its release then waits only for the
-      // item's QKs), so the loader can fetch the Q two items ahead early when items are short.
+      // their Q buffer; the others (items without key tiles, split parts, other d) give the
+      // buffer up now, and its release then waits only for the item's Q and QKs.
       // An item's first batch holds min(16, its key tiles) tiles, so this test and the one at
       // the item's end, on its tile count, agree.
       if (!(D == 64 && p.o_tma && slot < 0 && hdr.y >= kTmaStoreTiles)) {
