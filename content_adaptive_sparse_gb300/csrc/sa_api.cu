@@ -126,28 +126,89 @@ int check_attn_common(const void* q, const void* k, const void* v, const int64_t
 
 // ---------------------------------------------------------------- zlib (loaded at run time)
 
-typedef int (*compress2_fn)(unsigned char*, unsigned long*, const unsigned char*, unsigned long, int);
+// The public zlib stream record (zlib.h's z_stream, LP64 layout); declared here so that the
+// library builds where only the zlib run-time library is installed.
+struct ZStream {
+  const unsigned char* next_in;
+  unsigned int avail_in;
+  unsigned long total_in;
+  unsigned char* next_out;
+  unsigned int avail_out;
+  unsigned long total_out;
+  const char* msg;
+  void* state;
+  void* zalloc;
+  void* zfree;
+  void* opaque;
+  int data_type;
+  unsigned long adler;
+  unsigned long reserved;
+};
+
 typedef unsigned long (*compress_bound_fn)(unsigned long);
+typedef const char* (*zlib_version_fn)(void);
+typedef int (*deflate_init2_fn)(ZStream*, int, int, int, int, int, const char*, int);
+typedef int (*deflate_fn)(ZStream*, int);
+typedef int (*deflate_reset_fn)(ZStream*);
+typedef int (*deflate_end_fn)(ZStream*);
 
 struct Zlib {
-  compress2_fn compress2 = nullptr;
   compress_bound_fn bound = nullptr;
+  zlib_version_fn version = nullptr;
+  deflate_init2_fn init2 = nullptr;
+  deflate_fn deflate = nullptr;
+  deflate_reset_fn reset = nullptr;
+  deflate_end_fn end = nullptr;
+  bool ok() const { return bound && version && init2 && deflate && reset && end; }
 };
 
 const Zlib& zlib() {
-  static Zlib z;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
+  static const Zlib z = [] {
+    Zlib r;
     void* h = dlopen("libz.so.1", RTLD_NOW | RTLD_LOCAL);
     if (!h) h = dlopen("libz.so", RTLD_NOW | RTLD_LOCAL);
     if (h) {
-      z.compress2 = reinterpret_cast<compress2_fn>(dlsym(h, "compress2"));
-      z.bound = reinterpret_cast<compress_bound_fn>(dlsym(h, "compressBound"));
+      r.bound = reinterpret_cast<compress_bound_fn>(dlsym(h, "compressBound"));
+      r.version = reinterpret_cast<zlib_version_fn>(dlsym(h, "zlibVersion"));
+      r.init2 = reinterpret_cast<deflate_init2_fn>(dlsym(h, "deflateInit2_"));
+      r.deflate = reinterpret_cast<deflate_fn>(dlsym(h, "deflate"));
+      r.reset = reinterpret_cast<deflate_reset_fn>(dlsym(h, "deflateReset"));
+      r.end = reinterpret_cast<deflate_end_fn>(dlsym(h, "deflateEnd"));
     }
-  }
+    return r;
+  }();
   return z;
 }
+
+// One worker's deflate stream with the parameters of zlib's one-shot compress2 (method 8 =
+// deflate, 15 window bits, memory level 8, default strategy). deflateReset returns the stream to
+// the state a fresh init leaves, so each block's output is byte for byte compress2's; reusing
+// the stream saves the per-call allocation of its ~256 KB of tables.
+class Deflater {
+ public:
+  Deflater(const Zlib& z, int level) : z_(z) {
+    memset(&s_, 0, sizeof(s_));
+    ok_ = z_.init2(&s_, level, 8, 15, 8, 0, z_.version(), (int)sizeof(ZStream)) == 0;
+  }
+  ~Deflater() {
+    if (ok_) z_.end(&s_);
+  }
+  // Compressed length of src[0, n) (zlib framing), or -1 on error.
+  long length(const unsigned char* src, unsigned int n, unsigned char* buf, unsigned int cap) {
+    if (!ok_ || z_.reset(&s_) != 0) return -1;
+    s_.next_in = src;
+    s_.avail_in = n;
+    s_.next_out = buf;
+    s_.avail_out = cap;
+    if (z_.deflate(&s_, 4 /* finish */) != 1 /* stream end */) return -1;
+    return (long)(cap - s_.avail_out);
+  }
+
+ private:
+  const Zlib& z_;
+  ZStream s_;
+  bool ok_ = false;
+};
 
 }  // namespace
 
@@ -572,23 +633,24 @@ int sa_block_ratios(const uint8_t* h_bytes, int32_t batch, int32_t n_tokens, int
       level > 9 || n_threads < 0)
     return SA_ERR_INVALID_ARG;
   const Zlib& z = zlib();
-  if (!z.compress2 || !z.bound) return SA_ERR_UNSUPPORTED;
+  if (!z.ok()) return SA_ERR_UNSUPPORTED;
   const int64_t nb = n_tokens / block;
   const int64_t total = nb * batch;
   int threads = n_threads > 0 ? n_threads : (int)std::max(1u, std::thread::hardware_concurrency());
-  threads = (int)std::min<int64_t>(threads, std::max<int64_t>(1, total / 64));
+  threads = (int)std::min<int64_t>(threads, std::max<int64_t>(1, total / 16));
   std::atomic<int> failed{0};
   auto work = [&](int64_t begin, int64_t end) {
     std::vector<unsigned char> buf(z.bound((unsigned long)block));
+    Deflater dfl(z, level);
     for (int64_t idx = begin; idx < end; ++idx) {
       const int64_t s = idx / nb, i = idx % nb;
-      unsigned long out_len = (unsigned long)buf.size();
-      if (z.compress2(buf.data(), &out_len, h_bytes + s * (int64_t)n_tokens + i * block, (unsigned long)block, level) !=
-          0) {
+      const long len = dfl.length(h_bytes + s * (int64_t)n_tokens + i * block, (unsigned int)block, buf.data(),
+                                  (unsigned int)buf.size());
+      if (len < 0) {
         failed = 1;
         return;
       }
-      h_ratio[idx] = (float)((double)out_len / (double)block);
+      h_ratio[idx] = (float)((double)len / (double)block);
     }
   };
   if (threads <= 1) {

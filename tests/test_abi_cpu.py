@@ -53,6 +53,32 @@ def test_block_ratios_match_oracle(lib, name):
     assert r_lib.dtype == np.float32 and np.array_equal(r_lib, r_ora)
 
 
+@pytest.mark.parametrize("block", [32, 64, 128])
+def test_block_ratios_every_level_and_content(lib, block):
+    """Each worker reuses one deflate stream across its blocks: every level, and neighbouring
+    blocks of very different content (zeros, random bytes, short periods, text-like phrases),
+    must give the lengths of independent one-shot compressions."""
+    rng = np.random.default_rng(block)
+    n_blocks = 48
+    parts = []
+    for i in range(n_blocks):
+        kind = i % 4
+        if kind == 0:
+            parts.append(np.zeros(block, np.uint8))
+        elif kind == 1:
+            parts.append(rng.integers(0, 256, block, dtype=np.uint8))
+        elif kind == 2:
+            period = 1 + i % 7
+            parts.append(np.resize(rng.integers(0, 256, period, dtype=np.uint8), block))
+        else:
+            parts.append(bytes_phrase_random(i, block))
+    data = np.concatenate(parts).reshape(2, -1)
+    for level in range(10):
+        r_lib = sa.sa_block_ratios(data, block, level, n_threads=3)
+        r_ora = oracle.block_ratios(data, block, level)
+        assert np.array_equal(r_lib, r_ora), level
+
+
 def test_fib_offsets_match_oracle(lib):
     for lo, hi in (((1, 2), (2, 1)), ((1, 2), (3, 2))):
         for alpha in oracle.alpha_schedule(16, lo, hi):
