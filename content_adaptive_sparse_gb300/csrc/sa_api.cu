@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/sa_api.h: argument validation, the
 // closed-form CSR size bound, Fibonacci offsets, host zlib ratios and kernel dispatch.
 #include <dlfcn.h>
+#include <pthread.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -8,6 +9,10 @@
 #include <cmath>
 #include <numeric>
 #include <atomic>
+#include <condition_variable>
+#include <functional>
+#include <memory>
+#include <mutex>
 #include <thread>
 #include <vector>
 
@@ -209,6 +214,113 @@ class Deflater {
   ZStream s_;
   bool ok_ = false;
 };
+
+// Deflate stream of the calling thread for `level`, created on first use and kept for the
+// thread's lifetime (a stream zlib could not set up reports -1 for every block).
+Deflater* thread_deflater(const Zlib& z, int level) {
+  thread_local std::unique_ptr<Deflater> per_level[10];
+  std::unique_ptr<Deflater>& d = per_level[level];
+  if (!d) d.reset(new Deflater(z, level));
+  return d.get();
+}
+
+// Persistent host workers for the ratio pass. A call's blocks are handed out in chunks through
+// an atomic counter to the calling thread and up to (limit - 1) workers; workers sleep on a
+// condition variable between calls, so a call pays a wake-up instead of creating threads (and
+// their allocator state) each time. Calls are serialised by the pool.
+class HostPool {
+ public:
+  explicit HostPool(int n_workers) : workers_(n_workers) {
+    for (int i = 0; i < n_workers; ++i) std::thread([this] { worker(); }).detach();
+  }
+  int workers() const { return workers_; }
+
+  // Runs fn(begin, end) over [0, total) in chunks of `chunk` on the caller and up to
+  // limit - 1 workers; returns when every chunk is done and no worker still holds the job.
+  void run(int64_t total, int64_t chunk, int limit, const std::function<void(int64_t, int64_t)>& fn) {
+    std::lock_guard<std::mutex> call(call_mu_);
+    {
+      std::lock_guard<std::mutex> g(mu_);
+      fn_ = &fn;
+      total_ = total;
+      chunk_ = chunk;
+      next_.store(0);
+      seats_ = limit - 1;
+      open_ = true;
+      ++generation_;
+    }
+    cv_.notify_all();
+    drain();
+    std::unique_lock<std::mutex> g(mu_);
+    open_ = false;                               // no worker joins the job after this point
+    done_cv_.wait(g, [this] { return inside_ == 0; });
+    fn_ = nullptr;
+  }
+
+ private:
+  void drain() {
+    for (;;) {
+      const int64_t b = next_.fetch_add(chunk_);
+      if (b >= total_) return;
+      (*fn_)(b, std::min(total_, b + chunk_));
+    }
+  }
+  void worker() {
+    uint64_t seen = 0;
+    for (;;) {
+      {
+        std::unique_lock<std::mutex> g(mu_);
+        cv_.wait(g, [&] { return generation_ != seen; });
+        seen = generation_;
+        if (!open_ || seats_ <= 0) continue;
+        --seats_;
+        ++inside_;
+      }
+      drain();
+      {
+        std::lock_guard<std::mutex> g(mu_);
+        if (--inside_ == 0) done_cv_.notify_all();
+      }
+    }
+  }
+
+  const int workers_;
+  std::mutex call_mu_, mu_;
+  std::condition_variable cv_, done_cv_;
+  const std::function<void(int64_t, int64_t)>* fn_ = nullptr;
+  int64_t total_ = 0, chunk_ = 1;
+  std::atomic<int64_t> next_{0};
+  int seats_ = 0, inside_ = 0;
+  bool open_ = false;
+  uint64_t generation_ = 0;
+};
+
+// The process's pool (hardware concurrency - 1 workers), created on first use. A forked child
+// has none of the parent's workers: the fork handler drops the pointer (the parent's pool object
+// is left alone) and re-initialises the creation lock, so the child builds a pool of its own.
+pthread_mutex_t g_pool_mu = PTHREAD_MUTEX_INITIALIZER;
+HostPool* g_pool = nullptr;
+bool g_pool_hooked = false;
+
+void pool_after_fork_in_child() {
+  g_pool = nullptr;
+  pthread_mutex_init(&g_pool_mu, nullptr);
+}
+
+HostPool& host_pool() {
+  pthread_mutex_lock(&g_pool_mu);
+  if (g_pool == nullptr) {
+    if (!g_pool_hooked) {
+      pthread_atfork(nullptr, nullptr, pool_after_fork_in_child);
+      g_pool_hooked = true;
+    }
+    const int hw = (int)std::max(1u, std::thread::hardware_concurrency());
+    g_pool = new HostPool(std::min(hw, 256) - 1);
+  }
+  HostPool* p = g_pool;
+  pthread_mutex_unlock(&g_pool_mu);
+  return *p;
+}
 
 }  // namespace
 
@@ -636,16 +748,17 @@ int sa_block_ratios(const uint8_t* h_bytes, int32_t batch, int32_t n_tokens, int
   if (!z.ok()) return SA_ERR_UNSUPPORTED;
   const int64_t nb = n_tokens / block;
   const int64_t total = nb * batch;
-  int threads = n_threads > 0 ? n_threads : (int)std::max(1u, std::thread::hardware_concurrency());
-  threads = (int)std::min<int64_t>(threads, std::max<int64_t>(1, total / 16));
+  const int hw = (int)std::max(1u, std::thread::hardware_concurrency());
+  // at least 8 blocks per participating thread
+  const int threads = (int)std::min<int64_t>(n_threads > 0 ? n_threads : hw, std::max<int64_t>(1, total / 8));
   std::atomic<int> failed{0};
-  auto work = [&](int64_t begin, int64_t end) {
+  const std::function<void(int64_t, int64_t)> work = [&](int64_t begin, int64_t end) {
     std::vector<unsigned char> buf(z.bound((unsigned long)block));
-    Deflater dfl(z, level);
+    Deflater* dfl = thread_deflater(z, level);
     for (int64_t idx = begin; idx < end; ++idx) {
       const int64_t s = idx / nb, i = idx % nb;
-      const long len = dfl.length(h_bytes + s * (int64_t)n_tokens + i * block, (unsigned int)block, buf.data(),
-                                  (unsigned int)buf.size());
+      const long len = dfl->length(h_bytes + s * (int64_t)n_tokens + i * block, (unsigned int)block, buf.data(),
+                                   (unsigned int)buf.size());
       if (len < 0) {
         failed = 1;
         return;
@@ -656,13 +769,9 @@ int sa_block_ratios(const uint8_t* h_bytes, int32_t batch, int32_t n_tokens, int
   if (threads <= 1) {
     work(0, total);
   } else {
-    std::vector<std::thread> pool;
-    const int64_t per = (total + threads - 1) / threads;
-    for (int t = 0; t < threads; ++t) {
-      const int64_t b0 = t * per, b1 = std::min(total, b0 + per);
-      if (b0 < b1) pool.emplace_back(work, b0, b1);
-    }
-    for (auto& th : pool) th.join();
+    HostPool& pool = host_pool();
+    const int limit = std::min(threads, pool.workers() + 1);
+    pool.run(total, std::max<int64_t>(1, std::min<int64_t>(8, total / (4 * limit))), limit, work);
   }
   return failed ? SA_ERR_UNSUPPORTED : SA_OK;
 }

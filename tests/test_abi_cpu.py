@@ -79,6 +79,23 @@ def test_block_ratios_every_level_and_content(lib, block):
         assert np.array_equal(r_lib, r_ora), level
 
 
+def _ratios_in_child(data):
+    return sa.sa_block_ratios(data, 64, 6)
+
+
+@pytest.mark.filterwarnings("ignore:This process .* is multi-threaded:DeprecationWarning")
+def test_ratio_workers_after_fork(lib):
+    """The ratio pass keeps host worker threads between calls; a child forked after the parent
+    used them has none of them and must build its own (same ratios, no hang)."""
+    import multiprocessing
+    data = np.stack([bytes_phrase_random(s, 8192) for s in range(2)])
+    parent = sa.sa_block_ratios(data, 64, 6)          # the parent's workers exist from here on
+    with multiprocessing.get_context("fork").Pool(1) as pool:
+        child = pool.apply_async(_ratios_in_child, (data,)).get(timeout=120)
+    assert np.array_equal(parent, child)
+    assert np.array_equal(parent, oracle.block_ratios(data, 64, 6))
+
+
 def test_fib_offsets_match_oracle(lib):
     for lo, hi in (((1, 2), (2, 1)), ((1, 2), (3, 2))):
         for alpha in oracle.alpha_schedule(16, lo, hi):
