@@ -168,6 +168,25 @@ def _csr_edges(rp, ci, block, causal, heads) -> int:
     return total * heads
 
 
+def _csr_tile_elements(rp, ci, block, causal, heads) -> int:
+    """Score elements the forward kernel computes for a block CSR: each 128-token query tile
+    takes the union of its query blocks' rows (key blocks at or before a row's own block under
+    causality) and computes 128 rows x 32 keys per 32-key chunk of the union (b / 32 chunks per
+    block), masked or not."""
+    import numpy as np
+    nb = rp.shape[1] - 1
+    nq = max(1, 128 // block)
+    chunks = 0
+    for s in range(rp.shape[0]):
+        for t0 in range(0, nb, nq):
+            keys = []
+            for I in range(t0, min(nb, t0 + nq)):
+                row = ci[rp[s, I]:rp[s, I + 1]]
+                keys.append(row[row <= I] if causal else row)
+            chunks += len(np.unique(np.concatenate(keys))) * max(1, block // 32)
+    return chunks * 32 * 128 * heads
+
+
 class BlockSparseCase:
     """Ratios -> CSR -> attention for one compression-guided / BigBird workload."""
 
@@ -233,6 +252,9 @@ class BlockSparseCase:
         per_csr = sum(_csr_edges(rp.cpu().numpy(), ci.cpu().numpy(), b, self.causal, nh)
                       for (rp, ci), nh in zip(self.csrs, heads_of))
         self.edges = per_csr * (bt if self.csr_shared else 1)
+        # score elements the kernel computes (whole 32-key chunks of each query tile's union)
+        self.computed = sum(_csr_tile_elements(rp.cpu().numpy(), ci.cpu().numpy(), b, self.causal, nh)
+                            for (rp, ci), nh in zip(self.csrs, heads_of)) * (bt if self.csr_shared else 1)
         self.flops = 4 * self.edges * cfg["head_dim"]
         self.tokens = bt * n
 
@@ -748,6 +770,8 @@ def run_ours(args):
                      "kernel": "attn_fwd_kernel<64> (sa_attn_fwd)",
                      "peak_source": f"{peaks['source']} bf16 burst (kernel timed alone)",
                      "algorithmic_flops_per_launch": case.flops,
+                     "tile_fill": case.edges / case.computed,
+                     "computed_tflops": 4 * case.computed * cfg["head_dim"] / (attn_ms * 1e-3) / 1e12,
                      "frac_of_sustained": attn_tflops / peaks["bf16_tflops_sustained"]
                      if peaks.get("bf16_tflops_sustained") else None},
         "e2e": dict(e2e, host_ratio_ms_per_8k_sequence=ratio_ms),
@@ -897,6 +921,14 @@ def _measure_rows(torch, sa, dev, flush, peaks, max_over_ranks, only=None, steps
     return rows
 
 
+def _fill_fields(case, attn_ms: float) -> dict:
+    """Tile fill (mask edges / score elements the kernel computes) and the rate over the
+    computed elements: the part of a row's distance from peak that its 128 x 128 tiling takes."""
+    computed_tflops = 4 * case.computed * case.cfg["head_dim"] / (attn_ms * 1e-3) / 1e12
+    return {"tile_fill": case.edges / case.computed, "computed_elements": case.computed,
+            "computed_tflops": computed_tflops}
+
+
 def _row_bigbird(torch, dev, flush, peaks, max_over_ranks, steps, warm):
     rows = {}
     # BigBird 16K: CSR build + attention
@@ -906,7 +938,7 @@ def _row_bigbird(torch, dev, flush, peaks, max_over_ranks, steps, warm):
     rows["bigbird_16k"] = {"ms_per_step": max_over_ranks(tot), "attn_ms": a, "mask_ms": seg[0],
                            "effective_tflops": bb.flops / (a * 1e-3) / 1e12,
                            "frac_bf16_peak": bb.flops / (a * 1e-3) / 1e12 / peaks["bf16_tflops"],
-                           "tokens_per_s": bb.tokens / (tot * 1e-3), "edges": bb.edges}
+                           "tokens_per_s": bb.tokens / (tot * 1e-3), "edges": bb.edges, **_fill_fields(bb, a)}
     return rows
 
 
@@ -919,7 +951,7 @@ def _row_long(torch, dev, flush, peaks, max_over_ranks, steps, warm):
     rows["long_topk_64k"] = {"ms_per_step": max_over_ranks(tot), "attn_ms": a, "mask_ms": seg[0],
                              "effective_tflops": lc.flops / (a * 1e-3) / 1e12,
                              "frac_bf16_peak": lc.flops / (a * 1e-3) / 1e12 / peaks["bf16_tflops"],
-                             "tokens_per_s": lc.tokens / (tot * 1e-3), "edges": lc.edges}
+                             "tokens_per_s": lc.tokens / (tot * 1e-3), "edges": lc.edges, **_fill_fields(lc, a)}
     return rows
 
 
@@ -945,7 +977,8 @@ def _row_split(torch, dev, flush, peaks, max_over_ranks, steps, warm):
                         "effective_tflops": case.flops / (a * 1e-3) / 1e12,
                         "frac_bf16_peak": case.flops / (a * 1e-3) / 1e12 / peaks["bf16_tflops"],
                         "effective_tflops_without_split": case.flops / (b * 1e-3) / 1e12,
-                        "split_items": int(hdr[3]), "part_tiles": int(hdr[2]), "edges": case.edges}
+                        "split_items": int(hdr[3]), "part_tiles": int(hdr[2]), "edges": case.edges,
+                        **_fill_fields(case, a)}
         del case
         torch.cuda.empty_cache()
     return {"full_32k_one_head_split": out}
@@ -958,7 +991,7 @@ def _row_block_sparse(torch, dev, flush, peaks, max_over_ranks, steps, warm, nam
     return {name: {"ms_per_step": max_over_ranks(tot), "attn_ms": a, "mask_ms": seg[0],
                    "effective_tflops": case.flops / (a * 1e-3) / 1e12,
                    "frac_bf16_peak": case.flops / (a * 1e-3) / 1e12 / peaks["bf16_tflops"],
-                   "tokens_per_s": case.tokens / (tot * 1e-3), "edges": case.edges}}
+                   "tokens_per_s": case.tokens / (tot * 1e-3), "edges": case.edges, **_fill_fields(case, a)}}
 
 
 def _row_bwd(torch, dev, flush, peaks, max_over_ranks, steps, warm, name="bytelm_topk_8k"):
