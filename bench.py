@@ -806,7 +806,8 @@ def _measure_e2e(torch, sa, case, cfg, barrier, max_over_ranks, world) -> dict:
 
     nbk = cfg["n_tokens"] // cfg["block"]
     pinned = [t.pin_memory() for t in case.qkv_host]
-    ratio_threads = max(1, (os.cpu_count() or 2) // 2)
+    # half of the host's cores, shared among the ranks that run on this host
+    ratio_threads = max(1, (os.cpu_count() or 2) // (2 * int(os.environ.get("LOCAL_WORLD_SIZE", "1"))))
     ratios_pinned = [torch.empty((cfg["batch"], nbk), dtype=torch.float32).pin_memory() for _ in range(E2E_SETS)]
     o_host = [torch.empty(case.o.shape, dtype=torch.bfloat16).pin_memory() for _ in range(E2E_SETS)]
     lse_host = [torch.empty(case.lse.shape, dtype=torch.float32).pin_memory() for _ in range(E2E_SETS)]
