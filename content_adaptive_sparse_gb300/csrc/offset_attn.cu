@@ -13,16 +13,18 @@
 //     uses only key r: the diagonal of a 16 x 16 block. Computed with 8 mma.sync for QK
 //     and 8 for PV; the zero off-diagonal P entries cost tensor work, not memory traffic.
 //
-// Work item: one CTA of 4 warps per (sequence, head, 128-query tile); warp w owns queries
-// q0 + 32w .. q0 + 32w + 31 as two 16-query m-tiles and takes every key of them (band steps
-// and offsets), so no two warps merge softmax states. The band (K/V rows [q0 - 64, q0 + 128),
-// 48 KB) arrives by TMA once per CTA and is shared by the four warps. Once every warp is past
-// the band, its memory becomes four per-warp slab rings of two buffers: a warp streams the 32
-// K and V rows of each larger offset that its own queries use (8 KB) two offsets ahead, and
-// waits on nothing but its own copies (no cross-warp release of a buffer, no CTA barrier
-// between offsets). One slab, one wait and one refill serve two m-tiles, and the band's
-// over-fetch is 1.5x instead of 2x. At 65 KB of shared memory and <= 168 registers three CTAs
-// (12 warps, 384 queries in flight) share an SM.
+// Work item: one CTA of 4 warps per (sequence, head, query tile); warp w owns 16 * MT
+// consecutive queries as MT 16-query m-tiles (MT = 2 at head dimension 32 and 64, 1 at 128,
+// which keeps the O fragments at 64 registers) and takes every key of them (band steps and
+// offsets), so no two warps merge softmax states. The band (K/V rows [q0 - 64, q0 + 64 MT))
+// arrives by TMA once per CTA and is shared by the four warps. Once every warp is past the
+// band, its memory becomes four per-warp slab rings of two buffers: a warp streams the 16 * MT
+// K and V rows of each larger offset that its own queries use two offsets ahead, and waits on
+// nothing but its own copies (no cross-warp release of a buffer, no CTA barrier between
+// offsets). At head dimension 64: 128-query CTAs, 65 KB of shared memory, <= 168 registers,
+// three CTAs (12 warps, 384 queries in flight) per SM. K/V rows in shared memory follow the
+// layouts of mma_frag.cuh (head dimension 128: two 64-dimension column chunks per tile, each
+// loaded by its own TMA box).
 // Softmax: exact max over the band part, then the offsets with a lazily rescaled running
 // max (threshold 2^8).
 #include <cuda.h>
@@ -42,22 +44,31 @@ using namespace frag;
 
 __device__ unsigned int g_offset_err;
 
-constexpr int kMT = 2;                   // 16-query m-tiles per warp
-constexpr int kWarps = 4;
-constexpr int kQ = 16 * kMT * kWarps;    // queries per CTA (128)
-constexpr int kCtasPerSm = kMT == 1 ? 6 : 3;   // shared memory per CTA (33 / 65 KB), <= 170 registers
-constexpr int kRing = 2;                 // slab buffers per warp
-constexpr int kD = 64;                   // head dim supported by this kernel
-constexpr int kRowBytes = kD * 2;        // 128 B per K/V row
-constexpr int kBandMax = 64;             // deltas up to this go through the band
-constexpr int kBandRows = kQ + kBandMax; // band slab rows [q0 - 64, q0 + kQ)
-constexpr int kSlabRows = 16 * kMT;      // K (then V) rows of one warp's slab
-constexpr int kWarpSlabBytes = 2 * kSlabRows * kRowBytes;   // K and V rows of one warp's queries
-constexpr int kBandBytes = kBandRows * kRowBytes;
-constexpr int kRingBytes = kWarps * kRing * kWarpSlabBytes;
-constexpr int kSmemBytes = (2 * kBandBytes > kRingBytes ? 2 * kBandBytes : kRingBytes);
-static_assert(kBandRows <= 256 && kSlabRows <= 256, "TMA box rows");
-static_assert(kCtasPerSm * (1024 + kSmemBytes) <= 227 * 1024, "shared memory per SM");
+// Sizes at head dimension D (layouts as in mma_frag.cuh).
+template <int D>
+struct OffCfg {
+  static constexpr int MT = D == 128 ? 1 : 2;                // 16-query m-tiles per warp
+  static constexpr int WARPS = 4;
+  static constexpr int Q = 16 * MT * WARPS;                   // queries per CTA
+  static constexpr int BAND_MAX = 64;                         // deltas up to this go through the band
+  static constexpr int BAND_ROWS = Q + BAND_MAX;              // band rows [q0 - 64, q0 + Q)
+  static constexpr int SLAB_ROWS = 16 * MT;                   // K (then V) rows of one warp's slab
+  static constexpr int ROW_BYTES = 2 * D;
+  static constexpr int BOX_D = D < 64 ? D : 64;               // TMA box columns (one column chunk)
+  static constexpr int CHUNKS = D / BOX_D;
+  static constexpr int BAND_BYTES = BAND_ROWS * ROW_BYTES;    // one of K, V
+  static constexpr int SLAB_BYTES = SLAB_ROWS * ROW_BYTES;    // one of K, V
+  static constexpr int WARP_SLAB_BYTES = 2 * SLAB_BYTES;      // K rows, then V rows
+  static constexpr int RING = 2;                              // slab buffers per warp
+  static constexpr int RING_BYTES = WARPS * RING * WARP_SLAB_BYTES;
+  static constexpr int SMEM = 2 * BAND_BYTES > RING_BYTES ? 2 * BAND_BYTES : RING_BYTES;
+  static constexpr int CTAS_PER_SM = 3;
+  // column chunks (D = 128) must keep the 1024-byte alignment of the swizzled layout
+  static_assert(CHUNKS == 1 || ((BAND_ROWS * 128) % 1024 == 0 && (SLAB_ROWS * 128) % 1024 == 0), "chunk alignment");
+  static_assert(BAND_ROWS <= 256 && SLAB_ROWS <= 256, "TMA box rows");
+  static_assert(CTAS_PER_SM * (1024 + SMEM) <= 227 * 1024, "shared memory per SM");
+};
+constexpr int kBandMax = 64;
 constexpr int kMaxLarge = kMaxOffsets;
 
 struct OffParams {
@@ -75,18 +86,34 @@ struct OffParams {
   float scale_log2;
 };
 
-template <int NKT>
-__global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
+// One CTA's TMA loads of `rows` K or V rows starting at token `row0` into dst (column chunks
+// of a head dimension 128 tile cstride bytes apart); completion on bar.
+template <int D>
+__device__ __forceinline__ void load_rows(uint8_t* dst, uint32_t cstride, const CUtensorMap* map, uint64_t* bar,
+                                          int hk, int row0, int s) {
+  using C = OffCfg<D>;
+#pragma unroll
+  for (int c = 0; c < C::CHUNKS; ++c) tma_load_4d(dst + c * cstride, map, bar, c * C::BOX_D, hk, row0, s);
+}
+
+template <int D, int NKT>
+__global__ void __launch_bounds__(128, 3)
     offset_attn_kernel(const __grid_constant__ CUtensorMap tk_band, const __grid_constant__ CUtensorMap tv_band,
                        const __grid_constant__ CUtensorMap tk_slab, const __grid_constant__ CUtensorMap tv_slab,
                        const __grid_constant__ OffParams p) {
+  using C = OffCfg<D>;
+  using F = Frag<D>;
+  constexpr int kMT = C::MT;
+  constexpr int kRing = C::RING;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sKb = sm;                        // band K
-  uint8_t* sVb = sKb + kBandBytes;          // band V
+  uint8_t* sVb = sKb + C::BAND_BYTES;       // band V
+  constexpr uint32_t kBandCstride = C::BAND_ROWS * 128;   // head dimension 128: second column chunk
+  constexpr uint32_t kSlabCstride = C::SLAB_ROWS * 128;
   // once every warp is past the band, warp w's slab ring occupies its own kRing slabs of the
-  // same memory: buffer b at + b * kWarpSlabBytes, K rows first, then V rows
-  __shared__ uint64_t bar_band, bar_slab[kWarps][kRing];
+  // same memory: buffer b at + b * WARP_SLAB_BYTES, K rows first, then V rows
+  __shared__ uint64_t bar_band, bar_slab[C::WARPS][kRing];
   __shared__ int abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -94,27 +121,27 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
   const int h = blockIdx.x % p.heads;
   const int s = blockIdx.x / p.heads;
   const int tile = p.ntiles - 1 - (int)blockIdx.y;   // later tiles reach more offsets: start them first
-  const int q0 = tile * kQ;
+  const int q0 = tile * C::Q;
   const int hk = h / p.heads_per_kv;
   // larger offsets that reach at least one query of this warp
-  const int qw = q0 + kSlabRows * wq;        // first query of this warp (m-tile m: qw + 16 m)
+  const int qw = q0 + C::SLAB_ROWS * wq;     // first query of this warp (m-tile m: qw + 16 m)
   int n_off = 0;
-  while (n_off < p.n_large && p.large[n_off] <= qw + kSlabRows - 1) ++n_off;
+  while (n_off < p.n_large && p.large[n_off] <= qw + C::SLAB_ROWS - 1) ++n_off;
 
   if (tid == 0) {
     mbar_init(&bar_band, 1);
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w)
+    for (int w = 0; w < C::WARPS; ++w)
 #pragma unroll
       for (int b = 0; b < kRing; ++b) mbar_init(&bar_slab[w][b], 1);
     abort_flag = 0;
     fence_mbar_init();
-    mbar_arrive_expect_tx(&bar_band, (uint32_t)(2 * kBandBytes));
+    mbar_arrive_expect_tx(&bar_band, (uint32_t)(2 * C::BAND_BYTES));
   }
   __syncthreads();
   if (lane == 0) {
-    if (warp == 0) tma_load_4d(sKb, &tk_band, &bar_band, 0, hk, q0 - kBandMax, s);
-    if (warp == 1) tma_load_4d(sVb, &tv_band, &bar_band, 0, hk, q0 - kBandMax, s);
+    if (warp == 0) load_rows<D>(sKb, kBandCstride, &tk_band, &bar_band, hk, q0 - kBandMax, s);
+    if (warp == 1) load_rows<D>(sVb, kBandCstride, &tv_band, &bar_band, hk, q0 - kBandMax, s);
   }
 
   const int g = lane >> 2, t = lane & 3;     // mma fragment coordinates: rows g, g+8; cols 2t, 2t+1
@@ -122,35 +149,24 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
   const float kNegInf = __int_as_float(0xff800000);
 
   // Q operands straight from global memory (rows past the end read the last row; never stored)
-  uint32_t qa[kMT][4][4];
+  uint32_t qa[kMT][F::KS][4];
 #pragma unroll
   for (int m = 0; m < kMT; ++m) {
     const int qm = qw + 16 * m;
     const int last = p.n_tokens - 1;
     const int i_lo = qm + g < last ? qm + g : last, i_hi = qm + g + 8 < last ? qm + g + 8 : last;
-    const __nv_bfloat16* base = p.q + (int64_t)s * p.q_sb + (int64_t)h * p.q_sh + 16 * t;
-    const uint4* lo = reinterpret_cast<const uint4*>(base + (int64_t)i_lo * p.q_sn);
-    const uint4* hi = reinterpret_cast<const uint4*>(base + (int64_t)i_hi * p.q_sn);
-    const uint4 a = __ldg(lo), b = __ldg(lo + 1), x = __ldg(hi), y = __ldg(hi + 1);
-    const uint32_t wl[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    const uint32_t wh[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      qa[m][ks][0] = wl[2 * ks];
-      qa[m][ks][1] = wh[2 * ks];
-      qa[m][ks][2] = wl[2 * ks + 1];
-      qa[m][ks][3] = wh[2 * ks + 1];
-    }
+    const __nv_bfloat16* base = p.q + (int64_t)s * p.q_sb + (int64_t)h * p.q_sh;
+    load_qfrag<D>(base + (int64_t)i_lo * p.q_sn, base + (int64_t)i_hi * p.q_sn, t, qa[m]);
   }
 
   // warp-uniform wait results: the fragment code below uses full-warp shuffles
   bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_band, 0, &abort_flag, &g_offset_err, kErrTimeout));
 
-  float o[kMT][8][4];                        // O fragments per m-tile: d n-tiles 0..7
+  float o[kMT][F::NT][4];                    // O fragments per m-tile: D / 8 n-tiles
 #pragma unroll
   for (int m = 0; m < kMT; ++m)
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) o[m][nt][0] = o[m][nt][1] = o[m][nt][2] = o[m][nt][3] = 0.f;
+    for (int nt = 0; nt < F::NT; ++nt) o[m][nt][0] = o[m][nt][1] = o[m][nt][2] = o[m][nt][3] = 0.f;
   // running max of rows g, g+8 of each m-tile (log2 units) and the row sums
   float m_lo[kMT], m_hi[kMT], l_lo[kMT], l_hi[kMT];
 #pragma unroll
@@ -160,7 +176,7 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
   }
 
   if (ok) {
-    const uint32_t kb_tile = smem_u32(sKb), vb_tile = smem_u32(sVb);
+    const KV kb_tile{smem_u32(sKb), kBandCstride}, vb_tile{smem_u32(sVb), kBandCstride};
 #pragma unroll
     for (int m = 0; m < kMT; ++m) {
       // ---------------- band: keys [qm - Dr, qm + 16), band slab row = key - (q0 - 64)
@@ -179,10 +195,10 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
       float mx_lo = kNegInf, mx_hi = kNegInf;
 #pragma unroll
       for (int nt = 0; nt < 2 * NKT; ++nt) {
-        uint32_t u[8];
-        load_kfrag(kb_tile, row0 + 8 * nt + g, t, u);
+        uint32_t u[2 * F::KS];
+        load_kfrag<D>(kb_tile, row0 + 8 * nt + g, t, u);
         sb[nt][0] = sb[nt][1] = sb[nt][2] = sb[nt][3] = 0.f;
-        qk_ntile(sb[nt], qa[m], u);
+        qk_ntile<D>(sb[nt], qa[m], u);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float v = (keep >> (4 * nt + e)) & 1ull ? sb[nt][e] : kNegInf;
@@ -210,9 +226,9 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
         pa[3] = pack_bf16x2(ex2_approx(fmaf(sb[2 * j + 1][2], c, -m_hi[m])),
                             ex2_approx(fmaf(sb[2 * j + 1][3], c, -m_hi[m])));
         mma16816(lsum, pa, kOnesBf16x2, kOnesBf16x2);
-        uint32_t vb[4][4];
-        load_v16(vb_tile, row0 + 16 * j, lane, vb);
-        pv_16(o[m], pa, vb);
+        uint32_t vb[D / 16][4];
+        load_v16<D>(vb_tile, row0 + 16 * j, lane, vb);
+        pv_16<D>(o[m], pa, vb);
       }
       l_lo[m] = lsum[0];
       l_hi[m] = lsum[2];
@@ -220,17 +236,17 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
   }
 
   // The band is read: its memory becomes the warps' slab rings. Each warp streams the
-  // kSlabRows key and value rows of each larger offset that its own queries use, two slabs
+  // SLAB_ROWS key and value rows of each larger offset that its own queries use, two slabs
   // ahead, and waits on nothing but its own copies.
   __syncthreads();
-  uint8_t* ring = sm + wq * (kRing * kWarpSlabBytes);
+  uint8_t* ring = sm + wq * (kRing * C::WARP_SLAB_BYTES);
   int issued = 0;
   if (lane == 0 && !abort_flag) {
     for (; issued < kRing && issued < n_off; ++issued) {
-      uint8_t* dst = ring + issued * kWarpSlabBytes;
-      mbar_arrive_expect_tx(&bar_slab[wq][issued], (uint32_t)kWarpSlabBytes);
-      tma_load_4d(dst, &tk_slab, &bar_slab[wq][issued], 0, hk, qw - p.large[issued], s);
-      tma_load_4d(dst + kWarpSlabBytes / 2, &tv_slab, &bar_slab[wq][issued], 0, hk, qw - p.large[issued], s);
+      uint8_t* dst = ring + issued * C::WARP_SLAB_BYTES;
+      mbar_arrive_expect_tx(&bar_slab[wq][issued], (uint32_t)C::WARP_SLAB_BYTES);
+      load_rows<D>(dst, kSlabCstride, &tk_slab, &bar_slab[wq][issued], hk, qw - p.large[issued], s);
+      load_rows<D>(dst + C::SLAB_BYTES, kSlabCstride, &tv_slab, &bar_slab[wq][issued], hk, qw - p.large[issued], s);
     }
   }
   ok = ok && !abort_flag;
@@ -244,13 +260,14 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
     ok = __all_sync(0xffffffffu, mbar_wait(&bar_slab[wq][b], (uint32_t)(k / kRing) & 1u, &abort_flag,
                                            &g_offset_err, kErrTimeout));
     if (!ok) break;
-    const uint32_t kt = smem_u32(ring + b * kWarpSlabBytes);
+    const KV kt{smem_u32(ring + b * C::WARP_SLAB_BYTES), kSlabCstride};
+    const KV vt{kt.base + C::SLAB_BYTES, kSlabCstride};
     const int delta = p.large[k];
 #pragma unroll
     for (int m = 0; m < kMT; ++m) {
       const int qm = qw + 16 * m;
       float s_lo, s_hi;
-      diag_scores(kt, 16 * m, g, t, hl, e_sel, qa[m], s_lo, s_hi);
+      diag_scores<D>(kt, 16 * m, g, t, hl, e_sel, qa[m], s_lo, s_hi);
       if (qm + g - delta < 0) s_lo = kNegInf;
       if (qm + g + 8 - delta < 0) s_hi = kNegInf;
       // lazy running max (log2 units): rescale only when a score passes the max by 2^8
@@ -260,7 +277,7 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
       if (x_hi > m_hi[m] + 8.f) { a_hi = ex2_approx(m_hi[m] - x_hi); m_hi[m] = x_hi; }
       if (__any_sync(0xffffffffu, a_lo != 1.f || a_hi != 1.f)) {
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
+        for (int nt = 0; nt < F::NT; ++nt) {
           o[m][nt][0] *= a_lo;
           o[m][nt][1] *= a_lo;
           o[m][nt][2] *= a_hi;
@@ -272,15 +289,15 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
       const uint32_t pb = pack_bf16x2(ex2_approx(fmaf(s_lo, c, -m_lo[m])), ex2_approx(fmaf(s_hi, c, -m_hi[m])));
       l_lo[m] += __uint_as_float(pb << 16);
       l_hi[m] += __uint_as_float(pb & 0xffff0000u);
-      diag_pv(kt + kWarpSlabBytes / 2, 16 * m, lane, holder, e_sel, pb, o[m]);
+      diag_pv<D>(vt, 16 * m, lane, holder, e_sel, pb, o[m]);
     }
     // every lane has read the buffer: refill it with the slab kRing ahead
     __syncwarp();
     if (lane == 0 && issued < n_off && !abort_flag) {
-      uint8_t* dst = ring + b * kWarpSlabBytes;
-      mbar_arrive_expect_tx(&bar_slab[wq][b], (uint32_t)kWarpSlabBytes);
-      tma_load_4d(dst, &tk_slab, &bar_slab[wq][b], 0, hk, qw - p.large[issued], s);
-      tma_load_4d(dst + kWarpSlabBytes / 2, &tv_slab, &bar_slab[wq][b], 0, hk, qw - p.large[issued], s);
+      uint8_t* dst = ring + b * C::WARP_SLAB_BYTES;
+      mbar_arrive_expect_tx(&bar_slab[wq][b], (uint32_t)C::WARP_SLAB_BYTES);
+      load_rows<D>(dst, kSlabCstride, &tk_slab, &bar_slab[wq][b], hk, qw - p.large[issued], s);
+      load_rows<D>(dst + C::SLAB_BYTES, kSlabCstride, &tv_slab, &bar_slab[wq][b], hk, qw - p.large[issued], s);
       ++issued;
     }
   }
@@ -294,7 +311,7 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
       __nv_bfloat16* orow_lo = p.o + (int64_t)s * p.o_sb + (int64_t)i_lo * p.o_sn + (int64_t)h * p.o_sh;
       __nv_bfloat16* orow_hi = p.o + (int64_t)s * p.o_sb + (int64_t)i_hi * p.o_sn + (int64_t)h * p.o_sh;
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
+      for (int nt = 0; nt < F::NT; ++nt) {
         const int col = 8 * nt + 2 * t;
         if (i_lo < p.n_tokens)
           *reinterpret_cast<uint32_t*>(orow_lo + col) = pack_bf16x2(o[m][nt][0] * inv_lo, o[m][nt][1] * inv_lo);
@@ -319,37 +336,52 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
   }
 }
 
-template <int NKT>
+template <int D, int NKT>
 int launch_nkt(const CUtensorMap& kb, const CUtensorMap& vb, const CUtensorMap& ks, const CUtensorMap& vs,
                const OffParams& p, int batch, cudaStream_t stream) {
-  const size_t smem = 1024 + (size_t)kSmemBytes;
-  if (cudaFuncSetAttribute(offset_attn_kernel<NKT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+  using C = OffCfg<D>;
+  const size_t smem = 1024 + (size_t)C::SMEM;
+  if (cudaFuncSetAttribute(offset_attn_kernel<D, NKT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return SA_ERR_CUDA;
   dim3 grid((unsigned)(batch * p.heads), (unsigned)p.ntiles);
-  offset_attn_kernel<NKT><<<grid, kWarps * 32, smem, stream>>>(kb, vb, ks, vs, p);
+  offset_attn_kernel<D, NKT><<<grid, C::WARPS * 32, smem, stream>>>(kb, vb, ks, vs, p);
   return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+}
+
+template <int D>
+int launch_d(const OffsetArgs& a, OffParams& p, cudaStream_t stream) {
+  using C = OffCfg<D>;
+  const CUtensorMapSwizzle swz = D == 32 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
+  CUtensorMap kb, vb, ks, vs;
+  if (!encode_bhnd_map(&kb, a.k, a.batch, a.n_tokens, a.kv_heads, D, a.kv_strides[0], a.kv_strides[1],
+                       a.kv_strides[2], C::BOX_D, C::BAND_ROWS, swz) ||
+      !encode_bhnd_map(&vb, a.v, a.batch, a.n_tokens, a.kv_heads, D, a.kv_strides[0], a.kv_strides[1],
+                       a.kv_strides[2], C::BOX_D, C::BAND_ROWS, swz) ||
+      !encode_bhnd_map(&ks, a.k, a.batch, a.n_tokens, a.kv_heads, D, a.kv_strides[0], a.kv_strides[1],
+                       a.kv_strides[2], C::BOX_D, C::SLAB_ROWS, swz) ||
+      !encode_bhnd_map(&vs, a.v, a.batch, a.n_tokens, a.kv_heads, D, a.kv_strides[0], a.kv_strides[1],
+                       a.kv_strides[2], C::BOX_D, C::SLAB_ROWS, swz))
+    return SA_ERR_UNSUPPORTED;
+  p.ntiles = (a.n_tokens + C::Q - 1) / C::Q;
+  if (p.ntiles > 65535) return SA_ERR_UNSUPPORTED;
+  switch ((16 + p.dr) / 16) {
+    case 1: return launch_nkt<D, 1>(kb, vb, ks, vs, p, a.batch, stream);
+    case 2: return launch_nkt<D, 2>(kb, vb, ks, vs, p, a.batch, stream);
+    case 3: return launch_nkt<D, 3>(kb, vb, ks, vs, p, a.batch, stream);
+    case 4: return launch_nkt<D, 4>(kb, vb, ks, vs, p, a.batch, stream);
+    default: return launch_nkt<D, 5>(kb, vb, ks, vs, p, a.batch, stream);
+  }
 }
 
 }  // namespace
 
 int launch_offset_attn_fwd(const OffsetArgs& a, cudaStream_t stream) {
-  if (a.head_dim != kD) return SA_ERR_UNSUPPORTED;
-  CUtensorMap kb, vb, ks, vs;
-  if (!encode_bhnd_map(&kb, a.k, a.batch, a.n_tokens, a.kv_heads, kD, a.kv_strides[0], a.kv_strides[1],
-                       a.kv_strides[2], kD, kBandRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_bhnd_map(&vb, a.v, a.batch, a.n_tokens, a.kv_heads, kD, a.kv_strides[0], a.kv_strides[1],
-                       a.kv_strides[2], kD, kBandRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_bhnd_map(&ks, a.k, a.batch, a.n_tokens, a.kv_heads, kD, a.kv_strides[0], a.kv_strides[1],
-                       a.kv_strides[2], kD, kSlabRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_bhnd_map(&vs, a.v, a.batch, a.n_tokens, a.kv_heads, kD, a.kv_strides[0], a.kv_strides[1],
-                       a.kv_strides[2], kD, kSlabRows, CU_TENSOR_MAP_SWIZZLE_128B))
-    return SA_ERR_UNSUPPORTED;
+  if (a.head_dim != 32 && a.head_dim != 64 && a.head_dim != 128) return SA_ERR_UNSUPPORTED;
   OffParams p;
   p.n_tokens = a.n_tokens;
   p.heads = a.heads;
   p.heads_per_kv = a.heads / a.kv_heads;
-  p.ntiles = (a.n_tokens + kQ - 1) / kQ;
   // band: the window and every offset <= 64; distances 0..95 as a bit set
   uint32_t dist_mask[3] = {0u, 0u, 0u};
   int dmax = a.window;
@@ -390,12 +422,10 @@ int launch_offset_attn_fwd(const OffsetArgs& a, cudaStream_t stream) {
   p.o_sn = a.o_strides[1];
   p.o_sh = a.o_strides[2];
   p.scale_log2 = a.softmax_scale * 1.4426950408889634f;
-  switch (nkt) {
-    case 1: return launch_nkt<1>(kb, vb, ks, vs, p, a.batch, stream);
-    case 2: return launch_nkt<2>(kb, vb, ks, vs, p, a.batch, stream);
-    case 3: return launch_nkt<3>(kb, vb, ks, vs, p, a.batch, stream);
-    case 4: return launch_nkt<4>(kb, vb, ks, vs, p, a.batch, stream);
-    default: return launch_nkt<5>(kb, vb, ks, vs, p, a.batch, stream);
+  switch (a.head_dim) {
+    case 32: return launch_d<32>(a, p, stream);
+    case 64: return launch_d<64>(a, p, stream);
+    default: return launch_d<128>(a, p, stream);
   }
 }
 

@@ -564,13 +564,13 @@ int sa_offset_attn_fwd_list(const void* q, const void* k, const void* v, const i
   if (!(softmax_scale > 0.f)) return SA_ERR_INVALID_ARG;
   if (window < 0) return SA_ERR_INVALID_ARG;
   if (window > sa::kMaxWindow || n_offsets > sa::kMaxOffsets) return SA_ERR_UNSUPPORTED;
-  if (head_dim != 64) return SA_ERR_UNSUPPORTED;
+  if (head_dim != 32 && head_dim != 64 && head_dim != 128) return SA_ERR_UNSUPPORTED;
   for (int i = 0; i < n_offsets; ++i) {
     if (h_offsets[i] <= window || h_offsets[i] >= n_tokens) return SA_ERR_INVALID_ARG;
     if (i > 0 && h_offsets[i] <= h_offsets[i - 1]) return SA_ERR_INVALID_ARG;
   }
-  // grid: (batch x heads, 128-query tiles)
-  if ((int64_t)batch * heads > 0x7fffffff || (n_tokens + 127) / 128 > 65535) return SA_ERR_UNSUPPORTED;
+  // grid: (batch x heads, query tiles of 128, or 64 at head dimension 128)
+  if ((int64_t)batch * heads > 0x7fffffff || (n_tokens + 63) / 64 > 65535) return SA_ERR_UNSUPPORTED;
   if (!device_ok()) return SA_ERR_CUDA;
   sa::OffsetArgs a;
   a.q = q;
@@ -658,7 +658,8 @@ int sa_offset_attn_interp_fwd(const void* q, const void* k, const void* v, const
   if (st != SA_OK) return st;
   if (!(softmax_scale > 0.f) || !(alpha > 0.0) || !std::isfinite(alpha)) return SA_ERR_INVALID_ARG;
   if (window < 0 || n_rungs < 0 || (ladder != 0 && ladder != 1)) return SA_ERR_INVALID_ARG;
-  if (window > sa::kMaxWindow || head_dim != 64) return SA_ERR_UNSUPPORTED;
+  if (window > sa::kMaxWindow) return SA_ERR_UNSUPPORTED;
+  if (head_dim != 32 && head_dim != 64 && head_dim != 128) return SA_ERR_UNSUPPORTED;
   sa::InterpArgs a;
   a.n_rungs = 0;
   int64_t f = 1, g = 2;   // rung ladder
@@ -702,6 +703,7 @@ int sa_offset_attn_interp_fwd(const void* q, const void* k, const void* v, const
   a.n_tokens = n_tokens;
   a.heads = heads;
   a.kv_heads = kv_heads;
+  a.head_dim = head_dim;
   a.window = window;
   a.softmax_scale = softmax_scale;
   return sa::launch_offset_interp_fwd(a, static_cast<cudaStream_t>(stream));

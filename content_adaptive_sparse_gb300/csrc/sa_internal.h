@@ -87,7 +87,7 @@ struct InterpArgs {
   int64_t q_strides[3];
   int64_t kv_strides[3];
   int64_t o_strides[3];
-  int32_t batch, n_tokens, heads, kv_heads, window, n_rungs;
+  int32_t batch, n_tokens, heads, kv_heads, head_dim, window, n_rungs;
   int32_t lo[kMaxInterpRungs];   // floor of the rung distance
   float t[kMaxInterpRungs];      // weight of the farther row
   float softmax_scale;

@@ -245,8 +245,8 @@ int sa_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void*
  * alpha = alpha_num / alpha_den > 0 is the layer's scale as an exact fraction (the page's
  * per-layer linear stagger, see sa_layer_alpha). D is computed on the host exactly as
  * sa_fib_offsets returns it.
- *   head_dim == 64 (the page's model: 8 heads of 64); window in [0, 64]; at most 64
- *   distinct offsets beyond the window; n_tokens <= 65535 * 128 and batch * heads < 2^31
+ *   head_dim 32, 64 or 128 (the page's model: 8 heads of 64); window in [0, 64]; at most 64
+ *   distinct offsets beyond the window; n_tokens <= 65535 * 64 and batch * heads < 2^31
  *   (else SA_ERR_UNSUPPORTED); other arguments as in sa_attn_fwd. The kernel's copy waits
  *   are bounded: an expired wait leaves O and LSE incomplete and is reported by
  *   sa_device_status as SA_ERR_TIMEOUT. */
@@ -275,7 +275,7 @@ int sa_offset_attn_fwd_list(const void* q, const void* k, const void* v, const i
  *   for every rung with i - d_k >= 0 the key (1 - t) k[i - lo] + t k[i - lo - 1] and the
  *   value (1 - t) v[i - lo] + t v[i - lo - 1]
  * (a rung with an integer distance inside the window is the window row itself and is not
- * counted twice). head_dim == 64; window in [0, 64]; at most 64 rungs remain;
+ * counted twice). head_dim 32, 64 or 128; window in [0, 64]; at most 64 rungs remain;
  * n_tokens <= 65535 * 64; other arguments, size limits and the bounded-wait report as in
  * sa_offset_attn_fwd. alpha must be finite and > 0. */
 int sa_offset_attn_interp_fwd(const void* q, const void* k, const void* v, const int64_t q_strides[3],

@@ -200,20 +200,20 @@ def test_argument_validation_before_any_launch(lib):
     rp9 = P9(*([256] * 9))
     assert lib.sa_attn_fwd_heads(p16, p16, p16, s, s, s, 1, 8192, 12, 12, 64, 64, 1, 9, rp9, rp9, hm, 0,
                                  ctypes.c_float(0.125), p16, p16, p16, 4096, None) == -2
-    # interpolated gather: alpha must be positive, head_dim 64 only
+    # interpolated gather: alpha must be positive, head_dim 32, 64 or 128
     assert lib.sa_offset_attn_interp_fwd(p16, p16, p16, s, s, s, 1, 8192, 8, 8, 64, 8, ctypes.c_double(-0.5), 15, 0,
                                          ctypes.c_float(0.125), p16, p16, None) == -1
-    assert lib.sa_offset_attn_interp_fwd(p16, p16, p16, s, s, s, 1, 8192, 8, 8, 32, 8, ctypes.c_double(0.8), 15, 0,
+    assert lib.sa_offset_attn_interp_fwd(p16, p16, p16, s, s, s, 1, 8192, 8, 8, 96, 8, ctypes.c_double(0.8), 15, 0,
                                          ctypes.c_float(0.125), p16, p16, None) == -2
     offs = (ctypes.c_int32 * 2)(5, 9)        # offset inside the window -> invalid
     assert lib.sa_offset_attn_fwd_list(p16, p16, p16, s, s, s, 1, 8192, 8, 8, 64, 8, offs, 2,
                                        ctypes.c_float(0.125), p16, p16, None) == -1
-    # the page's parameters: alpha must be a positive fraction; d != 64 is not supported
+    # the page's parameters: alpha must be a positive fraction; head_dim 32, 64 or 128
     assert lib.sa_offset_attn_fwd(p16, p16, p16, s, s, s, 1, 8192, 8, 8, 64, 8, 1, 0, 15,
                                   ctypes.c_float(0.125), p16, p16, None) == -1
     assert lib.sa_offset_attn_fwd(p16, p16, p16, s, s, s, 1, 8192, 8, 8, 64, 8, -3, 2, 15,
                                   ctypes.c_float(0.125), p16, p16, None) == -1
-    assert lib.sa_offset_attn_fwd(p16, p16, p16, s, s, s, 1, 8192, 8, 8, 32, 8, 1, 1, 15,
+    assert lib.sa_offset_attn_fwd(p16, p16, p16, s, s, s, 1, 8192, 8, 8, 96, 8, 1, 1, 15,
                                   ctypes.c_float(0.125), p16, p16, None) == -2
 
 

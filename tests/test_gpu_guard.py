@@ -155,13 +155,14 @@ def test_guard_keyless_query_tile(d):
     _case(2, 256, 4, 2, d, 32, rows=rows, causal=1, seed=11 + d)
 
 
+@pytest.mark.parametrize("d", [32, 64, 128])
 @pytest.mark.parametrize("interp", [False, True])
-def test_guard_offset_kernels(interp):
-    """The window-plus-offset kernels (integer and interpolated): O and LSE guarded, a
-    length that is not a multiple of the 64-query tile."""
+def test_guard_offset_kernels(interp, d):
+    """The window-plus-offset kernels (integer and interpolated) at every head dimension: O
+    and LSE guarded, a length that is not a multiple of the 64- or 128-query tile."""
     torch = torch_cuda()
-    rng = np.random.default_rng(5)
-    bt, n, h, hkv, d, W = 2, 1000, 2, 1, 64, 8
+    rng = np.random.default_rng(5 + d)
+    bt, n, h, hkv, W = 2, 1000, 2, 1, 8
     qb = bf16_normal_bits(rng, (bt, n, h, d), 0.4)
     kb = bf16_normal_bits(rng, (bt, n, hkv, d), 0.4)
     vb = bf16_normal_bits(rng, (bt, n, hkv, d), 0.4)
@@ -183,4 +184,5 @@ def test_guard_offset_kernels(interp):
     assert sa.sa_device_status() == 0
     assert obuf.margins_intact() and _poisoned_slots_intact(obuf, {0}), "O written outside its view"
     assert lbuf.margins_intact(), "LSE written outside its buffer"
-    assert_attention_close(bf16_to_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref, "guarded offsets")
+    assert_attention_close(bf16_to_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref,
+                           f"guarded offsets d={d}")

@@ -12,12 +12,12 @@ from gpu_helpers import LSE_MAX_ABS, O_MAX_ABS, assert_attention_close, bf16_to_
 pytestmark = pytest.mark.gpu
 
 
-def _run(bt, n, h, hkv, window, alpha: Fraction, n_rungs=15, seed=0, qmul=1.0, ladder="fib"):
+def _run(bt, n, h, hkv, window, alpha: Fraction, n_rungs=15, seed=0, qmul=1.0, ladder="fib", d=64):
     torch = torch_cuda()
     rng = np.random.default_rng(seed)
-    qb = bf16_normal_bits(rng, (bt, n, h, 64), 0.125 * qmul)
-    kb = bf16_normal_bits(rng, (bt, n, hkv, 64), 0.125)
-    vb = bf16_normal_bits(rng, (bt, n, hkv, 64), 0.125)
+    qb = bf16_normal_bits(rng, (bt, n, h, d), 0.125 * qmul)
+    kb = bf16_normal_bits(rng, (bt, n, hkv, d), 0.125)
+    vb = bf16_normal_bits(rng, (bt, n, hkv, d), 0.125)
     if ladder == "fib":
         offs = sa.sa_fib_offsets(alpha.numerator, alpha.denominator, n_rungs, window, n)
         rungs = oracle.fib_rungs(n_rungs) if n_rungs else oracle.fib_rungs_upto(n)
@@ -31,7 +31,7 @@ def _run(bt, n, h, hkv, window, alpha: Fraction, n_rungs=15, seed=0, qmul=1.0, l
     o_ref, lse_ref = oracle.attention_offsets(bf16_bits_to_f64(qb), bf16_bits_to_f64(kb), bf16_bits_to_f64(vb),
                                               window, oracle.fib_offsets(alpha, rungs))
     return assert_attention_close(bf16_to_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref,
-                                  f"W={window} alpha={alpha}")
+                                  f"d={d} W={window} alpha={alpha}")
 
 
 @pytest.mark.parametrize("window", [6, 8, 10, 12])
@@ -150,12 +150,12 @@ def test_packed_strided_inputs():
 
 # ---------------------------------------------------------------- interpolated gather (continuous alpha)
 
-def _run_interp(bt, n, h, hkv, window, alpha, n_rungs=15, ladder=0, seed=0, qmul=1.0):
+def _run_interp(bt, n, h, hkv, window, alpha, n_rungs=15, ladder=0, seed=0, qmul=1.0, d=64):
     torch = torch_cuda()
     rng = np.random.default_rng(seed)
-    qb = bf16_normal_bits(rng, (bt, n, h, 64), 0.125 * qmul)
-    kb = bf16_normal_bits(rng, (bt, n, hkv, 64), 0.125)
-    vb = bf16_normal_bits(rng, (bt, n, hkv, 64), 0.125)
+    qb = bf16_normal_bits(rng, (bt, n, h, d), 0.125 * qmul)
+    kb = bf16_normal_bits(rng, (bt, n, hkv, d), 0.125)
+    vb = bf16_normal_bits(rng, (bt, n, hkv, d), 0.125)
     o, lse = sa.offset_attn_interp_fwd(to_dev(qb), to_dev(kb), to_dev(vb), window, alpha, n_rungs, ladder)
     torch.cuda.synchronize()
     assert sa.sa_device_status() == 0
@@ -167,7 +167,7 @@ def _run_interp(bt, n, h, hkv, window, alpha, n_rungs=15, ladder=0, seed=0, qmul
     o_ref, lse_ref = oracle.attention_offsets_interp(bf16_bits_to_f64(qb), bf16_bits_to_f64(kb),
                                                      bf16_bits_to_f64(vb), window, lt)
     return assert_attention_close(bf16_to_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref,
-                                  f"interp W={window} alpha={alpha}")
+                                  f"interp d={d} W={window} alpha={alpha}")
 
 
 @pytest.mark.parametrize("alpha", [0.8317, 1.2345, 0.5, 1.5])
@@ -237,3 +237,58 @@ def test_interp_ragged_length_and_tiny_sequences():
     _run_interp(2, 1003, 2, 1, 8, 0.6180, seed=31, qmul=2.0)
     _run_interp(1, 7, 1, 1, 3, 1.7, seed=32)
     _run_interp(1, 1, 1, 1, 0, 0.9, seed=33)
+
+
+# ---------------------------------------------------------------- head dimensions 32 and 128
+
+@pytest.mark.parametrize("d", [32, 128])
+@pytest.mark.parametrize("window,alpha,hkv,n_rungs", [
+    (8, Fraction(7, 10), 2, 15),     # GQA, the page's window
+    (12, Fraction(3, 2), 1, 15),     # four query heads on one KV head
+    (0, Fraction(2, 1), 2, 15),      # self plus offsets: one 16-key band step
+    (64, Fraction(1, 2), 2, 15),     # the widest band: five 16-key steps
+    (6, Fraction(13, 10), 2, 0),     # every rung up to N
+])
+def test_head_dims_32_128(d, window, alpha, hkv, n_rungs):
+    """1000 tokens: a ragged tail for the 128-query (d <= 64) and 64-query (d = 128) tiles."""
+    _run(2, 1000, 4, hkv, window, alpha, n_rungs=n_rungs, seed=100 + window + d, qmul=3.0, d=d)
+
+
+@pytest.mark.parametrize("d", [32, 128])
+def test_head_dims_pow2_and_short(d):
+    _run(1, 2048, 4, 2, 8, Fraction(9, 10), n_rungs=11, seed=7 + d, qmul=2.0, ladder="pow2", d=d)
+    _run(1, 130, 1, 1, 0, Fraction(1, 1), seed=8 + d, d=d)
+    _run(1, 64, 1, 1, 64, Fraction(1, 2), seed=9 + d, d=d)     # dense causal
+
+
+@pytest.mark.parametrize("d", [32, 128])
+def test_interp_head_dims_32_128(d):
+    _run_interp(2, 1003, 4, 2, 8, 0.8317, seed=200 + d, qmul=3.0, d=d)
+    _run_interp(1, 600, 2, 2, 8, 0.99, ladder=1, n_rungs=8, seed=201 + d, d=d)     # 63.36: band side
+    _run_interp(1, 600, 2, 2, 8, 1.01, ladder=1, n_rungs=8, seed=202 + d, d=d)     # 64.64: slab side
+    _run_interp(2, 500, 2, 1, 64, 1.3, n_rungs=0, seed=203 + d, d=d)               # widest window, all rungs
+    _run_interp(1, 7, 1, 1, 3, 1.7, seed=204 + d, d=d)
+
+
+@pytest.mark.parametrize("d", [32, 128])
+def test_interp_integer_alpha_matches_integer_offset_kernel_head_dims(d):
+    torch = torch_cuda()
+    rng = np.random.default_rng(300 + d)
+    n = 1024
+    qb, kb, vb = (bf16_normal_bits(rng, (1, n, 2, d), 0.3) for _ in range(3))
+    q, k, v = to_dev(qb), to_dev(kb), to_dev(vb)
+    for alpha in (1, 2):
+        o1, l1 = sa.offset_attn_interp_fwd(q, k, v, 8, float(alpha))
+        offs = sa.sa_fib_offsets(alpha, 1, 15, 8, n)
+        o2, l2 = sa.offset_attn_fwd(q, k, v, 8, offs)
+        torch.cuda.synchronize()
+        assert (o1.float() - o2.float()).abs().max().item() < 2 * O_MAX_ABS
+        assert (l1 - l2).abs().max().item() < 2 * LSE_MAX_ABS
+
+
+@pytest.mark.parametrize("d", [32, 128])
+def test_head_dims_whole_8k_layer(d):
+    """A whole 8K layer (2 sequences, 4 heads on 2 KV heads) at d = 32 and 128, every row
+    compared: the 64-query tiles of d = 128 and the slab rings over many waves."""
+    _run(2, 8192, 4, 2, 8, Fraction(2, 1), seed=400 + d, d=d)
+    _run_interp(2, 8192, 4, 2, 8, 1.618, seed=401 + d, d=d)
