@@ -15,12 +15,12 @@
 // Warp roles (512 threads, 16 warps; warp w runs on SM sub-partition w % 4):
 //   warps 0-3   softmax of pipeline 0, warp w reads TMEM lane quarter w (query rows 32w ..)
 //   warps 4-7   softmax of pipeline 1
-//   warps 12, 13 planners of pipeline 0 / 1: claim items, build the key-block union, publish
+//   warps 14, 15 planners of pipeline 0 / 1: claim items, build the key-block union, publish
 //               the item's key tiles into a ring of two batches (up to 16 tiles per entry):
 //               the next item's union is built under the current item, and a planner never
 //               claims many items ahead of its pipeline
 //   warps 8, 11 lane 0 loads Q, K and V of pipeline 0 / 1 by TMA as the batches arrive
-//   warps 14, 15 idle (the fourth warpgroup's remainder)
+//   warps 12, 13 idle (the fourth warpgroup's remainder)
 //   warps 9, 10 lane 0 issues the tcgen05 MMAs of pipeline 0 / 1 in the order QK_j, PV_{j-1}:
 //                 S = Q K_j^T   (N = keys of the tile, up to 128)
 //                 O += P_j V_j  (A = P_j from TMEM, B = V_j MN-major; K = 16 keys per MMA)
@@ -492,9 +492,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the launch allocation (checked on the host), so the growth always completes.
   static_assert(kSoftmaxRegs == 184 && kCtrlRegs == 72, "register split literals");
 
-  // pipeline 0: softmax warps 0-3, loader 8, MMA 9, planner 12;
-  // pipeline 1: softmax warps 4-7, MMA 10, loader 11, planner 13; warps 14, 15 idle
-  const int x = warp < 8 ? (warp >> 2) : ((warp == 8 || warp == 9 || warp == 12) ? 0 : 1);
+  // pipeline 0: softmax warps 0-3, loader 8, MMA 9, planner 14;
+  // pipeline 1: softmax warps 4-7, MMA 10, loader 11, planner 15; warps 12, 13 idle
+  // (sub-partition w % 4: the planners share 2 and 3 with an MMA thread and a loader, not 0
+  // and 1 with both; BigBird 16K 0.395-0.400 -> 0.389-0.392 ms, the rest within noise)
+  const int x = warp < 8 ? (warp >> 2) : ((warp == 8 || warp == 9 || warp == 14) ? 0 : 1);
   uint8_t* sQ = sbase + x * C::PIPE_BYTES;
   uint8_t* sK = sQ + C::QB * C::Q_BYTES;
   uint8_t* sV = sK + C::KS * C::KV_BYTES;
@@ -513,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 9 || warp == 10) {
       if ((threadIdx.x & 31) == 0) mma_issuer<D>(x, bars[x], ring[x], sQ, sK, sV, tmem, &abort_flag);
       __syncwarp();
-    } else if (warp == 12 || warp == 13) {
+    } else if (warp == 14 || warp == 15) {
       planner<D>(p, bars[x], ring[x], un, &abort_flag);
     }
   }
