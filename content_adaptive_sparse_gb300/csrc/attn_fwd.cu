@@ -39,6 +39,12 @@ namespace sa {
 namespace {
 
 constexpr int kSoftmaxWarps = 4;      // per pipeline: one per TMEM lane quarter
+// Register split of this kernel: softmax warpgroups 192, control warpgroups 64 (8 x 192 + 8 x 64
+// = 16 x 128). Measured against 184 / 72: 8K top-16 0.1912-0.1932 -> 0.1911 ms, BigBird 16K
+// 0.391-0.395 -> 0.390-0.391 ms; 200 / 56 (control code spills) no better.
+constexpr int kPipeSoftmaxRegs = 192;
+constexpr int kPipeCtrlRegs = 64;
+static_assert(8 * kPipeSoftmaxRegs + 8 * kPipeCtrlRegs == 16 * kLaunchRegs, "register split");
 // d = 64: items of at least this many key tiles store O by TMA (measured at 1, 2, 4 and 8:
 // 1-4 equal within noise, 8 slower on BigBird 16K; 1 = every item with key tiles)
 constexpr int kTmaStoreTiles = 1;
@@ -490,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Register split: warpgroups 0-1 (softmax) grow, warpgroups 2-3 (control) shrink, at the
   // top of their branches (the compiler budgets the code that follows by it); the sum equals
   // the launch allocation (checked on the host), so the growth always completes.
-  static_assert(kSoftmaxRegs == 184 && kCtrlRegs == 72, "register split literals");
+  static_assert(kPipeSoftmaxRegs == 192 && kPipeCtrlRegs == 64, "register split literals");
 
   // pipeline 0: softmax warps 0-3, loader 8, MMA 9, planner 14;
   // pipeline 1: softmax warps 4-7, MMA 10, loader 11, planner 15; warps 12, 13 idle
@@ -504,11 +510,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 8) {
     // warpgroups 0 and 1: one setmaxnreg instruction for both
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 184;" ::: "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
     softmax_epilogue<D>(p, x, bars[x], ring[x], tmem, sQ, &to, &abort_flag);
   } else {
     // warpgroups 2 and 3: one setmaxnreg instruction for both, then the roles
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;" ::: "memory");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 64;" ::: "memory");
     if (warp == 8 || warp == 11) {
       if ((threadIdx.x & 31) == 0) loader<D>(p, &tq, &tk, &tv, bars[x], ring[x], sQ, sK, sV, &abort_flag);
       __syncwarp();

@@ -33,7 +33,8 @@ constexpr int kMetaRing = 2;          // batch entries: items claimed ahead of t
 constexpr uint32_t kTmemCols = 512;
 // Register split (setmaxnreg): the launch gives every thread 128 registers; the two
 // warpgroups of control warps drop to kCtrlRegs so that the two softmax warpgroups can hold a
-// whole 128-key score row: 8 warps x 184 + 8 warps x 72 = 16 warps x 128 per thread.
+// whole 128-key score row: 8 warps x 184 + 8 warps x 72 = 16 warps x 128 per thread (the
+// one-stream kernel; the two-pipeline kernel splits 192 / 64).
 constexpr int kLaunchRegs = 128;
 constexpr int kSoftmaxRegs = 184;
 constexpr int kCtrlRegs = 72;
