@@ -138,14 +138,24 @@ def test_explicit_offset_sets(window, offs):
                  to_dev(vb), window, offs, f"W={window} offsets={offs[:4]}..")
 
 
-def test_packed_strided_inputs():
-    rng = np.random.default_rng(9)
+@pytest.mark.parametrize("d", [32, 64, 128])
+def test_packed_strided_inputs(d):
+    rng = np.random.default_rng(9 + d)
     bt, n, h = 2, 700, 4
-    packed = bf16_normal_bits(rng, (bt, n, 3, h, 64), 0.5)   # q, k, v interleaved per token
+    packed = bf16_normal_bits(rng, (bt, n, 3, h, d), 0.5 * (64 / d) ** 0.5)   # q, k, v interleaved per token
     t = to_dev(packed)
     f = bf16_bits_to_f64(packed)
     _run_offsets(f[:, :, 0], f[:, :, 1], f[:, :, 2], t[:, :, 0], t[:, :, 1], t[:, :, 2], 8,
-                 [9, 13, 21, 34, 55, 89, 144, 233, 377, 610], "packed qkv")
+                 [9, 13, 21, 34, 55, 89, 144, 233, 377, 610], f"packed qkv d={d}")
+    # the interpolated gather on the same strided views
+    torch = torch_cuda()
+    o, lse = sa.offset_attn_interp_fwd(t[:, :, 0], t[:, :, 1], t[:, :, 2], 8, 0.91)
+    torch.cuda.synchronize()
+    assert sa.sa_device_status() == 0
+    o_ref, lse_ref = oracle.attention_offsets_interp(f[:, :, 0], f[:, :, 1], f[:, :, 2], 8,
+                                                     oracle.interp_rungs(0.91, oracle.fib_rungs(15), 8))
+    assert_attention_close(bf16_to_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref,
+                           f"packed qkv interp d={d}")
 
 
 # ---------------------------------------------------------------- interpolated gather (continuous alpha)
